@@ -1,0 +1,423 @@
+"""Benchmark of the CPR Gated DeltaNet layer on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one CPR prefill / training forward of the trainer-shaped workload (1 sequence
+x 10,240 tokens, H=16, dk=dv=128, C=64, bf16 q/k/v, fp32 state), inputs resident in HBM,
+L2 flushed between steps.  The JSON line also carries the rollout-decode workload (256
+sequences x 1 token, prior lengths U[1,4096], steps/s), the roofline of each path's
+dominant kernel, the end-to-end number through the C ABI with host buffers, and the
+fp64 CPU oracle timed on this machine's cores.  Under torchrun every rank runs the same
+workload on its own GPU (independent problems: weak scaling, no collective on the data
+path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CPR-GDN prefill tokens/s, decode steps/s per layer; % of roofline; 1 GB300"
+# FP32 pipe: 152 SMs x 128 FP32 lanes x 2 flop (FMA) x 2.07 GHz (maximum SM clock)
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = str(gpu_index)
+        try:  # nvidia-smi numbering can differ from CUDA's: select the GPU by UUID
+            u = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            self.gpu = u if u.startswith("GPU-") else f"GPU-{u}"
+        except Exception:
+            pass
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------------------------
+# algorithmic work (per the method, independent of the kernels' own bookkeeping)
+# ------------------------------------------------------------------------------------
+
+def prefill_algorithmic(T, N, H, dk, dv, n_chunks, elem=2):
+    """Bytes and FP32 flops of one prefill: q,k,v read, o written, g,beta read, every
+    boundary state written, final states written; 7*dk*dv flops per token-head (S k: 2,
+    alpha S + u k^T: 3, S q: 2)."""
+    bytes_ = T * H * (2 * dk + dv) * elem + T * H * dv * elem + 2 * T * H * 4
+    bytes_ += n_chunks * H * dk * dv * 4 + N * H * dk * dv * 4
+    flops_intra = 7 * dk * dv * T * H
+    return bytes_, flops_intra
+
+
+def decode_algorithmic(B, H, dk, dv, C, n_resync, elem=2):
+    """Bytes of one decode step: state read + write, token q,k,v,g,beta read, o written,
+    the token's ring slot written; per resync: the ring chunk and S_b read, S_b and the
+    state written."""
+    per = 2 * dk * dv * 4 + (2 * dk + dv) * elem + 8 + dv * elem + (dk + dv) * elem + 8
+    res = C * (dk + dv) * elem + 8 * C + dk * dv * 4 + 2 * dk * dv * 4
+    return B * H * per + n_resync * H * res
+
+
+# ------------------------------------------------------------------------------------
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return dist, dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def _max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def cpu_baseline_oracle(x_cpu, C, target_s=12.0):
+    """The fp64 oracle as it stands, on this host's cores, over whole copies of the
+    workload until about target_s seconds have run.  Returns (tokens/s, threads, sample)."""
+    import numpy as np
+
+    import oracle
+
+    arrs = [np.ascontiguousarray(x_cpu[k].double().numpy()) for k in ("q", "k", "v", "g", "beta")]
+    cu = x_cpu["cu_seqlens"].numpy()
+    T = int(cu[-1])
+    reps, t_total = 0, 0.0
+    while t_total < target_s and reps < 50:
+        t0 = time.perf_counter()
+        oracle.recurrent(*arrs, cu, C, boundaries=True)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return T * reps / t_total, oracle.max_threads(), f"{reps} full run(s) of the {T}-token workload"
+
+
+def run_reference(args):
+    """--impl reference: the fp64 CPU oracle on the same workload, metric and unit."""
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:  # the CPU oracle runs once, on rank 0; other ranks exit without work
+        return
+    import numpy as np
+
+    import oracle
+    from linear_attention_cpr_gb300 import inputs
+
+    w = inputs.workload("trainer_fwd")
+    x = inputs.prefill_inputs(w)
+    arrs = [np.ascontiguousarray(x[k].double().numpy()) for k in ("q", "k", "v", "g", "beta")]
+    T_s = 2048  # one step = the first 2,048 tokens of the sequence, all 16 heads
+    sub = [a[:T_s] for a in arrs]
+    for _ in range(args.warmup):
+        oracle.recurrent(*sub, [0, T_s], w.C)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.recurrent(*sub, [0, T_s], w.C)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = T_s / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "trainer_fwd: 1 x 10,240 tokens, H=16, dk=dv=128, C=64",
+                       "sample": f"first {T_s} tokens x 16 heads per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"first {T_s} tokens of the 10,240-token sequence, 16 heads, per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import linear_attention_cpr_gb300 as cpr
+    from linear_attention_cpr_gb300 import build, inputs
+
+    dist, rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    cpr.load_library()
+    hbm_peak, hbm_kind = _peaks()
+    gen_dev = torch.Generator(device=dev)
+
+    # ---------------- prefill: trainer-forward shape ----------------
+    w = inputs.workload(args.workload)
+    x_cpu = inputs.prefill_inputs(w)
+    x = {k: v.to(dev) for k, v in x_cpu.items()}
+    T, H, dk, dv, C, N = w.total_tokens, w.H, w.dk, w.dv, w.C, len(w.seqlens)
+    n_chunks = cpr.cpr_gdn_num_chunks(x_cpu["cu_seqlens"], C)
+    out = torch.empty(T, H, dv, dtype=w.dtype, device=dev)
+    st = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    bnd = torch.empty(n_chunks, H, dk, dv, dtype=torch.float32, device=dev)
+    ws = torch.empty(cpr.cpr_gdn_prefill_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def prefill():
+        cpr.cpr_gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], C, out=out, state_out=st,
+                            boundary_states=bnd, workspace=ws)
+
+    for _ in range(args.warmup):
+        prefill()
+    torch.cuda.synchronize()
+    assert cpr.cpr_gdn_device_status(ws) == 0
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    kern = {"chunk_index": [], "chunk_prep": [], "boundary_chain": [], "intra_chunk": []}
+    step_ms = []
+    _barrier(dist)
+    with ClockSampler(local) as clocks:
+        cpr.cpr_gdn_set_profile_events(ev)
+        for _ in range(args.steps):
+            flush.zero_()  # L2 flush between steps (outside the events)
+            prefill()
+            ev[4].synchronize()
+            step_ms.append(ev[0].elapsed_time(ev[4]))
+            for i, name in enumerate(kern):
+                kern[name].append(ev[i].elapsed_time(ev[i + 1]))
+        cpr.cpr_gdn_set_profile_events(None)
+        _barrier(dist)
+    ms = statistics.fmean(step_ms)
+    ms_max = _max_over_ranks(dist, ms)
+    value = world * T / (ms_max / 1e3)
+    kern_ms = {k: statistics.fmean(v) for k, v in kern.items()}
+    alg_bytes, flops_intra = prefill_algorithmic(T, N, H, dk, dv, n_chunks)
+    intra_ms = kern_ms["intra_chunk"]
+    achieved = flops_intra / (intra_ms / 1e3) / 1e12
+    roofline = {"kernel": "k3_intra_chunk", "bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS,
+                "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
+                "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
+                "flops_per_launch": flops_intra}
+    t_roof_ms = max(alg_bytes / (hbm_peak * 1e9), flops_intra / (FP32_PEAK_TFLOPS * 1e12)) * 1e3
+
+    # ---------------- end to end through the C ABI with host buffers ----------------
+    pin = {k: v.pin_memory() for k, v in x_cpu.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    st_h = torch.empty(st.shape, dtype=st.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = out_h.numel() * out_h.element_size() + st_h.numel() * st_h.element_size()
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        e_a.record()
+        for k in x:
+            x[k].copy_(pin[k], non_blocking=True)
+        prefill()
+        out_h.copy_(out, non_blocking=True)
+        st_h.copy_(st, non_blocking=True)
+        e_b.record()
+        e_b.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(e_a.elapsed_time(e_b))
+    e2e_val = world * T / (_max_over_ranks(dist, statistics.fmean(e2e_ms)) / 1e3)
+
+    # ---------------- decode: rollout shape ----------------
+    decode = None
+    if not args.no_decode:
+        decode = run_decode(args, cpr, inputs, dev, hbm_peak, dist, world)
+
+    # ---------------- CPU oracle baseline (rank 0, N = 1 only) ----------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample = cpu_baseline_oracle(x_cpu, C)
+        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    launches = 4 * args.steps
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {N} x {T} tokens, H={H}, dk=dv={dk}, C={C}, bf16 q/k/v, fp32 state",
+                       "l2": "flushed between timed steps (2 x L2 buffer written)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roofline,
+            "prefill": {"kernels_ms": kern_ms, "algorithmic_bytes": alg_bytes, "t_roof_ms": t_roof_ms,
+                        "frac_of_t_roof": t_roof_ms / ms_max, "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": hbm_kind},
+            "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches + (decode["gpu_launches"] if decode else 0),
+            "clocks": clocks.summary(),
+            "decode": decode,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_decode(args, cpr, inputs, dev, hbm_peak, dist, world):
+    w = inputs.workload("rollout_decode")
+    B, H, dk, dv, C = len(w.seqlens), w.H, w.dk, w.dv, w.C
+    x = inputs.prefill_inputs(w, device=dev)  # prior context, drawn on the device
+    n_chunks = cpr.cpr_gdn_num_chunks(inputs.cu_seqlens_of(w.seqlens), C)
+    _, st, bnd, ws = cpr.cpr_gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], C,
+                                         n_chunks=n_chunks)
+    ring = cpr.cpr_gdn_ring_from_prefill(x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], C, bnd, st)
+    del x, bnd, ws
+    state = st
+    n_steps = args.decode_steps
+    toks = [inputs.decode_inputs(w, s, device=dev) for s in range(n_steps)]
+    pos0 = torch.tensor(w.seqlens, dtype=torch.int32)
+    pos = pos0.to(dev)
+    out = torch.empty(B, H, dv, dtype=w.dtype, device=dev)
+    dws = torch.empty(cpr.cpr_gdn_decode_workspace_size(B, H, dk, dv, C), dtype=torch.uint8, device=dev)
+
+    def step(s):
+        t = toks[s % n_steps]
+        cpr.cpr_gdn_decode(t["q"], t["k"], t["v"], t["g"], t["beta"], state, ring, pos, C, out=out, workspace=dws)
+        pos.add_(1)
+
+    warm = max(3, args.warmup)
+    for s in range(warm):
+        step(s)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    step_ms, k4, k5 = [], [], []
+    n_res = 0
+    _barrier(dist)
+    cpr.cpr_gdn_set_profile_events(ev)
+    for s in range(warm, warm + n_steps):
+        p_host = pos0 + s
+        n_res += int(((p_host % C) == C - 1).sum())
+        step(s)
+        ev[2].synchronize()
+        step_ms.append(ev[0].elapsed_time(ev[2]))
+        k4.append(ev[0].elapsed_time(ev[1]))
+        k5.append(ev[1].elapsed_time(ev[2]))
+    cpr.cpr_gdn_set_profile_events(None)
+    _barrier(dist)
+    assert cpr.cpr_gdn_device_status(dws) == 0
+    ms = _max_over_ranks(dist, statistics.fmean(step_ms))
+    k4_ms = statistics.fmean(k4)
+    bytes_step = decode_algorithmic(B, H, dk, dv, C, n_res / n_steps)
+    step_only = decode_algorithmic(B, H, dk, dv, C, 0)
+    ach = step_only / (k4_ms / 1e3) / 1e9
+    # end to end: the step's tokens from pinned host memory, the outputs back
+    pin = [{k: v.cpu().pin_memory() for k, v in t.items()} for t in toks[:8]]
+    dbuf = {k: v.clone() for k, v in toks[0].items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin[0].values())
+    d2h = out_h.numel() * out_h.element_size()
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e = []
+    for s in range(64):
+        e_a.record()
+        for k in dbuf:
+            dbuf[k].copy_(pin[s % 8][k], non_blocking=True)
+        cpr.cpr_gdn_decode(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], state, ring, pos, C, out=out,
+                           workspace=dws)
+        pos.add_(1)
+        out_h.copy_(out, non_blocking=True)
+        e_b.record()
+        e_b.synchronize()
+        e2e.append(e_a.elapsed_time(e_b))
+    e2e_ms = _max_over_ranks(dist, statistics.fmean(e2e[4:]))
+    return {
+        "metric": "decode steps/s per layer", "value": 1e3 / ms * world, "unit": "steps/s",
+        "ms_per_step": ms, "steps": n_steps, "workload": f"rollout_decode: B={B}, H={H}, dk=dv={dk}, C={C}, "
+        "prior lengths U[1,4096], state resident (> L2)",
+        "kernels_ms": {"decode_step": k4_ms, "resync": statistics.fmean(k5)},
+        "resyncs_per_step": n_res / n_steps,
+        "roofline": {"kernel": "k4_decode_step", "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": ach / hbm_peak, "traffic": None, "bytes_per_launch": step_only},
+        "t_roof_ms": bytes_step / (hbm_peak * 1e9) * 1e3,
+        "frac_of_t_roof": bytes_step / (hbm_peak * 1e9) * 1e3 / ms,
+        "e2e": {"value": 1e3 / e2e_ms * world, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * n_steps,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="trainer_fwd")
+    ap.add_argument("--decode-steps", type=int, default=512)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+/*
+ * cpr_gdn.h — C ABI of the Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet layer
+ * for one GB300 GPU (sm_103a).
+ *
+ * The method: "IsoExec: Eliminating Trainer-Inference Mismatch in SkyRL", section
+ * "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet", and "SkyRL IsoExec: vLLM 与
+ * Megatron 的 logprob 差 ...", section "Gated DeltaNet 的第三条路：chunkwise-parallel
+ * recurrent".  CPR keeps the token recurrence of Gated DeltaNet
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t q_t,
+ *     alpha_t = exp(g_t)
+ * (S is dv x dk, fp32) as the function that produces every output, and evaluates it
+ * in three steps:
+ *   1. the state at every chunk boundary (every C tokens from each sequence's start)
+ *      is produced by one fixed-order fp32 chunk-update function U(S_b, chunk);
+ *   2. the outputs inside each chunk are produced by the token recurrence starting
+ *      from the chunk's boundary state, all chunks in parallel;
+ *   3. decode runs the same token recurrence one token at a time and, when a token
+ *      completes a chunk, replaces its state by U(S_b, chunk) — the same U.
+ * Consequently prefill, training-forward and decode give bit-identical outputs and
+ * states, and no result depends on batch composition, packing or batch position.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers (unless the name ends in _host), on the
+ *     current CUDA device, row-major and contiguous.  The caller owns every buffer;
+ *     the library allocates no memory and reads no host memory during a call, and all
+ *     work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - dtype selects the element type of q, k, v, out and the ring's k, v:
+ *     CPR_DTYPE_BF16 (2 bytes) or CPR_DTYPE_F32 (4 bytes).  g, beta and every state
+ *     are fp32.
+ *   - A state is stored per (sequence, head) as [dk, dv]: element (j, i) holds S[i][j]
+ *     (row i of S is the value index).
+ *   - Supported shapes: dk == dv in {32, 64, 128}; C in {16, 32, 64} (not every pair
+ *     is built: cpr_gdn_supported() answers).  Other shapes return
+ *     CPR_ERR_UNSUPPORTED_SHAPE.
+ *   - Alignment: q, k, v, out, states, boundary states, ring buffers and the
+ *     workspace must be 16-byte aligned (CPR_ERR_MISALIGNED otherwise); g, beta,
+ *     cu_seqlens and pos 4-byte aligned.
+ *   - Errors: a negative return value means nothing was enqueued (argument checks)
+ *     or a launch failed (CPR_ERR_CUDA).  Checks that need device data (cu_seqlens,
+ *     pos) run on the device: they skip the offending work and record a bit in the
+ *     workspace status word, read with cpr_gdn_device_status().  Asynchronous CUDA
+ *     errors surface at the caller's next synchronisation.
+ */
+#ifndef CPR_GDN_H
+#define CPR_GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define CPR_OK 0
+#define CPR_ERR_INVALID_ARG (-1)       /* null pointer, negative size, bad dtype, ... */
+#define CPR_ERR_UNSUPPORTED_SHAPE (-2) /* (dk, dv, C) not built into this library */
+#define CPR_ERR_MISALIGNED (-3)        /* a pointer breaks the alignment rule above */
+#define CPR_ERR_WORKSPACE (-4)         /* workspace missing or smaller than required */
+#define CPR_ERR_CUDA (-5)              /* a kernel launch or CUDA runtime call failed */
+
+/* Bits of the device status word (cpr_gdn_device_status). */
+#define CPR_DEV_BAD_CU_SEQLENS 1u /* cu_seqlens[0] != 0, decreasing, or last != total_tokens */
+#define CPR_DEV_BOUNDARY_CAPACITY 2u /* more chunks than boundary_capacity */
+#define CPR_DEV_BAD_POS 4u        /* a decode position is negative */
+
+/* Element types of q, k, v, out and the ring's k, v. */
+#define CPR_DTYPE_BF16 0
+#define CPR_DTYPE_F32 1
+
+/*
+ * Decode ring: what decode keeps per (sequence, head) between calls so that it can
+ * resynchronise at the end of the current chunk.  All device pointers, caller-owned:
+ *   S_b   fp32  [B, H, dk, dv]  state at the start of the sequence's current chunk
+ *   k     dtype [B, H, C, dk]   keys of the current chunk so far (slot = position % C)
+ *   v     dtype [B, H, C, dv]   values of the current chunk so far
+ *   g     fp32  [B, H, C]       log-decays of the current chunk so far
+ *   beta  fp32  [B, H, C]       write strengths of the current chunk so far
+ * Decode reads and writes it in place; cpr_gdn_ring_from_prefill() fills it.
+ */
+typedef struct cpr_gdn_ring {
+    float* S_b;
+    void* k;
+    void* v;
+    float* g;
+    float* beta;
+} cpr_gdn_ring;
+
+/* 1 if (dk, dv, C, dtype) is built into this library, else 0. */
+int cpr_gdn_supported(int32_t dk, int32_t dv, int32_t C, int32_t dtype);
+
+/* Library ABI version (incremented on any change of these declarations). */
+int32_t cpr_gdn_version(void);
+
+/* Human-readable text of a return code. Never NULL; the string is static. */
+const char* cpr_gdn_strerror(int32_t code);
+
+/*
+ * Number of chunks of a packed batch: sum over sequences of ceil(L_n / C), where
+ * L_n = cu_seqlens_host[n+1] - cu_seqlens_host[n].  HOST pointer.  This is the row
+ * count of boundary_states.  Returns a negative code on invalid input.
+ */
+int64_t cpr_gdn_num_chunks(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t C);
+
+/*
+ * Bytes of device workspace cpr_gdn_prefill needs for a batch of n_seqs sequences
+ * holding total_tokens tokens (an upper bound: it does not depend on how the tokens
+ * are split between sequences).  0 on invalid arguments.
+ */
+size_t cpr_gdn_prefill_workspace_size(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk,
+                                      int32_t dv, int32_t C);
+
+/* Bytes of device workspace cpr_gdn_decode needs (the status word). */
+size_t cpr_gdn_decode_workspace_size(int32_t B, int32_t H, int32_t dk, int32_t dv, int32_t C);
+
+/*
+ * CPR prefill / training forward over a packed batch (CPR steps 1 and 2).
+ *   q, k        dtype [total_tokens, H, dk]     (caller applies any q scaling / key norm)
+ *   v           dtype [total_tokens, H, dv]
+ *   g, beta     fp32  [total_tokens, H]          g = log(alpha) <= 0, beta in [0, 1]
+ *   cu_seqlens  int32 [n_seqs + 1]  DEVICE; cu_seqlens[0] = 0, non-decreasing,
+ *               cu_seqlens[n_seqs] = total_tokens.  Every sequence starts at its own
+ *               position 0: the chunk grid is anchored there.
+ *   state_in    fp32  [n_seqs, H, dk, dv] initial states, or NULL for zero states.
+ * Outputs:
+ *   out         dtype [total_tokens, H, dv]   o_t = S_t q_t (rounded to nearest even
+ *               when dtype is bf16)
+ *   state_out   fp32  [n_seqs, H, dk, dv]     state after each sequence's last token:
+ *               U's result when L_n is a multiple of C, else the stepped state.
+ *               (state_in when L_n = 0.)
+ *   boundary_states fp32 [boundary_capacity, H, dk, dv]: row c holds the state at the
+ *               start of chunk c (chunks numbered in packed order, sequence by sequence;
+ *               row 0 of each sequence is its state_in).  Rows beyond the batch's chunk
+ *               count are not written.  If the count exceeds boundary_capacity nothing
+ *               is written and CPR_DEV_BOUNDARY_CAPACITY is recorded.
+ *   workspace   >= cpr_gdn_prefill_workspace_size(...) bytes, 16-byte aligned; holds
+ *               the status word of this call.  Calls sharing a workspace must not
+ *               overlap on the device.
+ * Buffers must not overlap each other, except that state_out may equal state_in.
+ */
+int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
+                        int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* state_in,
+                        void* out, float* state_out, float* boundary_states, int64_t boundary_capacity,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Fill a decode ring from a prefill's results so that decode continues each sequence
+ * at position L_n (CPR step 3 starts where prefill stopped).  Arguments as in
+ * cpr_gdn_prefill; ring buffers are sized for B = n_seqs.  For each (n, h): ring S_b =
+ * the boundary state of the sequence's last chunk if L_n % C != 0, else state_out
+ * (state_in if L_n = 0); ring slots 0 .. (L_n % C) - 1 receive that chunk's tokens.
+ * boundary_states and state_out are those the prefill wrote; cu_seqlens is DEVICE.
+ * k, v, g, beta and boundary_states may be NULL when total_tokens is 0.  A sequence
+ * whose cu_seqlens entries are decreasing or reach past total_tokens is skipped.
+ */
+int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, const float* beta,
+                                  const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                                  int32_t dv, int32_t C, int32_t dtype, const float* boundary_states,
+                                  const float* state_out, const cpr_gdn_ring* ring, void* stream);
+
+/*
+ * One CPR decode step for B sequences (CPR step 3): every sequence b receives one
+ * token at absolute position pos[b] (>= 0; the caller owns and advances pos).
+ *   q, k   dtype [B, H, dk];  v dtype [B, H, dv];  g, beta fp32 [B, H]
+ *   state  fp32 [B, H, dk, dv]  in/out: the sequence's recurrent state
+ *   ring   in/out (see cpr_gdn_ring); the token goes to slot pos[b] % C
+ *   pos    int32 [B] DEVICE
+ *   out    dtype [B, H, dv]
+ * The token is stepped by the same recurrence as prefill; when pos[b] % C == C - 1
+ * the state (and ring S_b) become U(ring S_b, ring chunk).  A negative pos[b] skips
+ * sequence b and records CPR_DEV_BAD_POS.  workspace >= cpr_gdn_decode_workspace_size.
+ */
+int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                       float* state, const cpr_gdn_ring* ring, const int32_t* pos, int32_t B, int32_t H,
+                       int32_t dk, int32_t dv, int32_t C, int32_t dtype, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * Profiling hook (used by the benchmark to time each kernel with CUDA events on the
+ * stream it runs on).  events: n_events cudaEvent_t handles created by the caller, or
+ * NULL to switch the hook off.  While it is on, every cpr_gdn_prefill records
+ * events[0] before its first kernel and events[i] after its i-th kernel (i = 1..4:
+ * chunk index, chunk prep, boundary chain, intra-chunk recurrence; needs n_events >= 5),
+ * and every cpr_gdn_decode records events[0] before and events[1], events[2] after its
+ * step and resync kernels.  Process-wide; not for concurrent calls from several threads.
+ */
+int32_t cpr_gdn_set_profile_events(void* const* events, int32_t n_events);
+
+/*
+ * Read the device status word of the last call that used `workspace` (waits for
+ * `stream`).  *status_out receives an OR of CPR_DEV_* bits, 0 when all device-side
+ * checks passed.  Returns CPR_OK or CPR_ERR_CUDA.
+ */
+int32_t cpr_gdn_device_status(const void* workspace, uint32_t* status_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPR_GDN_H */

@@ -1,0 +1,246 @@
+"""Thin Python binding of the C ABI in include/cpr_gdn.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls.  Tensors are torch
+tensors on the current CUDA device; torch supplies device memory and the stream, and
+every step of the layer runs in the library's CUDA kernels.  There is no fallback: if
+the compiled library is missing the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+CPR_DTYPE_BF16 = 0
+CPR_DTYPE_F32 = 1
+DEV_BAD_CU_SEQLENS = 1
+DEV_BOUNDARY_CAPACITY = 2
+DEV_BAD_POS = 4
+
+EXPORTED = (
+    "cpr_gdn_supported", "cpr_gdn_version", "cpr_gdn_strerror", "cpr_gdn_num_chunks",
+    "cpr_gdn_prefill_workspace_size", "cpr_gdn_decode_workspace_size", "cpr_gdn_prefill",
+    "cpr_gdn_ring_from_prefill", "cpr_gdn_decode", "cpr_gdn_device_status", "cpr_gdn_set_profile_events",
+)
+
+
+class CprError(RuntimeError):
+    def __init__(self, fn: str, code: int, text: str):
+        super().__init__(f"{fn} failed: {text} ({code})")
+        self.code = code
+
+
+class _Ring(ctypes.Structure):
+    _fields_ = [("S_b", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libcprgdn.so (built by ``linear_attention_cpr_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"CUDA library {path} is not built; run "
+                               "`python -m linear_attention_cpr_gb300.build` (nvcc, sm_103a)")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "cpr_gdn_supported": (ctypes.c_int, [I32, I32, I32, I32]),
+        "cpr_gdn_version": (I32, []),
+        "cpr_gdn_strerror": (ctypes.c_char_p, [I32]),
+        "cpr_gdn_num_chunks": (I64, [P, I32, I32]),
+        "cpr_gdn_prefill_workspace_size": (SZ, [I64, I32, I32, I32, I32, I32]),
+        "cpr_gdn_decode_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
+        "cpr_gdn_prefill": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P, P, P, I64, P, SZ, P]),
+        "cpr_gdn_ring_from_prefill": (I32, [P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P,
+                                            ctypes.POINTER(_Ring), P]),
+        "cpr_gdn_decode": (I32, [P, P, P, P, P, P, ctypes.POINTER(_Ring), P, I32, I32, I32, I32, I32, I32, P, P,
+                                 SZ, P]),
+        "cpr_gdn_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
+        "cpr_gdn_set_profile_events": (I32, [ctypes.POINTER(ctypes.c_void_p), I32]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        raise CprError(fn, code, load_library().cpr_gdn_strerror(code).decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return CPR_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return CPR_DTYPE_F32
+    raise TypeError(f"unsupported element type {t.dtype} (bf16 or fp32)")
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if t.numel() == 0:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def cpr_gdn_supported(dk: int, dv: int, C: int, dtype=torch.bfloat16) -> bool:
+    code = CPR_DTYPE_BF16 if dtype == torch.bfloat16 else CPR_DTYPE_F32
+    return bool(load_library().cpr_gdn_supported(dk, dv, C, code))
+
+
+def cpr_gdn_version() -> int:
+    return int(load_library().cpr_gdn_version())
+
+
+def cpr_gdn_strerror(code: int) -> str:
+    return load_library().cpr_gdn_strerror(code).decode()
+
+
+def cpr_gdn_num_chunks(cu_seqlens_host, C: int) -> int:
+    cu = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).cpu().contiguous()
+    n = int(load_library().cpr_gdn_num_chunks(cu.data_ptr(), cu.numel() - 1, C))
+    if n < 0:
+        raise CprError("cpr_gdn_num_chunks", n, cpr_gdn_strerror(n))
+    return n
+
+
+def cpr_gdn_prefill_workspace_size(total_tokens: int, n_seqs: int, H: int, dk: int, dv: int, C: int) -> int:
+    return int(load_library().cpr_gdn_prefill_workspace_size(total_tokens, n_seqs, H, dk, dv, C))
+
+
+def cpr_gdn_decode_workspace_size(B: int, H: int, dk: int, dv: int, C: int) -> int:
+    return int(load_library().cpr_gdn_decode_workspace_size(B, H, dk, dv, C))
+
+
+def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, C: int, state_in=None, *, out=None, state_out=None,
+                    boundary_states=None, workspace=None, n_chunks: int | None = None, stream=None):
+    """CPR prefill.  Returns (out, state_out, boundary_states, workspace).
+
+    ``cu_seqlens`` is an int32 CUDA tensor.  ``n_chunks`` (the batch's chunk count) is
+    read from a host copy of cu_seqlens when not given and boundary_states is None.
+    """
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    if out is None:
+        out = torch.empty(T, H, dv, dtype=q.dtype, device=dev)
+    if state_out is None:
+        state_out = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    if boundary_states is None:
+        if n_chunks is None:
+            n_chunks = cpr_gdn_num_chunks(cu_seqlens.cpu(), C)
+        boundary_states = torch.empty(max(n_chunks, 1), H, dk, dv, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(cpr_gdn_prefill_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
+    code = load_library().cpr_gdn_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, C, _dtype_code(q),
+        _ptr(state_in), _ptr(out), _ptr(state_out), _ptr(boundary_states), boundary_states.shape[0],
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("cpr_gdn_prefill", code)
+    return out, state_out, boundary_states, workspace
+
+
+@dataclass
+class Ring:
+    """Decode ring buffers (see cpr_gdn_ring in include/cpr_gdn.h)."""
+    S_b: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    g: torch.Tensor
+    beta: torch.Tensor
+
+    @staticmethod
+    def empty(B: int, H: int, dk: int, dv: int, C: int, dtype=torch.bfloat16, device="cuda") -> "Ring":
+        return Ring(S_b=torch.zeros(B, H, dk, dv, dtype=torch.float32, device=device),
+                    k=torch.zeros(B, H, C, dk, dtype=dtype, device=device),
+                    v=torch.zeros(B, H, C, dv, dtype=dtype, device=device),
+                    g=torch.zeros(B, H, C, dtype=torch.float32, device=device),
+                    beta=torch.zeros(B, H, C, dtype=torch.float32, device=device))
+
+    def _c(self) -> _Ring:
+        return _Ring(_ptr(self.S_b), _ptr(self.k), _ptr(self.v), _ptr(self.g), _ptr(self.beta))
+
+    def clone(self) -> "Ring":
+        return Ring(*(t.clone() for t in (self.S_b, self.k, self.v, self.g, self.beta)))
+
+    def index(self, idx) -> "Ring":
+        return Ring(*(t[idx].contiguous() for t in (self.S_b, self.k, self.v, self.g, self.beta)))
+
+
+def cpr_gdn_ring_from_prefill(k, v, g, beta, cu_seqlens, C: int, boundary_states, state_out, ring: Ring | None = None,
+                              stream=None) -> Ring:
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    if ring is None:
+        ring = Ring.empty(N, H, dk, dv, C, dtype=k.dtype, device=k.device)
+    rc = ring._c()
+    code = load_library().cpr_gdn_ring_from_prefill(
+        _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, C, _dtype_code(k),
+        _ptr(boundary_states), _ptr(state_out), ctypes.byref(rc), _stream(stream))
+    _check("cpr_gdn_ring_from_prefill", code)
+    return ring
+
+
+def cpr_gdn_decode(q, k, v, g, beta, state, ring: Ring, pos, C: int, *, out=None, workspace=None, stream=None):
+    """One decode step for B sequences; ``state`` and ``ring`` are updated in place.  Returns (out, workspace)."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(cpr_gdn_decode_workspace_size(B, H, dk, dv, C), dtype=torch.uint8, device=q.device)
+    rc = ring._c()
+    code = load_library().cpr_gdn_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), ctypes.byref(rc), _ptr(pos), B, H, dk, dv, C,
+        _dtype_code(q), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("cpr_gdn_decode", code)
+    return out, workspace
+
+
+def cpr_gdn_device_status(workspace, stream=None) -> int:
+    st = ctypes.c_uint32(0)
+    code = load_library().cpr_gdn_device_status(_ptr(workspace), ctypes.byref(st), _stream(stream))
+    _check("cpr_gdn_device_status", code)
+    return int(st.value)
+
+
+def cpr_gdn_set_profile_events(events) -> None:
+    """Record the given torch.cuda.Event objects between the library's kernels (None: off)."""
+    lib = load_library()
+    if events is None:
+        _check("cpr_gdn_set_profile_events", lib.cpr_gdn_set_profile_events(None, 0))
+        return
+    for e in events:  # make sure every event handle exists
+        if not e.cuda_event:
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check("cpr_gdn_set_profile_events", lib.cpr_gdn_set_profile_events(arr, len(events)))

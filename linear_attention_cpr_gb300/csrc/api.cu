@@ -1,0 +1,253 @@
+// api.cu — the C ABI declared in include/cpr_gdn.h: argument checks, shape dispatch
+// and launches.  No allocation, no host synchronisation (except
+// cpr_gdn_device_status, which reads the status word back).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+using namespace cpr;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool shape_built(int32_t dk, int32_t dv, int32_t C)
+{
+#define CPR_SHAPE_MATCH(DK, DV, CC) \
+    if (dk == DK && dv == DV && C == CC) return true;
+    CPR_FOR_EACH_SHAPE(CPR_SHAPE_MATCH)
+#undef CPR_SHAPE_MATCH
+    return false;
+}
+
+bool dtype_ok(int32_t dtype) { return dtype == CPR_DTYPE_BF16 || dtype == CPR_DTYPE_F32; }
+
+int32_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CPR_OK : CPR_ERR_CUDA; }
+
+constexpr int kMaxProfileEvents = 8;
+cudaEvent_t g_profile_events[kMaxProfileEvents] = {};
+int g_profile_n = 0;
+
+}  // namespace
+
+cudaEvent_t cpr::profile_event(int i) { return (i >= 0 && i < g_profile_n) ? g_profile_events[i] : nullptr; }
+
+extern "C" {
+
+int cpr_gdn_supported(int32_t dk, int32_t dv, int32_t C, int32_t dtype)
+{
+    return (dtype_ok(dtype) && shape_built(dk, dv, C)) ? 1 : 0;
+}
+
+int32_t cpr_gdn_version(void) { return 1; }
+
+const char* cpr_gdn_strerror(int32_t code)
+{
+    switch (code) {
+        case CPR_OK: return "ok";
+        case CPR_ERR_INVALID_ARG: return "invalid argument";
+        case CPR_ERR_UNSUPPORTED_SHAPE: return "unsupported (dk, dv, C) or dtype";
+        case CPR_ERR_MISALIGNED: return "misaligned pointer";
+        case CPR_ERR_WORKSPACE: return "workspace missing or too small";
+        case CPR_ERR_CUDA: return "CUDA launch or runtime error";
+        default: return "unknown error";
+    }
+}
+
+int64_t cpr_gdn_num_chunks(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t C)
+{
+    if (!cu_seqlens_host || n_seqs < 0 || C <= 0 || cu_seqlens_host[0] != 0) return CPR_ERR_INVALID_ARG;
+    int64_t total = 0;
+    for (int32_t n = 0; n < n_seqs; ++n) {
+        const int64_t L = (int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n];
+        if (L < 0) return CPR_ERR_INVALID_ARG;
+        total += (L + C - 1) / C;
+    }
+    return total;
+}
+
+size_t cpr_gdn_prefill_workspace_size(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk, int32_t dv,
+                                      int32_t C)
+{
+    if (total_tokens < 0 || n_seqs < 0 || H <= 0 || dk <= 0 || dv <= 0 || C <= 0) return 0;
+    return PrefillLayout(total_tokens, n_seqs, H, dk, dv, C).total;
+}
+
+size_t cpr_gdn_decode_workspace_size(int32_t B, int32_t H, int32_t dk, int32_t dv, int32_t C)
+{
+    if (B < 0 || H <= 0 || dk <= 0 || dv <= 0 || C <= 0) return 0;
+    return kAlign;
+}
+
+int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                        int32_t dv, int32_t C, int32_t dtype, const float* state_in, void* out, float* state_out,
+                        float* boundary_states, int64_t boundary_capacity, void* workspace,
+                        size_t workspace_bytes, void* stream)
+{
+    if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype) ||
+        boundary_capacity < 0)
+        return CPR_ERR_INVALID_ARG;
+    if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
+    if (n_seqs == 0) return CPR_OK;
+    if (!cu_seqlens || !state_out || !workspace) return CPR_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out || !boundary_states)) return CPR_ERR_INVALID_ARG;
+    const PrefillLayout lay(total_tokens, n_seqs, H, dk, dv, C);
+    if (workspace_bytes < lay.total) return CPR_ERR_WORKSPACE;
+    const void* a16[] = {q, k, v, out, state_out, boundary_states, workspace, state_in};
+    for (const void* p : a16)
+        if (p && !aligned(p, 16)) return CPR_ERR_MISALIGNED;
+    const void* a4[] = {g, beta, cu_seqlens};
+    for (const void* p : a4)
+        if (p && !aligned(p, 4)) return CPR_ERR_MISALIGNED;
+
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    PrefillArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.cu_seqlens = cu_seqlens;
+    a.n_seqs = n_seqs;
+    a.total_tokens = total_tokens;
+    a.H = H;
+    a.state_in = state_in;
+    a.out = out;
+    a.state_out = state_out;
+    a.boundary = boundary_states;
+    a.boundary_capacity = boundary_states ? boundary_capacity : 0;
+    a.ws = ws;
+    a.status = reinterpret_cast<uint32_t*>(ws);
+    a.cu_chunks = reinterpret_cast<int32_t*>(ws + lay.cu_chunks);
+    a.wt = reinterpret_cast<float*>(ws + lay.wt);
+    a.ut = reinterpret_cast<float*>(ws + lay.ut);
+    a.dvec = reinterpret_cast<float*>(ws + lay.dvec);
+    a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);
+    if (!boundary_states) {
+        // boundary states are also the chain's hand-off to the intra-chunk kernel
+        return CPR_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorInvalidValue;
+#define CPR_DISPATCH(DK, DV, CC)                                                                            \
+    if (dk == DK && dv == DV && C == CC)                                                                    \
+        e = (dtype == CPR_DTYPE_BF16) ? launch_prefill<DK, DV, CC, __nv_bfloat16>(a, s)                      \
+                                      : launch_prefill<DK, DV, CC, float>(a, s);
+    CPR_FOR_EACH_SHAPE(CPR_DISPATCH)
+#undef CPR_DISPATCH
+    return from_cuda(e);
+}
+
+int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, const float* beta,
+                                  const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
+                                  int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* boundary_states,
+                                  const float* state_out, const cpr_gdn_ring* ring, void* stream)
+{
+    if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype))
+        return CPR_ERR_INVALID_ARG;
+    if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
+    if (n_seqs == 0) return CPR_OK;
+    if (!ring || !ring->S_b || !ring->k || !ring->v || !ring->g || !ring->beta || !cu_seqlens || !state_out)
+        return CPR_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!boundary_states || !k || !v || !g || !beta)) return CPR_ERR_INVALID_ARG;
+    const void* a16[] = {k, v, boundary_states, state_out, ring->S_b, ring->k, ring->v};
+    for (const void* p : a16)
+        if (p && !aligned(p, 16)) return CPR_ERR_MISALIGNED;
+    const void* a4[] = {g, beta, cu_seqlens, ring->g, ring->beta};
+    for (const void* p : a4)
+        if (p && !aligned(p, 4)) return CPR_ERR_MISALIGNED;
+    RingArgs a;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.cu_seqlens = cu_seqlens;
+    a.n_seqs = n_seqs;
+    a.total_tokens = total_tokens;
+    a.H = H;
+    a.boundary = boundary_states;
+    a.state_out = state_out;
+    a.ring = *ring;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorInvalidValue;
+#define CPR_DISPATCH(DK, DV, CC)                                                                           \
+    if (dk == DK && dv == DV && C == CC)                                                                   \
+        e = (dtype == CPR_DTYPE_BF16) ? launch_ring_from_prefill<DK, DV, CC, __nv_bfloat16>(a, s)           \
+                                      : launch_ring_from_prefill<DK, DV, CC, float>(a, s);
+    CPR_FOR_EACH_SHAPE(CPR_DISPATCH)
+#undef CPR_DISPATCH
+    return from_cuda(e);
+}
+
+int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                       float* state, const cpr_gdn_ring* ring, const int32_t* pos, int32_t B, int32_t H, int32_t dk,
+                       int32_t dv, int32_t C, int32_t dtype, void* out, void* workspace, size_t workspace_bytes,
+                       void* stream)
+{
+    if (B < 0 || H <= 0 || H > 65535 || !dtype_ok(dtype)) return CPR_ERR_INVALID_ARG;
+    if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
+    if (B == 0) return CPR_OK;
+    if (!q || !k || !v || !g || !beta || !state || !ring || !pos || !out || !ring->S_b || !ring->k || !ring->v ||
+        !ring->g || !ring->beta)
+        return CPR_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kAlign) return CPR_ERR_WORKSPACE;
+    const void* a16[] = {q, k, v, out, state, ring->S_b, ring->k, ring->v, workspace};
+    for (const void* p : a16)
+        if (!aligned(p, 16)) return CPR_ERR_MISALIGNED;
+    const void* a4[] = {g, beta, pos, ring->g, ring->beta};
+    for (const void* p : a4)
+        if (!aligned(p, 4)) return CPR_ERR_MISALIGNED;
+    DecodeArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.state = state;
+    a.ring = *ring;
+    a.pos = pos;
+    a.B = B;
+    a.H = H;
+    a.out = out;
+    a.status = static_cast<uint32_t*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorInvalidValue;
+#define CPR_DISPATCH(DK, DV, CC)                                                                  \
+    if (dk == DK && dv == DV && C == CC)                                                          \
+        e = (dtype == CPR_DTYPE_BF16) ? launch_decode<DK, DV, CC, __nv_bfloat16>(a, s)             \
+                                      : launch_decode<DK, DV, CC, float>(a, s);
+    CPR_FOR_EACH_SHAPE(CPR_DISPATCH)
+#undef CPR_DISPATCH
+    return from_cuda(e);
+}
+
+int32_t cpr_gdn_set_profile_events(void* const* events, int32_t n_events)
+{
+    if (!events) {
+        g_profile_n = 0;
+        return CPR_OK;
+    }
+    if (n_events < 5 || n_events > kMaxProfileEvents) return CPR_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n_events; ++i) {
+        if (!events[i]) return CPR_ERR_INVALID_ARG;
+        g_profile_events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    g_profile_n = n_events;
+    return CPR_OK;
+}
+
+int32_t cpr_gdn_device_status(const void* workspace, uint32_t* status_out, void* stream)
+{
+    if (!workspace || !status_out) return CPR_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return CPR_ERR_CUDA;
+    *status_out = v;
+    return CPR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,307 @@
+// decode.cu — CPR decode: one token per sequence, with a resync every C tokens.
+//
+// "IsoExec: Eliminating Trainer-Inference Mismatch in SkyRL", section
+// "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet": decode runs the recurrent form
+// and resynchronises the hidden state every C tokens, which keeps its rounding rhythm
+// the same as prefill's.  Kernels, on the caller's stream:
+//   k4_decode_step   the token step of every (sequence, head) on the state in HBM (the
+//                    same per-element operations as prefill's intra-chunk kernel), the
+//                    output, and the token's slot in the ring
+//   k5_resync        for sequences whose token completed a chunk: U(ring S_b, ring
+//                    chunk) by the same routines as prefill's chunk prep and chain;
+//                    the result replaces both the state and ring S_b
+//   k6_ring_fill     builds a ring from a prefill's results
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "chunk_update.cuh"
+#include "common.cuh"
+#include "numerics.cuh"
+
+namespace cpr {
+
+template <int VPT>
+struct VecF;
+template <>
+struct VecF<1> {
+    static __device__ __forceinline__ void load(const float* p, float* d) { d[0] = *p; }
+    static __device__ __forceinline__ void store(float* p, const float* d) { *p = d[0]; }
+};
+template <>
+struct VecF<2> {
+    static __device__ __forceinline__ void load(const float* p, float* d)
+    {
+        const float2 x = *reinterpret_cast<const float2*>(p);
+        d[0] = x.x;
+        d[1] = x.y;
+    }
+    static __device__ __forceinline__ void store(float* p, const float* d)
+    {
+        *reinterpret_cast<float2*>(p) = make_float2(d[0], d[1]);
+    }
+};
+template <>
+struct VecF<4> {
+    static __device__ __forceinline__ void load(const float* p, float* d)
+    {
+        const float4 x = *reinterpret_cast<const float4*>(p);
+        d[0] = x.x;
+        d[1] = x.y;
+        d[2] = x.z;
+        d[3] = x.w;
+    }
+    static __device__ __forceinline__ void store(float* p, const float* d)
+    {
+        *reinterpret_cast<float4*>(p) = make_float4(d[0], d[1], d[2], d[3]);
+    }
+};
+
+// ------------------------------------------------------------------------------------
+// k4: decode step.  One CTA per (sequence, head), 8 warps: warp m owns key rows
+// [m*DK/8, (m+1)*DK/8) of the stored state (chain m of the canonical dot) and lane l
+// owns value columns [l*DV/32, (l+1)*DV/32).  Partial chains meet in shared memory and
+// every value column's dot is finished by the canonical tree.
+// ------------------------------------------------------------------------------------
+template <int DK, int DV, int C, typename T>
+__global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
+{
+    constexpr int L = DK / 8, VPT = DV / 32;
+    __shared__ __align__(16) float kf[DK];
+    __shared__ __align__(16) float qf[DK];
+    __shared__ __align__(16) float part[8][DV];
+    __shared__ __align__(16) float part2[8][DV];
+    __shared__ float sc[2];
+
+    const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
+    const int m = tid >> 5, lane = tid & 31;
+    const int p = a.pos[b];
+    if (p < 0) {
+        if (tid == 0 && h == 0) atomicOr(a.status, CPR_DEV_BAD_POS);
+        return;
+    }
+    const int r = p % C;
+    const size_t bh = (size_t)b * H + h;
+    const T* q = static_cast<const T*>(a.q);
+    const T* k = static_cast<const T*>(a.k);
+    const T* v = static_cast<const T*>(a.v);
+    T* rk = static_cast<T*>(a.ring.k);
+    T* rv = static_cast<T*>(a.ring.v);
+
+    for (int idx = tid; idx < DK; idx += 256) {
+        const T kk = k[bh * DK + idx];
+        kf[idx] = to_f32<T>(kk);
+        qf[idx] = to_f32<T>(q[bh * DK + idx]);
+        rk[(bh * C + r) * DK + idx] = kk;
+    }
+    for (int idx = tid; idx < DV; idx += 256) rv[(bh * C + r) * DV + idx] = v[bh * DV + idx];
+    if (tid == 0) {
+        const float gg = a.g[bh], bb = a.beta[bh];
+        sc[0] = decay_exp(gg);
+        sc[1] = bb;
+        a.ring.g[bh * C + r] = gg;
+        a.ring.beta[bh * C + r] = bb;
+    }
+    float s[L][VPT];
+    float* st = a.state + bh * DK * DV + (size_t)(m * L) * DV + lane * VPT;
+#pragma unroll
+    for (int t = 0; t < L; ++t) VecF<VPT>::load(st + (size_t)t * DV, s[t]);
+    __syncthreads();
+
+    const float alpha = sc[0], beta = sc[1];
+#pragma unroll
+    for (int e = 0; e < VPT; ++e) {
+        float c = __fmul_rn(s[0][e], kf[m * L]);
+#pragma unroll
+        for (int t = 1; t < L; ++t) c = __fmaf_rn(s[t][e], kf[m * L + t], c);
+        part[m][lane * VPT + e] = c;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < VPT; ++e) {
+        const int i = lane * VPT + e;
+        const float x = tree8(part[0][i], part[1][i], part[2][i], part[3][i], part[4][i], part[5][i], part[6][i],
+                              part[7][i]);
+        const float u = step_u(alpha, beta, to_f32<T>(v[bh * DV + i]), x);
+#pragma unroll
+        for (int t = 0; t < L; ++t) s[t][e] = step_s(s[t][e], alpha, u, kf[m * L + t]);
+        float c = __fmul_rn(s[0][e], qf[m * L]);
+#pragma unroll
+        for (int t = 1; t < L; ++t) c = __fmaf_rn(s[t][e], qf[m * L + t], c);
+        part2[m][i] = c;
+    }
+#pragma unroll
+    for (int t = 0; t < L; ++t) VecF<VPT>::store(st + (size_t)t * DV, s[t]);
+    __syncthreads();
+    if (m == 0) {
+        T* out = static_cast<T*>(a.out);
+#pragma unroll
+        for (int e = 0; e < VPT; ++e) {
+            const int i = lane * VPT + e;
+            const float o = tree8(part2[0][i], part2[1][i], part2[2][i], part2[3][i], part2[4][i], part2[5][i],
+                                  part2[6][i], part2[7][i]);
+            out[bh * DV + i] = from_f32<T>(o);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// k5: resync.  One CTA per (sequence, head); returns at once unless the sequence's
+// token completed a chunk.  Phase A is chunk_decays_and_A + chunk_column (as prefill's
+// k1), phase B is delta_tile + snew_tile over all value rows (as prefill's k2).
+// ------------------------------------------------------------------------------------
+template <int DK, int DV, int C>
+struct K5Smem {
+    static constexpr size_t floats = PrepSmem<DK, C>::floats + (size_t)DK * C + (size_t)C * DV + (size_t)DK * DV;
+    static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <int DK, int DV, int C, typename T>
+__global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
+{
+    extern __shared__ __align__(16) float sm5[];
+    const PrepSmem<DK, C> s(sm5);
+    constexpr int KS = PrepSmem<DK, C>::KS;
+    float* Wt = sm5 + PrepSmem<DK, C>::floats;  // [DK][C]
+    float* Us = Wt + DK * C;                     // [C][DV]  U~, then d * delta in place
+    float* St = Us + C * DV;                     // [DK][DV] ring S_b (storage order)
+
+    const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
+    const int p = a.pos[b];
+    if (p < 0 || p % C != C - 1) return;
+    const size_t bh = (size_t)b * H + h;
+    const T* rk = static_cast<const T*>(a.ring.k) + bh * C * DK;
+    const T* rv = static_cast<const T*>(a.ring.v) + bh * C * DV;
+    const float* sb = a.ring.S_b + bh * DK * DV;
+
+    for (int idx = tid; idx < C * DK; idx += blockDim.x) s.kf[(idx / DK) * KS + idx % DK] = to_f32<T>(rk[idx]);
+    for (int idx = tid; idx < DK * DV / 4; idx += blockDim.x)
+        reinterpret_cast<float4*>(St)[idx] = reinterpret_cast<const float4*>(sb)[idx];
+    if (tid < C) {
+        s.G[tid] = a.ring.g[bh * C + tid];
+        s.bs[tid] = a.ring.beta[bh * C + tid];
+    }
+    chunk_decays_and_A<DK, C>(s);
+    {
+        float x[C];
+        const int col = tid;
+        chunk_column<DK, DV, C, T>(s, col, rv, (size_t)DV, x);
+        if (col < DK) {
+#pragma unroll
+            for (int r = 0; r < C; ++r) Wt[col * C + r] = x[r];
+        } else {
+#pragma unroll
+            for (int r = 0; r < C; ++r) Us[r * DV + (col - DK)] = x[r];
+        }
+    }
+    __syncthreads();
+    for (int t = tid; t < (C / 4) * (DV / 4); t += blockDim.x) {
+        const int r0 = (t / (DV / 4)) * 4, n0 = (t % (DV / 4)) * 4;
+        float o[4][4];
+        delta_tile<DK>(Wt, C, St, DV, Us, DV, s.dvs, r0, n0, o);
+#pragma unroll
+        for (int aa = 0; aa < 4; ++aa)
+            *reinterpret_cast<float4*>(Us + (r0 + aa) * DV + n0) = make_float4(o[aa][0], o[aa][1], o[aa][2], o[aa][3]);
+    }
+    __syncthreads();
+    const float gamma = decay_exp(s.G[C - 1]);
+    float* st_out = a.state + bh * DK * DV;
+    float* sb_out = a.ring.S_b + bh * DK * DV;
+    for (int t = tid; t < (DV / 4) * (DK / 4); t += blockDim.x) {
+        const int c0 = (t % (DK / 4)) * 4, n0 = (t / (DK / 4)) * 4;
+        float o[4][4];
+        snew_tile<C>(St, DV, Us, DV, s.kf, KS, gamma, n0, c0, o);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const float4 val = make_float4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]);
+            *reinterpret_cast<float4*>(st_out + (size_t)(c0 + cc) * DV + n0) = val;
+            *reinterpret_cast<float4*>(sb_out + (size_t)(c0 + cc) * DV + n0) = val;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// k6: ring fill from a prefill.  One CTA per (sequence, head).
+// ------------------------------------------------------------------------------------
+template <int DK, int DV, int C, typename T>
+__global__ void __launch_bounds__(256) k6_ring_fill(RingArgs a)
+{
+    const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
+    __shared__ long long cbase;
+    __shared__ int valid;
+    if (tid == 0) {
+        long long acc = 0;
+        int ok = a.cu_seqlens[0] == 0;
+        for (int m = 0; m < n; ++m) {
+            const int Lm = a.cu_seqlens[m + 1] - a.cu_seqlens[m];
+            ok &= (Lm >= 0);
+            acc += (Lm > 0) ? (Lm + C - 1) / C : 0;
+        }
+        cbase = acc;
+        valid = ok && a.cu_seqlens[n + 1] >= a.cu_seqlens[n] && (int64_t)a.cu_seqlens[n + 1] <= a.total_tokens;
+    }
+    __syncthreads();
+    if (!valid) return;
+    const int64_t t0 = a.cu_seqlens[n];
+    const int64_t L = a.cu_seqlens[n + 1] - t0;
+    const int rem = (int)(L % C);
+    const size_t nh = (size_t)n * H + h;
+    const size_t SS = (size_t)DK * DV;
+    const float* src = (rem != 0) ? a.boundary + ((size_t)(cbase + (L + C - 1) / C - 1) * H + h) * SS
+                                   : a.state_out + nh * SS;
+    float* dst = a.ring.S_b + nh * SS;
+    for (size_t idx = tid; idx < SS / 4; idx += blockDim.x)
+        reinterpret_cast<float4*>(dst)[idx] = reinterpret_cast<const float4*>(src)[idx];
+    const T* k = static_cast<const T*>(a.k);
+    const T* v = static_cast<const T*>(a.v);
+    T* rk = static_cast<T*>(a.ring.k);
+    T* rv = static_cast<T*>(a.ring.v);
+    const int64_t tf = t0 + L - rem;  // first token of the final partial chunk
+    for (int idx = tid; idx < rem * DK; idx += blockDim.x) {
+        const int r = idx / DK, jj = idx % DK;
+        rk[(nh * C + r) * DK + jj] = k[((size_t)(tf + r) * H + h) * DK + jj];
+    }
+    for (int idx = tid; idx < rem * DV; idx += blockDim.x) {
+        const int r = idx / DV, jj = idx % DV;
+        rv[(nh * C + r) * DV + jj] = v[((size_t)(tf + r) * H + h) * DV + jj];
+    }
+    if (tid < rem) {
+        a.ring.g[nh * C + tid] = a.g[(size_t)(tf + tid) * H + h];
+        a.ring.beta[nh * C + tid] = a.beta[(size_t)(tf + tid) * H + h];
+    }
+}
+
+// ------------------------------------------------------------------------------------
+template <int DK, int DV, int C, typename T>
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    profile_mark(0, s);
+    k4_decode_step<DK, DV, C, T><<<dim3(a.B, a.H), 256, 0, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    profile_mark(1, s);
+    const size_t sm5 = K5Smem<DK, DV, C>::bytes;
+    e = cudaFuncSetAttribute(k5_resync<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
+    if (e != cudaSuccess) return e;
+    k5_resync<DK, DV, C, T><<<dim3(a.B, a.H), DK + DV, sm5, s>>>(a);
+    e = cudaGetLastError();
+    profile_mark(2, s);
+    return e;
+}
+
+template <int DK, int DV, int C, typename T>
+cudaError_t launch_ring_from_prefill(const RingArgs& a, cudaStream_t s)
+{
+    k6_ring_fill<DK, DV, C, T><<<dim3(a.n_seqs, a.H), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+#define CPR_INST_DECODE(DK, DV, C)                                                                         \
+    template cudaError_t launch_decode<DK, DV, C, float>(const DecodeArgs&, cudaStream_t);                \
+    template cudaError_t launch_decode<DK, DV, C, __nv_bfloat16>(const DecodeArgs&, cudaStream_t);        \
+    template cudaError_t launch_ring_from_prefill<DK, DV, C, float>(const RingArgs&, cudaStream_t);       \
+    template cudaError_t launch_ring_from_prefill<DK, DV, C, __nv_bfloat16>(const RingArgs&, cudaStream_t);
+CPR_FOR_EACH_SHAPE(CPR_INST_DECODE)
+
+}  // namespace cpr
