@@ -177,6 +177,35 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
                        size_t workspace_bytes, void* stream);
 
 /*
+ * Prefill for callers that cannot allocate device memory.  (The pages have no
+ * counterpart of this entry point; it belongs to this library's interface only.)
+ *
+ * Serving runtimes that reserve all device memory for their own pool, loops that must
+ * not hit the device synchronisation an allocation can cause, and C hosts without a
+ * device allocator cannot provide cpr_gdn_prefill's workspace.  This entry point takes
+ * the same arguments minus the workspace and uses a scratch array of
+ * CPR_GDN_NOALLOC_SCRATCH_BYTES owned by the library (a static device array: every GPU
+ * that loads the library's device code holds it until the process exits).  It calls no
+ * allocating routine.  The caller still provides every input and output buffer.
+ *   - Problems whose cpr_gdn_prefill_workspace_size() exceeds
+ *     CPR_GDN_NOALLOC_SCRATCH_BYTES are rejected with CPR_ERR_WORKSPACE before any work
+ *     is enqueued (for dk = dv = 128, C = 64 that is about 250 chunk-heads, e.g. 16 heads
+ *     x 15 chunks).
+ *   - The first call on each device looks up the scratch's device address with that
+ *     device current (this may load the library's device code): make it before any
+ *     stream capture begins.
+ *   - All calls share the scratch, which keeps the last call's contents (nothing in it
+ *     needs to start at zero).  Calls that overlap on the GPU race on it: serialise them.
+ *   - The device status word lives in that scratch and is not readable by the caller.
+ * Results are those cpr_gdn_prefill returns for the same arguments.
+ */
+#define CPR_GDN_NOALLOC_SCRATCH_BYTES (16u << 20)
+int32_t cpr_gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
+                                int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* state_in, void* out,
+                                float* state_out, float* boundary_states, int64_t boundary_capacity, void* stream);
+
+/*
  * Profiling hook (used by the benchmark to time each kernel with CUDA events on the
  * stream it runs on).  events: n_events cudaEvent_t handles created by the caller, or
  * NULL to switch the hook off.  While it is on, every cpr_gdn_prefill records

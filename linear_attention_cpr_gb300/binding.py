@@ -25,7 +25,9 @@ EXPORTED = (
     "cpr_gdn_supported", "cpr_gdn_version", "cpr_gdn_strerror", "cpr_gdn_num_chunks",
     "cpr_gdn_prefill_workspace_size", "cpr_gdn_decode_workspace_size", "cpr_gdn_prefill",
     "cpr_gdn_ring_from_prefill", "cpr_gdn_decode", "cpr_gdn_device_status", "cpr_gdn_set_profile_events",
+    "cpr_gdn_prefill_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 16 << 20  # CPR_GDN_NOALLOC_SCRATCH_BYTES
 
 
 class CprError(RuntimeError):
@@ -73,6 +75,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                  SZ, P]),
         "cpr_gdn_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
         "cpr_gdn_set_profile_events": (I32, [ctypes.POINTER(ctypes.c_void_p), I32]),
+        "cpr_gdn_prefill_noalloc": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P, P, P, I64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -244,3 +247,25 @@ def cpr_gdn_set_profile_events(events) -> None:
             e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check("cpr_gdn_set_profile_events", lib.cpr_gdn_set_profile_events(arr, len(events)))
+
+
+def cpr_gdn_prefill_noalloc(q, k, v, g, beta, cu_seqlens, C: int, state_in=None, *, out, state_out,
+                            boundary_states, stream=None):
+    """Prefill without a caller workspace: the library's static scratch is used instead.
+
+    For callers that must not allocate device memory while the layer runs (their runtime
+    owns a fixed memory pool, or an allocation's device synchronisation is unacceptable).
+    The caller passes every output buffer; this call allocates nothing.  Problems needing
+    more than NOALLOC_SCRATCH_BYTES of scratch raise CprError (CPR_ERR_WORKSPACE).  The
+    first call on a device looks up the scratch's address (make it before any stream
+    capture); calls that overlap on the GPU race on the shared scratch.
+    """
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    code = load_library().cpr_gdn_prefill_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, C, _dtype_code(q),
+        _ptr(state_in), _ptr(out), _ptr(state_out), _ptr(boundary_states), boundary_states.shape[0],
+        _stream(stream))
+    _check("cpr_gdn_prefill_noalloc", code)
+    return out, state_out, boundary_states
