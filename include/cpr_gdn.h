@@ -63,6 +63,7 @@ extern "C" {
 #define CPR_DEV_BAD_CU_SEQLENS 1u /* cu_seqlens[0] != 0, decreasing, or last != total_tokens */
 #define CPR_DEV_BOUNDARY_CAPACITY 2u /* more chunks than boundary_capacity */
 #define CPR_DEV_BAD_POS 4u        /* a decode position is negative */
+#define CPR_DEV_TIMEOUT 8u        /* a tensor-core wait gave up (work of that CTA skipped) */
 
 /* Element types of q, k, v, out and the ring's k, v. */
 #define CPR_DTYPE_BF16 0
@@ -189,8 +190,8 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
  * allocating routine.  The caller still provides every input and output buffer.
  *   - Problems whose cpr_gdn_prefill_workspace_size() exceeds
  *     CPR_GDN_NOALLOC_SCRATCH_BYTES are rejected with CPR_ERR_WORKSPACE before any work
- *     is enqueued (for dk = dv = 128, C = 64 that is about 250 chunk-heads, e.g. 16 heads
- *     x 15 chunks).
+ *     is enqueued (for dk = dv = 128, C = 64 that is about 120 chunk-heads, e.g. 16 heads
+ *     x 7 chunks).
  *   - The first call on each device looks up the scratch's device address with that
  *     device current (this may load the library's device code): make it before any
  *     stream capture begins.

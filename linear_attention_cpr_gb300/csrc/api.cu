@@ -121,9 +121,8 @@ int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float
     a.ws = ws;
     a.status = reinterpret_cast<uint32_t*>(ws);
     a.cu_chunks = reinterpret_cast<int32_t*>(ws + lay.cu_chunks);
-    a.wt = reinterpret_cast<float*>(ws + lay.wt);
-    a.ut = reinterpret_cast<float*>(ws + lay.ut);
-    a.dvec = reinterpret_cast<float*>(ws + lay.dvec);
+    a.mt = ws + lay.mt;
+    a.bt = reinterpret_cast<float*>(ws + lay.bt);
     a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);
     if (!boundary_states) {
         // boundary states are also the chain's hand-off to the intra-chunk kernel

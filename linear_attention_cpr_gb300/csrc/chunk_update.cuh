@@ -4,6 +4,7 @@
 #pragma once
 
 #include "numerics.cuh"
+#include "tc.cuh"
 
 namespace cpr {
 
@@ -21,6 +22,9 @@ struct PrepSmem {
     float* dvs;  // [C]  d_r
     __device__ explicit PrepSmem(float* base)
         : kf(base), A(base + C * KS), G(A + C * C), be(G + C), bs(be + C), dvs(bs + C) {}
+    // keys and A at `base`, the four per-token vectors at `vec`
+    __device__ PrepSmem(float* base, float* vec)
+        : kf(base), A(base + C * KS), G(vec), be(vec + C), bs(vec + 2 * C), dvs(vec + 3 * C) {}
 };
 
 // G, e, d, beta*e and the strictly lower-triangular A from kf, g (in G) and beta (in bs).
@@ -77,6 +81,285 @@ __device__ __forceinline__ void chunk_column(const PrepSmem<DK, C>& s, int col, 
         for (int r = 0; r < C; ++r) x[r] = __fmul_rn(s.bs[r], to_f32<T>(vbase[(size_t)r * vstride + (col - DK)]));
     }
     fwd_subst<C>(s.A, C, x);
+}
+
+// ======================================================================================
+// Tensor-core half of the chunk update.  U is applied in the matrix form
+//     S_new = S_b M + B,   M = gamma I - W^T (D K),   B = U~^T (D K),   D = diag(d_r)
+// (the WY relations above, with the state-dependent term written as S_b W^T (D K)).
+//   prep (state independent), two tcgen05 products with K = C:
+//        X = (D K)^T W   (M = 128 rows c, N = DK)   ->  Mt = gamma I - X   (Mt[c][c'] = M[c'][c])
+//        B = U~^T (D K)  (M = 128 rows i, N = DK)
+//        bf16 hi/lo splits of every operand, three products hi*hi + hi*lo + lo*hi
+//        accumulated in fp32 in TMEM; Mt is split into bf16 hi/lo (the chain's B operand
+//        image), B kept fp32 [DV][DK].
+//   chain step: D = S_b M as one tcgen05 product (M = 128 rows i, N = DK, K = DK), the
+//        state tile holding S_b's bf16 splits, three products as above; then
+//        S_new[i][c] = D[i][c] + B[i][c] (one add).
+// Both products have a fixed instruction sequence, so prefill's kernels and decode's
+// resync produce the same bits.  Rows beyond DK (or DV) of the M = 128 products are zero.
+// ======================================================================================
+template <int DK, int DV, int C>
+struct UCfg {
+    static constexpr int MPAD = 128;
+    static constexpr int NB = DK + DV;
+    static constexpr uint32_t AOP_SPLIT = MPAD * C * 2;  // bf16 (D K)^T tile, one split
+    static constexpr uint32_t BOP_SPLIT = NB * C * 2;    // bf16 [W | U~]^T tile, one split
+    static constexpr uint32_t MT_SPLIT = DK * DK * 2;    // bf16 Mt tile [DK][DK], one split
+    static constexpr uint32_t MT_BYTES = 2 * MT_SPLIT;
+    static constexpr uint32_t BT_BYTES = DK * DV * 4;    // fp32 B [DV][DK]
+    static constexpr uint32_t S_SPLIT = 64 * DK * 2;     // bf16 S tile of one 64-row slice, one split
+    static constexpr int NSLICE = (DV + 63) / 64;        // chain slices of 64 value rows
+    // prep shared memory: R1 = keys + A (FP32 phase), later the [W | U~] operand
+    static constexpr uint32_t R1A = (uint32_t)(sizeof(float) * ((size_t)C * PrepSmem<DK, C>::KS + (size_t)C * C));
+    static constexpr uint32_t R1 = (R1A > 2 * BOP_SPLIT ? R1A : 2 * BOP_SPLIT);
+    static constexpr uint32_t AOP_OFF = (R1 + 1023) / 1024 * 1024;
+    static constexpr uint32_t VEC_OFF = AOP_OFF + 2 * AOP_SPLIT;
+    static constexpr uint32_t PREP_BYTES = VEC_OFF + 4 * C * 4;
+    static constexpr uint32_t TMEM_COLS = 2 * DK <= 32 ? 32 : 2 * DK <= 64 ? 64 : 2 * DK <= 128 ? 128 : 256;
+    // decode resync (prep and one chain step in one CTA): [R1 | Mt] [Aop | Bt] [vectors] [S tile]
+    static constexpr uint32_t up1k(uint32_t x) { return (x + 1023) / 1024 * 1024; }
+    static constexpr uint32_t RS_BT_OFF = up1k(R1 > MT_BYTES ? R1 : MT_BYTES);
+    static constexpr uint32_t RS_VEC_OFF = up1k(RS_BT_OFF + (2 * AOP_SPLIT > BT_BYTES ? 2 * AOP_SPLIT : BT_BYTES));
+    static constexpr uint32_t RS_S_OFF = up1k(RS_VEC_OFF + 4 * C * 4);
+    static constexpr uint32_t RS_BAR_OFF = RS_S_OFF + NSLICE * 2 * S_SPLIT;
+    static constexpr uint32_t RS_BYTES = RS_BAR_OFF + 64;
+    static constexpr uint32_t PREP_BAR_OFF = (PREP_BYTES + 15) / 16 * 16;
+    static constexpr uint32_t PREP_SMEM = PREP_BAR_OFF + 64;
+    static constexpr uint32_t prep_idesc = tc::idesc_bf16(MPAD, DK);
+};
+
+// Build both prep operands in shared memory from the chunk's keys (s.kf, fp32), g (s.G)
+// and beta (s.bs); V element (r, n) at vbase[r * vstride + n].  All threads; contains
+// __syncthreads.  On return aop / bop hold the bf16 splits and are visible to the
+// tensor cores.
+template <int DK, int DV, int C, typename T>
+__device__ __forceinline__ void prep_operands(const PrepSmem<DK, C>& s, unsigned char* aop, unsigned char* bop,
+                                              const T* vbase, size_t vstride)
+{
+    using U = UCfg<DK, DV, C>;
+    constexpr int KS = PrepSmem<DK, C>::KS;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    chunk_decays_and_A<DK, C>(s);
+    // (D K)^T rows c: d_r * k_r[c] (zero rows beyond DK)
+    for (int row = tid; row < U::MPAD; row += nt) {
+#pragma unroll
+        for (int r0 = 0; r0 < C; r0 += 8) {
+            uint16_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float x = row < DK ? __fmul_rn(s.dvs[r0 + e], s.kf[(r0 + e) * KS + row]) : 0.0f;
+                tc::split_bf16(x, hi[e], lo[e]);
+            }
+            const uint32_t off = tc::tile_off<2>(row, r0, C);
+            *reinterpret_cast<uint4*>(aop + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
+                                                              hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
+            *reinterpret_cast<uint4*>(aop + U::AOP_SPLIT + off) =
+                make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
+                           lo[6] | (uint32_t)lo[7] << 16);
+        }
+    }
+    float x[C];
+    chunk_column<DK, DV, C, T>(s, tid, vbase, vstride, x);
+    __syncthreads();  // keys and A are dead: their space becomes the [W | U~]^T operand
+#pragma unroll
+    for (int r0 = 0; r0 < C; r0 += 8) {
+        uint16_t hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tc::split_bf16(x[r0 + e], hi[e], lo[e]);
+        const uint32_t off = tc::tile_off<2>(tid, r0, C);
+        *reinterpret_cast<uint4*>(bop + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
+                                                          hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
+        *reinterpret_cast<uint4*>(bop + U::BOP_SPLIT + off) =
+            make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
+                       lo[6] | (uint32_t)lo[7] << 16);
+    }
+    tc::fence_proxy_async();
+    __syncthreads();
+}
+
+// One thread: both prep products (X into TMEM columns [0, DK), B into [DK, 2 DK)), then
+// commit to mbar.  aop = (D K)^T tile (128 rows c, K = C); bop = [W | U~]^T tile (rows
+// 0..DK-1 = W^T, rows DK.. = U~^T).
+template <int DK, int DV, int C>
+__device__ __forceinline__ void prep_mma(uint32_t tmem, const unsigned char* aop, const unsigned char* bop,
+                                         uint64_t* mbar)
+{
+    using U = UCfg<DK, DV, C>;
+    constexpr uint32_t SBO = (C / 8) * 128;
+    const uint32_t ao = tc::smem_u32(aop), bo = tc::smem_u32(bop);
+    const uint32_t uo = bo + (DK / 8) * SBO;  // U~^T rows start after the DK rows of W^T
+    const uint32_t ha[3] = {0u, 0u, 1u}, hb[3] = {0u, 1u, 0u};  // hi*hi, hi*lo, lo*hi
+    tc::fence_after_sync();
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+            tc::mma_bf16(tmem, tc::sdesc(ao + ha[p] * U::AOP_SPLIT + k * 256, 128, SBO),
+                         tc::sdesc(bo + hb[p] * U::BOP_SPLIT + k * 256, 128, SBO), U::prep_idesc, (p | k) ? 1u : 0u);
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+            tc::mma_bf16(tmem + DK, tc::sdesc(uo + ha[p] * U::BOP_SPLIT + k * 256, 128, SBO),
+                         tc::sdesc(ao + hb[p] * U::AOP_SPLIT + k * 256, 128, SBO), U::prep_idesc, (p | k) ? 1u : 0u);
+    tc::commit(mbar);
+}
+
+// All threads, after the prep products completed: the Mt image (bf16 splits; rows c,
+// K = c') and B (fp32 [DV][DK]) to generic destinations.  Warp w reads TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31.
+template <int DK, int DV, int C>
+__device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsigned char* mt_out, float* b_out)
+{
+    using U = UCfg<DK, DV, C>;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    tc::fence_after_sync();
+    constexpr int NG = 2 * DK / 32;  // 32-column groups: X then B
+    const int q = warp & 3;
+    const int row = q * 32 + lane;  // this thread's TMEM lane
+    if (q * 32 < (DK > DV ? DK : DV)) {
+        for (int g = warp >> 2; g < NG; g += (nw + 3) / 4) {
+            float v[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(g * 32), v);
+            if (g < DK / 32) {  // Mt[c][c'] = gamma [c == c'] - X[c][c'], row c = this lane
+                if (row >= DK) continue;
+                const int col0 = g * 32;
+#pragma unroll
+                for (int e8 = 0; e8 < 32; e8 += 8) {
+                    uint16_t hi[8], lo[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int cc = col0 + e8 + e;
+                        const float m = (cc == row) ? __fsub_rn(gamma, v[e8 + e]) : -v[e8 + e];
+                        tc::split_bf16(m, hi[e], lo[e]);
+                    }
+                    const uint32_t off = tc::tile_off<2>(row, col0 + e8, DK);
+                    *reinterpret_cast<uint4*>(mt_out + off) =
+                        make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
+                                   hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
+                    *reinterpret_cast<uint4*>(mt_out + U::MT_SPLIT + off) =
+                        make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16,
+                                   lo[4] | (uint32_t)lo[5] << 16, lo[6] | (uint32_t)lo[7] << 16);
+                }
+            } else {  // B[i][c], row i = this lane
+                if (row >= DV) continue;
+                float4* dst = reinterpret_cast<float4*>(b_out + (size_t)row * DK + (g * 32 - DK));
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4)
+                    dst[e4] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
+            }
+        }
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+}
+
+// The chain product is issued per slice of 64 value rows (M = 64), in prefill (one CTA
+// per slice) and in decode's resync alike, so both run the same instruction shape.
+// M = 64 accumulator layout: slice row r -> TMEM lane 32*(r/16) + r%16.
+constexpr int kChainRows = 64;
+
+// S tile of one slice (bf16 splits, A operand: rows r = 0..63 <-> value rows row0 + r,
+// zero beyond DV; K = c) from a stored [DK][DV] fp32 state (NULL = zero).  All threads.
+template <int DK, int DV>
+__device__ __forceinline__ void stile_fill(unsigned char* stile, const float* src, int row0)
+{
+    constexpr uint32_t SPLIT = kChainRows * DK * 2;
+    for (int idx = threadIdx.x; idx < kChainRows * (DK / 8); idx += blockDim.x) {
+        const int r = idx % kChainRows, c0 = (idx / kChainRows) * 8, i = row0 + r;
+        uint16_t hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float x = (src && i < DV) ? src[(size_t)(c0 + e) * DV + i] : 0.0f;
+            tc::split_bf16(x, hi[e], lo[e]);
+        }
+        const uint32_t off = tc::tile_off<2>(r, c0, DK);
+        *reinterpret_cast<uint4*>(stile + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
+                                                            hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
+        *reinterpret_cast<uint4*>(stile + SPLIT + off) =
+            make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
+                       lo[6] | (uint32_t)lo[7] << 16);
+    }
+}
+
+// One thread: the chain product of one slice, D = S_slice M, into TMEM columns
+// [col, col + DK); commit to mbar when `commit_after`.
+template <int DK>
+__device__ __forceinline__ void chain_mma(uint32_t tmem_col, const unsigned char* stile, const unsigned char* mt,
+                                          uint64_t* mbar, bool commit_after = true)
+{
+    constexpr uint32_t SBO = (DK / 8) * 128;
+    constexpr uint32_t S_SPLIT = kChainRows * DK * 2, MT_SPLIT = DK * DK * 2;
+    constexpr uint32_t idesc = tc::idesc_bf16(kChainRows, DK);
+    const uint32_t so = tc::smem_u32(stile), mo = tc::smem_u32(mt);
+    const uint32_t hs[3] = {0u, 0u, 1u}, hm[3] = {0u, 1u, 0u};
+    tc::fence_after_sync();
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int k = 0; k < DK / 16; ++k)
+            tc::mma_bf16(tmem_col, tc::sdesc(so + hs[p] * S_SPLIT + k * 256, 128, SBO),
+                         tc::sdesc(mo + hm[p] * MT_SPLIT + k * 256, 128, SBO), idesc, (p | k) ? 1u : 0u);
+    if (commit_after) tc::commit(mbar);
+}
+
+// All threads (NW warps), after the chain product of one slice completed: for slice rows
+// r (value row i = row0 + r < DV), S_new[i][c] = D[r][c] + B[i][c], stored ([DK][DV] fp32)
+// to dst0 and (if not NULL) dst1, and split into stile (if not NULL) for the next product.
+// bslice: fp32 rows of B for this slice (row r at bslice + r * DK), generic address.
+template <int DK, int DV, int NW>
+__device__ __forceinline__ void chain_epilogue(uint32_t tmem_col, const float* bslice, int row0, float* dst0,
+                                               float* dst1, unsigned char* stile)
+{
+    constexpr uint32_t S_SPLIT = kChainRows * DK * 2;
+    constexpr int NG = DK / 32;                  // 32-column groups
+    constexpr int STEP = NW >= 4 ? NW / 4 : 1;   // warps sharing one TMEM quadrant
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = warp & 3;
+    const int r = q * 16 + (lane & 15);  // this thread's slice row (lanes 16..31 carry none)
+    const int i = row0 + r;
+    const bool have = (lane < 16) && (i < DV);
+    tc::fence_after_sync();
+    if (q < NW) {
+        for (int g = warp >> 2; g < NG; g += STEP) {
+            float v[32];
+            tc::tmem_ld32(tmem_col + ((uint32_t)(q * 32) << 16) + (uint32_t)(g * 32), v);
+            if (!have) continue;
+            const float4* b4 = reinterpret_cast<const float4*>(bslice + (size_t)r * DK + g * 32);
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 b = b4[e4];
+                v[4 * e4] = __fadd_rn(v[4 * e4], b.x);
+                v[4 * e4 + 1] = __fadd_rn(v[4 * e4 + 1], b.y);
+                v[4 * e4 + 2] = __fadd_rn(v[4 * e4 + 2], b.z);
+                v[4 * e4 + 3] = __fadd_rn(v[4 * e4 + 3], b.w);
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dst0[(size_t)(g * 32 + e) * DV + i] = v[e];
+            if (dst1) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) dst1[(size_t)(g * 32 + e) * DV + i] = v[e];
+            }
+            if (stile) {
+#pragma unroll
+                for (int e8 = 0; e8 < 32; e8 += 8) {
+                    uint16_t hi[8], lo[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) tc::split_bf16(v[e8 + e], hi[e], lo[e]);
+                    const uint32_t off = tc::tile_off<2>(r, g * 32 + e8, DK);
+                    *reinterpret_cast<uint4*>(stile + off) =
+                        make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
+                                   hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
+                    *reinterpret_cast<uint4*>(stile + S_SPLIT + off) =
+                        make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16,
+                                   lo[4] | (uint32_t)lo[5] << 16, lo[6] | (uint32_t)lo[7] << 16);
+                }
+            }
+        }
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
 }
 
 }  // namespace cpr

@@ -30,20 +30,21 @@ __host__ __device__ inline int64_t max_chunks_bound(int64_t total_tokens, int32_
 // Prefill workspace:
 //   [0, 256)       status word (uint32) and padding
 //   cu_chunks      int32 [n_seqs + 1]
-//   Wt             fp32 [max_chunks, H, DK, C]   (W of every full chunk, transposed)
-//   Ut             fp32 [max_chunks, H, C, DV]   (U~ of every full chunk)
-//   dvec           fp32 [max_chunks, H, C + 4]   (d_r for r < C, gamma at index C)
+//   mt             [max_chunks, H] tiles of 2 * dk * dk bf16: the chunk's M^T, bf16 hi/lo
+//                  splits, in the tensor cores' shared-memory image
+//   bt             fp32 [max_chunks, H, dv, dk]: the chunk's B
 struct PrefillLayout {
-    size_t cu_chunks, wt, ut, dvec, total;
+    size_t cu_chunks, mt, bt, total, mt_bytes, bt_bytes;
     __host__ __device__ PrefillLayout(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk, int32_t dv,
                                       int32_t C)
     {
         const int64_t mc = max_chunks_bound(total_tokens, n_seqs, C);
+        mt_bytes = (size_t)2 * dk * dk * 2;
+        bt_bytes = (size_t)dk * dv * 4;
         cu_chunks = kAlign;
-        wt = align_up(cu_chunks + sizeof(int32_t) * (size_t)(n_seqs + 1), kAlign);
-        ut = align_up(wt + sizeof(float) * (size_t)mc * H * dk * C, kAlign);
-        dvec = align_up(ut + sizeof(float) * (size_t)mc * H * C * dv, kAlign);
-        total = align_up(dvec + sizeof(float) * (size_t)mc * H * (C + 4), kAlign);
+        mt = align_up(cu_chunks + sizeof(int32_t) * (size_t)(n_seqs + 1), kAlign);
+        bt = align_up(mt + mt_bytes * (size_t)mc * H, kAlign);
+        total = align_up(bt + bt_bytes * (size_t)mc * H, kAlign);
     }
 };
 
@@ -65,9 +66,8 @@ struct PrefillArgs {
     unsigned char* ws;
     uint32_t* status;
     int32_t* cu_chunks;
-    float* wt;
-    float* ut;
-    float* dvec;
+    unsigned char* mt;
+    float* bt;
     int64_t max_chunks;
 };
 
@@ -119,6 +119,13 @@ cudaEvent_t profile_event(int i);
 inline void profile_mark(int i, cudaStream_t s)
 {
     if (cudaEvent_t e = profile_event(i)) cudaEventRecord(e, s);
+}
+
+// Dynamic shared memory that keeps at most 512 / tmem_cols CTAs on one SM (233,472 bytes
+// of shared memory per SM, 1 KB reserved per CTA), so the TMEM columns they allocate fit.
+constexpr size_t tmem_cap_smem(uint32_t tmem_cols)
+{
+    return 233472 / (512 / tmem_cols + 1) - 1024 + 16;
 }
 
 template <int DK, int DV, int C, typename T> cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);

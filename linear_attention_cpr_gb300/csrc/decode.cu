@@ -14,6 +14,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "chunk_update.cuh"
 #include "common.cuh"
 #include "numerics.cuh"
@@ -145,78 +147,76 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 }
 
 // ------------------------------------------------------------------------------------
-// k5: resync.  One CTA per (sequence, head); returns at once unless the sequence's
-// token completed a chunk.  Phase A is chunk_decays_and_A + chunk_column (as prefill's
-// k1), phase B is delta_tile + snew_tile over all value rows (as prefill's k2).
+// k5: resync.  One CTA per (sequence, head), DK + DV threads; returns at once unless the
+// sequence's token completed a chunk.  It runs the same routines as prefill: the FP32
+// phase and the prep product of k1_chunk_prep (prep_operands, prep_mma, prep_epilogue,
+// here into shared memory), then one chain product and epilogue of k2_chain (chain_mma,
+// chain_epilogue) on the ring's S_b.  The result replaces both the state and ring S_b.
 // ------------------------------------------------------------------------------------
-template <int DK, int DV, int C>
-struct K5Smem {
-    static constexpr size_t floats = PrepSmem<DK, C>::floats + (size_t)DK * C + (size_t)C * DV + (size_t)DK * DV;
-    static constexpr size_t bytes = floats * sizeof(float);
-};
-
 template <int DK, int DV, int C, typename T>
 __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
 {
-    extern __shared__ __align__(16) float sm5[];
-    const PrepSmem<DK, C> s(sm5);
+    using U = UCfg<DK, DV, C>;
+    extern __shared__ __align__(1024) unsigned char sm5[];
+    const PrepSmem<DK, C> s(reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5 + U::RS_VEC_OFF));
     constexpr int KS = PrepSmem<DK, C>::KS;
-    float* Wt = sm5 + PrepSmem<DK, C>::floats;  // [DK][C]
-    float* Us = Wt + DK * C;                     // [C][DV]  U~, then d * delta in place
-    float* St = Us + C * DV;                     // [DK][DV] ring S_b (storage order)
+    unsigned char* bop = sm5;                    // then the M^T image
+    unsigned char* aop = sm5 + U::RS_BT_OFF;     // then B^T
+    unsigned char* mt = sm5;
+    float* bt = reinterpret_cast<float*>(sm5 + U::RS_BT_OFF);
+    unsigned char* stile = sm5 + U::RS_S_OFF;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm5 + U::RS_BAR_OFF);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
 
     const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
     const int p = a.pos[b];
     if (p < 0 || p % C != C - 1) return;
     const size_t bh = (size_t)b * H + h;
+    const size_t SS = (size_t)DK * DV;
     const T* rk = static_cast<const T*>(a.ring.k) + bh * C * DK;
     const T* rv = static_cast<const T*>(a.ring.v) + bh * C * DV;
-    const float* sb = a.ring.S_b + bh * DK * DV;
 
+    if (tid < 32) tc::tmem_alloc(tslot, U::TMEM_COLS);
+    if (tid == 0) {
+        tc::mbar_init(mbar, 1);
+        tc::fence_mbar_init();
+    }
     for (int idx = tid; idx < C * DK; idx += blockDim.x) s.kf[(idx / DK) * KS + idx % DK] = to_f32<T>(rk[idx]);
-    for (int idx = tid; idx < DK * DV / 4; idx += blockDim.x)
-        reinterpret_cast<float4*>(St)[idx] = reinterpret_cast<const float4*>(sb)[idx];
     if (tid < C) {
         s.G[tid] = a.ring.g[bh * C + tid];
         s.bs[tid] = a.ring.beta[bh * C + tid];
     }
-    chunk_decays_and_A<DK, C>(s);
-    {
-        float x[C];
-        const int col = tid;
-        chunk_column<DK, DV, C, T>(s, col, rv, (size_t)DV, x);
-        if (col < DK) {
 #pragma unroll
-            for (int r = 0; r < C; ++r) Wt[col * C + r] = x[r];
-        } else {
+    for (int sl = 0; sl < U::NSLICE; ++sl)
+        stile_fill<DK, DV>(stile + sl * 2 * U::S_SPLIT, a.ring.S_b + bh * SS, sl * kChainRows);
+    tc::fence_before_sync();
+    prep_operands<DK, DV, C, T>(s, aop, bop, rv, (size_t)DV);  // also publishes the S tiles
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    if (tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
+    bool ok = __syncthreads_and(tc::mbar_wait(mbar, 0));
+    if (ok) prep_epilogue<DK, DV, C>(tmem, decay_exp(s.G[C - 1]), mt, bt);
+    __syncthreads();
+    if (ok) {
+        // the chain products of prefill, one 64-row slice at a time, into TMEM columns sl*DK
+        if (tid == 0) {
 #pragma unroll
-            for (int r = 0; r < C; ++r) Us[r * DV + (col - DK)] = x[r];
+            for (int sl = 0; sl < U::NSLICE; ++sl)
+                chain_mma<DK>(tmem + sl * DK, stile + sl * 2 * U::S_SPLIT, mt, mbar, sl == U::NSLICE - 1);
+        }
+        ok = __syncthreads_and(tc::mbar_wait(mbar, 1));
+        if (ok) {
+#pragma unroll
+            for (int sl = 0; sl < U::NSLICE; ++sl)
+                chain_epilogue<DK, DV, (DK + DV) / 32>(tmem + sl * DK, bt + (size_t)sl * kChainRows * DK,
+                                                       sl * kChainRows, a.state + bh * SS, a.ring.S_b + bh * SS,
+                                                       nullptr);
         }
     }
+    if (!ok && tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
     __syncthreads();
-    for (int t = tid; t < (C / 4) * (DV / 4); t += blockDim.x) {
-        const int r0 = (t / (DV / 4)) * 4, n0 = (t % (DV / 4)) * 4;
-        float o[4][4];
-        delta_tile<DK>(Wt, C, St, DV, Us, DV, s.dvs, r0, n0, o);
-#pragma unroll
-        for (int aa = 0; aa < 4; ++aa)
-            *reinterpret_cast<float4*>(Us + (r0 + aa) * DV + n0) = make_float4(o[aa][0], o[aa][1], o[aa][2], o[aa][3]);
-    }
-    __syncthreads();
-    const float gamma = decay_exp(s.G[C - 1]);
-    float* st_out = a.state + bh * DK * DV;
-    float* sb_out = a.ring.S_b + bh * DK * DV;
-    for (int t = tid; t < (DV / 4) * (DK / 4); t += blockDim.x) {
-        const int c0 = (t % (DK / 4)) * 4, n0 = (t / (DK / 4)) * 4;
-        float o[4][4];
-        snew_tile<C>(St, DV, Us, DV, s.kf, KS, gamma, n0, c0, o);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const float4 val = make_float4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]);
-            *reinterpret_cast<float4*>(st_out + (size_t)(c0 + cc) * DV + n0) = val;
-            *reinterpret_cast<float4*>(sb_out + (size_t)(c0 + cc) * DV + n0) = val;
-        }
-    }
+    tc::fence_after_sync();
+    if (tid < 32) tc::tmem_dealloc(tmem, U::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------------------
@@ -281,7 +281,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     profile_mark(1, s);
-    const size_t sm5 = K5Smem<DK, DV, C>::bytes;
+    // dynamic shared memory also caps the CTAs per SM so their TMEM columns fit in 512
+    const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::RS_BYTES, tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
     e = cudaFuncSetAttribute(k5_resync<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
     if (e != cudaSuccess) return e;
     k5_resync<DK, DV, C, T><<<dim3(a.B, a.H), DK + DV, sm5, s>>>(a);

@@ -131,8 +131,15 @@ __device__ __forceinline__ void fwd_subst(const float* A, int a_stride, float x[
 #pragma unroll
     for (int r = 1; r < C; ++r) {
         float acc = x[r];
+        const float4* row = reinterpret_cast<const float4*>(A + r * a_stride);  // 16-byte aligned rows
 #pragma unroll
-        for (int i = 0; i < r; ++i) acc = __fmaf_rn(-A[r * a_stride + i], x[i], acc);
+        for (int i4 = 0; i4 < r; i4 += 4) {
+            const float4 a4 = row[i4 / 4];
+            acc = __fmaf_rn(-a4.x, x[i4], acc);
+            if (i4 + 1 < r) acc = __fmaf_rn(-a4.y, x[i4 + 1], acc);
+            if (i4 + 2 < r) acc = __fmaf_rn(-a4.z, x[i4 + 2], acc);
+            if (i4 + 3 < r) acc = __fmaf_rn(-a4.w, x[i4 + 3], acc);
+        }
         x[r] = acc;
     }
 }

@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "chunk_update.cuh"
 #include "numerics.cuh"
@@ -71,15 +73,23 @@ __global__ void __launch_bounds__(1024) k0_chunk_index(const int32_t* __restrict
 }
 
 // ------------------------------------------------------------------------------------
-// k1: chunk prep.  One CTA per (chunk, head), DK + DV threads (one per column of
-// [W | U~]).  Exits for partial chunks.
+// k1: chunk prep.  One CTA per (chunk, head), DK + DV threads.  The FP32 phase (decays,
+// A, forward substitution for W and U~) is followed by one tcgen05 product giving
+// M^T and B^T of the chunk (chunk_update.cuh), written to the workspace: M^T as the
+// shared-memory image the chain kernel copies in one piece, B^T as fp32 rows.
+// Exits for partial chunks.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C, typename T>
 __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
 {
-    extern __shared__ __align__(16) float sm1[];
-    const PrepSmem<DK, C> s(sm1);
+    using U = UCfg<DK, DV, C>;
+    extern __shared__ __align__(1024) unsigned char sm1[];
+    const PrepSmem<DK, C> s(reinterpret_cast<float*>(sm1), reinterpret_cast<float*>(sm1 + U::VEC_OFF));
     constexpr int KS = PrepSmem<DK, C>::KS;
+    unsigned char* aop = sm1 + U::AOP_OFF;
+    unsigned char* bop = sm1;  // reuses the key / A space once the FP32 phase is done
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm1 + U::PREP_BAR_OFF);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
 
     const int64_t c = blockIdx.x;
     const int h = blockIdx.y, tid = threadIdx.x, H = a.H;
@@ -92,239 +102,290 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
 
-    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-        const int r = idx / DK, jj = idx % DK;
-        s.kf[r * KS + jj] = to_f32<T>(k[((t0 + r) * H + h) * DK + jj]);
+    if (tid < 32) tc::tmem_alloc(tslot, U::TMEM_COLS);
+    if (tid == 0) {
+        tc::mbar_init(mbar, 1);
+        tc::fence_mbar_init();
+    }
+    {
+        constexpr int VE = 16 / (int)sizeof(T), KV = DK / VE, NK = (C * KV + DK + DV - 1) / (DK + DV);
+        uint4 kr[NK];
+#pragma unroll
+        for (int q4 = 0; q4 < NK; ++q4) {
+            const int idx = tid + q4 * (DK + DV);
+            if (idx < C * KV)
+                kr[q4] = __ldg(reinterpret_cast<const uint4*>(k + ((t0 + idx / KV) * H + h) * DK + (idx % KV) * VE));
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < NK; ++q4) {
+            const int idx = tid + q4 * (DK + DV);
+            if (idx < C * KV) {
+                const T* ke = reinterpret_cast<const T*>(&kr[q4]);
+#pragma unroll
+                for (int e = 0; e < VE; ++e) s.kf[(idx / KV) * KS + (idx % KV) * VE + e] = to_f32<T>(ke[e]);
+            }
+        }
     }
     if (tid < C) {
         s.G[tid] = a.g[(t0 + tid) * H + h];
         s.bs[tid] = a.beta[(t0 + tid) * H + h];
     }
-    chunk_decays_and_A<DK, C>(s);
-    float x[C];
-    const int col = tid;
-    chunk_column<DK, DV, C, T>(s, col, v + ((size_t)t0 * H + h) * DV, (size_t)H * DV, x);
-    const size_t ch = (size_t)c * H + h;
-    if (col < DK) {
-        float4* dst = reinterpret_cast<float4*>(a.wt + (ch * DK + col) * C);
-#pragma unroll
-        for (int r = 0; r < C; r += 4) dst[r / 4] = make_float4(x[r], x[r + 1], x[r + 2], x[r + 3]);
-    } else {
-        float* dst = a.ut + ch * C * DV + (col - DK);
-#pragma unroll
-        for (int r = 0; r < C; ++r) dst[(size_t)r * DV] = x[r];
+    tc::fence_before_sync();
+    prep_operands<DK, DV, C, T>(s, aop, bop, v + ((size_t)t0 * H + h) * DV, (size_t)H * DV);
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    if (tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
+    const bool ok = __syncthreads_and(tc::mbar_wait(mbar, 0));  // uniform: the epilogue's TMEM loads are warp-wide
+    if (ok) {
+        const size_t ch = (size_t)c * H + h;
+        prep_epilogue<DK, DV, C>(tmem, decay_exp(s.G[C - 1]), a.mt + ch * U::MT_BYTES, a.bt + ch * DK * DV);
+    } else if (tid == 0) {
+        atomicOr(a.status, CPR_DEV_TIMEOUT);
     }
-    if (tid < C) a.dvec[ch * (C + 4) + tid] = s.dvs[tid];
-    if (tid == 0) a.dvec[ch * (C + 4) + C] = decay_exp(s.G[C - 1]);
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid < 32) tc::tmem_dealloc(tmem, U::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------------------
-// k2: boundary chain.  One CTA per (sequence, head, slice of NS value rows).  The
-// slice of the state lives in shared memory (storage order [DK][NS]); the next
-// chunk's W^T, U~ slice, decays and keys are prefetched with cp.async while the
-// current chunk is applied.  Slicing the value rows changes no bit: each state row
-// evolves on its own.
+// k2: boundary chain.  One CTA per (sequence, head, slice of 64 value rows), 256
+// threads.  The slice of the state lives in shared memory as the bf16-split A operand of
+// the chain product; each chunk's M^T image and the slice's rows of B are bulk-copied
+// into one of two buffers one chunk ahead (mbarrier transaction counts); thread 0 issues
+// the tcgen05 product and every warp runs the epilogue on its TMEM lanes, writing the
+// next boundary state.  Slices are independent: each value row evolves on its own.
 // ------------------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
-{
-    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
-
-template <int DK, int DV, int C, typename T>
+template <int DK, int DV>
 struct K2Cfg {
-    static constexpr int NS = 16;
-    static constexpr int DT = (C / 4) * (NS / 4);   // delta tiles
-    static constexpr int ST = (NS / 4) * (DK / 4);  // S_new tiles
-    static constexpr int THREADS = ((DT > ST ? DT : ST) + 31) / 32 * 32;
-    // one prefetch buffer: Wt [DK][C], Us [C][NS], dv [C + 4], kraw [C][DK] (T)
-    static constexpr size_t BUF_FLOATS = (size_t)DK * C + (size_t)C * NS + (C + 4);
-    static constexpr size_t KRAW_BYTES = (size_t)C * DK * sizeof(T);
-    static constexpr size_t BUF_BYTES = BUF_FLOATS * sizeof(float) + KRAW_BYTES;
-    static constexpr size_t bytes = 2 * BUF_BYTES + sizeof(float) * ((size_t)C * DK + (size_t)DK * NS + (size_t)C * NS);
+    static constexpr int ROWS = DV < kChainRows ? DV : kChainRows;  // value rows of one slice
+    static constexpr int NSLICE = (DV + kChainRows - 1) / kChainRows;
+    static constexpr uint32_t MT_BYTES = 2 * DK * DK * 2;
+    static constexpr uint32_t B_BYTES = ROWS * DK * 4;
+    static constexpr uint32_t STAGE = MT_BYTES + B_BYTES;
+    static constexpr uint32_t S_BYTES = 2 * kChainRows * DK * 2;
+    static constexpr uint32_t S_OFF = 2 * STAGE, BAR_OFF = S_OFF + S_BYTES;
+    static constexpr uint32_t bytes = BAR_OFF + 64;
+    static constexpr uint32_t TMEM_COLS = DK <= 32 ? 32 : DK <= 64 ? 64 : 128;
+    static constexpr uint32_t PIECE = 16384;
 };
 
 template <int DK, int DV, int C, typename T>
-__global__ void __launch_bounds__(K2Cfg<DK, DV, C, T>::THREADS) k2_chain(PrefillArgs a)
+__global__ void __launch_bounds__(256) k2_chain(PrefillArgs a)
 {
-    using Cf = K2Cfg<DK, DV, C, T>;
-    constexpr int NS = Cf::NS;
-    extern __shared__ __align__(16) unsigned char smraw[];
-    unsigned char* bufp[2] = {smraw, smraw + Cf::BUF_BYTES};
-    float* kf = reinterpret_cast<float*>(smraw + 2 * Cf::BUF_BYTES);  // [C][DK]
-    float* St = kf + C * DK;                                           // [DK][NS]
-    float* dd = St + DK * NS;                                          // [C][NS]
+    using Cf = K2Cfg<DK, DV>;
+    extern __shared__ __align__(1024) unsigned char sm2[];
+    unsigned char* stile = sm2 + Cf::S_OFF;
+    uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(sm2 + Cf::BAR_OFF);  // [2]
+    uint64_t* mbar_mma = mbar_ld + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_ld + 3);
+    int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int H = a.H, tid = threadIdx.x;
-    const int n = blockIdx.x / H, h = blockIdx.x % H, n0 = blockIdx.y * NS;
+    const int sl = blockIdx.x % Cf::NSLICE, nh_idx = blockIdx.x / Cf::NSLICE;
+    const int n = nh_idx / H, h = nh_idx % H, row0 = sl * kChainRows;
     if (*a.status) return;
     const int64_t t0 = a.cu_seqlens[n];
     const int64_t L = a.cu_seqlens[n + 1] - t0;
     const int64_t nfull = L / C, nch = a.cu_chunks[n + 1] - a.cu_chunks[n], cbase = a.cu_chunks[n];
-    const T* k = static_cast<const T*>(a.k);
-    const size_t SS = (size_t)DK * DV;
+    const size_t SS = (size_t)DK * DV, nh = (size_t)n * H + h;
+    const float* s_in = a.state_in ? a.state_in + nh * SS : nullptr;
 
-    for (int idx = tid; idx < DK * NS; idx += blockDim.x) {
-        const int jj = idx / NS, nn = idx % NS;
-        St[idx] = a.state_in ? a.state_in[((size_t)n * H + h) * SS + (size_t)jj * DV + n0 + nn] : 0.0f;
-    }
-    __syncthreads();
-    auto store_state = [&](float* dst) {  // dst: a [DK][DV] state; write our slice
-        for (int idx = tid; idx < DK * NS / 4; idx += blockDim.x) {
-            const int jj = idx / (NS / 4), q4 = idx % (NS / 4);
-            *reinterpret_cast<float4*>(dst + (size_t)jj * DV + n0 + 4 * q4) =
-                *reinterpret_cast<const float4*>(St + jj * NS + 4 * q4);
+    // this slice's columns of the stored states: element (c, row0 + r)
+    auto copy_slice = [&](float* dst) {
+        for (int idx = tid; idx < DK * Cf::ROWS; idx += blockDim.x) {
+            const int c = idx / Cf::ROWS, r = idx % Cf::ROWS;
+            dst[(size_t)c * DV + row0 + r] = s_in ? s_in[(size_t)c * DV + row0 + r] : 0.0f;
         }
     };
-    if (L == 0) {
-        store_state(a.state_out + ((size_t)n * H + h) * SS);
+    if (L == 0) {  // empty sequence: state_out = state_in
+        copy_slice(a.state_out + nh * SS);
         return;
     }
-    store_state(a.boundary + ((size_t)cbase * H + h) * SS);
+    copy_slice(a.boundary + ((size_t)cbase * H + h) * SS);
     if (nfull == 0) return;
 
-    auto issue = [&](int64_t jc, unsigned char* buf) {
-        const size_t ch = (size_t)(cbase + jc) * H + h;
-        float* Wt = reinterpret_cast<float*>(buf);
-        float* Us = Wt + DK * C;
-        float* dv = Us + C * NS;
-        unsigned char* kraw = buf + Cf::BUF_FLOATS * sizeof(float);
-        const float* gW = a.wt + ch * DK * C;
-        for (int idx = tid; idx < DK * C / 4; idx += blockDim.x) cp_async16(Wt + 4 * idx, gW + 4 * idx);
-        for (int idx = tid; idx < C * NS / 4; idx += blockDim.x) {
-            const int r = idx / (NS / 4), q4 = idx % (NS / 4);
-            cp_async16(Us + r * NS + 4 * q4, a.ut + (ch * C + r) * DV + n0 + 4 * q4);
-        }
-        for (int idx = tid; idx < (C + 4) / 4; idx += blockDim.x) cp_async16(dv + 4 * idx, a.dvec + ch * (C + 4) + 4 * idx);
-        constexpr int ROW16 = DK * (int)sizeof(T) / 16;
-        const int64_t tk = t0 + jc * C;
-        for (int idx = tid; idx < C * ROW16; idx += blockDim.x) {
-            const int r = idx / ROW16, q16 = idx % ROW16;
-            cp_async16(kraw + ((size_t)r * DK * sizeof(T)) + 16 * q16,
-                       reinterpret_cast<const unsigned char*>(k + ((tk + r) * H + h) * DK) + 16 * q16);
-        }
-    };
-
-    issue(0, bufp[0]);
-    cp_async_commit();
-    for (int64_t jc = 0; jc < nfull; ++jc) {
-        if (jc + 1 < nfull) issue(jc + 1, bufp[(jc + 1) & 1]);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        unsigned char* buf = bufp[jc & 1];
-        const float* Wt = reinterpret_cast<const float*>(buf);
-        const float* Us = Wt + DK * C;
-        const float* dv = Us + C * NS;
-        const T* kraw = reinterpret_cast<const T*>(buf + Cf::BUF_FLOATS * sizeof(float));
-        for (int idx = tid; idx < C * DK; idx += blockDim.x) kf[idx] = to_f32<T>(kraw[idx]);
-        const float gamma = dv[C];
-        for (int t = tid; t < Cf::DT; t += blockDim.x) {
-            const int r0 = (t / (NS / 4)) * 4, m0 = (t % (NS / 4)) * 4;
-            float o[4][4];
-            delta_tile<DK>(Wt, C, St, NS, Us, NS, dv, r0, m0, o);
-#pragma unroll
-            for (int aa = 0; aa < 4; ++aa)
-                *reinterpret_cast<float4*>(dd + (r0 + aa) * NS + m0) = make_float4(o[aa][0], o[aa][1], o[aa][2], o[aa][3]);
-        }
-        __syncthreads();
-        for (int t = tid; t < Cf::ST; t += blockDim.x) {
-            const int c0 = (t % (DK / 4)) * 4, m0 = (t / (DK / 4)) * 4;
-            float o[4][4];
-            snew_tile<C>(St, NS, dd, NS, kf, DK, gamma, m0, c0, o);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                *reinterpret_cast<float4*>(St + (c0 + cc) * NS + m0) = make_float4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]);
-        }
-        __syncthreads();
-        if (jc + 1 < nch)
-            store_state(a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS);
-        else
-            store_state(a.state_out + ((size_t)n * H + h) * SS);
+    if (tid < 32) tc::tmem_alloc(tslot, Cf::TMEM_COLS);
+    if (tid == 0) {
+        tc::mbar_init(&mbar_ld[0], 1);
+        tc::mbar_init(&mbar_ld[1], 1);
+        tc::mbar_init(mbar_mma, 1);
+        tc::fence_mbar_init();
+        *fail = 0;
     }
-    cp_async_wait<0>();
+    stile_fill<DK, DV>(stile, s_in, row0);
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    auto issue_load = [&](int64_t jc, int b) {
+        const size_t ch = (size_t)(cbase + jc) * H + h;
+        const unsigned char* src = a.mt + ch * Cf::MT_BYTES;
+        unsigned char* dst = sm2 + b * Cf::STAGE;
+        tc::mbar_arrive_expect_tx(&mbar_ld[b], Cf::STAGE);
+        for (uint32_t off = 0; off < Cf::MT_BYTES; off += Cf::PIECE)
+            tc::bulk_g2s(dst + off, src + off, min(Cf::PIECE, Cf::MT_BYTES - off), &mbar_ld[b]);
+        const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(a.bt + ch * SS + (size_t)row0 * DK);
+        for (uint32_t off = 0; off < Cf::B_BYTES; off += Cf::PIECE)
+            tc::bulk_g2s(dst + Cf::MT_BYTES + off, bsrc + off, min(Cf::PIECE, Cf::B_BYTES - off), &mbar_ld[b]);
+    };
+    if (tid == 0) issue_load(0, 0);
+    for (int64_t jc = 0; jc < nfull; ++jc) {
+        const int b = (int)(jc & 1);
+        unsigned char* stage = sm2 + b * Cf::STAGE;
+        if (tid == 0) {
+            if (jc + 1 < nfull) issue_load(jc + 1, b ^ 1);  // that stage's readers finished a step ago
+            if (tc::mbar_wait(&mbar_ld[b], (uint32_t)((jc >> 1) & 1)))
+                chain_mma<DK>(tmem, stile, stage, mbar_mma);
+            else
+                *fail = 1;
+        }
+        __syncthreads();
+        if (*fail) break;
+        if (!__syncthreads_and(tc::mbar_wait(mbar_mma, (uint32_t)(jc & 1)))) {
+            if (tid == 0) *fail = 1;
+            break;
+        }
+        float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS : a.state_out + nh * SS;
+        chain_epilogue<DK, DV, 8>(tmem, reinterpret_cast<const float*>(stage + Cf::MT_BYTES), row0, dst, nullptr,
+                                  (jc + 1 < nfull) ? stile : nullptr);
+        __syncthreads();
+    }
+    if (*fail && tid == 0) {
+        atomicOr(a.status, CPR_DEV_TIMEOUT);
+        tc::mbar_wait(&mbar_ld[0], 0, 1u << 20);  // let a copy still in flight land
+        tc::mbar_wait(&mbar_ld[1], 0, 1u << 20);
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid < 32) tc::tmem_dealloc(tmem, Cf::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------------------
-// k3: intra-chunk token recurrence.  One CTA per (chunk, head), DV threads; thread i
-// holds row i of the state as DK/2 pairs (S[p], S[p + DK/2]) so that the two halves of
-// the canonical dot's chains (chain m and chain m+4) advance in one paired FMA.
+// k3: intra-chunk token recurrence.  One CTA per (chunk, head), DV threads.  Thread
+// (warp w, lane l) owns two value rows, i0 = 16w + (l & 15) and i1 = i0 + DV/2, over one
+// half of the key columns, h = l >> 4 (columns [h*DK/2, (h+1)*DK/2)).  It keeps them as
+// pairs (S[i][c], S[i][c + DK/4]) so that chains m and m+2 of its half advance in one
+// paired FMA; each key/query value loaded from shared memory serves both rows.  The
+// half-warps hold the two halves of the canonical tree, ((c0+c1)+(c2+c3)) and
+// ((c4+c5)+(c6+c7)), and add them after one shuffle.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C>
 struct K3Smem {
-    static constexpr size_t bytes = sizeof(float) * ((size_t)2 * C * DK + (size_t)C * DV + 2 * C);
+    // key/query rows: half 0's DK/4 pairs, 4 floats of padding, half 1's pairs, 4 floats
+    // (the padding puts the two half-warps' broadcast loads in different banks)
+    static constexpr int ROW = DK + 8;
+    static constexpr size_t bytes = sizeof(float) * ((size_t)2 * C * ROW + (size_t)C * DV + 2 * C);
 };
 
-template <int DK, bool NEXT>
-__device__ __forceinline__ void k3_token(float2 (&Sp)[DK / 2], const float2* __restrict__ kr,
-                                         const float2* __restrict__ qr, const float2* __restrict__ kn,
-                                         float alpha, float u, float& o, float& xn)
+template <int DK>
+struct K3Row {
+    static constexpr int NP = DK / 4;  // pairs per row per thread (half of DK columns)
+};
+
+// Partial (this half) of the canonical dot of both rows with w (pairs of this half).
+template <int DK>
+__device__ __forceinline__ void k3_half_dot(const float2 (&S0)[DK / 4], const float2 (&S1)[DK / 4],
+                                            const float2* __restrict__ w, float& d0, float& d1)
 {
-    constexpr int L = DK / 8;
-    const float2 a2 = make_float2(alpha, alpha), u2 = make_float2(u, u);
-    float2 co[4], cx[4];
+    constexpr int L = DK / 8;  // pair p is chain p/L (x) and p/L + 2 (y)
+    float2 a0[2], a1[2];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int t = 0; t < L; t += 2) {
 #pragma unroll
-        for (int t = 0; t < L; t += 2) {
+        for (int m = 0; m < 2; ++m) {
+            const int p = m * L + t;
+            const float4 w4 = *reinterpret_cast<const float4*>(w + p);
+            const float2 w0 = make_float2(w4.x, w4.y), w1 = make_float2(w4.z, w4.w);
+            const bool first = (t == 0);
+            a0[m] = first ? __fmul2_rn(S0[p], w0) : __ffma2_rn(S0[p], w0, a0[m]);
+            a1[m] = first ? __fmul2_rn(S1[p], w0) : __ffma2_rn(S1[p], w0, a1[m]);
+            a0[m] = __ffma2_rn(S0[p + 1], w1, a0[m]);
+            a1[m] = __ffma2_rn(S1[p + 1], w1, a1[m]);
+        }
+    }
+    // chains (c0, c2) in a[0] and (c1, c3) in a[1]: (c0 + c1) + (c2 + c3)
+    const float2 s0 = __fadd2_rn(a0[0], a0[1]), s1 = __fadd2_rn(a1[0], a1[1]);
+    d0 = __fadd_rn(s0.x, s0.y);
+    d1 = __fadd_rn(s1.x, s1.y);
+}
+
+template <int DK, bool NEXT>
+__device__ __forceinline__ void k3_token(float2 (&S0)[DK / 4], float2 (&S1)[DK / 4], const float2* __restrict__ kr,
+                                         const float2* __restrict__ qr, const float2* __restrict__ kn, float alpha,
+                                         float u0, float u1, float& o0, float& o1, float& x0, float& x1)
+{
+    constexpr int L = DK / 8;  // pairs [0, L) carry chains (0, 2); pairs [L, 2L) chains (1, 3)
+    const float2 a2 = make_float2(alpha, alpha), u02 = make_float2(u0, u0), u12 = make_float2(u1, u1);
+    float2 co0[2], co1[2], cx0[2], cx1[2];
+#pragma unroll
+    for (int t = 0; t < L; t += 2) {
+        const bool first = (t == 0);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {  // both chain blocks in one pass: 8 independent chains in flight
             const int p = m * L + t;
             const float4 k4 = *reinterpret_cast<const float4*>(kr + p);
             const float4 q4 = *reinterpret_cast<const float4*>(qr + p);
             const float2 k0 = make_float2(k4.x, k4.y), k1 = make_float2(k4.z, k4.w);
             const float2 q0 = make_float2(q4.x, q4.y), q1 = make_float2(q4.z, q4.w);
-            const float2 s0 = __ffma2_rn(u2, k0, __fmul2_rn(a2, Sp[p]));
-            const float2 s1 = __ffma2_rn(u2, k1, __fmul2_rn(a2, Sp[p + 1]));
-            Sp[p] = s0;
-            Sp[p + 1] = s1;
-            co[m] = (t == 0) ? __fmul2_rn(s0, q0) : __ffma2_rn(s0, q0, co[m]);
-            co[m] = __ffma2_rn(s1, q1, co[m]);
+            const float2 s00 = __ffma2_rn(u02, k0, __fmul2_rn(a2, S0[p]));
+            const float2 s10 = __ffma2_rn(u12, k0, __fmul2_rn(a2, S1[p]));
+            const float2 s01 = __ffma2_rn(u02, k1, __fmul2_rn(a2, S0[p + 1]));
+            const float2 s11 = __ffma2_rn(u12, k1, __fmul2_rn(a2, S1[p + 1]));
+            S0[p] = s00;
+            S1[p] = s10;
+            S0[p + 1] = s01;
+            S1[p + 1] = s11;
+            co0[m] = first ? __fmul2_rn(s00, q0) : __ffma2_rn(s00, q0, co0[m]);
+            co1[m] = first ? __fmul2_rn(s10, q0) : __ffma2_rn(s10, q0, co1[m]);
             if (NEXT) {
                 const float4 n4 = *reinterpret_cast<const float4*>(kn + p);
                 const float2 n0 = make_float2(n4.x, n4.y), n1 = make_float2(n4.z, n4.w);
-                cx[m] = (t == 0) ? __fmul2_rn(s0, n0) : __ffma2_rn(s0, n0, cx[m]);
-                cx[m] = __ffma2_rn(s1, n1, cx[m]);
+                cx0[m] = first ? __fmul2_rn(s00, n0) : __ffma2_rn(s00, n0, cx0[m]);
+                cx1[m] = first ? __fmul2_rn(s10, n0) : __ffma2_rn(s10, n0, cx1[m]);
+                cx0[m] = __ffma2_rn(s01, n1, cx0[m]);
+                cx1[m] = __ffma2_rn(s11, n1, cx1[m]);
             }
+            co0[m] = __ffma2_rn(s01, q1, co0[m]);
+            co1[m] = __ffma2_rn(s11, q1, co1[m]);
         }
     }
-    o = tree8_pairs(co[0], co[1], co[2], co[3]);
-    if (NEXT) xn = tree8_pairs(cx[0], cx[1], cx[2], cx[3]);
+    {
+        const float2 t0 = __fadd2_rn(co0[0], co0[1]), t1 = __fadd2_rn(co1[0], co1[1]);
+        o0 = __fadd_rn(t0.x, t0.y);
+        o1 = __fadd_rn(t1.x, t1.y);
+    }
+    if (NEXT) {
+        const float2 t0 = __fadd2_rn(cx0[0], cx0[1]), t1 = __fadd2_rn(cx1[0], cx1[1]);
+        x0 = __fadd_rn(t0.x, t0.y);
+        x1 = __fadd_rn(t1.x, t1.y);
+    }
 }
 
-template <int DK>
-__device__ __forceinline__ float k3_dot(const float2 (&Sp)[DK / 2], const float2* __restrict__ w)
+// Both halves end with the same value: left half + right half (the canonical tree's root).
+__device__ __forceinline__ float k3_join(float mine, int half)
 {
-    constexpr int L = DK / 8;
-    float2 c[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-#pragma unroll
-        for (int t = 0; t < L; t += 2) {
-            const int p = m * L + t;
-            const float4 w4 = *reinterpret_cast<const float4*>(w + p);
-            const float2 w0 = make_float2(w4.x, w4.y), w1 = make_float2(w4.z, w4.w);
-            c[m] = (t == 0) ? __fmul2_rn(Sp[p], w0) : __ffma2_rn(Sp[p], w0, c[m]);
-            c[m] = __ffma2_rn(Sp[p + 1], w1, c[m]);
-        }
-    }
-    return tree8_pairs(c[0], c[1], c[2], c[3]);
+    const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+    return half == 0 ? __fadd_rn(mine, other) : __fadd_rn(other, mine);
 }
 
 template <int DK, int DV, int C, typename T>
 __global__ void __launch_bounds__(DV, 2) k3_intra_chunk(PrefillArgs a)
 {
-    static_assert(DK % 16 == 0, "DK must be a multiple of 16");
+    static_assert(DK % 32 == 0 && DV % 32 == 0, "DK and DV must be multiples of 32");
+    constexpr int NP = DK / 4;
     extern __shared__ __align__(16) float sm3[];
-    float2* kp = reinterpret_cast<float2*>(sm3);   // [C][DK/2] pairs (k[p], k[p + DK/2])
-    float2* qp = kp + C * (DK / 2);                 // [C][DK/2]
-    float* vs = reinterpret_cast<float*>(qp + C * (DK / 2));  // [C][DV]
-    float* al = vs + C * DV;                        // [C]
-    float* bt = al + C;                             // [C]
+    // keys and queries: row r, half h, pair p at float offset r*ROW + h*(DK/2 + 4) + 2p,
+    // holding (x[h*DK/2 + p], x[h*DK/2 + p + DK/4])
+    constexpr int ROW = K3Smem<DK, DV, C>::ROW;
+    float* kp = sm3;                    // [C][ROW]
+    float* qp = kp + C * ROW;           // [C][ROW]
+    float* vs = qp + C * ROW;           // [C][DV]
+    float* al = vs + C * DV;                                 // [C]
+    float* bt = al + C;                                      // [C]
 
     const int64_t c = blockIdx.x;
-    const int h = blockIdx.y, i = threadIdx.x, H = a.H;
+    const int hd = blockIdx.y, tid = threadIdx.x, H = a.H;
     if (c >= a.cu_chunks[a.n_seqs]) return;
     const int n = find_seq(a.cu_chunks, a.n_seqs, c);
     const int64_t j = c - a.cu_chunks[n];
@@ -336,46 +397,104 @@ __global__ void __launch_bounds__(DV, 2) k3_intra_chunk(PrefillArgs a)
     const T* v = static_cast<const T*>(a.v);
     T* out = static_cast<T*>(a.out);
 
-    // stage the chunk's keys, queries (as pairs) and values in shared memory
-    for (int idx = i; idx < len * DK; idx += DV) {
-        const int r = idx / DK, jj = idx % DK;
-        const size_t g = ((size_t)(t0 + r) * H + h) * DK + jj;
-        float* kd = reinterpret_cast<float*>(kp + r * (DK / 2) + (jj % (DK / 2))) + (jj / (DK / 2));
-        float* qd = reinterpret_cast<float*>(qp + r * (DK / 2) + (jj % (DK / 2))) + (jj / (DK / 2));
-        *kd = to_f32<T>(k[g]);
-        *qd = to_f32<T>(q[g]);
-    }
-    for (int r = 0; r < len; ++r) vs[r * DV + i] = to_f32<T>(v[((size_t)(t0 + r) * H + h) * DV + i]);
-    if (i < len) {
-        al[i] = decay_exp(a.g[(t0 + i) * H + h]);
-        bt[i] = a.beta[(t0 + i) * H + h];
-    }
-    // the chunk's boundary state, row i
-    float2 Sp[DK / 2];
-    const float* bsrc = a.boundary + ((size_t)c * H + h) * DK * DV + i;
+    // stage the chunk's keys, queries (as pairs) and values: every thread issues all of
+    // its 16-byte loads first, then converts and stores them
+    {
+        constexpr int VE = 16 / (int)sizeof(T);
+        constexpr int KV = DK / VE, VV = DV / VE;
+        constexpr int NK = (C * KV + DV - 1) / DV, NV = (C * VV + DV - 1) / DV;
+        uint4 kr[NK], qr[NK], vr[NV];
 #pragma unroll
-    for (int p = 0; p < DK / 2; ++p) Sp[p] = make_float2(bsrc[(size_t)p * DV], bsrc[(size_t)(p + DK / 2) * DV]);
+        for (int s = 0; s < NK; ++s) {
+            const int idx = tid + s * DV, r = idx / KV, cc = idx % KV;
+            if (r < len) {
+                const size_t g = ((size_t)(t0 + r) * H + hd) * DK + cc * VE;
+                kr[s] = __ldg(reinterpret_cast<const uint4*>(k + g));
+                qr[s] = __ldg(reinterpret_cast<const uint4*>(q + g));
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < NV; ++s) {
+            const int idx = tid + s * DV, r = idx / VV, cc = idx % VV;
+            if (r < len) vr[s] = __ldg(reinterpret_cast<const uint4*>(v + ((size_t)(t0 + r) * H + hd) * DV + cc * VE));
+        }
+#pragma unroll
+        for (int s = 0; s < NK; ++s) {
+            const int idx = tid + s * DV, r = idx / KV, cc = idx % KV;
+            if (r < len) {
+                const T* ke = reinterpret_cast<const T*>(&kr[s]);
+                const T* qe = reinterpret_cast<const T*>(&qr[s]);
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                    const int jj = cc * VE + e, hh = jj / (DK / 2), jl = jj % (DK / 2);
+                    const int pidx = r * ROW + hh * (DK / 2 + 4) + 2 * (jl % NP) + jl / NP;
+                    kp[pidx] = to_f32<T>(ke[e]);
+                    qp[pidx] = to_f32<T>(qe[e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < NV; ++s) {
+            const int idx = tid + s * DV, r = idx / VV, cc = idx % VV;
+            if (r < len) {
+                const T* ve = reinterpret_cast<const T*>(&vr[s]);
+#pragma unroll
+                for (int e = 0; e < VE; ++e) vs[r * DV + cc * VE + e] = to_f32<T>(ve[e]);
+            }
+        }
+    }
+    if (tid < len) {
+        al[tid] = decay_exp(a.g[(t0 + tid) * H + hd]);
+        bt[tid] = a.beta[(t0 + tid) * H + hd];
+    }
+    const int w = tid >> 5, lane = tid & 31, half = lane >> 4;
+    const int i0 = w * 16 + (lane & 15), i1 = i0 + DV / 2;
+    // the chunk's boundary state: rows i0, i1 over this half's columns
+    float2 S0[NP], S1[NP];
+    {
+        const float* bsrc = a.boundary + ((size_t)c * H + hd) * DK * DV + (size_t)(half * (DK / 2)) * DV;
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            S0[p] = make_float2(bsrc[(size_t)p * DV + i0], bsrc[(size_t)(p + NP) * DV + i0]);
+            S1[p] = make_float2(bsrc[(size_t)p * DV + i1], bsrc[(size_t)(p + NP) * DV + i1]);
+        }
+    }
     __syncthreads();
 
-    float x = k3_dot<DK>(Sp, kp);
-    T* orow = out + ((size_t)t0 * H + h) * DV + i;
+    const float2* kph = reinterpret_cast<const float2*>(kp + half * (DK / 2 + 4));
+    const float2* qph = reinterpret_cast<const float2*>(qp + half * (DK / 2 + 4));
+    constexpr int RP = ROW / 2;  // row stride in pairs
+    float x0, x1;
+    k3_half_dot<DK>(S0, S1, kph, x0, x1);
+    x0 = k3_join(x0, half);
+    x1 = k3_join(x1, half);
+    T* orow = out + ((size_t)t0 * H + hd) * DV;
     for (int r = 0; r < len; ++r) {
-        const float alpha = al[r];
-        const float u = step_u(alpha, bt[r], vs[r * DV + i], x);
-        float o, xn = 0.0f;
+        const float alpha = al[r], beta = bt[r];
+        const float u0 = step_u(alpha, beta, vs[r * DV + i0], x0);
+        const float u1 = step_u(alpha, beta, vs[r * DV + i1], x1);
+        float o0, o1;
         if (r + 1 < len)
-            k3_token<DK, true>(Sp, kp + r * (DK / 2), qp + r * (DK / 2), kp + (r + 1) * (DK / 2), alpha, u, o, xn);
+            k3_token<DK, true>(S0, S1, kph + r * RP, qph + r * RP, kph + (r + 1) * RP, alpha, u0, u1, o0, o1, x0, x1);
         else
-            k3_token<DK, false>(Sp, kp + r * (DK / 2), qp + r * (DK / 2), kp, alpha, u, o, xn);
-        orow[(size_t)r * H * DV] = from_f32<T>(o);
-        x = xn;
+            k3_token<DK, false>(S0, S1, kph + r * RP, qph + r * RP, kph, alpha, u0, u1, o0, o1, x0, x1);
+        o0 = k3_join(o0, half);
+        o1 = k3_join(o1, half);
+        if (r + 1 < len) {
+            x0 = k3_join(x0, half);
+            x1 = k3_join(x1, half);
+        }
+        // both halves hold both outputs: half 0 stores row i0, half 1 row i1 (no branch)
+        orow[(size_t)r * H * DV + (half ? i1 : i0)] = from_f32<T>(half ? o1 : o0);
     }
     if (j * C + len == L && len < C) {  // final partial chunk: the stepped state is state_out
-        float* dst = a.state_out + ((size_t)n * H + h) * DK * DV + i;
+        float* dst = a.state_out + ((size_t)n * H + hd) * DK * DV + (size_t)(half * (DK / 2)) * DV;
 #pragma unroll
-        for (int p = 0; p < DK / 2; ++p) {
-            dst[(size_t)p * DV] = Sp[p].x;
-            dst[(size_t)(p + DK / 2) * DV] = Sp[p].y;
+        for (int p = 0; p < NP; ++p) {
+            dst[(size_t)p * DV + i0] = S0[p].x;
+            dst[(size_t)(p + NP) * DV + i0] = S0[p].y;
+            dst[(size_t)p * DV + i1] = S1[p].x;
+            dst[(size_t)(p + NP) * DV + i1] = S1[p].y;
         }
     }
 }
@@ -391,7 +510,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
     if (e != cudaSuccess) return e;
     profile_mark(1, s);
 
-    const size_t sm1 = sizeof(float) * PrepSmem<DK, C>::floats;
+    // dynamic shared memory also caps the CTAs per SM so their TMEM columns fit in 512
+    const size_t sm1 = std::max<size_t>(UCfg<DK, DV, C>::PREP_SMEM, tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
     e = cudaFuncSetAttribute(k1_chunk_prep<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
     if (e != cudaSuccess) return e;
     k1_chunk_prep<DK, DV, C, T><<<dim3((unsigned)a.max_chunks, a.H), DK + DV, sm1, s>>>(a);
@@ -399,10 +519,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
     if (e != cudaSuccess) return e;
     profile_mark(2, s);
 
-    using Cf = K2Cfg<DK, DV, C, T>;
-    e = cudaFuncSetAttribute(k2_chain<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::bytes);
+    using Cf = K2Cfg<DK, DV>;
+    e = cudaFuncSetAttribute(k2_chain<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)std::max<size_t>(Cf::bytes, tmem_cap_smem(Cf::TMEM_COLS)));
     if (e != cudaSuccess) return e;
-    k2_chain<DK, DV, C, T><<<dim3((unsigned)(a.n_seqs * a.H), DV / Cf::NS), Cf::THREADS, Cf::bytes, s>>>(a);
+    const size_t sm2 = std::max<size_t>(Cf::bytes, tmem_cap_smem(Cf::TMEM_COLS));
+    k2_chain<DK, DV, C, T><<<dim3((unsigned)(a.n_seqs * a.H * Cf::NSLICE)), 256, sm2, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     profile_mark(3, s);
