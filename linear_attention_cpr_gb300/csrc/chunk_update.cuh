@@ -207,7 +207,9 @@ __device__ __forceinline__ void prep_mma(uint32_t tmem, const unsigned char* aop
 }
 
 // All threads, after the prep products completed: the Mt image (bf16 splits; rows c,
-// K = c') and B (fp32 [DV][DK]) to generic destinations.  Warp w reads TMEM lanes
+// K = c') and B (fp32 [DV][DK], 16-byte chunks of row i XOR-swizzled by i % 8 so that the
+// chain epilogue's row-wise reads do not collide in shared-memory banks) to generic
+// destinations.  Warp w reads TMEM lanes
 // 32*(w%4) .. 32*(w%4)+31.
 template <int DK, int DV, int C>
 __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsigned char* mt_out, float* b_out)
@@ -242,12 +244,14 @@ __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsign
                         make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16,
                                    lo[4] | (uint32_t)lo[5] << 16, lo[6] | (uint32_t)lo[7] << 16);
                 }
-            } else {  // B[i][c], row i = this lane
+            } else {  // B[i][c], row i = this lane; 16-byte chunk j of the row stored at j ^ (i % 8)
                 if (row >= DV) continue;
-                float4* dst = reinterpret_cast<float4*>(b_out + (size_t)row * DK + (g * 32 - DK));
+                float4* dst = reinterpret_cast<float4*>(b_out + (size_t)row * DK);
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4)
-                    dst[e4] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const int j = (g * 32 - DK) / 4 + e4;
+                    dst[j ^ (row & 7)] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
+                }
             }
         }
     }
@@ -261,12 +265,13 @@ __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsign
 constexpr int kChainRows = 64;
 
 // S tile of one slice (bf16 splits, A operand: rows r = 0..63 <-> value rows row0 + r,
-// zero beyond DV; K = c) from a stored [DK][DV] fp32 state (NULL = zero).  All threads.
+// zero beyond DV; K = c) from a stored [DK][DV] fp32 state (NULL = zero), by threads
+// tid = 0 .. nthreads-1.
 template <int DK, int DV>
-__device__ __forceinline__ void stile_fill(unsigned char* stile, const float* src, int row0)
+__device__ __forceinline__ void stile_fill(unsigned char* stile, const float* src, int row0, int tid, int nthreads)
 {
     constexpr uint32_t SPLIT = kChainRows * DK * 2;
-    for (int idx = threadIdx.x; idx < kChainRows * (DK / 8); idx += blockDim.x) {
+    for (int idx = tid; idx < kChainRows * (DK / 8); idx += nthreads) {
         const int r = idx % kChainRows, c0 = (idx / kChainRows) * 8, i = row0 + r;
         uint16_t hi[8], lo[8];
 #pragma unroll
@@ -304,62 +309,76 @@ __device__ __forceinline__ void chain_mma(uint32_t tmem_col, const unsigned char
     if (commit_after) tc::commit(mbar);
 }
 
-// All threads (NW warps), after the chain product of one slice completed: for slice rows
-// r (value row i = row0 + r < DV), S_new[i][c] = D[r][c] + B[i][c], stored ([DK][DV] fp32)
-// to dst0 and (if not NULL) dst1, and split into stile (if not NULL) for the next product.
-// bslice: fp32 rows of B for this slice (row r at bslice + r * DK), generic address.
-template <int DK, int DV, int NW>
-__device__ __forceinline__ void chain_epilogue(uint32_t tmem_col, const float* bslice, int row0, float* dst0,
-                                               float* dst1, unsigned char* stile)
+// Epilogue of the chain product of one slice, split across the threads of 4 * WPQ warps:
+// warp w covers slice rows 16 (w % 4) .. +15 and columns [(w / 4) CPW, +CPW); thread t of
+// the warp takes row 16 (w % 4) + t % 16 and CPT consecutive columns from
+// (w / 4) CPW + (t / 16) CPT (the tcgen05.ld 16x32bx2 layout of an M = 64 accumulator).
+template <int DK, int WPQ>
+struct ChainMap {
+    static constexpr int CPW = DK / WPQ;
+    static constexpr int CPT = CPW / 2;
+    static __device__ __forceinline__ int row() { return 16 * ((threadIdx.x >> 5) & 3) + (threadIdx.x & 15); }
+    static __device__ __forceinline__ int col0()
+    {
+        return (int)(threadIdx.x >> 7) * CPW + (int)((threadIdx.x >> 4) & 1) * CPT;
+    }
+};
+
+// This thread's values of S_new = D + B (slice row ChainMap::row(), columns col0() ..).
+// bslice: B rows of the slice, swizzled as written by prep_epilogue; rows beyond the
+// slice (value row >= DV) are left as the raw accumulator and must not be stored.
+template <int DK, int DV, int WPQ>
+__device__ __forceinline__ void chain_values(uint32_t tmem_col, const float* bslice, int row0,
+                                             float (&v)[ChainMap<DK, WPQ>::CPT])
 {
-    constexpr uint32_t S_SPLIT = kChainRows * DK * 2;
-    constexpr int NG = DK / 32;                  // 32-column groups
-    constexpr int STEP = NW >= 4 ? NW / 4 : 1;   // warps sharing one TMEM quadrant
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3;
-    const int r = q * 16 + (lane & 15);  // this thread's slice row (lanes 16..31 carry none)
-    const int i = row0 + r;
-    const bool have = (lane < 16) && (i < DV);
-    tc::fence_after_sync();
-    if (q < NW) {
-        for (int g = warp >> 2; g < NG; g += STEP) {
-            float v[32];
-            tc::tmem_ld32(tmem_col + ((uint32_t)(q * 32) << 16) + (uint32_t)(g * 32), v);
-            if (!have) continue;
-            const float4* b4 = reinterpret_cast<const float4*>(bslice + (size_t)r * DK + g * 32);
+    using Mp = ChainMap<DK, WPQ>;
+    const int warp = threadIdx.x >> 5;
+    const int q = warp & 3, h = warp >> 2;
+    tc::tmem_ld_16x2<Mp::CPT>(tmem_col + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * Mp::CPW), v);
+    const int r = Mp::row(), c0 = Mp::col0();
+    if (row0 + r < DV) {
+        const float4* brow = reinterpret_cast<const float4*>(bslice + (size_t)r * DK);
 #pragma unroll
-            for (int e4 = 0; e4 < 8; ++e4) {
-                const float4 b = b4[e4];
-                v[4 * e4] = __fadd_rn(v[4 * e4], b.x);
-                v[4 * e4 + 1] = __fadd_rn(v[4 * e4 + 1], b.y);
-                v[4 * e4 + 2] = __fadd_rn(v[4 * e4 + 2], b.z);
-                v[4 * e4 + 3] = __fadd_rn(v[4 * e4 + 3], b.w);
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) dst0[(size_t)(g * 32 + e) * DV + i] = v[e];
-            if (dst1) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) dst1[(size_t)(g * 32 + e) * DV + i] = v[e];
-            }
-            if (stile) {
-#pragma unroll
-                for (int e8 = 0; e8 < 32; e8 += 8) {
-                    uint16_t hi[8], lo[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) tc::split_bf16(v[e8 + e], hi[e], lo[e]);
-                    const uint32_t off = tc::tile_off<2>(r, g * 32 + e8, DK);
-                    *reinterpret_cast<uint4*>(stile + off) =
-                        make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
-                                   hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
-                    *reinterpret_cast<uint4*>(stile + S_SPLIT + off) =
-                        make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16,
-                                   lo[4] | (uint32_t)lo[5] << 16, lo[6] | (uint32_t)lo[7] << 16);
-                }
-            }
+        for (int k = 0; k < Mp::CPT / 4; ++k) {
+            const float4 b = brow[(c0 / 4 + k) ^ (r & 7)];
+            v[4 * k] = __fadd_rn(v[4 * k], b.x);
+            v[4 * k + 1] = __fadd_rn(v[4 * k + 1], b.y);
+            v[4 * k + 2] = __fadd_rn(v[4 * k + 2], b.z);
+            v[4 * k + 3] = __fadd_rn(v[4 * k + 3], b.w);
         }
     }
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
+}
+
+// Split this thread's values into the S tile (A operand of the next chain product).
+template <int DK, int WPQ>
+__device__ __forceinline__ void chain_refill(unsigned char* stile, const float (&v)[ChainMap<DK, WPQ>::CPT])
+{
+    using Mp = ChainMap<DK, WPQ>;
+    constexpr uint32_t S_SPLIT = kChainRows * DK * 2;
+    const int r = Mp::row(), c0 = Mp::col0();
+#pragma unroll
+    for (int e8 = 0; e8 < Mp::CPT; e8 += 8) {
+        uint16_t hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tc::split_bf16(v[e8 + e], hi[e], lo[e]);
+        const uint32_t off = tc::tile_off<2>(r, c0 + e8, DK);
+        *reinterpret_cast<uint4*>(stile + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
+                                                            hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
+        *reinterpret_cast<uint4*>(stile + S_SPLIT + off) =
+            make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
+                       lo[6] | (uint32_t)lo[7] << 16);
+    }
+}
+
+// Store this thread's values into a [DK][DV] state (element (c, row0 + row)).
+template <int DK, int DV, int WPQ>
+__device__ __forceinline__ void chain_store(float* dst, int row0, const float (&v)[ChainMap<DK, WPQ>::CPT])
+{
+    using Mp = ChainMap<DK, WPQ>;
+    const int i = row0 + Mp::row(), c0 = Mp::col0();
+    if (i >= DV) return;
+#pragma unroll
+    for (int e = 0; e < Mp::CPT; ++e) dst[(size_t)(c0 + e) * DV + i] = v[e];
 }
 
 }  // namespace cpr

@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     }
 #pragma unroll
     for (int sl = 0; sl < U::NSLICE; ++sl)
-        stile_fill<DK, DV>(stile + sl * 2 * U::S_SPLIT, a.ring.S_b + bh * SS, sl * kChainRows);
+        stile_fill<DK, DV>(stile + sl * 2 * U::S_SPLIT, a.ring.S_b + bh * SS, sl * kChainRows, tid, (int)blockDim.x);
     tc::fence_before_sync();
     prep_operands<DK, DV, C, T>(s, aop, bop, rv, (size_t)DV);  // also publishes the S tiles
     tc::fence_after_sync();
@@ -206,11 +206,16 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
         }
         ok = __syncthreads_and(tc::mbar_wait(mbar, 1));
         if (ok) {
+            tc::fence_after_sync();
+            constexpr int NW = (DK + DV) / 32, WPQ = NW >= 8 ? 2 : 1;
 #pragma unroll
-            for (int sl = 0; sl < U::NSLICE; ++sl)
-                chain_epilogue<DK, DV, (DK + DV) / 32>(tmem + sl * DK, bt + (size_t)sl * kChainRows * DK,
-                                                       sl * kChainRows, a.state + bh * SS, a.ring.S_b + bh * SS,
-                                                       nullptr);
+            for (int sl = 0; sl < U::NSLICE; ++sl) {
+                float v[ChainMap<DK, WPQ>::CPT];
+                chain_values<DK, DV, WPQ>(tmem + sl * DK, bt + (size_t)sl * kChainRows * DK, sl * kChainRows, v);
+                chain_store<DK, DV, WPQ>(a.state + bh * SS, sl * kChainRows, v);
+                chain_store<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
+            }
+            tc::fence_before_sync();
         }
     }
     if (!ok && tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);

@@ -148,12 +148,13 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
 }
 
 // ------------------------------------------------------------------------------------
-// k2: boundary chain.  One CTA per (sequence, head, slice of 64 value rows), 256
-// threads.  The slice of the state lives in shared memory as the bf16-split A operand of
-// the chain product; each chunk's M^T image and the slice's rows of B are bulk-copied
-// into one of two buffers one chunk ahead (mbarrier transaction counts); thread 0 issues
-// the tcgen05 product and every warp runs the epilogue on its TMEM lanes, writing the
-// next boundary state.  Slices are independent: each value row evolves on its own.
+// k2: boundary chain.  One CTA per (sequence, head, slice of 64 value rows), 9 warps.
+// Warp 8 is the producer: it bulk-copies each chunk's M^T image and the slice's rows of
+// B into one of two shared-memory stages one chunk ahead and issues the tcgen05 chain
+// product.  Warps 0-7 are the epilogue: they read the accumulator, add B, refill the
+// bf16-split state tile (A operand of the next product) and signal the producer, then
+// store the boundary state while the next product runs.  All hand-offs go through
+// mbarriers with bounded waits.  Slices are independent: each value row evolves alone.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV>
 struct K2Cfg {
@@ -167,20 +168,24 @@ struct K2Cfg {
     static constexpr uint32_t bytes = BAR_OFF + 64;
     static constexpr uint32_t TMEM_COLS = DK <= 32 ? 32 : DK <= 64 ? 64 : 128;
     static constexpr uint32_t PIECE = 16384;
+    static constexpr int THREADS = 9 * 32;
+    static constexpr int EPI = 256;  // epilogue threads (warps 0-7)
 };
 
 template <int DK, int DV, int C, typename T>
-__global__ void __launch_bounds__(256) k2_chain(PrefillArgs a)
+__global__ void __launch_bounds__(K2Cfg<DK, DV>::THREADS) k2_chain(PrefillArgs a)
 {
     using Cf = K2Cfg<DK, DV>;
+    using Mp = ChainMap<DK, 2>;
     extern __shared__ __align__(1024) unsigned char sm2[];
     unsigned char* stile = sm2 + Cf::S_OFF;
-    uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(sm2 + Cf::BAR_OFF);  // [2]
-    uint64_t* mbar_mma = mbar_ld + 2;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_ld + 3);
+    uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(sm2 + Cf::BAR_OFF);  // [2] stage landed
+    uint64_t* mbar_mma = mbar_ld + 2;                                    // product done
+    uint64_t* mbar_tile = mbar_ld + 3;                                   // state tile ready (256 arrivals)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_ld + 4);
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
-    const int H = a.H, tid = threadIdx.x;
+    const int H = a.H, tid = threadIdx.x, warp = tid >> 5;
     const int sl = blockIdx.x % Cf::NSLICE, nh_idx = blockIdx.x / Cf::NSLICE;
     const int n = nh_idx / H, h = nh_idx % H, row0 = sl * kChainRows;
     if (*a.status) return;
@@ -204,61 +209,74 @@ __global__ void __launch_bounds__(256) k2_chain(PrefillArgs a)
     copy_slice(a.boundary + ((size_t)cbase * H + h) * SS);
     if (nfull == 0) return;
 
-    if (tid < 32) tc::tmem_alloc(tslot, Cf::TMEM_COLS);
+    if (warp == 0) tc::tmem_alloc(tslot, Cf::TMEM_COLS);
     if (tid == 0) {
         tc::mbar_init(&mbar_ld[0], 1);
         tc::mbar_init(&mbar_ld[1], 1);
         tc::mbar_init(mbar_mma, 1);
+        tc::mbar_init(mbar_tile, Cf::EPI);
         tc::fence_mbar_init();
         *fail = 0;
     }
-    stile_fill<DK, DV>(stile, s_in, row0);
-    tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
-    auto issue_load = [&](int64_t jc, int b) {
-        const size_t ch = (size_t)(cbase + jc) * H + h;
-        const unsigned char* src = a.mt + ch * Cf::MT_BYTES;
-        unsigned char* dst = sm2 + b * Cf::STAGE;
-        tc::mbar_arrive_expect_tx(&mbar_ld[b], Cf::STAGE);
-        for (uint32_t off = 0; off < Cf::MT_BYTES; off += Cf::PIECE)
-            tc::bulk_g2s(dst + off, src + off, min(Cf::PIECE, Cf::MT_BYTES - off), &mbar_ld[b]);
-        const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(a.bt + ch * SS + (size_t)row0 * DK);
-        for (uint32_t off = 0; off < Cf::B_BYTES; off += Cf::PIECE)
-            tc::bulk_g2s(dst + Cf::MT_BYTES + off, bsrc + off, min(Cf::PIECE, Cf::B_BYTES - off), &mbar_ld[b]);
-    };
-    if (tid == 0) issue_load(0, 0);
-    for (int64_t jc = 0; jc < nfull; ++jc) {
-        const int b = (int)(jc & 1);
-        unsigned char* stage = sm2 + b * Cf::STAGE;
-        if (tid == 0) {
-            if (jc + 1 < nfull) issue_load(jc + 1, b ^ 1);  // that stage's readers finished a step ago
-            if (tc::mbar_wait(&mbar_ld[b], (uint32_t)((jc >> 1) & 1)))
-                chain_mma<DK>(tmem, stile, stage, mbar_mma);
-            else
-                *fail = 1;
+
+    if (warp == 8) {  // ----- producer -----
+        if ((tid & 31) == 0) {
+            auto issue_load = [&](int64_t jc, int b) {
+                const size_t ch = (size_t)(cbase + jc) * H + h;
+                const unsigned char* src = a.mt + ch * Cf::MT_BYTES;
+                unsigned char* dst = sm2 + b * Cf::STAGE;
+                tc::mbar_arrive_expect_tx(&mbar_ld[b], Cf::STAGE);
+                for (uint32_t off = 0; off < Cf::MT_BYTES; off += Cf::PIECE)
+                    tc::bulk_g2s(dst + off, src + off, min(Cf::PIECE, Cf::MT_BYTES - off), &mbar_ld[b]);
+                const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(a.bt + ch * SS + (size_t)row0 * DK);
+                for (uint32_t off = 0; off < Cf::B_BYTES; off += Cf::PIECE)
+                    tc::bulk_g2s(dst + Cf::MT_BYTES + off, bsrc + off, min(Cf::PIECE, Cf::B_BYTES - off), &mbar_ld[b]);
+            };
+            int64_t issued = 0;
+            issue_load(0, 0);
+            issued = 1;
+            for (int64_t jc = 0; jc < nfull; ++jc) {
+                if (!tc::mbar_wait(mbar_tile, (uint32_t)(jc & 1))) { *fail = 1; break; }
+                if (jc + 1 < nfull) {  // that stage's last readers (product jc-1, epilogue jc-1) are done
+                    issue_load(jc + 1, (int)((jc + 1) & 1));
+                    issued = jc + 2;
+                }
+                if (!tc::mbar_wait(&mbar_ld[jc & 1], (uint32_t)((jc >> 1) & 1))) { *fail = 1; break; }
+                chain_mma<DK>(tmem, stile, sm2 + (jc & 1) * Cf::STAGE, mbar_mma);
+            }
+            if (*fail) {  // let copies still in flight land before the CTA exits
+                for (int64_t jc = 0; jc < issued; ++jc) tc::mbar_wait(&mbar_ld[jc & 1], (uint32_t)((jc >> 1) & 1), 1u << 16);
+            }
         }
-        __syncthreads();
-        if (*fail) break;
-        if (!__syncthreads_and(tc::mbar_wait(mbar_mma, (uint32_t)(jc & 1)))) {
-            if (tid == 0) *fail = 1;
-            break;
+    } else {  // ----- epilogue warps 0-7 -----
+        stile_fill<DK, DV>(stile, s_in, row0, tid, Cf::EPI);
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        tc::mbar_arrive(mbar_tile);
+        for (int64_t jc = 0; jc < nfull; ++jc) {
+            const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(mbar_mma, (uint32_t)(jc & 1)));
+            if (!ok) { *fail = 1; break; }
+            tc::fence_after_sync();
+            float v[Mp::CPT];
+            chain_values<DK, DV, 2>(tmem, reinterpret_cast<const float*>(sm2 + (jc & 1) * Cf::STAGE + Cf::MT_BYTES), row0, v);
+            if (jc + 1 < nfull) {
+                chain_refill<DK, 2>(stile, v);
+                tc::fence_proxy_async();
+            }
+            tc::fence_before_sync();
+            if (jc + 1 < nfull) tc::mbar_arrive(mbar_tile);
+            float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS : a.state_out + nh * SS;
+            chain_store<DK, DV, 2>(dst, row0, v);
         }
-        float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS : a.state_out + nh * SS;
-        chain_epilogue<DK, DV, 8>(tmem, reinterpret_cast<const float*>(stage + Cf::MT_BYTES), row0, dst, nullptr,
-                                  (jc + 1 < nfull) ? stile : nullptr);
-        __syncthreads();
-    }
-    if (*fail && tid == 0) {
-        atomicOr(a.status, CPR_DEV_TIMEOUT);
-        tc::mbar_wait(&mbar_ld[0], 0, 1u << 20);  // let a copy still in flight land
-        tc::mbar_wait(&mbar_ld[1], 0, 1u << 20);
     }
     __syncthreads();
+    if (*fail && tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
     tc::fence_after_sync();
-    if (tid < 32) tc::tmem_dealloc(tmem, Cf::TMEM_COLS);
+    if (warp == 0) tc::tmem_dealloc(tmem, Cf::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------------------
@@ -524,7 +542,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
                              (int)std::max<size_t>(Cf::bytes, tmem_cap_smem(Cf::TMEM_COLS)));
     if (e != cudaSuccess) return e;
     const size_t sm2 = std::max<size_t>(Cf::bytes, tmem_cap_smem(Cf::TMEM_COLS));
-    k2_chain<DK, DV, C, T><<<dim3((unsigned)(a.n_seqs * a.H * Cf::NSLICE)), 256, sm2, s>>>(a);
+    k2_chain<DK, DV, C, T><<<dim3((unsigned)(a.n_seqs * a.H * Cf::NSLICE)), Cf::THREADS, sm2, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     profile_mark(3, s);
