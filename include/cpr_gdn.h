@@ -111,7 +111,8 @@ int64_t cpr_gdn_num_chunks(const int32_t* cu_seqlens_host, int32_t n_seqs, int32
 size_t cpr_gdn_prefill_workspace_size(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk,
                                       int32_t dv, int32_t C);
 
-/* Bytes of device workspace cpr_gdn_decode needs (the status word). */
+/* Bytes of device workspace cpr_gdn_decode needs (status word and the list of sequences
+ * whose token completes a chunk in this step). */
 size_t cpr_gdn_decode_workspace_size(int32_t B, int32_t H, int32_t dk, int32_t dv, int32_t C);
 
 /*

@@ -77,7 +77,7 @@ size_t cpr_gdn_prefill_workspace_size(int64_t total_tokens, int32_t n_seqs, int3
 size_t cpr_gdn_decode_workspace_size(int32_t B, int32_t H, int32_t dk, int32_t dv, int32_t C)
 {
     if (B < 0 || H <= 0 || dk <= 0 || dv <= 0 || C <= 0) return 0;
-    return kAlign;
+    return decode_workspace_bytes(B);
 }
 
 int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -191,7 +191,7 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
     if (!q || !k || !v || !g || !beta || !state || !ring || !pos || !out || !ring->S_b || !ring->k || !ring->v ||
         !ring->g || !ring->beta)
         return CPR_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < kAlign) return CPR_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < decode_workspace_bytes(B)) return CPR_ERR_WORKSPACE;
     const void* a16[] = {q, k, v, out, state, ring->S_b, ring->k, ring->v, workspace};
     for (const void* p : a16)
         if (!aligned(p, 16)) return CPR_ERR_MISALIGNED;
@@ -211,6 +211,12 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
     a.H = H;
     a.out = out;
     a.status = static_cast<uint32_t*>(workspace);
+    a.resync_count = static_cast<uint32_t*>(workspace) + 1;
+    a.resync_list = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + kAlign);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return CPR_ERR_CUDA;
+    a.num_sms = sms;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorInvalidValue;
 #define CPR_DISPATCH(DK, DV, CC)                                                                  \

@@ -34,12 +34,20 @@ __device__ __forceinline__ void chunk_decays_and_A(const PrepSmem<DK, C>& s)
 {
     const int tid = threadIdx.x;
     __syncthreads();
-    if (tid == 0) {
-        float acc = s.G[0];
-        for (int r = 1; r < C; ++r) {
-            acc = __fadd_rn(acc, s.G[r]);
-            s.G[r] = acc;
+    if (tid == 0) {  // sequential cumulative sum, in registers
+        float gr[C];
+#pragma unroll
+        for (int r = 0; r < C; r += 4) {
+            const float4 g4 = *reinterpret_cast<const float4*>(s.G + r);
+            gr[r] = g4.x;
+            gr[r + 1] = g4.y;
+            gr[r + 2] = g4.z;
+            gr[r + 3] = g4.w;
         }
+#pragma unroll
+        for (int r = 1; r < C; ++r) gr[r] = __fadd_rn(gr[r - 1], gr[r]);
+#pragma unroll
+        for (int r = 0; r < C; r += 4) *reinterpret_cast<float4*>(s.G + r) = make_float4(gr[r], gr[r + 1], gr[r + 2], gr[r + 3]);
     }
     __syncthreads();
     if (tid < C) {
@@ -112,7 +120,9 @@ struct UCfg {
     static constexpr int NSLICE = (DV + 63) / 64;        // chain slices of 64 value rows
     // prep shared memory: R1 = keys + A (FP32 phase), later the [W | U~] operand
     static constexpr uint32_t R1A = (uint32_t)(sizeof(float) * ((size_t)C * PrepSmem<DK, C>::KS + (size_t)C * C));
-    static constexpr uint32_t R1 = (R1A > 2 * BOP_SPLIT ? R1A : 2 * BOP_SPLIT);
+    static constexpr uint32_t mx(uint32_t x, uint32_t y) { return x > y ? x : y; }
+    // R1 also stages the prep outputs (M^T image, then B) before their bulk stores
+    static constexpr uint32_t R1 = mx(mx(R1A, 2 * BOP_SPLIT), mx(2 * DK * DK * 2, DK * DV * 4));
     static constexpr uint32_t AOP_OFF = (R1 + 1023) / 1024 * 1024;
     static constexpr uint32_t VEC_OFF = AOP_OFF + 2 * AOP_SPLIT;
     static constexpr uint32_t PREP_BYTES = VEC_OFF + 4 * C * 4;
@@ -208,11 +218,14 @@ __device__ __forceinline__ void prep_mma(uint32_t tmem, const unsigned char* aop
 
 // All threads, after the prep products completed: the Mt image (bf16 splits; rows c,
 // K = c') and B (fp32 [DV][DK], 16-byte chunks of row i XOR-swizzled by i % 8 so that the
-// chain epilogue's row-wise reads do not collide in shared-memory banks) to generic
-// destinations.  Warp w reads TMEM lanes
-// 32*(w%4) .. 32*(w%4)+31.
+// chain epilogue's row-wise reads do not collide in shared-memory banks).  With a
+// shared-memory staging area of at least max(Mt, B) bytes (its previous contents dead),
+// each of the two is assembled there and written to the global destination with bulk
+// copies; without one (staging NULL) they are written directly (shared-memory
+// destinations).  Contains __syncthreads.
 template <int DK, int DV, int C>
-__device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsigned char* mt_out, float* b_out)
+__device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsigned char* mt_out, float* b_out,
+                                              unsigned char* staging)
 {
     using U = UCfg<DK, DV, C>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
@@ -220,39 +233,57 @@ __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsign
     constexpr int NG = 2 * DK / 32;  // 32-column groups: X then B
     const int q = warp & 3;
     const int row = q * 32 + lane;  // this thread's TMEM lane
-    if (q * 32 < (DK > DV ? DK : DV)) {
-        for (int g = warp >> 2; g < NG; g += (nw + 3) / 4) {
-            float v[32];
-            tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(g * 32), v);
-            if (g < DK / 32) {  // Mt[c][c'] = gamma [c == c'] - X[c][c'], row c = this lane
-                if (row >= DK) continue;
-                const int col0 = g * 32;
+    for (int part = 0; part < 2; ++part) {  // 0: Mt, 1: B
+        unsigned char* mt_dst = staging ? staging : mt_out;
+        float* b_dst = staging ? reinterpret_cast<float*>(staging) : b_out;
+        if (q * 32 < (part == 0 ? DK : DV)) {
+            for (int g = warp >> 2; g < NG; g += (nw + 3) / 4) {
+                if ((g < DK / 32) != (part == 0)) continue;
+                float v[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(g * 32), v);
+                if (part == 0) {  // Mt[c][c'] = gamma [c == c'] - X[c][c'], row c = this lane
+                    if (row >= DK) continue;
+                    const int col0 = g * 32;
 #pragma unroll
-                for (int e8 = 0; e8 < 32; e8 += 8) {
-                    uint16_t hi[8], lo[8];
+                    for (int e8 = 0; e8 < 32; e8 += 8) {
+                        uint16_t hi[8], lo[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int cc = col0 + e8 + e;
-                        const float m = (cc == row) ? __fsub_rn(gamma, v[e8 + e]) : -v[e8 + e];
-                        tc::split_bf16(m, hi[e], lo[e]);
+                        for (int e = 0; e < 8; ++e) {
+                            const int cc = col0 + e8 + e;
+                            const float m = (cc == row) ? __fsub_rn(gamma, v[e8 + e]) : -v[e8 + e];
+                            tc::split_bf16(m, hi[e], lo[e]);
+                        }
+                        const uint32_t off = tc::tile_off<2>(row, col0 + e8, DK);
+                        *reinterpret_cast<uint4*>(mt_dst + off) =
+                            make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
+                                       hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
+                        *reinterpret_cast<uint4*>(mt_dst + U::MT_SPLIT + off) =
+                            make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16,
+                                       lo[4] | (uint32_t)lo[5] << 16, lo[6] | (uint32_t)lo[7] << 16);
                     }
-                    const uint32_t off = tc::tile_off<2>(row, col0 + e8, DK);
-                    *reinterpret_cast<uint4*>(mt_out + off) =
-                        make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
-                                   hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
-                    *reinterpret_cast<uint4*>(mt_out + U::MT_SPLIT + off) =
-                        make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16,
-                                   lo[4] | (uint32_t)lo[5] << 16, lo[6] | (uint32_t)lo[7] << 16);
-                }
-            } else {  // B[i][c], row i = this lane; 16-byte chunk j of the row stored at j ^ (i % 8)
-                if (row >= DV) continue;
-                float4* dst = reinterpret_cast<float4*>(b_out + (size_t)row * DK);
+                } else {  // B[i][c], row i = this lane; chunk j of the row stored at j ^ (i % 8)
+                    if (row >= DV) continue;
+                    float4* dst = reinterpret_cast<float4*>(b_dst + (size_t)row * DK);
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const int j = (g * 32 - DK) / 4 + e4;
-                    dst[j ^ (row & 7)] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const int j = (g * 32 - DK) / 4 + e4;
+                        dst[j ^ (row & 7)] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
+                    }
                 }
             }
+        }
+        if (staging) {  // one bulk store of the assembled part, then the staging area is free again
+            tc::fence_proxy_async();
+            __syncthreads();
+            if (tid == 0) {
+                const uint32_t bytes = part == 0 ? U::MT_BYTES : U::BT_BYTES;
+                unsigned char* gdst = part == 0 ? mt_out : reinterpret_cast<unsigned char*>(b_out);
+                for (uint32_t off = 0; off < bytes; off += 16384)
+                    tc::bulk_s2g(gdst + off, staging + off, min(16384u, bytes - off));
+                tc::bulk_commit();
+                tc::bulk_wait_read();
+            }
+            __syncthreads();
         }
     }
     tc::fence_proxy_async();

@@ -71,6 +71,9 @@ struct PrefillArgs {
     int64_t max_chunks;
 };
 
+// Decode workspace: [0, 256) status word, resync count; then int32 [B] resync list.
+inline size_t decode_workspace_bytes(int32_t B) { return kAlign + align_up(sizeof(int32_t) * (size_t)(B > 0 ? B : 1), kAlign); }
+
 struct DecodeArgs {
     const void* q;
     const void* k;
@@ -84,6 +87,9 @@ struct DecodeArgs {
     int32_t H;
     void* out;
     uint32_t* status;
+    uint32_t* resync_count;  // sequences appended to resync_list by the step kernel
+    int32_t* resync_list;    // [B]
+    int num_sms;
 };
 
 struct RingArgs {

@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
         sc[1] = bb;
         a.ring.g[bh * C + r] = gg;
         a.ring.beta[bh * C + r] = bb;
+        if (r == C - 1 && h == 0) a.resync_list[atomicAdd(a.resync_count, 1u)] = b;  // this token completes a chunk
     }
     float s[L][VPT];
     float* st = a.state + bh * DK * DV + (size_t)(m * L) * DV + lane * VPT;
@@ -147,17 +148,19 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 }
 
 // ------------------------------------------------------------------------------------
-// k5: resync.  One CTA per (sequence, head), DK + DV threads; returns at once unless the
-// sequence's token completed a chunk.  It runs the same routines as prefill: the FP32
-// phase and the prep product of k1_chunk_prep (prep_operands, prep_mma, prep_epilogue,
-// here into shared memory), then one chain product and epilogue of k2_chain (chain_mma,
-// chain_epilogue) on the ring's S_b.  The result replaces both the state and ring S_b.
+// k5: resync.  A persistent grid of at most one wave walks the (sequence, head) pairs of
+// the sequences whose token completed a chunk (k4 appends them to a list), DK + DV
+// threads per CTA.  Each pair runs the same routines as prefill: the FP32 phase and the
+// prep product of k1_chunk_prep (prep_operands, prep_mma, prep_epilogue, here into shared
+// memory), then the chain products and epilogue of k2_chain (chain_mma, chain_values) on
+// the ring's S_b.  The result replaces both the state and ring S_b.  The list's order
+// varies from run to run; each pair's result does not depend on it.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C, typename T>
-__global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
+__device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, unsigned char* sm5, uint32_t tmem,
+                                           uint64_t* mbar)
 {
     using U = UCfg<DK, DV, C>;
-    extern __shared__ __align__(1024) unsigned char sm5[];
     const PrepSmem<DK, C> s(reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5 + U::RS_VEC_OFF));
     constexpr int KS = PrepSmem<DK, C>::KS;
     unsigned char* bop = sm5;                    // then the M^T image
@@ -165,22 +168,13 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     unsigned char* mt = sm5;
     float* bt = reinterpret_cast<float*>(sm5 + U::RS_BT_OFF);
     unsigned char* stile = sm5 + U::RS_S_OFF;
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm5 + U::RS_BAR_OFF);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
 
-    const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
-    const int p = a.pos[b];
-    if (p < 0 || p % C != C - 1) return;
+    const int tid = threadIdx.x, H = a.H;
     const size_t bh = (size_t)b * H + h;
     const size_t SS = (size_t)DK * DV;
     const T* rk = static_cast<const T*>(a.ring.k) + bh * C * DK;
     const T* rv = static_cast<const T*>(a.ring.v) + bh * C * DV;
 
-    if (tid < 32) tc::tmem_alloc(tslot, U::TMEM_COLS);
-    if (tid == 0) {
-        tc::mbar_init(mbar, 1);
-        tc::fence_mbar_init();
-    }
     for (int idx = tid; idx < C * DK; idx += blockDim.x) s.kf[(idx / DK) * KS + idx % DK] = to_f32<T>(rk[idx]);
     if (tid < C) {
         s.G[tid] = a.ring.g[bh * C + tid];
@@ -192,33 +186,60 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     tc::fence_before_sync();
     prep_operands<DK, DV, C, T>(s, aop, bop, rv, (size_t)DV);  // also publishes the S tiles
     tc::fence_after_sync();
-    const uint32_t tmem = *tslot;
     if (tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
     bool ok = __syncthreads_and(tc::mbar_wait(mbar, 0));
-    if (ok) prep_epilogue<DK, DV, C>(tmem, decay_exp(s.G[C - 1]), mt, bt);
+    if (ok) prep_epilogue<DK, DV, C>(tmem, decay_exp(s.G[C - 1]), mt, bt, nullptr);
     __syncthreads();
-    if (ok) {
-        // the chain products of prefill, one 64-row slice at a time, into TMEM columns sl*DK
-        if (tid == 0) {
+    if (!ok) return false;
+    // the chain products of prefill, one 64-row slice at a time, into TMEM columns sl*DK
+    if (tid == 0) {
 #pragma unroll
-            for (int sl = 0; sl < U::NSLICE; ++sl)
-                chain_mma<DK>(tmem + sl * DK, stile + sl * 2 * U::S_SPLIT, mt, mbar, sl == U::NSLICE - 1);
-        }
-        ok = __syncthreads_and(tc::mbar_wait(mbar, 1));
-        if (ok) {
-            tc::fence_after_sync();
-            constexpr int NW = (DK + DV) / 32, WPQ = NW >= 8 ? 2 : 1;
+        for (int sl = 0; sl < U::NSLICE; ++sl)
+            chain_mma<DK>(tmem + sl * DK, stile + sl * 2 * U::S_SPLIT, mt, mbar, sl == U::NSLICE - 1);
+    }
+    ok = __syncthreads_and(tc::mbar_wait(mbar, 1));
+    if (!ok) return false;
+    tc::fence_after_sync();
+    constexpr int NW = (DK + DV) / 32, WPQ = NW >= 8 ? 2 : 1;
 #pragma unroll
-            for (int sl = 0; sl < U::NSLICE; ++sl) {
-                float v[ChainMap<DK, WPQ>::CPT];
-                chain_values<DK, DV, WPQ>(tmem + sl * DK, bt + (size_t)sl * kChainRows * DK, sl * kChainRows, v);
-                chain_store<DK, DV, WPQ>(a.state + bh * SS, sl * kChainRows, v);
-                chain_store<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
-            }
-            tc::fence_before_sync();
+    for (int sl = 0; sl < U::NSLICE; ++sl) {
+        float v[ChainMap<DK, WPQ>::CPT];
+        chain_values<DK, DV, WPQ>(tmem + sl * DK, bt + (size_t)sl * kChainRows * DK, sl * kChainRows, v);
+        chain_store<DK, DV, WPQ>(a.state + bh * SS, sl * kChainRows, v);
+        chain_store<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
+    }
+    tc::fence_before_sync();
+    __syncthreads();  // TMEM and shared memory are free for the next pair
+    tc::fence_after_sync();
+    return true;
+}
+
+template <int DK, int DV, int C, typename T>
+__global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
+{
+    using U = UCfg<DK, DV, C>;
+    extern __shared__ __align__(1024) unsigned char sm5[];
+    const uint32_t items = *a.resync_count * (uint32_t)a.H;
+    if (blockIdx.x >= items) return;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm5 + U::RS_BAR_OFF);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    const int tid = threadIdx.x;
+    if (tid < 32) tc::tmem_alloc(tslot, U::TMEM_COLS);
+    if (tid == 0) {
+        tc::mbar_init(mbar, 1);  // two phases per pair, so every pair starts on parity 0
+        tc::fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    for (uint32_t it = blockIdx.x; it < items; it += gridDim.x) {
+        if (!resync_one<DK, DV, C, T>(a, a.resync_list[it / a.H], (int)(it % a.H), sm5, tmem, mbar)) {
+            if (tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
+            break;  // uniform: the barrier's phase is unknown after a timeout
         }
     }
-    if (!ok && tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
+    tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     if (tid < 32) tc::tmem_dealloc(tmem, U::TMEM_COLS);
@@ -279,7 +300,7 @@ __global__ void __launch_bounds__(256) k6_ring_fill(RingArgs a)
 template <int DK, int DV, int C, typename T>
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
 {
-    cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s);
+    cudaError_t e = cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), s);  // status word and resync count
     if (e != cudaSuccess) return e;
     profile_mark(0, s);
     k4_decode_step<DK, DV, C, T><<<dim3(a.B, a.H), 256, 0, s>>>(a);
@@ -290,7 +311,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::RS_BYTES, tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
     e = cudaFuncSetAttribute(k5_resync<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
     if (e != cudaSuccess) return e;
-    k5_resync<DK, DV, C, T><<<dim3(a.B, a.H), DK + DV, sm5, s>>>(a);
+    const int grid = std::max(1, std::min(a.B * a.H, a.num_sms * (int)(232448 / sm5)));
+    k5_resync<DK, DV, C, T><<<grid, DK + DV, sm5, s>>>(a);
     e = cudaGetLastError();
     profile_mark(2, s);
     return e;

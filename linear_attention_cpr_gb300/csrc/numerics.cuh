@@ -12,7 +12,7 @@
 // bitwise exact across trainer forward, rollout prefill and rollout decode).
 //
 // Token step (gated delta rule; S is dv x dk, row i = value index):
-//   alpha = decay_exp(g)
+//   alpha = decay_exp(g)                          (e^g via 2^(g log2 e), see below)
 //   x_i   = dot_dk(S_i, k)                        (canonical tree, below)
 //   u_i   = beta * (v_i - alpha * x_i)            (mul, sub, mul)
 //   S_ij <- fma(u_i, k_j, alpha * S_ij)           (mul, fma)
@@ -40,9 +40,18 @@
 
 namespace cpr {
 
-// exp of every decay (alpha and the chunk-update decays): one out-of-line definition,
-// so that every kernel runs the identical instruction sequence.
-static __device__ __noinline__ float decay_exp(float x) { return expf(x); }
+// exp of every decay (alpha and the chunk-update decays), written from the identity
+// e^x = 2^(x log2 e): one round-to-nearest product with log2 e, then the hardware base-2
+// exponential (PTX ex2.approx.f32, relative error below 2^-22 of its argument's 2^y,
+// subnormal results kept).  Explicit instructions only, so every kernel computes the
+// same bits; the decays here are e^x with x <= 0, results in [0, 1].
+static __device__ __forceinline__ float decay_exp(float x)
+{
+    const float y = __fmul_rn(x, 1.4426950408889634f);  // log2(e), rounded to fp32
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
 
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
@@ -125,22 +134,17 @@ __device__ __forceinline__ void kk_tile(const float* ks, int ks_stride, int r0, 
 
 // Forward substitution of one column: x[r] = init[r] - sum_{i<r} A[r][i] x[i],
 // accumulated as fma(-A_ri, x_i, .) for i ascending.  A: fp32 smem [C][a_stride].
+// The loops run column-outermost (x[t] is final once the terms of columns < t are in),
+// so consecutive instructions are independent; every row still adds its terms in
+// ascending i, which is the operation sequence above.
 template <int C>
 __device__ __forceinline__ void fwd_subst(const float* A, int a_stride, float x[C])
 {
 #pragma unroll
-    for (int r = 1; r < C; ++r) {
-        float acc = x[r];
-        const float4* row = reinterpret_cast<const float4*>(A + r * a_stride);  // 16-byte aligned rows
+    for (int t = 0; t < C - 1; ++t) {
+        const float xt = x[t];
 #pragma unroll
-        for (int i4 = 0; i4 < r; i4 += 4) {
-            const float4 a4 = row[i4 / 4];
-            acc = __fmaf_rn(-a4.x, x[i4], acc);
-            if (i4 + 1 < r) acc = __fmaf_rn(-a4.y, x[i4 + 1], acc);
-            if (i4 + 2 < r) acc = __fmaf_rn(-a4.z, x[i4 + 2], acc);
-            if (i4 + 3 < r) acc = __fmaf_rn(-a4.w, x[i4 + 3], acc);
-        }
-        x[r] = acc;
+        for (int r = t + 1; r < C; ++r) x[r] = __fmaf_rn(-A[r * a_stride + t], xt, x[r]);
     }
 }
 

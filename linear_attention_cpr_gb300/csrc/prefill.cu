@@ -83,6 +83,7 @@ template <int DK, int DV, int C, typename T>
 __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
 {
     using U = UCfg<DK, DV, C>;
+    static_assert(U::R1 >= U::MT_BYTES && U::R1 >= U::BT_BYTES, "R1 stages the prep outputs");
     extern __shared__ __align__(1024) unsigned char sm1[];
     const PrepSmem<DK, C> s(reinterpret_cast<float*>(sm1), reinterpret_cast<float*>(sm1 + U::VEC_OFF));
     constexpr int KS = PrepSmem<DK, C>::KS;
@@ -138,11 +139,13 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
     const bool ok = __syncthreads_and(tc::mbar_wait(mbar, 0));  // uniform: the epilogue's TMEM loads are warp-wide
     if (ok) {
         const size_t ch = (size_t)c * H + h;
-        prep_epilogue<DK, DV, C>(tmem, decay_exp(s.G[C - 1]), a.mt + ch * U::MT_BYTES, a.bt + ch * DK * DV);
+        // the operand space (R1) is dead once the products completed: it stages the outputs
+        prep_epilogue<DK, DV, C>(tmem, decay_exp(s.G[C - 1]), a.mt + ch * U::MT_BYTES, a.bt + ch * DK * DV, sm1);
     } else if (tid == 0) {
         atomicOr(a.status, CPR_DEV_TIMEOUT);
     }
     __syncthreads();
+    if (tid == 0) tc::bulk_wait_all();
     tc::fence_after_sync();
     if (tid < 32) tc::tmem_dealloc(tmem, U::TMEM_COLS);
 }

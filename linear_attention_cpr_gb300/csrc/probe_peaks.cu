@@ -7,9 +7,19 @@
 //   lanes, or 16 pairs when paired != 0) for `iters` rounds; returns the kernel time
 //   in ms (CUDA events on `stream`).  FLOPs = blocks*threads*iters*16*2*(paired?2:1).
 //   sink: device buffer of blocks*threads floats (defeats dead-code elimination).
+// extern "C" int cpr_probe_decay_exp(const float* x, float* y, int n, void* stream)
+//   The library's decay exponential (numerics.cuh) on n device floats, for its tests.
 #include <cuda_runtime.h>
 
+#include "numerics.cuh"
+
 namespace {
+
+__global__ void probe_decay_exp(const float* x, float* y, int n)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) y[i] = cpr::decay_exp(x[i]);
+}
 
 __global__ void __launch_bounds__(256) probe_ffma(float* sink, int iters, float a, float b)
 {
@@ -69,4 +79,13 @@ extern "C" int cpr_probe_fp32(int paired, int blocks, int threads, int iters, fl
     if (err != cudaSuccess) return -5;
     *ms_out = ms;
     return 0;
+}
+
+// The library's decay exponential applied to n device floats (test hook): y[i] = e^x[i].
+extern "C" int cpr_probe_decay_exp(const float* x, float* y, int n, void* stream)
+{
+    if (!x || !y || n < 0) return -1;
+    if (n == 0) return 0;
+    probe_decay_exp<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }

@@ -100,6 +100,20 @@ __device__ __forceinline__ void bulk_g2s(void* smem, const void* gmem, uint32_t 
         : "memory");
 }
 
+// Bulk copy shared -> global (both 16-byte aligned, bytes a multiple of 16), tracked by
+// this thread's bulk group: commit with bulk_commit, wait with bulk_wait_read.
+__device__ __forceinline__ void bulk_s2g(void* gmem, const void* smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gmem), "r"(smem_u32(smem)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// Wait until every committed bulk store of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // Allocation (one full warp).  The TMEM address lands in *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols)
 {

@@ -85,7 +85,8 @@ def test_prefill_rejects_on_host(lib):
 
 def test_decode_rejects_on_host(lib):
     ring = binding._Ring(16, 16, 16, 16, 16)
-    base = [16, 16, 16, 16, 16, 16, ctypes.byref(ring), 16, 4, 2, 128, 128, 64, 0, 16, 16, 256, None]
+    ws = lib.cpr_gdn_decode_workspace_size(4, 2, 128, 128, 64)
+    base = [16, 16, 16, 16, 16, 16, ctypes.byref(ring), 16, 4, 2, 128, 128, 64, 0, 16, 16, ws, None]
     # `base` itself is never passed: its pointers are placeholders, only rejected variants run
     bad = list(base)
     bad[10], bad[11] = 96, 96

@@ -179,3 +179,25 @@ def test_device_checks_record_status():
     o, ws = cpr.cpr_gdn_decode(t["q"], t["k"], t["v"], t["g"], t["beta"], state, ring, pos, C, workspace=ws)
     torch.cuda.synchronize()
     assert cpr.cpr_gdn_device_status(ws) == 0
+
+
+def test_decay_exp_error_bound():
+    """The decay exponential e^x = 2^(x log2 e) (ex2.approx) against fp64 exp on x <= 0.
+    Rounding x log2 e to fp32 moves the exponent by up to |x log2 e| 2^-24, a relative
+    error of about |x| 2^-24 in e^x; ex2.approx adds at most 2^-22.  So the bound is
+    2^-21 + |x| 2^-23 (twice the sum) wherever e^x is a normal float, and 1 exactly at 0."""
+    import ctypes
+
+    probe = ctypes.CDLL(build.PROBE_LIB)
+    probe.cpr_probe_decay_exp.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    x = torch.cat([torch.zeros(1), -torch.logspace(-8, 1.9, 200000, dtype=torch.float64).float()]).cuda()
+    y = torch.empty_like(x)
+    assert probe.cpr_probe_decay_exp(x.data_ptr(), y.data_ptr(), x.numel(), None) == 0
+    torch.cuda.synchronize()
+    ref = torch.exp(x.double())
+    rel = ((y.double() - ref).abs() / ref).cpu()
+    normal = (ref > 1.2e-38).cpu()
+    bound = 2.0 ** -21 + x.abs().double().cpu() * 2.0 ** -23
+    excess = (rel - bound)[normal]
+    assert float(excess.max()) <= 0.0, float((rel / bound)[normal].max())
+    assert float(y[0]) == 1.0
