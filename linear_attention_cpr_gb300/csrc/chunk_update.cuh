@@ -3,6 +3,8 @@
 // kernel.  Element sequences are those of numerics.cuh.
 #pragma once
 
+#include <type_traits>
+
 #include "numerics.cuh"
 #include "tc.cuh"
 
@@ -15,7 +17,7 @@ struct PrepSmem {
     static constexpr int KS = DK + 4;
     static constexpr size_t floats = (size_t)C * KS + (size_t)C * C + 4 * (size_t)C;
     float* kf;   // [C][KS]
-    float* A;    // [C][C]
+    float* A;    // [C][C], transposed: A[i * C + r] = A_ri
     float* G;    // [C]  g on entry, G (sequential cumulative sum) after chunk_decays_and_A
     float* be;   // [C]  beta_r * e_r
     float* bs;   // [C]  beta_r
@@ -27,14 +29,64 @@ struct PrepSmem {
         : kf(base), A(base + C * KS), G(vec), be(vec + C), bs(vec + 2 * C), dvs(vec + 3 * C) {}
 };
 
-// G, e, d, beta*e and the strictly lower-triangular A from kf, g (in G) and beta (in bs).
-// Must be called by every thread of the CTA; contains __syncthreads.
-template <int DK, int C>
-__device__ __forceinline__ void chunk_decays_and_A(const PrepSmem<DK, C>& s)
+// The key Gram matrix kk = K K^T of one chunk on the tensor cores: one M = 64, N = C,
+// K = DK tcgen05 product (rows r, columns i) of the keys' bf16 splits.  bf16 keys are
+// their own hi split (lo = 0), so one product is the whole sum; fp32 keys take three
+// (hi*hi + hi*lo + lo*hi).  The tile holds C rows per split; rows C..63 of the M = 64
+// A operand read whatever follows (their accumulator rows are never used), so the
+// region must span SPAN bytes.
+template <int DK, int C, typename T>
+struct KKCfg {
+    static constexpr int NSPLIT = std::is_same<T, __nv_bfloat16>::value ? 1 : 2;
+    static constexpr uint32_t SPLIT = C * DK * 2;
+    static constexpr uint32_t SPAN = SPLIT + 64 * DK * 2;  // fp32 keys, the larger case
+    static constexpr uint32_t idesc = tc::idesc_bf16(64, C);
+};
+
+// G, e, d, beta*e and the strictly lower-triangular A (stored transposed: At[i][r] =
+// A_ri) from kf, g (in G) and beta (in bs); ktile: scratch of KKCfg::SPAN bytes for the
+// key tile; TMEM columns [tmem, tmem + C) hold kk; the product's completion arrives on
+// mbar with the given parity.  All DK + DV threads; contains __syncthreads.  Returns
+// false (uniformly) when the product's wait timed out; A is then undefined.
+template <int DK, int DV, int C, typename T>
+__device__ __forceinline__ bool chunk_decays_and_A(const PrepSmem<DK, C>& s, unsigned char* ktile, uint32_t tmem,
+                                                   uint64_t* mbar, uint32_t parity)
 {
+    using KC = KKCfg<DK, C, T>;
+    constexpr int KS = PrepSmem<DK, C>::KS;
+    constexpr int NWARP = (DK + DV) / 32;
+    static_assert(NWARP >= 4 || C <= 16 * NWARP, "every TMEM lane quadrant holding kk rows needs a warp");
     const int tid = threadIdx.x;
     __syncthreads();
-    if (tid == 0) {  // sequential cumulative sum, in registers
+    for (int idx = tid; idx < C * (DK / 8); idx += DK + DV) {
+        const int r = idx % C, c0 = (idx / C) * 8;
+        uint16_t hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tc::split_bf16(s.kf[r * KS + c0 + e], hi[e], lo[e]);
+        const uint32_t off = tc::tile_off<2>(r, c0, DK);
+        *reinterpret_cast<uint4*>(ktile + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
+                                                            hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
+        if (KC::NSPLIT == 2)
+            *reinterpret_cast<uint4*>(ktile + KC::SPLIT + off) =
+                make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
+                           lo[6] | (uint32_t)lo[7] << 16);
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        tc::fence_after_sync();
+        constexpr uint32_t SBO = (DK / 8) * 128;
+        const uint32_t ko = tc::smem_u32(ktile);
+        const uint32_t ha[3] = {0u, 0u, 1u}, hb[3] = {0u, 1u, 0u};
+#pragma unroll
+        for (int p = 0; p < (KC::NSPLIT == 2 ? 3 : 1); ++p)
+#pragma unroll
+            for (int k = 0; k < DK / 16; ++k)
+                tc::mma_bf16(tmem, tc::sdesc(ko + ha[p] * KC::SPLIT + k * 256, 128, SBO),
+                             tc::sdesc(ko + hb[p] * KC::SPLIT + k * 256, 128, SBO), KC::idesc, (p | k) ? 1u : 0u);
+        tc::commit(mbar);
+        // sequential cumulative sum, in registers, while the product runs
         float gr[C];
 #pragma unroll
         for (int r = 0; r < C; r += 4) {
@@ -54,25 +106,25 @@ __device__ __forceinline__ void chunk_decays_and_A(const PrepSmem<DK, C>& s)
         s.be[tid] = __fmul_rn(s.bs[tid], decay_exp(s.G[tid]));
         s.dvs[tid] = decay_exp(__fsub_rn(s.G[C - 1], s.G[tid]));
     }
-    constexpr int NT = C / 4;
-    for (int t = tid; t < NT * (NT + 1) / 2; t += blockDim.x) {
-        int R = 0, rem = t;
-        while (rem > R) {
-            rem -= R + 1;
-            ++R;
+    const bool ok = __syncthreads_and(tc::mbar_wait(mbar, parity));
+    if (ok) {
+        tc::fence_after_sync();
+        constexpr int WPQ = NWARP >= 8 ? 2 : 1;  // warps per TMEM lane quadrant
+        constexpr int CPW = C / WPQ, CPT = CPW / 2;
+        const int warp = tid >> 5, q = warp & 3, hh = warp >> 2;
+        if (warp < 4 * WPQ && 16 * q < C) {  // warp-uniform
+            float kk[CPT];
+            tc::tmem_ld_16x2<CPT>(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hh * CPW), kk);
+            const int r = 16 * q + (tid & 15), i0 = hh * CPW + ((tid >> 4) & 1) * CPT;
+            const float br = s.bs[r], Gr = s.G[r];
+#pragma unroll
+            for (int e = 0; e < CPT; ++e)
+                if (i0 + e < r) s.A[(i0 + e) * C + r] = a_entry(br, Gr, s.G[i0 + e], kk[e]);
         }
-        const int I = rem;
-        float acc[4][4];
-        kk_tile<DK>(s.kf, PrepSmem<DK, C>::KS, 4 * R, 4 * I, acc);
-#pragma unroll
-        for (int aa = 0; aa < 4; ++aa)
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-                const int r = 4 * R + aa, i = 4 * I + bb;
-                if (i < r) s.A[r * C + i] = a_entry(s.bs[r], s.G[r], s.G[i], acc[aa][bb]);
-            }
+        tc::fence_before_sync();
     }
     __syncthreads();
+    return ok;
 }
 
 // Column `col` of [W | U~] (col < DK: W, else U~ column col - DK) by forward
@@ -88,7 +140,7 @@ __device__ __forceinline__ void chunk_column(const PrepSmem<DK, C>& s, int col, 
 #pragma unroll
         for (int r = 0; r < C; ++r) x[r] = __fmul_rn(s.bs[r], to_f32<T>(vbase[(size_t)r * vstride + (col - DK)]));
     }
-    fwd_subst<C>(s.A, C, x);
+    fwd_subst<C>(s.A, x);
 }
 
 // ======================================================================================
@@ -124,13 +176,15 @@ struct UCfg {
     // R1 also stages the prep outputs (M^T image, then B) before their bulk stores
     static constexpr uint32_t R1 = mx(mx(R1A, 2 * BOP_SPLIT), mx(2 * DK * DK * 2, DK * DV * 4));
     static constexpr uint32_t AOP_OFF = (R1 + 1023) / 1024 * 1024;
-    static constexpr uint32_t VEC_OFF = AOP_OFF + 2 * AOP_SPLIT;
+    // the (D K)^T operand region first holds the key tile of the kk product
+    static constexpr uint32_t AOP_REGION = mx(2 * AOP_SPLIT, KKCfg<DK, C, float>::SPAN);
+    static constexpr uint32_t VEC_OFF = AOP_OFF + AOP_REGION;
     static constexpr uint32_t PREP_BYTES = VEC_OFF + 4 * C * 4;
-    static constexpr uint32_t TMEM_COLS = 2 * DK <= 32 ? 32 : 2 * DK <= 64 ? 64 : 2 * DK <= 128 ? 128 : 256;
+    static constexpr uint32_t TMEM_COLS = mx(2 * DK, C) <= 32 ? 32 : mx(2 * DK, C) <= 64 ? 64 : mx(2 * DK, C) <= 128 ? 128 : 256;
     // decode resync (prep and one chain step in one CTA): [R1 | Mt] [Aop | Bt] [vectors] [S tile]
     static constexpr uint32_t up1k(uint32_t x) { return (x + 1023) / 1024 * 1024; }
     static constexpr uint32_t RS_BT_OFF = up1k(R1 > MT_BYTES ? R1 : MT_BYTES);
-    static constexpr uint32_t RS_VEC_OFF = up1k(RS_BT_OFF + (2 * AOP_SPLIT > BT_BYTES ? 2 * AOP_SPLIT : BT_BYTES));
+    static constexpr uint32_t RS_VEC_OFF = up1k(RS_BT_OFF + mx(AOP_REGION, BT_BYTES));
     static constexpr uint32_t RS_S_OFF = up1k(RS_VEC_OFF + 4 * C * 4);
     static constexpr uint32_t RS_BAR_OFF = RS_S_OFF + NSLICE * 2 * S_SPLIT;
     static constexpr uint32_t RS_BYTES = RS_BAR_OFF + 64;
@@ -140,17 +194,19 @@ struct UCfg {
 };
 
 // Build both prep operands in shared memory from the chunk's keys (s.kf, fp32), g (s.G)
-// and beta (s.bs); V element (r, n) at vbase[r * vstride + n].  All threads; contains
-// __syncthreads.  On return aop / bop hold the bf16 splits and are visible to the
-// tensor cores.
+// and beta (s.bs); V element (r, n) at vbase[r * vstride + n].  All DK + DV threads;
+// contains __syncthreads.  The kk product uses TMEM columns [tmem, tmem + C) and one
+// phase of mbar (parity given).  On a true return aop / bop hold the bf16 splits and are
+// visible to the tensor cores; false (uniform) means the kk product timed out.
 template <int DK, int DV, int C, typename T>
-__device__ __forceinline__ void prep_operands(const PrepSmem<DK, C>& s, unsigned char* aop, unsigned char* bop,
-                                              const T* vbase, size_t vstride)
+__device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned char* aop, unsigned char* bop,
+                                              const T* vbase, size_t vstride, uint32_t tmem, uint64_t* mbar,
+                                              uint32_t parity)
 {
     using U = UCfg<DK, DV, C>;
     constexpr int KS = PrepSmem<DK, C>::KS;
     const int tid = threadIdx.x, nt = blockDim.x;
-    chunk_decays_and_A<DK, C>(s);
+    if (!chunk_decays_and_A<DK, DV, C, T>(s, aop, tmem, mbar, parity)) return false;
     // (D K)^T rows c: d_r * k_r[c] (zero rows beyond DK)
     for (int row = tid; row < U::MPAD; row += nt) {
 #pragma unroll
@@ -186,6 +242,7 @@ __device__ __forceinline__ void prep_operands(const PrepSmem<DK, C>& s, unsigned
     }
     tc::fence_proxy_async();
     __syncthreads();
+    return true;
 }
 
 // One thread: both prep products (X into TMEM columns [0, DK), B into [DK, 2 DK)), then

@@ -150,15 +150,15 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 // ------------------------------------------------------------------------------------
 // k5: resync.  A persistent grid of at most one wave walks the (sequence, head) pairs of
 // the sequences whose token completed a chunk (k4 appends them to a list), DK + DV
-// threads per CTA.  Each pair runs the same routines as prefill: the FP32 phase and the
-// prep product of k1_chunk_prep (prep_operands, prep_mma, prep_epilogue, here into shared
+// threads per CTA.  Each pair runs the same routines as prefill: the key Gram product, the
+// FP32 phase and the prep product of k1_chunk_prep (prep_operands, prep_mma, prep_epilogue, here into shared
 // memory), then the chain products and epilogue of k2_chain (chain_mma, chain_values) on
 // the ring's S_b.  The result replaces both the state and ring S_b.  The list's order
 // varies from run to run; each pair's result does not depend on it.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C, typename T>
 __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, unsigned char* sm5, uint32_t tmem,
-                                           uint64_t* mbar)
+                                           uint64_t* mbar, uint32_t& phase)
 {
     using U = UCfg<DK, DV, C>;
     const PrepSmem<DK, C> s(reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5 + U::RS_VEC_OFF));
@@ -184,10 +184,14 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     for (int sl = 0; sl < U::NSLICE; ++sl)
         stile_fill<DK, DV>(stile + sl * 2 * U::S_SPLIT, a.ring.S_b + bh * SS, sl * kChainRows, tid, (int)blockDim.x);
     tc::fence_before_sync();
-    prep_operands<DK, DV, C, T>(s, aop, bop, rv, (size_t)DV);  // also publishes the S tiles
+    // also publishes the S tiles
+    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, rv, (size_t)DV, tmem, mbar, phase & 1);
+    ++phase;
+    if (!ok) return false;
     tc::fence_after_sync();
     if (tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
-    bool ok = __syncthreads_and(tc::mbar_wait(mbar, 0));
+    ok = __syncthreads_and(tc::mbar_wait(mbar, phase & 1));
+    ++phase;
     if (ok) prep_epilogue<DK, DV, C>(tmem, decay_exp(s.G[C - 1]), mt, bt, nullptr);
     __syncthreads();
     if (!ok) return false;
@@ -197,7 +201,8 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
         for (int sl = 0; sl < U::NSLICE; ++sl)
             chain_mma<DK>(tmem + sl * DK, stile + sl * 2 * U::S_SPLIT, mt, mbar, sl == U::NSLICE - 1);
     }
-    ok = __syncthreads_and(tc::mbar_wait(mbar, 1));
+    ok = __syncthreads_and(tc::mbar_wait(mbar, phase & 1));
+    ++phase;
     if (!ok) return false;
     tc::fence_after_sync();
     constexpr int NW = (DK + DV) / 32, WPQ = NW >= 8 ? 2 : 1;
@@ -226,15 +231,16 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     const int tid = threadIdx.x;
     if (tid < 32) tc::tmem_alloc(tslot, U::TMEM_COLS);
     if (tid == 0) {
-        tc::mbar_init(mbar, 1);  // two phases per pair, so every pair starts on parity 0
+        tc::mbar_init(mbar, 1);  // three phases per pair: kk, prep, chain
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
+    uint32_t phase = 0;
     for (uint32_t it = blockIdx.x; it < items; it += gridDim.x) {
-        if (!resync_one<DK, DV, C, T>(a, a.resync_list[it / a.H], (int)(it % a.H), sm5, tmem, mbar)) {
+        if (!resync_one<DK, DV, C, T>(a, a.resync_list[it / a.H], (int)(it % a.H), sm5, tmem, mbar, phase)) {
             if (tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
             break;  // uniform: the barrier's phase is unknown after a timeout
         }

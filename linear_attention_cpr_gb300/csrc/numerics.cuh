@@ -25,13 +25,16 @@
 // pages fix only that one fixed-order fp32 function produces every boundary state):
 //   G_0 = g_0, G_r = G_{r-1} + g_r              (sequential)
 //   e_r = decay_exp(G_r),  d_r = decay_exp(G_{C-1} - G_r),  gamma = e_{C-1}
-//   kk_ri = k_r[0]*k_i[0], then fma over j = 1 .. dk-1          (i < r)
+//   kk_ri = sum_j k_r[j] k_i[j]: a tcgen05 product of the keys' bf16 splits, fp32
+//           accumulation (exact products for bf16 keys; hi*hi + hi*lo + lo*hi for fp32)
 //   A_ri  = (beta_r * decay_exp(G_r - G_i)) * kk_ri              (i < r, else 0)
 //   W_r[c]  = (beta_r * e_r) * k_r[c],  then fma(-A_ri, W_i[c], .) for i = 0 .. r-1
 //   U~_r[n] = beta_r * v_r[n],          then fma(-A_ri, U~_i[n], .) for i = 0 .. r-1
-//   p_rn  = W_r[0]*S_b[n][0], then fma over j = 1 .. dk-1
-//   dd_rn = d_r * (U~_r[n] - p_rn)
-//   S_new[n][c] = gamma * S_b[n][c], then fma(dd_rn, k_r[c], .) for r = 0 .. C-1
+//   then, in matrix form with D = diag(d_r) (chunk_update.cuh):
+//   M^T = gamma I - (D K)^T W,  B = U~^T (D K):  tcgen05 products (M = 128, N = dk,
+//         K = C) of bf16 hi/lo splits, hi*hi + hi*lo + lo*hi, fp32 accumulation
+//   S_new = S_b M + B:  per 64 value rows, a tcgen05 product of S_b's splits with M's
+//         (M = 64, N = dk, K = dk, the same three products), then one fp32 add of B
 #pragma once
 
 #include <cuda_bf16.h>
@@ -105,113 +108,27 @@ __device__ __forceinline__ float a_entry(float beta_r, float Gr, float Gi, float
     return __fmul_rn(__fmul_rn(beta_r, decay_exp(__fsub_rn(Gr, Gi))), kk);
 }
 
-// kk[a][b] = k_{r0+a} . k_{i0+b} over DK entries, sequential in j.
-// ks: fp32 [C][ks_stride] (rows 16-byte aligned).
-template <int DK>
-__device__ __forceinline__ void kk_tile(const float* ks, int ks_stride, int r0, int i0, float acc[4][4])
-{
-#pragma unroll
-    for (int j = 0; j < DK; j += 4) {
-        float4 ar[4], bi[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) ar[a] = *reinterpret_cast<const float4*>(ks + (r0 + a) * ks_stride + j);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) bi[b] = *reinterpret_cast<const float4*>(ks + (i0 + b) * ks_stride + j);
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                if (j == 0)
-                    acc[a][b] = __fmul_rn(ar[a].x, bi[b].x);
-                else
-                    acc[a][b] = __fmaf_rn(ar[a].x, bi[b].x, acc[a][b]);
-                acc[a][b] = __fmaf_rn(ar[a].y, bi[b].y, acc[a][b]);
-                acc[a][b] = __fmaf_rn(ar[a].z, bi[b].z, acc[a][b]);
-                acc[a][b] = __fmaf_rn(ar[a].w, bi[b].w, acc[a][b]);
-            }
-    }
-}
-
 // Forward substitution of one column: x[r] = init[r] - sum_{i<r} A[r][i] x[i],
-// accumulated as fma(-A_ri, x_i, .) for i ascending.  A: fp32 smem [C][a_stride].
-// The loops run column-outermost (x[t] is final once the terms of columns < t are in),
-// so consecutive instructions are independent; every row still adds its terms in
-// ascending i, which is the operation sequence above.
+// accumulated as fma(-A_ri, x_i, .) for i ascending.  At: fp32 smem [C][C] holding A
+// transposed (At[i * C + r] = A_ri, 16-byte aligned rows).  The loops run column-outermost
+// (x[t] is final once the terms of columns < t are in), so consecutive instructions are
+// independent and a column's coefficients come in 16-byte loads; every row still adds
+// its terms in ascending i, which is the operation sequence above.
 template <int C>
-__device__ __forceinline__ void fwd_subst(const float* A, int a_stride, float x[C])
+__device__ __forceinline__ void fwd_subst(const float* At, float x[C])
 {
 #pragma unroll
     for (int t = 0; t < C - 1; ++t) {
         const float xt = x[t];
 #pragma unroll
-        for (int r = t + 1; r < C; ++r) x[r] = __fmaf_rn(-A[r * a_stride + t], xt, x[r]);
+        for (int r4 = ((t + 1) / 4) * 4; r4 < C; r4 += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(At + t * C + r4);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (r4 + e > t) x[r4 + e] = __fmaf_rn(-av[e], xt, x[r4 + e]);
+        }
     }
-}
-
-// dd[a][b] for r = r0+a, n = n0+b:  d_r * (U~_r[n] - W_r . S_b[n]), the dot sequential
-// in j.  Wt: fp32 [DK][wt_stride] (W transposed), St: fp32 [DK][st_stride] (S_b stored
-// [dk][dv], the slice's column n at offset n), Us: fp32 [C][us_stride], dvec[C].
-template <int DK>
-__device__ __forceinline__ void delta_tile(const float* Wt, int wt_stride, const float* St, int st_stride,
-                                           const float* Us, int us_stride, const float* dvec, int r0,
-                                           int n0, float out[4][4])
-{
-    float acc[4][4];
-#pragma unroll 8
-    for (int j = 0; j < DK; ++j) {
-        const float4 w = *reinterpret_cast<const float4*>(Wt + j * wt_stride + r0);
-        const float4 s = *reinterpret_cast<const float4*>(St + j * st_stride + n0);
-        const float wv[4] = {w.x, w.y, w.z, w.w};
-        const float sv[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-                acc[a][b] = (j == 0) ? __fmul_rn(wv[a], sv[b]) : __fmaf_rn(wv[a], sv[b], acc[a][b]);
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const float4 u = *reinterpret_cast<const float4*>(Us + (r0 + a) * us_stride + n0);
-        const float uv[4] = {u.x, u.y, u.z, u.w};
-        const float d = dvec[r0 + a];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) out[a][b] = __fmul_rn(d, __fsub_rn(uv[b], acc[a][b]));
-    }
-}
-
-// S_new for value rows n0..n0+3 and key columns c0..c0+3, returned as out[c][n]
-// (storage order): gamma * S_b[n][c], then fma(dd_rn, k_r[c], .) for r = 0 .. C-1.
-// St: fp32 [DK][st_stride] (S_b storage slice), dd: fp32 [C][dd_stride], ks: fp32
-// [C][ks_stride].
-template <int C>
-__device__ __forceinline__ void snew_tile(const float* St, int st_stride, const float* dd, int dd_stride,
-                                          const float* ks, int ks_stride, float gamma, int n0, int c0,
-                                          float out[4][4])
-{
-    float acc[4][4];  // [c][n]
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const float4 s = *reinterpret_cast<const float4*>(St + (c0 + c) * st_stride + n0);
-        acc[c][0] = __fmul_rn(gamma, s.x);
-        acc[c][1] = __fmul_rn(gamma, s.y);
-        acc[c][2] = __fmul_rn(gamma, s.z);
-        acc[c][3] = __fmul_rn(gamma, s.w);
-    }
-#pragma unroll 8
-    for (int r = 0; r < C; ++r) {
-        const float4 d = *reinterpret_cast<const float4*>(dd + r * dd_stride + n0);
-        const float4 kv = *reinterpret_cast<const float4*>(ks + r * ks_stride + c0);
-        const float dv4[4] = {d.x, d.y, d.z, d.w};
-        const float kv4[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int n = 0; n < 4; ++n) acc[c][n] = __fmaf_rn(dv4[n], kv4[c], acc[c][n]);
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int n = 0; n < 4; ++n) out[c][n] = acc[c][n];
 }
 
 }  // namespace cpr

@@ -157,6 +157,18 @@ template <int N>
 __device__ __forceinline__ void tmem_ld_16x2(uint32_t taddr, float (&v)[N]);
 
 template <>
+__device__ __forceinline__ void tmem_ld_16x2<4>(uint32_t taddr, float (&v)[4])
+{
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x4.b32 {%0,%1,%2,%3}, [%4], 4;\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+template <>
 __device__ __forceinline__ void tmem_ld_16x2<8>(uint32_t taddr, float (&v)[8])
 {
     uint32_t r[8];

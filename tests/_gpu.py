@@ -51,6 +51,7 @@ def assert_close_to_oracle(o_gpu, st_gpu, o_ref, st_ref, o_tol, bnd_gpu=None, bn
     num = np.sqrt(((s - st_ref) ** 2).sum(axis=(-2, -1)))
     den = np.sqrt((st_ref ** 2).sum(axis=(-2, -1)))
     rel = np.where(den > 0, num / np.maximum(den, 1e-300), num)
+    print(f"parity {what}: max|do| {max_err:.3e} (tol {o_tol}), state rel Frobenius {float(rel.max()):.3e}")
     assert float(rel.max()) <= STATE_RTOL, f"{what}: state rel Frobenius {float(rel.max()):.3e}"
     if bnd_gpu is not None:
         b = bnd_gpu.cpu().double().numpy()[: bnd_ref.shape[0]]
