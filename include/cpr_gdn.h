@@ -211,10 +211,11 @@ int32_t cpr_gdn_prefill_noalloc(const void* q, const void* k, const void* v, con
  * Profiling hook (used by the benchmark to time each kernel with CUDA events on the
  * stream it runs on).  events: n_events cudaEvent_t handles created by the caller, or
  * NULL to switch the hook off.  While it is on, every cpr_gdn_prefill records
- * events[0] before its first kernel and events[i] after its i-th kernel (i = 1..4:
- * chunk index, chunk prep, boundary chain, intra-chunk recurrence; needs n_events >= 5),
- * and every cpr_gdn_decode records events[0] before and events[1], events[2] after its
- * step and resync kernels.  Process-wide; not for concurrent calls from several threads.
+ * events[0] before its first kernel and events[i] after its i-th kernel (i = 1..3:
+ * chunk index, chunk prep, boundary chain with the intra-chunk recurrence; needs
+ * n_events >= 4), and every cpr_gdn_decode records events[0] before and events[1],
+ * events[2] after its step and resync kernels.  Process-wide; not for concurrent calls
+ * from several threads.
  */
 int32_t cpr_gdn_set_profile_events(void* const* events, int32_t n_events);
 

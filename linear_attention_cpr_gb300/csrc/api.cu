@@ -33,6 +33,21 @@ int g_profile_n = 0;
 
 cudaEvent_t cpr::profile_event(int i) { return (i >= 0 && i < g_profile_n) ? g_profile_events[i] : nullptr; }
 
+namespace {
+// SM count of the current device, cached per device (0 on error).
+int num_sms()
+{
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cached[dev] = sms;
+    return sms;
+}
+}  // namespace
+
 extern "C" {
 
 int cpr_gdn_supported(int32_t dk, int32_t dv, int32_t C, int32_t dtype)
@@ -123,6 +138,9 @@ int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float
     a.cu_chunks = reinterpret_cast<int32_t*>(ws + lay.cu_chunks);
     a.mt = ws + lay.mt;
     a.bt = reinterpret_cast<float*>(ws + lay.bt);
+    a.ready = reinterpret_cast<uint32_t*>(ws + lay.ready);
+    a.num_sms = num_sms();
+    if (a.num_sms <= 0) return CPR_ERR_CUDA;
     a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);
     if (!boundary_states) {
         // boundary states are also the chain's hand-off to the intra-chunk kernel
@@ -213,10 +231,8 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
     a.status = static_cast<uint32_t*>(workspace);
     a.resync_count = static_cast<uint32_t*>(workspace) + 1;
     a.resync_list = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + kAlign);
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return CPR_ERR_CUDA;
-    a.num_sms = sms;
+    a.num_sms = num_sms();
+    if (a.num_sms <= 0) return CPR_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorInvalidValue;
 #define CPR_DISPATCH(DK, DV, CC)                                                                  \
@@ -234,7 +250,7 @@ int32_t cpr_gdn_set_profile_events(void* const* events, int32_t n_events)
         g_profile_n = 0;
         return CPR_OK;
     }
-    if (n_events < 5 || n_events > kMaxProfileEvents) return CPR_ERR_INVALID_ARG;
+    if (n_events < 4 || n_events > kMaxProfileEvents) return CPR_ERR_INVALID_ARG;
     for (int32_t i = 0; i < n_events; ++i) {
         if (!events[i]) return CPR_ERR_INVALID_ARG;
         g_profile_events[i] = static_cast<cudaEvent_t>(events[i]);

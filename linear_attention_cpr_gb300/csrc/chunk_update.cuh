@@ -60,16 +60,11 @@ __device__ __forceinline__ bool chunk_decays_and_A(const PrepSmem<DK, C>& s, uns
     __syncthreads();
     for (int idx = tid; idx < C * (DK / 8); idx += DK + DV) {
         const int r = idx % C, c0 = (idx / C) * 8;
-        uint16_t hi[8], lo[8];
+        float xs[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) tc::split_bf16(s.kf[r * KS + c0 + e], hi[e], lo[e]);
+        for (int e = 0; e < 8; ++e) xs[e] = s.kf[r * KS + c0 + e];
         const uint32_t off = tc::tile_off<2>(r, c0, DK);
-        *reinterpret_cast<uint4*>(ktile + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
-                                                            hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
-        if (KC::NSPLIT == 2)
-            *reinterpret_cast<uint4*>(ktile + KC::SPLIT + off) =
-                make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
-                           lo[6] | (uint32_t)lo[7] << 16);
+        tc::split8_store(xs, ktile + off, KC::NSPLIT == 2 ? ktile + KC::SPLIT + off : nullptr);
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
@@ -150,11 +145,11 @@ __device__ __forceinline__ void chunk_column(const PrepSmem<DK, C>& s, int col, 
 //   prep (state independent), two tcgen05 products with K = C:
 //        X = (D K)^T W   (M = 128 rows c, N = DK)   ->  Mt = gamma I - X   (Mt[c][c'] = M[c'][c])
 //        B = U~^T (D K)  (M = 128 rows i, N = DK)
-//        bf16 hi/lo splits of every operand, three products hi*hi + hi*lo + lo*hi
-//        accumulated in fp32 in TMEM; Mt is split into bf16 hi/lo (the chain's B operand
-//        image), B kept fp32 [DV][DK].
-//   chain step: D = S_b M as one tcgen05 product (M = 128 rows i, N = DK, K = DK), the
-//        state tile holding S_b's bf16 splits, three products as above; then
+//        bf16 hi/lo splits of every operand (tc::split_f32), three products
+//        hi*hi + hi*lo + lo*hi accumulated in fp32 in TMEM; Mt is split the same way
+//        (the chain's B operand image), B kept fp32 [DV][DK].
+//   chain step: D = S_b M as tcgen05 products per 64 value rows (M = 64, N = DK,
+//        K = DK), the state tile holding S_b's bf16 splits, three products as above; then
 //        S_new[i][c] = D[i][c] + B[i][c] (one add).
 // Both products have a fixed instruction sequence, so prefill's kernels and decode's
 // resync produce the same bits.  Rows beyond DK (or DV) of the M = 128 products are zero.
@@ -211,18 +206,11 @@ __device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned
     for (int row = tid; row < U::MPAD; row += nt) {
 #pragma unroll
         for (int r0 = 0; r0 < C; r0 += 8) {
-            uint16_t hi[8], lo[8];
+            float xs[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float x = row < DK ? __fmul_rn(s.dvs[r0 + e], s.kf[(r0 + e) * KS + row]) : 0.0f;
-                tc::split_bf16(x, hi[e], lo[e]);
-            }
+            for (int e = 0; e < 8; ++e) xs[e] = row < DK ? __fmul_rn(s.dvs[r0 + e], s.kf[(r0 + e) * KS + row]) : 0.0f;
             const uint32_t off = tc::tile_off<2>(row, r0, C);
-            *reinterpret_cast<uint4*>(aop + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
-                                                              hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
-            *reinterpret_cast<uint4*>(aop + U::AOP_SPLIT + off) =
-                make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
-                           lo[6] | (uint32_t)lo[7] << 16);
+            tc::split8_store(xs, aop + off, aop + U::AOP_SPLIT + off);
         }
     }
     float x[C];
@@ -230,15 +218,8 @@ __device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned
     __syncthreads();  // keys and A are dead: their space becomes the [W | U~]^T operand
 #pragma unroll
     for (int r0 = 0; r0 < C; r0 += 8) {
-        uint16_t hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) tc::split_bf16(x[r0 + e], hi[e], lo[e]);
         const uint32_t off = tc::tile_off<2>(tid, r0, C);
-        *reinterpret_cast<uint4*>(bop + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
-                                                          hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
-        *reinterpret_cast<uint4*>(bop + U::BOP_SPLIT + off) =
-            make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
-                       lo[6] | (uint32_t)lo[7] << 16);
+        tc::split8_store(*reinterpret_cast<const float(*)[8]>(x + r0), bop + off, bop + U::BOP_SPLIT + off);
     }
     tc::fence_proxy_async();
     __syncthreads();
@@ -303,20 +284,14 @@ __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsign
                     const int col0 = g * 32;
 #pragma unroll
                     for (int e8 = 0; e8 < 32; e8 += 8) {
-                        uint16_t hi[8], lo[8];
+                        float xs[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int cc = col0 + e8 + e;
-                            const float m = (cc == row) ? __fsub_rn(gamma, v[e8 + e]) : -v[e8 + e];
-                            tc::split_bf16(m, hi[e], lo[e]);
+                            xs[e] = (cc == row) ? __fsub_rn(gamma, v[e8 + e]) : -v[e8 + e];
                         }
                         const uint32_t off = tc::tile_off<2>(row, col0 + e8, DK);
-                        *reinterpret_cast<uint4*>(mt_dst + off) =
-                            make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
-                                       hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
-                        *reinterpret_cast<uint4*>(mt_dst + U::MT_SPLIT + off) =
-                            make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16,
-                                       lo[4] | (uint32_t)lo[5] << 16, lo[6] | (uint32_t)lo[7] << 16);
+                        tc::split8_store(xs, mt_dst + off, mt_dst + U::MT_SPLIT + off);
                     }
                 } else {  // B[i][c], row i = this lane; chunk j of the row stored at j ^ (i % 8)
                     if (row >= DV) continue;
@@ -361,18 +336,11 @@ __device__ __forceinline__ void stile_fill(unsigned char* stile, const float* sr
     constexpr uint32_t SPLIT = kChainRows * DK * 2;
     for (int idx = tid; idx < kChainRows * (DK / 8); idx += nthreads) {
         const int r = idx % kChainRows, c0 = (idx / kChainRows) * 8, i = row0 + r;
-        uint16_t hi[8], lo[8];
+        float xs[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float x = (src && i < DV) ? src[(size_t)(c0 + e) * DV + i] : 0.0f;
-            tc::split_bf16(x, hi[e], lo[e]);
-        }
+        for (int e = 0; e < 8; ++e) xs[e] = (src && i < DV) ? src[(size_t)(c0 + e) * DV + i] : 0.0f;
         const uint32_t off = tc::tile_off<2>(r, c0, DK);
-        *reinterpret_cast<uint4*>(stile + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
-                                                            hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
-        *reinterpret_cast<uint4*>(stile + SPLIT + off) =
-            make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
-                       lo[6] | (uint32_t)lo[7] << 16);
+        tc::split8_store(xs, stile + off, stile + SPLIT + off);
     }
 }
 
@@ -437,6 +405,39 @@ __device__ __forceinline__ void chain_values(uint32_t tmem_col, const float* bsl
     }
 }
 
+// This thread's B values of a slice (row ChainMap::row(), columns col0() ..) read from
+// global memory: bt is a chunk's B (fp32 [DV][DK], 16-byte chunks of row i swizzled by
+// i % 8 as prep_epilogue writes them); rows beyond DV get zeros (never stored).
+template <int DK, int DV, int WPQ>
+__device__ __forceinline__ void chain_load_b(const float* __restrict__ bt, int row0,
+                                             float (&b)[ChainMap<DK, WPQ>::CPT])
+{
+    using Mp = ChainMap<DK, WPQ>;
+    const int r = Mp::row(), c0 = Mp::col0(), i = row0 + r;
+#pragma unroll
+    for (int k = 0; k < Mp::CPT / 4; ++k) {
+        const float4 x = i < DV ? __ldg(reinterpret_cast<const float4*>(bt + (size_t)i * DK) + ((c0 / 4 + k) ^ (r & 7)))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        b[4 * k] = x.x;
+        b[4 * k + 1] = x.y;
+        b[4 * k + 2] = x.z;
+        b[4 * k + 3] = x.w;
+    }
+}
+
+// S_new = D + B for this thread's values, B already in registers (as chain_values).
+template <int DK, int WPQ>
+__device__ __forceinline__ void chain_values_reg(uint32_t tmem_col, const float (&b)[ChainMap<DK, WPQ>::CPT],
+                                                 float (&v)[ChainMap<DK, WPQ>::CPT])
+{
+    using Mp = ChainMap<DK, WPQ>;
+    const int warp = threadIdx.x >> 5;
+    const int q = warp & 3, h = warp >> 2;
+    tc::tmem_ld_16x2<Mp::CPT>(tmem_col + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * Mp::CPW), v);
+#pragma unroll
+    for (int e = 0; e < Mp::CPT; ++e) v[e] = __fadd_rn(v[e], b[e]);
+}
+
 // Split this thread's values into the S tile (A operand of the next chain product).
 template <int DK, int WPQ>
 __device__ __forceinline__ void chain_refill(unsigned char* stile, const float (&v)[ChainMap<DK, WPQ>::CPT])
@@ -446,15 +447,8 @@ __device__ __forceinline__ void chain_refill(unsigned char* stile, const float (
     const int r = Mp::row(), c0 = Mp::col0();
 #pragma unroll
     for (int e8 = 0; e8 < Mp::CPT; e8 += 8) {
-        uint16_t hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) tc::split_bf16(v[e8 + e], hi[e], lo[e]);
         const uint32_t off = tc::tile_off<2>(r, c0 + e8, DK);
-        *reinterpret_cast<uint4*>(stile + off) = make_uint4(hi[0] | (uint32_t)hi[1] << 16, hi[2] | (uint32_t)hi[3] << 16,
-                                                            hi[4] | (uint32_t)hi[5] << 16, hi[6] | (uint32_t)hi[7] << 16);
-        *reinterpret_cast<uint4*>(stile + S_SPLIT + off) =
-            make_uint4(lo[0] | (uint32_t)lo[1] << 16, lo[2] | (uint32_t)lo[3] << 16, lo[4] | (uint32_t)lo[5] << 16,
-                       lo[6] | (uint32_t)lo[7] << 16);
+        tc::split8_store(*reinterpret_cast<const float(*)[8]>(v + e8), stile + off, stile + S_SPLIT + off);
     }
 }
 

@@ -32,7 +32,8 @@
 //   U~_r[n] = beta_r * v_r[n],          then fma(-A_ri, U~_i[n], .) for i = 0 .. r-1
 //   then, in matrix form with D = diag(d_r) (chunk_update.cuh):
 //   M^T = gamma I - (D K)^T W,  B = U~^T (D K):  tcgen05 products (M = 128, N = dk,
-//         K = C) of bf16 hi/lo splits, hi*hi + hi*lo + lo*hi, fp32 accumulation
+//         K = C) of bf16 hi/lo splits (Dekker's splitting, tc.cuh), hi*hi + hi*lo +
+//         lo*hi, fp32 accumulation
 //   S_new = S_b M + B:  per 64 value rows, a tcgen05 product of S_b's splits with M's
 //         (M = 64, N = dk, K = dk, the same three products), then one fp32 add of B
 #pragma once

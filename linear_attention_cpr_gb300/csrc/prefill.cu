@@ -3,17 +3,19 @@
 // "SkyRL IsoExec: vLLM 与 Megatron 的 logprob 差 ...", section "Gated DeltaNet 的第三条路：
 // chunkwise-parallel recurrent": training and prefill first compute the recurrent
 // state at each chunk boundary, then a parallel recurrent scan produces the outputs
-// inside each chunk.  Four kernels, all on the caller's stream:
+// inside each chunk.  Three kernels, all on the caller's stream:
 //   k0_chunk_index   cu_chunks[n] = sum_{m<n} ceil(L_m / C), with device-side checks
 //   k1_chunk_prep    the state-independent half of U for every full chunk (parallel):
 //                    G, decays, A, and W, U~ by forward substitution
-//   k2_chain         the state-dependent half of U, sequential over each sequence's
-//                    chunks, one CTA per (sequence, head, slice of value rows): writes
-//                    every boundary state (and state_out when L is a multiple of C)
-//   k3_intra_chunk   the token recurrence inside every chunk from its boundary state,
-//                    one CTA per (chunk, head), one thread per value row holding that
-//                    row of the state in registers; writes o (and state_out for a
-//                    final partial chunk)
+//   k23_chain_and_intra  one cooperative launch with two roles:
+//                    chain CTAs: the state-dependent half of U, sequential over each
+//                    sequence's chunks, one CTA per (sequence, head, slice of value rows)
+//                    at a time: every boundary state (and state_out when L is a multiple
+//                    of C), each published as soon as it is stored;
+//                    item groups: the token recurrence inside every chunk from its
+//                    boundary state, one group of DV threads per (chunk, head), one thread
+//                    per two value rows holding them in registers; writes o (and
+//                    state_out for a final partial chunk)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -154,373 +156,452 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
 }
 
 // ------------------------------------------------------------------------------------
-// k2: boundary chain.  One CTA per (sequence, head, slice of 64 value rows), 9 warps.
-// Warp 8 is the producer: it bulk-copies each chunk's M^T image and the slice's rows of
-// B into one of two shared-memory stages one chunk ahead and issues the tcgen05 chain
-// product.  Warps 0-7 are the epilogue: they read the accumulator, add B, refill the
-// bf16-split state tile (A operand of the next product) and signal the producer, then
-// store the boundary state while the next product runs.  All hand-offs go through
-// mbarriers with bounded waits.  Slices are independent: each value row evolves alone.
+// Hand-off between the chain CTAs and the intra-chunk items of one launch.
+// ready[c * H + h] counts the slices of chunk c's boundary state (head h) that are
+// stored; a chain CTA's threads fence their stores, meet at a barrier, and one thread
+// adds 1.  All CTAs of the launch are resident (cooperative launch) and chain CTAs wait
+// on nothing but their own copies and products, so every wait below ends; it is still
+// bounded (about 4 s) and reports a timeout instead of hanging.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void named_bar(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ int wait_published(const uint32_t* flag, uint32_t target)
+{
+    if (ld_acquire(flag) >= target) return 1;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        __nanosleep(128);
+        if (ld_acquire(flag) >= target) return 1;
+        if (global_ns() - t0 > 4000000000ull) break;
+    }
+    return 0;
+}
+
+// ------------------------------------------------------------------------------------
+// Boundary chain of one (sequence, head, slice of 64 value rows), by a CTA of 8 warps.
+// Each step, the epilogue warps read the accumulator, add B (loaded from global memory
+// into registers one chunk ahead), refill the bf16-split state tile (A operand of the
+// next product) and arrive on an mbarrier; lane 0 of warp 7 is also the producer: it bulk-copies each chunk's M^T image into one
+// of three shared-memory stages two chunks ahead and issues the tcgen05 chain product
+// once every epilogue thread has arrived.  The boundary state is stored while the next
+// product runs and published for the intra-chunk items one step later (so that the
+// publishing fence waits for nothing).  All waits are bounded; a timeout is reported in
+// the status word.  Slices are independent: each value row evolves alone.  A chain CTA
+// runs its chains one after another; its mbarrier phases continue across them.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV>
 struct K2Cfg {
     static constexpr int ROWS = DV < kChainRows ? DV : kChainRows;  // value rows of one slice
     static constexpr int NSLICE = (DV + kChainRows - 1) / kChainRows;
     static constexpr uint32_t MT_BYTES = 2 * DK * DK * 2;
-    static constexpr uint32_t B_BYTES = ROWS * DK * 4;
-    static constexpr uint32_t STAGE = MT_BYTES + B_BYTES;
+    static constexpr int NSTAGE = 3;  // M^T images in flight: the one in use and two ahead
+    static constexpr uint32_t STAGE = MT_BYTES;
     static constexpr uint32_t S_BYTES = 2 * kChainRows * DK * 2;
-    static constexpr uint32_t S_OFF = 2 * STAGE, BAR_OFF = S_OFF + S_BYTES;
+    static constexpr uint32_t S_OFF = NSTAGE * STAGE, BAR_OFF = S_OFF + S_BYTES;
     static constexpr uint32_t bytes = BAR_OFF + 64;
     static constexpr uint32_t TMEM_COLS = DK <= 32 ? 32 : DK <= 64 ? 64 : 128;
     static constexpr uint32_t PIECE = 16384;
-    static constexpr int THREADS = 9 * 32;
-    static constexpr int EPI = 256;  // epilogue threads (warps 0-7)
+    static constexpr int THREADS = 256;
+    static constexpr int WPQ = 2;                 // epilogue warps per TMEM lane quadrant
+    static constexpr int EPI = 4 * WPQ * 32;      // epilogue threads
 };
 
+// Publish one slice of a boundary state: the CTA's stores to it were issued before a
+// barrier this thread has passed; the fence orders them before the count.
+__device__ __forceinline__ void publish(uint32_t* flag)
+{
+    __threadfence();
+    atomicAdd(flag, 1u);
+}
+
 template <int DK, int DV, int C, typename T>
-__global__ void __launch_bounds__(K2Cfg<DK, DV>::THREADS) k2_chain(PrefillArgs a)
+__device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* sm2, int cta, int ncta)
 {
     using Cf = K2Cfg<DK, DV>;
-    using Mp = ChainMap<DK, 2>;
-    extern __shared__ __align__(1024) unsigned char sm2[];
+    using Mp = ChainMap<DK, Cf::WPQ>;
     unsigned char* stile = sm2 + Cf::S_OFF;
-    uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(sm2 + Cf::BAR_OFF);  // [2] stage landed
-    uint64_t* mbar_mma = mbar_ld + 2;                                    // product done
-    uint64_t* mbar_tile = mbar_ld + 3;                                   // state tile ready (256 arrivals)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_ld + 4);
-    int* fail = reinterpret_cast<int*>(tslot + 1);
+    uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(sm2 + Cf::BAR_OFF);  // [NSTAGE] stage landed
+    uint64_t* mbar_mma = mbar_ld + Cf::NSTAGE;                           // product done
+    uint64_t* mbar_tile = mbar_mma + 1;                                  // state tile ready (EPI arrivals)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_tile + 1);
+    volatile int* mma_ok = reinterpret_cast<volatile int*>(tslot + 1);  // thread 0's wait result
 
     const int H = a.H, tid = threadIdx.x, warp = tid >> 5;
-    const int sl = blockIdx.x % Cf::NSLICE, nh_idx = blockIdx.x / Cf::NSLICE;
-    const int n = nh_idx / H, h = nh_idx % H, row0 = sl * kChainRows;
-    if (*a.status) return;
-    const int64_t t0 = a.cu_seqlens[n];
-    const int64_t L = a.cu_seqlens[n + 1] - t0;
-    const int64_t nfull = L / C, nch = a.cu_chunks[n + 1] - a.cu_chunks[n], cbase = a.cu_chunks[n];
-    const size_t SS = (size_t)DK * DV, nh = (size_t)n * H + h;
-    const float* s_in = a.state_in ? a.state_in + nh * SS : nullptr;
-
-    // this slice's columns of the stored states: element (c, row0 + r)
-    auto copy_slice = [&](float* dst) {
-        for (int idx = tid; idx < DK * Cf::ROWS; idx += blockDim.x) {
-            const int c = idx / Cf::ROWS, r = idx % Cf::ROWS;
-            dst[(size_t)c * DV + row0 + r] = s_in ? s_in[(size_t)c * DV + row0 + r] : 0.0f;
-        }
-    };
-    if (L == 0) {  // empty sequence: state_out = state_in
-        copy_slice(a.state_out + nh * SS);
-        return;
-    }
-    copy_slice(a.boundary + ((size_t)cbase * H + h) * SS);
-    if (nfull == 0) return;
-
+    const bool producer = (tid == Cf::THREADS - 32);
+    const bool epi = tid < Cf::EPI;
+    const size_t SS = (size_t)DK * DV;
     if (warp == 0) tc::tmem_alloc(tslot, Cf::TMEM_COLS);
     if (tid == 0) {
-        tc::mbar_init(&mbar_ld[0], 1);
-        tc::mbar_init(&mbar_ld[1], 1);
+        for (int b = 0; b < Cf::NSTAGE; ++b) tc::mbar_init(&mbar_ld[b], 1);
         tc::mbar_init(mbar_mma, 1);
         tc::mbar_init(mbar_tile, Cf::EPI);
         tc::fence_mbar_init();
-        *fail = 0;
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
 
-    if (warp == 8) {  // ----- producer -----
-        if ((tid & 31) == 0) {
-            auto issue_load = [&](int64_t jc, int b) {
-                const size_t ch = (size_t)(cbase + jc) * H + h;
-                const unsigned char* src = a.mt + ch * Cf::MT_BYTES;
-                unsigned char* dst = sm2 + b * Cf::STAGE;
-                tc::mbar_arrive_expect_tx(&mbar_ld[b], Cf::STAGE);
-                for (uint32_t off = 0; off < Cf::MT_BYTES; off += Cf::PIECE)
-                    tc::bulk_g2s(dst + off, src + off, min(Cf::PIECE, Cf::MT_BYTES - off), &mbar_ld[b]);
-                const unsigned char* bsrc = reinterpret_cast<const unsigned char*>(a.bt + ch * SS + (size_t)row0 * DK);
-                for (uint32_t off = 0; off < Cf::B_BYTES; off += Cf::PIECE)
-                    tc::bulk_g2s(dst + Cf::MT_BYTES + off, bsrc + off, min(Cf::PIECE, Cf::B_BYTES - off), &mbar_ld[b]);
-            };
-            int64_t issued = 0;
-            issue_load(0, 0);
-            issued = 1;
-            for (int64_t jc = 0; jc < nfull; ++jc) {
-                if (!tc::mbar_wait(mbar_tile, (uint32_t)(jc & 1))) { *fail = 1; break; }
-                if (jc + 1 < nfull) {  // that stage's last readers (product jc-1, epilogue jc-1) are done
-                    issue_load(jc + 1, (int)((jc + 1) & 1));
-                    issued = jc + 2;
-                }
-                if (!tc::mbar_wait(&mbar_ld[jc & 1], (uint32_t)((jc >> 1) & 1))) { *fail = 1; break; }
-                chain_mma<DK>(tmem, stile, sm2 + (jc & 1) * Cf::STAGE, mbar_mma);
+    int64_t G = 0;  // chain steps this CTA has run: the phase count of its mbarriers
+    bool failed = false;
+    const int nchains = a.n_seqs * H * Cf::NSLICE;
+    for (int ci = cta; ci < nchains && !failed; ci += ncta) {
+        const int sl = ci % Cf::NSLICE, nh_idx = ci / Cf::NSLICE;
+        const int n = nh_idx / H, h = nh_idx % H, row0 = sl * kChainRows;
+        const int64_t t0 = a.cu_seqlens[n];
+        const int64_t L = a.cu_seqlens[n + 1] - t0;
+        const int64_t nfull = L / C, nch = a.cu_chunks[n + 1] - a.cu_chunks[n], cbase = a.cu_chunks[n];
+        const size_t nh = (size_t)n * H + h;
+        const float* s_in = a.state_in ? a.state_in + nh * SS : nullptr;
+        uint32_t* ready = a.ready + (size_t)cbase * H + h;  // + jc * H for chunk cbase + jc
+
+        // this slice's columns of the stored states: element (c, row0 + r)
+        auto copy_slice = [&](float* dst) {
+            for (int idx = tid; idx < DK * Cf::ROWS; idx += Cf::THREADS) {
+                const int c = idx / Cf::ROWS, r = idx % Cf::ROWS;
+                dst[(size_t)c * DV + row0 + r] = s_in ? s_in[(size_t)c * DV + row0 + r] : 0.0f;
             }
-            if (*fail) {  // let copies still in flight land before the CTA exits
-                for (int64_t jc = 0; jc < issued; ++jc) tc::mbar_wait(&mbar_ld[jc & 1], (uint32_t)((jc >> 1) & 1), 1u << 16);
-            }
+        };
+        if (L == 0) {  // empty sequence: state_out = state_in
+            copy_slice(a.state_out + nh * SS);
+            continue;
         }
-    } else {  // ----- epilogue warps 0-7 -----
-        stile_fill<DK, DV>(stile, s_in, row0, tid, Cf::EPI);
+        copy_slice(a.boundary + ((size_t)cbase * H + h) * SS);
+        __syncthreads();
+        if (tid == 0) publish(ready);
+        if (nfull == 0) continue;
+
+        // producer (one thread): M^T stage loads and the chain products
+        int64_t issued = 0;
+        auto issue_load = [&](int64_t jc) {
+            const size_t ch = (size_t)(cbase + jc) * H + h;
+            const unsigned char* src = a.mt + ch * Cf::MT_BYTES;
+            const int b = (int)((G + jc) % Cf::NSTAGE);
+            unsigned char* dst = sm2 + b * Cf::STAGE;
+            tc::mbar_arrive_expect_tx(&mbar_ld[b], Cf::STAGE);
+            for (uint32_t off = 0; off < Cf::MT_BYTES; off += Cf::PIECE)
+                tc::bulk_g2s(dst + off, src + off, min(Cf::PIECE, Cf::MT_BYTES - off), &mbar_ld[b]);
+        };
+        auto ld_parity = [&](int64_t jc) { return (uint32_t)(((G + jc) / Cf::NSTAGE) & 1); };
+        auto produce = [&](int64_t jc) -> bool {  // step jc's product, once its state tile is written
+            if (!tc::mbar_wait(mbar_tile, (uint32_t)((G + jc) & 1))) return false;
+            if (!tc::mbar_wait(&mbar_ld[(G + jc) % Cf::NSTAGE], ld_parity(jc))) return false;
+            chain_mma<DK>(tmem, stile, sm2 + ((G + jc) % Cf::NSTAGE) * Cf::STAGE, mbar_mma);
+            if (issued < nfull) issue_load(issued++);  // product jc-1 is done: its stage is free
+            return true;
+        };
+
+        bool pfail = false;
+        stile_fill<DK, DV>(stile, s_in, row0, tid, Cf::THREADS);
         tc::fence_proxy_async();
         tc::fence_before_sync();
-        tc::mbar_arrive(mbar_tile);
-        for (int64_t jc = 0; jc < nfull; ++jc) {
-            const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(mbar_mma, (uint32_t)(jc & 1)));
-            if (!ok) { *fail = 1; break; }
-            tc::fence_after_sync();
-            float v[Mp::CPT];
-            chain_values<DK, DV, 2>(tmem, reinterpret_cast<const float*>(sm2 + (jc & 1) * Cf::STAGE + Cf::MT_BYTES), row0, v);
-            if (jc + 1 < nfull) {
-                chain_refill<DK, 2>(stile, v);
-                tc::fence_proxy_async();
-            }
-            tc::fence_before_sync();
-            if (jc + 1 < nfull) tc::mbar_arrive(mbar_tile);
-            float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS : a.state_out + nh * SS;
-            chain_store<DK, DV, 2>(dst, row0, v);
+        float bv[Mp::CPT];
+        if (epi) {
+            tc::mbar_arrive(mbar_tile);
+            chain_load_b<DK, DV, Cf::WPQ>(a.bt + ((size_t)cbase * H + h) * SS, row0, bv);
         }
+        if (producer) {
+            for (; issued < Cf::NSTAGE - 1 && issued < nfull; ++issued) issue_load(issued);
+            pfail = !produce(0);
+        }
+        __syncwarp();
+        for (int64_t jc = 0; jc < nfull; ++jc) {
+            bool ok = !pfail;
+            if (epi) {
+                // one thread polls the product's mbarrier, the epilogue meets it at a hardware
+                // barrier (polling by every warp would compete with the product for shared memory)
+                if (tid == 0) *mma_ok = tc::mbar_wait(mbar_mma, (uint32_t)((G + jc) & 1)) ? 1 : 0;
+                named_bar(1, Cf::EPI);
+                ok = ok && *mma_ok != 0;
+                if (*mma_ok) {
+                    tc::fence_after_sync();
+                    float v[Mp::CPT];
+                    chain_values_reg<DK, Cf::WPQ>(tmem, bv, v);
+                    if (jc + 1 < nfull) {
+                        chain_refill<DK, Cf::WPQ>(stile, v);
+                        tc::fence_proxy_async();
+                    }
+                    tc::fence_before_sync();
+                    if (jc + 1 < nfull) tc::mbar_arrive(mbar_tile);
+                    // the boundary state completed one step ago: every store to it was issued
+                    // before the last barrier (published before this thread's next loads, which
+                    // the fence would otherwise wait for)
+                    if (tid == 0 && jc >= 1) publish(ready + (size_t)jc * H);
+                    if (jc + 1 < nfull) {
+                        // the producer issues the next product before its own loads and stores
+                        if (producer) pfail = !produce(jc + 1);
+                        __syncwarp();
+                        chain_load_b<DK, DV, Cf::WPQ>(a.bt + ((size_t)(cbase + jc + 1) * H + h) * SS, row0, bv);
+                    }
+                    float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS
+                                                : a.state_out + nh * SS;
+                    chain_store<DK, DV, Cf::WPQ>(dst, row0, v);
+                }
+            } else if (producer && ok && jc + 1 < nfull) {  // (epilogue warps include the producer when DK >= 64)
+                pfail = !produce(jc + 1);
+            }
+            __syncwarp();
+            // one vote per step: a wait timed out somewhere (the CTA stops: its mbarrier
+            // phases are unknown) or the step's stores are all issued
+            if (__syncthreads_or(!ok || pfail)) {
+                failed = true;
+                break;
+            }
+        }
+        if (!failed && tid == 0 && nfull < nch) publish(ready + (size_t)nfull * H);
+        if (failed && producer) {  // let copies still in flight land before the CTA exits
+            for (int64_t jc = 0; jc < issued; ++jc)
+                tc::mbar_wait(&mbar_ld[(G + jc) % Cf::NSTAGE], ld_parity(jc), 1u << 16);
+        }
+        G += nfull;
     }
     __syncthreads();
-    if (*fail && tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
+    if (failed && tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
     tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(tmem, Cf::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------------------
-// k3: intra-chunk token recurrence.  One CTA per (chunk, head), DV threads.  Thread
-// (warp w, lane l) owns two value rows, i0 = 16w + (l & 15) and i1 = i0 + DV/2, over one
-// half of the key columns, h = l >> 4 (columns [h*DK/2, (h+1)*DK/2)).  It keeps them as
-// pairs (S[i][c], S[i][c + DK/4]) so that chains m and m+2 of its half advance in one
-// paired FMA; each key/query value loaded from shared memory serves both rows.  The
-// half-warps hold the two halves of the canonical tree, ((c0+c1)+(c2+c3)) and
-// ((c4+c5)+(c6+c7)), and add them after one shuffle.
+// Intra-chunk token recurrence of one (chunk, head) item, by a group of DV threads.
+// Thread i holds value row i of the state over all key columns, as pairs
+// (S[i][m L + t], S[i][(m + 4) L + t]) for m = 0..3, t = 0..L-1 (L = DK / 8), so that
+// chains m and m + 4 of the canonical dot advance in one paired FMA and the tree ends
+// inside the thread.  Every lane of a warp reads the same key / query values from shared
+// memory (broadcast loads).
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C>
 struct K3Smem {
-    // key/query rows: half 0's DK/4 pairs, 4 floats of padding, half 1's pairs, 4 floats
-    // (the padding puts the two half-warps' broadcast loads in different banks)
-    static constexpr int ROW = DK + 8;
+    static constexpr int ROW = DK;   // key / query row: pair (m, t) at float offset 2 (m L + t)
+    static constexpr int NT = DV;    // threads of a group
+    // keys and queries (fp32 pairs), values as stored (at most fp32), alpha and beta
     static constexpr size_t bytes = sizeof(float) * ((size_t)2 * C * ROW + (size_t)C * DV + 2 * C);
 };
 
+// Chain sums of the row with w: acc[m] = (chain m, chain m + 4).
 template <int DK>
-struct K3Row {
-    static constexpr int NP = DK / 4;  // pairs per row per thread (half of DK columns)
-};
-
-// Partial (this half) of the canonical dot of both rows with w (pairs of this half).
-template <int DK>
-__device__ __forceinline__ void k3_half_dot(const float2 (&S0)[DK / 4], const float2 (&S1)[DK / 4],
-                                            const float2* __restrict__ w, float& d0, float& d1)
+__device__ __forceinline__ void k3_dot(const float2 (&S)[DK / 2], const float2* __restrict__ w, float2 (&acc)[4])
 {
-    constexpr int L = DK / 8;  // pair p is chain p/L (x) and p/L + 2 (y)
-    float2 a0[2], a1[2];
+    constexpr int L = DK / 8;
 #pragma unroll
     for (int t = 0; t < L; t += 2) {
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
+        for (int m = 0; m < 4; ++m) {
             const int p = m * L + t;
             const float4 w4 = *reinterpret_cast<const float4*>(w + p);
             const float2 w0 = make_float2(w4.x, w4.y), w1 = make_float2(w4.z, w4.w);
-            const bool first = (t == 0);
-            a0[m] = first ? __fmul2_rn(S0[p], w0) : __ffma2_rn(S0[p], w0, a0[m]);
-            a1[m] = first ? __fmul2_rn(S1[p], w0) : __ffma2_rn(S1[p], w0, a1[m]);
-            a0[m] = __ffma2_rn(S0[p + 1], w1, a0[m]);
-            a1[m] = __ffma2_rn(S1[p + 1], w1, a1[m]);
+            acc[m] = (t == 0) ? __fmul2_rn(S[p], w0) : __ffma2_rn(S[p], w0, acc[m]);
+            acc[m] = __ffma2_rn(S[p + 1], w1, acc[m]);
         }
     }
-    // chains (c0, c2) in a[0] and (c1, c3) in a[1]: (c0 + c1) + (c2 + c3)
-    const float2 s0 = __fadd2_rn(a0[0], a0[1]), s1 = __fadd2_rn(a1[0], a1[1]);
-    d0 = __fadd_rn(s0.x, s0.y);
-    d1 = __fadd_rn(s1.x, s1.y);
 }
 
+// One token: S <- alpha S + u k^T, then the chain sums of S q (and of S k_next).
 template <int DK, bool NEXT>
-__device__ __forceinline__ void k3_token(float2 (&S0)[DK / 4], float2 (&S1)[DK / 4], const float2* __restrict__ kr,
+__device__ __forceinline__ void k3_token(float2 (&S)[DK / 2], const float2* __restrict__ kr,
                                          const float2* __restrict__ qr, const float2* __restrict__ kn, float alpha,
-                                         float u0, float u1, float& o0, float& o1, float& x0, float& x1)
+                                         float u, float2 (&o)[4], float2 (&x)[4])
 {
-    constexpr int L = DK / 8;  // pairs [0, L) carry chains (0, 2); pairs [L, 2L) chains (1, 3)
-    const float2 a2 = make_float2(alpha, alpha), u02 = make_float2(u0, u0), u12 = make_float2(u1, u1);
-    float2 co0[2], co1[2], cx0[2], cx1[2];
+    constexpr int L = DK / 8;
+    const float2 a2 = make_float2(alpha, alpha), u2 = make_float2(u, u);
 #pragma unroll
     for (int t = 0; t < L; t += 2) {
         const bool first = (t == 0);
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {  // both chain blocks in one pass: 8 independent chains in flight
+        for (int m = 0; m < 4; ++m) {
             const int p = m * L + t;
             const float4 k4 = *reinterpret_cast<const float4*>(kr + p);
             const float4 q4 = *reinterpret_cast<const float4*>(qr + p);
-            const float2 k0 = make_float2(k4.x, k4.y), k1 = make_float2(k4.z, k4.w);
-            const float2 q0 = make_float2(q4.x, q4.y), q1 = make_float2(q4.z, q4.w);
-            const float2 s00 = __ffma2_rn(u02, k0, __fmul2_rn(a2, S0[p]));
-            const float2 s10 = __ffma2_rn(u12, k0, __fmul2_rn(a2, S1[p]));
-            const float2 s01 = __ffma2_rn(u02, k1, __fmul2_rn(a2, S0[p + 1]));
-            const float2 s11 = __ffma2_rn(u12, k1, __fmul2_rn(a2, S1[p + 1]));
-            S0[p] = s00;
-            S1[p] = s10;
-            S0[p + 1] = s01;
-            S1[p + 1] = s11;
-            co0[m] = first ? __fmul2_rn(s00, q0) : __ffma2_rn(s00, q0, co0[m]);
-            co1[m] = first ? __fmul2_rn(s10, q0) : __ffma2_rn(s10, q0, co1[m]);
+            const float2 s0 = __ffma2_rn(u2, make_float2(k4.x, k4.y), __fmul2_rn(a2, S[p]));
+            const float2 s1 = __ffma2_rn(u2, make_float2(k4.z, k4.w), __fmul2_rn(a2, S[p + 1]));
+            S[p] = s0;
+            S[p + 1] = s1;
+            o[m] = first ? __fmul2_rn(s0, make_float2(q4.x, q4.y)) : __ffma2_rn(s0, make_float2(q4.x, q4.y), o[m]);
+            o[m] = __ffma2_rn(s1, make_float2(q4.z, q4.w), o[m]);
             if (NEXT) {
                 const float4 n4 = *reinterpret_cast<const float4*>(kn + p);
-                const float2 n0 = make_float2(n4.x, n4.y), n1 = make_float2(n4.z, n4.w);
-                cx0[m] = first ? __fmul2_rn(s00, n0) : __ffma2_rn(s00, n0, cx0[m]);
-                cx1[m] = first ? __fmul2_rn(s10, n0) : __ffma2_rn(s10, n0, cx1[m]);
-                cx0[m] = __ffma2_rn(s01, n1, cx0[m]);
-                cx1[m] = __ffma2_rn(s11, n1, cx1[m]);
+                x[m] = first ? __fmul2_rn(s0, make_float2(n4.x, n4.y)) : __ffma2_rn(s0, make_float2(n4.x, n4.y), x[m]);
+                x[m] = __ffma2_rn(s1, make_float2(n4.z, n4.w), x[m]);
             }
-            co0[m] = __ffma2_rn(s01, q1, co0[m]);
-            co1[m] = __ffma2_rn(s11, q1, co1[m]);
         }
     }
-    {
-        const float2 t0 = __fadd2_rn(co0[0], co0[1]), t1 = __fadd2_rn(co1[0], co1[1]);
-        o0 = __fadd_rn(t0.x, t0.y);
-        o1 = __fadd_rn(t1.x, t1.y);
-    }
-    if (NEXT) {
-        const float2 t0 = __fadd2_rn(cx0[0], cx0[1]), t1 = __fadd2_rn(cx1[0], cx1[1]);
-        x0 = __fadd_rn(t0.x, t0.y);
-        x1 = __fadd_rn(t1.x, t1.y);
-    }
-}
-
-// Both halves end with the same value: left half + right half (the canonical tree's root).
-__device__ __forceinline__ float k3_join(float mine, int half)
-{
-    const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-    return half == 0 ? __fadd_rn(mine, other) : __fadd_rn(other, mine);
 }
 
 template <int DK, int DV, int C, typename T>
-__global__ void __launch_bounds__(DV, 2) k3_intra_chunk(PrefillArgs a)
+__device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int hd, int tid, float* sm3, int bar)
 {
     static_assert(DK % 32 == 0 && DV % 32 == 0, "DK and DV must be multiples of 32");
-    constexpr int NP = DK / 4;
-    extern __shared__ __align__(16) float sm3[];
-    // keys and queries: row r, half h, pair p at float offset r*ROW + h*(DK/2 + 4) + 2p,
-    // holding (x[h*DK/2 + p], x[h*DK/2 + p + DK/4])
-    constexpr int ROW = K3Smem<DK, DV, C>::ROW;
-    float* kp = sm3;                    // [C][ROW]
-    float* qp = kp + C * ROW;           // [C][ROW]
-    float* vs = qp + C * ROW;           // [C][DV]
-    float* al = vs + C * DV;                                 // [C]
-    float* bt = al + C;                                      // [C]
+    using S3 = K3Smem<DK, DV, C>;
+    constexpr int NT = S3::NT, L = DK / 8, ROW = S3::ROW, NP = DK / 2;
+    float* kp = sm3;                                      // [C][ROW] keys as pairs
+    float* qp = kp + C * ROW;                             // [C][ROW] queries as pairs
+    T* vs = reinterpret_cast<T*>(qp + C * ROW);           // [C][DV], as stored
+    float* al = reinterpret_cast<float*>(vs + C * DV);    // [C]
+    float* bt = al + C;                                   // [C]
 
-    const int64_t c = blockIdx.x;
-    const int hd = blockIdx.y, tid = threadIdx.x, H = a.H;
-    if (c >= a.cu_chunks[a.n_seqs]) return;
+    const int H = a.H;
     const int n = find_seq(a.cu_chunks, a.n_seqs, c);
     const int64_t j = c - a.cu_chunks[n];
-    const int64_t L = a.cu_seqlens[n + 1] - a.cu_seqlens[n];
+    const int64_t Ls = a.cu_seqlens[n + 1] - a.cu_seqlens[n];
     const int64_t t0 = a.cu_seqlens[n] + j * C;
-    const int len = (int)min((int64_t)C, L - j * C);
+    const int len = (int)min((int64_t)C, Ls - j * C);
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
     T* out = static_cast<T*>(a.out);
 
-    // stage the chunk's keys, queries (as pairs) and values: every thread issues all of
-    // its 16-byte loads first, then converts and stores them
+    // stage the chunk: values as they are (16-byte asynchronous copies, converted when
+    // used), keys and queries as fp32 pairs (loads issued a few at a time, then converted)
     {
         constexpr int VE = 16 / (int)sizeof(T);
         constexpr int KV = DK / VE, VV = DV / VE;
-        constexpr int NK = (C * KV + DV - 1) / DV, NV = (C * VV + DV - 1) / DV;
-        uint4 kr[NK], qr[NK], vr[NV];
-#pragma unroll
-        for (int s = 0; s < NK; ++s) {
-            const int idx = tid + s * DV, r = idx / KV, cc = idx % KV;
-            if (r < len) {
-                const size_t g = ((size_t)(t0 + r) * H + hd) * DK + cc * VE;
-                kr[s] = __ldg(reinterpret_cast<const uint4*>(k + g));
-                qr[s] = __ldg(reinterpret_cast<const uint4*>(q + g));
-            }
-        }
+        constexpr int NK = (C * KV + NT - 1) / NT, NV = (C * VV + NT - 1) / NT;
 #pragma unroll
         for (int s = 0; s < NV; ++s) {
-            const int idx = tid + s * DV, r = idx / VV, cc = idx % VV;
-            if (r < len) vr[s] = __ldg(reinterpret_cast<const uint4*>(v + ((size_t)(t0 + r) * H + hd) * DV + cc * VE));
+            const int idx = tid + s * NT, r = idx / VV, cc = idx % VV;
+            if (r < len) tc::cp_async16(vs + r * DV + cc * VE, v + ((size_t)(t0 + r) * H + hd) * DV + cc * VE);
         }
+        constexpr int P = NK < 4 ? NK : 4;  // loads in flight per pass
 #pragma unroll
-        for (int s = 0; s < NK; ++s) {
-            const int idx = tid + s * DV, r = idx / KV, cc = idx % KV;
-            if (r < len) {
-                const T* ke = reinterpret_cast<const T*>(&kr[s]);
-                const T* qe = reinterpret_cast<const T*>(&qr[s]);
+        for (int s0 = 0; s0 < NK; s0 += P) {
+            uint4 kr[P], qr[P];
 #pragma unroll
-                for (int e = 0; e < VE; ++e) {
-                    const int jj = cc * VE + e, hh = jj / (DK / 2), jl = jj % (DK / 2);
-                    const int pidx = r * ROW + hh * (DK / 2 + 4) + 2 * (jl % NP) + jl / NP;
-                    kp[pidx] = to_f32<T>(ke[e]);
-                    qp[pidx] = to_f32<T>(qe[e]);
+            for (int s = 0; s < P; ++s) {
+                const int idx = tid + (s0 + s) * NT, r = idx / KV, cc = idx % KV;
+                if (s0 + s < NK && r < len) {
+                    const size_t g = ((size_t)(t0 + r) * H + hd) * DK + cc * VE;
+                    kr[s] = __ldg(reinterpret_cast<const uint4*>(k + g));
+                    qr[s] = __ldg(reinterpret_cast<const uint4*>(q + g));
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < P; ++s) {
+                const int idx = tid + (s0 + s) * NT, r = idx / KV, cc = idx % KV;
+                if (s0 + s < NK && r < len) {
+                    const T* ke = reinterpret_cast<const T*>(&kr[s]);
+                    const T* qe = reinterpret_cast<const T*>(&qr[s]);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) {
+                        // column jj: chain block b = jj / L, entry t = jj % L -> pair (b % 4, t), slot b / 4
+                        const int jj = cc * VE + e, blk = jj / L, t = jj % L;
+                        const int pidx = r * ROW + 2 * ((blk & 3) * L + t) + (blk >> 2);
+                        kp[pidx] = to_f32<T>(ke[e]);
+                        qp[pidx] = to_f32<T>(qe[e]);
+                    }
                 }
             }
         }
-#pragma unroll
-        for (int s = 0; s < NV; ++s) {
-            const int idx = tid + s * DV, r = idx / VV, cc = idx % VV;
-            if (r < len) {
-                const T* ve = reinterpret_cast<const T*>(&vr[s]);
-#pragma unroll
-                for (int e = 0; e < VE; ++e) vs[r * DV + cc * VE + e] = to_f32<T>(ve[e]);
-            }
-        }
+        tc::cp_async_wait_all();
     }
     if (tid < len) {
         al[tid] = decay_exp(a.g[(t0 + tid) * H + hd]);
         bt[tid] = a.beta[(t0 + tid) * H + hd];
     }
-    const int w = tid >> 5, lane = tid & 31, half = lane >> 4;
-    const int i0 = w * 16 + (lane & 15), i1 = i0 + DV / 2;
-    // the chunk's boundary state: rows i0, i1 over this half's columns
-    float2 S0[NP], S1[NP];
-    {
-        const float* bsrc = a.boundary + ((size_t)c * H + hd) * DK * DV + (size_t)(half * (DK / 2)) * DV;
-#pragma unroll
-        for (int p = 0; p < NP; ++p) {
-            S0[p] = make_float2(bsrc[(size_t)p * DV + i0], bsrc[(size_t)(p + NP) * DV + i0]);
-            S1[p] = make_float2(bsrc[(size_t)p * DV + i1], bsrc[(size_t)(p + NP) * DV + i1]);
-        }
+    // the chunk's boundary state comes from the chain CTAs of this launch: wait until
+    // every slice of it is published (bounded)
+    __shared__ int wait_ok[8];
+    const int gi = bar - 1;
+    if (tid == 0) wait_ok[gi] = wait_published(a.ready + (size_t)c * H + hd, (uint32_t)K2Cfg<DK, DV>::NSLICE);
+    named_bar(bar, NT);
+    if (!wait_ok[gi]) {
+        if (tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
+        named_bar(bar, NT);
+        return;
     }
-    __syncthreads();
+    const int i = tid;  // this thread's value row
+    // the chunk's boundary state: row i over all key columns
+    float2 S[NP];
+    {
+        const float* bsrc = a.boundary + ((size_t)c * H + hd) * DK * DV + i;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int t = 0; t < L; ++t)
+                S[m * L + t] = make_float2(bsrc[(size_t)(m * L + t) * DV], bsrc[(size_t)((m + 4) * L + t) * DV]);
+    }
 
-    const float2* kph = reinterpret_cast<const float2*>(kp + half * (DK / 2 + 4));
-    const float2* qph = reinterpret_cast<const float2*>(qp + half * (DK / 2 + 4));
+    const float2* kq = reinterpret_cast<const float2*>(kp);
+    const float2* qq = reinterpret_cast<const float2*>(qp);
     constexpr int RP = ROW / 2;  // row stride in pairs
-    float x0, x1;
-    k3_half_dot<DK>(S0, S1, kph, x0, x1);
-    x0 = k3_join(x0, half);
-    x1 = k3_join(x1, half);
-    T* orow = out + ((size_t)t0 * H + hd) * DV;
+    float x;
+    {
+        float2 acc[4];
+        k3_dot<DK>(S, kq, acc);
+        x = tree8_pairs(acc[0], acc[1], acc[2], acc[3]);
+    }
+    T* orow = out + ((size_t)t0 * H + hd) * DV + i;
     for (int r = 0; r < len; ++r) {
         const float alpha = al[r], beta = bt[r];
-        const float u0 = step_u(alpha, beta, vs[r * DV + i0], x0);
-        const float u1 = step_u(alpha, beta, vs[r * DV + i1], x1);
-        float o0, o1;
-        if (r + 1 < len)
-            k3_token<DK, true>(S0, S1, kph + r * RP, qph + r * RP, kph + (r + 1) * RP, alpha, u0, u1, o0, o1, x0, x1);
-        else
-            k3_token<DK, false>(S0, S1, kph + r * RP, qph + r * RP, kph, alpha, u0, u1, o0, o1, x0, x1);
-        o0 = k3_join(o0, half);
-        o1 = k3_join(o1, half);
+        const float u = step_u(alpha, beta, to_f32<T>(vs[r * DV + i]), x);
+        float2 o[4], xn[4];
         if (r + 1 < len) {
-            x0 = k3_join(x0, half);
-            x1 = k3_join(x1, half);
+            k3_token<DK, true>(S, kq + r * RP, qq + r * RP, kq + (r + 1) * RP, alpha, u, o, xn);
+            x = tree8_pairs(xn[0], xn[1], xn[2], xn[3]);
+        } else {
+            k3_token<DK, false>(S, kq + r * RP, qq + r * RP, kq, alpha, u, o, xn);
         }
-        // both halves hold both outputs: half 0 stores row i0, half 1 row i1 (no branch)
-        orow[(size_t)r * H * DV + (half ? i1 : i0)] = from_f32<T>(half ? o1 : o0);
+        orow[(size_t)r * H * DV] = from_f32<T>(tree8_pairs(o[0], o[1], o[2], o[3]));
     }
-    if (j * C + len == L && len < C) {  // final partial chunk: the stepped state is state_out
-        float* dst = a.state_out + ((size_t)n * H + hd) * DK * DV + (size_t)(half * (DK / 2)) * DV;
+    if (j * C + len == Ls && len < C) {  // final partial chunk: the stepped state is state_out
+        float* dst = a.state_out + ((size_t)n * H + hd) * DK * DV + i;
 #pragma unroll
-        for (int p = 0; p < NP; ++p) {
-            dst[(size_t)p * DV + i0] = S0[p].x;
-            dst[(size_t)(p + NP) * DV + i0] = S0[p].y;
-            dst[(size_t)p * DV + i1] = S1[p].x;
-            dst[(size_t)(p + NP) * DV + i1] = S1[p].y;
-        }
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int t = 0; t < L; ++t) {
+                dst[(size_t)(m * L + t) * DV] = S[m * L + t].x;
+                dst[(size_t)((m + 4) * L + t) * DV] = S[m * L + t].y;
+            }
     }
+    named_bar(bar, NT);  // the group's shared memory is reused by its next item
+}
+
+// ------------------------------------------------------------------------------------
+// k23: boundary chain and intra-chunk recurrence in one cooperative launch of one CTA per
+// SM slot, 8 warps each.  CTAs [0, n_chain) run the chains (chain_role); the others run
+// the (chunk, head) items of the intra-chunk recurrence in chunk order, 256 / DV groups
+// of DV threads per CTA, each item starting as soon as its boundary state is published.  The chain's latency-bound steps thus overlap the FP32-bound items.
+// ------------------------------------------------------------------------------------
+template <int DK, int DV, int C>
+struct K23Cfg {
+    static constexpr int GROUPS = K2Cfg<DK, DV>::THREADS / K3Smem<DK, DV, C>::NT;
+    static constexpr size_t GROUP_BYTES = (K3Smem<DK, DV, C>::bytes + 1023) / 1024 * 1024;
+    static constexpr size_t bytes = K2Cfg<DK, DV>::bytes > GROUPS * GROUP_BYTES ? K2Cfg<DK, DV>::bytes : GROUPS * GROUP_BYTES;
+    static_assert(GROUPS >= 1 && GROUPS <= 8, "item groups use named barriers 1..8");
+};
+
+template <int DK, int DV, int C, typename T>
+__global__ void __launch_bounds__(K2Cfg<DK, DV>::THREADS, 1) k23_chain_and_intra(PrefillArgs a, int n_chain)
+{
+    using F = K23Cfg<DK, DV, C>;
+    constexpr int NT = K3Smem<DK, DV, C>::NT;
+    extern __shared__ __align__(1024) unsigned char sm23[];
+    if (*a.status) return;
+    if ((int)blockIdx.x < n_chain) {
+        chain_role<DK, DV, C, T>(a, sm23, blockIdx.x, n_chain);
+        return;
+    }
+    const int g = threadIdx.x / NT;
+    const int64_t items = (int64_t)a.cu_chunks[a.n_seqs] * a.H;
+    const int64_t stride = (int64_t)(gridDim.x - n_chain) * F::GROUPS;
+    float* smg = reinterpret_cast<float*>(sm23 + g * F::GROUP_BYTES);
+    for (int64_t t = (int64_t)(blockIdx.x - n_chain) * F::GROUPS + g; t < items; t += stride)
+        intra_item<DK, DV, C, T>(a, t / a.H, (int)(t % a.H), (int)threadIdx.x % NT, smg, 1 + g);
 }
 
 // ------------------------------------------------------------------------------------
@@ -544,21 +625,24 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
     profile_mark(2, s);
 
     using Cf = K2Cfg<DK, DV>;
-    e = cudaFuncSetAttribute(k2_chain<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)std::max<size_t>(Cf::bytes, tmem_cap_smem(Cf::TMEM_COLS)));
+    e = cudaMemsetAsync(a.ready, 0, sizeof(uint32_t) * (size_t)a.max_chunks * a.H, s);
     if (e != cudaSuccess) return e;
-    const size_t sm2 = std::max<size_t>(Cf::bytes, tmem_cap_smem(Cf::TMEM_COLS));
-    k2_chain<DK, DV, C, T><<<dim3((unsigned)(a.n_seqs * a.H * Cf::NSLICE)), Cf::THREADS, sm2, s>>>(a);
-    e = cudaGetLastError();
+    auto kern = k23_chain_and_intra<DK, DV, C, T>;
+    const size_t sm23 = std::max<size_t>(K23Cfg<DK, DV, C>::bytes, tmem_cap_smem(Cf::TMEM_COLS));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm23);
     if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cf::THREADS, sm23);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1 || a.num_sms < 2) return cudaErrorInvalidConfiguration;
+    const int grid = per_sm * a.num_sms;
+    const int chains = a.n_seqs * a.H * Cf::NSLICE;
+    const int n_chain = std::max(1, std::min(chains, grid / 4));
+    PrefillArgs args = a;
+    int nc = n_chain;
+    void* params[] = {&args, &nc};
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cf::THREADS), params, sm23, s);
     profile_mark(3, s);
-
-    const size_t sm3 = K3Smem<DK, DV, C>::bytes;
-    e = cudaFuncSetAttribute(k3_intra_chunk<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3);
-    if (e != cudaSuccess) return e;
-    k3_intra_chunk<DK, DV, C, T><<<dim3((unsigned)a.max_chunks, a.H), DV, sm3, s>>>(a);
-    e = cudaGetLastError();
-    profile_mark(4, s);
     return e;
 }
 

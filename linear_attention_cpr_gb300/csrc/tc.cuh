@@ -91,6 +91,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint3
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) global -> shared,
 // completing as transaction bytes on mbar.
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), and the wait for all
+// of this thread's copies.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_g2s(void* smem, const void* gmem, uint32_t bytes, uint64_t* mbar)
 {
     asm volatile(
@@ -216,13 +225,36 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* mbar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(mbar)) : "memory");
 }
 
-// bf16 hi/lo split of an fp32 value: hi = bf16(x), lo = bf16(x - hi) (x - hi is exact).
-__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo)
+// Two-term bf16 split of an fp32 value, x = hi + lo + e.  hi is the head of Dekker's
+// splitting (Veltkamp's method with the constant 2^16 + 1): a value with at most 8
+// significant bits, so exactly a bf16, computed with three fp32 operations; lo = x - hi is
+// exact in fp32 and is truncated to bf16 when packed (its upper 16 bits), so
+// |e| < 2^-15 |x|.  Every step is an explicit round-to-nearest fp32 operation or a bit
+// move, so all kernels produce the same splits.
+__device__ __forceinline__ void split_f32(float x, float& hi, float& lo)
 {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    const __nv_bfloat16 l = __float2bfloat16_rn(__fsub_rn(x, __bfloat162float(h)));
-    hi = __bfloat16_as_ushort(h);
-    lo = __bfloat16_as_ushort(l);
+    const float t = __fmul_rn(x, 65537.0f);
+    hi = __fsub_rn(t, __fsub_rn(t, x));
+    lo = __fsub_rn(x, hi);
+}
+
+// bf16 pair (a in the low half, b in the high half) from the upper 16 bits of two fp32s.
+__device__ __forceinline__ uint32_t pack_upper(float a, float b)
+{
+    return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);
+}
+
+// Split 8 consecutive values into 16-byte hi and lo bf16 rows (lo_dst may be NULL).
+__device__ __forceinline__ void split8_store(const float (&x)[8], unsigned char* hi_dst, unsigned char* lo_dst)
+{
+    float h[8], l[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) split_f32(x[e], h[e], l[e]);
+    *reinterpret_cast<uint4*>(hi_dst) =
+        make_uint4(pack_upper(h[0], h[1]), pack_upper(h[2], h[3]), pack_upper(h[4], h[5]), pack_upper(h[6], h[7]));
+    if (lo_dst)
+        *reinterpret_cast<uint4*>(lo_dst) =
+            make_uint4(pack_upper(l[0], l[1]), pack_upper(l[2], l[3]), pack_upper(l[4], l[5]), pack_upper(l[6], l[7]));
 }
 
 }  // namespace tc
