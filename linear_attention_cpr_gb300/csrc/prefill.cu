@@ -380,67 +380,113 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
 
 // ------------------------------------------------------------------------------------
 // Intra-chunk token recurrence of one (chunk, head) item, by a group of DV threads.
-// Thread i holds value row i of the state over all key columns, as pairs
-// (S[i][m L + t], S[i][(m + 4) L + t]) for m = 0..3, t = 0..L-1 (L = DK / 8), so that
-// chains m and m + 4 of the canonical dot advance in one paired FMA and the tree ends
-// inside the thread.  Every lane of a warp reads the same key / query values from shared
-// memory (broadcast loads).
+// Thread (warp w, lane l) owns two value rows, i0 = 16w + (l & 15) and i1 = i0 + DV/2,
+// over one half of the key columns, h = l >> 4 (columns [h*DK/2, (h+1)*DK/2)).  It keeps
+// them as pairs (S[i][c], S[i][c + DK/4]) so that chains m and m+2 of its half advance in
+// one paired FMA; each key/query value loaded from shared memory serves both rows (two
+// distinct addresses per warp-wide load, one per half).  The half-warps hold the two
+// halves of the canonical tree, ((c0+c1)+(c2+c3)) and ((c4+c5)+(c6+c7)), and add them
+// after one shuffle.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C>
 struct K3Smem {
-    static constexpr int ROW = DK;   // key / query row: pair (m, t) at float offset 2 (m L + t)
-    static constexpr int NT = DV;    // threads of a group
+    // key/query rows: half 0's DK/4 pairs, 4 floats of padding, half 1's pairs, 4 floats
+    // (the padding puts the two half-warps' broadcast loads in different banks)
+    static constexpr int ROW = DK + 8;
+    static constexpr int NT = DV;  // threads of a group
     // keys and queries (fp32 pairs), values as stored (at most fp32), alpha and beta
     static constexpr size_t bytes = sizeof(float) * ((size_t)2 * C * ROW + (size_t)C * DV + 2 * C);
 };
 
-// Chain sums of the row with w: acc[m] = (chain m, chain m + 4).
 template <int DK>
-__device__ __forceinline__ void k3_dot(const float2 (&S)[DK / 2], const float2* __restrict__ w, float2 (&acc)[4])
+struct K3Row {
+    static constexpr int NP = DK / 4;  // pairs per row per thread (half of DK columns)
+};
+
+// Partial (this half) of the canonical dot of both rows with w (pairs of this half).
+template <int DK>
+__device__ __forceinline__ void k3_half_dot(const float2 (&S0)[DK / 4], const float2 (&S1)[DK / 4],
+                                            const float2* __restrict__ w, float& d0, float& d1)
 {
-    constexpr int L = DK / 8;
+    constexpr int L = DK / 8;  // pair p is chain p/L (x) and p/L + 2 (y)
+    float2 a0[2], a1[2];
 #pragma unroll
     for (int t = 0; t < L; t += 2) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < 2; ++m) {
             const int p = m * L + t;
             const float4 w4 = *reinterpret_cast<const float4*>(w + p);
             const float2 w0 = make_float2(w4.x, w4.y), w1 = make_float2(w4.z, w4.w);
-            acc[m] = (t == 0) ? __fmul2_rn(S[p], w0) : __ffma2_rn(S[p], w0, acc[m]);
-            acc[m] = __ffma2_rn(S[p + 1], w1, acc[m]);
+            const bool first = (t == 0);
+            a0[m] = first ? __fmul2_rn(S0[p], w0) : __ffma2_rn(S0[p], w0, a0[m]);
+            a1[m] = first ? __fmul2_rn(S1[p], w0) : __ffma2_rn(S1[p], w0, a1[m]);
+            a0[m] = __ffma2_rn(S0[p + 1], w1, a0[m]);
+            a1[m] = __ffma2_rn(S1[p + 1], w1, a1[m]);
         }
     }
+    // chains (c0, c2) in a[0] and (c1, c3) in a[1]: (c0 + c1) + (c2 + c3)
+    const float2 s0 = __fadd2_rn(a0[0], a0[1]), s1 = __fadd2_rn(a1[0], a1[1]);
+    d0 = __fadd_rn(s0.x, s0.y);
+    d1 = __fadd_rn(s1.x, s1.y);
 }
 
-// One token: S <- alpha S + u k^T, then the chain sums of S q (and of S k_next).
 template <int DK, bool NEXT>
-__device__ __forceinline__ void k3_token(float2 (&S)[DK / 2], const float2* __restrict__ kr,
+__device__ __forceinline__ void k3_token(float2 (&S0)[DK / 4], float2 (&S1)[DK / 4], const float2* __restrict__ kr,
                                          const float2* __restrict__ qr, const float2* __restrict__ kn, float alpha,
-                                         float u, float2 (&o)[4], float2 (&x)[4])
+                                         float u0, float u1, float& o0, float& o1, float& x0, float& x1)
 {
-    constexpr int L = DK / 8;
-    const float2 a2 = make_float2(alpha, alpha), u2 = make_float2(u, u);
+    constexpr int L = DK / 8;  // pairs [0, L) carry chains (0, 2); pairs [L, 2L) chains (1, 3)
+    const float2 a2 = make_float2(alpha, alpha), u02 = make_float2(u0, u0), u12 = make_float2(u1, u1);
+    float2 co0[2], co1[2], cx0[2], cx1[2];
 #pragma unroll
     for (int t = 0; t < L; t += 2) {
         const bool first = (t == 0);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < 2; ++m) {  // both chain blocks in one pass: 8 independent chains in flight
             const int p = m * L + t;
             const float4 k4 = *reinterpret_cast<const float4*>(kr + p);
             const float4 q4 = *reinterpret_cast<const float4*>(qr + p);
-            const float2 s0 = __ffma2_rn(u2, make_float2(k4.x, k4.y), __fmul2_rn(a2, S[p]));
-            const float2 s1 = __ffma2_rn(u2, make_float2(k4.z, k4.w), __fmul2_rn(a2, S[p + 1]));
-            S[p] = s0;
-            S[p + 1] = s1;
-            o[m] = first ? __fmul2_rn(s0, make_float2(q4.x, q4.y)) : __ffma2_rn(s0, make_float2(q4.x, q4.y), o[m]);
-            o[m] = __ffma2_rn(s1, make_float2(q4.z, q4.w), o[m]);
+            const float2 k0 = make_float2(k4.x, k4.y), k1 = make_float2(k4.z, k4.w);
+            const float2 q0 = make_float2(q4.x, q4.y), q1 = make_float2(q4.z, q4.w);
+            const float2 s00 = __ffma2_rn(u02, k0, __fmul2_rn(a2, S0[p]));
+            const float2 s10 = __ffma2_rn(u12, k0, __fmul2_rn(a2, S1[p]));
+            const float2 s01 = __ffma2_rn(u02, k1, __fmul2_rn(a2, S0[p + 1]));
+            const float2 s11 = __ffma2_rn(u12, k1, __fmul2_rn(a2, S1[p + 1]));
+            S0[p] = s00;
+            S1[p] = s10;
+            S0[p + 1] = s01;
+            S1[p + 1] = s11;
+            co0[m] = first ? __fmul2_rn(s00, q0) : __ffma2_rn(s00, q0, co0[m]);
+            co1[m] = first ? __fmul2_rn(s10, q0) : __ffma2_rn(s10, q0, co1[m]);
             if (NEXT) {
                 const float4 n4 = *reinterpret_cast<const float4*>(kn + p);
-                x[m] = first ? __fmul2_rn(s0, make_float2(n4.x, n4.y)) : __ffma2_rn(s0, make_float2(n4.x, n4.y), x[m]);
-                x[m] = __ffma2_rn(s1, make_float2(n4.z, n4.w), x[m]);
+                const float2 n0 = make_float2(n4.x, n4.y), n1 = make_float2(n4.z, n4.w);
+                cx0[m] = first ? __fmul2_rn(s00, n0) : __ffma2_rn(s00, n0, cx0[m]);
+                cx1[m] = first ? __fmul2_rn(s10, n0) : __ffma2_rn(s10, n0, cx1[m]);
+                cx0[m] = __ffma2_rn(s01, n1, cx0[m]);
+                cx1[m] = __ffma2_rn(s11, n1, cx1[m]);
             }
+            co0[m] = __ffma2_rn(s01, q1, co0[m]);
+            co1[m] = __ffma2_rn(s11, q1, co1[m]);
         }
     }
+    {
+        const float2 t0 = __fadd2_rn(co0[0], co0[1]), t1 = __fadd2_rn(co1[0], co1[1]);
+        o0 = __fadd_rn(t0.x, t0.y);
+        o1 = __fadd_rn(t1.x, t1.y);
+    }
+    if (NEXT) {
+        const float2 t0 = __fadd2_rn(cx0[0], cx0[1]), t1 = __fadd2_rn(cx1[0], cx1[1]);
+        x0 = __fadd_rn(t0.x, t0.y);
+        x1 = __fadd_rn(t1.x, t1.y);
+    }
+}
+
+// Both halves end with the same value: left half + right half (the canonical tree's root).
+__device__ __forceinline__ float k3_join(float mine, int half)
+{
+    const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+    return half == 0 ? __fadd_rn(mine, other) : __fadd_rn(other, mine);
 }
 
 template <int DK, int DV, int C, typename T>
@@ -448,9 +494,11 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
 {
     static_assert(DK % 32 == 0 && DV % 32 == 0, "DK and DV must be multiples of 32");
     using S3 = K3Smem<DK, DV, C>;
-    constexpr int NT = S3::NT, L = DK / 8, ROW = S3::ROW, NP = DK / 2;
-    float* kp = sm3;                                      // [C][ROW] keys as pairs
-    float* qp = kp + C * ROW;                             // [C][ROW] queries as pairs
+    constexpr int NT = S3::NT, NP = DK / 4, ROW = S3::ROW;
+    // keys and queries: row r, half h, pair p at float offset r*ROW + h*(DK/2 + 4) + 2p,
+    // holding (x[h*DK/2 + p], x[h*DK/2 + p + DK/4])
+    float* kp = sm3;                                      // [C][ROW]
+    float* qp = kp + C * ROW;                             // [C][ROW]
     T* vs = reinterpret_cast<T*>(qp + C * ROW);           // [C][DV], as stored
     float* al = reinterpret_cast<float*>(vs + C * DV);    // [C]
     float* bt = al + C;                                   // [C]
@@ -477,7 +525,7 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
             const int idx = tid + s * NT, r = idx / VV, cc = idx % VV;
             if (r < len) tc::cp_async16(vs + r * DV + cc * VE, v + ((size_t)(t0 + r) * H + hd) * DV + cc * VE);
         }
-        constexpr int P = NK < 4 ? NK : 4;  // loads in flight per pass
+        constexpr int P = NK < 2 ? NK : 2;  // loads in flight per pass
 #pragma unroll
         for (int s0 = 0; s0 < NK; s0 += P) {
             uint4 kr[P], qr[P];
@@ -498,9 +546,8 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
                     const T* qe = reinterpret_cast<const T*>(&qr[s]);
 #pragma unroll
                     for (int e = 0; e < VE; ++e) {
-                        // column jj: chain block b = jj / L, entry t = jj % L -> pair (b % 4, t), slot b / 4
-                        const int jj = cc * VE + e, blk = jj / L, t = jj % L;
-                        const int pidx = r * ROW + 2 * ((blk & 3) * L + t) + (blk >> 2);
+                        const int jj = cc * VE + e, hh = jj / (DK / 2), jl = jj % (DK / 2);
+                        const int pidx = r * ROW + hh * (DK / 2 + 4) + 2 * (jl % NP) + jl / NP;
                         kp[pidx] = to_f32<T>(ke[e]);
                         qp[pidx] = to_f32<T>(qe[e]);
                     }
@@ -524,49 +571,54 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
         named_bar(bar, NT);
         return;
     }
-    const int i = tid;  // this thread's value row
-    // the chunk's boundary state: row i over all key columns
-    float2 S[NP];
+    const int w = tid >> 5, lane = tid & 31, half = lane >> 4;
+    const int i0 = w * 16 + (lane & 15), i1 = i0 + DV / 2;
+    // the chunk's boundary state: rows i0, i1 over this half's columns
+    float2 S0[NP], S1[NP];
     {
-        const float* bsrc = a.boundary + ((size_t)c * H + hd) * DK * DV + i;
+        const float* bsrc = a.boundary + ((size_t)c * H + hd) * DK * DV + (size_t)(half * (DK / 2)) * DV;
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int t = 0; t < L; ++t)
-                S[m * L + t] = make_float2(bsrc[(size_t)(m * L + t) * DV], bsrc[(size_t)((m + 4) * L + t) * DV]);
+        for (int p = 0; p < NP; ++p) {
+            S0[p] = make_float2(bsrc[(size_t)p * DV + i0], bsrc[(size_t)(p + NP) * DV + i0]);
+            S1[p] = make_float2(bsrc[(size_t)p * DV + i1], bsrc[(size_t)(p + NP) * DV + i1]);
+        }
     }
 
-    const float2* kq = reinterpret_cast<const float2*>(kp);
-    const float2* qq = reinterpret_cast<const float2*>(qp);
+    const float2* kph = reinterpret_cast<const float2*>(kp + half * (DK / 2 + 4));
+    const float2* qph = reinterpret_cast<const float2*>(qp + half * (DK / 2 + 4));
     constexpr int RP = ROW / 2;  // row stride in pairs
-    float x;
-    {
-        float2 acc[4];
-        k3_dot<DK>(S, kq, acc);
-        x = tree8_pairs(acc[0], acc[1], acc[2], acc[3]);
-    }
-    T* orow = out + ((size_t)t0 * H + hd) * DV + i;
+    float x0, x1;
+    k3_half_dot<DK>(S0, S1, kph, x0, x1);
+    x0 = k3_join(x0, half);
+    x1 = k3_join(x1, half);
+    T* orow = out + ((size_t)t0 * H + hd) * DV;
     for (int r = 0; r < len; ++r) {
         const float alpha = al[r], beta = bt[r];
-        const float u = step_u(alpha, beta, to_f32<T>(vs[r * DV + i]), x);
-        float2 o[4], xn[4];
+        const float u0 = step_u(alpha, beta, to_f32<T>(vs[r * DV + i0]), x0);
+        const float u1 = step_u(alpha, beta, to_f32<T>(vs[r * DV + i1]), x1);
+        float o0, o1;
+        if (r + 1 < len)
+            k3_token<DK, true>(S0, S1, kph + r * RP, qph + r * RP, kph + (r + 1) * RP, alpha, u0, u1, o0, o1, x0, x1);
+        else
+            k3_token<DK, false>(S0, S1, kph + r * RP, qph + r * RP, kph, alpha, u0, u1, o0, o1, x0, x1);
+        o0 = k3_join(o0, half);
+        o1 = k3_join(o1, half);
         if (r + 1 < len) {
-            k3_token<DK, true>(S, kq + r * RP, qq + r * RP, kq + (r + 1) * RP, alpha, u, o, xn);
-            x = tree8_pairs(xn[0], xn[1], xn[2], xn[3]);
-        } else {
-            k3_token<DK, false>(S, kq + r * RP, qq + r * RP, kq, alpha, u, o, xn);
+            x0 = k3_join(x0, half);
+            x1 = k3_join(x1, half);
         }
-        orow[(size_t)r * H * DV] = from_f32<T>(tree8_pairs(o[0], o[1], o[2], o[3]));
+        // both halves hold both outputs: half 0 stores row i0, half 1 row i1 (no branch)
+        orow[(size_t)r * H * DV + (half ? i1 : i0)] = from_f32<T>(half ? o1 : o0);
     }
     if (j * C + len == Ls && len < C) {  // final partial chunk: the stepped state is state_out
-        float* dst = a.state_out + ((size_t)n * H + hd) * DK * DV + i;
+        float* dst = a.state_out + ((size_t)n * H + hd) * DK * DV + (size_t)(half * (DK / 2)) * DV;
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int t = 0; t < L; ++t) {
-                dst[(size_t)(m * L + t) * DV] = S[m * L + t].x;
-                dst[(size_t)((m + 4) * L + t) * DV] = S[m * L + t].y;
-            }
+        for (int p = 0; p < NP; ++p) {
+            dst[(size_t)p * DV + i0] = S0[p].x;
+            dst[(size_t)(p + NP) * DV + i0] = S0[p].y;
+            dst[(size_t)p * DV + i1] = S1[p].x;
+            dst[(size_t)(p + NP) * DV + i1] = S1[p].y;
+        }
     }
     named_bar(bar, NT);  // the group's shared memory is reused by its next item
 }
