@@ -122,8 +122,9 @@ __device__ __forceinline__ bool chunk_decays_and_A(const PrepSmem<DK, C>& s, uns
     return ok;
 }
 
-// Column `col` of [W | U~] (col < DK: W, else U~ column col - DK) by forward
-// substitution.  V element (r, n) of the chunk is vbase[r * vstride + n].
+// Column `col` of the right-hand sides [W0 | U0] (col < DK: W0_r[col] = (beta_r e_r)
+// k_r[col], else U0_r[n] = beta_r v_r[n] with n = col - DK).  V element (r, n) of the
+// chunk is vbase[r * vstride + n].
 template <int DK, int DV, int C, typename T>
 __device__ __forceinline__ void chunk_column(const PrepSmem<DK, C>& s, int col, const T* vbase, size_t vstride,
                                              float x[C])
@@ -135,16 +136,18 @@ __device__ __forceinline__ void chunk_column(const PrepSmem<DK, C>& s, int col, 
 #pragma unroll
         for (int r = 0; r < C; ++r) x[r] = __fmul_rn(s.bs[r], to_f32<T>(vbase[(size_t)r * vstride + (col - DK)]));
     }
-    fwd_subst<C>(s.A, x);
 }
 
 // ======================================================================================
-// Tensor-core half of the chunk update.  U is applied in the matrix form
-//     S_new = S_b M + B,   M = gamma I - W^T (D K),   B = U~^T (D K),   D = diag(d_r)
-// (the WY relations above, with the state-dependent term written as S_b W^T (D K)).
-//   prep (state independent), two tcgen05 products with K = C:
-//        X = (D K)^T W   (M = 128 rows c, N = DK)   ->  Mt = gamma I - X   (Mt[c][c'] = M[c'][c])
-//        B = U~^T (D K)  (M = 128 rows i, N = DK)
+// Tensor-core half of the chunk update.  With W = T W0 and U~ = T U0 (the WY relations
+// above; T = (I + A)^-1, W0_r = (beta_r e_r) k_r, U0_r = beta_r v_r), U is applied in the
+// matrix form
+//     S_new = S_b M + B,   M = gamma I - W^T (D K),   B = U~^T (D K),   D = diag(d_r),
+// with W^T (D K) = W0^T Z and U~^T (D K) = U0^T Z, Z = T^T (D K):
+//   prep (state independent), tcgen05 products with K = C:
+//        Z^T = (D K)^T T   (M = 128 rows c, N = C)
+//        X = Z^T W0        (M = 128 rows c, N = DK)   ->  Mt = gamma I - X   (Mt[c][c'] = M[c'][c])
+//        B = U0^T Z        (M = 128 rows i, N = DK)
 //        bf16 hi/lo splits of every operand (tc::split_f32), three products
 //        hi*hi + hi*lo + lo*hi accumulated in fp32 in TMEM; Mt is split the same way
 //        (the chain's B operand image), B kept fp32 [DV][DK].
@@ -190,18 +193,21 @@ struct UCfg {
 
 // Build both prep operands in shared memory from the chunk's keys (s.kf, fp32), g (s.G)
 // and beta (s.bs); V element (r, n) at vbase[r * vstride + n].  All DK + DV threads;
-// contains __syncthreads.  The kk product uses TMEM columns [tmem, tmem + C) and one
-// phase of mbar (parity given).  On a true return aop / bop hold the bf16 splits and are
-// visible to the tensor cores; false (uniform) means the kk product timed out.
+// contains __syncthreads.  Three phases of mbar (the key Gram product, the Z product),
+// counted by `phase`; TMEM columns [tmem, tmem + C) are scratch.  On a true return aop
+// holds Z^T = (D K)^T T and bop the right-hand sides [W0 | U0]^T, both as bf16 splits
+// visible to the tensor cores; false (uniform) means a product timed out.
 template <int DK, int DV, int C, typename T>
 __device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned char* aop, unsigned char* bop,
                                               const T* vbase, size_t vstride, uint32_t tmem, uint64_t* mbar,
-                                              uint32_t parity)
+                                              uint32_t& phase)
 {
     using U = UCfg<DK, DV, C>;
     constexpr int KS = PrepSmem<DK, C>::KS;
-    const int tid = threadIdx.x, nt = blockDim.x;
-    if (!chunk_decays_and_A<DK, DV, C, T>(s, aop, tmem, mbar, parity)) return false;
+    constexpr uint32_t TT_SPLIT = C * C * 2;  // one bf16 split of the T^T tile
+    const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
+    if (!chunk_decays_and_A<DK, DV, C, T>(s, aop, tmem, mbar, phase & 1)) return false;
+    ++phase;
     // (D K)^T rows c: d_r * k_r[c] (zero rows beyond DK)
     for (int row = tid; row < U::MPAD; row += nt) {
 #pragma unroll
@@ -213,9 +219,61 @@ __device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned
             tc::split8_store(xs, aop + off, aop + U::AOP_SPLIT + off);
         }
     }
+    // T = (I + A)^-1 by forward substitution, column j by thread j
     float x[C];
-    chunk_column<DK, DV, C, T>(s, tid, vbase, vstride, x);
-    __syncthreads();  // keys and A are dead: their space becomes the [W | U~]^T operand
+    if (tid < C) {
+#pragma unroll
+        for (int r = 0; r < C; ++r) x[r] = (r == tid) ? 1.0f : 0.0f;
+        fwd_subst<C>(s.A, x);
+    }
+    __syncthreads();  // A is dead: its space holds T^T (rows j, K = r), bf16 splits
+    unsigned char* tt = reinterpret_cast<unsigned char*>(s.A);
+    if (tid < C) {
+#pragma unroll
+        for (int r0 = 0; r0 < C; r0 += 8) {
+            const uint32_t off = tc::tile_off<2>(tid, r0, C);
+            tc::split8_store(*reinterpret_cast<const float(*)[8]>(x + r0), tt + off, tt + TT_SPLIT + off);
+        }
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {  // Z^T = (D K)^T T into TMEM columns [0, C): M = 128 rows c, N = C, K = C
+        tc::fence_after_sync();
+        constexpr uint32_t SBO = (C / 8) * 128;
+        constexpr uint32_t idesc = tc::idesc_bf16(U::MPAD, C);
+        const uint32_t ao = tc::smem_u32(aop), to = tc::smem_u32(tt);
+        const uint32_t ha[3] = {0u, 0u, 1u}, hb[3] = {0u, 1u, 0u};
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+#pragma unroll
+            for (int k = 0; k < C / 16; ++k)
+                tc::mma_bf16(tmem, tc::sdesc(ao + ha[p] * U::AOP_SPLIT + k * 256, 128, SBO),
+                             tc::sdesc(to + hb[p] * TT_SPLIT + k * 256, 128, SBO), idesc, (p | k) ? 1u : 0u);
+        tc::commit(mbar);
+    }
+    chunk_column<DK, DV, C, T>(s, tid, vbase, vstride, x);  // this thread's row of [W0 | U0]^T, while Z runs
+    bool ok = __syncthreads_and(tc::mbar_wait(mbar, phase & 1));
+    ++phase;
+    if (!ok) return false;
+    // Z^T (fp32 in TMEM, row c = lane) -> bf16 splits over the (D K)^T operand
+    tc::fence_after_sync();
+    {
+        const int q = warp & 3, row = q * 32 + lane;
+        for (int g = warp >> 2; g * 32 < C; g += (nt / 32 + 3) / 4) {  // warp-uniform
+            float v[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(g * 32), v);
+#pragma unroll
+            for (int e8 = 0; e8 < 32; e8 += 8) {
+                if (g * 32 + e8 < C) {
+                    const uint32_t off = tc::tile_off<2>(row, g * 32 + e8, C);
+                    tc::split8_store(*reinterpret_cast<const float(*)[8]>(v + e8), aop + off, aop + U::AOP_SPLIT + off);
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();  // keys and T^T are dead: their space becomes the [W0 | U0]^T operand
 #pragma unroll
     for (int r0 = 0; r0 < C; r0 += 8) {
         const uint32_t off = tc::tile_off<2>(tid, r0, C);
@@ -227,8 +285,8 @@ __device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned
 }
 
 // One thread: both prep products (X into TMEM columns [0, DK), B into [DK, 2 DK)), then
-// commit to mbar.  aop = (D K)^T tile (128 rows c, K = C); bop = [W | U~]^T tile (rows
-// 0..DK-1 = W^T, rows DK.. = U~^T).
+// commit to mbar.  aop = Z^T tile (128 rows c, K = C); bop = [W0 | U0]^T tile (rows
+// 0..DK-1 = W0^T, rows DK.. = U0^T).
 template <int DK, int DV, int C>
 __device__ __forceinline__ void prep_mma(uint32_t tmem, const unsigned char* aop, const unsigned char* bop,
                                          uint64_t* mbar)

@@ -185,8 +185,7 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
         stile_fill<DK, DV>(stile + sl * 2 * U::S_SPLIT, a.ring.S_b + bh * SS, sl * kChainRows, tid, (int)blockDim.x);
     tc::fence_before_sync();
     // also publishes the S tiles
-    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, rv, (size_t)DV, tmem, mbar, phase & 1);
-    ++phase;
+    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, rv, (size_t)DV, tmem, mbar, phase);
     if (!ok) return false;
     tc::fence_after_sync();
     if (tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
@@ -231,7 +230,7 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     const int tid = threadIdx.x;
     if (tid < 32) tc::tmem_alloc(tslot, U::TMEM_COLS);
     if (tid == 0) {
-        tc::mbar_init(mbar, 1);  // three phases per pair: kk, prep, chain
+        tc::mbar_init(mbar, 1);  // four phases per pair: kk, Z, prep, chain
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();

@@ -28,10 +28,11 @@
 //   kk_ri = sum_j k_r[j] k_i[j]: a tcgen05 product of the keys' bf16 splits, fp32
 //           accumulation (exact products for bf16 keys; hi*hi + hi*lo + lo*hi for fp32)
 //   A_ri  = (beta_r * decay_exp(G_r - G_i)) * kk_ri              (i < r, else 0)
-//   W_r[c]  = (beta_r * e_r) * k_r[c],  then fma(-A_ri, W_i[c], .) for i = 0 .. r-1
-//   U~_r[n] = beta_r * v_r[n],          then fma(-A_ri, U~_i[n], .) for i = 0 .. r-1
+//   T = (I + A)^-1, column j by substitution: T_rj = [r == j], then fma(-A_ri, T_ij, .)
+//         for i = 0 .. r-1                                          (fwd_subst below)
+//   W0_r[c] = (beta_r * e_r) * k_r[c],  U0_r[n] = beta_r * v_r[n]   (W = T W0, U~ = T U0)
 //   then, in matrix form with D = diag(d_r) (chunk_update.cuh):
-//   M^T = gamma I - (D K)^T W,  B = U~^T (D K):  tcgen05 products (M = 128, N = dk,
+//   Z^T = (D K)^T T, M^T = gamma I - Z^T W0, B = U0^T Z:  tcgen05 products (M = 128,
 //         K = C) of bf16 hi/lo splits (Dekker's splitting, tc.cuh), hi*hi + hi*lo +
 //         lo*hi, fp32 accumulation
 //   S_new = S_b M + B:  per 64 value rows, a tcgen05 product of S_b's splits with M's

@@ -76,8 +76,8 @@ __global__ void __launch_bounds__(1024) k0_chunk_index(const int32_t* __restrict
 
 // ------------------------------------------------------------------------------------
 // k1: chunk prep.  One CTA per (chunk, head), DK + DV threads.  The key Gram product on
-// the tensor cores and the FP32 phase (decays, A, forward substitution for W and U~) are
-// followed by one tcgen05 product giving
+// the tensor cores, the FP32 phase (decays, A, T = (I + A)^-1 by forward substitution)
+// and the Z product are followed by one tcgen05 product giving
 // M^T and B^T of the chunk (chunk_update.cuh), written to the workspace: M^T as the
 // shared-memory image the chain kernel copies in one piece, B^T as fp32 rows.
 // Exits for partial chunks.
@@ -138,10 +138,11 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
-    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, v + ((size_t)t0 * H + h) * DV, (size_t)H * DV, tmem, mbar, 0);
+    uint32_t phase = 0;
+    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, v + ((size_t)t0 * H + h) * DV, (size_t)H * DV, tmem, mbar, phase);
     tc::fence_after_sync();
     if (ok && tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
-    ok = __syncthreads_and(ok && tc::mbar_wait(mbar, 1));  // uniform: the epilogue's TMEM loads are warp-wide
+    ok = __syncthreads_and(ok && tc::mbar_wait(mbar, phase & 1));  // uniform: the epilogue's TMEM loads are warp-wide
     if (ok) {
         const size_t ch = (size_t)c * H + h;
         // the operand space (R1) is dead once the products completed: it stages the outputs
