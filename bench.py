@@ -31,6 +31,11 @@ METRIC = "CPR-GDN prefill tokens/s, decode steps/s per layer; % of roofline; 1 G
 # FP32 pipe: 152 SMs x 128 FP32 lanes x 2 flop (FMA) x 2.07 GHz (maximum SM clock)
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 L2_BYTES = 129 * 1024 * 1024
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
+# of the kernel as it now stands: k23_chain_and_intra at trainer_fwd, k4_decode_step at
+# rollout_decode.  Reset to None whenever the kernel changes.
+TRAFFIC_K23_TRAINER_FWD = 578.144512e6 + 200.238336e6
+TRAFFIC_K4_ROLLOUT_DECODE = 271.846656e6 + 210.828800e6
 
 
 def _peaks():
@@ -64,7 +69,7 @@ class ClockSampler:
             self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.tmp, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -257,7 +262,8 @@ def run_ours(args):
     intra_ms = kern_ms["chain_and_intra"]
     achieved = flops_intra / (intra_ms / 1e3) / 1e12
     roofline = {"kernel": "k23_chain_and_intra", "bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS,
-                "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS,
+                "traffic": TRAFFIC_K23_TRAINER_FWD if w.name == "trainer_fwd" else None,
                 "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
                 "flops_per_launch": flops_intra}
     t_roof_ms = max(alg_bytes / (hbm_peak * 1e9), flops_intra / (FP32_PEAK_TFLOPS * 1e12)) * 1e3
@@ -392,7 +398,7 @@ def run_decode(args, cpr, inputs, dev, hbm_peak, dist, world):
         "kernels_ms": {"decode_step": k4_ms, "resync": statistics.fmean(k5)},
         "resyncs_per_step": n_res / n_steps,
         "roofline": {"kernel": "k4_decode_step", "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": ach / hbm_peak, "traffic": None, "bytes_per_launch": step_only},
+                     "frac": ach / hbm_peak, "traffic": TRAFFIC_K4_ROLLOUT_DECODE, "bytes_per_launch": step_only},
         "t_roof_ms": bytes_step / (hbm_peak * 1e9) * 1e3,
         "frac_of_t_roof": bytes_step / (hbm_peak * 1e9) * 1e3 / ms,
         "e2e": {"value": 1e3 / e2e_ms * world, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -403,7 +409,7 @@ def run_decode(args, cpr, inputs, dev, hbm_peak, dist, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="trainer_fwd")
