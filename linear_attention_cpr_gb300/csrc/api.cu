@@ -229,8 +229,6 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
     a.H = H;
     a.out = out;
     a.status = static_cast<uint32_t*>(workspace);
-    a.resync_count = static_cast<uint32_t*>(workspace) + 1;
-    a.resync_list = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + kAlign);
     a.num_sms = num_sms();
     if (a.num_sms <= 0) return CPR_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -75,8 +75,8 @@ struct PrefillArgs {
     int num_sms;
 };
 
-// Decode workspace: [0, 256) status word, resync count; then int32 [B] resync list.
-inline size_t decode_workspace_bytes(int32_t B) { return kAlign + align_up(sizeof(int32_t) * (size_t)(B > 0 ? B : 1), kAlign); }
+// Decode workspace: [0, 256) status word.
+inline size_t decode_workspace_bytes(int32_t) { return kAlign; }
 
 struct DecodeArgs {
     const void* q;
@@ -91,8 +91,6 @@ struct DecodeArgs {
     int32_t H;
     void* out;
     uint32_t* status;
-    uint32_t* resync_count;  // sequences appended to resync_list by the step kernel
-    int32_t* resync_list;    // [B]
     int num_sms;
 };
 

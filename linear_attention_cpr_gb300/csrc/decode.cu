@@ -102,7 +102,6 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
         sc[1] = bb;
         a.ring.g[bh * C + r] = gg;
         a.ring.beta[bh * C + r] = bb;
-        if (r == C - 1 && h == 0) a.resync_list[atomicAdd(a.resync_count, 1u)] = b;  // this token completes a chunk
     }
     float s[L][VPT];
     float* st = a.state + bh * DK * DV + (size_t)(m * L) * DV + lane * VPT;
@@ -148,13 +147,15 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 }
 
 // ------------------------------------------------------------------------------------
-// k5: resync.  A persistent grid of at most one wave walks the (sequence, head) pairs of
-// the sequences whose token completed a chunk (k4 appends them to a list), DK + DV
-// threads per CTA.  Each pair runs the same routines as prefill: the key Gram product, the
-// FP32 phase and the prep product of k1_chunk_prep (prep_operands, prep_mma, prep_epilogue, here into shared
-// memory), then the chain products and epilogue of k2_chain (chain_mma, chain_values) on
-// the ring's S_b.  The result replaces both the state and ring S_b.  The list's order
-// varies from run to run; each pair's result does not depend on it.
+// k5: resync, on a second stream while k4 steps every sequence.  A grid of at most one
+// wave walks the (sequence, head) pairs of the sequences whose token completes a chunk
+// (found from pos), DK + DV threads per CTA.  Each pair runs the same routines as prefill:
+// the key Gram product, the FP32 phase and the prep products of k1_chunk_prep
+// (prep_operands, prep_mma, prep_epilogue, here into shared memory), then the chain
+// products and epilogue of the chain role (chain_mma, chain_values) on the ring's S_b.
+// The result replaces ring S_b only; k7 copies it into the state once k4 is done (k4
+// reads and writes the state meanwhile).  The chunk's last token is read from the step's
+// inputs, since k4 writes its ring slot at the same time.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C, typename T>
 __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, unsigned char* sm5, uint32_t tmem,
@@ -168,24 +169,36 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     unsigned char* mt = sm5;
     float* bt = reinterpret_cast<float*>(sm5 + U::RS_BT_OFF);
     unsigned char* stile = sm5 + U::RS_S_OFF;
+    T* vsm = reinterpret_cast<T*>(sm5 + U::RS_V_OFF);
 
     const int tid = threadIdx.x, H = a.H;
     const size_t bh = (size_t)b * H + h;
     const size_t SS = (size_t)DK * DV;
     const T* rk = static_cast<const T*>(a.ring.k) + bh * C * DK;
     const T* rv = static_cast<const T*>(a.ring.v) + bh * C * DV;
+    // tokens 0..C-2 of the chunk come from the ring, token C-1 (this step's) from the inputs:
+    // the step kernel writes its ring slot concurrently
+    const T* tk = static_cast<const T*>(a.k) + bh * DK;
+    const T* tv = static_cast<const T*>(a.v) + bh * DV;
 
-    for (int idx = tid; idx < C * DK; idx += blockDim.x) s.kf[(idx / DK) * KS + idx % DK] = to_f32<T>(rk[idx]);
+    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+        const int r = idx / DK, j = idx % DK;
+        s.kf[r * KS + j] = to_f32<T>(r < C - 1 ? rk[idx] : tk[j]);
+    }
+    for (int idx = tid; idx < C * DV; idx += blockDim.x) {
+        const int r = idx / DV, n = idx % DV;
+        vsm[idx] = r < C - 1 ? rv[idx] : tv[n];
+    }
     if (tid < C) {
-        s.G[tid] = a.ring.g[bh * C + tid];
-        s.bs[tid] = a.ring.beta[bh * C + tid];
+        s.G[tid] = tid < C - 1 ? a.ring.g[bh * C + tid] : a.g[bh];
+        s.bs[tid] = tid < C - 1 ? a.ring.beta[bh * C + tid] : a.beta[bh];
     }
 #pragma unroll
     for (int sl = 0; sl < U::NSLICE; ++sl)
         stile_fill<DK, DV>(stile + sl * 2 * U::S_SPLIT, a.ring.S_b + bh * SS, sl * kChainRows, tid, (int)blockDim.x);
     tc::fence_before_sync();
     // also publishes the S tiles
-    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, rv, (size_t)DV, tmem, mbar, phase);
+    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, vsm, (size_t)DV, tmem, mbar, phase);
     if (!ok) return false;
     tc::fence_after_sync();
     if (tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
@@ -209,7 +222,6 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     for (int sl = 0; sl < U::NSLICE; ++sl) {
         float v[ChainMap<DK, WPQ>::CPT];
         chain_values<DK, DV, WPQ>(tmem + sl * DK, bt + (size_t)sl * kChainRows * DK, sl * kChainRows, v);
-        chain_store<DK, DV, WPQ>(a.state + bh * SS, sl * kChainRows, v);
         chain_store<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
     }
     tc::fence_before_sync();
@@ -223,8 +235,39 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
 {
     using U = UCfg<DK, DV, C>;
     extern __shared__ __align__(1024) unsigned char sm5[];
-    const uint32_t items = *a.resync_count * (uint32_t)a.H;
+    __shared__ int warp_cnt[(DK + DV) / 32];
+    __shared__ int found;
+    // the sequences whose token completes a chunk, in ascending order: rank n <-> the n-th b
+    // with pos[b] % C == C - 1 (pos >= 0); every CTA counts them from pos
+    auto completes = [&](int b) { const int p = a.pos[b]; return p >= 0 && p % C == C - 1; };
+    int total = 0;
+    for (int b0 = 0; b0 < a.B; b0 += blockDim.x)
+        total += __syncthreads_count((int)threadIdx.x + b0 < a.B && completes((int)threadIdx.x + b0));
+    const uint32_t items = (uint32_t)total * (uint32_t)a.H;
     if (blockIdx.x >= items) return;
+    // b of rank n: a block-wide scan over pos (all threads)
+    auto seq_of_rank = [&](int n) -> int {
+        const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+        int before = 0;
+        for (int b0 = 0; b0 < a.B; b0 += blockDim.x) {
+            const bool q = tid + b0 < a.B && completes(tid + b0);
+            const unsigned m = __ballot_sync(0xffffffffu, q);
+            if (lane == 0) warp_cnt[wid] = __popc(m);
+            if (tid == 0) found = -1;
+            __syncthreads();
+            int rank = before + __popc(m & ((1u << lane) - 1u));
+            for (int w = 0; w < wid; ++w) rank += warp_cnt[w];
+            if (q && rank == n) found = tid + b0;
+            int chunk_total = 0;
+            for (int w = 0; w < nw; ++w) chunk_total += warp_cnt[w];
+            __syncthreads();
+            const int f = found;
+            __syncthreads();
+            if (f >= 0) return f;
+            before += chunk_total;
+        }
+        return 0;  // not reached: n < total
+    };
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm5 + U::RS_BAR_OFF);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
     const int tid = threadIdx.x;
@@ -239,7 +282,8 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     const uint32_t tmem = *tslot;
     uint32_t phase = 0;
     for (uint32_t it = blockIdx.x; it < items; it += gridDim.x) {
-        if (!resync_one<DK, DV, C, T>(a, a.resync_list[it / a.H], (int)(it % a.H), sm5, tmem, mbar, phase)) {
+        const int b = seq_of_rank((int)(it / a.H));
+        if (!resync_one<DK, DV, C, T>(a, b, (int)(it % a.H), sm5, tmem, mbar, phase)) {
             if (tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
             break;  // uniform: the barrier's phase is unknown after a timeout
         }
@@ -302,22 +346,71 @@ __global__ void __launch_bounds__(256) k6_ring_fill(RingArgs a)
 }
 
 // ------------------------------------------------------------------------------------
+// k7: resync commit.  One CTA per (sequence, head): for a sequence whose token completed a
+// chunk, state <- ring S_b (the resynchronised state).
+// ------------------------------------------------------------------------------------
+template <int DK, int DV, int C>
+__global__ void __launch_bounds__(256) k7_resync_commit(DecodeArgs a)
+{
+    const int b = blockIdx.x, h = blockIdx.y;
+    const int p = a.pos[b];
+    if (p < 0 || p % C != C - 1) return;
+    const size_t off = ((size_t)b * a.H + h) * DK * DV;
+    const float4* src = reinterpret_cast<const float4*>(a.ring.S_b + off);
+    float4* dst = reinterpret_cast<float4*>(a.state + off);
+    for (int i = threadIdx.x; i < DK * DV / 4; i += blockDim.x) dst[i] = src[i];
+}
+
+namespace {
+// Per-device side stream and fork/join events of the decode launch (created on first use).
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+cudaError_t side_stream(SideStream*& out)
+{
+    static SideStream per_device[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    SideStream& ss = per_device[dev];
+    if (!ss.stream) {
+        if ((e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    out = &ss;
+    return cudaSuccess;
+}
+}  // namespace
+
 template <int DK, int DV, int C, typename T>
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
 {
-    cudaError_t e = cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), s);  // status word and resync count
+    cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
+    SideStream* ss = nullptr;
+    if ((e = side_stream(ss)) != cudaSuccess) return e;
     profile_mark(0, s);
-    k4_decode_step<DK, DV, C, T><<<dim3(a.B, a.H), 256, 0, s>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    profile_mark(1, s);
+    // fork: the resync runs on the side stream while the step kernel runs on s
+    if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss->stream, ss->fork, 0)) != cudaSuccess) return e;
     // dynamic shared memory also caps the CTAs per SM so their TMEM columns fit in 512
     const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::RS_BYTES, tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
     e = cudaFuncSetAttribute(k5_resync<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
     if (e != cudaSuccess) return e;
-    const int grid = std::max(1, std::min(a.B * a.H, a.num_sms * (int)(232448 / sm5)));
-    k5_resync<DK, DV, C, T><<<grid, DK + DV, sm5, s>>>(a);
+    // at most half the SMs, so the step kernel keeps the rest while the resync runs
+    const int grid = std::max(1, std::min(a.B * a.H, std::max(1, a.num_sms / 2) * (int)(232448 / sm5)));
+    k5_resync<DK, DV, C, T><<<grid, DK + DV, sm5, ss->stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k4_decode_step<DK, DV, C, T><<<dim3(a.B, a.H), 256, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    profile_mark(1, s);
+    // join, then the resynchronised states replace the stepped ones
+    if ((e = cudaEventRecord(ss->join, ss->stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, ss->join, 0)) != cudaSuccess) return e;
+    k7_resync_commit<DK, DV, C><<<dim3(a.B, a.H), 256, 0, s>>>(a);
     e = cudaGetLastError();
     profile_mark(2, s);
     return e;
