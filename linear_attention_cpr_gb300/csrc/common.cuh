@@ -33,7 +33,8 @@ __host__ __device__ inline int64_t max_chunks_bound(int64_t total_tokens, int32_
 //   mt             [max_chunks, H] tiles of 2 * dk * dk bf16: the chunk's M^T, bf16 hi/lo
 //                  splits, in the tensor cores' shared-memory image
 //   bt             fp32 [max_chunks, H, dv, dk]: the chunk's B
-//   ready          uint32 [max_chunks, H]: slices of each boundary state published
+//   ready          uint32 [max_chunks, H]: slices of each boundary state published, then
+//                  one uint32: the next intra-chunk item to claim
 struct PrefillLayout {
     size_t cu_chunks, mt, bt, ready, total, mt_bytes, bt_bytes;
     __host__ __device__ PrefillLayout(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk, int32_t dv,
@@ -46,7 +47,7 @@ struct PrefillLayout {
         mt = align_up(cu_chunks + sizeof(int32_t) * (size_t)(n_seqs + 1), kAlign);
         bt = align_up(mt + mt_bytes * (size_t)mc * H, kAlign);
         ready = align_up(bt + bt_bytes * (size_t)mc * H, kAlign);
-        total = align_up(ready + sizeof(uint32_t) * (size_t)mc * H, kAlign);
+        total = align_up(ready + sizeof(uint32_t) * ((size_t)mc * H + 1), kAlign);
     }
 };
 

@@ -183,14 +183,16 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-__device__ __forceinline__ int wait_published(const uint32_t* flag, uint32_t target)
+// Wait until *flag >= target; gives up (returns 0) after about 4 s, or at once when another
+// CTA of the launch has recorded a timeout in the status word.
+__device__ __forceinline__ int wait_published(const uint32_t* flag, uint32_t target, const uint32_t* status)
 {
     if (ld_acquire(flag) >= target) return 1;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 0; it < (1u << 26); ++it) {
         __nanosleep(128);
         if (ld_acquire(flag) >= target) return 1;
-        if (global_ns() - t0 > 4000000000ull) break;
+        if ((ld_acquire(status) & CPR_DEV_TIMEOUT) || global_ns() - t0 > 4000000000ull) break;
     }
     return 0;
 }
@@ -375,8 +377,14 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
     }
     __syncthreads();
     if (failed && tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
+    if (tid == 0) {  // the shared memory is reused by the items
+        for (int b = 0; b < Cf::NSTAGE; ++b) tc::mbar_inval(&mbar_ld[b]);
+        tc::mbar_inval(mbar_mma);
+        tc::mbar_inval(mbar_tile);
+    }
     tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(tmem, Cf::TMEM_COLS);
+    __syncthreads();
 }
 
 // ------------------------------------------------------------------------------------
@@ -565,7 +573,7 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
     // every slice of it is published (bounded)
     __shared__ int wait_ok[8];
     const int gi = bar - 1;
-    if (tid == 0) wait_ok[gi] = wait_published(a.ready + (size_t)c * H + hd, (uint32_t)K2Cfg<DK, DV>::NSLICE);
+    if (tid == 0) wait_ok[gi] = wait_published(a.ready + (size_t)c * H + hd, (uint32_t)K2Cfg<DK, DV>::NSLICE, a.status);
     named_bar(bar, NT);
     if (!wait_ok[gi]) {
         if (tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
@@ -626,9 +634,10 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
 
 // ------------------------------------------------------------------------------------
 // k23: boundary chain and intra-chunk recurrence in one cooperative launch of one CTA per
-// SM slot, 8 warps each.  CTAs [0, n_chain) run the chains (chain_role); the others run
-// the (chunk, head) items of the intra-chunk recurrence in chunk order, 256 / DV groups
-// of DV threads per CTA, each item starting as soon as its boundary state is published.  The chain's latency-bound steps thus overlap the FP32-bound items.
+// SM slot, 8 warps each.  CTAs [0, n_chain) run the chains (chain_role) and then join the
+// others on the (chunk, head) items of the intra-chunk recurrence: 256 / DV groups of DV
+// threads per CTA claim items in chunk order from a counter, each item starting as soon
+// as its boundary state is published.  The chain's latency-bound steps thus overlap the FP32-bound items.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C>
 struct K23Cfg {
@@ -645,16 +654,20 @@ __global__ void __launch_bounds__(K2Cfg<DK, DV>::THREADS, 1) k23_chain_and_intra
     constexpr int NT = K3Smem<DK, DV, C>::NT;
     extern __shared__ __align__(1024) unsigned char sm23[];
     if (*a.status) return;
-    if ((int)blockIdx.x < n_chain) {
-        chain_role<DK, DV, C, T>(a, sm23, blockIdx.x, n_chain);
-        return;
-    }
-    const int g = threadIdx.x / NT;
-    const int64_t items = (int64_t)a.cu_chunks[a.n_seqs] * a.H;
-    const int64_t stride = (int64_t)(gridDim.x - n_chain) * F::GROUPS;
+    // chain CTAs join the items once their chains are done
+    if ((int)blockIdx.x < n_chain) chain_role<DK, DV, C, T>(a, sm23, blockIdx.x, n_chain);
+    const int g = threadIdx.x / NT, gtid = (int)threadIdx.x % NT;
+    const uint32_t items = (uint32_t)a.cu_chunks[a.n_seqs] * (uint32_t)a.H;
+    uint32_t* next_item = a.ready + (size_t)a.max_chunks * a.H;
+    __shared__ uint32_t claimed[F::GROUPS];
     float* smg = reinterpret_cast<float*>(sm23 + g * F::GROUP_BYTES);
-    for (int64_t t = (int64_t)(blockIdx.x - n_chain) * F::GROUPS + g; t < items; t += stride)
-        intra_item<DK, DV, C, T>(a, t / a.H, (int)(t % a.H), (int)threadIdx.x % NT, smg, 1 + g);
+    for (;;) {  // items are claimed in chunk order, one group at a time
+        if (gtid == 0) claimed[g] = atomicAdd(next_item, 1u);
+        named_bar(1 + g, NT);
+        const uint32_t t = claimed[g];
+        if (t >= items) break;
+        intra_item<DK, DV, C, T>(a, t / a.H, (int)(t % a.H), gtid, smg, 1 + g);  // ends with a group barrier
+    }
 }
 
 // ------------------------------------------------------------------------------------
@@ -678,7 +691,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
     profile_mark(2, s);
 
     using Cf = K2Cfg<DK, DV>;
-    e = cudaMemsetAsync(a.ready, 0, sizeof(uint32_t) * (size_t)a.max_chunks * a.H, s);
+    e = cudaMemsetAsync(a.ready, 0, sizeof(uint32_t) * ((size_t)a.max_chunks * a.H + 1), s);  // and the item counter
     if (e != cudaSuccess) return e;
     auto kern = k23_chain_and_intra<DK, DV, C, T>;
     const size_t sm23 = std::max<size_t>(K23Cfg<DK, DV, C>::bytes, tmem_cap_smem(Cf::TMEM_COLS));

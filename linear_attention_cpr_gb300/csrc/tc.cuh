@@ -89,6 +89,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint3
     return false;
 }
 
+// Invalidate an mbarrier whose shared memory is about to be reused for other data.
+__device__ __forceinline__ void mbar_inval(uint64_t* mbar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(smem_u32(mbar)) : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) global -> shared,
 // completing as transaction bytes on mbar.
 // 16-byte asynchronous copy global -> shared (both 16-byte aligned), and the wait for all
