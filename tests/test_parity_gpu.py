@@ -201,3 +201,34 @@ def test_decay_exp_error_bound():
     excess = (rel - bound)[normal]
     assert float(excess.max()) <= 0.0, float((rel / bound)[normal].max())
     assert float(y[0]) == 1.0
+
+
+@pytest.mark.parametrize("case", ["beta_zero", "alpha_one", "whole_chunks"])
+def test_degenerate_inputs_match_oracle(case):
+    """Degenerate cases of the recurrence, on the main shape (d128, C64, bf16):
+    beta = 0 leaves only the decay, S_t = (prod alpha) S_0 (checked in closed form too);
+    alpha = 1 (g = 0) is the ungated delta rule; lengths that are multiples of C end on a
+    chunk update (state_out is U's result, not a stepped state)."""
+    d, C, H = 128, 64, 2
+    lens = [2 * C, C, 3 * C] if case == "whole_chunks" else [C + 7, 2 * C + 1]
+    seqs = [_gpu.tokens(L, H, d, d, torch.bfloat16, seed=60 + i) for i, L in enumerate(lens)]
+    for s in seqs:
+        if case == "beta_zero":
+            s["beta"] = torch.zeros_like(s["beta"])
+        if case == "alpha_one":
+            s["g"] = torch.zeros_like(s["g"])
+    x = _gpu.pack(seqs)
+    gen = torch.Generator().manual_seed(61)
+    s0 = 0.3 * torch.randn(len(lens), H, d, d, generator=gen)
+    out, st, bnd = _gpu.prefill(_gpu.to_dev(x), C, state_in=s0.cuda())
+    o_ref, st_ref, bnd_ref = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], C,
+                                              state_in=s0)
+    _gpu.assert_close_to_oracle(out, st, o_ref, st_ref, _gpu.O_TOL_BF16, bnd, bnd_ref, what=case)
+    if case == "beta_zero":
+        cu = x["cu_seqlens"]
+        for n in range(len(lens)):
+            decay = torch.exp(x["g"][int(cu[n]):int(cu[n + 1])].double().sum(0))  # [H]
+            want = decay[:, None, None] * s0[n].double()
+            got = st[n].cpu().double()
+            rel = ((got - want).norm() / want.norm()).item()
+            assert rel <= _gpu.STATE_RTOL, rel
