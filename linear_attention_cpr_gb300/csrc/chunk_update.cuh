@@ -185,8 +185,8 @@ struct UCfg {
     static constexpr uint32_t RS_VEC_OFF = up1k(RS_BT_OFF + mx(AOP_REGION, BT_BYTES));
     static constexpr uint32_t RS_S_OFF = up1k(RS_VEC_OFF + 4 * C * 4);
     static constexpr uint32_t RS_BAR_OFF = RS_S_OFF + NSLICE * 2 * S_SPLIT;
-    static constexpr uint32_t RS_V_OFF = RS_BAR_OFF + 64;  // the chunk's values, as stored (at most fp32)
-    static constexpr uint32_t RS_BYTES = RS_V_OFF + C * DV * 4;
+    static constexpr uint32_t RS_V_OFF = RS_BAR_OFF + 64;  // the chunk's values, as stored
+    static constexpr uint32_t rs_bytes(uint32_t value_bytes) { return RS_V_OFF + C * DV * value_bytes; }
     static constexpr uint32_t PREP_BAR_OFF = (PREP_BYTES + 15) / 16 * 16;
     static constexpr uint32_t PREP_SMEM = PREP_BAR_OFF + 64;
     static constexpr uint32_t prep_idesc = tc::idesc_bf16(MPAD, DK);

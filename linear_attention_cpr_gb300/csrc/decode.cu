@@ -397,7 +397,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(ss->stream, ss->fork, 0)) != cudaSuccess) return e;
     // dynamic shared memory also caps the CTAs per SM so their TMEM columns fit in 512
-    const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::RS_BYTES, tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
+    const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::rs_bytes(sizeof(T)), tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
     e = cudaFuncSetAttribute(k5_resync<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
     if (e != cudaSuccess) return e;
     // at most half the SMs, so the step kernel keeps the rest while the resync runs
