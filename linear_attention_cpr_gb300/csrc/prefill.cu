@@ -29,17 +29,20 @@ namespace cpr {
 
 // ------------------------------------------------------------------------------------
 // k0: chunk index.  One CTA of 1024 threads; each thread owns a contiguous range of
-// sequences.  On invalid cu_seqlens (or too many chunks) every cu_chunks entry is 0,
+// sequences (a shuffle scan gives each range's first chunk).  It also zeroes k23's
+// publication counters.  On invalid cu_seqlens (or too many chunks) every cu_chunks entry is 0,
 // so the later kernels find no chunk, and the status word records why.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) k0_chunk_index(const int32_t* __restrict__ cu, int32_t n_seqs,
                                                       int64_t total_tokens, int32_t C, int64_t capacity,
                                                       int32_t* __restrict__ cu_chunks,
-                                                      uint32_t* __restrict__ status)
+                                                      uint32_t* __restrict__ status, uint32_t* __restrict__ ready,
+                                                      int64_t n_ready)
 {
-    __shared__ long long part[1024];
+    __shared__ long long warp_sum[32];
     __shared__ unsigned bad;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    for (int64_t i = tid; i < n_ready; i += 1024) ready[i] = 0u;  // the chain/item counters of k23
     if (tid == 0) bad = (cu[0] != 0 || (int64_t)cu[n_seqs] != total_tokens) ? CPR_DEV_BAD_CU_SEQLENS : 0u;
     __syncthreads();
     const int per = (n_seqs + 1023) / 1024;
@@ -50,27 +53,39 @@ __global__ void __launch_bounds__(1024) k0_chunk_index(const int32_t* __restrict
         if (L < 0) atomicOr(&bad, CPR_DEV_BAD_CU_SEQLENS);
         s += (L > 0) ? (L + C - 1) / C : 0;
     }
-    part[tid] = s;
+    // exclusive prefix sum of s over the 1024 threads: warp scans, then a scan of the warp sums
+    long long incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
     __syncthreads();
-    if (tid == 0) {
-        long long run = 0;
-        for (int t = 0; t < 1024; ++t) {
-            const long long x = part[t];
-            part[t] = run;
-            run += x;
+    if (wid == 0) {
+        long long w = warp_sum[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += y;
         }
-        if (!bad && run > capacity) bad = CPR_DEV_BOUNDARY_CAPACITY;
-        if (!bad && run > 0x7fffffffLL) bad = CPR_DEV_BOUNDARY_CAPACITY;
+        warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const long long total = warp_sum[31];
+    if (tid == 0) {
+        if (!bad && total > capacity) bad = CPR_DEV_BOUNDARY_CAPACITY;
+        if (!bad && total > 0x7fffffffLL) bad = CPR_DEV_BOUNDARY_CAPACITY;
     }
     __syncthreads();
     const bool ok = (bad == 0);
-    long long run = part[tid];
+    long long run = incl - s + (wid > 0 ? warp_sum[wid - 1] : 0);
     for (int n = n0; n < n1; ++n) {
         cu_chunks[n] = ok ? (int32_t)run : 0;
         const int L = cu[n + 1] - cu[n];
         run += (L > 0) ? (L + C - 1) / C : 0;
     }
-    if (tid == 1023) cu_chunks[n_seqs] = ok ? (int32_t)run : 0;  // part[1023] + its own range = total
+    if (tid == 1023) cu_chunks[n_seqs] = ok ? (int32_t)total : 0;
     if (tid == 0) *status = bad;
 }
 
@@ -676,7 +691,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
 {
     profile_mark(0, s);
     k0_chunk_index<<<1, 1024, 0, s>>>(a.cu_seqlens, a.n_seqs, a.total_tokens, C, a.boundary_capacity,
-                                      a.cu_chunks, a.status);
+                                      a.cu_chunks, a.status, a.ready, (int64_t)a.max_chunks * a.H + 1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     profile_mark(1, s);
@@ -691,8 +706,6 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
     profile_mark(2, s);
 
     using Cf = K2Cfg<DK, DV>;
-    e = cudaMemsetAsync(a.ready, 0, sizeof(uint32_t) * ((size_t)a.max_chunks * a.H + 1), s);  // and the item counter
-    if (e != cudaSuccess) return e;
     auto kern = k23_chain_and_intra<DK, DV, C, T>;
     const size_t sm23 = std::max<size_t>(K23Cfg<DK, DV, C>::bytes, tmem_cap_smem(Cf::TMEM_COLS));
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm23);
