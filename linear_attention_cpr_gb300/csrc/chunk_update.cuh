@@ -166,8 +166,6 @@ struct UCfg {
     static constexpr uint32_t MT_SPLIT = DK * DK * 2;    // bf16 Mt tile [DK][DK], one split
     static constexpr uint32_t MT_BYTES = 2 * MT_SPLIT;
     static constexpr uint32_t BT_BYTES = DK * DV * 4;    // fp32 B [DV][DK]
-    static constexpr uint32_t S_SPLIT = 64 * DK * 2;     // bf16 S tile of one 64-row slice, one split
-    static constexpr int NSLICE = (DV + 63) / 64;        // chain slices of 64 value rows
     // prep shared memory: R1 = keys + A (FP32 phase), later the [W | U~] operand
     static constexpr uint32_t R1A = (uint32_t)(sizeof(float) * ((size_t)C * PrepSmem<DK, C>::KS + (size_t)C * C));
     static constexpr uint32_t mx(uint32_t x, uint32_t y) { return x > y ? x : y; }
@@ -179,12 +177,11 @@ struct UCfg {
     static constexpr uint32_t VEC_OFF = AOP_OFF + AOP_REGION;
     static constexpr uint32_t PREP_BYTES = VEC_OFF + 4 * C * 4;
     static constexpr uint32_t TMEM_COLS = mx(2 * DK, C) <= 32 ? 32 : mx(2 * DK, C) <= 64 ? 64 : mx(2 * DK, C) <= 128 ? 128 : 256;
-    // decode resync (prep and one chain step in one CTA): [R1 | Mt] [Aop | Bt] [vectors] [S tile]
+    // decode resync (prep and one chain step in one CTA): [R1 | Mt] [Aop | Bt] [vectors] [values]
     static constexpr uint32_t up1k(uint32_t x) { return (x + 1023) / 1024 * 1024; }
     static constexpr uint32_t RS_BT_OFF = up1k(R1 > MT_BYTES ? R1 : MT_BYTES);
     static constexpr uint32_t RS_VEC_OFF = up1k(RS_BT_OFF + mx(AOP_REGION, BT_BYTES));
-    static constexpr uint32_t RS_S_OFF = up1k(RS_VEC_OFF + 4 * C * 4);
-    static constexpr uint32_t RS_BAR_OFF = RS_S_OFF + NSLICE * 2 * S_SPLIT;
+    static constexpr uint32_t RS_BAR_OFF = up1k(RS_VEC_OFF + 4 * C * 4);
     static constexpr uint32_t RS_V_OFF = RS_BAR_OFF + 64;  // the chunk's values, as stored
     static constexpr uint32_t rs_bytes(uint32_t value_bytes) { return RS_V_OFF + C * DV * value_bytes; }
     static constexpr uint32_t PREP_BAR_OFF = (PREP_BYTES + 15) / 16 * 16;
@@ -386,42 +383,26 @@ __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsign
 // M = 64 accumulator layout: slice row r -> TMEM lane 32*(r/16) + r%16.
 constexpr int kChainRows = 64;
 
-// S tile of one slice (bf16 splits, A operand: rows r = 0..63 <-> value rows row0 + r,
-// zero beyond DV; K = c) from a stored [DK][DV] fp32 state (NULL = zero), by threads
-// tid = 0 .. nthreads-1.
-template <int DK, int DV>
-__device__ __forceinline__ void stile_fill(unsigned char* stile, const float* src, int row0, int tid, int nthreads)
-{
-    constexpr uint32_t SPLIT = kChainRows * DK * 2;
-    for (int idx = tid; idx < kChainRows * (DK / 8); idx += nthreads) {
-        const int r = idx % kChainRows, c0 = (idx / kChainRows) * 8, i = row0 + r;
-        float xs[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) xs[e] = (src && i < DV) ? src[(size_t)(c0 + e) * DV + i] : 0.0f;
-        const uint32_t off = tc::tile_off<2>(r, c0, DK);
-        tc::split8_store(xs, stile + off, stile + SPLIT + off);
-    }
-}
-
 // One thread: the chain product of one slice, D = S_slice M, into TMEM columns
-// [col, col + DK); commit to mbar when `commit_after`.
+// [tmem_d, tmem_d + DK), with S_slice as the A operand in TMEM (bf16 hi in columns
+// [tmem_a, tmem_a + DK/2), lo in [tmem_a + DK/2, tmem_a + DK), the M = 64 row layout,
+// written by chain_put_a) and the M^T image mt (bf16 hi / lo [DK][DK], K-major) as B;
+// three products hi*hi + hi*lo + lo*hi; commit to mbar.
 template <int DK>
-__device__ __forceinline__ void chain_mma(uint32_t tmem_col, const unsigned char* stile, const unsigned char* mt,
-                                          uint64_t* mbar, bool commit_after = true)
+__device__ __forceinline__ void chain_mma(uint32_t tmem_d, uint32_t tmem_a, const unsigned char* mt, uint64_t* mbar)
 {
-    constexpr uint32_t SBO = (DK / 8) * 128;
-    constexpr uint32_t S_SPLIT = kChainRows * DK * 2, MT_SPLIT = DK * DK * 2;
+    constexpr uint32_t SBO = (DK / 8) * 128, MT_SPLIT = DK * DK * 2;
     constexpr uint32_t idesc = tc::idesc_bf16(kChainRows, DK);
-    const uint32_t so = tc::smem_u32(stile), mo = tc::smem_u32(mt);
-    const uint32_t hs[3] = {0u, 0u, 1u}, hm[3] = {0u, 1u, 0u};
+    const uint32_t mo = tc::smem_u32(mt);
+    const uint32_t ha[3] = {0u, 0u, DK / 2}, hm[3] = {0u, 1u, 0u};
     tc::fence_after_sync();
 #pragma unroll
     for (int p = 0; p < 3; ++p)
 #pragma unroll
         for (int k = 0; k < DK / 16; ++k)
-            tc::mma_bf16(tmem_col, tc::sdesc(so + hs[p] * S_SPLIT + k * 256, 128, SBO),
-                         tc::sdesc(mo + hm[p] * MT_SPLIT + k * 256, 128, SBO), idesc, (p | k) ? 1u : 0u);
-    if (commit_after) tc::commit(mbar);
+            tc::mma_bf16_ta(tmem_d, tmem_a + ha[p] + k * 8, tc::sdesc(mo + hm[p] * MT_SPLIT + k * 256, 128, SBO), idesc,
+                            (p | k) ? 1u : 0u);
+    tc::commit(mbar);
 }
 
 // Epilogue of the chain product of one slice, split across the threads of 4 * WPQ warps:
@@ -497,18 +478,39 @@ __device__ __forceinline__ void chain_values_reg(uint32_t tmem_col, const float 
     for (int e = 0; e < Mp::CPT; ++e) v[e] = __fadd_rn(v[e], b[e]);
 }
 
-// Split this thread's values into the S tile (A operand of the next chain product).
-template <int DK, int WPQ>
-__device__ __forceinline__ void chain_refill(unsigned char* stile, const float (&v)[ChainMap<DK, WPQ>::CPT])
+// This thread's values (the ChainMap layout) of a stored [DK][DV] fp32 state, for the
+// slice starting at value row row0; zeros beyond DV or for a NULL source.
+template <int DK, int DV, int WPQ>
+__device__ __forceinline__ void chain_load_state(const float* src, int row0, float (&v)[ChainMap<DK, WPQ>::CPT])
 {
     using Mp = ChainMap<DK, WPQ>;
-    constexpr uint32_t S_SPLIT = kChainRows * DK * 2;
-    const int r = Mp::row(), c0 = Mp::col0();
+    const int i = row0 + Mp::row(), c0 = Mp::col0();
 #pragma unroll
-    for (int e8 = 0; e8 < Mp::CPT; e8 += 8) {
-        const uint32_t off = tc::tile_off<2>(r, c0 + e8, DK);
-        tc::split8_store(*reinterpret_cast<const float(*)[8]>(v + e8), stile + off, stile + S_SPLIT + off);
+    for (int e = 0; e < Mp::CPT; ++e) v[e] = (src && i < DV) ? src[(size_t)(c0 + e) * DV + i] : 0.0f;
+}
+
+// Write this thread's values as the slice's A operand in TMEM: bf16 hi / lo splits
+// (tc::split_f32, lo truncated to its upper 16 bits), two values per 32-bit column, hi in
+// [tmem_a, tmem_a + DK/2), lo in [tmem_a + DK/2, tmem_a + DK); then wait for the stores.
+template <int DK, int WPQ>
+__device__ __forceinline__ void chain_put_a(uint32_t tmem_a, const float (&v)[ChainMap<DK, WPQ>::CPT])
+{
+    using Mp = ChainMap<DK, WPQ>;
+    constexpr int W = Mp::CPT / 2;
+    uint32_t hi[W], lo[W];
+#pragma unroll
+    for (int e = 0; e < W; ++e) {
+        float h0, l0, h1, l1;
+        tc::split_f32(v[2 * e], h0, l0);
+        tc::split_f32(v[2 * e + 1], h1, l1);
+        hi[e] = tc::pack_upper(h0, h1);
+        lo[e] = tc::pack_upper(l0, l1);
     }
+    const int warp = threadIdx.x >> 5;
+    const uint32_t base = tmem_a + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * (Mp::CPW / 2));
+    tc::tmem_st_16x2<W>(base, hi);
+    tc::tmem_st_16x2<W>(base + DK / 2, lo);
+    tc::tmem_wait_st();
 }
 
 // Store this thread's values into a [DK][DV] state (element (c, row0 + row)).

@@ -168,7 +168,6 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     unsigned char* aop = sm5 + U::RS_BT_OFF;     // then B^T
     unsigned char* mt = sm5;
     float* bt = reinterpret_cast<float*>(sm5 + U::RS_BT_OFF);
-    unsigned char* stile = sm5 + U::RS_S_OFF;
     T* vsm = reinterpret_cast<T*>(sm5 + U::RS_V_OFF);
 
     const int tid = threadIdx.x, H = a.H;
@@ -193,11 +192,7 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
         s.G[tid] = tid < C - 1 ? a.ring.g[bh * C + tid] : a.g[bh];
         s.bs[tid] = tid < C - 1 ? a.ring.beta[bh * C + tid] : a.beta[bh];
     }
-#pragma unroll
-    for (int sl = 0; sl < U::NSLICE; ++sl)
-        stile_fill<DK, DV>(stile + sl * 2 * U::S_SPLIT, a.ring.S_b + bh * SS, sl * kChainRows, tid, (int)blockDim.x);
     tc::fence_before_sync();
-    // also publishes the S tiles
     bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, vsm, (size_t)DV, tmem, mbar, phase);
     if (!ok) return false;
     tc::fence_after_sync();
@@ -207,22 +202,29 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     if (ok) prep_epilogue<DK, DV, C>(tmem, decay_exp(s.G[C - 1]), mt, bt, nullptr);
     __syncthreads();
     if (!ok) return false;
-    // the chain products of prefill, one 64-row slice at a time, into TMEM columns sl*DK
-    if (tid == 0) {
-#pragma unroll
-        for (int sl = 0; sl < U::NSLICE; ++sl)
-            chain_mma<DK>(tmem + sl * DK, stile + sl * 2 * U::S_SPLIT, mt, mbar, sl == U::NSLICE - 1);
-    }
-    ok = __syncthreads_and(tc::mbar_wait(mbar, phase & 1));
-    ++phase;
-    if (!ok) return false;
-    tc::fence_after_sync();
+    // the chain product of prefill's chain CTAs, one 64-row slice at a time: the slice of
+    // ring S_b as the A operand in TMEM columns [DK, 2 DK), the product into [0, DK) (the
+    // prep products' columns are free again)
     constexpr int NW = (DK + DV) / 32, WPQ = NW >= 8 ? 2 : 1;
-#pragma unroll
-    for (int sl = 0; sl < U::NSLICE; ++sl) {
+    for (int sl = 0; sl < (DV + kChainRows - 1) / kChainRows; ++sl) {
+        {
+            float v[ChainMap<DK, WPQ>::CPT];
+            chain_load_state<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
+            tc::fence_after_sync();
+            chain_put_a<DK, WPQ>(tmem + DK, v);
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) chain_mma<DK>(tmem, tmem + DK, mt, mbar);
+        ok = __syncthreads_and(tc::mbar_wait(mbar, phase & 1));
+        ++phase;
+        if (!ok) return false;
+        tc::fence_after_sync();
         float v[ChainMap<DK, WPQ>::CPT];
-        chain_values<DK, DV, WPQ>(tmem + sl * DK, bt + (size_t)sl * kChainRows * DK, sl * kChainRows, v);
+        chain_values<DK, DV, WPQ>(tmem, bt + (size_t)sl * kChainRows * DK, sl * kChainRows, v);
         chain_store<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
+        tc::fence_before_sync();
+        __syncthreads();  // this slice's TMEM reads and S_b reads are done
     }
     tc::fence_before_sync();
     __syncthreads();  // TMEM and shared memory are free for the next pair
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     const int tid = threadIdx.x;
     if (tid < 32) tc::tmem_alloc(tslot, U::TMEM_COLS);
     if (tid == 0) {
-        tc::mbar_init(mbar, 1);  // four phases per pair: kk, Z, prep, chain
+        tc::mbar_init(mbar, 1);  // phases per pair: kk, Z, prep, one per chain slice
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();

@@ -215,8 +215,8 @@ __device__ __forceinline__ int wait_published(const uint32_t* flag, uint32_t tar
 // ------------------------------------------------------------------------------------
 // Boundary chain of one (sequence, head, slice of 64 value rows), by a CTA of 8 warps.
 // Each step, the epilogue warps read the accumulator, add B (loaded from global memory
-// into registers one chunk ahead), refill the bf16-split state tile (A operand of the
-// next product) and arrive on an mbarrier; lane 0 of warp 7 is also the producer: it bulk-copies each chunk's M^T image into one
+// into registers one chunk ahead), write the bf16-split state tile (A operand of the
+// next product) back into TMEM and arrive on an mbarrier; lane 0 of warp 7 is also the producer: it bulk-copies each chunk's M^T image into one
 // of three shared-memory stages two chunks ahead and issues the tcgen05 chain product
 // once every epilogue thread has arrived.  The boundary state is stored while the next
 // product runs and published for the intra-chunk items one step later (so that the
@@ -231,10 +231,10 @@ struct K2Cfg {
     static constexpr uint32_t MT_BYTES = 2 * DK * DK * 2;
     static constexpr int NSTAGE = 3;  // M^T images in flight: the one in use and two ahead
     static constexpr uint32_t STAGE = MT_BYTES;
-    static constexpr uint32_t S_BYTES = 2 * kChainRows * DK * 2;
-    static constexpr uint32_t S_OFF = NSTAGE * STAGE, BAR_OFF = S_OFF + S_BYTES;
+    static constexpr uint32_t BAR_OFF = NSTAGE * STAGE;
     static constexpr uint32_t bytes = BAR_OFF + 64;
-    static constexpr uint32_t TMEM_COLS = DK <= 32 ? 32 : DK <= 64 ? 64 : 128;
+    // TMEM: the accumulator in columns [0, DK), the state tile (A operand) in [DK, 2 DK)
+    static constexpr uint32_t TMEM_COLS = 2 * DK <= 64 ? 64 : 2 * DK <= 128 ? 128 : 256;
     static constexpr uint32_t PIECE = 16384;
     static constexpr int THREADS = 256;
     static constexpr int WPQ = 2;                 // epilogue warps per TMEM lane quadrant
@@ -254,7 +254,6 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
 {
     using Cf = K2Cfg<DK, DV>;
     using Mp = ChainMap<DK, Cf::WPQ>;
-    unsigned char* stile = sm2 + Cf::S_OFF;
     uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(sm2 + Cf::BAR_OFF);  // [NSTAGE] stage landed
     uint64_t* mbar_mma = mbar_ld + Cf::NSTAGE;                           // product done
     uint64_t* mbar_tile = mbar_mma + 1;                                  // state tile ready (EPI arrivals)
@@ -321,17 +320,19 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
         auto produce = [&](int64_t jc) -> bool {  // step jc's product, once its state tile is written
             if (!tc::mbar_wait(mbar_tile, (uint32_t)((G + jc) & 1))) return false;
             if (!tc::mbar_wait(&mbar_ld[(G + jc) % Cf::NSTAGE], ld_parity(jc))) return false;
-            chain_mma<DK>(tmem, stile, sm2 + ((G + jc) % Cf::NSTAGE) * Cf::STAGE, mbar_mma);
+            chain_mma<DK>(tmem, tmem + DK, sm2 + ((G + jc) % Cf::NSTAGE) * Cf::STAGE, mbar_mma);
             if (issued < nfull) issue_load(issued++);  // product jc-1 is done: its stage is free
             return true;
         };
 
         bool pfail = false;
-        stile_fill<DK, DV>(stile, s_in, row0, tid, Cf::THREADS);
-        tc::fence_proxy_async();
-        tc::fence_before_sync();
         float bv[Mp::CPT];
         if (epi) {
+            float v0[Mp::CPT];
+            chain_load_state<DK, DV, Cf::WPQ>(s_in, row0, v0);
+            tc::fence_after_sync();  // the previous chain's products are done (behind a barrier)
+            chain_put_a<DK, Cf::WPQ>(tmem + DK, v0);
+            tc::fence_before_sync();
             tc::mbar_arrive(mbar_tile);
             chain_load_b<DK, DV, Cf::WPQ>(a.bt + ((size_t)cbase * H + h) * SS, row0, bv);
         }
@@ -352,10 +353,7 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
                     tc::fence_after_sync();
                     float v[Mp::CPT];
                     chain_values_reg<DK, Cf::WPQ>(tmem, bv, v);
-                    if (jc + 1 < nfull) {
-                        chain_refill<DK, Cf::WPQ>(stile, v);
-                        tc::fence_proxy_async();
-                    }
+                    if (jc + 1 < nfull) chain_put_a<DK, Cf::WPQ>(tmem + DK, v);
                     tc::fence_before_sync();
                     if (jc + 1 < nfull) tc::mbar_arrive(mbar_tile);
                     // the boundary state completed one step ago: every store to it was issued
