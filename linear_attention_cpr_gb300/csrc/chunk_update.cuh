@@ -150,7 +150,7 @@ __device__ __forceinline__ void chunk_column(const PrepSmem<DK, C>& s, int col, 
 //        B = U0^T Z        (M = 128 rows i, N = DK)
 //        bf16 hi/lo splits of every operand (tc::split_f32), three products
 //        hi*hi + hi*lo + lo*hi accumulated in fp32 in TMEM; Mt is split the same way
-//        (the chain's B operand image), B kept fp32 [DV][DK].
+//        (the chain's B operand image), B kept fp32, stored [DK][DV] like a state.
 //   chain step: D = S_b M as tcgen05 products per 64 value rows (M = 64, N = DK,
 //        K = DK), the state tile holding S_b's bf16 splits, three products as above; then
 //        S_new[i][c] = D[i][c] + B[i][c] (one add).
@@ -165,7 +165,7 @@ struct UCfg {
     static constexpr uint32_t BOP_SPLIT = NB * C * 2;    // bf16 [W | U~]^T tile, one split
     static constexpr uint32_t MT_SPLIT = DK * DK * 2;    // bf16 Mt tile [DK][DK], one split
     static constexpr uint32_t MT_BYTES = 2 * MT_SPLIT;
-    static constexpr uint32_t BT_BYTES = DK * DV * 4;    // fp32 B [DV][DK]
+    static constexpr uint32_t BT_BYTES = DK * DV * 4;    // fp32 B, stored [DK][DV] like a state
     // prep shared memory: R1 = keys + A (FP32 phase), later the [W | U~] operand
     static constexpr uint32_t R1A = (uint32_t)(sizeof(float) * ((size_t)C * PrepSmem<DK, C>::KS + (size_t)C * C));
     static constexpr uint32_t mx(uint32_t x, uint32_t y) { return x > y ? x : y; }
@@ -311,12 +311,12 @@ __device__ __forceinline__ void prep_mma(uint32_t tmem, const unsigned char* aop
 }
 
 // All threads, after the prep products completed: the Mt image (bf16 splits; rows c,
-// K = c') and B (fp32 [DV][DK], 16-byte chunks of row i XOR-swizzled by i % 8 so that the
-// chain epilogue's row-wise reads do not collide in shared-memory banks).  With a
-// shared-memory staging area of at least max(Mt, B) bytes (its previous contents dead),
-// each of the two is assembled there and written to the global destination with bulk
-// copies; without one (staging NULL) they are written directly (shared-memory
-// destinations).  Contains __syncthreads.
+// K = c') and B (fp32, element (i, c) at c * DV + i, the layout of a state).  With a
+// shared-memory staging area of at least Mt's bytes (its previous contents dead), Mt is
+// assembled there and written to the global destination with bulk copies; without one
+// (staging NULL) it is written directly.  B is written directly (consecutive lanes hold
+// consecutive rows i, so each warp store is 128 contiguous bytes).  Contains
+// __syncthreads.
 template <int DK, int DV, int C>
 __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsigned char* mt_out, float* b_out,
                                               unsigned char* staging)
@@ -329,7 +329,7 @@ __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsign
     const int row = q * 32 + lane;  // this thread's TMEM lane
     for (int part = 0; part < 2; ++part) {  // 0: Mt, 1: B
         unsigned char* mt_dst = staging ? staging : mt_out;
-        float* b_dst = staging ? reinterpret_cast<float*>(staging) : b_out;
+        float* b_dst = b_out;
         if (q * 32 < (part == 0 ? DK : DV)) {
             for (int g = warp >> 2; g < NG; g += (nw + 3) / 4) {
                 if ((g < DK / 32) != (part == 0)) continue;
@@ -349,29 +349,22 @@ __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsign
                         const uint32_t off = tc::tile_off<2>(row, col0 + e8, DK);
                         tc::split8_store(xs, mt_dst + off, mt_dst + U::MT_SPLIT + off);
                     }
-                } else {  // B[i][c], row i = this lane; chunk j of the row stored at j ^ (i % 8)
+                } else {  // B[i][c] at c * DV + i, row i = this lane (a warp writes 128 contiguous bytes)
                     if (row >= DV) continue;
-                    float4* dst = reinterpret_cast<float4*>(b_dst + (size_t)row * DK);
+                    float* dst = b_dst + (size_t)(g * 32 - DK) * DV + row;
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const int j = (g * 32 - DK) / 4 + e4;
-                        dst[j ^ (row & 7)] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
-                    }
+                    for (int e = 0; e < 32; ++e) dst[(size_t)e * DV] = v[e];
                 }
             }
         }
-        if (staging) {  // one bulk store of the assembled part, then the staging area is free again
+        if (staging && part == 0) {  // bulk stores of the assembled Mt, in flight while B is stored
             tc::fence_proxy_async();
             __syncthreads();
             if (tid == 0) {
-                const uint32_t bytes = part == 0 ? U::MT_BYTES : U::BT_BYTES;
-                unsigned char* gdst = part == 0 ? mt_out : reinterpret_cast<unsigned char*>(b_out);
-                for (uint32_t off = 0; off < bytes; off += 16384)
-                    tc::bulk_s2g(gdst + off, staging + off, min(16384u, bytes - off));
+                for (uint32_t off = 0; off < U::MT_BYTES; off += 16384)
+                    tc::bulk_s2g(mt_out + off, staging + off, min(16384u, U::MT_BYTES - off));
                 tc::bulk_commit();
-                tc::bulk_wait_read();
             }
-            __syncthreads();
         }
     }
     tc::fence_proxy_async();
@@ -421,48 +414,34 @@ struct ChainMap {
 };
 
 // This thread's values of S_new = D + B (slice row ChainMap::row(), columns col0() ..).
-// bslice: B rows of the slice, swizzled as written by prep_epilogue; rows beyond the
-// slice (value row >= DV) are left as the raw accumulator and must not be stored.
+// b: the chunk's B (element (i, c) at c * DV + i, as prep_epilogue writes it); rows beyond
+// DV are left as the raw accumulator and must not be stored.
 template <int DK, int DV, int WPQ>
-__device__ __forceinline__ void chain_values(uint32_t tmem_col, const float* bslice, int row0,
+__device__ __forceinline__ void chain_values(uint32_t tmem_col, const float* b, int row0,
                                              float (&v)[ChainMap<DK, WPQ>::CPT])
 {
     using Mp = ChainMap<DK, WPQ>;
     const int warp = threadIdx.x >> 5;
     const int q = warp & 3, h = warp >> 2;
     tc::tmem_ld_16x2<Mp::CPT>(tmem_col + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * Mp::CPW), v);
-    const int r = Mp::row(), c0 = Mp::col0();
-    if (row0 + r < DV) {
-        const float4* brow = reinterpret_cast<const float4*>(bslice + (size_t)r * DK);
+    const int i = row0 + Mp::row(), c0 = Mp::col0();
+    if (i < DV) {
 #pragma unroll
-        for (int k = 0; k < Mp::CPT / 4; ++k) {
-            const float4 b = brow[(c0 / 4 + k) ^ (r & 7)];
-            v[4 * k] = __fadd_rn(v[4 * k], b.x);
-            v[4 * k + 1] = __fadd_rn(v[4 * k + 1], b.y);
-            v[4 * k + 2] = __fadd_rn(v[4 * k + 2], b.z);
-            v[4 * k + 3] = __fadd_rn(v[4 * k + 3], b.w);
-        }
+        for (int e = 0; e < Mp::CPT; ++e) v[e] = __fadd_rn(v[e], b[(size_t)(c0 + e) * DV + i]);
     }
 }
 
 // This thread's B values of a slice (row ChainMap::row(), columns col0() ..) read from
-// global memory: bt is a chunk's B (fp32 [DV][DK], 16-byte chunks of row i swizzled by
-// i % 8 as prep_epilogue writes them); rows beyond DV get zeros (never stored).
+// global memory: bt is a chunk's B (element (i, c) at c * DV + i); rows beyond DV get
+// zeros (never stored).
 template <int DK, int DV, int WPQ>
 __device__ __forceinline__ void chain_load_b(const float* __restrict__ bt, int row0,
                                              float (&b)[ChainMap<DK, WPQ>::CPT])
 {
     using Mp = ChainMap<DK, WPQ>;
-    const int r = Mp::row(), c0 = Mp::col0(), i = row0 + r;
+    const int i = row0 + Mp::row(), c0 = Mp::col0();
 #pragma unroll
-    for (int k = 0; k < Mp::CPT / 4; ++k) {
-        const float4 x = i < DV ? __ldg(reinterpret_cast<const float4*>(bt + (size_t)i * DK) + ((c0 / 4 + k) ^ (r & 7)))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        b[4 * k] = x.x;
-        b[4 * k + 1] = x.y;
-        b[4 * k + 2] = x.z;
-        b[4 * k + 3] = x.w;
-    }
+    for (int e = 0; e < Mp::CPT; ++e) b[e] = i < DV ? __ldg(bt + (size_t)(c0 + e) * DV + i) : 0.0f;
 }
 
 // S_new = D + B for this thread's values, B already in registers (as chain_values).

@@ -32,7 +32,7 @@ __host__ __device__ inline int64_t max_chunks_bound(int64_t total_tokens, int32_
 //   cu_chunks      int32 [n_seqs + 1]
 //   mt             [max_chunks, H] tiles of 2 * dk * dk bf16: the chunk's M^T, bf16 hi/lo
 //                  splits, in the tensor cores' shared-memory image
-//   bt             fp32 [max_chunks, H, dv, dk]: the chunk's B
+//   bt             fp32 [max_chunks, H, dk, dv]: the chunk's B (laid out like a state)
 //   ready          uint32 [max_chunks, H]: slices of each boundary state published, then
 //                  one uint32: the next intra-chunk item to claim
 struct PrefillLayout {

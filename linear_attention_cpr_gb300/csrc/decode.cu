@@ -221,7 +221,7 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
         if (!ok) return false;
         tc::fence_after_sync();
         float v[ChainMap<DK, WPQ>::CPT];
-        chain_values<DK, DV, WPQ>(tmem, bt + (size_t)sl * kChainRows * DK, sl * kChainRows, v);
+        chain_values<DK, DV, WPQ>(tmem, bt, sl * kChainRows, v);
         chain_store<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
         tc::fence_before_sync();
         __syncthreads();  // this slice's TMEM reads and S_b reads are done

@@ -101,7 +101,7 @@ template <int DK, int DV, int C, typename T>
 __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
 {
     using U = UCfg<DK, DV, C>;
-    static_assert(U::R1 >= U::MT_BYTES && U::R1 >= U::BT_BYTES, "R1 stages the prep outputs");
+    static_assert(U::R1 >= U::MT_BYTES, "R1 stages the M^T image");
     extern __shared__ __align__(1024) unsigned char sm1[];
     const PrepSmem<DK, C> s(reinterpret_cast<float*>(sm1), reinterpret_cast<float*>(sm1 + U::VEC_OFF));
     constexpr int KS = PrepSmem<DK, C>::KS;
