@@ -171,9 +171,10 @@ int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, 
  * The token is stepped by the same recurrence as prefill; when pos[b] % C == C - 1
  * the state (and ring S_b) become U(ring S_b, ring chunk).  A negative pos[b] skips
  * sequence b and records CPR_DEV_BAD_POS.  workspace >= cpr_gdn_decode_workspace_size.
- * The resync runs on a second stream owned by the library (one per device, created on
- * the first call) that forks from `stream` and joins it again before the call's last
- * kernel: work issued on `stream` after the call sees every result.
+ * The resync (and the step of those sequences' tokens) runs on a second stream owned by
+ * the library (one per device, created on the first call) that forks from `stream` and
+ * joins it again at the end of the call: work issued on `stream` after the call sees
+ * every result.
  */
 int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
                        float* state, const cpr_gdn_ring* ring, const int32_t* pos, int32_t B, int32_t H,

@@ -4,12 +4,14 @@
 // "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet": decode runs the recurrent form
 // and resynchronises the hidden state every C tokens, which keeps its rounding rhythm
 // the same as prefill's.  Kernels, on the caller's stream:
-//   k4_decode_step   the token step of every (sequence, head) on the state in HBM (the
-//                    same per-element operations as prefill's intra-chunk kernel), the
-//                    output, and the token's slot in the ring
-//   k5_resync        for sequences whose token completed a chunk: U(ring S_b, ring
-//                    chunk) by the same routines as prefill's chunk prep and chain;
-//                    the result replaces both the state and ring S_b
+//   k4_decode_step   the token step of every (sequence, head) whose token does not
+//                    complete a chunk, on the state in HBM (the same per-element
+//                    operations as prefill's intra-chunk kernel): the output, the new
+//                    state and the token's slot in the ring
+//   k5_resync        on a second stream, for sequences whose token completes a chunk:
+//                    the token's output by the same operations, then U(ring S_b, ring
+//                    chunk) by the same routines as prefill's chunk prep and chain; the
+//                    result replaces both the state and ring S_b
 //   k6_ring_fill     builds a ring from a prefill's results
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -62,7 +64,8 @@ struct VecF<4> {
 // k4: decode step.  One CTA per (sequence, head), 8 warps: warp m owns key rows
 // [m*DK/8, (m+1)*DK/8) of the stored state (chain m of the canonical dot) and lane l
 // owns value columns [l*DV/32, (l+1)*DV/32).  Partial chains meet in shared memory and
-// every value column's dot is finished by the canonical tree.
+// every value column's dot is finished by the canonical tree.  Sequences whose token
+// completes a chunk are left to k5 (their stepped state is replaced by the resync).
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C, typename T>
 __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
@@ -82,6 +85,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
         return;
     }
     const int r = p % C;
+    if (r == C - 1) return;  // k5 steps this token and resynchronises the state
     const size_t bh = (size_t)b * H + h;
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
@@ -153,10 +157,55 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 // the key Gram product, the FP32 phase and the prep products of k1_chunk_prep
 // (prep_operands, prep_mma, prep_epilogue, here into shared memory), then the chain
 // products and epilogue of the chain role (chain_mma, chain_values) on the ring's S_b.
-// The result replaces ring S_b only; k7 copies it into the state once k4 is done (k4
-// reads and writes the state meanwhile).  The chunk's last token is read from the step's
-// inputs, since k4 writes its ring slot at the same time.
+// The result replaces ring S_b and the state.  The chunk's last token (this step's) is
+// read from the step's inputs; k4 leaves these sequences alone.
 // ------------------------------------------------------------------------------------
+
+// The output of this step's token for (b, h), from the state before the step, by the
+// element sequence of k4 (per value column i: the eight chains of S k as fmul then fma
+// over their DK/8 rows, the canonical tree, u, then the chains of S' q over the stepped
+// rows).  Threads i < DV take column i; the stepped state itself is not kept.  kf, qf:
+// DK floats of shared scratch each, part: 8 * DV.  Ends with a barrier.
+template <int DK, int DV, int C, typename T>
+__device__ __forceinline__ void completing_token_output(const DecodeArgs& a, size_t bh, float* kf, float* qf,
+                                                        float* part)
+{
+    constexpr int L = DK / 8;
+    const int tid = threadIdx.x;
+    const T* q = static_cast<const T*>(a.q);
+    const T* k = static_cast<const T*>(a.k);
+    for (int idx = tid; idx < DK; idx += blockDim.x) {
+        kf[idx] = to_f32<T>(k[bh * DK + idx]);
+        qf[idx] = to_f32<T>(q[bh * DK + idx]);
+    }
+    __syncthreads();
+    if (tid < DV) {
+        const int i = tid;
+        const float* S = a.state + bh * DK * DV + i;  // S[c][i] at c * DV
+        const float alpha = decay_exp(a.g[bh]), beta = a.beta[bh];
+        float* c = part + i;  // chain m at c[m * DV]
+#pragma unroll 1
+        for (int m = 0; m < 8; ++m) {
+            float acc = __fmul_rn(S[(size_t)(m * L) * DV], kf[m * L]);
+#pragma unroll
+            for (int t = 1; t < L; ++t) acc = __fmaf_rn(S[(size_t)(m * L + t) * DV], kf[m * L + t], acc);
+            c[m * DV] = acc;
+        }
+        const float x = tree8(c[0], c[DV], c[2 * DV], c[3 * DV], c[4 * DV], c[5 * DV], c[6 * DV], c[7 * DV]);
+        const float u = step_u(alpha, beta, to_f32<T>(static_cast<const T*>(a.v)[bh * DV + i]), x);
+#pragma unroll 1
+        for (int m = 0; m < 8; ++m) {
+            float acc = __fmul_rn(step_s(S[(size_t)(m * L) * DV], alpha, u, kf[m * L]), qf[m * L]);
+#pragma unroll
+            for (int t = 1; t < L; ++t)
+                acc = __fmaf_rn(step_s(S[(size_t)(m * L + t) * DV], alpha, u, kf[m * L + t]), qf[m * L + t], acc);
+            c[m * DV] = acc;
+        }
+        const float o = tree8(c[0], c[DV], c[2 * DV], c[3 * DV], c[4 * DV], c[5 * DV], c[6 * DV], c[7 * DV]);
+        static_cast<T*>(a.out)[bh * DV + i] = from_f32<T>(o);
+    }
+    __syncthreads();  // every read of the old state is done before the resync replaces it
+}
 template <int DK, int DV, int C, typename T>
 __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, unsigned char* sm5, uint32_t tmem,
                                            uint64_t* mbar, uint32_t& phase)
@@ -179,6 +228,8 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     // the step kernel writes its ring slot concurrently
     const T* tk = static_cast<const T*>(a.k) + bh * DK;
     const T* tv = static_cast<const T*>(a.v) + bh * DV;
+    completing_token_output<DK, DV, C, T>(a, bh, reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5) + DK,
+                                          reinterpret_cast<float*>(sm5) + 2 * DK);
 
     for (int idx = tid; idx < C * DK; idx += blockDim.x) {
         const int r = idx / DK, j = idx % DK;
@@ -223,6 +274,7 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
         float v[ChainMap<DK, WPQ>::CPT];
         chain_values<DK, DV, WPQ>(tmem, bt, sl * kChainRows, v);
         chain_store<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
+        chain_store<DK, DV, WPQ>(a.state + bh * SS, sl * kChainRows, v);
         tc::fence_before_sync();
         __syncthreads();  // this slice's TMEM reads and S_b reads are done
     }
@@ -347,22 +399,6 @@ __global__ void __launch_bounds__(256) k6_ring_fill(RingArgs a)
     }
 }
 
-// ------------------------------------------------------------------------------------
-// k7: resync commit.  One CTA per (sequence, head): for a sequence whose token completed a
-// chunk, state <- ring S_b (the resynchronised state).
-// ------------------------------------------------------------------------------------
-template <int DK, int DV, int C>
-__global__ void __launch_bounds__(256) k7_resync_commit(DecodeArgs a)
-{
-    const int b = blockIdx.x, h = blockIdx.y;
-    const int p = a.pos[b];
-    if (p < 0 || p % C != C - 1) return;
-    const size_t off = ((size_t)b * a.H + h) * DK * DV;
-    const float4* src = reinterpret_cast<const float4*>(a.ring.S_b + off);
-    float4* dst = reinterpret_cast<float4*>(a.state + off);
-    for (int i = threadIdx.x; i < DK * DV / 4; i += blockDim.x) dst[i] = src[i];
-}
-
 namespace {
 // Per-device side stream and fork/join events of the decode launch (created on first use).
 struct SideStream {
@@ -409,13 +445,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     k4_decode_step<DK, DV, C, T><<<dim3(a.B, a.H), 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_mark(1, s);
-    // join, then the resynchronised states replace the stepped ones
+    // join: work issued on s after this call sees the resync's results
     if ((e = cudaEventRecord(ss->join, ss->stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(s, ss->join, 0)) != cudaSuccess) return e;
-    k7_resync_commit<DK, DV, C><<<dim3(a.B, a.H), 256, 0, s>>>(a);
-    e = cudaGetLastError();
     profile_mark(2, s);
-    return e;
+    return cudaSuccess;
 }
 
 template <int DK, int DV, int C, typename T>
