@@ -242,11 +242,10 @@ struct K2Cfg {
 };
 
 // Publish one slice of a boundary state: the CTA's stores to it were issued before a
-// barrier this thread has passed; the fence orders them before the count.
+// barrier this thread has passed; the release orders them before the count.
 __device__ __forceinline__ void publish(uint32_t* flag)
 {
-    __threadfence();
-    atomicAdd(flag, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(flag) : "memory");
 }
 
 template <int DK, int DV, int C, typename T>
@@ -258,10 +257,11 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
     uint64_t* mbar_mma = mbar_ld + Cf::NSTAGE;                           // product done
     uint64_t* mbar_tile = mbar_mma + 1;                                  // state tile ready (EPI arrivals)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_tile + 1);
-    volatile int* mma_ok = reinterpret_cast<volatile int*>(tslot + 1);  // thread 0's wait result
+    volatile int* mma_ok = reinterpret_cast<volatile int*>(tslot + 1);  // [2] thread 0's wait results, by step parity
 
     const int H = a.H, tid = threadIdx.x, warp = tid >> 5;
     const bool producer = (tid == Cf::THREADS - 32);
+    const bool publisher = (tid == 32);  // neither the poller (thread 0) nor in the producer's warp
     const bool epi = tid < Cf::EPI;
     const size_t SS = (size_t)DK * DV;
     if (warp == 0) tc::tmem_alloc(tslot, Cf::TMEM_COLS);
@@ -302,7 +302,7 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
         }
         copy_slice(a.boundary + ((size_t)cbase * H + h) * SS);
         __syncthreads();
-        if (tid == 0) publish(ready);
+        if (publisher) publish(ready);
         if (nfull == 0) continue;
 
         // producer (one thread): M^T stage loads and the chain products
@@ -341,47 +341,43 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
             pfail = !produce(0);
         }
         __syncwarp();
+        // A wait that times out ends the chain for every thread: the producer then issues no
+        // product, so thread 0's wait for it times out too and every thread reads the same
+        // result after the barrier.
+        bool ok = true;
         for (int64_t jc = 0; jc < nfull; ++jc) {
-            bool ok = !pfail;
             if (epi) {
                 // one thread polls the product's mbarrier, the epilogue meets it at a hardware
                 // barrier (polling by every warp would compete with the product for shared memory)
-                if (tid == 0) *mma_ok = tc::mbar_wait(mbar_mma, (uint32_t)((G + jc) & 1)) ? 1 : 0;
+                if (tid == 0) mma_ok[jc & 1] = tc::mbar_wait(mbar_mma, (uint32_t)((G + jc) & 1)) ? 1 : 0;
                 named_bar(1, Cf::EPI);
-                ok = ok && *mma_ok != 0;
-                if (*mma_ok) {
-                    tc::fence_after_sync();
-                    float v[Mp::CPT];
-                    chain_values_reg<DK, Cf::WPQ>(tmem, bv, v);
-                    if (jc + 1 < nfull) chain_put_a<DK, Cf::WPQ>(tmem + DK, v);
-                    tc::fence_before_sync();
-                    if (jc + 1 < nfull) tc::mbar_arrive(mbar_tile);
-                    // the boundary state completed one step ago: every store to it was issued
-                    // before the last barrier (published before this thread's next loads, which
-                    // the fence would otherwise wait for)
-                    if (tid == 0 && jc >= 1) publish(ready + (size_t)jc * H);
-                    if (jc + 1 < nfull) {
-                        // the producer issues the next product before its own loads and stores
-                        if (producer) pfail = !produce(jc + 1);
-                        __syncwarp();
-                        chain_load_b<DK, DV, Cf::WPQ>(a.bt + ((size_t)(cbase + jc + 1) * H + h) * SS, row0, bv);
-                    }
-                    float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS
-                                                : a.state_out + nh * SS;
-                    chain_store<DK, DV, Cf::WPQ>(dst, row0, v);
+                ok = mma_ok[jc & 1] != 0;
+                if (!ok) break;
+                tc::fence_after_sync();
+                float v[Mp::CPT];
+                chain_values_reg<DK, Cf::WPQ>(tmem, bv, v);
+                if (jc + 1 < nfull) chain_put_a<DK, Cf::WPQ>(tmem + DK, v);
+                tc::fence_before_sync();
+                if (jc + 1 < nfull) tc::mbar_arrive(mbar_tile);
+                // the boundary state completed one step ago: every store to it was issued
+                // before the barrier above
+                if (publisher && jc >= 1) publish(ready + (size_t)jc * H);
+                if (jc + 1 < nfull) {
+                    // the producer issues the next product before its own loads and stores
+                    if (producer) pfail = !produce(jc + 1);
+                    __syncwarp();
+                    chain_load_b<DK, DV, Cf::WPQ>(a.bt + ((size_t)(cbase + jc + 1) * H + h) * SS, row0, bv);
                 }
-            } else if (producer && ok && jc + 1 < nfull) {  // (epilogue warps include the producer when DK >= 64)
+                float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS
+                                            : a.state_out + nh * SS;
+                chain_store<DK, DV, Cf::WPQ>(dst, row0, v);
+            } else if (producer && jc + 1 < nfull) {  // (epilogue warps include the producer when DK >= 64)
                 pfail = !produce(jc + 1);
             }
-            __syncwarp();
-            // one vote per step: a wait timed out somewhere (the CTA stops: its mbarrier
-            // phases are unknown) or the step's stores are all issued
-            if (__syncthreads_or(!ok || pfail)) {
-                failed = true;
-                break;
-            }
         }
-        if (!failed && tid == 0 && nfull < nch) publish(ready + (size_t)nfull * H);
+        // the last step's stores are issued; every thread holds the same ok
+        failed = __syncthreads_or(!ok || pfail) != 0;
+        if (!failed && publisher && nfull < nch) publish(ready + (size_t)nfull * H);
         if (failed && producer) {  // let copies still in flight land before the CTA exits
             for (int64_t jc = 0; jc < issued; ++jc)
                 tc::mbar_wait(&mbar_ld[(G + jc) % Cf::NSTAGE], ld_parity(jc), 1u << 16);
