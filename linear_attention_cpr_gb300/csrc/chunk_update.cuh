@@ -151,9 +151,9 @@ __device__ __forceinline__ void chunk_column(const PrepSmem<DK, C>& s, int col, 
 //        bf16 hi/lo splits of every operand (tc::split_f32), three products
 //        hi*hi + hi*lo + lo*hi accumulated in fp32 in TMEM; Mt is split the same way
 //        (the chain's B operand image), B kept fp32, stored [DK][DV] like a state.
-//   chain step: D = S_b M as tcgen05 products per 64 value rows (M = 64, N = DK,
-//        K = DK), the state tile holding S_b's bf16 splits, three products as above; then
-//        S_new[i][c] = D[i][c] + B[i][c] (one add).
+//   chain step: D = S_b M as one tcgen05 product per (sequence, head) (M = 128 value
+//        rows, N = DK, K = DK), the state tile holding S_b's bf16 splits, three products
+//        as above; then S_new[i][c] = D[i][c] + B[i][c] (one add).
 // Both products have a fixed instruction sequence, so prefill's kernels and decode's
 // resync produce the same bits.  Rows beyond DK (or DV) of the M = 128 products are zero.
 // ======================================================================================
@@ -371,16 +371,16 @@ __device__ __forceinline__ void prep_epilogue(uint32_t tmem, float gamma, unsign
     tc::fence_before_sync();
 }
 
-// The chain product is issued per slice of 64 value rows (M = 64), in prefill (one CTA
-// per slice) and in decode's resync alike, so both run the same instruction shape.
-// M = 64 accumulator layout: slice row r -> TMEM lane 32*(r/16) + r%16.
-constexpr int kChainRows = 64;
+// The chain product: one M = 128 product per (sequence, head), value row i in TMEM lane i
+// (rows beyond DV read a zero state tile and are never stored), the same instruction
+// shape in prefill's chain CTAs and in decode's resync.
+constexpr int kChainRows = 128;
 
-// One thread: the chain product of one slice, D = S_slice M, into TMEM columns
-// [tmem_d, tmem_d + DK), with S_slice as the A operand in TMEM (bf16 hi in columns
-// [tmem_a, tmem_a + DK/2), lo in [tmem_a + DK/2, tmem_a + DK), the M = 64 row layout,
-// written by chain_put_a) and the M^T image mt (bf16 hi / lo [DK][DK], K-major) as B;
-// three products hi*hi + hi*lo + lo*hi; commit to mbar.
+// One thread: the chain product D = S M into TMEM columns [tmem_d, tmem_d + DK), with S as
+// the A operand in TMEM (bf16 hi in columns [tmem_a, tmem_a + DK/2), lo in
+// [tmem_a + DK/2, tmem_a + DK), row i in lane i, written by chain_put_a) and the M^T
+// image mt (bf16 hi / lo [DK][DK], K-major) as B; three products hi*hi + hi*lo + lo*hi;
+// commit to mbar.
 template <int DK>
 __device__ __forceinline__ void chain_mma(uint32_t tmem_d, uint32_t tmem_a, const unsigned char* mt, uint64_t* mbar)
 {
@@ -398,106 +398,119 @@ __device__ __forceinline__ void chain_mma(uint32_t tmem_d, uint32_t tmem_a, cons
     tc::commit(mbar);
 }
 
-// Epilogue of the chain product of one slice, split across the threads of 4 * WPQ warps:
-// warp w covers slice rows 16 (w % 4) .. +15 and columns [(w / 4) CPW, +CPW); thread t of
-// the warp takes row 16 (w % 4) + t % 16 and CPT consecutive columns from
-// (w / 4) CPW + (t / 16) CPT (the tcgen05.ld 16x32bx2 layout of an M = 64 accumulator).
-template <int DK, int WPQ>
+// Epilogue of the chain product across NW warps: warp w reads TMEM lane quadrant w % 4
+// (rows 32 (w % 4) .. +31, one per lane) and column part w / QW of CP parts; thread t takes
+// row 32 ((t / 32) % 4) + t % 32 and the CPT consecutive columns from (t / 32 / QW) CPT.
+// With fewer than four warps only the first NW quadrants (rows < 32 NW) are covered.
+template <int DK, int NW>
 struct ChainMap {
-    static constexpr int CPW = DK / WPQ;
-    static constexpr int CPT = CPW / 2;
-    static __device__ __forceinline__ int row() { return 16 * ((threadIdx.x >> 5) & 3) + (threadIdx.x & 15); }
-    static __device__ __forceinline__ int col0()
-    {
-        return (int)(threadIdx.x >> 7) * CPW + (int)((threadIdx.x >> 4) & 1) * CPT;
-    }
+    static constexpr int QW = NW < 4 ? NW : 4;
+    static constexpr int CP = NW / QW;
+    static constexpr int CPT = DK / CP;                    // values per thread
+    static constexpr int BLK = CPT < 32 ? CPT : 32;        // columns per tcgen05.ld 32x32b
+    static constexpr int ROWS = 32 * QW;                   // rows covered
+    static_assert(CPT % 16 == 0 && CPT % BLK == 0, "whole 32x32b blocks of paired columns");
+    static __device__ __forceinline__ int row(int t) { return 32 * ((t >> 5) & 3) + (t & 31); }
+    static __device__ __forceinline__ int col0(int t) { return ((t >> 5) / QW) * CPT; }
+    static __device__ __forceinline__ uint32_t lanes(int t) { return (uint32_t)(((t >> 5) & 3) * 32) << 16; }
 };
 
-// This thread's values of S_new = D + B (slice row ChainMap::row(), columns col0() ..).
-// b: the chunk's B (element (i, c) at c * DV + i, as prep_epilogue writes it); rows beyond
-// DV are left as the raw accumulator and must not be stored.
-template <int DK, int DV, int WPQ>
-__device__ __forceinline__ void chain_values(uint32_t tmem_col, const float* b, int row0,
-                                             float (&v)[ChainMap<DK, WPQ>::CPT])
+// This thread's accumulator values from TMEM columns at tmem_col.
+template <int DK, int NW>
+__device__ __forceinline__ void chain_acc(uint32_t tmem_col, int t, float (&v)[ChainMap<DK, NW>::CPT])
 {
-    using Mp = ChainMap<DK, WPQ>;
-    const int warp = threadIdx.x >> 5;
-    const int q = warp & 3, h = warp >> 2;
-    tc::tmem_ld_16x2<Mp::CPT>(tmem_col + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * Mp::CPW), v);
-    const int i = row0 + Mp::row(), c0 = Mp::col0();
+    using Mp = ChainMap<DK, NW>;
+#pragma unroll
+    for (int b = 0; b < Mp::CPT / Mp::BLK; ++b) {
+        float x[Mp::BLK];
+        tc::tmem_ld_32x32b<Mp::BLK>(tmem_col + Mp::lanes(t) + (uint32_t)(Mp::col0(t) + b * Mp::BLK), x);
+#pragma unroll
+        for (int e = 0; e < Mp::BLK; ++e) v[b * Mp::BLK + e] = x[e];
+    }
+}
+
+// This thread's values of S_new = D + B (row ChainMap::row(t), its columns).  b: the
+// chunk's B (element (i, c) at c * DV + i, as prep_epilogue writes it); rows beyond DV are
+// left as the raw accumulator and must not be stored.
+template <int DK, int DV, int NW>
+__device__ __forceinline__ void chain_values(uint32_t tmem_col, const float* b, int t,
+                                             float (&v)[ChainMap<DK, NW>::CPT])
+{
+    using Mp = ChainMap<DK, NW>;
+    chain_acc<DK, NW>(tmem_col, t, v);
+    const int i = Mp::row(t), c0 = Mp::col0(t);
     if (i < DV) {
 #pragma unroll
         for (int e = 0; e < Mp::CPT; ++e) v[e] = __fadd_rn(v[e], b[(size_t)(c0 + e) * DV + i]);
     }
 }
 
-// This thread's B values of a slice (row ChainMap::row(), columns col0() ..) read from
-// global memory: bt is a chunk's B (element (i, c) at c * DV + i); rows beyond DV get
-// zeros (never stored).
-template <int DK, int DV, int WPQ>
-__device__ __forceinline__ void chain_load_b(const float* __restrict__ bt, int row0,
-                                             float (&b)[ChainMap<DK, WPQ>::CPT])
+// This thread's B values read from global memory: bt is a chunk's B (element (i, c) at
+// c * DV + i); rows beyond DV get zeros (never stored).
+template <int DK, int DV, int NW>
+__device__ __forceinline__ void chain_load_b(const float* __restrict__ bt, int t, float (&b)[ChainMap<DK, NW>::CPT])
 {
-    using Mp = ChainMap<DK, WPQ>;
-    const int i = row0 + Mp::row(), c0 = Mp::col0();
+    using Mp = ChainMap<DK, NW>;
+    const int i = Mp::row(t), c0 = Mp::col0(t);
 #pragma unroll
     for (int e = 0; e < Mp::CPT; ++e) b[e] = i < DV ? __ldg(bt + (size_t)(c0 + e) * DV + i) : 0.0f;
 }
 
 // S_new = D + B for this thread's values, B already in registers (as chain_values).
-template <int DK, int WPQ>
-__device__ __forceinline__ void chain_values_reg(uint32_t tmem_col, const float (&b)[ChainMap<DK, WPQ>::CPT],
-                                                 float (&v)[ChainMap<DK, WPQ>::CPT])
+template <int DK, int NW>
+__device__ __forceinline__ void chain_values_reg(uint32_t tmem_col, int t, const float (&b)[ChainMap<DK, NW>::CPT],
+                                                 float (&v)[ChainMap<DK, NW>::CPT])
 {
-    using Mp = ChainMap<DK, WPQ>;
-    const int warp = threadIdx.x >> 5;
-    const int q = warp & 3, h = warp >> 2;
-    tc::tmem_ld_16x2<Mp::CPT>(tmem_col + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * Mp::CPW), v);
+    using Mp = ChainMap<DK, NW>;
+    chain_acc<DK, NW>(tmem_col, t, v);
 #pragma unroll
     for (int e = 0; e < Mp::CPT; ++e) v[e] = __fadd_rn(v[e], b[e]);
 }
 
-// This thread's values (the ChainMap layout) of a stored [DK][DV] fp32 state, for the
-// slice starting at value row row0; zeros beyond DV or for a NULL source.
-template <int DK, int DV, int WPQ>
-__device__ __forceinline__ void chain_load_state(const float* src, int row0, float (&v)[ChainMap<DK, WPQ>::CPT])
+// This thread's values of a stored [DK][DV] fp32 state; zeros beyond DV or for a NULL
+// source.
+template <int DK, int DV, int NW>
+__device__ __forceinline__ void chain_load_state(const float* src, int t, float (&v)[ChainMap<DK, NW>::CPT])
 {
-    using Mp = ChainMap<DK, WPQ>;
-    const int i = row0 + Mp::row(), c0 = Mp::col0();
+    using Mp = ChainMap<DK, NW>;
+    const int i = Mp::row(t), c0 = Mp::col0(t);
 #pragma unroll
     for (int e = 0; e < Mp::CPT; ++e) v[e] = (src && i < DV) ? src[(size_t)(c0 + e) * DV + i] : 0.0f;
 }
 
-// Write this thread's values as the slice's A operand in TMEM: bf16 hi / lo splits
-// (tc::split_f32, lo truncated to its upper 16 bits), two values per 32-bit column, hi in
+// Write this thread's values as its row of the A operand in TMEM: bf16 hi / lo splits
+// (tc::split_f32, lo truncated to its upper 16 bits), two values per 32-bit column (the
+// value of column c in TMEM column c / 2, even c in the low half), hi in
 // [tmem_a, tmem_a + DK/2), lo in [tmem_a + DK/2, tmem_a + DK); then wait for the stores.
-template <int DK, int WPQ>
-__device__ __forceinline__ void chain_put_a(uint32_t tmem_a, const float (&v)[ChainMap<DK, WPQ>::CPT])
+template <int DK, int NW>
+__device__ __forceinline__ void chain_put_a(uint32_t tmem_a, int t, const float (&v)[ChainMap<DK, NW>::CPT])
 {
-    using Mp = ChainMap<DK, WPQ>;
-    constexpr int W = Mp::CPT / 2;
-    uint32_t hi[W], lo[W];
+    using Mp = ChainMap<DK, NW>;
+    constexpr int W = Mp::BLK / 2;
 #pragma unroll
-    for (int e = 0; e < W; ++e) {
-        float h0, l0, h1, l1;
-        tc::split_f32(v[2 * e], h0, l0);
-        tc::split_f32(v[2 * e + 1], h1, l1);
-        hi[e] = tc::pack_upper(h0, h1);
-        lo[e] = tc::pack_upper(l0, l1);
+    for (int b = 0; b < Mp::CPT / Mp::BLK; ++b) {
+        uint32_t hi[W], lo[W];
+#pragma unroll
+        for (int e = 0; e < W; ++e) {
+            float h0, l0, h1, l1;
+            tc::split_f32(v[b * Mp::BLK + 2 * e], h0, l0);
+            tc::split_f32(v[b * Mp::BLK + 2 * e + 1], h1, l1);
+            hi[e] = tc::pack_upper(h0, h1);
+            lo[e] = tc::pack_upper(l0, l1);
+        }
+        const uint32_t base = tmem_a + Mp::lanes(t) + (uint32_t)((Mp::col0(t) + b * Mp::BLK) / 2);
+        tc::tmem_st_32x32b<W>(base, hi);
+        tc::tmem_st_32x32b<W>(base + DK / 2, lo);
     }
-    const int warp = threadIdx.x >> 5;
-    const uint32_t base = tmem_a + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * (Mp::CPW / 2));
-    tc::tmem_st_16x2<W>(base, hi);
-    tc::tmem_st_16x2<W>(base + DK / 2, lo);
     tc::tmem_wait_st();
 }
 
-// Store this thread's values into a [DK][DV] state (element (c, row0 + row)).
-template <int DK, int DV, int WPQ>
-__device__ __forceinline__ void chain_store(float* dst, int row0, const float (&v)[ChainMap<DK, WPQ>::CPT])
+// Store this thread's values into a [DK][DV] state (element (c, row)).
+template <int DK, int DV, int NW>
+__device__ __forceinline__ void chain_store(float* dst, int t, const float (&v)[ChainMap<DK, NW>::CPT])
 {
-    using Mp = ChainMap<DK, WPQ>;
-    const int i = row0 + Mp::row(), c0 = Mp::col0();
+    using Mp = ChainMap<DK, NW>;
+    const int i = Mp::row(t), c0 = Mp::col0(t);
     if (i >= DV) return;
 #pragma unroll
     for (int e = 0; e < Mp::CPT; ++e) dst[(size_t)(c0 + e) * DV + i] = v[e];

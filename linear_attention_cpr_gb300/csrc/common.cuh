@@ -33,7 +33,7 @@ __host__ __device__ inline int64_t max_chunks_bound(int64_t total_tokens, int32_
 //   mt             [max_chunks, H] tiles of 2 * dk * dk bf16: the chunk's M^T, bf16 hi/lo
 //                  splits, in the tensor cores' shared-memory image
 //   bt             fp32 [max_chunks, H, dk, dv]: the chunk's B (laid out like a state)
-//   ready          uint32 [max_chunks, H]: slices of each boundary state published, then
+//   ready          uint32 [max_chunks, H]: publications of each boundary state, then
 //                  one uint32: the next intra-chunk item to claim
 struct PrefillLayout {
     size_t cu_chunks, mt, bt, ready, total, mt_bytes, bt_bytes;

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 // (found from pos), DK + DV threads per CTA.  Each pair runs the same routines as prefill:
 // the key Gram product, the FP32 phase and the prep products of k1_chunk_prep
 // (prep_operands, prep_mma, prep_epilogue, here into shared memory), then the chain
-// products and epilogue of the chain role (chain_mma, chain_values) on the ring's S_b.
+// product and epilogue of the chain role (chain_mma, chain_values) on the ring's S_b.
 // The result replaces ring S_b and the state.  The chunk's last token (this step's) is
 // read from the step's inputs; k4 leaves these sequences alone.
 // ------------------------------------------------------------------------------------
@@ -253,30 +253,28 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     if (ok) prep_epilogue<DK, DV, C>(tmem, decay_exp(s.G[C - 1]), mt, bt, nullptr);
     __syncthreads();
     if (!ok) return false;
-    // the chain product of prefill's chain CTAs, one 64-row slice at a time: the slice of
-    // ring S_b as the A operand in TMEM columns [DK, 2 DK), the product into [0, DK) (the
-    // prep products' columns are free again)
-    constexpr int NW = (DK + DV) / 32, WPQ = NW >= 8 ? 2 : 1;
-    for (int sl = 0; sl < (DV + kChainRows - 1) / kChainRows; ++sl) {
-        {
-            float v[ChainMap<DK, WPQ>::CPT];
-            chain_load_state<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
-            tc::fence_after_sync();
-            chain_put_a<DK, WPQ>(tmem + DK, v);
-        }
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) chain_mma<DK>(tmem, tmem + DK, mt, mbar);
-        ok = __syncthreads_and(tc::mbar_wait(mbar, phase & 1));
-        ++phase;
-        if (!ok) return false;
+    // the chain product of prefill's chain CTAs: ring S_b as the A operand in TMEM columns
+    // [DK, 2 DK), the product into [0, DK) (the prep products' columns are free again)
+    constexpr int NW = (DK + DV) / 32;
+    static_assert(ChainMap<DK, NW>::ROWS >= DV, "the warps cover every value row");
+    {
+        float v[ChainMap<DK, NW>::CPT];
+        chain_load_state<DK, DV, NW>(a.ring.S_b + bh * SS, tid, v);
         tc::fence_after_sync();
-        float v[ChainMap<DK, WPQ>::CPT];
-        chain_values<DK, DV, WPQ>(tmem, bt, sl * kChainRows, v);
-        chain_store<DK, DV, WPQ>(a.ring.S_b + bh * SS, sl * kChainRows, v);
-        chain_store<DK, DV, WPQ>(a.state + bh * SS, sl * kChainRows, v);
-        tc::fence_before_sync();
-        __syncthreads();  // this slice's TMEM reads and S_b reads are done
+        chain_put_a<DK, NW>(tmem + DK, tid, v);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) chain_mma<DK>(tmem, tmem + DK, mt, mbar);
+    ok = __syncthreads_and(tc::mbar_wait(mbar, phase & 1));
+    ++phase;
+    if (!ok) return false;
+    tc::fence_after_sync();
+    {
+        float v[ChainMap<DK, NW>::CPT];
+        chain_values<DK, DV, NW>(tmem, bt, tid, v);
+        chain_store<DK, DV, NW>(a.ring.S_b + bh * SS, tid, v);
+        chain_store<DK, DV, NW>(a.state + bh * SS, tid, v);
     }
     tc::fence_before_sync();
     __syncthreads();  // TMEM and shared memory are free for the next pair
@@ -327,7 +325,7 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     const int tid = threadIdx.x;
     if (tid < 32) tc::tmem_alloc(tslot, U::TMEM_COLS);
     if (tid == 0) {
-        tc::mbar_init(mbar, 1);  // phases per pair: kk, Z, prep, one per chain slice
+        tc::mbar_init(mbar, 1);  // phases per pair: kk, Z, prep, chain
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();

@@ -9,8 +9,8 @@
 //                    G, decays, A, and W, U~ by forward substitution
 //   k23_chain_and_intra  one cooperative launch with two roles:
 //                    chain CTAs: the state-dependent half of U, sequential over each
-//                    sequence's chunks, one CTA per (sequence, head, slice of value rows)
-//                    at a time: every boundary state (and state_out when L is a multiple
+//                    sequence's chunks, one CTA per (sequence, head) at a time: every
+//                    boundary state (and state_out when L is a multiple
 //                    of C), each published as soon as it is stored;
 //                    item groups: the token recurrence inside every chunk from its
 //                    boundary state, one group of DV threads per (chunk, head), one thread
@@ -173,9 +173,9 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
 
 // ------------------------------------------------------------------------------------
 // Hand-off between the chain CTAs and the intra-chunk items of one launch.
-// ready[c * H + h] counts the slices of chunk c's boundary state (head h) that are
-// stored; a chain CTA's threads fence their stores, meet at a barrier, and one thread
-// adds 1.  All CTAs of the launch are resident (cooperative launch) and chain CTAs wait
+// ready[c * H + h] counts the publications of chunk c's boundary state (head h): a chain
+// CTA's threads issue their stores, meet at a barrier, and one thread adds 1 with release
+// semantics.  All CTAs of the launch are resident (cooperative launch) and chain CTAs wait
 // on nothing but their own copies and products, so every wait below ends; it is still
 // bounded (about 4 s) and reports a timeout instead of hanging.
 // ------------------------------------------------------------------------------------
@@ -213,21 +213,21 @@ __device__ __forceinline__ int wait_published(const uint32_t* flag, uint32_t tar
 }
 
 // ------------------------------------------------------------------------------------
-// Boundary chain of one (sequence, head, slice of 64 value rows), by a CTA of 8 warps.
-// Each step, the epilogue warps read the accumulator, add B (loaded from global memory
-// into registers one chunk ahead), write the bf16-split state tile (A operand of the
-// next product) back into TMEM and arrive on an mbarrier; lane 0 of warp 7 is also the producer: it bulk-copies each chunk's M^T image into one
-// of three shared-memory stages two chunks ahead and issues the tcgen05 chain product
-// once every epilogue thread has arrived.  The boundary state is stored while the next
-// product runs and published for the intra-chunk items one step later (so that the
-// publishing fence waits for nothing).  All waits are bounded; a timeout is reported in
-// the status word.  Slices are independent: each value row evolves alone.  A chain CTA
-// runs its chains one after another; its mbarrier phases continue across them.
+// Boundary chain of one (sequence, head), by a CTA of 8 warps.  Each step, the epilogue
+// warps read the accumulator (value row i in TMEM lane i), add B (loaded from global
+// memory into registers one chunk ahead), write the bf16-split state tile back into TMEM
+// and arrive on an mbarrier; lane 0 of warp 7 is also the producer: it bulk-copies each
+// chunk's M^T image into one of three shared-memory stages two chunks ahead and issues the
+// tcgen05 chain product (M = 128) once every epilogue thread has arrived.  The boundary
+// state is stored while the next product runs and published for the intra-chunk items one
+// step later by a thread that neither polls nor produces.  All waits are bounded; a
+// timeout is reported in the status word.  A chain CTA runs its chains one after another;
+// its mbarrier phases continue across them.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV>
 struct K2Cfg {
-    static constexpr int ROWS = DV < kChainRows ? DV : kChainRows;  // value rows of one slice
-    static constexpr int NSLICE = (DV + kChainRows - 1) / kChainRows;
+    static_assert(DV <= kChainRows, "one chain product covers every value row");
+    static constexpr int NSLICE = 1;  // publications per boundary state
     static constexpr uint32_t MT_BYTES = 2 * DK * DK * 2;
     static constexpr int NSTAGE = 3;  // M^T images in flight: the one in use and two ahead
     static constexpr uint32_t STAGE = MT_BYTES;
@@ -237,12 +237,11 @@ struct K2Cfg {
     static constexpr uint32_t TMEM_COLS = 2 * DK <= 64 ? 64 : 2 * DK <= 128 ? 128 : 256;
     static constexpr uint32_t PIECE = 16384;
     static constexpr int THREADS = 256;
-    static constexpr int WPQ = 2;                 // epilogue warps per TMEM lane quadrant
-    static constexpr int EPI = 4 * WPQ * 32;      // epilogue threads
+    static constexpr int NW = THREADS / 32;  // epilogue warps (all)
 };
 
-// Publish one slice of a boundary state: the CTA's stores to it were issued before a
-// barrier this thread has passed; the release orders them before the count.
+// Publish a boundary state: the CTA's stores to it were issued before a barrier this
+// thread has passed; the release orders them before the count.
 __device__ __forceinline__ void publish(uint32_t* flag)
 {
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(flag) : "memory");
@@ -252,23 +251,22 @@ template <int DK, int DV, int C, typename T>
 __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* sm2, int cta, int ncta)
 {
     using Cf = K2Cfg<DK, DV>;
-    using Mp = ChainMap<DK, Cf::WPQ>;
+    using Mp = ChainMap<DK, Cf::NW>;
     uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(sm2 + Cf::BAR_OFF);  // [NSTAGE] stage landed
     uint64_t* mbar_mma = mbar_ld + Cf::NSTAGE;                           // product done
-    uint64_t* mbar_tile = mbar_mma + 1;                                  // state tile ready (EPI arrivals)
+    uint64_t* mbar_tile = mbar_mma + 1;                                  // state tile ready (all threads)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_tile + 1);
     volatile int* mma_ok = reinterpret_cast<volatile int*>(tslot + 1);  // [2] thread 0's wait results, by step parity
 
     const int H = a.H, tid = threadIdx.x, warp = tid >> 5;
     const bool producer = (tid == Cf::THREADS - 32);
     const bool publisher = (tid == 32);  // neither the poller (thread 0) nor in the producer's warp
-    const bool epi = tid < Cf::EPI;
     const size_t SS = (size_t)DK * DV;
     if (warp == 0) tc::tmem_alloc(tslot, Cf::TMEM_COLS);
     if (tid == 0) {
         for (int b = 0; b < Cf::NSTAGE; ++b) tc::mbar_init(&mbar_ld[b], 1);
         tc::mbar_init(mbar_mma, 1);
-        tc::mbar_init(mbar_tile, Cf::EPI);
+        tc::mbar_init(mbar_tile, Cf::THREADS);
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -278,10 +276,9 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
 
     int64_t G = 0;  // chain steps this CTA has run: the phase count of its mbarriers
     bool failed = false;
-    const int nchains = a.n_seqs * H * Cf::NSLICE;
+    const int nchains = a.n_seqs * H;
     for (int ci = cta; ci < nchains && !failed; ci += ncta) {
-        const int sl = ci % Cf::NSLICE, nh_idx = ci / Cf::NSLICE;
-        const int n = nh_idx / H, h = nh_idx % H, row0 = sl * kChainRows;
+        const int n = ci / H, h = ci % H;
         const int64_t t0 = a.cu_seqlens[n];
         const int64_t L = a.cu_seqlens[n + 1] - t0;
         const int64_t nfull = L / C, nch = a.cu_chunks[n + 1] - a.cu_chunks[n], cbase = a.cu_chunks[n];
@@ -289,18 +286,14 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
         const float* s_in = a.state_in ? a.state_in + nh * SS : nullptr;
         uint32_t* ready = a.ready + (size_t)cbase * H + h;  // + jc * H for chunk cbase + jc
 
-        // this slice's columns of the stored states: element (c, row0 + r)
-        auto copy_slice = [&](float* dst) {
-            for (int idx = tid; idx < DK * Cf::ROWS; idx += Cf::THREADS) {
-                const int c = idx / Cf::ROWS, r = idx % Cf::ROWS;
-                dst[(size_t)c * DV + row0 + r] = s_in ? s_in[(size_t)c * DV + row0 + r] : 0.0f;
-            }
+        auto copy_state = [&](float* dst) {
+            for (size_t idx = tid; idx < SS; idx += Cf::THREADS) dst[idx] = s_in ? s_in[idx] : 0.0f;
         };
         if (L == 0) {  // empty sequence: state_out = state_in
-            copy_slice(a.state_out + nh * SS);
+            copy_state(a.state_out + nh * SS);
             continue;
         }
-        copy_slice(a.boundary + ((size_t)cbase * H + h) * SS);
+        copy_state(a.boundary + ((size_t)cbase * H + h) * SS);
         __syncthreads();
         if (publisher) publish(ready);
         if (nfull == 0) continue;
@@ -327,14 +320,14 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
 
         bool pfail = false;
         float bv[Mp::CPT];
-        if (epi) {
+        {
             float v0[Mp::CPT];
-            chain_load_state<DK, DV, Cf::WPQ>(s_in, row0, v0);
+            chain_load_state<DK, DV, Cf::NW>(s_in, tid, v0);
             tc::fence_after_sync();  // the previous chain's products are done (behind a barrier)
-            chain_put_a<DK, Cf::WPQ>(tmem + DK, v0);
+            chain_put_a<DK, Cf::NW>(tmem + DK, tid, v0);
             tc::fence_before_sync();
             tc::mbar_arrive(mbar_tile);
-            chain_load_b<DK, DV, Cf::WPQ>(a.bt + ((size_t)cbase * H + h) * SS, row0, bv);
+            chain_load_b<DK, DV, Cf::NW>(a.bt + ((size_t)cbase * H + h) * SS, tid, bv);
         }
         if (producer) {
             for (; issued < Cf::NSTAGE - 1 && issued < nfull; ++issued) issue_load(issued);
@@ -346,34 +339,30 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
         // result after the barrier.
         bool ok = true;
         for (int64_t jc = 0; jc < nfull; ++jc) {
-            if (epi) {
-                // one thread polls the product's mbarrier, the epilogue meets it at a hardware
-                // barrier (polling by every warp would compete with the product for shared memory)
-                if (tid == 0) mma_ok[jc & 1] = tc::mbar_wait(mbar_mma, (uint32_t)((G + jc) & 1)) ? 1 : 0;
-                named_bar(1, Cf::EPI);
-                ok = mma_ok[jc & 1] != 0;
-                if (!ok) break;
-                tc::fence_after_sync();
-                float v[Mp::CPT];
-                chain_values_reg<DK, Cf::WPQ>(tmem, bv, v);
-                if (jc + 1 < nfull) chain_put_a<DK, Cf::WPQ>(tmem + DK, v);
-                tc::fence_before_sync();
-                if (jc + 1 < nfull) tc::mbar_arrive(mbar_tile);
-                // the boundary state completed one step ago: every store to it was issued
-                // before the barrier above
-                if (publisher && jc >= 1) publish(ready + (size_t)jc * H);
-                if (jc + 1 < nfull) {
-                    // the producer issues the next product before its own loads and stores
-                    if (producer) pfail = !produce(jc + 1);
-                    __syncwarp();
-                    chain_load_b<DK, DV, Cf::WPQ>(a.bt + ((size_t)(cbase + jc + 1) * H + h) * SS, row0, bv);
-                }
-                float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS
-                                            : a.state_out + nh * SS;
-                chain_store<DK, DV, Cf::WPQ>(dst, row0, v);
-            } else if (producer && jc + 1 < nfull) {  // (epilogue warps include the producer when DK >= 64)
-                pfail = !produce(jc + 1);
+            // one thread polls the product's mbarrier, the others meet it at a hardware
+            // barrier (polling by every warp would compete with the product for shared memory)
+            if (tid == 0) mma_ok[jc & 1] = tc::mbar_wait(mbar_mma, (uint32_t)((G + jc) & 1)) ? 1 : 0;
+            __syncthreads();
+            ok = mma_ok[jc & 1] != 0;
+            if (!ok) break;
+            tc::fence_after_sync();
+            float v[Mp::CPT];
+            chain_values_reg<DK, Cf::NW>(tmem, tid, bv, v);
+            if (jc + 1 < nfull) chain_put_a<DK, Cf::NW>(tmem + DK, tid, v);
+            tc::fence_before_sync();
+            if (jc + 1 < nfull) tc::mbar_arrive(mbar_tile);
+            // the boundary state completed one step ago: every store to it was issued before
+            // the barrier above
+            if (publisher && jc >= 1) publish(ready + (size_t)jc * H);
+            if (jc + 1 < nfull) {
+                // the producer issues the next product before its own loads and stores
+                if (producer) pfail = !produce(jc + 1);
+                __syncwarp();
+                chain_load_b<DK, DV, Cf::NW>(a.bt + ((size_t)(cbase + jc + 1) * H + h) * SS, tid, bv);
             }
+            float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS
+                                        : a.state_out + nh * SS;
+            chain_store<DK, DV, Cf::NW>(dst, tid, v);
         }
         // the last step's stores are issued; every thread holds the same ok
         failed = __syncthreads_or(!ok || pfail) != 0;
@@ -578,8 +567,8 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
         al[tid] = decay_exp(a.g[(t0 + tid) * H + hd]);
         bt[tid] = a.beta[(t0 + tid) * H + hd];
     }
-    // the chunk's boundary state comes from the chain CTAs of this launch: wait until
-    // every slice of it is published (bounded)
+    // the chunk's boundary state comes from the chain CTAs of this launch: wait until it is
+    // published (bounded)
     __shared__ int wait_ok[8];
     const int gi = bar - 1;
     if (tid == 0) wait_ok[gi] = wait_published(a.ready + (size_t)c * H + hd, (uint32_t)K2Cfg<DK, DV>::NSLICE, a.status);
@@ -709,7 +698,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
     if (e != cudaSuccess) return e;
     if (per_sm < 1 || a.num_sms < 2) return cudaErrorInvalidConfiguration;
     const int grid = per_sm * a.num_sms;
-    const int chains = a.n_seqs * a.H * Cf::NSLICE;
+    const int chains = a.n_seqs * a.H;
     const int n_chain = std::max(1, std::min(chains, grid / 4));
     PrefillArgs args = a;
     int nc = n_chain;
