@@ -429,22 +429,6 @@ __device__ __forceinline__ void chain_acc(uint32_t tmem_col, int t, float (&v)[C
     }
 }
 
-// This thread's values of S_new = D + B (row ChainMap::row(t), its columns).  b: the
-// chunk's B (element (i, c) at c * DV + i, as prep_epilogue writes it); rows beyond DV are
-// left as the raw accumulator and must not be stored.
-template <int DK, int DV, int NW>
-__device__ __forceinline__ void chain_values(uint32_t tmem_col, const float* b, int t,
-                                             float (&v)[ChainMap<DK, NW>::CPT])
-{
-    using Mp = ChainMap<DK, NW>;
-    chain_acc<DK, NW>(tmem_col, t, v);
-    const int i = Mp::row(t), c0 = Mp::col0(t);
-    if (i < DV) {
-#pragma unroll
-        for (int e = 0; e < Mp::CPT; ++e) v[e] = __fadd_rn(v[e], b[(size_t)(c0 + e) * DV + i]);
-    }
-}
-
 // This thread's B values read from global memory: bt is a chunk's B (element (i, c) at
 // c * DV + i); rows beyond DV get zeros (never stored).
 template <int DK, int DV, int NW>
@@ -503,6 +487,51 @@ __device__ __forceinline__ void chain_put_a(uint32_t tmem_a, int t, const float 
         tc::tmem_st_32x32b<W>(base + DK / 2, lo);
     }
     tc::tmem_wait_st();
+}
+
+// Block b of this thread's values (columns col0 + b BLK .. + BLK) of a stored [DK][DV]
+// state written as its part of the A operand: the blockwise form of chain_load_state and
+// chain_put_a (fewer live registers; the same values and TMEM contents).
+template <int DK, int DV, int NW>
+__device__ __forceinline__ void chain_put_state_block(const float* src, uint32_t tmem_a, int t, int b)
+{
+    using Mp = ChainMap<DK, NW>;
+    constexpr int W = Mp::BLK / 2;
+    const int i = Mp::row(t), c0 = Mp::col0(t) + b * Mp::BLK;
+    float v[Mp::BLK];
+#pragma unroll
+    for (int e = 0; e < Mp::BLK; ++e) v[e] = (src && i < DV) ? src[(size_t)(c0 + e) * DV + i] : 0.0f;
+    uint32_t hi[W], lo[W];
+#pragma unroll
+    for (int e = 0; e < W; ++e) {
+        float h0, l0, h1, l1;
+        tc::split_f32(v[2 * e], h0, l0);
+        tc::split_f32(v[2 * e + 1], h1, l1);
+        hi[e] = tc::pack_upper(h0, h1);
+        lo[e] = tc::pack_upper(l0, l1);
+    }
+    const uint32_t base = tmem_a + Mp::lanes(t) + (uint32_t)(c0 / 2);
+    tc::tmem_st_32x32b<W>(base, hi);
+    tc::tmem_st_32x32b<W>(base + DK / 2, lo);
+}
+
+// Block b of this thread's values of S_new = D + B (B element (i, c) at c * DV + i),
+// stored into two [DK][DV] states: the blockwise form of chain_values and chain_store.
+template <int DK, int DV, int NW>
+__device__ __forceinline__ void chain_store_block(uint32_t tmem_col, const float* bsrc, float* dst0, float* dst1, int t,
+                                                  int b)
+{
+    using Mp = ChainMap<DK, NW>;
+    const int i = Mp::row(t), c0 = Mp::col0(t) + b * Mp::BLK;
+    float v[Mp::BLK];
+    tc::tmem_ld_32x32b<Mp::BLK>(tmem_col + Mp::lanes(t) + (uint32_t)c0, v);
+    if (i >= DV) return;
+#pragma unroll
+    for (int e = 0; e < Mp::BLK; ++e) {
+        const float x = __fadd_rn(v[e], bsrc[(size_t)(c0 + e) * DV + i]);
+        dst0[(size_t)(c0 + e) * DV + i] = x;
+        dst1[(size_t)(c0 + e) * DV + i] = x;
+    }
 }
 
 // Store this thread's values into a [DK][DV] state (element (c, row)).

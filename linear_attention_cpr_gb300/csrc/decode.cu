@@ -257,12 +257,11 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     // [DK, 2 DK), the product into [0, DK) (the prep products' columns are free again)
     constexpr int NW = (DK + DV) / 32;
     static_assert(ChainMap<DK, NW>::ROWS >= DV, "the warps cover every value row");
-    {
-        float v[ChainMap<DK, NW>::CPT];
-        chain_load_state<DK, DV, NW>(a.ring.S_b + bh * SS, tid, v);
-        tc::fence_after_sync();
-        chain_put_a<DK, NW>(tmem + DK, tid, v);
-    }
+    constexpr int NB = ChainMap<DK, NW>::CPT / ChainMap<DK, NW>::BLK;  // column blocks per thread
+    tc::fence_after_sync();
+#pragma unroll 1
+    for (int b = 0; b < NB; ++b) chain_put_state_block<DK, DV, NW>(a.ring.S_b + bh * SS, tmem + DK, tid, b);
+    tc::tmem_wait_st();
     tc::fence_before_sync();
     __syncthreads();
     if (tid == 0) chain_mma<DK>(tmem, tmem + DK, mt, mbar);
@@ -270,12 +269,9 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     ++phase;
     if (!ok) return false;
     tc::fence_after_sync();
-    {
-        float v[ChainMap<DK, NW>::CPT];
-        chain_values<DK, DV, NW>(tmem, bt, tid, v);
-        chain_store<DK, DV, NW>(a.ring.S_b + bh * SS, tid, v);
-        chain_store<DK, DV, NW>(a.state + bh * SS, tid, v);
-    }
+#pragma unroll 1
+    for (int b = 0; b < NB; ++b)
+        chain_store_block<DK, DV, NW>(tmem, bt, a.ring.S_b + bh * SS, a.state + bh * SS, tid, b);
     tc::fence_before_sync();
     __syncthreads();  // TMEM and shared memory are free for the next pair
     tc::fence_after_sync();

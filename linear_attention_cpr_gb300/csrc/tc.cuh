@@ -230,39 +230,6 @@ __device__ __forceinline__ void tmem_st_32x32b<32>(uint32_t taddr, const uint32_
                  : "memory");
 }
 
-// tcgen05.st 16x32bx2 with N 32-bit columns per half: thread t of the warp writes TMEM
-// lane (quadrant base + t % 16), columns [taddr_col + (t / 16) * N, + N) (the layout of
-// tmem_ld_16x2).  The caller waits with tmem_wait_st() before the data is used.
-template <int N>
-__device__ __forceinline__ void tmem_st_16x2(uint32_t taddr, const uint32_t (&r)[N]);
-
-template <>
-__device__ __forceinline__ void tmem_st_16x2<4>(uint32_t taddr, const uint32_t (&r)[4])
-{
-    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x4.b32 [%0], 4, {%1,%2,%3,%4};\n" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
-                 "r"(r[2]), "r"(r[3])
-                 : "memory");
-}
-
-template <>
-__device__ __forceinline__ void tmem_st_16x2<8>(uint32_t taddr, const uint32_t (&r)[8])
-{
-    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], 8, {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-
-template <>
-__device__ __forceinline__ void tmem_st_16x2<16>(uint32_t taddr, const uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
-            taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 // tcgen05.mma kind::f16 with the A operand in TMEM (same lanes as the accumulator rows;
