@@ -34,8 +34,8 @@ L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
 # of the kernel as it now stands: k23_chain_and_intra at trainer_fwd, k4_decode_step at
 # rollout_decode.  Reset to None whenever the kernel changes.
-TRAFFIC_K23_TRAINER_FWD = 571.400448e6 + 199.158784e6
-TRAFFIC_K4_ROLLOUT_DECODE = 271.847168e6 + 210.993664e6
+TRAFFIC_K23_TRAINER_FWD = 462.891008e6 + 180.198144e6
+TRAFFIC_K4_ROLLOUT_DECODE = 267.599872e6 + 206.738176e6
 
 
 def _peaks():
