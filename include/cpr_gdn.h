@@ -182,6 +182,34 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
                        size_t workspace_bytes, void* stream);
 
 /*
+ * Continuation prefill (a rollout's chunked prefill): every sequence n continues from
+ * absolute position pos0[n] with the state and ring that decode (or an earlier prefill
+ * with cpr_gdn_ring_from_prefill) left, and receives the L_n = cu_seqlens[n + 1] -
+ * cu_seqlens[n] tokens at positions pos0[n] .. pos0[n] + L_n - 1.  The results are those
+ * of decode run token by token over the same tokens, bit for bit (and so those of one
+ * prefill over each whole sequence):
+ *   - the first tokens, up to the end of the chunk that pos0[n] lies in (none when pos0[n]
+ *     is a multiple of C), are stepped from `state` by decode's token step and go to the
+ *     ring; a chunk they complete is resynchronised as in decode;
+ *   - the remaining tokens, which start at a chunk boundary, run as in cpr_gdn_prefill from
+ *     the resulting state; boundary_states receives the start states of their chunks,
+ *     indexed as cpr_gdn_prefill indexes chunks of those remainders (its capacity counts
+ *     their chunks, cpr_gdn_num_chunks of the remaining lengths);
+ *   - `state` and the ring end as decode leaves them at position pos0[n] + L_n.
+ *   q, k, v, g, beta, cu_seqlens (DEVICE), out: as in cpr_gdn_prefill
+ *   pos0   int32 [n_seqs] DEVICE, >= 0
+ *   state  fp32 [n_seqs, H, dk, dv] in/out;  ring in/out (B = n_seqs)
+ * workspace >= cpr_gdn_prefill_workspace_size(total_tokens, n_seqs, H, dk, dv, C).  A
+ * negative pos0[n] records CPR_DEV_BAD_POS in the workspace's status word and the call
+ * then leaves every output as it was.
+ */
+int32_t cpr_gdn_prefill_continue(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                 const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
+                                 int32_t dk, int32_t dv, int32_t C, int32_t dtype, const int32_t* pos0, float* state,
+                                 const cpr_gdn_ring* ring, void* out, float* boundary_states,
+                                 int64_t boundary_capacity, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Prefill for callers that cannot allocate device memory.  (The pages have no
  * counterpart of this entry point; it belongs to this library's interface only.)
  *

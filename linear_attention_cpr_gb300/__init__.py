@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     cpr_gdn_device_status,
     cpr_gdn_num_chunks,
     cpr_gdn_prefill,
+    cpr_gdn_prefill_continue,
     cpr_gdn_prefill_noalloc,
     cpr_gdn_prefill_workspace_size,
     cpr_gdn_ring_from_prefill,
@@ -21,5 +22,6 @@ from .binding import (  # noqa: F401
     cpr_gdn_strerror,
     cpr_gdn_supported,
     cpr_gdn_version,
+    continue_chunks,
     load_library,
 )

@@ -25,7 +25,7 @@ EXPORTED = (
     "cpr_gdn_supported", "cpr_gdn_version", "cpr_gdn_strerror", "cpr_gdn_num_chunks",
     "cpr_gdn_prefill_workspace_size", "cpr_gdn_decode_workspace_size", "cpr_gdn_prefill",
     "cpr_gdn_ring_from_prefill", "cpr_gdn_decode", "cpr_gdn_device_status", "cpr_gdn_set_profile_events",
-    "cpr_gdn_prefill_noalloc",
+    "cpr_gdn_prefill_noalloc", "cpr_gdn_prefill_continue",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # CPR_GDN_NOALLOC_SCRATCH_BYTES
 
@@ -76,6 +76,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         "cpr_gdn_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
         "cpr_gdn_set_profile_events": (I32, [ctypes.POINTER(ctypes.c_void_p), I32]),
         "cpr_gdn_prefill_noalloc": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P, P, P, I64, P]),
+        "cpr_gdn_prefill_continue": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P,
+                                           ctypes.POINTER(_Ring), P, P, I64, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -211,6 +213,47 @@ def cpr_gdn_ring_from_prefill(k, v, g, beta, cu_seqlens, C: int, boundary_states
         _ptr(boundary_states), _ptr(state_out), ctypes.byref(rc), _stream(stream))
     _check("cpr_gdn_ring_from_prefill", code)
     return ring
+
+
+def continue_chunks(cu_seqlens_host, pos0_host, C: int) -> int:
+    """Chunks of the remainders of a continuation (what its boundary_states must hold)."""
+    cu = [int(x) for x in cu_seqlens_host]
+    p0 = [int(x) for x in pos0_host]
+    n = 0
+    for i in range(len(cu) - 1):
+        L = cu[i + 1] - cu[i]
+        f = 0 if p0[i] % C == 0 else min(C - p0[i] % C, L)
+        n += -(-(L - f) // C)
+    return n
+
+
+def cpr_gdn_prefill_continue(q, k, v, g, beta, cu_seqlens, pos0, C: int, state, ring: Ring, *, out=None,
+                             boundary_states=None, workspace=None, n_chunks: int | None = None, stream=None):
+    """Continuation prefill: each sequence continues from absolute position pos0[n] with
+    ``state`` and ``ring`` (updated in place).  Returns (out, boundary_states, workspace).
+
+    ``cu_seqlens`` and ``pos0`` are int32 CUDA tensors; ``n_chunks`` (the remainders' chunk
+    count) is read from host copies of both when not given and boundary_states is None.
+    """
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    if out is None:
+        out = torch.empty(T, H, dv, dtype=q.dtype, device=dev)
+    if boundary_states is None:
+        if n_chunks is None:
+            n_chunks = continue_chunks(cu_seqlens.cpu(), pos0.cpu(), C)
+        boundary_states = torch.empty(max(n_chunks, 1), H, dk, dv, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(cpr_gdn_prefill_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
+    rc = ring._c()
+    code = load_library().cpr_gdn_prefill_continue(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, C, _dtype_code(q),
+        _ptr(pos0), _ptr(state), ctypes.byref(rc), _ptr(out), _ptr(boundary_states), boundary_states.shape[0],
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("cpr_gdn_prefill_continue", code)
+    return out, boundary_states, workspace
 
 
 def cpr_gdn_decode(q, k, v, g, beta, state, ring: Ring, pos, C: int, *, out=None, workspace=None, stream=None):

@@ -118,7 +118,7 @@ int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float
         if (p && !aligned(p, 4)) return CPR_ERR_MISALIGNED;
 
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    PrefillArgs a;
+    PrefillArgs a{};
     a.q = q;
     a.k = k;
     a.v = v;
@@ -157,6 +157,67 @@ int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float
     return from_cuda(e);
 }
 
+int32_t cpr_gdn_prefill_continue(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                 const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
+                                 int32_t dk, int32_t dv, int32_t C, int32_t dtype, const int32_t* pos0, float* state,
+                                 const cpr_gdn_ring* ring, void* out, float* boundary_states,
+                                 int64_t boundary_capacity, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype) ||
+        boundary_capacity < 0)
+        return CPR_ERR_INVALID_ARG;
+    if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
+    if (n_seqs == 0) return CPR_OK;
+    if (!cu_seqlens || !pos0 || !state || !workspace || !boundary_states || !ring || !ring->S_b || !ring->k ||
+        !ring->v || !ring->g || !ring->beta)
+        return CPR_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return CPR_ERR_INVALID_ARG;
+    const PrefillLayout lay(total_tokens, n_seqs, H, dk, dv, C);
+    if (workspace_bytes < lay.total) return CPR_ERR_WORKSPACE;
+    const void* a16[] = {q, k, v, out, state, boundary_states, workspace, ring->S_b, ring->k, ring->v};
+    for (const void* p : a16)
+        if (p && !aligned(p, 16)) return CPR_ERR_MISALIGNED;
+    const void* a4[] = {g, beta, cu_seqlens, pos0, ring->g, ring->beta};
+    for (const void* p : a4)
+        if (p && !aligned(p, 4)) return CPR_ERR_MISALIGNED;
+
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    PrefillArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.cu_seqlens = cu_seqlens;
+    a.skip = reinterpret_cast<const int32_t*>(ws + lay.skip);
+    a.n_seqs = n_seqs;
+    a.total_tokens = total_tokens;
+    a.H = H;
+    a.state_in = state;
+    a.out = out;
+    a.state_out = state;
+    a.boundary = boundary_states;
+    a.boundary_capacity = boundary_capacity;
+    a.ws = ws;
+    a.status = reinterpret_cast<uint32_t*>(ws);
+    a.cu_chunks = reinterpret_cast<int32_t*>(ws + lay.cu_chunks);
+    a.mt = ws + lay.mt;
+    a.bt = reinterpret_cast<float*>(ws + lay.bt);
+    a.ready = reinterpret_cast<uint32_t*>(ws + lay.ready);
+    a.num_sms = num_sms();
+    if (a.num_sms <= 0) return CPR_ERR_CUDA;
+    a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorInvalidValue;
+#define CPR_DISPATCH(DK, DV, CC)                                                                             \
+    if (dk == DK && dv == DV && C == CC)                                                                     \
+        e = (dtype == CPR_DTYPE_BF16) ? launch_prefill_continue<DK, DV, CC, __nv_bfloat16>(a, pos0, state, *ring, s) \
+                                      : launch_prefill_continue<DK, DV, CC, float>(a, pos0, state, *ring, s);
+    CPR_FOR_EACH_SHAPE(CPR_DISPATCH)
+#undef CPR_DISPATCH
+    return from_cuda(e);
+}
+
 int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, const float* beta,
                                   const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
                                   int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* boundary_states,
@@ -175,7 +236,7 @@ int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, 
     const void* a4[] = {g, beta, cu_seqlens, ring->g, ring->beta};
     for (const void* p : a4)
         if (p && !aligned(p, 4)) return CPR_ERR_MISALIGNED;
-    RingArgs a;
+    RingArgs a{};
     a.k = k;
     a.v = v;
     a.g = g;
@@ -216,7 +277,7 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
     const void* a4[] = {g, beta, pos, ring->g, ring->beta};
     for (const void* p : a4)
         if (!aligned(p, 4)) return CPR_ERR_MISALIGNED;
-    DecodeArgs a;
+    DecodeArgs a{};
     a.q = q;
     a.k = k;
     a.v = v;

@@ -35,8 +35,10 @@ __host__ __device__ inline int64_t max_chunks_bound(int64_t total_tokens, int32_
 //   bt             fp32 [max_chunks, H, dk, dv]: the chunk's B (laid out like a state)
 //   ready          uint32 [max_chunks, H]: publications of each boundary state, then
 //                  one uint32: the next intra-chunk item to claim
+//   skip, pos_last int32 [n_seqs] each (continuation only): tokens that fill each
+//                  sequence's current chunk, and the position of the last of them (-1: none)
 struct PrefillLayout {
-    size_t cu_chunks, mt, bt, ready, total, mt_bytes, bt_bytes;
+    size_t cu_chunks, mt, bt, ready, skip, pos_last, total, mt_bytes, bt_bytes;
     __host__ __device__ PrefillLayout(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk, int32_t dv,
                                       int32_t C)
     {
@@ -47,7 +49,9 @@ struct PrefillLayout {
         mt = align_up(cu_chunks + sizeof(int32_t) * (size_t)(n_seqs + 1), kAlign);
         bt = align_up(mt + mt_bytes * (size_t)mc * H, kAlign);
         ready = align_up(bt + bt_bytes * (size_t)mc * H, kAlign);
-        total = align_up(ready + sizeof(uint32_t) * ((size_t)mc * H + 1), kAlign);
+        skip = align_up(ready + sizeof(uint32_t) * ((size_t)mc * H + 1), kAlign);
+        pos_last = align_up(skip + sizeof(int32_t) * (size_t)n_seqs, kAlign);
+        total = align_up(pos_last + sizeof(int32_t) * (size_t)n_seqs, kAlign);
     }
 };
 
@@ -58,6 +62,7 @@ struct PrefillArgs {
     const float* g;
     const float* beta;
     const int32_t* cu_seqlens;
+    const int32_t* skip;  // NULL, or tokens of each sequence already consumed (continuation)
     int32_t n_seqs;
     int64_t total_tokens;
     int32_t H;
@@ -93,6 +98,7 @@ struct DecodeArgs {
     void* out;
     uint32_t* status;
     int num_sms;
+    int resync_only;  // continuation: every token of a completed chunk is in the ring, no output
 };
 
 struct RingArgs {
@@ -101,6 +107,8 @@ struct RingArgs {
     const float* g;
     const float* beta;
     const int32_t* cu_seqlens;
+    const int32_t* skip;      // as PrefillArgs::skip
+    const uint32_t* status;   // NULL, or a status word: nonzero means do nothing
     int32_t n_seqs;
     int64_t total_tokens;
     int32_t H;
@@ -108,6 +116,13 @@ struct RingArgs {
     const float* state_out;
     cpr_gdn_ring ring;
 };
+
+// First token of sequence n's part of a batch: cu_seqlens[n], plus skip[n] when a
+// continuation has already consumed that many of its tokens.
+__device__ __forceinline__ int64_t seq_begin(const int32_t* cu, const int32_t* skip, int n)
+{
+    return (int64_t)cu[n] + (skip ? skip[n] : 0);
+}
 
 // Index of the sequence owning global chunk c: the n with cu_chunks[n] <= c < cu_chunks[n+1].
 __device__ __forceinline__ int find_seq(const int32_t* cu_chunks, int n_seqs, int64_t c)
@@ -137,7 +152,16 @@ constexpr size_t tmem_cap_smem(uint32_t tmem_cols)
     return 233472 / (512 / tmem_cols + 1) - 1024 + 16;
 }
 
+// k0 alone: the chunk index (and, for a continuation, each sequence's fill tokens).
+cudaError_t launch_chunk_index(const PrefillArgs& a, int32_t C, const int32_t* pos0, int32_t* skip,
+                               int32_t* pos_last, cudaStream_t s);
 template <int DK, int DV, int C, typename T> cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+// Continuation (pos0: absolute position of each sequence's first token): the chunk index
+// with the fill lengths, the fill of each sequence's current chunk and its resync, then
+// the prefill of the rest and the ring.
+template <int DK, int DV, int C, typename T>
+cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, float* state, const cpr_gdn_ring& ring,
+                                    cudaStream_t s);
 template <int DK, int DV, int C, typename T> cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 template <int DK, int DV, int C, typename T> cudaError_t launch_ring_from_prefill(const RingArgs& a, cudaStream_t s);
 

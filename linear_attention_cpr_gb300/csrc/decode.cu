@@ -13,6 +13,8 @@
 //                    chunk) by the same routines as prefill's chunk prep and chain; the
 //                    result replaces both the state and ring S_b
 //   k6_ring_fill     builds a ring from a prefill's results
+//   k8_chunk_fill    (continuation) steps the tokens that fill each sequence's current
+//                    chunk, several per sequence, on the state held in registers
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -59,6 +61,62 @@ struct VecF<4> {
         *reinterpret_cast<float4*>(p) = make_float4(d[0], d[1], d[2], d[3]);
     }
 };
+
+// ------------------------------------------------------------------------------------
+// The token step of k4 (the same operations in the same order) as a routine, for the
+// chunk fill, on a state held in registers by 8 warps: warp m owns key rows
+// [m*DK/8, (m+1)*DK/8) (chain m of the canonical dot), lane l value columns
+// [l*DV/32, (l+1)*DV/32); s[t][e] = S[m DK/8 + t][l DV/32 + e].  kf, qf: the token's key
+// and query (fp32, shared); part, part2: [8][DV] shared scratch; v: the token's values;
+// st: NULL, or where the stepped state goes (row stride DV, this thread's first element).
+// Partial chains meet in shared memory and every value column's dot is finished by the
+// canonical tree; warp 0 writes o.  Contains two __syncthreads (the callers' shared inputs
+// must be written before the call).
+// ------------------------------------------------------------------------------------
+template <int DK, int DV, typename T>
+__device__ __forceinline__ void token_step(float (&s)[DK / 8][DV / 32], const float* __restrict__ kf,
+                                           const float* __restrict__ qf, float (*__restrict__ part)[DV],
+                                           float (*__restrict__ part2)[DV], float alpha, float beta,
+                                           const T* __restrict__ v, T* __restrict__ out, float* __restrict__ st)
+{
+    constexpr int L = DK / 8, VPT = DV / 32;
+    const int m = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int e = 0; e < VPT; ++e) {
+        float c = __fmul_rn(s[0][e], kf[m * L]);
+#pragma unroll
+        for (int t = 1; t < L; ++t) c = __fmaf_rn(s[t][e], kf[m * L + t], c);
+        part[m][lane * VPT + e] = c;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < VPT; ++e) {
+        const int i = lane * VPT + e;
+        const float x = tree8(part[0][i], part[1][i], part[2][i], part[3][i], part[4][i], part[5][i], part[6][i],
+                              part[7][i]);
+        const float u = step_u(alpha, beta, to_f32<T>(v[i]), x);
+#pragma unroll
+        for (int t = 0; t < L; ++t) s[t][e] = step_s(s[t][e], alpha, u, kf[m * L + t]);
+        float c = __fmul_rn(s[0][e], qf[m * L]);
+#pragma unroll
+        for (int t = 1; t < L; ++t) c = __fmaf_rn(s[t][e], qf[m * L + t], c);
+        part2[m][i] = c;
+    }
+    if (st) {
+#pragma unroll
+        for (int t = 0; t < L; ++t) VecF<VPT>::store(st + (size_t)t * DV, s[t]);
+    }
+    __syncthreads();
+    if (m == 0) {
+#pragma unroll
+        for (int e = 0; e < VPT; ++e) {
+            const int i = lane * VPT + e;
+            const float o = tree8(part2[0][i], part2[1][i], part2[2][i], part2[3][i], part2[4][i], part2[5][i],
+                                  part2[6][i], part2[7][i]);
+            out[i] = from_f32<T>(o);
+        }
+    }
+}
 
 // ------------------------------------------------------------------------------------
 // k4: decode step.  One CTA per (sequence, head), 8 warps: warp m owns key rows
@@ -151,6 +209,66 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 }
 
 // ------------------------------------------------------------------------------------
+// k8: chunk fill for a continuation.  One CTA per (sequence, head), k4's mapping: the
+// sequence's first skip[n] tokens (those that fill the chunk it is in, from position
+// pos0[n]) are stepped one after another by k4's token step on the state held in
+// registers; each token goes to its ring slot and its output to `out`.  The stepped state
+// is written back; when the chunk completes, the resync (k5) then replaces it.
+// ------------------------------------------------------------------------------------
+template <int DK, int DV, int C, typename T>
+__global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t* __restrict__ cu_seqlens,
+                                                     const int32_t* __restrict__ pos0,
+                                                     const int32_t* __restrict__ skip)
+{
+    constexpr int L = DK / 8, VPT = DV / 32;
+    __shared__ __align__(16) float kf[DK];
+    __shared__ __align__(16) float qf[DK];
+    __shared__ __align__(16) float part[8][DV];
+    __shared__ __align__(16) float part2[8][DV];
+    __shared__ float sc[2];
+
+    const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
+    const int m = tid >> 5, lane = tid & 31;
+    const int f = skip[n];
+    if (*a.status || f <= 0) return;
+    const int r0 = pos0[n] % C;
+    const size_t nh = (size_t)n * H + h;
+    const T* q = static_cast<const T*>(a.q);
+    const T* k = static_cast<const T*>(a.k);
+    const T* v = static_cast<const T*>(a.v);
+    T* out = static_cast<T*>(a.out);
+    T* rk = static_cast<T*>(a.ring.k);
+    T* rv = static_cast<T*>(a.ring.v);
+
+    float s[L][VPT];
+    float* st = a.state + nh * DK * DV + (size_t)(m * L) * DV + lane * VPT;
+#pragma unroll
+    for (int t = 0; t < L; ++t) VecF<VPT>::load(st + (size_t)t * DV, s[t]);
+    for (int t = 0; t < f; ++t) {
+        const size_t tok = ((size_t)cu_seqlens[n] + t) * H + h;  // packed token index x H + h
+        const int r = r0 + t;                                    // its ring slot
+        for (int idx = tid; idx < DK; idx += 256) {
+            const T kk = k[tok * DK + idx];
+            kf[idx] = to_f32<T>(kk);
+            qf[idx] = to_f32<T>(q[tok * DK + idx]);
+            rk[(nh * C + r) * DK + idx] = kk;
+        }
+        for (int idx = tid; idx < DV; idx += 256) rv[(nh * C + r) * DV + idx] = v[tok * DV + idx];
+        if (tid == 0) {
+            const float gg = a.g[tok], bb = a.beta[tok];
+            sc[0] = decay_exp(gg);
+            sc[1] = bb;
+            a.ring.g[nh * C + r] = gg;
+            a.ring.beta[nh * C + r] = bb;
+        }
+        __syncthreads();
+        token_step<DK, DV, T>(s, kf, qf, part, part2, sc[0], sc[1], v + tok * DV, out + tok * DV,
+                              t + 1 == f ? st : nullptr);
+        __syncthreads();  // kf, qf, sc and the partial sums are rewritten for the next token
+    }
+}
+
+// ------------------------------------------------------------------------------------
 // k5: resync, on a second stream while k4 steps every sequence.  A grid of at most one
 // wave walks the (sequence, head) pairs of the sequences whose token completes a chunk
 // (found from pos), DK + DV threads per CTA.  Each pair runs the same routines as prefill:
@@ -225,11 +343,13 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     const T* rk = static_cast<const T*>(a.ring.k) + bh * C * DK;
     const T* rv = static_cast<const T*>(a.ring.v) + bh * C * DV;
     // tokens 0..C-2 of the chunk come from the ring, token C-1 (this step's) from the inputs:
-    // the step kernel writes its ring slot concurrently
-    const T* tk = static_cast<const T*>(a.k) + bh * DK;
-    const T* tv = static_cast<const T*>(a.v) + bh * DV;
-    completing_token_output<DK, DV, C, T>(a, bh, reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5) + DK,
-                                          reinterpret_cast<float*>(sm5) + 2 * DK);
+    // the step kernel writes its ring slot concurrently (a continuation's fill has written
+    // every slot, and has produced the token's output)
+    const T* tk = a.resync_only ? rk + (size_t)(C - 1) * DK : static_cast<const T*>(a.k) + bh * DK;
+    const T* tv = a.resync_only ? rv + (size_t)(C - 1) * DV : static_cast<const T*>(a.v) + bh * DV;
+    if (!a.resync_only)
+        completing_token_output<DK, DV, C, T>(a, bh, reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5) + DK,
+                                              reinterpret_cast<float*>(sm5) + 2 * DK);
 
     for (int idx = tid; idx < C * DK; idx += blockDim.x) {
         const int r = idx / DK, j = idx % DK;
@@ -240,8 +360,9 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
         vsm[idx] = r < C - 1 ? rv[idx] : tv[n];
     }
     if (tid < C) {
-        s.G[tid] = tid < C - 1 ? a.ring.g[bh * C + tid] : a.g[bh];
-        s.bs[tid] = tid < C - 1 ? a.ring.beta[bh * C + tid] : a.beta[bh];
+        const bool ring_slot = tid < C - 1 || a.resync_only;
+        s.G[tid] = ring_slot ? a.ring.g[bh * C + tid] : a.g[bh];
+        s.bs[tid] = ring_slot ? a.ring.beta[bh * C + tid] : a.beta[bh];
     }
     tc::fence_before_sync();
     bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, vsm, (size_t)DV, tmem, mbar, phase);
@@ -287,6 +408,7 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     __shared__ int found;
     // the sequences whose token completes a chunk, in ascending order: rank n <-> the n-th b
     // with pos[b] % C == C - 1 (pos >= 0); every CTA counts them from pos
+    if (a.resync_only && *a.status) return;  // a continuation whose index step failed
     auto completes = [&](int b) { const int p = a.pos[b]; return p >= 0 && p % C == C - 1; };
     int total = 0;
     for (int b0 = 0; b0 < a.B; b0 += blockDim.x)
@@ -351,21 +473,24 @@ __global__ void __launch_bounds__(256) k6_ring_fill(RingArgs a)
     const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
     __shared__ long long cbase;
     __shared__ int valid;
+    if (a.status && *a.status) return;
     if (tid == 0) {
         long long acc = 0;
         int ok = a.cu_seqlens[0] == 0;
         for (int m = 0; m < n; ++m) {
-            const int Lm = a.cu_seqlens[m + 1] - a.cu_seqlens[m];
+            const int64_t Lm = a.cu_seqlens[m + 1] - seq_begin(a.cu_seqlens, a.skip, m);
             ok &= (Lm >= 0);
             acc += (Lm > 0) ? (Lm + C - 1) / C : 0;
         }
         cbase = acc;
-        valid = ok && a.cu_seqlens[n + 1] >= a.cu_seqlens[n] && (int64_t)a.cu_seqlens[n + 1] <= a.total_tokens;
+        valid = ok && a.cu_seqlens[n + 1] >= seq_begin(a.cu_seqlens, a.skip, n) &&
+                (int64_t)a.cu_seqlens[n + 1] <= a.total_tokens;
     }
     __syncthreads();
     if (!valid) return;
-    const int64_t t0 = a.cu_seqlens[n];
+    const int64_t t0 = seq_begin(a.cu_seqlens, a.skip, n);
     const int64_t L = a.cu_seqlens[n + 1] - t0;
+    if (a.skip && L == 0) return;  // a continuation that stayed in its chunk: the fill kept the ring
     const int rem = (int)(L % C);
     const size_t nh = (size_t)n * H + h;
     const size_t SS = (size_t)DK * DV;
@@ -453,11 +578,73 @@ cudaError_t launch_ring_from_prefill(const RingArgs& a, cudaStream_t s)
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------------
+// Continuation prefill: the chunk index (which also takes each sequence's fill tokens),
+// the fill (k8) and the resync of the chunks it completes (k5, resync only, after k8 on the
+// same stream), the prefill of the remaining tokens from the resulting states in place,
+// and the ring for the final partial chunks.
+// ------------------------------------------------------------------------------------
+template <int DK, int DV, int C, typename T>
+cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, float* state,
+                                    const cpr_gdn_ring& ring, cudaStream_t s)
+{
+    int32_t* skip = const_cast<int32_t*>(a.skip);
+    int32_t* pos_last = reinterpret_cast<int32_t*>(a.ws + PrefillLayout(a.total_tokens, a.n_seqs, a.H, DK, DV, C).pos_last);
+    cudaError_t e = launch_chunk_index(a, C, pos0, skip, pos_last, s);
+    if (e != cudaSuccess) return e;
+    DecodeArgs d{};
+    d.q = a.q;
+    d.k = a.k;
+    d.v = a.v;
+    d.g = a.g;
+    d.beta = a.beta;
+    d.state = state;
+    d.ring = ring;
+    d.pos = pos_last;
+    d.B = a.n_seqs;
+    d.H = a.H;
+    d.out = a.out;
+    d.status = a.status;
+    d.num_sms = a.num_sms;
+    d.resync_only = 1;
+    k8_chunk_fill<DK, DV, C, T><<<dim3((unsigned)a.n_seqs, a.H), 256, 0, s>>>(d, a.cu_seqlens, pos0, skip);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::rs_bytes(sizeof(T)), tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
+    e = cudaFuncSetAttribute(k5_resync<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
+    if (e != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(a.n_seqs * a.H, a.num_sms * (int)(232448 / sm5)));
+    k5_resync<DK, DV, C, T><<<grid, DK + DV, sm5, s>>>(d);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    PrefillArgs p = a;
+    p.state_in = state;
+    p.state_out = state;
+    if ((e = launch_prefill<DK, DV, C, T>(p, s)) != cudaSuccess) return e;
+    RingArgs ra;
+    ra.k = a.k;
+    ra.v = a.v;
+    ra.g = a.g;
+    ra.beta = a.beta;
+    ra.cu_seqlens = a.cu_seqlens;
+    ra.skip = a.skip;
+    ra.n_seqs = a.n_seqs;
+    ra.total_tokens = a.total_tokens;
+    ra.H = a.H;
+    ra.boundary = a.boundary;
+    ra.state_out = state;
+    ra.ring = ring;
+    ra.status = a.status;
+    return launch_ring_from_prefill<DK, DV, C, T>(ra, s);
+}
+
 #define CPR_INST_DECODE(DK, DV, C)                                                                         \
     template cudaError_t launch_decode<DK, DV, C, float>(const DecodeArgs&, cudaStream_t);                \
     template cudaError_t launch_decode<DK, DV, C, __nv_bfloat16>(const DecodeArgs&, cudaStream_t);        \
     template cudaError_t launch_ring_from_prefill<DK, DV, C, float>(const RingArgs&, cudaStream_t);       \
-    template cudaError_t launch_ring_from_prefill<DK, DV, C, __nv_bfloat16>(const RingArgs&, cudaStream_t);
+    template cudaError_t launch_ring_from_prefill<DK, DV, C, __nv_bfloat16>(const RingArgs&, cudaStream_t); \
+    template cudaError_t launch_prefill_continue<DK, DV, C, float>(const PrefillArgs&, const int32_t*, float*, \
+                                                                   const cpr_gdn_ring&, cudaStream_t);      \
+    template cudaError_t launch_prefill_continue<DK, DV, C, __nv_bfloat16>(const PrefillArgs&, const int32_t*, \
+                                                                           float*, const cpr_gdn_ring&, cudaStream_t);
 CPR_FOR_EACH_SHAPE(CPR_INST_DECODE)
 
 }  // namespace cpr

@@ -31,13 +31,17 @@ namespace cpr {
 // k0: chunk index.  One CTA of 1024 threads; each thread owns a contiguous range of
 // sequences (a shuffle scan gives each range's first chunk).  It also zeroes k23's
 // publication counters.  On invalid cu_seqlens (or too many chunks) every cu_chunks entry is 0,
-// so the later kernels find no chunk, and the status word records why.
+// so the later kernels find no chunk, and the status word records why.  For a continuation
+// (pos0 non-NULL) it first takes from each sequence the tokens that fill its current chunk
+// (skip[n] of them; pos_last[n] = the position of the last, or -1) and indexes the chunks of
+// the rest.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) k0_chunk_index(const int32_t* __restrict__ cu, int32_t n_seqs,
                                                       int64_t total_tokens, int32_t C, int64_t capacity,
                                                       int32_t* __restrict__ cu_chunks,
                                                       uint32_t* __restrict__ status, uint32_t* __restrict__ ready,
-                                                      int64_t n_ready)
+                                                      int64_t n_ready, const int32_t* __restrict__ pos0,
+                                                      int32_t* __restrict__ skip, int32_t* __restrict__ pos_last)
 {
     __shared__ long long warp_sum[32];
     __shared__ unsigned bad;
@@ -49,8 +53,19 @@ __global__ void __launch_bounds__(1024) k0_chunk_index(const int32_t* __restrict
     const int n0 = min(n_seqs, tid * per), n1 = min(n_seqs, n0 + per);
     long long s = 0;
     for (int n = n0; n < n1; ++n) {
-        const int L = cu[n + 1] - cu[n];
+        int L = cu[n + 1] - cu[n];
         if (L < 0) atomicOr(&bad, CPR_DEV_BAD_CU_SEQLENS);
+        if (pos0) {
+            const int p = pos0[n];
+            int f = 0;
+            if (p < 0)
+                atomicOr(&bad, CPR_DEV_BAD_POS);
+            else if (p % C != 0)
+                f = min(C - p % C, max(L, 0));
+            skip[n] = f;
+            pos_last[n] = f > 0 ? p + f - 1 : -1;
+            L -= f;
+        }
         s += (L > 0) ? (L + C - 1) / C : 0;
     }
     // exclusive prefix sum of s over the 1024 threads: warp scans, then a scan of the warp sums
@@ -82,7 +97,7 @@ __global__ void __launch_bounds__(1024) k0_chunk_index(const int32_t* __restrict
     long long run = incl - s + (wid > 0 ? warp_sum[wid - 1] : 0);
     for (int n = n0; n < n1; ++n) {
         cu_chunks[n] = ok ? (int32_t)run : 0;
-        const int L = cu[n + 1] - cu[n];
+        const int L = cu[n + 1] - cu[n] - (pos0 ? skip[n] : 0);
         run += (L > 0) ? (L + C - 1) / C : 0;
     }
     if (tid == 1023) cu_chunks[n_seqs] = ok ? (int32_t)total : 0;
@@ -115,9 +130,10 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
     if (c >= a.cu_chunks[a.n_seqs]) return;
     const int n = find_seq(a.cu_chunks, a.n_seqs, c);
     const int64_t j = c - a.cu_chunks[n];
-    const int64_t L = a.cu_seqlens[n + 1] - a.cu_seqlens[n];
+    const int64_t tb = seq_begin(a.cu_seqlens, a.skip, n);
+    const int64_t L = a.cu_seqlens[n + 1] - tb;
     if ((j + 1) * C > L) return;  // partial chunk: no update
-    const int64_t t0 = a.cu_seqlens[n] + j * C;
+    const int64_t t0 = tb + j * C;
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
 
@@ -279,7 +295,7 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
     const int nchains = a.n_seqs * H;
     for (int ci = cta; ci < nchains && !failed; ci += ncta) {
         const int n = ci / H, h = ci % H;
-        const int64_t t0 = a.cu_seqlens[n];
+        const int64_t t0 = seq_begin(a.cu_seqlens, a.skip, n);
         const int64_t L = a.cu_seqlens[n + 1] - t0;
         const int64_t nfull = L / C, nch = a.cu_chunks[n + 1] - a.cu_chunks[n], cbase = a.cu_chunks[n];
         const size_t nh = (size_t)n * H + h;
@@ -513,8 +529,9 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
     const int H = a.H;
     const int n = find_seq(a.cu_chunks, a.n_seqs, c);
     const int64_t j = c - a.cu_chunks[n];
-    const int64_t Ls = a.cu_seqlens[n + 1] - a.cu_seqlens[n];
-    const int64_t t0 = a.cu_seqlens[n] + j * C;
+    const int64_t tb = seq_begin(a.cu_seqlens, a.skip, n);
+    const int64_t Ls = a.cu_seqlens[n + 1] - tb;
+    const int64_t t0 = tb + j * C;
     const int len = (int)min((int64_t)C, Ls - j * C);
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
@@ -669,12 +686,22 @@ __global__ void __launch_bounds__(K2Cfg<DK, DV>::THREADS, 1) k23_chain_and_intra
 }
 
 // ------------------------------------------------------------------------------------
+cudaError_t launch_chunk_index(const PrefillArgs& a, int32_t C, const int32_t* pos0, int32_t* skip,
+                               int32_t* pos_last, cudaStream_t s)
+{
+    k0_chunk_index<<<1, 1024, 0, s>>>(a.cu_seqlens, a.n_seqs, a.total_tokens, C, a.boundary_capacity, a.cu_chunks,
+                                      a.status, a.ready, (int64_t)a.max_chunks * a.H + 1, pos0, skip, pos_last);
+    return cudaGetLastError();
+}
+
 template <int DK, int DV, int C, typename T>
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
 {
     profile_mark(0, s);
-    k0_chunk_index<<<1, 1024, 0, s>>>(a.cu_seqlens, a.n_seqs, a.total_tokens, C, a.boundary_capacity,
-                                      a.cu_chunks, a.status, a.ready, (int64_t)a.max_chunks * a.H + 1);
+    if (!a.skip)  // (a continuation has run the chunk index itself)
+        k0_chunk_index<<<1, 1024, 0, s>>>(a.cu_seqlens, a.n_seqs, a.total_tokens, C, a.boundary_capacity,
+                                          a.cu_chunks, a.status, a.ready, (int64_t)a.max_chunks * a.H + 1, nullptr,
+                                          nullptr, nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     profile_mark(1, s);
