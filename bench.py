@@ -301,6 +301,7 @@ def run_ours(args):
     decode = None
     if not args.no_decode:
         decode = run_decode(args, cpr, inputs, dev, hbm_peak, dist, world)
+    continuation = run_continuation(args, cpr, inputs, dev, hbm_peak, dist, world) if not args.no_decode else None
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only) ----------------
     cpu = None
@@ -321,9 +322,11 @@ def run_ours(args):
             "prefill": {"kernels_ms": kern_ms, "algorithmic_bytes": alg_bytes, "t_roof_ms": t_roof_ms,
                         "frac_of_t_roof": t_roof_ms / ms_max, "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": hbm_kind},
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches + (decode["gpu_launches"] if decode else 0),
+            "gpu_launches": launches + (decode["gpu_launches"] if decode else 0) +
+                            (continuation["gpu_launches"] if continuation else 0),
             "clocks": clocks.summary(),
             "decode": decode,
+            "continuation": continuation,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -410,6 +413,85 @@ def run_decode(args, cpr, inputs, dev, hbm_peak, dist, world):
         "frac_of_t_roof": bytes_step / (hbm_peak * 1e9) * 1e3 / ms,
         "e2e": {"value": 1e3 / e2e_ms * world, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * n_steps,
+    }
+
+
+def run_continuation(args, cpr, inputs, dev, hbm_peak, dist, world):
+    """Continuation prefill: the rollout_prefill sequences (5 x 2,048), each resumed at a
+    seeded position in [1, 2047] with the state and ring a prefill of its first part left;
+    the continuation of the rest is timed (state and ring restored outside the events)."""
+    w = inputs.workload("rollout_prefill")
+    H, dk, dv, C = w.H, w.dk, w.dv, w.C
+    x = inputs.prefill_inputs(w, device=dev)
+    lens = list(w.seqlens)
+    gen = torch.Generator().manual_seed(w.seed + 17)
+    splits = [int(torch.randint(1, L, (1,), generator=gen)) for L in lens]
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    keys = ("q", "k", "v", "g", "beta")
+
+    def pack(parts):
+        p = {k: torch.cat([t[k] for t in parts], 0).contiguous() for k in keys}
+        p["cu_seqlens"] = inputs.cu_seqlens_of([t["q"].shape[0] for t in parts]).to(dev)
+        return p
+
+    seqs = [{k: x[k][cu[n]:cu[n + 1]] for k in keys} for n in range(len(lens))]
+    first = pack([{k: t[k][:s] for k in keys} for t, s in zip(seqs, splits)])
+    second = pack([{k: t[k][s:] for k in keys} for t, s in zip(seqs, splits)])
+    _, st1, bnd1, _ = cpr.cpr_gdn_prefill(first["q"], first["k"], first["v"], first["g"], first["beta"],
+                                          first["cu_seqlens"], C)
+    ring0 = cpr.cpr_gdn_ring_from_prefill(first["k"], first["v"], first["g"], first["beta"], first["cu_seqlens"], C,
+                                          bnd1, st1)
+    pos0 = torch.tensor(splits, dtype=torch.int32, device=dev)
+    n_chunks = cpr.continue_chunks(second["cu_seqlens"].cpu(), splits, C)
+    T2 = second["q"].shape[0]
+    out = torch.empty(T2, H, dv, dtype=w.dtype, device=dev)
+    bnd = torch.empty(max(n_chunks, 1), H, dk, dv, dtype=torch.float32, device=dev)
+    ws = torch.empty(cpr.cpr_gdn_prefill_workspace_size(T2, len(lens), H, dk, dv, C), dtype=torch.uint8, device=dev)
+    state = st1.clone()
+    ring = ring0.clone()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def call():
+        cpr.cpr_gdn_prefill_continue(second["q"], second["k"], second["v"], second["g"], second["beta"],
+                                     second["cu_seqlens"], pos0, C, state, ring, out=out, boundary_states=bnd,
+                                     workspace=ws)
+
+    def restore():
+        state.copy_(st1)
+        for a, b in zip((ring.S_b, ring.k, ring.v, ring.g, ring.beta),
+                        (ring0.S_b, ring0.k, ring0.v, ring0.g, ring0.beta)):
+            a.copy_(b)
+
+    for _ in range(args.warmup):
+        restore()
+        call()
+    torch.cuda.synchronize()
+    assert cpr.cpr_gdn_device_status(ws) == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ms = []
+    steps = max(3, min(args.steps, 50))
+    _barrier(dist)
+    for _ in range(steps):
+        restore()
+        flush.zero_()
+        e0.record()
+        call()
+        e1.record()
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    _barrier(dist)
+    ms_max = _max_over_ranks(dist, statistics.fmean(ms))
+    _, flops = prefill_algorithmic(T2, len(lens), H, dk, dv, n_chunks)
+    t_roof = flops / (FP32_PEAK_TFLOPS * 1e12) * 1e3
+    return {
+        "metric": "continuation prefill tokens/s per layer", "value": weak_scaling_rate(world, T2, ms_max),
+        "unit": "tokens/s", "ms_per_step": ms_max, "steps": steps,
+        "workload": f"rollout_prefill resumed: 5 x 2,048 tokens, H={H}, dk=dv={dk}, C={C}, bf16; each sequence "
+                    f"resumed at a seeded position (first parts {splits}), {T2} tokens continued",
+        "t_roof_ms": t_roof, "frac_of_t_roof": t_roof / ms_max,
+        "gpu_launches": 6 * steps,
     }
 
 
