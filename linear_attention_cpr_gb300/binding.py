@@ -25,7 +25,8 @@ EXPORTED = (
     "cpr_gdn_supported", "cpr_gdn_version", "cpr_gdn_strerror", "cpr_gdn_num_chunks",
     "cpr_gdn_prefill_workspace_size", "cpr_gdn_decode_workspace_size", "cpr_gdn_prefill",
     "cpr_gdn_ring_from_prefill", "cpr_gdn_decode", "cpr_gdn_device_status", "cpr_gdn_set_profile_events",
-    "cpr_gdn_prefill_noalloc", "cpr_gdn_prefill_continue",
+    "cpr_gdn_prefill_noalloc", "cpr_gdn_prefill_continue", "cpr_gdn_prefill_grouped",
+    "cpr_gdn_ring_from_prefill_grouped", "cpr_gdn_decode_grouped", "cpr_gdn_prefill_continue_grouped",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # CPR_GDN_NOALLOC_SCRATCH_BYTES
 
@@ -78,6 +79,14 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         "cpr_gdn_prefill_noalloc": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P, P, P, I64, P]),
         "cpr_gdn_prefill_continue": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P,
                                            ctypes.POINTER(_Ring), P, P, I64, P, SZ, P]),
+        "cpr_gdn_prefill_grouped": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, I32, P, P, P, P, I64,
+                                          P, SZ, P]),
+        "cpr_gdn_ring_from_prefill_grouped": (I32, [P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, I32, P, P,
+                                                    ctypes.POINTER(_Ring), P]),
+        "cpr_gdn_decode_grouped": (I32, [P, P, P, P, P, P, ctypes.POINTER(_Ring), P, I32, I32, I32, I32, I32, I32,
+                                         I32, P, P, SZ, P]),
+        "cpr_gdn_prefill_continue_grouped": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, I32, P, P,
+                                                   ctypes.POINTER(_Ring), P, P, I64, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -151,8 +160,8 @@ def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, C: int, state_in=None, *, out=
     ``cu_seqlens`` is an int32 CUDA tensor.  ``n_chunks`` (the batch's chunk count) is
     read from a host copy of cu_seqlens when not given and boundary_states is None.
     """
-    T, H, dk = q.shape
-    dv = v.shape[-1]
+    T, Hk, dk = q.shape
+    H, dv = v.shape[1], v.shape[-1]  # value heads; H / Hk value heads share each query/key head
     N = cu_seqlens.numel() - 1
     dev = q.device
     if out is None:
@@ -165,11 +174,11 @@ def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, C: int, state_in=None, *, out=
         boundary_states = torch.empty(max(n_chunks, 1), H, dk, dv, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = torch.empty(cpr_gdn_prefill_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
-    code = load_library().cpr_gdn_prefill(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, C, _dtype_code(q),
+    code = load_library().cpr_gdn_prefill_grouped(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, Hk, dk, dv, C, _dtype_code(q),
         _ptr(state_in), _ptr(out), _ptr(state_out), _ptr(boundary_states), boundary_states.shape[0],
         _ptr(workspace), workspace.numel(), _stream(stream))
-    _check("cpr_gdn_prefill", code)
+    _check("cpr_gdn_prefill_grouped", code)
     return out, state_out, boundary_states, workspace
 
 
@@ -202,16 +211,16 @@ class Ring:
 
 def cpr_gdn_ring_from_prefill(k, v, g, beta, cu_seqlens, C: int, boundary_states, state_out, ring: Ring | None = None,
                               stream=None) -> Ring:
-    T, H, dk = k.shape
-    dv = v.shape[-1]
+    T, Hk, dk = k.shape
+    H, dv = v.shape[1], v.shape[-1]
     N = cu_seqlens.numel() - 1
     if ring is None:
         ring = Ring.empty(N, H, dk, dv, C, dtype=k.dtype, device=k.device)
     rc = ring._c()
-    code = load_library().cpr_gdn_ring_from_prefill(
-        _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, C, _dtype_code(k),
+    code = load_library().cpr_gdn_ring_from_prefill_grouped(
+        _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, Hk, dk, dv, C, _dtype_code(k),
         _ptr(boundary_states), _ptr(state_out), ctypes.byref(rc), _stream(stream))
-    _check("cpr_gdn_ring_from_prefill", code)
+    _check("cpr_gdn_ring_from_prefill_grouped", code)
     return ring
 
 
@@ -235,8 +244,8 @@ def cpr_gdn_prefill_continue(q, k, v, g, beta, cu_seqlens, pos0, C: int, state, 
     ``cu_seqlens`` and ``pos0`` are int32 CUDA tensors; ``n_chunks`` (the remainders' chunk
     count) is read from host copies of both when not given and boundary_states is None.
     """
-    T, H, dk = q.shape
-    dv = v.shape[-1]
+    T, Hk, dk = q.shape
+    H, dv = v.shape[1], v.shape[-1]
     N = cu_seqlens.numel() - 1
     dev = q.device
     if out is None:
@@ -248,27 +257,27 @@ def cpr_gdn_prefill_continue(q, k, v, g, beta, cu_seqlens, pos0, C: int, state, 
     if workspace is None:
         workspace = torch.empty(cpr_gdn_prefill_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
     rc = ring._c()
-    code = load_library().cpr_gdn_prefill_continue(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, C, _dtype_code(q),
+    code = load_library().cpr_gdn_prefill_continue_grouped(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, Hk, dk, dv, C, _dtype_code(q),
         _ptr(pos0), _ptr(state), ctypes.byref(rc), _ptr(out), _ptr(boundary_states), boundary_states.shape[0],
         _ptr(workspace), workspace.numel(), _stream(stream))
-    _check("cpr_gdn_prefill_continue", code)
+    _check("cpr_gdn_prefill_continue_grouped", code)
     return out, boundary_states, workspace
 
 
 def cpr_gdn_decode(q, k, v, g, beta, state, ring: Ring, pos, C: int, *, out=None, workspace=None, stream=None):
     """One decode step for B sequences; ``state`` and ``ring`` are updated in place.  Returns (out, workspace)."""
-    B, H, dk = q.shape
-    dv = v.shape[-1]
+    B, Hk, dk = q.shape
+    H, dv = v.shape[1], v.shape[-1]
     if out is None:
         out = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
     if workspace is None:
         workspace = torch.empty(cpr_gdn_decode_workspace_size(B, H, dk, dv, C), dtype=torch.uint8, device=q.device)
     rc = ring._c()
-    code = load_library().cpr_gdn_decode(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), ctypes.byref(rc), _ptr(pos), B, H, dk, dv, C,
-        _dtype_code(q), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
-    _check("cpr_gdn_decode", code)
+    code = load_library().cpr_gdn_decode_grouped(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), ctypes.byref(rc), _ptr(pos), B, H, Hk, dk, dv,
+        C, _dtype_code(q), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("cpr_gdn_decode_grouped", code)
     return out, workspace
 
 
@@ -305,6 +314,8 @@ def cpr_gdn_prefill_noalloc(q, k, v, g, beta, cu_seqlens, C: int, state_in=None,
     """
     T, H, dk = q.shape
     dv = v.shape[-1]
+    if v.shape[1] != H:
+        raise ValueError("cpr_gdn_prefill_noalloc takes one query/key head per value head")
     N = cu_seqlens.numel() - 1
     code = load_library().cpr_gdn_prefill_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, C, _dtype_code(q),

@@ -11,6 +11,8 @@ using namespace cpr;
 namespace {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+// H value heads over Hk query/key heads: Hk divides H.
+bool heads_ok(int32_t H, int32_t Hk) { return Hk > 0 && Hk <= H && H % Hk == 0; }
 
 bool shape_built(int32_t dk, int32_t dv, int32_t C)
 {
@@ -95,14 +97,14 @@ size_t cpr_gdn_decode_workspace_size(int32_t B, int32_t H, int32_t dk, int32_t d
     return decode_workspace_bytes(B);
 }
 
-int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                        const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H, int32_t dk,
-                        int32_t dv, int32_t C, int32_t dtype, const float* state_in, void* out, float* state_out,
-                        float* boundary_states, int64_t boundary_capacity, void* workspace,
-                        size_t workspace_bytes, void* stream)
+int32_t cpr_gdn_prefill_grouped(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
+                                int32_t Hk, int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* state_in,
+                                void* out, float* state_out, float* boundary_states, int64_t boundary_capacity,
+                                void* workspace, size_t workspace_bytes, void* stream)
 {
     if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype) ||
-        boundary_capacity < 0)
+        boundary_capacity < 0 || !heads_ok(H, Hk))
         return CPR_ERR_INVALID_ARG;
     if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
     if (n_seqs == 0) return CPR_OK;
@@ -128,6 +130,7 @@ int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float
     a.n_seqs = n_seqs;
     a.total_tokens = total_tokens;
     a.H = H;
+    a.Hk = Hk;
     a.state_in = state_in;
     a.out = out;
     a.state_out = state_out;
@@ -157,14 +160,15 @@ int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float
     return from_cuda(e);
 }
 
-int32_t cpr_gdn_prefill_continue(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                 const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
-                                 int32_t dk, int32_t dv, int32_t C, int32_t dtype, const int32_t* pos0, float* state,
-                                 const cpr_gdn_ring* ring, void* out, float* boundary_states,
-                                 int64_t boundary_capacity, void* workspace, size_t workspace_bytes, void* stream)
+int32_t cpr_gdn_prefill_continue_grouped(const void* q, const void* k, const void* v, const float* g,
+                                         const float* beta, const int32_t* cu_seqlens, int32_t n_seqs,
+                                         int64_t total_tokens, int32_t H, int32_t Hk, int32_t dk, int32_t dv, int32_t C,
+                                         int32_t dtype, const int32_t* pos0, float* state, const cpr_gdn_ring* ring,
+                                         void* out, float* boundary_states, int64_t boundary_capacity, void* workspace,
+                                         size_t workspace_bytes, void* stream)
 {
     if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype) ||
-        boundary_capacity < 0)
+        boundary_capacity < 0 || !heads_ok(H, Hk))
         return CPR_ERR_INVALID_ARG;
     if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
     if (n_seqs == 0) return CPR_OK;
@@ -193,6 +197,7 @@ int32_t cpr_gdn_prefill_continue(const void* q, const void* k, const void* v, co
     a.n_seqs = n_seqs;
     a.total_tokens = total_tokens;
     a.H = H;
+    a.Hk = Hk;
     a.state_in = state;
     a.out = out;
     a.state_out = state;
@@ -218,12 +223,14 @@ int32_t cpr_gdn_prefill_continue(const void* q, const void* k, const void* v, co
     return from_cuda(e);
 }
 
-int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, const float* beta,
-                                  const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
-                                  int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* boundary_states,
-                                  const float* state_out, const cpr_gdn_ring* ring, void* stream)
+int32_t cpr_gdn_ring_from_prefill_grouped(const void* k, const void* v, const float* g, const float* beta,
+                                          const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
+                                          int32_t Hk, int32_t dk, int32_t dv, int32_t C, int32_t dtype,
+                                          const float* boundary_states, const float* state_out,
+                                          const cpr_gdn_ring* ring, void* stream)
 {
-    if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype))
+    if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype) ||
+        !heads_ok(H, Hk))
         return CPR_ERR_INVALID_ARG;
     if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
     if (n_seqs == 0) return CPR_OK;
@@ -245,6 +252,7 @@ int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, 
     a.n_seqs = n_seqs;
     a.total_tokens = total_tokens;
     a.H = H;
+    a.Hk = Hk;
     a.boundary = boundary_states;
     a.state_out = state_out;
     a.ring = *ring;
@@ -259,12 +267,12 @@ int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, 
     return from_cuda(e);
 }
 
-int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                       float* state, const cpr_gdn_ring* ring, const int32_t* pos, int32_t B, int32_t H, int32_t dk,
-                       int32_t dv, int32_t C, int32_t dtype, void* out, void* workspace, size_t workspace_bytes,
-                       void* stream)
+int32_t cpr_gdn_decode_grouped(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                               float* state, const cpr_gdn_ring* ring, const int32_t* pos, int32_t B, int32_t H,
+                               int32_t Hk, int32_t dk, int32_t dv, int32_t C, int32_t dtype, void* out,
+                               void* workspace, size_t workspace_bytes, void* stream)
 {
-    if (B < 0 || H <= 0 || H > 65535 || !dtype_ok(dtype)) return CPR_ERR_INVALID_ARG;
+    if (B < 0 || H <= 0 || H > 65535 || !dtype_ok(dtype) || !heads_ok(H, Hk)) return CPR_ERR_INVALID_ARG;
     if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
     if (B == 0) return CPR_OK;
     if (!q || !k || !v || !g || !beta || !state || !ring || !pos || !out || !ring->S_b || !ring->k || !ring->v ||
@@ -288,6 +296,7 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
     a.pos = pos;
     a.B = B;
     a.H = H;
+    a.Hk = Hk;
     a.out = out;
     a.status = static_cast<uint32_t*>(workspace);
     a.num_sms = num_sms();
@@ -328,6 +337,47 @@ int32_t cpr_gdn_device_status(const void* workspace, uint32_t* status_out, void*
     if (e != cudaSuccess) return CPR_ERR_CUDA;
     *status_out = v;
     return CPR_OK;
+}
+
+// The entry points with one query/key head per value head.
+int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                        int32_t dv, int32_t C, int32_t dtype, const float* state_in, void* out, float* state_out,
+                        float* boundary_states, int64_t boundary_capacity, void* workspace,
+                        size_t workspace_bytes, void* stream)
+{
+    return cpr_gdn_prefill_grouped(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, H, H, dk, dv, C, dtype,
+                                   state_in, out, state_out, boundary_states, boundary_capacity, workspace,
+                                   workspace_bytes, stream);
+}
+
+int32_t cpr_gdn_prefill_continue(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                 const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
+                                 int32_t dk, int32_t dv, int32_t C, int32_t dtype, const int32_t* pos0, float* state,
+                                 const cpr_gdn_ring* ring, void* out, float* boundary_states,
+                                 int64_t boundary_capacity, void* workspace, size_t workspace_bytes, void* stream)
+{
+    return cpr_gdn_prefill_continue_grouped(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, H, H, dk, dv, C,
+                                            dtype, pos0, state, ring, out, boundary_states, boundary_capacity,
+                                            workspace, workspace_bytes, stream);
+}
+
+int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, const float* beta,
+                                  const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
+                                  int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* boundary_states,
+                                  const float* state_out, const cpr_gdn_ring* ring, void* stream)
+{
+    return cpr_gdn_ring_from_prefill_grouped(k, v, g, beta, cu_seqlens, n_seqs, total_tokens, H, H, dk, dv, C, dtype,
+                                             boundary_states, state_out, ring, stream);
+}
+
+int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                       float* state, const cpr_gdn_ring* ring, const int32_t* pos, int32_t B, int32_t H, int32_t dk,
+                       int32_t dv, int32_t C, int32_t dtype, void* out, void* workspace, size_t workspace_bytes,
+                       void* stream)
+{
+    return cpr_gdn_decode_grouped(q, k, v, g, beta, state, ring, pos, B, H, H, dk, dv, C, dtype, out, workspace,
+                                  workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -65,7 +65,8 @@ struct PrefillArgs {
     const int32_t* skip;  // NULL, or tokens of each sequence already consumed (continuation)
     int32_t n_seqs;
     int64_t total_tokens;
-    int32_t H;
+    int32_t H;   // value heads (states, v, g, beta, o)
+    int32_t Hk;  // query/key heads: value head h reads q/k head h / (H / Hk)
     const float* state_in;
     void* out;
     float* state_out;
@@ -95,6 +96,7 @@ struct DecodeArgs {
     const int32_t* pos;
     int32_t B;
     int32_t H;
+    int32_t Hk;  // as PrefillArgs::Hk
     void* out;
     uint32_t* status;
     int num_sms;
@@ -112,10 +114,14 @@ struct RingArgs {
     int32_t n_seqs;
     int64_t total_tokens;
     int32_t H;
+    int32_t Hk;               // as PrefillArgs::Hk
     const float* boundary;
     const float* state_out;
     cpr_gdn_ring ring;
 };
+
+// The query/key head that value head h reads (H value heads over Hk query/key heads).
+__device__ __forceinline__ int qk_head(int h, int H, int Hk) { return h / (H / Hk); }
 
 // First token of sequence n's part of a batch: cu_seqlens[n], plus skip[n] when a
 // continuation has already consumed that many of its tokens.

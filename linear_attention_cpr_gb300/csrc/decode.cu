@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
     const int r = p % C;
     if (r == C - 1) return;  // k5 steps this token and resynchronises the state
     const size_t bh = (size_t)b * H + h;
+    const size_t bhk = (size_t)b * a.Hk + qk_head(h, H, a.Hk);
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
@@ -152,9 +153,9 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
     T* rv = static_cast<T*>(a.ring.v);
 
     for (int idx = tid; idx < DK; idx += 256) {
-        const T kk = k[bh * DK + idx];
+        const T kk = k[bhk * DK + idx];
         kf[idx] = to_f32<T>(kk);
-        qf[idx] = to_f32<T>(q[bh * DK + idx]);
+        qf[idx] = to_f32<T>(q[bhk * DK + idx]);
         rk[(bh * C + r) * DK + idx] = kk;
     }
     for (int idx = tid; idx < DV; idx += 256) rv[(bh * C + r) * DV + idx] = v[bh * DV + idx];
@@ -246,11 +247,12 @@ __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t
     for (int t = 0; t < L; ++t) VecF<VPT>::load(st + (size_t)t * DV, s[t]);
     for (int t = 0; t < f; ++t) {
         const size_t tok = ((size_t)cu_seqlens[n] + t) * H + h;  // packed token index x H + h
+        const size_t tokk = ((size_t)cu_seqlens[n] + t) * a.Hk + qk_head(h, H, a.Hk);
         const int r = r0 + t;                                    // its ring slot
         for (int idx = tid; idx < DK; idx += 256) {
-            const T kk = k[tok * DK + idx];
+            const T kk = k[tokk * DK + idx];
             kf[idx] = to_f32<T>(kk);
-            qf[idx] = to_f32<T>(q[tok * DK + idx]);
+            qf[idx] = to_f32<T>(q[tokk * DK + idx]);
             rk[(nh * C + r) * DK + idx] = kk;
         }
         for (int idx = tid; idx < DV; idx += 256) rv[(nh * C + r) * DV + idx] = v[tok * DV + idx];
@@ -292,9 +294,10 @@ __device__ __forceinline__ void completing_token_output(const DecodeArgs& a, siz
     const int tid = threadIdx.x;
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
+    const size_t bhk = (bh / a.H) * a.Hk + qk_head((int)(bh % a.H), a.H, a.Hk);
     for (int idx = tid; idx < DK; idx += blockDim.x) {
-        kf[idx] = to_f32<T>(k[bh * DK + idx]);
-        qf[idx] = to_f32<T>(q[bh * DK + idx]);
+        kf[idx] = to_f32<T>(k[bhk * DK + idx]);
+        qf[idx] = to_f32<T>(q[bhk * DK + idx]);
     }
     __syncthreads();
     if (tid < DV) {
@@ -345,7 +348,8 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     // tokens 0..C-2 of the chunk come from the ring, token C-1 (this step's) from the inputs:
     // the step kernel writes its ring slot concurrently (a continuation's fill has written
     // every slot, and has produced the token's output)
-    const T* tk = a.resync_only ? rk + (size_t)(C - 1) * DK : static_cast<const T*>(a.k) + bh * DK;
+    const size_t bhk = (size_t)b * a.Hk + qk_head(h, H, a.Hk);
+    const T* tk = a.resync_only ? rk + (size_t)(C - 1) * DK : static_cast<const T*>(a.k) + bhk * DK;
     const T* tv = a.resync_only ? rv + (size_t)(C - 1) * DV : static_cast<const T*>(a.v) + bh * DV;
     if (!a.resync_only)
         completing_token_output<DK, DV, C, T>(a, bh, reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5) + DK,
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(256) k6_ring_fill(RingArgs a)
     const int64_t tf = t0 + L - rem;  // first token of the final partial chunk
     for (int idx = tid; idx < rem * DK; idx += blockDim.x) {
         const int r = idx / DK, jj = idx % DK;
-        rk[(nh * C + r) * DK + jj] = k[((size_t)(tf + r) * H + h) * DK + jj];
+        rk[(nh * C + r) * DK + jj] = k[((size_t)(tf + r) * a.Hk + qk_head(h, H, a.Hk)) * DK + jj];
     }
     for (int idx = tid; idx < rem * DV; idx += blockDim.x) {
         const int r = idx / DV, jj = idx % DV;
@@ -603,6 +607,7 @@ cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, f
     d.pos = pos_last;
     d.B = a.n_seqs;
     d.H = a.H;
+    d.Hk = a.Hk;
     d.out = a.out;
     d.status = a.status;
     d.num_sms = a.num_sms;
@@ -629,6 +634,7 @@ cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, f
     ra.n_seqs = a.n_seqs;
     ra.total_tokens = a.total_tokens;
     ra.H = a.H;
+    ra.Hk = a.Hk;
     ra.boundary = a.boundary;
     ra.state_out = state;
     ra.ring = ring;

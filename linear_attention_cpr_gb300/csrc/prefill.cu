@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
     const int64_t L = a.cu_seqlens[n + 1] - tb;
     if ((j + 1) * C > L) return;  // partial chunk: no update
     const int64_t t0 = tb + j * C;
+    const int hk = qk_head(h, H, a.Hk);
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
 
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
         for (int q4 = 0; q4 < NK; ++q4) {
             const int idx = tid + q4 * (DK + DV);
             if (idx < C * KV)
-                kr[q4] = __ldg(reinterpret_cast<const uint4*>(k + ((t0 + idx / KV) * H + h) * DK + (idx % KV) * VE));
+                kr[q4] = __ldg(reinterpret_cast<const uint4*>(k + ((t0 + idx / KV) * a.Hk + hk) * DK + (idx % KV) * VE));
         }
 #pragma unroll
         for (int q4 = 0; q4 < NK; ++q4) {
@@ -533,6 +534,7 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
     const int64_t Ls = a.cu_seqlens[n + 1] - tb;
     const int64_t t0 = tb + j * C;
     const int len = (int)min((int64_t)C, Ls - j * C);
+    const int hk = qk_head(hd, H, a.Hk);
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
@@ -557,7 +559,7 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
             for (int s = 0; s < P; ++s) {
                 const int idx = tid + (s0 + s) * NT, r = idx / KV, cc = idx % KV;
                 if (s0 + s < NK && r < len) {
-                    const size_t g = ((size_t)(t0 + r) * H + hd) * DK + cc * VE;
+                    const size_t g = ((size_t)(t0 + r) * a.Hk + hk) * DK + cc * VE;
                     kr[s] = __ldg(reinterpret_cast<const uint4*>(k + g));
                     qr[s] = __ldg(reinterpret_cast<const uint4*>(q + g));
                 }
