@@ -120,8 +120,10 @@ struct RingArgs {
     cpr_gdn_ring ring;
 };
 
-// The query/key head that value head h reads (H value heads over Hk query/key heads).
-__device__ __forceinline__ int qk_head(int h, int H, int Hk) { return h / (H / Hk); }
+// The query/key head that value head h reads (H value heads over Hk query/key heads).  The
+// division sits in a separate call so that the usual case, Hk = H, runs none of it.
+static __device__ __noinline__ int qk_head_grouped(int h, int H, int Hk) { return h / (H / Hk); }
+__device__ __forceinline__ int qk_head(int h, int H, int Hk) { return Hk == H ? h : qk_head_grouped(h, H, Hk); }
 
 // First token of sequence n's part of a batch: cu_seqlens[n], plus skip[n] when a
 // continuation has already consumed that many of its tokens.

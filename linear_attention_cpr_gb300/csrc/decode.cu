@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
     __shared__ __align__(16) float part2[8][DV];
     __shared__ float sc[2];
 
-    const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
+    // grid (sequence, query/key head, value head within its group): no division for the head
+    const int b = blockIdx.x, h = blockIdx.y * gridDim.z + blockIdx.z, tid = threadIdx.x, H = a.H;
     const int m = tid >> 5, lane = tid & 31;
     const int p = a.pos[b];
     if (p < 0) {
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
     const int r = p % C;
     if (r == C - 1) return;  // k5 steps this token and resynchronises the state
     const size_t bh = (size_t)b * H + h;
-    const size_t bhk = (size_t)b * a.Hk + qk_head(h, H, a.Hk);
+    const size_t bhk = (size_t)b * a.Hk + blockIdx.y;
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
@@ -294,7 +295,7 @@ __device__ __forceinline__ void completing_token_output(const DecodeArgs& a, siz
     const int tid = threadIdx.x;
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
-    const size_t bhk = (bh / a.H) * a.Hk + qk_head((int)(bh % a.H), a.H, a.Hk);
+    const size_t bhk = a.Hk == a.H ? bh : (bh / a.H) * a.Hk + qk_head((int)(bh % a.H), a.H, a.Hk);
     for (int idx = tid; idx < DK; idx += blockDim.x) {
         kf[idx] = to_f32<T>(k[bhk * DK + idx]);
         qf[idx] = to_f32<T>(q[bhk * DK + idx]);
@@ -565,7 +566,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     const int grid = std::max(1, std::min(a.B * a.H, std::max(1, a.num_sms / 2) * (int)(232448 / sm5)));
     k5_resync<DK, DV, C, T><<<grid, DK + DV, sm5, ss->stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k4_decode_step<DK, DV, C, T><<<dim3(a.B, a.H), 256, 0, s>>>(a);
+    k4_decode_step<DK, DV, C, T><<<dim3(a.B, a.Hk, a.H / a.Hk), 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_mark(1, s);
     // join: work issued on s after this call sees the resync's results

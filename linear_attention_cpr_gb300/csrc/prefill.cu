@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(1024) k0_chunk_index(const int32_t* __restrict
 // shared-memory image the chain kernel copies in one piece, B^T as fp32 rows.
 // Exits for partial chunks.
 // ------------------------------------------------------------------------------------
-template <int DK, int DV, int C, typename T>
+template <int DK, int DV, int C, typename T, bool GROUPED>
 __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
 {
     using U = UCfg<DK, DV, C>;
@@ -126,7 +126,9 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
 
     const int64_t c = blockIdx.x;
-    const int h = blockIdx.y, tid = threadIdx.x, H = a.H;
+    // grid (chunk, query/key head, value head within its group) when grouped, else
+    // (chunk, head): no division for the head either way
+    const int h = GROUPED ? blockIdx.y * gridDim.z + blockIdx.z : blockIdx.y, tid = threadIdx.x, H = a.H;
     if (c >= a.cu_chunks[a.n_seqs]) return;
     const int n = find_seq(a.cu_chunks, a.n_seqs, c);
     const int64_t j = c - a.cu_chunks[n];
@@ -134,8 +136,8 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
     const int64_t L = a.cu_seqlens[n + 1] - tb;
     if ((j + 1) * C > L) return;  // partial chunk: no update
     const int64_t t0 = tb + j * C;
-    const int hk = qk_head(h, H, a.Hk);
     const T* k = static_cast<const T*>(a.k);
+    const int kH = GROUPED ? a.Hk : H, kh = GROUPED ? (int)blockIdx.y : h;  // query/key heads, this one
     const T* v = static_cast<const T*>(a.v);
 
     if (tid < 32) tc::tmem_alloc(tslot, U::TMEM_COLS);
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
         for (int q4 = 0; q4 < NK; ++q4) {
             const int idx = tid + q4 * (DK + DV);
             if (idx < C * KV)
-                kr[q4] = __ldg(reinterpret_cast<const uint4*>(k + ((t0 + idx / KV) * a.Hk + hk) * DK + (idx % KV) * VE));
+                kr[q4] = __ldg(reinterpret_cast<const uint4*>(k + ((t0 + idx / KV) * kH + kh) * DK + (idx % KV) * VE));
         }
 #pragma unroll
         for (int q4 = 0; q4 < NK; ++q4) {
@@ -710,9 +712,17 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
 
     // dynamic shared memory also caps the CTAs per SM so their TMEM columns fit in 512
     const size_t sm1 = std::max<size_t>(UCfg<DK, DV, C>::PREP_SMEM, tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
-    e = cudaFuncSetAttribute(k1_chunk_prep<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
-    if (e != cudaSuccess) return e;
-    k1_chunk_prep<DK, DV, C, T><<<dim3((unsigned)a.max_chunks, a.H), DK + DV, sm1, s>>>(a);
+    if (a.Hk == a.H) {
+        e = cudaFuncSetAttribute(k1_chunk_prep<DK, DV, C, T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sm1);
+        if (e != cudaSuccess) return e;
+        k1_chunk_prep<DK, DV, C, T, false><<<dim3((unsigned)a.max_chunks, a.H), DK + DV, sm1, s>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(k1_chunk_prep<DK, DV, C, T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sm1);
+        if (e != cudaSuccess) return e;
+        k1_chunk_prep<DK, DV, C, T, true><<<dim3((unsigned)a.max_chunks, a.Hk, a.H / a.Hk), DK + DV, sm1, s>>>(a);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     profile_mark(2, s);
