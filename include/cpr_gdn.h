@@ -210,17 +210,24 @@ int32_t cpr_gdn_prefill_continue(const void* q, const void* k, const void* v, co
                                  int64_t boundary_capacity, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Grouped value heads: the four calls above with H value heads over Hk query/key heads
- * (Hk divides H; value head h reads query/key head h / (H / Hk)).  q and k are then
- * [.., Hk, dk]; v, g, beta, out, states and the ring keep H heads (the ring holds each
- * value head's copy of its keys).  Every other argument, and the results per value head,
- * are those of the call without the suffix, which is the case Hk = H.
+ * Grouped value heads and options: the four calls above with H value heads over Hk
+ * query/key heads (Hk divides H; value head h reads query/key head h / (H / Hk)).  q and k
+ * are then [.., Hk, dk]; v, g, beta, out, states and the ring keep H heads (the ring holds
+ * each value head's copy of its keys, as given).  `flags` (prefill, decode, continuation):
+ *   CPR_QK_L2NORM  the kernels L2-normalise every key and query row before use:
+ *                  k / sqrt(sum k^2 + 1e-6) and q / sqrt(sum q^2 + 1e-6) * dk^-1/2, the sum
+ *                  of squares in the canonical dot order, the square root and reciprocal
+ *                  correctly rounded, so every path normalises to the same bits.  A decode
+ *                  or continuation must use the flag its prefill used.
+ * Every other argument, and the results per value head, are those of the call without the
+ * suffix, which is the case Hk = H, flags = 0.
  */
+#define CPR_QK_L2NORM 1u
 int32_t cpr_gdn_prefill_grouped(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                 const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
-                                int32_t Hk, int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* state_in,
-                                void* out, float* state_out, float* boundary_states, int64_t boundary_capacity,
-                                void* workspace, size_t workspace_bytes, void* stream);
+                                int32_t Hk, uint32_t flags, int32_t dk, int32_t dv, int32_t C, int32_t dtype,
+                                const float* state_in, void* out, float* state_out, float* boundary_states,
+                                int64_t boundary_capacity, void* workspace, size_t workspace_bytes, void* stream);
 int32_t cpr_gdn_ring_from_prefill_grouped(const void* k, const void* v, const float* g, const float* beta,
                                           const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
                                           int32_t Hk, int32_t dk, int32_t dv, int32_t C, int32_t dtype,
@@ -228,14 +235,15 @@ int32_t cpr_gdn_ring_from_prefill_grouped(const void* k, const void* v, const fl
                                           const cpr_gdn_ring* ring, void* stream);
 int32_t cpr_gdn_decode_grouped(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                float* state, const cpr_gdn_ring* ring, const int32_t* pos, int32_t B, int32_t H,
-                               int32_t Hk, int32_t dk, int32_t dv, int32_t C, int32_t dtype, void* out,
-                               void* workspace, size_t workspace_bytes, void* stream);
+                               int32_t Hk, uint32_t flags, int32_t dk, int32_t dv, int32_t C, int32_t dtype,
+                               void* out, void* workspace, size_t workspace_bytes, void* stream);
 int32_t cpr_gdn_prefill_continue_grouped(const void* q, const void* k, const void* v, const float* g,
                                          const float* beta, const int32_t* cu_seqlens, int32_t n_seqs,
-                                         int64_t total_tokens, int32_t H, int32_t Hk, int32_t dk, int32_t dv, int32_t C,
-                                         int32_t dtype, const int32_t* pos0, float* state, const cpr_gdn_ring* ring,
-                                         void* out, float* boundary_states, int64_t boundary_capacity, void* workspace,
-                                         size_t workspace_bytes, void* stream);
+                                         int64_t total_tokens, int32_t H, int32_t Hk, uint32_t flags, int32_t dk,
+                                         int32_t dv, int32_t C, int32_t dtype, const int32_t* pos0, float* state,
+                                         const cpr_gdn_ring* ring, void* out, float* boundary_states,
+                                         int64_t boundary_capacity, void* workspace, size_t workspace_bytes,
+                                         void* stream);
 
 /*
  * Prefill for callers that cannot allocate device memory.  (The pages have no

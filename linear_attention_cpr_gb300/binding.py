@@ -61,7 +61,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                "`python -m linear_attention_cpr_gb300.build` (nvcc, sm_103a)")
         _build.build()
     lib = ctypes.CDLL(path)
-    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    P, I32, I64, SZ, U32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint32
     sig = {
         "cpr_gdn_supported": (ctypes.c_int, [I32, I32, I32, I32]),
         "cpr_gdn_version": (I32, []),
@@ -79,14 +79,14 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         "cpr_gdn_prefill_noalloc": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P, P, P, I64, P]),
         "cpr_gdn_prefill_continue": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P,
                                            ctypes.POINTER(_Ring), P, P, I64, P, SZ, P]),
-        "cpr_gdn_prefill_grouped": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, I32, P, P, P, P, I64,
-                                          P, SZ, P]),
+        "cpr_gdn_prefill_grouped": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, U32, I32, I32, I32, I32, P, P, P, P,
+                                          I64, P, SZ, P]),
         "cpr_gdn_ring_from_prefill_grouped": (I32, [P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, I32, P, P,
                                                     ctypes.POINTER(_Ring), P]),
-        "cpr_gdn_decode_grouped": (I32, [P, P, P, P, P, P, ctypes.POINTER(_Ring), P, I32, I32, I32, I32, I32, I32,
-                                         I32, P, P, SZ, P]),
-        "cpr_gdn_prefill_continue_grouped": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, I32, P, P,
-                                                   ctypes.POINTER(_Ring), P, P, I64, P, SZ, P]),
+        "cpr_gdn_decode_grouped": (I32, [P, P, P, P, P, P, ctypes.POINTER(_Ring), P, I32, I32, I32, U32, I32, I32,
+                                         I32, I32, P, P, SZ, P]),
+        "cpr_gdn_prefill_continue_grouped": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, U32, I32, I32, I32, I32, P,
+                                                   P, ctypes.POINTER(_Ring), P, P, I64, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -99,6 +99,13 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
 def _check(fn: str, code: int) -> None:
     if code != 0:
         raise CprError(fn, code, load_library().cpr_gdn_strerror(code).decode())
+
+
+QK_L2NORM = 1  # CPR_QK_L2NORM
+
+
+def _flags(qk_l2norm: bool) -> int:
+    return QK_L2NORM if qk_l2norm else 0
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -154,7 +161,8 @@ def cpr_gdn_decode_workspace_size(B: int, H: int, dk: int, dv: int, C: int) -> i
 
 
 def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, C: int, state_in=None, *, out=None, state_out=None,
-                    boundary_states=None, workspace=None, n_chunks: int | None = None, stream=None):
+                    boundary_states=None, workspace=None, n_chunks: int | None = None, qk_l2norm: bool = False,
+                    stream=None):
     """CPR prefill.  Returns (out, state_out, boundary_states, workspace).
 
     ``cu_seqlens`` is an int32 CUDA tensor.  ``n_chunks`` (the batch's chunk count) is
@@ -175,8 +183,8 @@ def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, C: int, state_in=None, *, out=
     if workspace is None:
         workspace = torch.empty(cpr_gdn_prefill_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
     code = load_library().cpr_gdn_prefill_grouped(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, Hk, dk, dv, C, _dtype_code(q),
-        _ptr(state_in), _ptr(out), _ptr(state_out), _ptr(boundary_states), boundary_states.shape[0],
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, Hk, _flags(qk_l2norm), dk, dv, C,
+        _dtype_code(q), _ptr(state_in), _ptr(out), _ptr(state_out), _ptr(boundary_states), boundary_states.shape[0],
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check("cpr_gdn_prefill_grouped", code)
     return out, state_out, boundary_states, workspace
@@ -237,7 +245,8 @@ def continue_chunks(cu_seqlens_host, pos0_host, C: int) -> int:
 
 
 def cpr_gdn_prefill_continue(q, k, v, g, beta, cu_seqlens, pos0, C: int, state, ring: Ring, *, out=None,
-                             boundary_states=None, workspace=None, n_chunks: int | None = None, stream=None):
+                             boundary_states=None, workspace=None, n_chunks: int | None = None,
+                             qk_l2norm: bool = False, stream=None):
     """Continuation prefill: each sequence continues from absolute position pos0[n] with
     ``state`` and ``ring`` (updated in place).  Returns (out, boundary_states, workspace).
 
@@ -258,14 +267,16 @@ def cpr_gdn_prefill_continue(q, k, v, g, beta, cu_seqlens, pos0, C: int, state, 
         workspace = torch.empty(cpr_gdn_prefill_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
     rc = ring._c()
     code = load_library().cpr_gdn_prefill_continue_grouped(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, Hk, dk, dv, C, _dtype_code(q),
-        _ptr(pos0), _ptr(state), ctypes.byref(rc), _ptr(out), _ptr(boundary_states), boundary_states.shape[0],
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, Hk, _flags(qk_l2norm), dk, dv, C,
+        _dtype_code(q), _ptr(pos0), _ptr(state), ctypes.byref(rc), _ptr(out), _ptr(boundary_states),
+        boundary_states.shape[0],
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check("cpr_gdn_prefill_continue_grouped", code)
     return out, boundary_states, workspace
 
 
-def cpr_gdn_decode(q, k, v, g, beta, state, ring: Ring, pos, C: int, *, out=None, workspace=None, stream=None):
+def cpr_gdn_decode(q, k, v, g, beta, state, ring: Ring, pos, C: int, *, out=None, workspace=None,
+                   qk_l2norm: bool = False, stream=None):
     """One decode step for B sequences; ``state`` and ``ring`` are updated in place.  Returns (out, workspace)."""
     B, Hk, dk = q.shape
     H, dv = v.shape[1], v.shape[-1]
@@ -275,8 +286,8 @@ def cpr_gdn_decode(q, k, v, g, beta, state, ring: Ring, pos, C: int, *, out=None
         workspace = torch.empty(cpr_gdn_decode_workspace_size(B, H, dk, dv, C), dtype=torch.uint8, device=q.device)
     rc = ring._c()
     code = load_library().cpr_gdn_decode_grouped(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), ctypes.byref(rc), _ptr(pos), B, H, Hk, dk, dv,
-        C, _dtype_code(q), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), ctypes.byref(rc), _ptr(pos), B, H, Hk,
+        _flags(qk_l2norm), dk, dv, C, _dtype_code(q), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("cpr_gdn_decode_grouped", code)
     return out, workspace
 

@@ -99,12 +99,13 @@ size_t cpr_gdn_decode_workspace_size(int32_t B, int32_t H, int32_t dk, int32_t d
 
 int32_t cpr_gdn_prefill_grouped(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                 const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
-                                int32_t Hk, int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* state_in,
+                                int32_t Hk, uint32_t flags, int32_t dk, int32_t dv, int32_t C, int32_t dtype,
+                                const float* state_in,
                                 void* out, float* state_out, float* boundary_states, int64_t boundary_capacity,
                                 void* workspace, size_t workspace_bytes, void* stream)
 {
     if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype) ||
-        boundary_capacity < 0 || !heads_ok(H, Hk))
+        boundary_capacity < 0 || !heads_ok(H, Hk) || (flags & ~CPR_QK_L2NORM))
         return CPR_ERR_INVALID_ARG;
     if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
     if (n_seqs == 0) return CPR_OK;
@@ -131,6 +132,7 @@ int32_t cpr_gdn_prefill_grouped(const void* q, const void* k, const void* v, con
     a.total_tokens = total_tokens;
     a.H = H;
     a.Hk = Hk;
+    a.qk_norm = (flags & CPR_QK_L2NORM) ? 1 : 0;
     a.state_in = state_in;
     a.out = out;
     a.state_out = state_out;
@@ -162,13 +164,14 @@ int32_t cpr_gdn_prefill_grouped(const void* q, const void* k, const void* v, con
 
 int32_t cpr_gdn_prefill_continue_grouped(const void* q, const void* k, const void* v, const float* g,
                                          const float* beta, const int32_t* cu_seqlens, int32_t n_seqs,
-                                         int64_t total_tokens, int32_t H, int32_t Hk, int32_t dk, int32_t dv, int32_t C,
-                                         int32_t dtype, const int32_t* pos0, float* state, const cpr_gdn_ring* ring,
+                                         int64_t total_tokens, int32_t H, int32_t Hk, uint32_t flags, int32_t dk,
+                                         int32_t dv, int32_t C, int32_t dtype, const int32_t* pos0, float* state,
+                                         const cpr_gdn_ring* ring,
                                          void* out, float* boundary_states, int64_t boundary_capacity, void* workspace,
                                          size_t workspace_bytes, void* stream)
 {
     if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype) ||
-        boundary_capacity < 0 || !heads_ok(H, Hk))
+        boundary_capacity < 0 || !heads_ok(H, Hk) || (flags & ~CPR_QK_L2NORM))
         return CPR_ERR_INVALID_ARG;
     if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
     if (n_seqs == 0) return CPR_OK;
@@ -198,6 +201,7 @@ int32_t cpr_gdn_prefill_continue_grouped(const void* q, const void* k, const voi
     a.total_tokens = total_tokens;
     a.H = H;
     a.Hk = Hk;
+    a.qk_norm = (flags & CPR_QK_L2NORM) ? 1 : 0;
     a.state_in = state;
     a.out = out;
     a.state_out = state;
@@ -269,10 +273,11 @@ int32_t cpr_gdn_ring_from_prefill_grouped(const void* k, const void* v, const fl
 
 int32_t cpr_gdn_decode_grouped(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                float* state, const cpr_gdn_ring* ring, const int32_t* pos, int32_t B, int32_t H,
-                               int32_t Hk, int32_t dk, int32_t dv, int32_t C, int32_t dtype, void* out,
+                               int32_t Hk, uint32_t flags, int32_t dk, int32_t dv, int32_t C, int32_t dtype, void* out,
                                void* workspace, size_t workspace_bytes, void* stream)
 {
-    if (B < 0 || H <= 0 || H > 65535 || !dtype_ok(dtype) || !heads_ok(H, Hk)) return CPR_ERR_INVALID_ARG;
+    if (B < 0 || H <= 0 || H > 65535 || !dtype_ok(dtype) || !heads_ok(H, Hk) || (flags & ~CPR_QK_L2NORM))
+        return CPR_ERR_INVALID_ARG;
     if (!shape_built(dk, dv, C)) return CPR_ERR_UNSUPPORTED_SHAPE;
     if (B == 0) return CPR_OK;
     if (!q || !k || !v || !g || !beta || !state || !ring || !pos || !out || !ring->S_b || !ring->k || !ring->v ||
@@ -297,6 +302,7 @@ int32_t cpr_gdn_decode_grouped(const void* q, const void* k, const void* v, cons
     a.B = B;
     a.H = H;
     a.Hk = Hk;
+    a.qk_norm = (flags & CPR_QK_L2NORM) ? 1 : 0;
     a.out = out;
     a.status = static_cast<uint32_t*>(workspace);
     a.num_sms = num_sms();
@@ -346,7 +352,7 @@ int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float
                         float* boundary_states, int64_t boundary_capacity, void* workspace,
                         size_t workspace_bytes, void* stream)
 {
-    return cpr_gdn_prefill_grouped(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, H, H, dk, dv, C, dtype,
+    return cpr_gdn_prefill_grouped(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, H, H, 0u, dk, dv, C, dtype,
                                    state_in, out, state_out, boundary_states, boundary_capacity, workspace,
                                    workspace_bytes, stream);
 }
@@ -357,7 +363,7 @@ int32_t cpr_gdn_prefill_continue(const void* q, const void* k, const void* v, co
                                  const cpr_gdn_ring* ring, void* out, float* boundary_states,
                                  int64_t boundary_capacity, void* workspace, size_t workspace_bytes, void* stream)
 {
-    return cpr_gdn_prefill_continue_grouped(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, H, H, dk, dv, C,
+    return cpr_gdn_prefill_continue_grouped(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, H, H, 0u, dk, dv, C,
                                             dtype, pos0, state, ring, out, boundary_states, boundary_capacity,
                                             workspace, workspace_bytes, stream);
 }
@@ -376,7 +382,7 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
                        int32_t dv, int32_t C, int32_t dtype, void* out, void* workspace, size_t workspace_bytes,
                        void* stream)
 {
-    return cpr_gdn_decode_grouped(q, k, v, g, beta, state, ring, pos, B, H, H, dk, dv, C, dtype, out, workspace,
+    return cpr_gdn_decode_grouped(q, k, v, g, beta, state, ring, pos, B, H, H, 0u, dk, dv, C, dtype, out, workspace,
                                   workspace_bytes, stream);
 }
 

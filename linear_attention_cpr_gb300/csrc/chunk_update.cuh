@@ -31,8 +31,8 @@ struct PrepSmem {
 
 // The key Gram matrix kk = K K^T of one chunk on the tensor cores: one M = 64, N = C,
 // K = DK tcgen05 product (rows r, columns i) of the keys' bf16 splits.  bf16 keys are
-// their own hi split (lo = 0), so one product is the whole sum; fp32 keys take three
-// (hi*hi + hi*lo + lo*hi).  The tile holds C rows per split; rows C..63 of the M = 64
+// their own hi split (lo = 0), so one product is the whole sum; fp32 keys, and keys
+// normalised in the kernel, take three (hi*hi + hi*lo + lo*hi).  The tile holds C rows per split; rows C..63 of the M = 64
 // A operand read whatever follows (their accumulator rows are never used), so the
 // region must span SPAN bytes.
 template <int DK, int C, typename T>
@@ -46,13 +46,15 @@ struct KKCfg {
 // G, e, d, beta*e and the strictly lower-triangular A (stored transposed: At[i][r] =
 // A_ri) from kf, g (in G) and beta (in bs); ktile: scratch of KKCfg::SPAN bytes for the
 // key tile; TMEM columns [tmem, tmem + C) hold kk; the product's completion arrives on
-// mbar with the given parity.  All DK + DV threads; contains __syncthreads.  Returns
+// mbar with the given parity.  keys_as_given: kf holds the keys exactly as stored (not
+// normalised in the kernel).  All DK + DV threads; contains __syncthreads.  Returns
 // false (uniformly) when the product's wait timed out; A is then undefined.
 template <int DK, int DV, int C, typename T>
 __device__ __forceinline__ bool chunk_decays_and_A(const PrepSmem<DK, C>& s, unsigned char* ktile, uint32_t tmem,
-                                                   uint64_t* mbar, uint32_t parity)
+                                                   uint64_t* mbar, uint32_t parity, bool keys_as_given)
 {
     using KC = KKCfg<DK, C, T>;
+    const bool three = KC::NSPLIT == 2 || !keys_as_given;  // uniform
     constexpr int KS = PrepSmem<DK, C>::KS;
     constexpr int NWARP = (DK + DV) / 32;
     static_assert(NWARP >= 4 || C <= 16 * NWARP, "every TMEM lane quadrant holding kk rows needs a warp");
@@ -64,7 +66,7 @@ __device__ __forceinline__ bool chunk_decays_and_A(const PrepSmem<DK, C>& s, uns
 #pragma unroll
         for (int e = 0; e < 8; ++e) xs[e] = s.kf[r * KS + c0 + e];
         const uint32_t off = tc::tile_off<2>(r, c0, DK);
-        tc::split8_store(xs, ktile + off, KC::NSPLIT == 2 ? ktile + KC::SPLIT + off : nullptr);
+        tc::split8_store(xs, ktile + off, three ? ktile + KC::SPLIT + off : nullptr);
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
@@ -75,7 +77,7 @@ __device__ __forceinline__ bool chunk_decays_and_A(const PrepSmem<DK, C>& s, uns
         const uint32_t ko = tc::smem_u32(ktile);
         const uint32_t ha[3] = {0u, 0u, 1u}, hb[3] = {0u, 1u, 0u};
 #pragma unroll
-        for (int p = 0; p < (KC::NSPLIT == 2 ? 3 : 1); ++p)
+        for (int p = 0; p < (three ? 3 : 1); ++p)
 #pragma unroll
             for (int k = 0; k < DK / 16; ++k)
                 tc::mma_bf16(tmem, tc::sdesc(ko + ha[p] * KC::SPLIT + k * 256, 128, SBO),
@@ -190,7 +192,8 @@ struct UCfg {
 };
 
 // Build both prep operands in shared memory from the chunk's keys (s.kf, fp32), g (s.G)
-// and beta (s.bs); V element (r, n) at vbase[r * vstride + n].  All DK + DV threads;
+// and beta (s.bs); V element (r, n) at vbase[r * vstride + n]; keys_as_given as for
+// chunk_decays_and_A.  All DK + DV threads;
 // contains __syncthreads.  Three phases of mbar (the key Gram product, the Z product),
 // counted by `phase`; TMEM columns [tmem, tmem + C) are scratch.  On a true return aop
 // holds Z^T = (D K)^T T and bop the right-hand sides [W0 | U0]^T, both as bf16 splits
@@ -198,13 +201,13 @@ struct UCfg {
 template <int DK, int DV, int C, typename T>
 __device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned char* aop, unsigned char* bop,
                                               const T* vbase, size_t vstride, uint32_t tmem, uint64_t* mbar,
-                                              uint32_t& phase)
+                                              uint32_t& phase, bool keys_as_given)
 {
     using U = UCfg<DK, DV, C>;
     constexpr int KS = PrepSmem<DK, C>::KS;
     constexpr uint32_t TT_SPLIT = C * C * 2;  // one bf16 split of the T^T tile
     const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
-    if (!chunk_decays_and_A<DK, DV, C, T>(s, aop, tmem, mbar, phase & 1)) return false;
+    if (!chunk_decays_and_A<DK, DV, C, T>(s, aop, tmem, mbar, phase & 1, keys_as_given)) return false;
     ++phase;
     // (D K)^T rows c: d_r * k_r[c] (zero rows beyond DK)
     for (int row = tid; row < U::MPAD; row += nt) {

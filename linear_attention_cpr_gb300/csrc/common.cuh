@@ -67,6 +67,7 @@ struct PrefillArgs {
     int64_t total_tokens;
     int32_t H;   // value heads (states, v, g, beta, o)
     int32_t Hk;  // query/key heads: value head h reads q/k head h / (H / Hk)
+    int32_t qk_norm;  // queries and keys L2-normalised in the kernels (CPR_QK_L2NORM)
     const float* state_in;
     void* out;
     float* state_out;
@@ -96,7 +97,8 @@ struct DecodeArgs {
     const int32_t* pos;
     int32_t B;
     int32_t H;
-    int32_t Hk;  // as PrefillArgs::Hk
+    int32_t Hk;       // as PrefillArgs::Hk
+    int32_t qk_norm;  // as PrefillArgs::qk_norm
     void* out;
     uint32_t* status;
     int num_sms;

@@ -118,6 +118,24 @@ __device__ __forceinline__ void token_step(float (&s)[DK / 8][DV / 32], const fl
     }
 }
 
+// The token's key and query (shared, fp32) L2-normalised in place by the whole CTA: the
+// two inverse norms by two threads of different warps (into scratch[0..1]), then one
+// product per entry (two for the query) -- the arithmetic of l2_normalise_row.  Contains
+// two __syncthreads.
+template <int DK>
+__device__ __forceinline__ void l2_normalise_qk(float* kf, float* qf, float* scratch)
+{
+    const int tid = threadIdx.x;
+    if (tid == 0) scratch[0] = l2_inv<DK>([&](int c) { return kf[c]; });
+    if (tid == 32) scratch[1] = l2_inv<DK>([&](int c) { return qf[c]; });
+    __syncthreads();
+    for (int c = tid; c < DK; c += blockDim.x) {
+        kf[c] = __fmul_rn(kf[c], scratch[0]);
+        qf[c] = __fmul_rn(__fmul_rn(qf[c], scratch[1]), query_scale<DK>());
+    }
+    __syncthreads();
+}
+
 // ------------------------------------------------------------------------------------
 // k4: decode step.  One CTA per (sequence, head), 8 warps: warp m owns key rows
 // [m*DK/8, (m+1)*DK/8) of the stored state (chain m of the canonical dot) and lane l
@@ -133,7 +151,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
     __shared__ __align__(16) float qf[DK];
     __shared__ __align__(16) float part[8][DV];
     __shared__ __align__(16) float part2[8][DV];
-    __shared__ float sc[2];
+    __shared__ float sc[4];
 
     // grid (sequence, query/key head, value head within its group): no division for the head
     const int b = blockIdx.x, h = blockIdx.y * gridDim.z + blockIdx.z, tid = threadIdx.x, H = a.H;
@@ -172,6 +190,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 #pragma unroll
     for (int t = 0; t < L; ++t) VecF<VPT>::load(st + (size_t)t * DV, s[t]);
     __syncthreads();
+    if (a.qk_norm) l2_normalise_qk<DK>(kf, qf, sc + 2);
 
     const float alpha = sc[0], beta = sc[1];
 #pragma unroll
@@ -227,7 +246,7 @@ __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t
     __shared__ __align__(16) float qf[DK];
     __shared__ __align__(16) float part[8][DV];
     __shared__ __align__(16) float part2[8][DV];
-    __shared__ float sc[2];
+    __shared__ float sc[4];
 
     const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
     const int m = tid >> 5, lane = tid & 31;
@@ -265,6 +284,7 @@ __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t
             a.ring.beta[nh * C + r] = bb;
         }
         __syncthreads();
+        if (a.qk_norm) l2_normalise_qk<DK>(kf, qf, sc + 2);
         token_step<DK, DV, T>(s, kf, qf, part, part2, sc[0], sc[1], v + tok * DV, out + tok * DV,
                               t + 1 == f ? st : nullptr);
         __syncthreads();  // kf, qf, sc and the partial sums are rewritten for the next token
@@ -301,6 +321,7 @@ __device__ __forceinline__ void completing_token_output(const DecodeArgs& a, siz
         qf[idx] = to_f32<T>(q[bhk * DK + idx]);
     }
     __syncthreads();
+    if (a.qk_norm) l2_normalise_qk<DK>(kf, qf, part);  // (part is free until the dots)
     if (tid < DV) {
         const int i = tid;
         const float* S = a.state + bh * DK * DV + i;  // S[c][i] at c * DV
@@ -369,8 +390,12 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
         s.G[tid] = ring_slot ? a.ring.g[bh * C + tid] : a.g[bh];
         s.bs[tid] = ring_slot ? a.ring.beta[bh * C + tid] : a.beta[bh];
     }
+    if (a.qk_norm) {  // the chunk's keys L2-normalised in place, one row per thread
+        __syncthreads();
+        if (tid < C) l2_normalise_row<DK>(s.kf + tid * KS, [](int cc) { return cc; }, false);
+    }
     tc::fence_before_sync();
-    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, vsm, (size_t)DV, tmem, mbar, phase);
+    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, vsm, (size_t)DV, tmem, mbar, phase, !a.qk_norm);
     if (!ok) return false;
     tc::fence_after_sync();
     if (tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
@@ -609,6 +634,7 @@ cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, f
     d.B = a.n_seqs;
     d.H = a.H;
     d.Hk = a.Hk;
+    d.qk_norm = a.qk_norm;
     d.out = a.out;
     d.status = a.status;
     d.num_sms = a.num_sms;

@@ -101,6 +101,50 @@ __device__ __forceinline__ float step_s(float s, float alpha, float u, float kj)
 }
 
 // ----------------------------------------------------------------------------------
+// In-kernel L2 normalisation of queries and keys (the CPR_QK_L2NORM option): a key becomes
+// k / sqrt(sum k^2 + eps), a query q / sqrt(sum q^2 + eps) * dk^-1/2.  The sum of squares
+// runs in dot_dk's order (eight chains over contiguous blocks of dk/8 entries, first term a
+// product, then the canonical tree); the square root and the reciprocal are correctly
+// rounded; then one product per entry (two for a query, the scale last).  x(c) is entry c.
+// ----------------------------------------------------------------------------------
+constexpr float kL2Eps = 1e-6f;
+
+template <int DK>
+__device__ __forceinline__ constexpr float query_scale()
+{
+    static_assert(DK == 32 || DK == 64 || DK == 128, "dk^-1/2 for the built shapes");
+    return DK == 32 ? 0x1.6a09e6p-3f : DK == 64 ? 0x1.0p-3f : 0x1.6a09e6p-4f;  // 1/sqrt(dk), rounded
+}
+
+template <int DK, typename F>
+__device__ __forceinline__ float l2_inv(F x)
+{
+    constexpr int L = DK / 8;
+    float c[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        float acc = __fmul_rn(x(m * L), x(m * L));
+#pragma unroll
+        for (int t = 1; t < L; ++t) acc = __fmaf_rn(x(m * L + t), x(m * L + t), acc);
+        c[m] = acc;
+    }
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(tree8(c[0], c[1], c[2], c[3], c[4], c[5], c[6], c[7]), kL2Eps)));
+}
+
+// Normalise a row held in shared memory (entry c at row[pos(c)]), in place; `query` adds
+// the dk^-1/2 scale.  One thread per row.
+template <int DK, typename P>
+__device__ __forceinline__ void l2_normalise_row(float* row, P pos, bool query)
+{
+    const float inv = l2_inv<DK>([&](int c) { return row[pos(c)]; });
+#pragma unroll 8
+    for (int c = 0; c < DK; ++c) {
+        const float y = __fmul_rn(row[pos(c)], inv);
+        row[pos(c)] = query ? __fmul_rn(y, query_scale<DK>()) : y;
+    }
+}
+
+// ----------------------------------------------------------------------------------
 // Chunk-update pieces.  Tile functions compute 4 x 4 blocks of one contraction; each
 // element's sequence is the one stated above whatever tile or thread computes it.
 // ----------------------------------------------------------------------------------

@@ -171,9 +171,14 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if (a.qk_norm) {  // the keys L2-normalised in place, one row per thread
+        if (tid < C) l2_normalise_row<DK>(s.kf + tid * KS, [](int cc) { return cc; }, false);
+        __syncthreads();
+    }
     const uint32_t tmem = *tslot;
     uint32_t phase = 0;
-    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, v + ((size_t)t0 * H + h) * DV, (size_t)H * DV, tmem, mbar, phase);
+    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, v + ((size_t)t0 * H + h) * DV, (size_t)H * DV, tmem, mbar, phase,
+                                          !a.qk_norm);
     tc::fence_after_sync();
     if (ok && tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
     ok = __syncthreads_and(ok && tc::mbar_wait(mbar, phase & 1));  // uniform: the epilogue's TMEM loads are warp-wide
@@ -587,6 +592,17 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
     if (tid < len) {
         al[tid] = decay_exp(a.g[(t0 + tid) * H + hd]);
         bt[tid] = a.beta[(t0 + tid) * H + hd];
+    }
+    if (a.qk_norm) {  // keys and queries L2-normalised in place, one row per thread
+        named_bar(bar, NT);
+        if (tid < 2 * len) {
+            const bool query = tid >= len;
+            float* row = query ? qp + (tid - len) * ROW : kp + tid * ROW;
+            l2_normalise_row<DK>(row, [](int cc) {
+                const int hh = cc / (DK / 2), jl = cc % (DK / 2);
+                return hh * (DK / 2 + 4) + 2 * (jl % (DK / 4)) + jl / (DK / 4);
+            }, query);
+        }
     }
     // the chunk's boundary state comes from the chain CTAs of this launch: wait until it is
     // published (bounded)
