@@ -46,15 +46,15 @@ struct KKCfg {
 // G, e, d, beta*e and the strictly lower-triangular A (stored transposed: At[i][r] =
 // A_ri) from kf, g (in G) and beta (in bs); ktile: scratch of KKCfg::SPAN bytes for the
 // key tile; TMEM columns [tmem, tmem + C) hold kk; the product's completion arrives on
-// mbar with the given parity.  keys_as_given: kf holds the keys exactly as stored (not
+// mbar with the given parity.  KEYS_AS_GIVEN: kf holds the keys exactly as stored (not
 // normalised in the kernel).  All DK + DV threads; contains __syncthreads.  Returns
 // false (uniformly) when the product's wait timed out; A is then undefined.
-template <int DK, int DV, int C, typename T>
+template <int DK, int DV, int C, typename T, bool KEYS_AS_GIVEN>
 __device__ __forceinline__ bool chunk_decays_and_A(const PrepSmem<DK, C>& s, unsigned char* ktile, uint32_t tmem,
-                                                   uint64_t* mbar, uint32_t parity, bool keys_as_given)
+                                                   uint64_t* mbar, uint32_t parity)
 {
     using KC = KKCfg<DK, C, T>;
-    const bool three = KC::NSPLIT == 2 || !keys_as_given;  // uniform
+    constexpr bool three = KC::NSPLIT == 2 || !KEYS_AS_GIVEN;
     constexpr int KS = PrepSmem<DK, C>::KS;
     constexpr int NWARP = (DK + DV) / 32;
     static_assert(NWARP >= 4 || C <= 16 * NWARP, "every TMEM lane quadrant holding kk rows needs a warp");
@@ -192,22 +192,22 @@ struct UCfg {
 };
 
 // Build both prep operands in shared memory from the chunk's keys (s.kf, fp32), g (s.G)
-// and beta (s.bs); V element (r, n) at vbase[r * vstride + n]; keys_as_given as for
+// and beta (s.bs); V element (r, n) at vbase[r * vstride + n]; KEYS_AS_GIVEN as for
 // chunk_decays_and_A.  All DK + DV threads;
 // contains __syncthreads.  Three phases of mbar (the key Gram product, the Z product),
 // counted by `phase`; TMEM columns [tmem, tmem + C) are scratch.  On a true return aop
 // holds Z^T = (D K)^T T and bop the right-hand sides [W0 | U0]^T, both as bf16 splits
 // visible to the tensor cores; false (uniform) means a product timed out.
-template <int DK, int DV, int C, typename T>
+template <int DK, int DV, int C, typename T, bool KEYS_AS_GIVEN>
 __device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned char* aop, unsigned char* bop,
                                               const T* vbase, size_t vstride, uint32_t tmem, uint64_t* mbar,
-                                              uint32_t& phase, bool keys_as_given)
+                                              uint32_t& phase)
 {
     using U = UCfg<DK, DV, C>;
     constexpr int KS = PrepSmem<DK, C>::KS;
     constexpr uint32_t TT_SPLIT = C * C * 2;  // one bf16 split of the T^T tile
     const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
-    if (!chunk_decays_and_A<DK, DV, C, T>(s, aop, tmem, mbar, phase & 1, keys_as_given)) return false;
+    if (!chunk_decays_and_A<DK, DV, C, T, KEYS_AS_GIVEN>(s, aop, tmem, mbar, phase & 1)) return false;
     ++phase;
     // (D K)^T rows c: d_r * k_r[c] (zero rows beyond DK)
     for (int row = tid; row < U::MPAD; row += nt) {

@@ -143,7 +143,7 @@ __device__ __forceinline__ void l2_normalise_qk(float* kf, float* qf, float* scr
 // every value column's dot is finished by the canonical tree.  Sequences whose token
 // completes a chunk are left to k5 (their stepped state is replaced by the resync).
 // ------------------------------------------------------------------------------------
-template <int DK, int DV, int C, typename T>
+template <int DK, int DV, int C, typename T, bool QK_NORM>
 __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 {
     constexpr int L = DK / 8, VPT = DV / 32;
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 #pragma unroll
     for (int t = 0; t < L; ++t) VecF<VPT>::load(st + (size_t)t * DV, s[t]);
     __syncthreads();
-    if (a.qk_norm) l2_normalise_qk<DK>(kf, qf, sc + 2);
+    if (QK_NORM) l2_normalise_qk<DK>(kf, qf, sc + 2);  // (a separate build: the usual one is untouched)
 
     const float alpha = sc[0], beta = sc[1];
 #pragma unroll
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t
 // over their DK/8 rows, the canonical tree, u, then the chains of S' q over the stepped
 // rows).  Threads i < DV take column i; the stepped state itself is not kept.  kf, qf:
 // DK floats of shared scratch each, part: 8 * DV.  Ends with a barrier.
-template <int DK, int DV, int C, typename T>
+template <int DK, int DV, int C, typename T, bool QK_NORM>
 __device__ __forceinline__ void completing_token_output(const DecodeArgs& a, size_t bh, float* kf, float* qf,
                                                         float* part)
 {
@@ -321,7 +321,7 @@ __device__ __forceinline__ void completing_token_output(const DecodeArgs& a, siz
         qf[idx] = to_f32<T>(q[bhk * DK + idx]);
     }
     __syncthreads();
-    if (a.qk_norm) l2_normalise_qk<DK>(kf, qf, part);  // (part is free until the dots)
+    if (QK_NORM) l2_normalise_qk<DK>(kf, qf, part);  // (part is free until the dots)
     if (tid < DV) {
         const int i = tid;
         const float* S = a.state + bh * DK * DV + i;  // S[c][i] at c * DV
@@ -349,7 +349,7 @@ __device__ __forceinline__ void completing_token_output(const DecodeArgs& a, siz
     }
     __syncthreads();  // every read of the old state is done before the resync replaces it
 }
-template <int DK, int DV, int C, typename T>
+template <int DK, int DV, int C, typename T, bool QK_NORM>
 __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, unsigned char* sm5, uint32_t tmem,
                                            uint64_t* mbar, uint32_t& phase)
 {
@@ -374,7 +374,7 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     const T* tk = a.resync_only ? rk + (size_t)(C - 1) * DK : static_cast<const T*>(a.k) + bhk * DK;
     const T* tv = a.resync_only ? rv + (size_t)(C - 1) * DV : static_cast<const T*>(a.v) + bh * DV;
     if (!a.resync_only)
-        completing_token_output<DK, DV, C, T>(a, bh, reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5) + DK,
+        completing_token_output<DK, DV, C, T, QK_NORM>(a, bh, reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5) + DK,
                                               reinterpret_cast<float*>(sm5) + 2 * DK);
 
     for (int idx = tid; idx < C * DK; idx += blockDim.x) {
@@ -390,12 +390,12 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
         s.G[tid] = ring_slot ? a.ring.g[bh * C + tid] : a.g[bh];
         s.bs[tid] = ring_slot ? a.ring.beta[bh * C + tid] : a.beta[bh];
     }
-    if (a.qk_norm) {  // the chunk's keys L2-normalised in place, one row per thread
+    if (QK_NORM) {  // the chunk's keys L2-normalised in place, one row per thread
         __syncthreads();
         if (tid < C) l2_normalise_row<DK>(s.kf + tid * KS, [](int cc) { return cc; }, false);
     }
     tc::fence_before_sync();
-    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, vsm, (size_t)DV, tmem, mbar, phase, !a.qk_norm);
+    bool ok = prep_operands<DK, DV, C, T, !QK_NORM>(s, aop, bop, vsm, (size_t)DV, tmem, mbar, phase);
     if (!ok) return false;
     tc::fence_after_sync();
     if (tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
@@ -429,7 +429,7 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     return true;
 }
 
-template <int DK, int DV, int C, typename T>
+template <int DK, int DV, int C, typename T, bool QK_NORM>
 __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
 {
     using U = UCfg<DK, DV, C>;
@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
     uint32_t phase = 0;
     for (uint32_t it = blockIdx.x; it < items; it += gridDim.x) {
         const int b = seq_of_rank((int)(it / a.H));
-        if (!resync_one<DK, DV, C, T>(a, b, (int)(it % a.H), sm5, tmem, mbar, phase)) {
+        if (!resync_one<DK, DV, C, T, QK_NORM>(a, b, (int)(it % a.H), sm5, tmem, mbar, phase)) {
             if (tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
             break;  // uniform: the barrier's phase is unknown after a timeout
         }
@@ -585,13 +585,17 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     if ((e = cudaStreamWaitEvent(ss->stream, ss->fork, 0)) != cudaSuccess) return e;
     // dynamic shared memory also caps the CTAs per SM so their TMEM columns fit in 512
     const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::rs_bytes(sizeof(T)), tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
-    e = cudaFuncSetAttribute(k5_resync<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
+    auto k5 = a.qk_norm ? k5_resync<DK, DV, C, T, true> : k5_resync<DK, DV, C, T, false>;
+    e = cudaFuncSetAttribute(k5, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
     if (e != cudaSuccess) return e;
     // at most half the SMs, so the step kernel keeps the rest while the resync runs
     const int grid = std::max(1, std::min(a.B * a.H, std::max(1, a.num_sms / 2) * (int)(232448 / sm5)));
-    k5_resync<DK, DV, C, T><<<grid, DK + DV, sm5, ss->stream>>>(a);
+    k5<<<grid, DK + DV, sm5, ss->stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k4_decode_step<DK, DV, C, T><<<dim3(a.B, a.Hk, a.H / a.Hk), 256, 0, s>>>(a);
+    if (a.qk_norm)
+        k4_decode_step<DK, DV, C, T, true><<<dim3(a.B, a.Hk, a.H / a.Hk), 256, 0, s>>>(a);
+    else
+        k4_decode_step<DK, DV, C, T, false><<<dim3(a.B, a.Hk, a.H / a.Hk), 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_mark(1, s);
     // join: work issued on s after this call sees the resync's results
@@ -642,10 +646,11 @@ cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, f
     k8_chunk_fill<DK, DV, C, T><<<dim3((unsigned)a.n_seqs, a.H), 256, 0, s>>>(d, a.cu_seqlens, pos0, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::rs_bytes(sizeof(T)), tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
-    e = cudaFuncSetAttribute(k5_resync<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
+    auto k5 = d.qk_norm ? k5_resync<DK, DV, C, T, true> : k5_resync<DK, DV, C, T, false>;
+    e = cudaFuncSetAttribute(k5, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
     if (e != cudaSuccess) return e;
     const int grid = std::max(1, std::min(a.n_seqs * a.H, a.num_sms * (int)(232448 / sm5)));
-    k5_resync<DK, DV, C, T><<<grid, DK + DV, sm5, s>>>(d);
+    k5<<<grid, DK + DV, sm5, s>>>(d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     PrefillArgs p = a;
     p.state_in = state;

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(1024) k0_chunk_index(const int32_t* __restrict
 // shared-memory image the chain kernel copies in one piece, B^T as fp32 rows.
 // Exits for partial chunks.
 // ------------------------------------------------------------------------------------
-template <int DK, int DV, int C, typename T, bool GROUPED>
+template <int DK, int DV, int C, typename T, bool GROUPED, bool QK_NORM>
 __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
 {
     using U = UCfg<DK, DV, C>;
@@ -171,14 +171,14 @@ __global__ void __launch_bounds__(DK + DV) k1_chunk_prep(PrefillArgs a)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (a.qk_norm) {  // the keys L2-normalised in place, one row per thread
+    if (QK_NORM) {  // the keys L2-normalised in place, one row per thread
         if (tid < C) l2_normalise_row<DK>(s.kf + tid * KS, [](int cc) { return cc; }, false);
         __syncthreads();
     }
     const uint32_t tmem = *tslot;
     uint32_t phase = 0;
-    bool ok = prep_operands<DK, DV, C, T>(s, aop, bop, v + ((size_t)t0 * H + h) * DV, (size_t)H * DV, tmem, mbar, phase,
-                                          !a.qk_norm);
+    bool ok = prep_operands<DK, DV, C, T, !QK_NORM>(s, aop, bop, v + ((size_t)t0 * H + h) * DV, (size_t)H * DV, tmem,
+                                                   mbar, phase);
     tc::fence_after_sync();
     if (ok && tid == 0) prep_mma<DK, DV, C>(tmem, aop, bop, mbar);
     ok = __syncthreads_and(ok && tc::mbar_wait(mbar, phase & 1));  // uniform: the epilogue's TMEM loads are warp-wide
@@ -728,17 +728,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
 
     // dynamic shared memory also caps the CTAs per SM so their TMEM columns fit in 512
     const size_t sm1 = std::max<size_t>(UCfg<DK, DV, C>::PREP_SMEM, tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
-    if (a.Hk == a.H) {
-        e = cudaFuncSetAttribute(k1_chunk_prep<DK, DV, C, T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sm1);
-        if (e != cudaSuccess) return e;
-        k1_chunk_prep<DK, DV, C, T, false><<<dim3((unsigned)a.max_chunks, a.H), DK + DV, sm1, s>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(k1_chunk_prep<DK, DV, C, T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sm1);
-        if (e != cudaSuccess) return e;
-        k1_chunk_prep<DK, DV, C, T, true><<<dim3((unsigned)a.max_chunks, a.Hk, a.H / a.Hk), DK + DV, sm1, s>>>(a);
-    }
+    // separate builds for grouped heads and for normalised keys: the usual one is untouched
+    auto k1 = (a.Hk == a.H) ? (a.qk_norm ? k1_chunk_prep<DK, DV, C, T, false, true> : k1_chunk_prep<DK, DV, C, T, false, false>)
+                            : (a.qk_norm ? k1_chunk_prep<DK, DV, C, T, true, true> : k1_chunk_prep<DK, DV, C, T, true, false>);
+    e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
+    if (e != cudaSuccess) return e;
+    k1<<<dim3((unsigned)a.max_chunks, a.Hk, a.H / a.Hk), DK + DV, sm1, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     profile_mark(2, s);
