@@ -34,8 +34,8 @@ L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
 # of the kernel as it now stands: k23_chain_and_intra at trainer_fwd, k4_decode_step at
 # rollout_decode.  Reset to None whenever the kernel changes.
-TRAFFIC_K23_TRAINER_FWD = 462.891008e6 + 180.198144e6
-TRAFFIC_K4_ROLLOUT_DECODE = 267.599872e6 + 206.738176e6
+TRAFFIC_K23_TRAINER_FWD = 462.875904e6 + 178.874624e6
+TRAFFIC_K4_ROLLOUT_DECODE = 267.607808e6 + 206.803712e6
 
 
 def _peaks():
@@ -405,7 +405,7 @@ def run_decode(args, cpr, inputs, dev, hbm_peak, dist, world):
         "metric": "decode steps/s per layer", "value": 1e3 / ms * world, "unit": "steps/s",
         "ms_per_step": ms, "steps": n_steps, "workload": f"rollout_decode: B={B}, H={H}, dk=dv={dk}, C={C}, "
         "prior lengths U[1,4096], state resident (> L2)",
-        "kernels_ms": {"decode_step": k4_ms, "resync": statistics.fmean(k5)},
+        "kernels_ms": {"step_with_concurrent_resync": k4_ms, "join": statistics.fmean(k5)},
         "resyncs_per_step": n_res / n_steps,
         "roofline": {"kernel": "k4_decode_step", "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
                      "frac": ach / hbm_peak, "traffic": TRAFFIC_K4_ROLLOUT_DECODE, "bytes_per_launch": step_only},
