@@ -302,6 +302,7 @@ def run_ours(args):
     if not args.no_decode:
         decode = run_decode(args, cpr, inputs, dev, hbm_peak, dist, world)
     continuation = run_continuation(args, cpr, inputs, dev, hbm_peak, dist, world) if not args.no_decode else None
+    pik_line = run_pik(args, cpr, inputs, dev, dist, world) if not args.no_pik else None
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only) ----------------
     cpu = None
@@ -323,10 +324,12 @@ def run_ours(args):
                         "frac_of_t_roof": t_roof_ms / ms_max, "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": hbm_kind},
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches + (decode["gpu_launches"] if decode else 0) +
-                            (continuation["gpu_launches"] if continuation else 0),
+                            (continuation["gpu_launches"] if continuation else 0) +
+                            (pik_line["gpu_launches"] if pik_line else 0),
             "clocks": clocks.summary(),
             "decode": decode,
             "continuation": continuation,
+            "pik": pik_line,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -495,6 +498,68 @@ def run_continuation(args, cpr, inputs, dev, hbm_peak, dist, world):
     }
 
 
+def _bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 8192^3, burst)"
+    return 1900.0, "fallback"
+
+
+def run_pik(args, cpr, inputs, dev, dist, world):
+    """Deterministic K-split product (pik): Y = X W^T with M = N = K = 8,192 and eight
+    leaves, as one call over the whole tree, and as two rank calls of four leaves each plus
+    the combine of their roots (the same bits).  The operands (2 x 128 MB) and the result
+    (256 MB) exceed L2, so no flush is needed between calls."""
+    M = N = K = 8192
+    L = 8
+    x, w = inputs.gemm_operands(M, N, K, seed=0, device=dev)
+    y = torch.empty(M, N, dtype=torch.float32, device=dev)
+    parts = torch.empty(2, M, N, dtype=torch.float32, device=dev)
+    ws = torch.empty(cpr.cpr_pik_workspace_size(), dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def whole():
+        cpr.cpr_pik_gemm(x, w, L, out=y, workspace=ws)
+
+    def two_ranks():
+        cpr.cpr_pik_gemm(x, w, L, (0, 4), out=parts[0], workspace=ws)
+        cpr.cpr_pik_gemm(x, w, L, (4, 8), out=parts[1], workspace=ws)
+        cpr.cpr_pik_combine(parts, out=y)
+
+    def timed(fn, steps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        _barrier(dist)
+        ms = []
+        for _ in range(steps):
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        _barrier(dist)
+        return _max_over_ranks(dist, statistics.fmean(ms))
+
+    steps = max(3, min(args.steps, 20))
+    ms = timed(whole, steps)
+    ms2 = timed(two_ranks, steps)
+    assert cpr.cpr_gdn_device_status(ws) == 0
+    flops = 2.0 * M * N * K
+    tf = flops / (ms * 1e-3) / 1e12
+    peak, kind = _bf16_peak()
+    return {
+        "metric": "pik deterministic K-split GEMM TFLOP/s", "value": tf * world, "unit": "TFLOP/s",
+        "ms_per_call": ms, "steps": steps,
+        "workload": f"Y = X W^T, M = N = K = {M}, bf16 operands, fp32 accumulation and result, {L} leaves",
+        "roofline": {"kernel": "k_pik_leaves", "bound": "tensor", "achieved": tf, "peak": peak, "peak_kind": kind,
+                     "unit": "TFLOP/s", "frac": tf / peak, "traffic": None, "flops_per_launch": flops},
+        "two_ranks_ms": ms2,
+        "gpu_launches": 4 * steps,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -505,6 +570,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=512)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pik", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -22,6 +22,9 @@ from .binding import (  # noqa: F401
     cpr_gdn_strerror,
     cpr_gdn_supported,
     cpr_gdn_version,
+    cpr_pik_combine,
+    cpr_pik_gemm,
+    cpr_pik_workspace_size,
     continue_chunks,
     load_library,
 )

@@ -27,6 +27,7 @@ EXPORTED = (
     "cpr_gdn_ring_from_prefill", "cpr_gdn_decode", "cpr_gdn_device_status", "cpr_gdn_set_profile_events",
     "cpr_gdn_prefill_noalloc", "cpr_gdn_prefill_continue", "cpr_gdn_prefill_grouped",
     "cpr_gdn_ring_from_prefill_grouped", "cpr_gdn_decode_grouped", "cpr_gdn_prefill_continue_grouped",
+    "cpr_pik_workspace_size", "cpr_pik_gemm", "cpr_pik_combine",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # CPR_GDN_NOALLOC_SCRATCH_BYTES
 
@@ -87,6 +88,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                          I32, I32, P, P, SZ, P]),
         "cpr_gdn_prefill_continue_grouped": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, U32, I32, I32, I32, I32, P,
                                                    P, ctypes.POINTER(_Ring), P, P, I64, P, SZ, P]),
+        "cpr_pik_workspace_size": (SZ, []),
+        "cpr_pik_gemm": (I32, [P, P, P, I32, I32, I32, I32, I32, I32, P, P]),
+        "cpr_pik_combine": (I32, [P, I32, I64, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -334,3 +338,44 @@ def cpr_gdn_prefill_noalloc(q, k, v, g, beta, cu_seqlens, C: int, state_in=None,
         _stream(stream))
     _check("cpr_gdn_prefill_noalloc", code)
     return out, state_out, boundary_states
+
+
+def cpr_pik_workspace_size() -> int:
+    return int(load_library().cpr_pik_workspace_size())
+
+
+def cpr_pik_gemm(x, w, n_leaves: int, leaves=None, *, out=None, workspace=None, stream=None):
+    """Deterministic K-split product Y = X W^T (x bf16 [M, K], w bf16 [N, K]; fp32 result):
+    the subtree root of leaves [lo, hi) = ``leaves`` of the fixed n_leaves-leaf tree, or
+    the whole product when ``leaves`` is None.  Returns (out, workspace)."""
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("x and w disagree on K")
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise TypeError("x and w must be bf16")
+    lo, hi = (0, n_leaves) if leaves is None else leaves
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(cpr_pik_workspace_size(), dtype=torch.uint8, device=x.device)
+    code = load_library().cpr_pik_gemm(_ptr(x), _ptr(w), _ptr(out), M, N, K, n_leaves, lo, hi, _ptr(workspace),
+                                       _stream(stream))
+    _check("cpr_pik_gemm", code)
+    return out, workspace
+
+
+def cpr_pik_combine(parts, *, out=None, stream=None):
+    """The top of the fixed tree over the subtree roots parts[0..P) (fp32 [P, ...]);
+    returns out (fp32, the shape of parts[0])."""
+    if parts.dtype != torch.float32:
+        raise TypeError("parts must be fp32")
+    P = parts.shape[0]
+    if out is None:
+        out = torch.empty(parts.shape[1:], dtype=torch.float32, device=parts.device)
+    count = out.numel()
+    if parts.numel() != P * count:
+        raise ValueError("out must hold one part")
+    code = load_library().cpr_pik_combine(_ptr(parts), P, count, _ptr(out), _stream(stream))
+    _check("cpr_pik_combine", code)
+    return out

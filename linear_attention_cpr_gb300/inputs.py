@@ -10,8 +10,8 @@ Value recipe (every workload):
   beta = sigmoid(N(0, 1));  initial state S_0 = 0.  q, k, v are rounded to bf16 unless
   the workload is fp32; g and beta stay fp32.  Draw order: q, k, v, g, beta.
 
-The pages measure real model activations (Qwen3.5 hybrid GDN layers during RL on
-DAPO-Math-17k); those are not available, and these synthetic tensors stand in for them
+The pages measure real model activations (the hybrid model's GDN layers during RL on a
+math-problem dataset); those are not available, and these synthetic tensors stand in for them
 with the shapes the pages' per-layer table quotes (1 x 10,240 tokens for the trainer,
 5 x 2,048 for rollout prefill, 256 sequences x 1 token for rollout decode).
 """
@@ -121,3 +121,14 @@ def random_tokens(T: int, H: int, dk: int, dv: int, dtype=torch.float32, seed: i
     """Tokens with the workload value recipe for arbitrary small shapes (tests)."""
     gen = torch.Generator(device=device).manual_seed(seed)
     return draw_tokens(T, H, dk, dv, dtype, gen, device)
+
+
+def gemm_operands(M: int, N: int, K: int, seed: int = 0, device="cpu"):
+    """Operands of the deterministic K-split product Y = X W^T: x [M, K] and w [N, K] in
+    bf16, entries N(0, 1) rounded to bf16 (the scale of normalised activations and of a
+    unit-variance weight; the product's entries then have standard deviation sqrt(K)).
+    Draw order: x, then w."""
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, K, generator=gen).to(torch.bfloat16)
+    w = torch.randn(N, K, generator=gen).to(torch.bfloat16)
+    return x.to(device), w.to(device)

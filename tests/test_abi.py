@@ -11,13 +11,16 @@ import linear_attention_cpr_gb300 as cpr
 from linear_attention_cpr_gb300 import binding, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "cpr_gdn.h")
+INCLUDE = os.path.join(ROOT, "include")
 
 
 def _declared():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(cpr_gdn_\w+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(cpr_\w+)\s*\(", text))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
