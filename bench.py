@@ -225,6 +225,13 @@ def run_ours(args):
     cpr.load_library()
     hbm_peak, hbm_kind = _peaks()
     gen_dev = torch.Generator(device=dev)
+    if args.only_pik:  # the deterministic K-split product alone (profiling and quick checks)
+        line = run_pik(args, cpr, inputs, dev, dist, world)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
 
     # ---------------- prefill: trainer-forward shape ----------------
     w = inputs.workload(args.workload)
@@ -509,9 +516,9 @@ def _bf16_peak():
 def run_pik(args, cpr, inputs, dev, dist, world):
     """Deterministic K-split product (pik): Y = X W^T with M = N = K = 8,192 and eight
     leaves, as one call over the whole tree, and as two rank calls of four leaves each plus
-    the combine of their roots (the same bits).  The operands (2 x 128 MB) and the result
+    the combine of their roots (the same bits); and the product under a four-leaf contract.  The operands (2 x 128 MB) and the result
     (256 MB) exceed L2, so no flush is needed between calls."""
-    M = N = K = 8192
+    M = N = K = args.pik_size
     L = 8
     x, w = inputs.gemm_operands(M, N, K, seed=0, device=dev)
     y = torch.empty(M, N, dtype=torch.float32, device=dev)
@@ -522,13 +529,16 @@ def run_pik(args, cpr, inputs, dev, dist, world):
     def whole():
         cpr.cpr_pik_gemm(x, w, L, out=y, workspace=ws)
 
+    def whole4():
+        cpr.cpr_pik_gemm(x, w, 4, out=y, workspace=ws)
+
     def two_ranks():
         cpr.cpr_pik_gemm(x, w, L, (0, 4), out=parts[0], workspace=ws)
         cpr.cpr_pik_gemm(x, w, L, (4, 8), out=parts[1], workspace=ws)
         cpr.cpr_pik_combine(parts, out=y)
 
     def timed(fn, steps):
-        for _ in range(3):
+        for _ in range(args.warmup):
             fn()
         torch.cuda.synchronize()
         _barrier(dist)
@@ -545,6 +555,7 @@ def run_pik(args, cpr, inputs, dev, dist, world):
     steps = max(3, min(args.steps, 20))
     ms = timed(whole, steps)
     ms2 = timed(two_ranks, steps)
+    ms4 = timed(whole4, steps)
     assert cpr.cpr_gdn_device_status(ws) == 0
     flops = 2.0 * M * N * K
     tf = flops / (ms * 1e-3) / 1e12
@@ -555,8 +566,8 @@ def run_pik(args, cpr, inputs, dev, dist, world):
         "workload": f"Y = X W^T, M = N = K = {M}, bf16 operands, fp32 accumulation and result, {L} leaves",
         "roofline": {"kernel": "k_pik_leaves", "bound": "tensor", "achieved": tf, "peak": peak, "peak_kind": kind,
                      "unit": "TFLOP/s", "frac": tf / peak, "traffic": None, "flops_per_launch": flops},
-        "two_ranks_ms": ms2,
-        "gpu_launches": 4 * steps,
+        "two_ranks_ms": ms2, "four_leaves_ms": ms4, "four_leaves_tflops": flops / (ms4 * 1e-3) / 1e12,
+        "gpu_launches": 5 * steps,
     }
 
 
@@ -571,6 +582,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pik", action="store_true")
+    ap.add_argument("--only-pik", action="store_true")
+    ap.add_argument("--pik-size", type=int, default=8192, help="M = N = K of the pik product (a multiple of 512)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -7,10 +7,12 @@
 // one binary tree over the leaves fixes how their partial sums meet, so the result does
 // not depend on how the leaves are shared among ranks.
 //
-// k_pik_leaves: one CTA per 128 x BN output tile.  Each leaf of the CTA's range
-// accumulates in its own TMEM slot of BN columns (BN = 128: up to four leaves; BN = 64:
-// up to eight, 512 columns either way), so the main loop never waits for a reduction; the
-// epilogue sums the slots with the tree in registers.  Operands are staged by every thread
+// k_pik_leaves: one CTA per 128 x 128 output tile.  Up to four leaves: each leaf of the
+// CTA's range accumulates in its own TMEM slot of 128 columns, the main loop never waits
+// for a reduction, and the epilogue sums the slots with the tree in registers.  Eight
+// leaves: slot popcount(j) takes leaf j, and as each odd leaf completes the loop waits for
+// its products and merges the finished pairs of the tree in TMEM (a binary counter: at
+// most four live partials), leaving the root in slot 0.  Operands are staged by every thread
 // with 16-byte cp.async into the no-swizzle K-major core-matrix layout (tc.cuh), six
 // stages of 64 K elements, and one thread issues the MMAs (4 per stage, K = 16 each) and
 // commits each stage to an mbarrier that frees it.  The leaf's instruction sequence, and
@@ -38,7 +40,7 @@ constexpr int kGroupM = 8;    // m-tiles per raster group (the concurrently runn
 
 template <int BN>
 struct PikCfg {
-    static constexpr int SLOTS = 512 / BN;  // leaf accumulators that fit in TMEM
+    static constexpr int SLOTS = 512 / BN;  // partial sums that fit in TMEM
     static constexpr uint32_t A_BYTES = kBM * kBK * 2, B_BYTES = BN * kBK * 2, STAGE = A_BYTES + B_BYTES;
     static constexpr uint32_t SBO = (kBK / 8) * 128;  // step between 8-row core groups
     static constexpr size_t BAR_OFF = (size_t)kStages * STAGE;
@@ -113,7 +115,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_pik_leaves(const PikArgs a)
     const int64_t m0 = (int64_t)(g0 + r % gsz) * kBM, n0 = (int64_t)(r / gsz) * BN;
 
     const int nl = a.leaf_hi - a.leaf_lo;
-    const uint32_t cols = nl * BN <= 32 ? 32u : nl * BN <= 64 ? 64u : nl * BN <= 128 ? 128u : nl * BN <= 256 ? 256u : 512u;
+    const bool merge = nl > Cf::SLOTS;  // more leaves than slots: merge pairs as they complete
+    const int used = merge ? Cf::SLOTS : nl;
+    const uint32_t cols = used * BN <= 32 ? 32u : used * BN <= 64 ? 64u : used * BN <= 128 ? 128u : used * BN <= 256 ? 256u : 512u;
     if (warp == 0) tc::tmem_alloc(tslot, cols);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) tc::mbar_init(&mma_done[s], 1);
@@ -146,7 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_pik_leaves(const PikArgs a)
         if (tid == 0) {
             tc::fence_after_sync();
             const uint32_t sa = tc::smem_u32(smem + (s % kStages) * Cf::STAGE), sb = sa + Cf::A_BYTES;
-            const uint32_t d = tmem + (uint32_t)((s / spl) * BN);
+            const int j = s / spl;  // leaf
+            const uint32_t d = tmem + (uint32_t)((merge ? __popc(j) : j) * BN);
             const bool first = (s % spl) == 0;  // a leaf's first instruction overwrites its slot
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
@@ -164,6 +169,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_pik_leaves(const PikArgs a)
             if (ok) load(nxt);
         }
         cp_async_commit();
+        if (merge && s % spl == spl - 1 && ((s / spl) & 1)) {
+            // leaf j (odd) is complete once its products are: merge the finished pairs, left
+            // (earlier leaves) + right, ctz(j + 1) levels, into the lower slot
+            const int j = s / spl;
+            ok = tc::mbar_wait(&mma_done[s % kStages], (uint32_t)((s / kStages) & 1)) && ok;
+            tc::fence_after_sync();
+            const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+            for (int top = __popc(j), m = __ffs(j + 1) - 1; m > 0; --m, --top) {
+#pragma unroll 1
+                for (int cb = 0; cb < BN / 32; ++cb) {
+                    float l[32], r[32];
+                    uint32_t o[32];
+                    const uint32_t dst = tmem + lanes + (uint32_t)((top - 1) * BN + cb * 32);
+                    tc::tmem_ld_32x32b<32>(dst, l);
+                    tc::tmem_ld_32x32b<32>(tmem + lanes + (uint32_t)(top * BN + cb * 32), r);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__fadd_rn(l[e], r[e]));
+                    tc::tmem_st_32x32b<32>(dst, o);
+                }
+                tc::tmem_wait_st();
+            }
+            tc::fence_before_sync();  // the next products are issued after the loop's barrier
+        }
     }
     if (S > 0) ok = tc::mbar_wait(&mma_done[(S - 1) % kStages], (uint32_t)(((S - 1) / kStages) & 1)) && ok;
     asm volatile("cp.async.wait_all;\n" ::: "memory");
@@ -172,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pik_leaves(const PikArgs a)
 
     if (!failed) {
         constexpr int MAXL = Cf::SLOTS, E = 8;
+        const int parts = merge ? 1 : nl;  // partials left in slots 0 .. parts-1
         const int row = warp * 32 + (tid & 31);
         const int64_t gm = m0 + row;
         const uint32_t lanes = (uint32_t)(warp * 32) << 16;
@@ -180,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_pik_leaves(const PikArgs a)
             float v[MAXL][E];
 #pragma unroll
             for (int l = 0; l < MAXL; ++l)
-                if (l < nl) tc::tmem_ld_32x32b<E>(tmem + lanes + (uint32_t)(l * BN + cb * E), v[l]);
-            leaf_tree<MAXL, E>(v, nl);
+                if (l < parts) tc::tmem_ld_32x32b<E>(tmem + lanes + (uint32_t)(l * BN + cb * E), v[l]);
+            leaf_tree<MAXL, E>(v, parts);
             const int64_t c0 = n0 + cb * E;
             if (gm < a.M) {
                 float* dst = a.y + gm * a.N + c0;
@@ -269,9 +298,7 @@ extern "C" int32_t cpr_pik_gemm(const void* x, const void* w, float* y, int32_t 
     PikArgs a{static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), y, M, N, K, n_leaves,
               leaf_lo, leaf_hi, (al16(y) && N % 4 == 0) ? 1 : 0, static_cast<uint32_t*>(workspace)};
     if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s) != cudaSuccess) return CPR_ERR_CUDA;
-    // The tile width is a function of the contract's leaf count alone, so every call of
-    // one contract runs the same instruction shape.
-    const cudaError_t e = n_leaves <= 4 ? launch_pik<128>(a, s) : launch_pik<64>(a, s);
+    const cudaError_t e = launch_pik<128>(a, s);
     return e == cudaSuccess ? CPR_OK : CPR_ERR_CUDA;
 }
 
