@@ -7,17 +7,22 @@
 // one binary tree over the leaves fixes how their partial sums meet, so the result does
 // not depend on how the leaves are shared among ranks.
 //
-// k_pik_leaves: one CTA per 128 x 128 output tile.  Up to four leaves: each leaf of the
-// CTA's range accumulates in its own TMEM slot of 128 columns, the main loop never waits
-// for a reduction, and the epilogue sums the slots with the tree in registers.  Eight
-// leaves: slot popcount(j) takes leaf j, and as each odd leaf completes the loop waits for
-// its products and merges the finished pairs of the tree in TMEM (a binary counter: at
-// most four live partials), leaving the root in slot 0.  Operands are staged by every thread
-// with 16-byte cp.async into the no-swizzle K-major core-matrix layout (tc.cuh), six
-// stages of 64 K elements, and one thread issues the MMAs (4 per stage, K = 16 each) and
-// commits each stage to an mbarrier that frees it.  The leaf's instruction sequence, and
-// so every bit of its partial, is the same whichever tile shape or leaf range a call uses.
+// k_pik_leaves: one CTA per 128 x 128 output tile, in clusters of 2 x 2 tiles.  A tile's
+// operands are 128 rows of X and 128 rows of W per 64 K elements; the two CTAs of a cluster
+// that share the X rows (same m) each load half of them (four of the eight 16-byte K
+// slabs) with TMA and multicast it to both, and likewise for the W rows of the two CTAs
+// that share n, so each CTA pulls half its operand bytes from L2.  Warp 0 issues the
+// loads into six stages, warp 1 issues the MMAs (4 per stage, K = 16 each) and commits
+// each stage to the stage-free barriers of all four CTAs; warps 4-7 merge partials and
+// run the epilogue.  Up to four leaves: each leaf of the CTA's range accumulates in its
+// own TMEM slot of 128 columns, the loop never waits for a reduction, and the epilogue
+// sums the slots with the tree in registers.  Eight leaves: slot popcount(j) takes leaf j;
+// when an odd leaf completes, warps 4-7 merge the finished pairs of the tree in TMEM (a
+// binary counter: at most four live partials) before the next leaf starts, leaving the
+// root in slot 0.  A leaf's instruction sequence, and so every bit of its partial, is the
+// same whichever leaf range a call covers.
 // k_pik_combine: the top of the same tree over the ranks' subtree roots (HBM-bound).
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -31,59 +36,56 @@
 namespace cpr {
 namespace {
 
-constexpr int kBM = 128;      // tile rows (M of the MMA instruction; row i in TMEM lane i)
-constexpr int kBK = 64;       // K elements per stage
-constexpr int kStages = 6;    // shared-memory stages
-constexpr int kLag = 2;       // products kept queued before a stage is refilled
-constexpr int kThreads = 128; // 4 warps: loads, epilogue (warp w reads lane quadrant w); thread 0 issues
-constexpr int kGroupM = 8;    // m-tiles per raster group (the concurrently running tiles share operands in L2)
-
-template <int BN>
-struct PikCfg {
-    static constexpr int SLOTS = 512 / BN;  // partial sums that fit in TMEM
-    static constexpr uint32_t A_BYTES = kBM * kBK * 2, B_BYTES = BN * kBK * 2, STAGE = A_BYTES + B_BYTES;
-    static constexpr uint32_t SBO = (kBK / 8) * 128;  // step between 8-row core groups
-    static constexpr size_t BAR_OFF = (size_t)kStages * STAGE;
-    static constexpr size_t SMEM = BAR_OFF + 128;
-};
+constexpr int kBM = 128;       // tile rows (M of the MMA instruction; row i in TMEM lane i)
+constexpr int kBN = 128;       // tile columns (N of the MMA instruction)
+constexpr int kBK = 64;        // K elements per stage: eight 16-byte slabs
+constexpr int kStages = 6;     // shared-memory stages
+constexpr int kThreads = 256;  // warp 0: loads, warp 1: MMAs, warps 4-7: merges and epilogue
+constexpr int kCluster = 4;    // 2 (m) x 2 (n) tiles; rank r holds m-offset r & 1, n-offset r >> 1
+constexpr int kGroupC = 4;     // cluster rows per raster group (concurrent tiles share operands in L2)
+constexpr int kSlots = 512 / kBN;  // partial sums that fit in TMEM
+constexpr uint32_t kSlab = kBM * 16;                 // one K slab of a 128-row operand tile (2 KB)
+constexpr uint32_t kOpBytes = 8 * kSlab;             // 16 KB per operand per stage
+constexpr uint32_t kStage = 2 * kOpBytes;            // X then W
+constexpr size_t kBarOff = (size_t)kStages * kStage;
+constexpr size_t kSmem = kBarOff + 256 + 1024;       // barriers, TMEM slot, alignment slack
 
 struct PikArgs {
-    const __nv_bfloat16* x;
-    const __nv_bfloat16* w;
     float* y;
     int32_t M, N, K, n_leaves, leaf_lo, leaf_hi;
     int vec_store;  // y rows start 16-byte aligned: store 4 values at a time
     uint32_t* status;
 };
 
-__device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, uint32_t src_bytes)
+__device__ __forceinline__ uint32_t cluster_rank()
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(tc::smem_u32(smem)), "l"(gmem),
-                 "r"(src_bytes)
-                 : "memory");
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group()
+__device__ __forceinline__ void cluster_sync()
 {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-// Rows [row0, row0 + ROWS) x K elements [k0, k0 + 64) of a [rows, K] bf16 matrix into a
-// core-matrix tile: 16-byte piece c (8 K elements) is row 8 (c / 64) + c % 8, K piece
-// (c / 8) % 8, and lands at byte 16 c of the tile.  Rows at or beyond `rows` read zeros.
-template <int ROWS>
-__device__ __forceinline__ void load_tile(unsigned char* dst, const __nv_bfloat16* src, int64_t row0, int rows,
-                                          int64_t K, int64_t k0, int tid)
+// One 8-element x 128-row box of a [rows, K] bf16 tensor map at (k, row0), multicast to
+// the same shared-memory offset in every CTA of `mask`, completing bytes on their mbar.
+__device__ __forceinline__ void tma_slab(void* dst, const CUtensorMap* map, int32_t k, int32_t row0, uint64_t* mbar,
+                                         uint16_t mask)
 {
-#pragma unroll
-    for (int i = 0; i < ROWS * 8 / kThreads; ++i) {
-        const int c = tid + i * kThreads;
-        const int r = ((c >> 6) << 3) | (c & 7), kc = (c >> 3) & 7;
-        const int64_t gr = row0 + r;
-        const bool in = gr < rows;
-        cp_async16_zfill(dst + c * 16, src + (in ? gr : 0) * K + k0 + kc * 8, in ? 16u : 0u);
-    }
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(tc::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row0), "r"(tc::smem_u32(mbar)), "h"(mask)
+        : "memory");
+}
+
+// Arrive on mbar (same offset) in every CTA of `mask` once this thread's MMAs are done.
+__device__ __forceinline__ void commit_cluster(uint64_t* mbar, uint16_t mask)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n"
+                 ::"r"(tc::smem_u32(mbar)), "h"(mask)
+                 : "memory");
 }
 
 // The fixed tree over n (a power of two) adjacent values: pairs of neighbours first.
@@ -99,119 +101,148 @@ __device__ __forceinline__ void leaf_tree(float (&v)[MAXL][E], int n)
                 for (int e = 0; e < E; ++e) v[l][e] = __fadd_rn(v[l][e], v[l + wdt][e]);
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1) k_pik_leaves(const PikArgs a)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
+    k_pik_leaves(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw, const PikArgs a)
 {
-    using Cf = PikCfg<BN>;
-    extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* mma_done = reinterpret_cast<uint64_t*>(smem + Cf::BAR_OFF);  // [kStages] stage read by its products
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_done + kStages);
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // [kStages] stage landed (own + peers' bytes)
+    uint64_t* empty = full + kStages;                              // [kStages] stage read by all four CTAs
+    uint64_t* leaf_done = empty + kStages;                         // an odd leaf's products are done
+    uint64_t* merged = leaf_done + 1;                              // its pairs are merged
+    uint64_t* acc_done = merged + 1;                               // every product is done
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_done + 1);
     const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t rank = cluster_rank();
+    const int dm = rank & 1, dn = rank >> 1;
 
-    // grouped raster: kGroupM m-tiles side by side walk the n-tiles together
-    const int tiles_m = (a.M + kBM - 1) / kBM, tiles_n = (a.N + BN - 1) / BN;
-    const int per_group = kGroupM * tiles_n, b = blockIdx.x;
-    const int g0 = (b / per_group) * kGroupM, gsz = min(kGroupM, tiles_m - g0), r = b % per_group;
-    const int64_t m0 = (int64_t)(g0 + r % gsz) * kBM, n0 = (int64_t)(r / gsz) * BN;
+    // grouped raster over clusters
+    const int tiles_m = (a.M + kBM - 1) / kBM, tiles_n = (a.N + kBN - 1) / kBN;
+    const int cl_m = (tiles_m + 1) / 2, cl_n = (tiles_n + 1) / 2;
+    const int c = blockIdx.x / kCluster, per_group = kGroupC * cl_n;
+    const int g0 = (c / per_group) * kGroupC, gsz = min(kGroupC, cl_m - g0), r = c % per_group;
+    const int mt = 2 * (g0 + r % gsz) + dm, nt = 2 * (r / gsz) + dn;
+    const int32_t m0 = mt * kBM, n0 = nt * kBN;  // rows past M or N load zeros and are not stored
+    const uint16_t mask_x = (uint16_t)((1u << dm) | (1u << (dm + 2)));  // CTAs sharing these X rows
+    const uint16_t mask_w = (uint16_t)(3u << (2 * dn));                 // CTAs sharing these W rows
 
     const int nl = a.leaf_hi - a.leaf_lo;
-    const bool merge = nl > Cf::SLOTS;  // more leaves than slots: merge pairs as they complete
-    const int used = merge ? Cf::SLOTS : nl;
-    const uint32_t cols = used * BN <= 32 ? 32u : used * BN <= 64 ? 64u : used * BN <= 128 ? 128u : used * BN <= 256 ? 256u : 512u;
+    const bool merge = nl > kSlots;
+    const int used = merge ? kSlots : nl;
+    const uint32_t cols = used <= 1 ? 128u : used <= 2 ? 256u : 512u;
     if (warp == 0) tc::tmem_alloc(tslot, cols);
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) tc::mbar_init(&mma_done[s], 1);
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], kCluster);
+        }
+        tc::mbar_init(leaf_done, 1);
+        tc::mbar_init(merged, 128);
+        tc::mbar_init(acc_done, 1);
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();
     __syncthreads();
+    cluster_sync();  // every CTA's barriers exist before any multicast reaches them
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
 
-    const int64_t K = a.K, KL = K / a.n_leaves, kbase = (int64_t)a.leaf_lo * KL;
+    const int64_t KL = (int64_t)a.K / a.n_leaves;
     const int spl = (int)(KL / kBK), S = nl * spl;  // stages per leaf, in all
-    auto load = [&](int s) {
-        unsigned char* st = smem + (s % kStages) * Cf::STAGE;
-        const int64_t k0 = kbase + (int64_t)s * kBK;
-        load_tile<kBM>(st, a.x, m0, a.M, K, k0, tid);
-        load_tile<BN>(st + Cf::A_BYTES, a.w, n0, a.N, K, k0, tid);
-    };
-
-    for (int s = 0; s < kStages - kLag; ++s) {  // one group per stage, empty past the end
-        if (s < S) load(s);
-        cp_async_commit();
-    }
+    const int32_t kbase = (int32_t)((int64_t)a.leaf_lo * KL);
     bool ok = true;
-    constexpr uint32_t idesc = tc::idesc_bf16(kBM, BN);
-    for (int s = 0; s < S; ++s) {
-        cp_async_wait_group<kStages - kLag - 1>();  // this thread's pieces of stage s have landed
-        tc::fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) {
+
+    if (tid == 0) {
+        // producer: this CTA's half of the X slabs (by n-offset) and of the W slabs (by m-offset)
+        for (int s = 0; s < S && ok; ++s) {
+            const int b = s % kStages;
+            if (s >= kStages) ok = tc::mbar_wait(&empty[b], (uint32_t)((s / kStages - 1) & 1));
+            if (!ok) break;
+            unsigned char* st = smem + (size_t)b * kStage;
+            tc::mbar_arrive_expect_tx(&full[b], kStage);
+            const int32_t k0 = kbase + s * kBK;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int kx = 4 * dn + q, kw = 4 * dm + q;
+                tma_slab(st + kx * kSlab, &tx, k0 + 8 * kx, m0, &full[b], mask_x);
+                tma_slab(st + kOpBytes + kw * kSlab, &tw, k0 + 8 * kw, n0, &full[b], mask_w);
+            }
+        }
+        // every arrival meant for this CTA's stage barriers has landed before it can exit
+        for (int b = 0; b < kStages && b < S; ++b) {
+            const int uses = (S - b + kStages - 1) / kStages;
+            ok = tc::mbar_wait(&empty[b], (uint32_t)((uses - 1) & 1)) && ok;
+        }
+    } else if (tid == 32) {
+        // MMA issuer
+        constexpr uint32_t idesc = tc::idesc_bf16(kBM, kBN);
+        int events = 0;
+        for (int s = 0; s < S && ok; ++s) {
+            const int b = s % kStages;
+            ok = tc::mbar_wait(&full[b], (uint32_t)((s / kStages) & 1));
+            if (!ok) break;
             tc::fence_after_sync();
-            const uint32_t sa = tc::smem_u32(smem + (s % kStages) * Cf::STAGE), sb = sa + Cf::A_BYTES;
-            const int j = s / spl;  // leaf
-            const uint32_t d = tmem + (uint32_t)((merge ? __popc(j) : j) * BN);
+            const int j = s / spl;
+            const uint32_t d = tmem + (uint32_t)((merge ? __popc(j) : j) * kBN);
+            const uint32_t sx = tc::smem_u32(smem + (size_t)b * kStage), sw = sx + kOpBytes;
             const bool first = (s % spl) == 0;  // a leaf's first instruction overwrites its slot
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-                tc::mma_bf16(d, tc::sdesc(sa + k * 256, 128, Cf::SBO), tc::sdesc(sb + k * 256, 128, Cf::SBO), idesc,
-                             (first && k == 0) ? 0u : 1u);
-            tc::commit(&mma_done[s % kStages]);
-        }
-        // refill the stage of step s - kLag (its products are done) with step s + kStages - kLag
-        const int nxt = s + kStages - kLag;
-        if (nxt < S) {
-            if (s >= kLag) {
-                const int p = s - kLag;
-                ok = tc::mbar_wait(&mma_done[p % kStages], (uint32_t)((p / kStages) & 1)) && ok;
+                tc::mma_bf16(d, tc::sdesc(sx + k * 2 * kSlab, kSlab, 128), tc::sdesc(sw + k * 2 * kSlab, kSlab, 128),
+                             idesc, (first && k == 0) ? 0u : 1u);
+            commit_cluster(&empty[b], (uint16_t)((1u << kCluster) - 1));
+            if (merge && s % spl == spl - 1 && (j & 1)) {
+                tc::commit(leaf_done);
+                ok = tc::mbar_wait(merged, (uint32_t)(events & 1));
+                ++events;
+                tc::fence_after_sync();
             }
-            if (ok) load(nxt);
         }
-        cp_async_commit();
-        if (merge && s % spl == spl - 1 && ((s / spl) & 1)) {
-            // leaf j (odd) is complete once its products are: merge the finished pairs, left
-            // (earlier leaves) + right, ctz(j + 1) levels, into the lower slot
-            const int j = s / spl;
-            ok = tc::mbar_wait(&mma_done[s % kStages], (uint32_t)((s / kStages) & 1)) && ok;
-            tc::fence_after_sync();
-            const uint32_t lanes = (uint32_t)(warp * 32) << 16;
-            for (int top = __popc(j), m = __ffs(j + 1) - 1; m > 0; --m, --top) {
+        tc::commit(acc_done);
+    } else if (warp >= 4) {
+        const int q = warp & 3;
+        const uint32_t lanes = (uint32_t)(q * 32) << 16;
+        if (merge) {
+            for (int j = 1, e = 0; j < nl; j += 2, ++e) {
+                ok = tc::mbar_wait(leaf_done, (uint32_t)(e & 1)) && ok;
+                tc::fence_after_sync();
+                for (int top = __popc(j), m = __ffs(j + 1) - 1; m > 0; --m, --top) {
 #pragma unroll 1
-                for (int cb = 0; cb < BN / 32; ++cb) {
-                    float l[32], r[32];
-                    uint32_t o[32];
-                    const uint32_t dst = tmem + lanes + (uint32_t)((top - 1) * BN + cb * 32);
-                    tc::tmem_ld_32x32b<32>(dst, l);
-                    tc::tmem_ld_32x32b<32>(tmem + lanes + (uint32_t)(top * BN + cb * 32), r);
+                    for (int cb = 0; cb < kBN / 32; ++cb) {
+                        float l[32], rr[32];
+                        uint32_t o[32];
+                        const uint32_t dst = tmem + lanes + (uint32_t)((top - 1) * kBN + cb * 32);
+                        tc::tmem_ld_32x32b<32>(dst, l);
+                        tc::tmem_ld_32x32b<32>(tmem + lanes + (uint32_t)(top * kBN + cb * 32), rr);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__fadd_rn(l[e], r[e]));
-                    tc::tmem_st_32x32b<32>(dst, o);
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fadd_rn(l[i], rr[i]));
+                        tc::tmem_st_32x32b<32>(dst, o);
+                    }
+                    tc::tmem_wait_st();
                 }
-                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                tc::mbar_arrive(merged);
             }
-            tc::fence_before_sync();  // the next products are issued after the loop's barrier
         }
+        ok = tc::mbar_wait(acc_done, 0u) && ok;
+        tc::fence_after_sync();
     }
-    if (S > 0) ok = tc::mbar_wait(&mma_done[(S - 1) % kStages], (uint32_t)(((S - 1) / kStages) & 1)) && ok;
-    asm volatile("cp.async.wait_all;\n" ::: "memory");
     const bool failed = __syncthreads_or(!ok) != 0;
-    tc::fence_after_sync();
 
-    if (!failed) {
-        constexpr int MAXL = Cf::SLOTS, E = 8;
+    if (!failed && warp >= 4) {
+        constexpr int E = 8;
         const int parts = merge ? 1 : nl;  // partials left in slots 0 .. parts-1
-        const int row = warp * 32 + (tid & 31);
-        const int64_t gm = m0 + row;
-        const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+        const int row = (warp & 3) * 32 + (tid & 31);
+        const int64_t gm = (int64_t)m0 + row;
+        const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
 #pragma unroll 1
-        for (int cb = 0; cb < BN / E; ++cb) {
-            float v[MAXL][E];
+        for (int cb = 0; cb < kBN / E; ++cb) {
+            float v[kSlots][E];
 #pragma unroll
-            for (int l = 0; l < MAXL; ++l)
-                if (l < parts) tc::tmem_ld_32x32b<E>(tmem + lanes + (uint32_t)(l * BN + cb * E), v[l]);
-            leaf_tree<MAXL, E>(v, parts);
-            const int64_t c0 = n0 + cb * E;
+            for (int l = 0; l < kSlots; ++l)
+                if (l < parts) tc::tmem_ld_32x32b<E>(tmem + lanes + (uint32_t)(l * kBN + cb * E), v[l]);
+            leaf_tree<kSlots, E>(v, parts);
+            const int64_t c0 = (int64_t)n0 + cb * E;
             if (gm < a.M) {
                 float* dst = a.y + gm * a.N + c0;
                 if (a.vec_store && c0 + E <= a.N) {
@@ -228,8 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pik_leaves(const PikArgs a)
     if (failed && tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
     tc::fence_before_sync();
     __syncthreads();
-    if (tid == 0)
-        for (int s = 0; s < kStages; ++s) tc::mbar_inval(&mma_done[s]);
+    cluster_sync();  // no CTA leaves while a peer may still write its shared memory
     if (warp == 0) tc::tmem_dealloc(tmem, cols);
 }
 
@@ -265,15 +295,39 @@ __global__ void __launch_bounds__(256) k_pik_combine(const float* parts, int64_t
 bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-template <int BN>
-cudaError_t launch_pik(const PikArgs& a, cudaStream_t s)
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link to libcuda).
+EncodeTiled encode_tiled()
 {
-    using Cf = PikCfg<BN>;
-    cudaError_t e = cudaFuncSetAttribute(k_pik_leaves<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
-    if (e != cudaSuccess) return e;
-    const int64_t tiles = (int64_t)((a.M + kBM - 1) / kBM) * ((a.N + BN - 1) / BN);
-    k_pik_leaves<BN><<<(unsigned)tiles, kThreads, Cf::SMEM, s>>>(a);
-    return cudaGetLastError();
+    static EncodeTiled fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    return fn;
+}
+
+// Tensor map of a [rows, K] bf16 matrix whose box is one 16-byte K slab of 128 rows: a box
+// lands as 128 consecutive 16-byte rows, the slab of the core-matrix layout the MMA
+// descriptors read (K-adjacent cores kSlab apart, 8-row groups 128 bytes apart).  Rows
+// past the end read zeros.
+bool slab_map(CUtensorMap* m, const void* base, int32_t rows, int32_t K)
+{
+    const EncodeTiled f = encode_tiled();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {8, (cuuint32_t)kBM}, es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -291,15 +345,20 @@ extern "C" int32_t cpr_pik_gemm(const void* x, const void* w, float* y, int32_t 
     if (K % (kBK * n_leaves) != 0) return CPR_ERR_INVALID_ARG;
     const int nl = leaf_hi - leaf_lo;
     if (leaf_lo < 0 || leaf_hi > n_leaves || !pow2(nl) || leaf_lo % nl != 0) return CPR_ERR_INVALID_ARG;
-    if ((int64_t)((M + kBM - 1) / kBM) * ((N + 63) / 64) > 0x7fffffff) return CPR_ERR_INVALID_ARG;
+    if ((int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN) > 0x7fffffff / 2) return CPR_ERR_INVALID_ARG;
     if (!workspace) return CPR_ERR_WORKSPACE;
     if (!al16(x) || !al16(w) || !al16(workspace) || ((uintptr_t)y & 3u)) return CPR_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    PikArgs a{static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), y, M, N, K, n_leaves,
-              leaf_lo, leaf_hi, (al16(y) && N % 4 == 0) ? 1 : 0, static_cast<uint32_t*>(workspace)};
+    PikArgs a{y, M, N, K, n_leaves, leaf_lo, leaf_hi, (al16(y) && N % 4 == 0) ? 1 : 0,
+              static_cast<uint32_t*>(workspace)};
+    CUtensorMap mx, mw;
+    if (!slab_map(&mx, x, M, K) || !slab_map(&mw, w, N, K)) return CPR_ERR_CUDA;
     if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s) != cudaSuccess) return CPR_ERR_CUDA;
-    const cudaError_t e = launch_pik<128>(a, s);
-    return e == cudaSuccess ? CPR_OK : CPR_ERR_CUDA;
+    if (cudaFuncSetAttribute(k_pik_leaves, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) != cudaSuccess)
+        return CPR_ERR_CUDA;
+    const int64_t clusters = (int64_t)((M + 2 * kBM - 1) / (2 * kBM)) * ((N + 2 * kBN - 1) / (2 * kBN));
+    k_pik_leaves<<<(unsigned)(clusters * kCluster), kThreads, kSmem, s>>>(mx, mw, a);
+    return cudaGetLastError() == cudaSuccess ? CPR_OK : CPR_ERR_CUDA;
 }
 
 extern "C" int32_t cpr_pik_combine(const float* parts, int32_t n_parts, int64_t count, float* y, void* stream)
