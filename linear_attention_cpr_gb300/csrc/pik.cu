@@ -8,10 +8,11 @@
 // not depend on how the leaves are shared among ranks.
 //
 // k_pik_leaves: one CTA per 128 x 128 output tile, in clusters of 2 x 2 tiles.  A tile's
-// operands are 128 rows of X and 128 rows of W per 64 K elements; the two CTAs of a cluster
-// that share the X rows (same m) each load half of them (four of the eight 16-byte K
-// slabs) with TMA and multicast it to both, and likewise for the W rows of the two CTAs
-// that share n, so each CTA pulls half its operand bytes from L2.  Warp 0 issues the
+// operands are 128 rows of X and 128 rows of W per 64 K elements, each row 128 bytes in
+// the tensor cores' 128-byte-swizzled K-major layout; the two CTAs of a cluster that share
+// the X rows (same m) each load 64 of them with one TMA box and multicast it to both, and
+// likewise for the W rows of the two CTAs that share n, so each CTA pulls half its
+// operand bytes from L2.  Warp 0 issues the
 // loads into six stages, warp 1 issues the MMAs (4 per stage, K = 16 each) and commits
 // each stage to the stage-free barriers of all four CTAs; warps 4-7 merge partials and
 // run the epilogue.  Up to four leaves: each leaf of the CTA's range accumulates in its
@@ -44,8 +45,8 @@ constexpr int kThreads = 256;  // warp 0: loads, warp 1: MMAs, warps 4-7: merges
 constexpr int kCluster = 4;    // 2 (m) x 2 (n) tiles; rank r holds m-offset r & 1, n-offset r >> 1
 constexpr int kGroupC = 4;     // cluster rows per raster group (concurrent tiles share operands in L2)
 constexpr int kSlots = 512 / kBN;  // partial sums that fit in TMEM
-constexpr uint32_t kSlab = kBM * 16;                 // one K slab of a 128-row operand tile (2 KB)
-constexpr uint32_t kOpBytes = 8 * kSlab;             // 16 KB per operand per stage
+constexpr uint32_t kHalf = 64 * 128;                 // 64 rows of 128 bytes: one TMA box (8 KB)
+constexpr uint32_t kOpBytes = 2 * kHalf;             // 16 KB per operand per stage
 constexpr uint32_t kStage = 2 * kOpBytes;            // X then W
 constexpr size_t kBarOff = (size_t)kStages * kStage;
 constexpr size_t kSmem = kBarOff + 256 + 1024;       // barriers, TMEM slot, alignment slack
@@ -68,9 +69,9 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-// One 8-element x 128-row box of a [rows, K] bf16 tensor map at (k, row0), multicast to
+// One 64-element x 64-row box of a [rows, K] bf16 tensor map at (k, row0), multicast to
 // the same shared-memory offset in every CTA of `mask`, completing bytes on their mbar.
-__device__ __forceinline__ void tma_slab(void* dst, const CUtensorMap* map, int32_t k, int32_t row0, uint64_t* mbar,
+__device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int32_t k, int32_t row0, uint64_t* mbar,
                                          uint16_t mask)
 {
     asm volatile(
@@ -78,6 +79,19 @@ __device__ __forceinline__ void tma_slab(void* dst, const CUtensorMap* map, int3
         " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(tc::smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row0), "r"(tc::smem_u32(mbar)), "h"(mask)
         : "memory");
+}
+
+// Shared-memory descriptor of a K-major operand in the 128-byte swizzle: rows of 128 bytes,
+// 8-row groups 1024 bytes apart (SBO), the tile 1024-byte aligned; the start address
+// advances 32 bytes per 16 K elements inside the swizzled row.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;              // LBO: unused by a swizzled K-major operand
+    d |= (uint64_t)(1024 >> 4) << 32;    // SBO
+    d |= (uint64_t)1 << 46;              // descriptor version of the 5th-generation tensor cores
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
 }
 
 // Arrive on mbar (same offset) in every CTA of `mask` once this thread's MMAs are done.
@@ -153,7 +167,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     if (tid == 0) {
-        // producer: this CTA's half of the X slabs (by n-offset) and of the W slabs (by m-offset)
+        // producer: this CTA's half of the X rows (by n-offset) and of the W rows (by m-offset)
         for (int s = 0; s < S && ok; ++s) {
             const int b = s % kStages;
             if (s >= kStages) ok = tc::mbar_wait(&empty[b], (uint32_t)((s / kStages - 1) & 1));
@@ -161,12 +175,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             unsigned char* st = smem + (size_t)b * kStage;
             tc::mbar_arrive_expect_tx(&full[b], kStage);
             const int32_t k0 = kbase + s * kBK;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int kx = 4 * dn + q, kw = 4 * dm + q;
-                tma_slab(st + kx * kSlab, &tx, k0 + 8 * kx, m0, &full[b], mask_x);
-                tma_slab(st + kOpBytes + kw * kSlab, &tw, k0 + 8 * kw, n0, &full[b], mask_w);
-            }
+            tma_box(st + dn * kHalf, &tx, k0, m0 + 64 * dn, &full[b], mask_x);
+            tma_box(st + kOpBytes + dm * kHalf, &tw, k0, n0 + 64 * dm, &full[b], mask_w);
         }
         // every arrival meant for this CTA's stage barriers has landed before it can exit
         for (int b = 0; b < kStages && b < S; ++b) {
@@ -188,8 +198,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             const bool first = (s % spl) == 0;  // a leaf's first instruction overwrites its slot
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-                tc::mma_bf16(d, tc::sdesc(sx + k * 2 * kSlab, kSlab, 128), tc::sdesc(sw + k * 2 * kSlab, kSlab, 128),
-                             idesc, (first && k == 0) ? 0u : 1u);
+                tc::mma_bf16(d, sdesc_sw128(sx + k * 32), sdesc_sw128(sw + k * 32), idesc, (first && k == 0) ? 0u : 1u);
             commit_cluster(&empty[b], (uint16_t)((1u << kCluster) - 1));
             if (merge && s % spl == spl - 1 && (j & 1)) {
                 tc::commit(leaf_done);
@@ -314,19 +323,18 @@ EncodeTiled encode_tiled()
     return fn;
 }
 
-// Tensor map of a [rows, K] bf16 matrix whose box is one 16-byte K slab of 128 rows: a box
-// lands as 128 consecutive 16-byte rows, the slab of the core-matrix layout the MMA
-// descriptors read (K-adjacent cores kSlab apart, 8-row groups 128 bytes apart).  Rows
-// past the end read zeros.
-bool slab_map(CUtensorMap* m, const void* base, int32_t rows, int32_t K)
+// Tensor map of a [rows, K] bf16 matrix whose box is 64 K elements x 64 rows, landing as
+// 64 rows of 128 bytes in the 128-byte swizzle the MMA descriptors read.  Rows past the
+// end read zeros.
+bool box_map(CUtensorMap* m, const void* base, int32_t rows, int32_t K)
 {
     const EncodeTiled f = encode_tiled();
     if (!f) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {8, (cuuint32_t)kBM}, es[2] = {1, 1};
+    const cuuint32_t box[2] = {64, 64}, es[2] = {1, 1};
     return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -352,7 +360,7 @@ extern "C" int32_t cpr_pik_gemm(const void* x, const void* w, float* y, int32_t 
     PikArgs a{y, M, N, K, n_leaves, leaf_lo, leaf_hi, (al16(y) && N % 4 == 0) ? 1 : 0,
               static_cast<uint32_t*>(workspace)};
     CUtensorMap mx, mw;
-    if (!slab_map(&mx, x, M, K) || !slab_map(&mw, w, N, K)) return CPR_ERR_CUDA;
+    if (!box_map(&mx, x, M, K) || !box_map(&mw, w, N, K)) return CPR_ERR_CUDA;
     if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s) != cudaSuccess) return CPR_ERR_CUDA;
     if (cudaFuncSetAttribute(k_pik_leaves, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) != cudaSuccess)
         return CPR_ERR_CUDA;

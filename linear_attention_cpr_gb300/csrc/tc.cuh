@@ -2,11 +2,12 @@
 // shared-memory matrix descriptors, instruction descriptors, TMEM allocation, MMA issue
 // and commit, mbarriers with bounded waits, bulk global->shared copies, TMEM loads.
 //
-// Operand layout used everywhere (verified against a CPU reference on this GPU): no
+// Operand layout of the layer kernels (verified against a CPU reference on this GPU): no
 // swizzle, K-major; a tile of R rows x K elements is made of "core matrices" of 8 rows x
 // 16 bytes, core (i, kk) stored at byte (i * (K*esize/16) + kk) * 128, row r of a core at
 // +16*r.  In the descriptor, LBO is the byte step between cores adjacent along K (128)
 // and SBO the step between 8-row groups (K*esize/16 * 128).
+// (pik.cu uses the 128-byte-swizzled K-major layout instead, with its own descriptor.)
 // Accumulator layout: M = 128 -> row m in TMEM lane m; M = 64 -> rows 16q..16q+15 in
 // lanes 32q..32q+15.  Column j of D is TMEM column (base + j).
 #pragma once
