@@ -54,6 +54,8 @@ size_t cpr_pik_workspace_size(void);
  *   leaf_lo, leaf_hi   0 <= leaf_lo < leaf_hi <= n_leaves, leaf_hi - leaf_lo a power of two
  *              that divides leaf_lo (a complete subtree); (0, n_leaves) is the whole product
  *   workspace  cpr_pik_workspace_size() bytes, 16-byte aligned; its status word is reset
+ * Host work per call: two TMA descriptors of x and w are encoded (the driver's tensor-map
+ * encoder, found through the CUDA runtime; CPR_ERR_CUDA if it is unavailable).
  * Returns CPR_OK, CPR_ERR_INVALID_ARG, CPR_ERR_MISALIGNED, CPR_ERR_WORKSPACE or
  * CPR_ERR_CUDA.  Does not synchronise. */
 int32_t cpr_pik_gemm(const void* x, const void* w, float* y, int32_t M, int32_t N, int32_t K, int32_t n_leaves,

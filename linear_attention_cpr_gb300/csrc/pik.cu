@@ -12,10 +12,9 @@
 // the tensor cores' 128-byte-swizzled K-major layout; the two CTAs of a cluster that share
 // the X rows (same m) each load 64 of them with one TMA box and multicast it to both, and
 // likewise for the W rows of the two CTAs that share n, so each CTA pulls half its
-// operand bytes from L2.  Warp 0 issues the
-// loads into six stages, warp 1 issues the MMAs (4 per stage, K = 16 each) and commits
-// each stage to the stage-free barriers of all four CTAs; warps 4-7 merge partials and
-// run the epilogue.  Up to four leaves: each leaf of the CTA's range accumulates in its
+// operand bytes from L2.  Warp 0 issues the loads into six stages, warp 1 issues the
+// MMAs (4 per stage, K = 16 each) and commits each stage to the stage-free barriers of
+// all four CTAs; warps 4-7 merge partials and run the epilogue.  Up to four leaves: each leaf of the CTA's range accumulates in its
 // own TMEM slot of 128 columns, the loop never waits for a reduction, and the epilogue
 // sums the slots with the tree in registers.  Eight leaves: slot popcount(j) takes leaf j;
 // when an odd leaf completes, warps 4-7 merge the finished pairs of the tree in TMEM (a
@@ -39,7 +38,7 @@ namespace {
 
 constexpr int kBM = 128;       // tile rows (M of the MMA instruction; row i in TMEM lane i)
 constexpr int kBN = 128;       // tile columns (N of the MMA instruction)
-constexpr int kBK = 64;        // K elements per stage: eight 16-byte slabs
+constexpr int kBK = 64;        // K elements per stage: one 128-byte swizzled row per operand row
 constexpr int kStages = 6;     // shared-memory stages
 constexpr int kThreads = 256;  // warp 0: loads, warp 1: MMAs, warps 4-7: merges and epilogue
 constexpr int kCluster = 4;    // 2 (m) x 2 (n) tiles; rank r holds m-offset r & 1, n-offset r >> 1
