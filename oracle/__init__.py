@@ -19,6 +19,10 @@ Functions (all inputs are converted to float64 exactly; layouts as in cpr_oracle
 ``bruteforce``  materialised products of per-token transition matrices for one
                 (sequence, head); tiny sizes only.
 
+Modules beside it: ``oracle.pik`` (the deterministic K-split product: fp32 tree, exact
+product, error bound) and ``oracle.backward`` (the exact adjoint of the recurrence, for
+the backward pass).
+
 Sources: "IsoExec: Eliminating Trainer-Inference Mismatch in SkyRL", section
 "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet"; "SkyRL IsoExec: vLLM 与 Megatron
 的 logprob 差 ...", section "Gated DeltaNet 的第三条路：chunkwise-parallel recurrent";

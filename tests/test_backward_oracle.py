@@ -1,0 +1,106 @@
+"""Pins of the backward oracle (oracle/backward.py, the exact adjoint of the gated delta
+rule), CPU only: central finite differences of the pinned forward oracle, a single-token
+closed form, and planted mistakes that the pins must catch."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import backward
+
+
+def _problem(seed, lens=(4, 2), H=2, dk=3, dv=2):
+    rng = np.random.default_rng(seed)
+    T, N = sum(lens), len(lens)
+    k = rng.standard_normal((T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    x = dict(
+        q=rng.standard_normal((T, H, dk)) * dk ** -0.5,
+        k=k,
+        v=rng.standard_normal((T, H, dv)),
+        g=-0.5 * np.log1p(np.exp(rng.standard_normal((T, H)))),
+        beta=1.0 / (1.0 + np.exp(-rng.standard_normal((T, H)))),
+        state_in=rng.standard_normal((N, H, dk, dv)) * 0.5,
+    )
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    d_out = rng.standard_normal((T, H, dv))
+    d_state = rng.standard_normal((N, H, dk, dv))
+    return x, cu, d_out, d_state
+
+
+def _loss(x, cu, d_out, d_state):
+    o, st, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, 4, state_in=x["state_in"],
+                                boundaries=False)
+    return float(np.sum(d_out * o) + np.sum(d_state * st))
+
+
+def _fd_grads(x, cu, d_out, d_state, h=1e-6):
+    out = {}
+    for name in ("q", "k", "v", "g", "beta", "state_in"):
+        grad = np.zeros_like(x[name])
+        for idx in np.ndindex(x[name].shape):
+            xp = {kk: vv.copy() for kk, vv in x.items()}
+            xm = {kk: vv.copy() for kk, vv in x.items()}
+            xp[name][idx] += h
+            xm[name][idx] -= h
+            grad[idx] = (_loss(xp, cu, d_out, d_state) - _loss(xm, cu, d_out, d_state)) / (2 * h)
+        out[name] = grad
+    return out
+
+
+_NAMES = {"q": "dq", "k": "dk", "v": "dv", "g": "dg", "beta": "dbeta", "state_in": "d_state_in"}
+
+
+def _matches_fd(grads, fd):
+    return all(np.allclose(grads[_NAMES[n]], fd[n], rtol=1e-6, atol=1e-7) for n in fd)
+
+
+@pytest.fixture(scope="module")
+def case():
+    oracle.build()
+    x, cu, d_out, d_state = _problem(0)
+    return x, cu, d_out, d_state, _fd_grads(x, cu, d_out, d_state)
+
+
+def test_backward_matches_finite_differences(case):
+    x, cu, d_out, d_state, fd = case
+    grads = backward.recurrent_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, d_out, d_state,
+                                        state_in=x["state_in"])
+    for n in fd:
+        np.testing.assert_allclose(grads[_NAMES[n]], fd[n], rtol=1e-6, atol=1e-7, err_msg=n)
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4])
+def test_finite_differences_catch_planted_mistakes(case, mutant):
+    x, cu, d_out, d_state, fd = case
+    grads = backward.recurrent_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, d_out, d_state,
+                                        state_in=x["state_in"], mutant=mutant)
+    assert not _matches_fd(grads, fd)
+
+
+def test_single_token_closed_form():
+    # S_0 = 0, one token: o = beta (k . q) v, S_1 = beta v k^T.  With L = dO . o:
+    #   dq = beta (dO . v) k,  dk = beta (dO . v) q,  dv = beta (k . q) dO,
+    #   dbeta = (k . q)(dO . v),  dg = 0,
+    #   dL/dS_0 = alpha (dO q^T - beta (k . q) dO k^T)   (S is dv x dk; stored transposed)
+    rng = np.random.default_rng(3)
+    dk_, dv_ = 4, 3
+    q, k, v = rng.standard_normal((1, 1, dk_)), rng.standard_normal((1, 1, dk_)), rng.standard_normal((1, 1, dv_))
+    g, beta = np.array([[-0.3]]), np.array([[0.7]])
+    dO = rng.standard_normal((1, 1, dv_))
+    gr = backward.recurrent_backward(q, k, v, g, beta, [0, 1], dO)
+    qq, kk, vv, d = q[0, 0], k[0, 0], v[0, 0], dO[0, 0]
+    b, a = 0.7, np.exp(-0.3)
+    np.testing.assert_allclose(gr["dq"][0, 0], b * (d @ vv) * kk, rtol=1e-13)
+    np.testing.assert_allclose(gr["dk"][0, 0], b * (d @ vv) * qq, rtol=1e-13)
+    np.testing.assert_allclose(gr["dv"][0, 0], b * (kk @ qq) * d, rtol=1e-13)
+    np.testing.assert_allclose(gr["dbeta"][0, 0], (kk @ qq) * (d @ vv), rtol=1e-13)
+    assert gr["dg"][0, 0] == 0.0
+    dS0 = a * (np.outer(d, qq) - b * (kk @ qq) * np.outer(d, kk))
+    np.testing.assert_allclose(gr["d_state_in"][0, 0], dS0.T, rtol=1e-13, atol=1e-15)
+
+
+def test_zero_upstream_gives_zero_gradients():
+    x, cu, d_out, d_state = _problem(5)
+    gr = backward.recurrent_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, np.zeros_like(d_out),
+                                     state_in=x["state_in"])
+    assert all(not np.any(gr[n]) for n in gr)
