@@ -92,3 +92,78 @@ def recurrent_backward(q, k, v, g, beta, cu_seqlens, d_out, d_state_out=None, st
             d_state_in[n, h] = dS.T
     grads["d_state_in"] = d_state_in
     return grads
+
+
+def chunked_backward(q, k, v, g, beta, cu_seqlens, d_out, C, d_state_out=None, state_in=None):
+    """The same gradients by the chunk schedule a GPU backward would run (fp64):
+    1. boundary states S_b by the forward recurrence (what a forward pass saves);
+    2. per chunk, its transition P = A_1 ... A_n (A_t = alpha_t (I - beta_t k_t k_t^T) acting
+       on the right of the row-vector state, S_t = S_{t-1} A_t + beta_t v_t k_t^T) and
+       qt_t = P_t q_t (P_t = A_1 ... A_t);
+    3. a reverse chain over each sequence's chunks: dS_b = dS_{b+1} P^T + sum_t do_t qt_t^T,
+       from dS at the sequence's end;
+    4. per chunk, the reverse token recurrence of ``recurrent_backward`` from dS_{b+1},
+       with the states recomputed from S_b.
+    Returns the dict of ``recurrent_backward`` plus ``chain_mismatch``: the largest
+    difference between the chain's dS_b and the one each chunk's reverse recurrence arrives
+    at (both exact up to rounding)."""
+    q, k, v, g, beta, d_out = (_f64(x) for x in (q, k, v, g, beta, d_out))
+    cu = [int(c) for c in np.asarray(cu_seqlens).reshape(-1)]
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = len(cu) - 1
+    s_in = np.zeros((N, H, dk, dv)) if state_in is None else _f64(state_in)
+    ds_out = np.zeros((N, H, dk, dv)) if d_state_out is None else _f64(d_state_out)
+    out = {name: np.zeros_like(x) for name, x in (("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dbeta", beta))}
+    d_state_in = np.zeros((N, H, dk, dv))
+    mismatch = 0.0
+    eye = np.eye(dk)
+    for n in range(N):
+        for h in range(H):
+            t0, t1 = cu[n], cu[n + 1]
+            starts = list(range(t0, t1, C))
+            # 1. boundary states
+            S = s_in[n, h].T.copy()
+            bounds = []
+            for c0 in starts:
+                bounds.append(S.copy())
+                for t in range(c0, min(c0 + C, t1)):
+                    a = np.exp(g[t, h])
+                    St = a * S
+                    S = St + np.outer(beta[t, h] * (v[t, h] - St @ k[t, h]), k[t, h])
+            # 2. per-chunk transitions and propagated queries
+            Ps, qts = [], []
+            for c0 in starts:
+                P = eye.copy()
+                qt = []
+                for t in range(c0, min(c0 + C, t1)):
+                    A = np.exp(g[t, h]) * (eye - beta[t, h] * np.outer(k[t, h], k[t, h]))
+                    P = P @ A
+                    qt.append(P @ q[t, h])
+                Ps.append(P)
+                qts.append(qt)
+            # 3. reverse chain: dS at every chunk's end, then its start
+            d_end = [None] * len(starts)
+            dS = ds_out[n, h].T.copy()
+            d_start = [None] * len(starts)
+            for j in range(len(starts) - 1, -1, -1):
+                d_end[j] = dS.copy()
+                c0 = starts[j]
+                dS = dS @ Ps[j].T
+                for i, t in enumerate(range(c0, min(c0 + C, t1))):
+                    dS = dS + np.outer(d_out[t, h], qts[j][i])
+                d_start[j] = dS.copy()
+            d_state_in[n, h] = dS.T if starts else ds_out[n, h]
+            # 4. per-chunk reverse token recurrence from the chunk's end adjoint
+            for j, c0 in enumerate(starts):
+                c1 = min(c0 + C, t1)
+                sub = slice(c0, c1)
+                gr = recurrent_backward(q[sub, h:h + 1], k[sub, h:h + 1], v[sub, h:h + 1], g[sub, h:h + 1],
+                                        beta[sub, h:h + 1], [0, c1 - c0], d_out[sub, h:h + 1],
+                                        d_state_out=d_end[j].T[None, None], state_in=bounds[j].T[None, None])
+                for name in ("dq", "dk", "dv", "dg", "dbeta"):
+                    out[name][sub, h] = gr[name][:, 0]
+                mismatch = max(mismatch, float(np.max(np.abs(gr["d_state_in"][0, 0] - d_start[j].T))))
+    out["d_state_in"] = d_state_in
+    out["chain_mismatch"] = mismatch
+    return out

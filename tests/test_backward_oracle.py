@@ -104,3 +104,15 @@ def test_zero_upstream_gives_zero_gradients():
     gr = backward.recurrent_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, np.zeros_like(d_out),
                                      state_in=x["state_in"])
     assert all(not np.any(gr[n]) for n in gr)
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 4, 8])
+def test_chunked_schedule_equals_token_adjoint(C):
+    x, cu, d_out, d_state = _problem(7, lens=(9, 0, 5, 1), H=2, dk=4, dv=3)
+    ref = backward.recurrent_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, d_out, d_state,
+                                      state_in=x["state_in"])
+    got = backward.chunked_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, d_out, C, d_state,
+                                    state_in=x["state_in"])
+    for name in ref:
+        np.testing.assert_allclose(got[name], ref[name], rtol=1e-10, atol=1e-12, err_msg=name)
+    assert got["chain_mismatch"] < 1e-12
