@@ -307,18 +307,19 @@ using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, 
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// The driver's tensor-map encoder, looked up once through the runtime (no link to libcuda).
+// The driver's tensor-map encoder, looked up once through the runtime (no link to libcuda;
+// the static's initialisation is thread-safe).
 EncodeTiled encode_tiled()
 {
-    static EncodeTiled fn = nullptr;
-    if (!fn) {
+    static const EncodeTiled fn = [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+        const bool found =
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(p);
-    }
+            q == cudaDriverEntryPointSuccess;
+        return found ? reinterpret_cast<EncodeTiled>(p) : static_cast<EncodeTiled>(nullptr);
+    }();
     return fn;
 }
 
