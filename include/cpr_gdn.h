@@ -174,7 +174,8 @@ int32_t cpr_gdn_ring_from_prefill(const void* k, const void* v, const float* g, 
  * The resync (and the step of those sequences' tokens) runs on a second stream owned by
  * the library (one per device, created on the first call) that forks from `stream` and
  * joins it again at the end of the call: work issued on `stream` after the call sees
- * every result.
+ * every result.  Calls on one device share that stream; calls from several host threads
+ * take turns on it (a lock held while each call enqueues its work).
  */
 int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
                        float* state, const cpr_gdn_ring* ring, const int32_t* pos, int32_t B, int32_t H,

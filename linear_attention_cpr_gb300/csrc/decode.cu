@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "chunk_update.cuh"
 #include "common.cuh"
@@ -553,18 +554,21 @@ namespace {
 struct SideStream {
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex use;  // held by one call from its fork to its join
 };
 cudaError_t side_stream(SideStream*& out)
 {
     static SideStream per_device[64];
+    static std::mutex create;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     SideStream& ss = per_device[dev];
-    if (!ss.stream) {
-        if ((e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(create);
+    if (!ss.join) {
+        if (!ss.stream && (e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if (!ss.fork && (e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
         if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
     }
     out = &ss;
@@ -579,6 +583,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     if (e != cudaSuccess) return e;
     SideStream* ss = nullptr;
     if ((e = side_stream(ss)) != cudaSuccess) return e;
+    // calls from several host threads take turns on the shared side stream and its events
+    std::lock_guard<std::mutex> turn(ss->use);
     profile_mark(0, s);
     // fork: the resync runs on the side stream while the step kernel runs on s
     if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return e;
