@@ -187,3 +187,16 @@ def test_tree_pins_catch_planted_mistakes():
         assert not _tree_pins_hold(mutant), mutant.__name__
     # fp32 addition commutes: swapping operands is not a mistake and must pass
     assert _tree_pins_hold(right_first)
+
+
+def test_binding_checks_before_any_device_work():
+    import torch
+
+    import linear_attention_cpr_gb300 as cpr
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        cpr.cpr_pik_gemm(x.float(), torch.zeros(4, 64, dtype=torch.bfloat16), 1)
+    with pytest.raises(ValueError):
+        cpr.cpr_pik_gemm(x, torch.zeros(4, 128, dtype=torch.bfloat16), 1)  # K disagrees
+    with pytest.raises(TypeError):
+        cpr.cpr_pik_combine(torch.zeros(2, 8, dtype=torch.float64))
