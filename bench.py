@@ -513,6 +513,22 @@ def _bf16_peak():
     return 1900.0, "fallback"
 
 
+def pik_cpu_baseline(x, w, rows=512):
+    """The pik oracle's exact product (fp64, numpy) timed on the host cores for the first
+    `rows` rows of X against all of W; reported in the product's own unit."""
+    from oracle import pik
+
+    xs = x[:rows].float().cpu().double().numpy()
+    ws = w.float().cpu().double().numpy()
+    pik.gemm_exact(xs[:8], ws)  # warm the BLAS threads
+    t0 = time.perf_counter()
+    pik.gemm_exact(xs, ws)
+    sec = time.perf_counter() - t0
+    flops = 2.0 * xs.shape[0] * ws.shape[0] * ws.shape[1]
+    return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {xs.shape[0]} rows of X against all of W ({sec:.2f} s)"}
+
+
 def run_pik(args, cpr, inputs, dev, dist, world):
     """Deterministic K-split product (pik): Y = X W^T with M = N = K = 8,192 and eight
     leaves, as one call over the whole tree, and as two rank calls of four leaves each plus
@@ -553,6 +569,9 @@ def run_pik(args, cpr, inputs, dev, dist, world):
         return _max_over_ranks(dist, statistics.fmean(ms))
 
     steps = max(3, min(args.steps, 20))
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = pik_cpu_baseline(x, w)
     ms = timed(whole, steps)
     ms2 = timed(two_ranks, steps)
     ms4 = timed(whole4, steps)
@@ -566,6 +585,7 @@ def run_pik(args, cpr, inputs, dev, dist, world):
         "workload": f"Y = X W^T, M = N = K = {M}, bf16 operands, fp32 accumulation and result, {L} leaves",
         "roofline": {"kernel": "k_pik_leaves", "bound": "tensor", "achieved": tf, "peak": peak, "peak_kind": kind,
                      "unit": "TFLOP/s", "frac": tf / peak, "traffic": None, "flops_per_launch": flops},
+        "cpu_baseline": cpu,
         "two_ranks_ms": ms2, "four_leaves_ms": ms4, "four_leaves_tflops": flops / (ms4 * 1e-3) / 1e12,
         "gpu_launches": 5 * steps,
     }
