@@ -167,3 +167,115 @@ def chunked_backward(q, k, v, g, beta, cu_seqlens, d_out, C, d_state_out=None, s
     out["d_state_in"] = d_state_in
     out["chain_mismatch"] = mismatch
     return out
+
+
+def _wy_chunk_forward(Sb, Q, K, V, g, b):
+    """One chunk of n tokens in the WY form (fp64): S_b (dv x dk) and the chunk's
+    q, k [n, dk], v [n, dv], g, beta [n].  Returns the intermediates the adjoint needs."""
+    n = len(g)
+    G = np.cumsum(g)
+    gam = np.exp(G)
+    low = np.tril(np.ones((n, n)), -1)  # i < r
+    lowd = np.tril(np.ones((n, n)))     # i <= r
+    E = np.exp(G[:, None] - G[None, :]) * lowd
+    KK = K @ K.T
+    L = KK * E * low
+    A = b[:, None] * L
+    T = np.linalg.inv(np.eye(n) + A)
+    Ut = T @ (b[:, None] * V)
+    W = T @ ((b * gam)[:, None] * K)
+    U = Ut - W @ Sb.T
+    Pm = (Q @ K.T) * E  # lower with diagonal
+    O = gam[:, None] * (Q @ Sb.T) + Pm @ U
+    d = np.exp(G[-1] - G)
+    S_end = gam[-1] * Sb + U.T @ (d[:, None] * K)
+    return dict(G=G, gam=gam, low=low, E=E, KK=KK, L=L, T=T, Ut=Ut, W=W, U=U, Pm=Pm, O=O, d=d, S_end=S_end)
+
+
+def _wy_chunk_backward(Sb, Q, K, V, g, b, dO, dS_end):
+    """Adjoint of one chunk in the WY form: returns (dS_b, dq, dk, dv, dg, dbeta)."""
+    f = _wy_chunk_forward(Sb, Q, K, V, g, b)
+    G, gam, low, E, KK, L, T, W, U, Pm, d = (f[x] for x in ("G", "gam", "low", "E", "KK", "L", "T", "W", "U", "Pm", "d"))
+    n = len(g)
+    dSb = np.zeros_like(Sb)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    dgam, dd, db = np.zeros(n), np.zeros(n), np.zeros(n)
+    # S_end = gam_last S_b + U^T diag(d) K
+    dSb += gam[-1] * dS_end
+    dgam[-1] += np.sum(dS_end * Sb)
+    dU = (d[:, None] * K) @ dS_end.T
+    UdS = U @ dS_end
+    dK += d[:, None] * UdS
+    dd += np.sum(UdS * K, axis=1)
+    # O = diag(gam) Q S_b^T + Pm U
+    dQ += gam[:, None] * (dO @ Sb)
+    dSb += dO.T @ (gam[:, None] * Q)
+    dgam += np.sum(dO * (Q @ Sb.T), axis=1)
+    dPm = (dO @ U.T) * np.tril(np.ones((n, n)))
+    dU += Pm.T @ dO
+    dQK = dPm * E
+    dQ += dQK @ K
+    dK += dQK.T @ Q
+    dE = dPm * (Q @ K.T)
+    # U = Ut - W S_b^T
+    dUt = dU
+    dW = -dU @ Sb
+    dSb += -dU.T @ W
+    # Ut = T diag(b) V,  W = T diag(b gam) K
+    bV, bgK = b[:, None] * V, (b * gam)[:, None] * K
+    dT = dUt @ bV.T + dW @ bgK.T
+    TdUt, TdW = T.T @ dUt, T.T @ dW
+    dV += b[:, None] * TdUt
+    db += np.sum(TdUt * V, axis=1) + gam * np.sum(TdW * K, axis=1)
+    dK += (b * gam)[:, None] * TdW
+    dgam += b * np.sum(TdW * K, axis=1)
+    # T = (I + A)^-1,  A = diag(b) L  (strictly lower)
+    dA = -(T.T @ dT @ T.T) * low
+    db += np.sum(dA * L, axis=1)
+    dL = b[:, None] * dA
+    # L = (K K^T) o E o low
+    dKK = dL * E * low
+    dK += (dKK + dKK.T) @ K
+    dE += dL * KK * low
+    # the gates: gam_r = e^{G_r}, d_i = e^{G_last - G_i}, E_ri = e^{G_r - G_i}
+    dG = gam * dgam
+    dG[-1] += np.sum(d * dd)
+    dG -= d * dd
+    ED = E * dE
+    dG += np.sum(ED, axis=1) - np.sum(ED, axis=0)
+    dg = np.cumsum(dG[::-1])[::-1]  # G = cumsum(g)
+    return dSb, dQ, dK, dV, dg, db
+
+
+def wy_chunked_backward(q, k, v, g, beta, cu_seqlens, d_out, C, d_state_out=None, state_in=None):
+    """The same gradients with every chunk's adjoint taken through the WY form (fp64):
+    the in-chunk work is matrix products (what tensor cores would run), and each chunk
+    hands dS_b to the previous one.  Same returns as ``recurrent_backward``."""
+    q, k, v, g, beta, d_out = (_f64(x) for x in (q, k, v, g, beta, d_out))
+    cu = [int(c) for c in np.asarray(cu_seqlens).reshape(-1)]
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = len(cu) - 1
+    s_in = np.zeros((N, H, dk, dv)) if state_in is None else _f64(state_in)
+    ds_out = np.zeros((N, H, dk, dv)) if d_state_out is None else _f64(d_state_out)
+    out = {name: np.zeros_like(x) for name, x in (("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dbeta", beta))}
+    d_state_in = np.zeros((N, H, dk, dv))
+    for n in range(N):
+        for h in range(H):
+            t0, t1 = cu[n], cu[n + 1]
+            starts = list(range(t0, t1, C))
+            bounds, S = [], s_in[n, h].T.copy()
+            for c0 in starts:
+                bounds.append(S)
+                sl = slice(c0, min(c0 + C, t1))
+                S = _wy_chunk_forward(S, q[sl, h], k[sl, h], v[sl, h], g[sl, h], beta[sl, h])["S_end"]
+            dS = ds_out[n, h].T.copy()
+            for j in range(len(starts) - 1, -1, -1):
+                sl = slice(starts[j], min(starts[j] + C, t1))
+                dS, dQ, dK, dV, dg, db = _wy_chunk_backward(bounds[j], q[sl, h], k[sl, h], v[sl, h], g[sl, h],
+                                                            beta[sl, h], d_out[sl, h], dS)
+                out["dq"][sl, h], out["dk"][sl, h], out["dv"][sl, h] = dQ, dK, dV
+                out["dg"][sl, h], out["dbeta"][sl, h] = dg, db
+            d_state_in[n, h] = dS.T
+    out["d_state_in"] = d_state_in
+    return out

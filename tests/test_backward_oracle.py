@@ -116,3 +116,16 @@ def test_chunked_schedule_equals_token_adjoint(C):
     for name in ref:
         np.testing.assert_allclose(got[name], ref[name], rtol=1e-10, atol=1e-12, err_msg=name)
     assert got["chain_mismatch"] < 1e-12
+
+
+@pytest.mark.parametrize("C,lens,dk,dv", [(1, (9, 0, 5, 1), 4, 3), (3, (9, 0, 5, 1), 4, 3), (8, (9, 0, 5, 1), 4, 3),
+                                          (16, (40, 17), 8, 6)])
+def test_wy_chunk_adjoint_equals_token_adjoint(C, lens, dk, dv):
+    # every chunk's adjoint through the WY form (matrix products only) = the token adjoint
+    x, cu, d_out, d_state = _problem(11, lens=lens, H=2, dk=dk, dv=dv)
+    ref = backward.recurrent_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, d_out, d_state,
+                                      state_in=x["state_in"])
+    got = backward.wy_chunked_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, d_out, C, d_state,
+                                       state_in=x["state_in"])
+    for name in ref:
+        np.testing.assert_allclose(got[name], ref[name], rtol=1e-9, atol=1e-11, err_msg=name)
