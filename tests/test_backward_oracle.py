@@ -129,3 +129,27 @@ def test_wy_chunk_adjoint_equals_token_adjoint(C, lens, dk, dv):
                                        state_in=x["state_in"])
     for name in ref:
         np.testing.assert_allclose(got[name], ref[name], rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+def test_chain_terms_in_wy_form():
+    # the chain's per-chunk terms from the forward's WY intermediates: the chunk map
+    # M = P = gamma_n I - W^T diag(d) K, and the propagated queries
+    # P_t q_t = (diag(gamma) Q - ((Q K^T) o D) W)_t, against the products of the token
+    # transitions A_t = alpha_t (I - beta_t k_t k_t^T)
+    rng = np.random.default_rng(13)
+    n, dk, dv = 7, 5, 4
+    K = rng.standard_normal((n, dk))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    Q = rng.standard_normal((n, dk))
+    V = rng.standard_normal((n, dv))
+    g = -0.5 * np.log1p(np.exp(rng.standard_normal(n)))
+    b = 1.0 / (1.0 + np.exp(-rng.standard_normal(n)))
+    f = backward._wy_chunk_forward(np.zeros((dv, dk)), Q, K, V, g, b)
+    P, qt = np.eye(dk), []
+    for t in range(n):
+        P = P @ (np.exp(g[t]) * (np.eye(dk) - b[t] * np.outer(K[t], K[t])))
+        qt.append(P @ Q[t])
+    M = f["gam"][-1] * np.eye(dk) - f["W"].T @ (f["d"][:, None] * K)
+    np.testing.assert_allclose(M, P, rtol=1e-12, atol=1e-14)
+    Qt = f["gam"][:, None] * Q - f["Pm"] @ f["W"]
+    np.testing.assert_allclose(Qt, np.array(qt), rtol=1e-12, atol=1e-14)
