@@ -14,9 +14,9 @@
 // likewise for the W rows of the two CTAs that share n, so each CTA pulls half its
 // operand bytes from L2.  Warp 0 issues the loads into six stages, warp 1 issues the
 // MMAs (4 per stage, K = 16 each) and commits each stage to the stage-free barriers of
-// all four CTAs; warps 4-7 merge partials and run the epilogue.  Up to four leaves: each leaf of the CTA's range accumulates in its
-// own TMEM slot of 128 columns, the loop never waits for a reduction, and the epilogue
-// sums the slots with the tree in registers.  Eight leaves: slot popcount(j) takes leaf j;
+// all four CTAs; warps 4-7 merge partials and run the epilogue.  Up to four leaves: each
+// leaf of the CTA's range accumulates in its own TMEM slot of 128 columns, the loop never
+// waits for a reduction, and the epilogue sums the slots with the tree in registers.  Eight leaves: slot popcount(j) takes leaf j;
 // when an odd leaf completes, warps 4-7 merge the finished pairs of the tree in TMEM (a
 // binary counter: at most four live partials) before the next leaf starts, leaving the
 // root in slot 0.  A leaf's instruction sequence, and so every bit of its partial, is the
