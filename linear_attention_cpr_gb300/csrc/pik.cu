@@ -16,9 +16,10 @@
 // MMAs (4 per stage, K = 16 each) and commits each stage to the stage-free barriers of
 // all four CTAs; warps 4-7 merge partials and run the epilogue.  Up to four leaves: each
 // leaf of the CTA's range accumulates in its own TMEM slot of 128 columns, the loop never
-// waits for a reduction, and the epilogue sums the slots with the tree in registers.  Eight leaves: slot popcount(j) takes leaf j;
-// when an odd leaf completes, warps 4-7 merge the finished pairs of the tree in TMEM (a
-// binary counter: at most four live partials) before the next leaf starts, leaving the
+// waits for a reduction, and the epilogue sums the slots with the tree in registers.
+// Eight leaves: slot popcount(j) takes leaf j; when an odd leaf completes, warps 4-7
+// merge the finished pairs of the tree in TMEM (a binary counter: at most four live
+// partials) before the next leaf starts, leaving the
 // root in slot 0.  A leaf's instruction sequence, and so every bit of its partial, is the
 // same whichever leaf range a call covers.
 // k_pik_combine: the top of the same tree over the ranks' subtree roots (HBM-bound).
@@ -376,7 +377,8 @@ extern "C" int32_t cpr_pik_combine(const float* parts, int32_t n_parts, int64_t 
     if (!al16(parts) || !al16(y)) return CPR_ERR_MISALIGNED;
     if (count == 0) return CPR_OK;
     int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return CPR_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int vec = count % 4 == 0;
