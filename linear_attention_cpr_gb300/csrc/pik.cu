@@ -19,9 +19,9 @@
 // waits for a reduction, and the epilogue sums the slots with the tree in registers.
 // Eight leaves: slot popcount(j) takes leaf j; when an odd leaf completes, warps 4-7
 // merge the finished pairs of the tree in TMEM (a binary counter: at most four live
-// partials) before the next leaf starts, leaving the
-// root in slot 0.  A leaf's instruction sequence, and so every bit of its partial, is the
-// same whichever leaf range a call covers.
+// partials) before the next leaf starts, leaving the root in slot 0.  A leaf's
+// instruction sequence, and so every bit of its partial, is the same whichever leaf range
+// a call covers.
 // k_pik_combine: the top of the same tree over the ranks' subtree roots (HBM-bound).
 #include <cuda.h>
 #include <cuda_bf16.h>
