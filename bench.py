@@ -4,12 +4,21 @@
 
 One step = one CPR prefill / training forward of the trainer-shaped workload (1 sequence
 x 10,240 tokens, H=16, dk=dv=128, C=64, bf16 q/k/v, fp32 state), inputs resident in HBM,
-L2 flushed between steps.  The JSON line also carries the rollout-decode workload (256
-sequences x 1 token, prior lengths U[1,4096], steps/s), the roofline of each path's
-dominant kernel, the end-to-end number through the C ABI with host buffers, and the
-fp64 CPU oracle timed on this machine's cores.  Under torchrun every rank runs the same
-workload on its own GPU (independent problems: weak scaling, no collective on the data
-path); rank 0 prints the line.
+L2 flushed between steps.  The JSON line also carries, each with its own rate and
+roofline:
+  - decode: the rollout-decode workload (256 sequences x 1 token, prior lengths
+    U[1,4096], steps/s);
+  - continuation: the rollout prefill resumed at seeded positions;
+  - rollout_prefill: the 5 x 2,048 packed rollout prefill in one call;
+  - varlen_stress: 32 packed sequences of log-uniform lengths (H=32), prefill and then
+    128 decode steps;
+  - tiny: the fp32 case's prefill and decode-step latency;
+  - pik: the deterministic K-split product (one GPU only);
+  - fp32_peak_probe: the FP32-pipe peak measured on this GPU by the committed probe;
+plus the end-to-end number through the C ABI with host buffers, and the fp64 CPU oracle
+timed on this machine's cores.  Under torchrun every rank runs the same workload on its
+own GPU (independent problems: weak scaling, no collective on the data path); rank 0
+prints the line.
 """
 from __future__ import annotations
 
@@ -214,6 +223,206 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def measure_fp32_peak(dev):
+    """FP32-pipe peak of this GPU from the committed probe (csrc/probe_peaks.cu): scalar
+    FFMA and paired f32x2 FMA over every SM, the larger of the two, in TFLOP/s."""
+    import ctypes
+
+    from linear_attention_cpr_gb300 import build
+
+    lib = ctypes.CDLL(build.PROBE_LIB)
+    lib.cpr_probe_fp32.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, threads, iters = sms * 8, 256, 20000
+    sink = torch.empty(blocks * threads, dtype=torch.float32, device=dev)
+    ms = ctypes.c_float(0.0)
+    best = {}
+    for paired in (0, 1):
+        vals = []
+        for _ in range(4):
+            rc = lib.cpr_probe_fp32(paired, blocks, threads, iters, ctypes.c_void_p(sink.data_ptr()),
+                                    ctypes.byref(ms), None)
+            if rc != 0:
+                return None
+            vals.append(ms.value)
+        flops = blocks * threads * iters * 16 * 2 * (2 if paired else 1)
+        best["ffma2" if paired else "ffma"] = flops / (min(vals[1:]) * 1e-3) / 1e12
+    return {"tflops": max(best.values()), "ffma": best["ffma"], "ffma2": best["ffma2"],
+            "how": f"{blocks} CTAs x {threads} threads x {iters} rounds of 16 independent FMA chains"}
+
+
+def time_prefill(cpr, w, x, dev, steps, warmup, dist, flush, p32_meas=None):
+    """Time one workload's prefill through the C ABI (inputs resident, L2 flushed between
+    steps outside the events) with the per-kernel events of the profiling hook.  Returns
+    the line's fields: ms per step, kernel times, tokens/s, roofline of k23 (FP32 bound)."""
+    T, H, dk, dv, C, N = w.total_tokens, w.H, w.dk, w.dv, w.C, len(w.seqlens)
+    n_chunks = cpr.cpr_gdn_num_chunks(x["cu_seqlens"].cpu(), C)
+    out = torch.empty(T, H, dv, dtype=w.dtype, device=dev)
+    st = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    bnd = torch.empty(max(n_chunks, 1), H, dk, dv, dtype=torch.float32, device=dev)
+    ws = torch.empty(cpr.cpr_gdn_prefill_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
+
+    def prefill():
+        cpr.cpr_gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], C, out=out, state_out=st,
+                            boundary_states=bnd, workspace=ws)
+
+    for _ in range(warmup):
+        prefill()
+    torch.cuda.synchronize()
+    assert cpr.cpr_gdn_device_status(ws) == 0
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    kern = {"chunk_index": [], "chunk_prep": [], "chain_and_intra": []}
+    step_ms = []
+    _barrier(dist)
+    cpr.cpr_gdn_set_profile_events(ev)
+    for _ in range(steps):
+        flush.zero_()
+        prefill()
+        ev[3].synchronize()
+        step_ms.append(ev[0].elapsed_time(ev[3]))
+        for i, name in enumerate(kern):
+            kern[name].append(ev[i].elapsed_time(ev[i + 1]))
+    cpr.cpr_gdn_set_profile_events(None)
+    _barrier(dist)
+    ms_max = _max_over_ranks(dist, statistics.fmean(step_ms))
+    kern_ms = {k: statistics.fmean(v) for k, v in kern.items()}
+    alg_bytes, flops = prefill_algorithmic(T, N, H, dk, dv, n_chunks, elem=2 if w.dtype == torch.bfloat16 else 4)
+    achieved = flops / (kern_ms["chain_and_intra"] / 1e3) / 1e12
+    roof = {"kernel": "k23_chain_and_intra", "bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS,
+            "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
+            "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz", "flops_per_launch": flops}
+    if p32_meas:
+        roof["peak_measured"] = p32_meas["tflops"]
+        roof["frac_of_measured"] = achieved / p32_meas["tflops"]
+    hbm_peak, _ = _peaks()
+    t_roof_ms = max(alg_bytes / (hbm_peak * 1e9), flops / (FP32_PEAK_TFLOPS * 1e12)) * 1e3
+    return {"ms_per_step": ms_max, "value": weak_scaling_rate(dist.get_world_size() if dist else 1, T, ms_max),
+            "unit": "tokens/s", "steps": steps, "kernels_ms": kern_ms, "algorithmic_bytes": alg_bytes,
+            "t_roof_ms": t_roof_ms, "frac_of_t_roof": t_roof_ms / ms_max, "roofline": roof, "n_chunks": n_chunks,
+            "gpu_launches": 3 * steps}
+
+
+def time_decode_steps(cpr, w, state, ring, pos0, dev, steps, warmup, dist, flush, hbm_peak):
+    """Time `steps` decode steps of a workload's sequences from a prefilled state and ring,
+    one step per timed region (events of the profiling hook), L2 flushed between steps when
+    the resident state is smaller than L2.  Returns the line's fields."""
+    B, H, dk, dv, C = len(w.seqlens), w.H, w.dk, w.dv, w.C
+    toks = [inputs_decode(w, s, dev) for s in range(min(steps, 64))]
+    pos = pos0.clone().to(dev)
+    out = torch.empty(B, H, dv, dtype=w.dtype, device=dev)
+    dws = torch.empty(cpr.cpr_gdn_decode_workspace_size(B, H, dk, dv, C), dtype=torch.uint8, device=dev)
+    small = B * H * dk * dv * 4 < L2_BYTES
+
+    def step(s):
+        t = toks[s % len(toks)]
+        cpr.cpr_gdn_decode(t["q"], t["k"], t["v"], t["g"], t["beta"], state, ring, pos, C, out=out, workspace=dws)
+        pos.add_(1)
+
+    for s in range(warmup):
+        step(s)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    step_ms, k4 = [], []
+    n_res = 0
+    pos_host = pos0.clone().cpu() + warmup
+    _barrier(dist)
+    cpr.cpr_gdn_set_profile_events(ev)
+    for s in range(warmup, warmup + steps):
+        n_res += int(((pos_host % C) == C - 1).sum())
+        pos_host += 1
+        if small:
+            flush.zero_()
+        step(s)
+        ev[2].synchronize()
+        step_ms.append(ev[0].elapsed_time(ev[2]))
+        k4.append(ev[0].elapsed_time(ev[1]))
+    cpr.cpr_gdn_set_profile_events(None)
+    _barrier(dist)
+    assert cpr.cpr_gdn_device_status(dws) == 0
+    ms = _max_over_ranks(dist, statistics.fmean(step_ms))
+    k4_ms = statistics.fmean(k4)
+    bytes_step = decode_algorithmic(B, H, dk, dv, C, n_res / steps, elem=2 if w.dtype == torch.bfloat16 else 4)
+    step_only = decode_algorithmic(B, H, dk, dv, C, 0, elem=2 if w.dtype == torch.bfloat16 else 4)
+    ach = step_only / (k4_ms / 1e3) / 1e9
+    world = dist.get_world_size() if dist else 1
+    return {"metric": "decode steps/s per layer", "value": 1e3 / ms * world, "unit": "steps/s", "ms_per_step": ms,
+            "steps": steps, "kernels_ms": {"step_with_concurrent_resync": k4_ms},
+            "resyncs_per_step": n_res / steps, "l2": "flushed between steps" if small else "state larger than L2",
+            "roofline": {"kernel": "k4_decode_step", "bound": "hbm", "achieved": ach, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": ach / hbm_peak, "traffic": None, "bytes_per_launch": step_only},
+            "t_roof_ms": bytes_step / (hbm_peak * 1e9) * 1e3,
+            "frac_of_t_roof": bytes_step / (hbm_peak * 1e9) * 1e3 / ms, "gpu_launches": 2 * steps}
+
+
+def inputs_decode(w, s, dev):
+    from linear_attention_cpr_gb300 import inputs
+
+    return inputs.decode_inputs(w, s, device=dev)
+
+
+def run_extra_workloads(args, cpr, inputs, dev, dist, world, flush, p32_meas, hbm_peak):
+    """The other configurations of the layer, each with its own line: the one-shot rollout
+    prefill (5 x 2,048 packed), the varlen stress batch (prefill, then 128 decode steps) and
+    the tiny fp32 case (latency in microseconds)."""
+    res = {}
+    steps = max(3, min(args.steps, 50))
+    # rollout prefill: the five sequences in one packed call
+    w = inputs.workload("rollout_prefill")
+    xc = inputs.prefill_inputs(w)
+    x = {k: v.to(dev) for k, v in xc.items()}
+    line = time_prefill(cpr, w, x, dev, steps, args.warmup, dist, flush, p32_meas)
+    line.update({"metric": "rollout prefill tokens/s per layer",
+                 "workload": f"rollout_prefill: 5 x 2,048 tokens packed in one call, H={w.H}, dk=dv={w.dk}, "
+                             f"C={w.C}, bf16 q/k/v"})
+    if world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample = cpu_baseline_oracle(xc, w.C, target_s=5.0)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    res["rollout_prefill"] = line
+    del x
+    # varlen stress: prefill of the packed batch, then decode steps of every sequence
+    w = inputs.workload("varlen_stress")
+    xc = inputs.prefill_inputs(w)
+    x = {k: v.to(dev) for k, v in xc.items()}
+    line = time_prefill(cpr, w, x, dev, steps, args.warmup, dist, flush, p32_meas)
+    line.update({"metric": "varlen prefill tokens/s per layer",
+                 "workload": f"varlen_stress: {len(w.seqlens)} sequences, log-uniform lengths in [64, 8192], "
+                             f"{w.total_tokens} tokens, H={w.H}, dk=dv={w.dk}, C={w.C}, bf16 q/k/v"})
+    if world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample = cpu_baseline_oracle(xc, w.C, target_s=3.0)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    _, st, bnd, _ = cpr.cpr_gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], w.C)
+    ring = cpr.cpr_gdn_ring_from_prefill(x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], w.C, bnd, st)
+    pos0 = torch.tensor(w.seqlens, dtype=torch.int32)
+    dec = time_decode_steps(cpr, w, st, ring, pos0, dev, w.decode_steps, args.warmup, dist, flush, hbm_peak)
+    dec["workload"] = (f"varlen_stress decode: {len(w.seqlens)} sequences x 1 token after the prefill, H={w.H}, "
+                       f"dk=dv={w.dk}, C={w.C}, {w.decode_steps} steps")
+    line["decode"] = dec
+    res["varlen_stress"] = line
+    del x, st, bnd, ring
+    # tiny fp32: latency of one prefill and of one decode step
+    w = inputs.workload("tiny")
+    xc = inputs.prefill_inputs(w)
+    x = {k: v.to(dev) for k, v in xc.items()}
+    line = time_prefill(cpr, w, x, dev, steps, args.warmup, dist, flush, p32_meas)
+    pre = {k: v[:w.total_tokens - 1] for k, v in x.items() if k != "cu_seqlens"}
+    cu_pre = inputs.cu_seqlens_of([w.total_tokens - 1]).to(dev)
+    _, st, bnd, _ = cpr.cpr_gdn_prefill(pre["q"], pre["k"], pre["v"], pre["g"], pre["beta"], cu_pre, w.C)
+    ring = cpr.cpr_gdn_ring_from_prefill(pre["k"], pre["v"], pre["g"], pre["beta"], cu_pre, w.C, bnd, st)
+    dec = time_decode_steps(cpr, w, st, ring, torch.tensor([w.total_tokens - 1], dtype=torch.int32), dev, steps,
+                            args.warmup, dist, flush, hbm_peak)
+    res["tiny"] = {"metric": "tiny fp32 latency per layer", "workload": "tiny: 1 x 256 tokens, H=2, dk=dv=32, "
+                   "C=16, fp32 q/k/v (latency-bound: no roofline fraction)",
+                   "prefill_us": 1e3 * line["ms_per_step"], "prefill_kernels_us":
+                   {k: 1e3 * v for k, v in line["kernels_ms"].items()},
+                   "decode_step_us": 1e3 * dec["ms_per_step"], "steps": steps,
+                   "gpu_launches": line["gpu_launches"] + dec["gpu_launches"]}
+    return res
+
+
+
 def run_ours(args):
     import linear_attention_cpr_gb300 as cpr
     from linear_attention_cpr_gb300 import build, inputs
@@ -226,6 +435,8 @@ def run_ours(args):
     hbm_peak, hbm_kind = _peaks()
     gen_dev = torch.Generator(device=dev)
     if args.only_pik:  # the deterministic K-split product alone (profiling and quick checks)
+        if world > 1:
+            raise SystemExit("--only-pik runs on one GPU only")
         line = run_pik(args, cpr, inputs, dev, dist, world)
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -309,7 +520,15 @@ def run_ours(args):
     if not args.no_decode:
         decode = run_decode(args, cpr, inputs, dev, hbm_peak, dist, world)
     continuation = run_continuation(args, cpr, inputs, dev, hbm_peak, dist, world) if not args.no_decode else None
-    pik_line = run_pik(args, cpr, inputs, dev, dist, world) if not args.no_pik else None
+    # the K-split product is a one-GPU leg: under torchrun it is left out on every rank
+    pik_line = run_pik(args, cpr, inputs, dev, dist, world) if not args.no_pik and world == 1 else None
+
+    p32_meas = measure_fp32_peak(dev)
+    if p32_meas:
+        roofline["peak_measured"] = p32_meas["tflops"]
+        roofline["frac_of_measured"] = roofline["achieved"] / p32_meas["tflops"]
+    extra = None if args.no_extra else run_extra_workloads(args, cpr, inputs, dev, dist, world, flush, p32_meas,
+                                                           hbm_peak)
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only) ----------------
     cpu = None
@@ -332,11 +551,17 @@ def run_ours(args):
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches + (decode["gpu_launches"] if decode else 0) +
                             (continuation["gpu_launches"] if continuation else 0) +
-                            (pik_line["gpu_launches"] if pik_line else 0),
+                            (pik_line["gpu_launches"] if pik_line else 0) +
+                            (sum(v["gpu_launches"] + (v.get("decode") or {}).get("gpu_launches", 0)
+                                 for v in extra.values()) if extra else 0),
             "clocks": clocks.summary(),
             "decode": decode,
             "continuation": continuation,
             "pik": pik_line,
+            "rollout_prefill": extra["rollout_prefill"] if extra else None,
+            "varlen_stress": extra["varlen_stress"] if extra else None,
+            "tiny": extra["tiny"] if extra else None,
+            "fp32_peak_probe": p32_meas,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -602,6 +827,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pik", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the rollout_prefill, varlen_stress and tiny lines")
     ap.add_argument("--only-pik", action="store_true")
     ap.add_argument("--pik-size", type=int, default=8192, help="M = N = K of the pik product (a multiple of 512)")
     args = ap.parse_args()

@@ -63,7 +63,7 @@ extern "C" {
 #define CPR_DEV_BAD_CU_SEQLENS 1u /* cu_seqlens[0] != 0, decreasing, or last != total_tokens */
 #define CPR_DEV_BOUNDARY_CAPACITY 2u /* more chunks than boundary_capacity */
 #define CPR_DEV_BAD_POS 4u        /* a decode position is negative */
-#define CPR_DEV_TIMEOUT 8u        /* a tensor-core wait gave up (work of that CTA skipped) */
+#define CPR_DEV_TIMEOUT 8u        /* a bounded device wait gave up (the work behind it skipped) */
 
 /* Element types of q, k, v, out and the ring's k, v. */
 #define CPR_DTYPE_BF16 0
@@ -263,17 +263,30 @@ int32_t cpr_gdn_prefill_continue_grouped(const void* q, const void* k, const voi
  *     x 7 chunks).
  *   - The first call on each device looks up the scratch's device address with that
  *     device current (this may load the library's device code): make it before any
- *     stream capture begins.
+ *     stream capture begins.  The address is remembered per device for the life of the
+ *     process; cudaDeviceReset invalidates it, so do not call this entry point on a
+ *     device after resetting it.
  *   - All calls share the scratch, which keeps the last call's contents (nothing in it
  *     needs to start at zero).  Calls that overlap on the GPU race on it: serialise them.
- *   - The device status word lives in that scratch and is not readable by the caller.
- * Results are those cpr_gdn_prefill returns for the same arguments.
+ *   - The device status word of the last call lives in that scratch; read it with
+ *     cpr_gdn_prefill_noalloc_status.
+ * Results are bit for bit those cpr_gdn_prefill returns for the same arguments.
  */
 #define CPR_GDN_NOALLOC_SCRATCH_BYTES (16u << 20)
 int32_t cpr_gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                 const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,
                                 int32_t dk, int32_t dv, int32_t C, int32_t dtype, const float* state_in, void* out,
                                 float* state_out, float* boundary_states, int64_t boundary_capacity, void* stream);
+
+/*
+ * Device status word of the last cpr_gdn_prefill_noalloc call on the current device (an
+ * OR of CPR_DEV_* bits, 0 when every device-side check passed, e.g. CPR_DEV_TIMEOUT when
+ * a bounded wait gave up and some outputs were not written).  Waits for `stream`, copies
+ * the word from the library's scratch into *status_out and allocates nothing; the same
+ * first-call and reset rules as cpr_gdn_prefill_noalloc apply.  Returns CPR_OK,
+ * CPR_ERR_INVALID_ARG (status_out NULL) or CPR_ERR_CUDA.
+ */
+int32_t cpr_gdn_prefill_noalloc_status(uint32_t* status_out, void* stream);
 
 /*
  * Profiling hook (used by the benchmark to time each kernel with CUDA events on the
@@ -286,6 +299,18 @@ int32_t cpr_gdn_prefill_noalloc(const void* q, const void* k, const void* v, con
  * from several threads.
  */
 int32_t cpr_gdn_set_profile_events(void* const* events, int32_t n_events);
+
+/*
+ * Test hook for the failure path of the prefill's one device-side wait on other CTAs
+ * (an intra-chunk item waiting for its boundary state to be published by the chain).
+ * While extra_publications > 0, every item waits for that many publications more than
+ * the chain ever makes, so each wait runs out after limit_ns nanoseconds (0: the
+ * default of about 4 s), the item is skipped (its outputs are not written) and the call
+ * records CPR_DEV_TIMEOUT in its status word; the context stays usable.
+ * cpr_gdn_set_wait_test(0, 0) restores normal operation.  Process-wide, read when a
+ * prefill is enqueued; not for concurrent use with other calls.  Returns CPR_OK.
+ */
+int32_t cpr_gdn_set_wait_test(uint32_t extra_publications, uint64_t limit_ns);
 
 /*
  * Read the device status word of the last call that used `workspace` (waits for

@@ -18,9 +18,11 @@
  *     that subtree's root; cpr_pik_combine then finishes the same tree over the ranks'
  *     roots.  The result is therefore bit-identical for every rank count that divides
  *     n_leaves, including one rank computing everything in a single cpr_pik_gemm call.
- * The library moves no partial sums between GPUs: a caller with several GPUs gathers
- * the roots (any transport) and calls cpr_pik_combine; on one GPU the roots are
- * consecutive buffers.
+ * Every call runs on one GPU, the current device, over that GPU's own memory.  The
+ * library moves no partial sums between GPUs: a caller with several GPUs computes each
+ * rank's subtree root on that rank's GPU, gathers the roots into one buffer with its own
+ * transport, and then calls cpr_pik_combine there; on one GPU the roots are consecutive
+ * buffers.
  *
  * Conventions (as in cpr_gdn.h): device pointers on the current device, row-major and
  * contiguous; the caller owns every buffer; all work is enqueued on `stream`; the
@@ -45,8 +47,11 @@ extern "C" {
 size_t cpr_pik_workspace_size(void);
 
 /* Subtree root of leaves [leaf_lo, leaf_hi) of Y = X W^T.
- *   x          bf16 [M, K] (K contiguous), 16-byte aligned
- *   w          bf16 [N, K] (K contiguous: the layout of a linear layer's weight), 16-byte aligned
+ *   x          bf16 [M, K] (K contiguous), 16-byte aligned, device memory of the current device
+ *   w          bf16 [N, K] (K contiguous: the layout of a linear layer's weight), 16-byte
+ *              aligned, device memory of the current device (host, managed or another GPU's
+ *              memory is rejected with CPR_ERR_INVALID_ARG: the operands are read through
+ *              tensor maps that must describe this GPU's own buffers)
  *   y          fp32 [M, N], written (not accumulated); 4-byte aligned
  *   M, N       >= 1, any value (ragged tiles are masked)
  *   K          a multiple of 64 * n_leaves

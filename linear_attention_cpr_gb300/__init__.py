@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     cpr_gdn_prefill,
     cpr_gdn_prefill_continue,
     cpr_gdn_prefill_noalloc,
+    cpr_gdn_prefill_noalloc_status,
     cpr_gdn_prefill_workspace_size,
     cpr_gdn_ring_from_prefill,
     cpr_gdn_set_profile_events,

@@ -25,9 +25,9 @@ EXPORTED = (
     "cpr_gdn_supported", "cpr_gdn_version", "cpr_gdn_strerror", "cpr_gdn_num_chunks",
     "cpr_gdn_prefill_workspace_size", "cpr_gdn_decode_workspace_size", "cpr_gdn_prefill",
     "cpr_gdn_ring_from_prefill", "cpr_gdn_decode", "cpr_gdn_device_status", "cpr_gdn_set_profile_events",
-    "cpr_gdn_prefill_noalloc", "cpr_gdn_prefill_continue", "cpr_gdn_prefill_grouped",
+    "cpr_gdn_prefill_noalloc", "cpr_gdn_prefill_noalloc_status", "cpr_gdn_prefill_continue", "cpr_gdn_prefill_grouped",
     "cpr_gdn_ring_from_prefill_grouped", "cpr_gdn_decode_grouped", "cpr_gdn_prefill_continue_grouped",
-    "cpr_pik_workspace_size", "cpr_pik_gemm", "cpr_pik_combine",
+    "cpr_pik_workspace_size", "cpr_pik_gemm", "cpr_pik_combine", "cpr_gdn_set_wait_test",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # CPR_GDN_NOALLOC_SCRATCH_BYTES
 
@@ -78,6 +78,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         "cpr_gdn_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
         "cpr_gdn_set_profile_events": (I32, [ctypes.POINTER(ctypes.c_void_p), I32]),
         "cpr_gdn_prefill_noalloc": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P, P, P, I64, P]),
+        "cpr_gdn_prefill_noalloc_status": (I32, [ctypes.POINTER(ctypes.c_uint32), P]),
+        "cpr_gdn_set_wait_test": (I32, [U32, ctypes.c_uint64]),
         "cpr_gdn_prefill_continue": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P,
                                            ctypes.POINTER(_Ring), P, P, I64, P, SZ, P]),
         "cpr_gdn_prefill_grouped": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, U32, I32, I32, I32, I32, P, P, P, P,
@@ -296,6 +298,13 @@ def cpr_gdn_decode(q, k, v, g, beta, state, ring: Ring, pos, C: int, *, out=None
     return out, workspace
 
 
+def cpr_gdn_set_wait_test(extra_publications: int, limit_ns: int = 0) -> None:
+    """Timeout-test hook: while extra_publications > 0 the prefill's intra-chunk items
+    wait for publications that never come and give up after limit_ns (0: about 4 s),
+    recording CPR_DEV_TIMEOUT.  (0, 0) restores normal operation."""
+    _check("cpr_gdn_set_wait_test", load_library().cpr_gdn_set_wait_test(int(extra_publications), int(limit_ns)))
+
+
 def cpr_gdn_device_status(workspace, stream=None) -> int:
     st = ctypes.c_uint32(0)
     code = load_library().cpr_gdn_device_status(_ptr(workspace), ctypes.byref(st), _stream(stream))
@@ -338,6 +347,15 @@ def cpr_gdn_prefill_noalloc(q, k, v, g, beta, cu_seqlens, C: int, state_in=None,
         _stream(stream))
     _check("cpr_gdn_prefill_noalloc", code)
     return out, state_out, boundary_states
+
+
+def cpr_gdn_prefill_noalloc_status(stream=None) -> int:
+    """Status word (CPR_DEV_* bits) of the last cpr_gdn_prefill_noalloc call on the current
+    device, read from the library's scratch (waits for the stream)."""
+    st = ctypes.c_uint32(0)
+    code = load_library().cpr_gdn_prefill_noalloc_status(ctypes.byref(st), _stream(stream))
+    _check("cpr_gdn_prefill_noalloc_status", code)
+    return int(st.value)
 
 
 def cpr_pik_workspace_size() -> int:

@@ -27,6 +27,11 @@ bool dtype_ok(int32_t dtype) { return dtype == CPR_DTYPE_BF16 || dtype == CPR_DT
 
 int32_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CPR_OK : CPR_ERR_CUDA; }
 
+// Timeout-test hook (cpr_gdn_set_wait_test): extra publications the intra-chunk items
+// wait for, and their wait limit (0: the default).
+uint32_t g_wait_extra = 0;
+uint64_t g_wait_limit_ns = 0;
+
 constexpr int kMaxProfileEvents = 8;
 cudaEvent_t g_profile_events[kMaxProfileEvents] = {};
 int g_profile_n = 0;
@@ -57,7 +62,7 @@ int cpr_gdn_supported(int32_t dk, int32_t dv, int32_t C, int32_t dtype)
     return (dtype_ok(dtype) && shape_built(dk, dv, C)) ? 1 : 0;
 }
 
-int32_t cpr_gdn_version(void) { return 1; }
+int32_t cpr_gdn_version(void) { return 2; }
 
 const char* cpr_gdn_strerror(int32_t code)
 {
@@ -147,6 +152,8 @@ int32_t cpr_gdn_prefill_grouped(const void* q, const void* k, const void* v, con
     a.num_sms = num_sms();
     if (a.num_sms <= 0) return CPR_ERR_CUDA;
     a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);
+    a.wait_extra = g_wait_extra;
+    a.wait_limit_ns = g_wait_limit_ns;
     if (!boundary_states) {
         // boundary states are also the chain's hand-off to the intra-chunk kernel
         return CPR_ERR_INVALID_ARG;
@@ -216,6 +223,8 @@ int32_t cpr_gdn_prefill_continue_grouped(const void* q, const void* k, const voi
     a.num_sms = num_sms();
     if (a.num_sms <= 0) return CPR_ERR_CUDA;
     a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);
+    a.wait_extra = g_wait_extra;
+    a.wait_limit_ns = g_wait_limit_ns;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorInvalidValue;
 #define CPR_DISPATCH(DK, DV, CC)                                                                             \
@@ -330,6 +339,13 @@ int32_t cpr_gdn_set_profile_events(void* const* events, int32_t n_events)
         g_profile_events[i] = static_cast<cudaEvent_t>(events[i]);
     }
     g_profile_n = n_events;
+    return CPR_OK;
+}
+
+int32_t cpr_gdn_set_wait_test(uint32_t extra_publications, uint64_t limit_ns)
+{
+    g_wait_extra = extra_publications;
+    g_wait_limit_ns = limit_ns;
     return CPR_OK;
 }
 

@@ -81,6 +81,11 @@ struct PrefillArgs {
     uint32_t* ready;
     int64_t max_chunks;
     int num_sms;
+    // the items' wait for a published boundary state: the count it waits for is
+    // NSLICE + wait_extra (0 except in the timeout test, where nothing reaches it), and it
+    // gives up after wait_limit_ns (0: the default of about 4 s)
+    uint32_t wait_extra;
+    uint64_t wait_limit_ns;
 };
 
 // Decode workspace: [0, 256) status word.

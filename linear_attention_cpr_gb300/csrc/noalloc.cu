@@ -16,13 +16,19 @@
 // that device current, the entry point asks the runtime for the array's device address
 // with cudaGetSymbolAddress, checks the result and remembers it for that device.
 // Because that first call may load the library's device code, make it before any stream
-// capture begins.
+// capture begins.  cudaDeviceReset on a device unloads the module and so invalidates the
+// remembered address: a process that resets a device must not call these entry points
+// on it afterwards.
 //
 // All calls share the one array and it keeps the last call's contents.  Nothing in it
 // has to start at zero: every call's first kernel rewrites the status word and the chunk
 // index, and each later kernel reads only what an earlier kernel of the same call wrote.
 // Calls that can overlap on the GPU (different streams, or different host threads)
 // race on the array and must be serialised by the caller.
+//
+// The prefill's device-side checks (bad cu_seqlens, boundary capacity, a bounded wait
+// that gave up) set bits in a status word at the start of the scratch;
+// cpr_gdn_prefill_noalloc_status reads it back, again without allocating.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -56,6 +62,14 @@ cudaError_t scratch_address(void** out)
 }
 
 }  // namespace
+
+extern "C" int32_t cpr_gdn_prefill_noalloc_status(uint32_t* status_out, void* stream)
+{
+    if (!status_out) return CPR_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return CPR_ERR_CUDA;
+    return cpr_gdn_device_status(scratch, status_out, stream);
+}
 
 extern "C" int32_t cpr_gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float* g,
                                            const float* beta, const int32_t* cu_seqlens, int32_t n_seqs,

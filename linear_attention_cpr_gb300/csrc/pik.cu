@@ -7,21 +7,20 @@
 // one binary tree over the leaves fixes how their partial sums meet, so the result does
 // not depend on how the leaves are shared among ranks.
 //
-// k_pik_leaves: one CTA per 128 x 128 output tile, in clusters of 2 x 2 tiles.  A tile's
-// operands are 128 rows of X and 128 rows of W per 64 K elements, each row 128 bytes in
-// the tensor cores' 128-byte-swizzled K-major layout; the two CTAs of a cluster that share
-// the X rows (same m) each load 64 of them with one TMA box and multicast it to both, and
-// likewise for the W rows of the two CTAs that share n, so each CTA pulls half its
-// operand bytes from L2.  Warp 0 issues the loads into six stages, warp 1 issues the
-// MMAs (4 per stage, K = 16 each) and commits each stage to the stage-free barriers of
-// all four CTAs; warps 4-7 merge partials and run the epilogue.  Up to four leaves: each
-// leaf of the CTA's range accumulates in its own TMEM slot of 128 columns, the loop never
-// waits for a reduction, and the epilogue sums the slots with the tree in registers.
-// Eight leaves: slot popcount(j) takes leaf j; when an odd leaf completes, warps 4-7
-// merge the finished pairs of the tree in TMEM (a binary counter: at most four live
-// partials) before the next leaf starts, leaving the root in slot 0.  A leaf's
-// instruction sequence, and so every bit of its partial, is the same whichever leaf range
-// a call covers.
+// k_pik_leaves: one CTA per 128 x 128 output tile.  A tile's operands are 128 rows of X
+// and 128 rows of W per 64 K elements, each row 128 bytes in the tensor cores'
+// 128-byte-swizzled K-major layout; each CTA loads its own X and W boxes (one TMA box of
+// 128 rows each, into its own shared memory, completing on its own barrier).  Tiles are
+// rastered in groups of kGroup tile rows, so the CTAs resident at one time share their
+// operand rows in L2.  Warp 0 issues the loads into six stages, warp 1 issues the MMAs (4
+// per stage, K = 16 each) and commits each stage to its stage-free barrier; warps 4-7
+// merge partials and run the epilogue.  Up to four leaves: each leaf of the CTA's range
+// accumulates in its own TMEM slot of 128 columns, the loop never waits for a reduction,
+// and the epilogue sums the slots with the tree in registers.  Eight leaves: slot
+// popcount(j) takes leaf j; when an odd leaf completes, warps 4-7 merge the finished pairs
+// of the tree in TMEM (a binary counter: at most four live partials) before the next leaf
+// starts, leaving the root in slot 0.  A leaf's instruction sequence, and so every bit of
+// its partial, is the same whichever leaf range a call covers.
 // k_pik_combine: the top of the same tree over the ranks' subtree roots (HBM-bound).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -42,11 +41,9 @@ constexpr int kBN = 128;       // tile columns (N of the MMA instruction)
 constexpr int kBK = 64;        // K elements per stage: one 128-byte swizzled row per operand row
 constexpr int kStages = 6;     // shared-memory stages
 constexpr int kThreads = 256;  // warp 0: loads, warp 1: MMAs, warps 4-7: merges and epilogue
-constexpr int kCluster = 4;    // 2 (m) x 2 (n) tiles; rank r holds m-offset r & 1, n-offset r >> 1
-constexpr int kGroupC = 4;     // cluster rows per raster group (concurrent tiles share operands in L2)
+constexpr int kGroup = 8;      // tile rows per raster group (concurrent tiles share operands in L2)
 constexpr int kSlots = 512 / kBN;  // partial sums that fit in TMEM
-constexpr uint32_t kHalf = 64 * 128;                 // 64 rows of 128 bytes: one TMA box (8 KB)
-constexpr uint32_t kOpBytes = 2 * kHalf;             // 16 KB per operand per stage
+constexpr uint32_t kOpBytes = 128 * 128;             // 128 rows of 128 bytes: one TMA box (16 KB)
 constexpr uint32_t kStage = 2 * kOpBytes;            // X then W
 constexpr size_t kBarOff = (size_t)kStages * kStage;
 constexpr size_t kSmem = kBarOff + 256 + 1024;       // barriers, TMEM slot, alignment slack
@@ -58,26 +55,14 @@ struct PikArgs {
     uint32_t* status;
 };
 
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-// One 64-element x 64-row box of a [rows, K] bf16 tensor map at (k, row0), multicast to
-// the same shared-memory offset in every CTA of `mask`, completing bytes on their mbar.
-__device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int32_t k, int32_t row0, uint64_t* mbar,
-                                         uint16_t mask)
+// One 64-element x 128-row box of a [rows, K] bf16 tensor map at (k, row0), into this
+// CTA's shared memory, completing its bytes on this CTA's mbar.
+__device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int32_t k, int32_t row0, uint64_t* mbar)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(tc::smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row0), "r"(tc::smem_u32(mbar)), "h"(mask)
+        "cp.async.bulk.tensor.2d.shared::cta.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(tc::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row0), "r"(tc::smem_u32(mbar))
         : "memory");
 }
 
@@ -94,14 +79,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
     return d;
 }
 
-// Arrive on mbar (same offset) in every CTA of `mask` once this thread's MMAs are done.
-__device__ __forceinline__ void commit_cluster(uint64_t* mbar, uint16_t mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n"
-                 ::"r"(tc::smem_u32(mbar)), "h"(mask)
-                 : "memory");
-}
-
 // The fixed tree over n (a power of two) adjacent values: pairs of neighbours first.
 template <int MAXL, int E>
 __device__ __forceinline__ void leaf_tree(float (&v)[MAXL][E], int n)
@@ -115,30 +92,25 @@ __device__ __forceinline__ void leaf_tree(float (&v)[MAXL][E], int n)
                 for (int e = 0; e < E; ++e) v[l][e] = __fadd_rn(v[l][e], v[l + wdt][e]);
 }
 
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     k_pik_leaves(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw, const PikArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // [kStages] stage landed (own + peers' bytes)
-    uint64_t* empty = full + kStages;                              // [kStages] stage read by all four CTAs
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // [kStages] stage landed
+    uint64_t* empty = full + kStages;                              // [kStages] stage read by the MMAs
     uint64_t* leaf_done = empty + kStages;                         // an odd leaf's products are done
     uint64_t* merged = leaf_done + 1;                              // its pairs are merged
     uint64_t* acc_done = merged + 1;                               // every product is done
     uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_done + 1);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const uint32_t rank = cluster_rank();
-    const int dm = rank & 1, dn = rank >> 1;
 
-    // grouped raster over clusters
+    // grouped raster over tiles: kGroup tile rows walk the tile columns together
     const int tiles_m = (a.M + kBM - 1) / kBM, tiles_n = (a.N + kBN - 1) / kBN;
-    const int cl_m = (tiles_m + 1) / 2, cl_n = (tiles_n + 1) / 2;
-    const int c = blockIdx.x / kCluster, per_group = kGroupC * cl_n;
-    const int g0 = (c / per_group) * kGroupC, gsz = min(kGroupC, cl_m - g0), r = c % per_group;
-    const int mt = 2 * (g0 + r % gsz) + dm, nt = 2 * (r / gsz) + dn;
+    const int c = blockIdx.x, per_group = kGroup * tiles_n;
+    const int g0 = (c / per_group) * kGroup, gsz = min(kGroup, tiles_m - g0), r = c % per_group;
+    const int mt = g0 + r % gsz, nt = r / gsz;
     const int32_t m0 = mt * kBM, n0 = nt * kBN;  // rows past M or N load zeros and are not stored
-    const uint16_t mask_x = (uint16_t)((1u << dm) | (1u << (dm + 2)));  // CTAs sharing these X rows
-    const uint16_t mask_w = (uint16_t)(3u << (2 * dn));                 // CTAs sharing these W rows
 
     const int nl = a.leaf_hi - a.leaf_lo;
     const bool merge = nl > kSlots;
@@ -148,7 +120,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], kCluster);
+            tc::mbar_init(&empty[s], 1);
         }
         tc::mbar_init(leaf_done, 1);
         tc::mbar_init(merged, 128);
@@ -157,7 +129,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
-    cluster_sync();  // every CTA's barriers exist before any multicast reaches them
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
 
@@ -167,7 +138,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     if (tid == 0) {
-        // producer: this CTA's half of the X rows (by n-offset) and of the W rows (by m-offset)
+        // producer: the tile's 128 X rows and 128 W rows of each 64-element K step
         for (int s = 0; s < S && ok; ++s) {
             const int b = s % kStages;
             if (s >= kStages) ok = tc::mbar_wait(&empty[b], (uint32_t)((s / kStages - 1) & 1));
@@ -175,8 +146,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             unsigned char* st = smem + (size_t)b * kStage;
             tc::mbar_arrive_expect_tx(&full[b], kStage);
             const int32_t k0 = kbase + s * kBK;
-            tma_box(st + dn * kHalf, &tx, k0, m0 + 64 * dn, &full[b], mask_x);
-            tma_box(st + kOpBytes + dm * kHalf, &tw, k0, n0 + 64 * dm, &full[b], mask_w);
+            tma_box(st, &tx, k0, m0, &full[b]);
+            tma_box(st + kOpBytes, &tw, k0, n0, &full[b]);
         }
         // every arrival meant for this CTA's stage barriers has landed before it can exit
         for (int b = 0; b < kStages && b < S; ++b) {
@@ -199,7 +170,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
                 tc::mma_bf16(d, sdesc_sw128(sx + k * 32), sdesc_sw128(sw + k * 32), idesc, (first && k == 0) ? 0u : 1u);
-            commit_cluster(&empty[b], (uint16_t)((1u << kCluster) - 1));
+            tc::commit(&empty[b]);
             if (merge && s % spl == spl - 1 && (j & 1)) {
                 tc::commit(leaf_done);
                 ok = tc::mbar_wait(merged, (uint32_t)(events & 1));
@@ -268,7 +239,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     if (failed && tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
     tc::fence_before_sync();
     __syncthreads();
-    cluster_sync();  // no CTA leaves while a peer may still write its shared memory
     if (warp == 0) tc::tmem_dealloc(tmem, cols);
 }
 
@@ -302,6 +272,20 @@ __global__ void __launch_bounds__(256) k_pik_combine(const float* parts, int64_t
 }
 
 bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+// True when p is device memory of the current device (not host, managed or a peer GPU's
+// memory): the tensor maps are only ever built over this GPU's own buffers.
+bool on_this_device(const void* p)
+{
+    int dev = -1;
+    cudaPointerAttributes at{};
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the (non-sticky) error an unknown pointer leaves
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
 bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -324,8 +308,8 @@ EncodeTiled encode_tiled()
     return fn;
 }
 
-// Tensor map of a [rows, K] bf16 matrix whose box is 64 K elements x 64 rows, landing as
-// 64 rows of 128 bytes in the 128-byte swizzle the MMA descriptors read.  Rows past the
+// Tensor map of a [rows, K] bf16 matrix whose box is 64 K elements x 128 rows, landing as
+// 128 rows of 128 bytes in the 128-byte swizzle the MMA descriptors read.  Rows past the
 // end read zeros.
 bool box_map(CUtensorMap* m, const void* base, int32_t rows, int32_t K)
 {
@@ -333,7 +317,7 @@ bool box_map(CUtensorMap* m, const void* base, int32_t rows, int32_t K)
     if (!f) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {64, 64}, es[2] = {1, 1};
+    const cuuint32_t box[2] = {64, 128}, es[2] = {1, 1};
     return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -357,6 +341,7 @@ extern "C" int32_t cpr_pik_gemm(const void* x, const void* w, float* y, int32_t 
     if ((int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN) > 0x7fffffff / 2) return CPR_ERR_INVALID_ARG;
     if (!workspace) return CPR_ERR_WORKSPACE;
     if (!al16(x) || !al16(w) || !al16(workspace) || ((uintptr_t)y & 3u)) return CPR_ERR_MISALIGNED;
+    if (!on_this_device(x) || !on_this_device(w)) return CPR_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     PikArgs a{y, M, N, K, n_leaves, leaf_lo, leaf_hi, (al16(y) && N % 4 == 0) ? 1 : 0,
               static_cast<uint32_t*>(workspace)};
@@ -365,8 +350,8 @@ extern "C" int32_t cpr_pik_gemm(const void* x, const void* w, float* y, int32_t 
     if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s) != cudaSuccess) return CPR_ERR_CUDA;
     if (cudaFuncSetAttribute(k_pik_leaves, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) != cudaSuccess)
         return CPR_ERR_CUDA;
-    const int64_t clusters = (int64_t)((M + 2 * kBM - 1) / (2 * kBM)) * ((N + 2 * kBN - 1) / (2 * kBN));
-    k_pik_leaves<<<(unsigned)(clusters * kCluster), kThreads, kSmem, s>>>(mx, mw, a);
+    const int64_t tiles = (int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    k_pik_leaves<<<(unsigned)tiles, kThreads, kSmem, s>>>(mx, mw, a);
     return cudaGetLastError() == cudaSuccess ? CPR_OK : CPR_ERR_CUDA;
 }
 

@@ -222,16 +222,18 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-// Wait until *flag >= target; gives up (returns 0) after about 4 s, or at once when another
-// CTA of the launch has recorded a timeout in the status word.
-__device__ __forceinline__ int wait_published(const uint32_t* flag, uint32_t target, const uint32_t* status)
+// Wait until *flag >= target; gives up (returns 0) after limit_ns (0: about 4 s), or at
+// once when another CTA of the launch has recorded a timeout in the status word.
+__device__ __forceinline__ int wait_published(const uint32_t* flag, uint32_t target, const uint32_t* status,
+                                              uint64_t limit_ns)
 {
     if (ld_acquire(flag) >= target) return 1;
+    const uint64_t limit = limit_ns ? limit_ns : 4000000000ull;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 0; it < (1u << 26); ++it) {
         __nanosleep(128);
         if (ld_acquire(flag) >= target) return 1;
-        if ((ld_acquire(status) & CPR_DEV_TIMEOUT) || global_ns() - t0 > 4000000000ull) break;
+        if ((ld_acquire(status) & CPR_DEV_TIMEOUT) || global_ns() - t0 > limit) break;
     }
     return 0;
 }
@@ -608,7 +610,9 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
     // published (bounded)
     __shared__ int wait_ok[8];
     const int gi = bar - 1;
-    if (tid == 0) wait_ok[gi] = wait_published(a.ready + (size_t)c * H + hd, (uint32_t)K2Cfg<DK, DV>::NSLICE, a.status);
+    if (tid == 0)
+        wait_ok[gi] = wait_published(a.ready + (size_t)c * H + hd, (uint32_t)K2Cfg<DK, DV>::NSLICE + a.wait_extra,
+                                     a.status, a.wait_limit_ns);
     named_bar(bar, NT);
     if (!wait_ok[gi]) {
         if (tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
