@@ -146,6 +146,49 @@ int32_t cpr_gdn_prefill(const void* q, const void* k, const void* v, const float
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The CPR backward: gradients of a loss L with respect to the layer's inputs, given its
+ * upstream gradients dL/do and dL/dS_T.  ("IsoExec: Eliminating Trainer-Inference
+ * Mismatch in SkyRL", section "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet",
+ * per-layer table, row "Trainer Fwd+Bwd": the pages time the trainer's backward but do
+ * not describe it; this is the exact adjoint of the token recurrence above, run back
+ * over the forward's chunk grid.)  Three steps on `stream`:
+ *   1. per chunk, independent of the states: the chunk's linear map M (S_end = S_b M + B)
+ *      and C_b = dO^T Qt, where row t of Qt is the chunk's query t carried back through
+ *      the chunk's first t token transitions;
+ *   2. per (sequence, head), from the last chunk to the first, the adjoint at every chunk
+ *      boundary: dS_b = dS_end M^T + C_b (starting from d_state_out);
+ *   3. per chunk, in parallel: the chunk's gradients from its boundary state (saved by the
+ *      forward) and the adjoint at its end, through the WY form of the chunk.
+ * All arithmetic is fp32 in a fixed order without atomics: results are reproducible and
+ * independent of how sequences are packed or ordered in the batch.
+ *   q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, H, dk, dv, C, dtype: as given to
+ *               the forward (cpr_gdn_prefill) whose gradients are wanted
+ *   boundary_states fp32 [boundary_capacity, H, dk, dv]: the forward's boundary states
+ *               (the state at the start of every chunk, as cpr_gdn_prefill wrote them)
+ *   d_out       dtype [total_tokens, H, dv]   dL/do
+ *   d_state_out fp32 [n_seqs, H, dk, dv]      dL/d(state_out), or NULL for zero
+ * Outputs (fp32, written, not accumulated):
+ *   dq, dk_out  [total_tokens, H, dk];  dv_out [total_tokens, H, dv];
+ *   dg, dbeta   [total_tokens, H]  (dg is dL/dg with g = log alpha)
+ *   d_state_in  [n_seqs, H, dk, dv]  dL/d(state_in), or NULL if not wanted
+ *   workspace   >= cpr_gdn_backward_workspace_size(...) bytes, 16-byte aligned; holds the
+ *               status word (cpr_gdn_device_status)
+ * Shapes: those cpr_gdn_backward_supported() accepts (every built (dk, dv, C) in bf16; fp32
+ * where the chunk kernels fit one CTA's shared memory).  Returns CPR_OK or a negative
+ * code as for cpr_gdn_prefill; device-side checks of cu_seqlens and boundary_capacity
+ * record CPR_DEV_* bits and skip the work.
+ */
+size_t cpr_gdn_backward_workspace_size(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk, int32_t dv,
+                                       int32_t C);
+int cpr_gdn_backward_supported(int32_t dk, int32_t dv, int32_t C, int32_t dtype);
+int32_t cpr_gdn_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                         int32_t dv, int32_t C, int32_t dtype, const float* boundary_states,
+                         int64_t boundary_capacity, const void* d_out, const float* d_state_out, float* dq,
+                         float* dk_out, float* dv_out, float* dg, float* dbeta, float* d_state_in, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * Fill a decode ring from a prefill's results so that decode continues each sequence
  * at position L_n (CPR step 3 starts where prefill stopped).  Arguments as in
  * cpr_gdn_prefill; ring buffers are sized for B = n_seqs.  For each (n, h): ring S_b =

@@ -9,6 +9,9 @@ resync every C tokens, so that prefill, training forward and decode agree bit fo
 from .binding import (  # noqa: F401
     CprError,
     Ring,
+    cpr_gdn_backward,
+    cpr_gdn_backward_supported,
+    cpr_gdn_backward_workspace_size,
     cpr_gdn_decode,
     cpr_gdn_decode_workspace_size,
     cpr_gdn_device_status,
@@ -20,6 +23,7 @@ from .binding import (  # noqa: F401
     cpr_gdn_prefill_workspace_size,
     cpr_gdn_ring_from_prefill,
     cpr_gdn_set_profile_events,
+    cpr_gdn_set_wait_test,
     cpr_gdn_strerror,
     cpr_gdn_supported,
     cpr_gdn_version,

@@ -28,6 +28,7 @@ EXPORTED = (
     "cpr_gdn_prefill_noalloc", "cpr_gdn_prefill_noalloc_status", "cpr_gdn_prefill_continue", "cpr_gdn_prefill_grouped",
     "cpr_gdn_ring_from_prefill_grouped", "cpr_gdn_decode_grouped", "cpr_gdn_prefill_continue_grouped",
     "cpr_pik_workspace_size", "cpr_pik_gemm", "cpr_pik_combine", "cpr_gdn_set_wait_test",
+    "cpr_gdn_backward_workspace_size", "cpr_gdn_backward_supported", "cpr_gdn_backward",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # CPR_GDN_NOALLOC_SCRATCH_BYTES
 
@@ -80,6 +81,10 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         "cpr_gdn_prefill_noalloc": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P, P, P, I64, P]),
         "cpr_gdn_prefill_noalloc_status": (I32, [ctypes.POINTER(ctypes.c_uint32), P]),
         "cpr_gdn_set_wait_test": (I32, [U32, ctypes.c_uint64]),
+        "cpr_gdn_backward_workspace_size": (SZ, [I64, I32, I32, I32, I32, I32]),
+        "cpr_gdn_backward_supported": (ctypes.c_int, [I32, I32, I32, I32]),
+        "cpr_gdn_backward": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, I64, P, P, P, P, P, P, P,
+                                   P, P, SZ, P]),
         "cpr_gdn_prefill_continue": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P,
                                            ctypes.POINTER(_Ring), P, P, I64, P, SZ, P]),
         "cpr_gdn_prefill_grouped": (I32, [P, P, P, P, P, P, I32, I64, I32, I32, U32, I32, I32, I32, I32, P, P, P, P,
@@ -194,6 +199,45 @@ def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, C: int, state_in=None, *, out=
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check("cpr_gdn_prefill_grouped", code)
     return out, state_out, boundary_states, workspace
+
+
+def cpr_gdn_backward_workspace_size(total_tokens: int, n_seqs: int, H: int, dk: int, dv: int, C: int) -> int:
+    return int(load_library().cpr_gdn_backward_workspace_size(total_tokens, n_seqs, H, dk, dv, C))
+
+
+def cpr_gdn_backward_supported(dk: int, dv: int, C: int, dtype=torch.bfloat16) -> bool:
+    code = CPR_DTYPE_BF16 if dtype == torch.bfloat16 else CPR_DTYPE_F32
+    return bool(load_library().cpr_gdn_backward_supported(dk, dv, C, code))
+
+
+def cpr_gdn_backward(q, k, v, g, beta, cu_seqlens, C: int, boundary_states, d_out, d_state_out=None, *,
+                     grads=None, d_state_in=True, workspace=None, stream=None):
+    """CPR backward.  Returns (dict(dq, dk, dv, dg, dbeta, d_state_in), workspace).
+
+    ``boundary_states`` are the forward's (cpr_gdn_prefill on the same batch and C);
+    ``d_out`` has the element type of q; gradients are fp32.  ``grads`` may hold
+    preallocated outputs under those names; ``d_state_in=False`` skips that output."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    gr = dict(grads or {})
+    gr.setdefault("dq", torch.empty(T, H, dk, dtype=torch.float32, device=dev))
+    gr.setdefault("dk", torch.empty(T, H, dk, dtype=torch.float32, device=dev))
+    gr.setdefault("dv", torch.empty(T, H, dv, dtype=torch.float32, device=dev))
+    gr.setdefault("dg", torch.empty(T, H, dtype=torch.float32, device=dev))
+    gr.setdefault("dbeta", torch.empty(T, H, dtype=torch.float32, device=dev))
+    if d_state_in is True:
+        gr.setdefault("d_state_in", torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev))
+    if workspace is None:
+        workspace = torch.empty(cpr_gdn_backward_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
+    code = load_library().cpr_gdn_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H, dk, dv, C, _dtype_code(q),
+        _ptr(boundary_states), boundary_states.shape[0], _ptr(d_out), _ptr(d_state_out), _ptr(gr["dq"]),
+        _ptr(gr["dk"]), _ptr(gr["dv"]), _ptr(gr["dg"]), _ptr(gr["dbeta"]), _ptr(gr.get("d_state_in")),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("cpr_gdn_backward", code)
+    return gr, workspace
 
 
 @dataclass

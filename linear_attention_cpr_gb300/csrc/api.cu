@@ -96,6 +96,89 @@ size_t cpr_gdn_prefill_workspace_size(int64_t total_tokens, int32_t n_seqs, int3
     return PrefillLayout(total_tokens, n_seqs, H, dk, dv, C).total;
 }
 
+size_t cpr_gdn_backward_workspace_size(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk, int32_t dv,
+                                       int32_t C)
+{
+    if (total_tokens < 0 || n_seqs < 0 || H <= 0 || dk <= 0 || dv <= 0 || C <= 0) return 0;
+    return BackwardLayout(total_tokens, n_seqs, H, dk, dv, C).total;
+}
+
+int cpr_gdn_backward_supported(int32_t dk, int32_t dv, int32_t C, int32_t dtype)
+{
+    if (!dtype_ok(dtype) || !shape_built(dk, dv, C)) return 0;
+    bool fits = false;
+#define CPR_FITS(DK, DV, CC)                                                                        \
+    if (dk == DK && dv == DV && C == CC)                                                             \
+        fits = (dtype == CPR_DTYPE_BF16) ? backward_fits<DK, DV, CC, __nv_bfloat16>()                \
+                                         : backward_fits<DK, DV, CC, float>();
+    CPR_FOR_EACH_SHAPE(CPR_FITS)
+#undef CPR_FITS
+    return fits ? 1 : 0;
+}
+
+int32_t cpr_gdn_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                         int32_t dv, int32_t C, int32_t dtype, const float* boundary_states,
+                         int64_t boundary_capacity, const void* d_out, const float* d_state_out, float* dq,
+                         float* dk_out, float* dv_out, float* dg, float* dbeta, float* d_state_in, void* workspace,
+                         size_t workspace_bytes, void* stream)
+{
+    if (n_seqs < 0 || total_tokens < 0 || total_tokens > 0x7fffffffLL || H <= 0 || H > 65535 || !dtype_ok(dtype) ||
+        boundary_capacity < 0)
+        return CPR_ERR_INVALID_ARG;
+    if (!shape_built(dk, dv, C) || !cpr_gdn_backward_supported(dk, dv, C, dtype)) return CPR_ERR_UNSUPPORTED_SHAPE;
+    if (n_seqs == 0) return CPR_OK;
+    if (!cu_seqlens || !workspace) return CPR_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !d_out || !boundary_states || !dq || !dk_out ||
+                             !dv_out || !dg || !dbeta))
+        return CPR_ERR_INVALID_ARG;
+    const BackwardLayout lay(total_tokens, n_seqs, H, dk, dv, C);
+    if (workspace_bytes < lay.total) return CPR_ERR_WORKSPACE;
+    const void* a16[] = {q, k, v, d_out, boundary_states, d_state_out, dq, dk_out, dv_out, d_state_in, workspace};
+    for (const void* p : a16)
+        if (p && !aligned(p, 16)) return CPR_ERR_MISALIGNED;
+    const void* a4[] = {g, beta, cu_seqlens, dg, dbeta};
+    for (const void* p : a4)
+        if (p && !aligned(p, 4)) return CPR_ERR_MISALIGNED;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    BackwardArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.cu_seqlens = cu_seqlens;
+    a.n_seqs = n_seqs;
+    a.total_tokens = total_tokens;
+    a.H = H;
+    a.boundary = boundary_states;
+    a.boundary_capacity = boundary_states ? boundary_capacity : 0;
+    a.d_out = d_out;
+    a.d_state_out = d_state_out;
+    a.dq = dq;
+    a.dk = dk_out;
+    a.dv = dv_out;
+    a.dg = dg;
+    a.dbeta = dbeta;
+    a.d_state_in = d_state_in;
+    a.status = reinterpret_cast<uint32_t*>(ws);
+    a.ready = reinterpret_cast<uint32_t*>(ws + 4);
+    a.cu_chunks = reinterpret_cast<int32_t*>(ws + lay.cu_chunks);
+    a.mt = reinterpret_cast<float*>(ws + lay.mt);
+    a.cb = reinterpret_cast<float*>(ws + lay.cb);
+    a.d_end = reinterpret_cast<float*>(ws + lay.d_end);
+    a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorInvalidValue;
+#define CPR_DISPATCH(DK, DV, CC)                                                                   \
+    if (dk == DK && dv == DV && C == CC)                                                           \
+        e = (dtype == CPR_DTYPE_BF16) ? launch_backward<DK, DV, CC, __nv_bfloat16>(a, s)            \
+                                      : launch_backward<DK, DV, CC, float>(a, s);
+    CPR_FOR_EACH_SHAPE(CPR_DISPATCH)
+#undef CPR_DISPATCH
+    return from_cuda(e);
+}
+
 size_t cpr_gdn_decode_workspace_size(int32_t B, int32_t H, int32_t dk, int32_t dv, int32_t C)
 {
     if (B < 0 || H <= 0 || dk <= 0 || dv <= 0 || C <= 0) return 0;

@@ -88,6 +88,55 @@ struct PrefillArgs {
     uint64_t wait_limit_ns;
 };
 
+// Backward workspace:
+//   [0, 256)       status word (uint32) and padding (a spare word for k0's counter slot)
+//   cu_chunks      int32 [n_seqs + 1]
+//   mt             fp32 [max_chunks, H, dk, dk]: each chunk's M^T (element (c', c) = M[c][c'])
+//   cb             fp32 [max_chunks, H, dk, dv]: each chunk's C_b = dO^T Qt, laid out like a state
+//   d_end          fp32 [max_chunks, H, dk, dv]: the adjoint of the state at each chunk's end
+struct BackwardLayout {
+    size_t cu_chunks, mt, cb, d_end, total;
+    __host__ __device__ BackwardLayout(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk, int32_t dv,
+                                       int32_t C)
+    {
+        const int64_t mc = max_chunks_bound(total_tokens, n_seqs, C);
+        cu_chunks = kAlign;
+        mt = align_up(cu_chunks + sizeof(int32_t) * (size_t)(n_seqs + 1), kAlign);
+        cb = align_up(mt + (size_t)dk * dk * 4 * (size_t)mc * H, kAlign);
+        d_end = align_up(cb + (size_t)dk * dv * 4 * (size_t)mc * H, kAlign);
+        total = align_up(d_end + (size_t)dk * dv * 4 * (size_t)mc * H, kAlign);
+    }
+};
+
+struct BackwardArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    const int32_t* cu_seqlens;
+    int32_t n_seqs;
+    int64_t total_tokens;
+    int32_t H;
+    const float* boundary;     // the forward's boundary states [n_chunks, H, dk, dv]
+    int64_t boundary_capacity;
+    const void* d_out;         // [T, H, dv], the element type of q, k, v
+    const float* d_state_out;  // [N, H, dk, dv] or NULL (zero)
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dg;
+    float* dbeta;
+    float* d_state_in;         // [N, H, dk, dv] or NULL (not wanted)
+    uint32_t* status;
+    uint32_t* ready;           // k0's counter slot (a spare word of the status block)
+    int32_t* cu_chunks;
+    float* mt;
+    float* cb;
+    float* d_end;
+    int64_t max_chunks;
+};
+
 // Decode workspace: [0, 256) status word.
 inline size_t decode_workspace_bytes(int32_t) { return kAlign; }
 
@@ -179,5 +228,9 @@ cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, f
                                     cudaStream_t s);
 template <int DK, int DV, int C, typename T> cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 template <int DK, int DV, int C, typename T> cudaError_t launch_ring_from_prefill(const RingArgs& a, cudaStream_t s);
+// The CPR backward (k0, then the chunk maps, the reverse chain and the chunk gradients).
+template <int DK, int DV, int C, typename T> cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
+// Whether the backward's chunk kernels fit one CTA's shared memory for this shape and type.
+template <int DK, int DV, int C, typename T> bool backward_fits();
 
 }  // namespace cpr
