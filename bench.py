@@ -13,6 +13,7 @@ roofline:
   - varlen_stress: 32 packed sequences of log-uniform lengths (H=32), prefill and then
     128 decode steps;
   - tiny: the fp32 case's prefill and decode-step latency;
+  - train_fwd_bwd: the trainer's forward and backward (cpr_gdn_backward) at 1 x 10,240;
   - pik: the deterministic K-split product (one GPU only);
   - fp32_peak_probe: the FP32-pipe peak measured on this GPU by the committed probe;
 plus the end-to-end number through the C ABI with host buffers, and the fp64 CPU oracle
@@ -361,6 +362,121 @@ def inputs_decode(w, s, dev):
     return inputs.decode_inputs(w, s, device=dev)
 
 
+def backward_algorithmic(n_chunks, H, dk, dv, C):
+    """FP32 flops of one backward as the three kernels evaluate it, per (chunk, head) with
+    n = C tokens (multiply-adds x 2):
+      chunk maps: K K^T, Q K^T, W, Qt (4 n^2 d), M^T and C_b (2 n d^2), T (n^3 / 6);
+      reverse chain: dS M^T (dk^2 dv);
+      chunk gradients: 10 products of n^2 d (K K^T, Q K^T, U, dPm, Pm^T dO, dQK K, dQK^T Q,
+      dT, T^T dU, (dKK + dKK^T) K), 5 of n d^2 (K S_b^T, dO S_b, diag(d) K dS^T, U dS,
+      T^T dU S_b), 2 of n^3 (T^T dT, X T^T) and T (n^3 / 6)."""
+    d = dk
+    maps = 4 * C * C * d + 2 * C * d * d + C ** 3 // 6
+    chain = dk * dk * dv
+    grads = 10 * C * C * d + 5 * C * d * d + 2 * C ** 3 + C ** 3 // 6
+    return {"chunk_maps": 2 * maps * n_chunks * H, "reverse_chain": 2 * chain * n_chunks * H,
+            "chunk_grads": 2 * grads * n_chunks * H}
+
+
+def run_train_fwd_bwd(args, cpr, inputs, dev, dist, world, flush, p32_meas):
+    """Trainer forward + backward at 1 x 10,240 tokens (H=16, d=128, C=64): cpr_gdn_prefill
+    then cpr_gdn_backward on the same batch (the forward's boundary states are the saved
+    states), upstream gradients dL/do seeded, L2 flushed between steps."""
+    w = inputs.workload("trainer_fwd")
+    xc = inputs.prefill_inputs(w)
+    x = {k: v.to(dev) for k, v in xc.items()}
+    T, H, dk, dv, C, N = w.total_tokens, w.H, w.dk, w.dv, w.C, len(w.seqlens)
+    n_chunks = cpr.cpr_gdn_num_chunks(xc["cu_seqlens"], C)
+    gen = torch.Generator().manual_seed(7)
+    d_out = torch.randn(T, H, dv, generator=gen).to(w.dtype).to(dev)
+    out = torch.empty(T, H, dv, dtype=w.dtype, device=dev)
+    st = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    bnd = torch.empty(n_chunks, H, dk, dv, dtype=torch.float32, device=dev)
+    ws = torch.empty(cpr.cpr_gdn_prefill_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
+    bws = torch.empty(cpr.cpr_gdn_backward_workspace_size(T, N, H, dk, dv, C), dtype=torch.uint8, device=dev)
+    grads = {"dq": torch.empty(T, H, dk, device=dev), "dk": torch.empty(T, H, dk, device=dev),
+             "dv": torch.empty(T, H, dv, device=dev), "dg": torch.empty(T, H, device=dev),
+             "dbeta": torch.empty(T, H, device=dev), "d_state_in": torch.empty(N, H, dk, dv, device=dev)}
+
+    def fwd():
+        cpr.cpr_gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], C, out=out, state_out=st,
+                            boundary_states=bnd, workspace=ws)
+
+    def bwd():
+        cpr.cpr_gdn_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], C, bnd, d_out,
+                             grads=grads, workspace=bws)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    assert cpr.cpr_gdn_device_status(ws) == 0 and cpr.cpr_gdn_device_status(bws) == 0
+    steps = max(3, min(args.steps, 30))
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    total, fwd_ms, kern = [], [], {"chunk_maps": [], "reverse_chain": [], "chunk_grads": []}
+    _barrier(dist)
+    for _ in range(steps):
+        flush.zero_()
+        e[0].record()
+        fwd()
+        e[1].record()
+        cpr.cpr_gdn_set_profile_events(ev)
+        bwd()
+        cpr.cpr_gdn_set_profile_events(None)
+        ev[4].synchronize()
+        total.append(e[0].elapsed_time(ev[4]))
+        fwd_ms.append(e[0].elapsed_time(e[1]))
+        for i, name in enumerate(kern):
+            kern[name].append(ev[i + 1].elapsed_time(ev[i + 2]))
+    _barrier(dist)
+    ms = _max_over_ranks(dist, statistics.fmean(total))
+    kern_ms = {k: statistics.fmean(v) for k, v in kern.items()}
+    flops = backward_algorithmic(n_chunks, H, dk, dv, C)
+    _, f_fwd = prefill_algorithmic(T, N, H, dk, dv, n_chunks)
+    ach = flops["chunk_grads"] / (kern_ms["chunk_grads"] / 1e3) / 1e12
+    roof = {"kernel": "kb3_chunk_grads", "bound": "alu", "achieved": ach, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+            "frac": ach / FP32_PEAK_TFLOPS, "traffic": None, "flops_per_launch": flops["chunk_grads"],
+            "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"}
+    if p32_meas:
+        roof["peak_measured"] = p32_meas["tflops"]
+        roof["frac_of_measured"] = ach / p32_meas["tflops"]
+    t_roof = (f_fwd + sum(flops.values())) / (FP32_PEAK_TFLOPS * 1e12) * 1e3
+    line = {"metric": "trainer forward + backward tokens/s per layer", "value": weak_scaling_rate(world, T, ms),
+            "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "workload": f"trainer_fwd + backward: 1 x {T} tokens, H={H}, dk=dv={dk}, C={C}, bf16 q/k/v/dO, "
+                        "fp32 gradients",
+            "forward_ms": statistics.fmean(fwd_ms), "backward_kernels_ms": kern_ms,
+            "backward_flops": flops, "t_roof_ms": t_roof, "frac_of_t_roof": t_roof / ms, "roofline": roof,
+            "gpu_launches": 7 * steps}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = backward_cpu_baseline(xc, d_out.cpu(), C)
+    return line
+
+
+def backward_cpu_baseline(xc, d_out, C, heads=2):
+    """The oracle's forward (C, host threads) and WY-chunked adjoint (fp64, numpy) on the
+    first `heads` heads of the trainer sequence; tokens/s of forward + backward scaled to
+    all heads."""
+    import numpy as np
+
+    import oracle
+    from oracle import backward
+
+    H = xc["q"].shape[1]
+    sub = {k: np.ascontiguousarray(xc[k][:, :heads].double().numpy()) for k in ("q", "k", "v", "g", "beta")}
+    cu = xc["cu_seqlens"].numpy()
+    t0 = time.perf_counter()
+    oracle.recurrent(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], cu, C, boundaries=True)
+    backward.wy_chunked_backward(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], cu,
+                                 d_out[:, :heads].double().numpy(), C)
+    sec = time.perf_counter() - t0
+    T = int(cu[-1])
+    return {"value": T * heads / H / sec, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"forward + backward of heads 0..{heads - 1} of the {T}-token sequence ({sec:.1f} s), "
+                      f"scaled to {H} heads"}
+
+
 def run_extra_workloads(args, cpr, inputs, dev, dist, world, flush, p32_meas, hbm_peak):
     """The other configurations of the layer, each with its own line: the one-shot rollout
     prefill (5 x 2,048 packed), the varlen stress batch (prefill, then 128 decode steps) and
@@ -529,6 +645,7 @@ def run_ours(args):
         roofline["frac_of_measured"] = roofline["achieved"] / p32_meas["tflops"]
     extra = None if args.no_extra else run_extra_workloads(args, cpr, inputs, dev, dist, world, flush, p32_meas,
                                                            hbm_peak)
+    train = None if args.no_extra else run_train_fwd_bwd(args, cpr, inputs, dev, dist, world, flush, p32_meas)
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only) ----------------
     cpu = None
@@ -553,7 +670,8 @@ def run_ours(args):
                             (continuation["gpu_launches"] if continuation else 0) +
                             (pik_line["gpu_launches"] if pik_line else 0) +
                             (sum(v["gpu_launches"] + (v.get("decode") or {}).get("gpu_launches", 0)
-                                 for v in extra.values()) if extra else 0),
+                                 for v in extra.values()) if extra else 0) +
+                            (train["gpu_launches"] if train else 0),
             "clocks": clocks.summary(),
             "decode": decode,
             "continuation": continuation,
@@ -561,6 +679,7 @@ def run_ours(args):
             "rollout_prefill": extra["rollout_prefill"] if extra else None,
             "varlen_stress": extra["varlen_stress"] if extra else None,
             "tiny": extra["tiny"] if extra else None,
+            "train_fwd_bwd": train,
             "fp32_peak_probe": p32_meas,
             "cpu_baseline": cpu,
         }

@@ -454,6 +454,19 @@ __device__ __forceinline__ void chain_values_reg(uint32_t tmem_col, int t, const
     for (int e = 0; e < Mp::CPT; ++e) v[e] = __fadd_rn(v[e], b[e]);
 }
 
+// S_new = D + B for this thread's values, B read from a [DK][DV] fp32 image in shared
+// memory (element (c, i) of B at c * DV + i; rows beyond DV add zero and are never stored).
+template <int DK, int DV, int NW>
+__device__ __forceinline__ void chain_values_smem(uint32_t tmem_col, int t, const float* sb,
+                                                  float (&v)[ChainMap<DK, NW>::CPT])
+{
+    using Mp = ChainMap<DK, NW>;
+    chain_acc<DK, NW>(tmem_col, t, v);
+    const int i = Mp::row(t), c0 = Mp::col0(t);
+#pragma unroll
+    for (int e = 0; e < Mp::CPT; ++e) v[e] = __fadd_rn(v[e], i < DV ? sb[(c0 + e) * DV + i] : 0.0f);
+}
+
 // This thread's values of a stored [DK][DV] fp32 state; zeros beyond DV or for a NULL
 // source.
 template <int DK, int DV, int NW>

@@ -240,11 +240,14 @@ __device__ __forceinline__ int wait_published(const uint32_t* flag, uint32_t tar
 
 // ------------------------------------------------------------------------------------
 // Boundary chain of one (sequence, head), by a CTA of 8 warps.  Each step, the epilogue
-// warps read the accumulator (value row i in TMEM lane i), add B (loaded from global
-// memory into registers one chunk ahead), write the bf16-split state tile back into TMEM
-// and arrive on an mbarrier; lane 0 of warp 7 is also the producer: it bulk-copies each
-// chunk's M^T image into one of three shared-memory stages two chunks ahead and issues the
-// tcgen05 chain product (M = 128) once every epilogue thread has arrived.  The boundary
+// warps read the accumulator (value row i in TMEM lane i), add B (from shared memory),
+// write the bf16-split state tile back into TMEM and arrive on an mbarrier; lane 0 of
+// warp 7 is also the producer: it bulk-copies each chunk's M^T image into one of two
+// shared-memory stages one chunk ahead, issues the tcgen05 chain product (M = 128) once
+// every epilogue thread has arrived; as soon as every thread has read a chunk's B (an
+// mbarrier of its own, before the tile is written), it bulk-copies the next chunk's B
+// into the B buffer, ahead of the next M^T copy; both images are prefetched into L2 a few
+// chunks ahead of their copies.  The boundary
 // state is stored while the next product runs and published for the intra-chunk items one
 // step later by a thread that neither polls nor produces.  All waits are bounded; a
 // timeout is reported in the status word.  A chain CTA runs its chains one after another;
@@ -255,16 +258,23 @@ struct K2Cfg {
     static_assert(DV <= kChainRows, "one chain product covers every value row");
     static constexpr int NSLICE = 1;  // publications per boundary state
     static constexpr uint32_t MT_BYTES = 2 * DK * DK * 2;
-    static constexpr int NSTAGE = 3;  // M^T images in flight: the one in use and two ahead
+    static constexpr int NSTAGE = 2;  // M^T images in flight: the one in use and one ahead
     static constexpr uint32_t STAGE = MT_BYTES;
-    static constexpr uint32_t BAR_OFF = NSTAGE * STAGE;
-    static constexpr uint32_t bytes = BAR_OFF + 64;
+    static constexpr uint32_t BT_BYTES = DK * DV * 4;  // one chunk's B (fp32, laid out like a state)
+    static constexpr uint32_t B_OFF = NSTAGE * STAGE;
+    static constexpr uint32_t BAR_OFF = B_OFF + BT_BYTES;
+    static constexpr uint32_t bytes = BAR_OFF + 128;
     // TMEM: the accumulator in columns [0, DK), the state tile (A operand) in [DK, 2 DK)
     static constexpr uint32_t TMEM_COLS = 2 * DK <= 64 ? 64 : 2 * DK <= 128 ? 128 : 256;
     static constexpr uint32_t PIECE = 16384;
     static constexpr int THREADS = 256;
     static constexpr int NW = THREADS / 32;  // epilogue warps (all)
 };
+
+// How many chain steps ahead the producer prefetches a chunk's M^T and B images into L2
+// (k1 wrote them long before, so they come from HBM; the shared-memory copies one step
+// ahead then hit in L2).
+constexpr int kPrefetchAhead = 3;
 
 // Publish a boundary state: the CTA's stores to it were issued before a barrier this
 // thread has passed; the release orders them before the count.
@@ -281,7 +291,10 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
     uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(sm2 + Cf::BAR_OFF);  // [NSTAGE] stage landed
     uint64_t* mbar_mma = mbar_ld + Cf::NSTAGE;                           // product done
     uint64_t* mbar_tile = mbar_mma + 1;                                  // state tile ready (all threads)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_tile + 1);
+    uint64_t* mbar_b = mbar_tile + 1;                                    // the chunk's B landed
+    uint64_t* mbar_bread = mbar_b + 1;                                   // every thread read the chunk's B
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_bread + 1);
+    const float* sb = reinterpret_cast<const float*>(sm2 + Cf::B_OFF);  // [DK][DV]
     volatile int* mma_ok = reinterpret_cast<volatile int*>(tslot + 1);  // [2] thread 0's wait results, by step parity
 
     const int H = a.H, tid = threadIdx.x, warp = tid >> 5;
@@ -293,6 +306,8 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
         for (int b = 0; b < Cf::NSTAGE; ++b) tc::mbar_init(&mbar_ld[b], 1);
         tc::mbar_init(mbar_mma, 1);
         tc::mbar_init(mbar_tile, Cf::THREADS);
+        tc::mbar_init(mbar_b, 1);
+        tc::mbar_init(mbar_bread, Cf::THREADS);
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -300,7 +315,8 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
 
-    int64_t G = 0;  // chain steps this CTA has run: the phase count of its mbarriers
+    int64_t G = 0;   // chain steps this CTA has run: the phase count of its mbarriers
+    int64_t RB = 0;  // completed phases of mbar_bread (one per step that has a successor)
     bool failed = false;
     const int nchains = a.n_seqs * H;
     for (int ci = cta; ci < nchains && !failed; ci += ncta) {
@@ -336,16 +352,32 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
                 tc::bulk_g2s(dst + off, src + off, min(Cf::PIECE, Cf::MT_BYTES - off), &mbar_ld[b]);
         };
         auto ld_parity = [&](int64_t jc) { return (uint32_t)(((G + jc) / Cf::NSTAGE) & 1); };
+        int64_t b_issued = 0;
+        auto issue_b = [&](int64_t jc) {  // chunk jc's B into the B buffer (every thread read the last one)
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(a.bt + ((size_t)(cbase + jc) * H + h) * SS);
+            unsigned char* dst = sm2 + Cf::B_OFF;
+            tc::mbar_arrive_expect_tx(mbar_b, Cf::BT_BYTES);
+            for (uint32_t off = 0; off < Cf::BT_BYTES; off += Cf::PIECE)
+                tc::bulk_g2s(dst + off, src + off, min(Cf::PIECE, Cf::BT_BYTES - off), mbar_b);
+            ++b_issued;
+        };
+        // both images of chunk jc into L2 a few steps before their shared-memory copies
+        auto prefetch = [&](int64_t jc) {
+            if (jc >= nfull) return;
+            const size_t ch = (size_t)(cbase + jc) * H + h;
+            tc::prefetch_l2(a.mt + ch * Cf::MT_BYTES, Cf::MT_BYTES);
+            tc::prefetch_l2(a.bt + ch * SS, Cf::BT_BYTES);
+        };
         auto produce = [&](int64_t jc) -> bool {  // step jc's product, once its state tile is written
             if (!tc::mbar_wait(mbar_tile, (uint32_t)((G + jc) & 1))) return false;
             if (!tc::mbar_wait(&mbar_ld[(G + jc) % Cf::NSTAGE], ld_parity(jc))) return false;
             chain_mma<DK>(tmem, tmem + DK, sm2 + ((G + jc) % Cf::NSTAGE) * Cf::STAGE, mbar_mma);
             if (issued < nfull) issue_load(issued++);  // product jc-1 is done: its stage is free
+            prefetch(jc + kPrefetchAhead);
             return true;
         };
 
         bool pfail = false;
-        float bv[Mp::CPT];
         {
             float v0[Mp::CPT];
             chain_load_state<DK, DV, Cf::NW>(s_in, tid, v0);
@@ -353,10 +385,11 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
             chain_put_a<DK, Cf::NW>(tmem + DK, tid, v0);
             tc::fence_before_sync();
             tc::mbar_arrive(mbar_tile);
-            chain_load_b<DK, DV, Cf::NW>(a.bt + ((size_t)cbase * H + h) * SS, tid, bv);
         }
         if (producer) {
+            for (int64_t jc = 1; jc < kPrefetchAhead; ++jc) prefetch(jc);
             for (; issued < Cf::NSTAGE - 1 && issued < nfull; ++issued) issue_load(issued);
+            issue_b(0);
             pfail = !produce(0);
         }
         __syncwarp();
@@ -367,14 +400,29 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
         for (int64_t jc = 0; jc < nfull; ++jc) {
             // one thread polls the product's mbarrier, the others meet it at a hardware
             // barrier (polling by every warp would compete with the product for shared memory)
-            if (tid == 0) mma_ok[jc & 1] = tc::mbar_wait(mbar_mma, (uint32_t)((G + jc) & 1)) ? 1 : 0;
+            if (tid == 0)
+                mma_ok[jc & 1] = (tc::mbar_wait(mbar_mma, (uint32_t)((G + jc) & 1)) &&
+                                  tc::mbar_wait(mbar_b, (uint32_t)((G + jc) & 1))) ? 1 : 0;
             __syncthreads();
             ok = mma_ok[jc & 1] != 0;
             if (!ok) break;
             tc::fence_after_sync();
             float v[Mp::CPT];
-            chain_values_reg<DK, Cf::NW>(tmem, tid, bv, v);
-            if (jc + 1 < nfull) chain_put_a<DK, Cf::NW>(tmem + DK, tid, v);
+            chain_values_smem<DK, DV, Cf::NW>(tmem, tid, sb, v);
+            if (jc + 1 < nfull) {
+                tc::mbar_arrive(mbar_bread);
+                if (warp == Cf::NW - 1) {  // the producer's warp stays converged around its wait
+                    __syncwarp();
+                    // chunk jc+1's B into the buffer as soon as every thread has read chunk jc's
+                    if (producer && !pfail) {
+                        pfail = !tc::mbar_wait(mbar_bread, (uint32_t)(RB & 1));
+                        if (!pfail) issue_b(jc + 1);
+                    }
+                    __syncwarp();
+                }
+                ++RB;
+                chain_put_a<DK, Cf::NW>(tmem + DK, tid, v);
+            }
             tc::fence_before_sync();
             if (jc + 1 < nfull) tc::mbar_arrive(mbar_tile);
             // the boundary state completed one step ago: every store to it was issued before
@@ -384,7 +432,6 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
                 // the producer issues the next product before its own loads and stores
                 if (producer) pfail = !produce(jc + 1);
                 __syncwarp();
-                chain_load_b<DK, DV, Cf::NW>(a.bt + ((size_t)(cbase + jc + 1) * H + h) * SS, tid, bv);
             }
             float* dst = (jc + 1 < nch) ? a.boundary + ((size_t)(cbase + jc + 1) * H + h) * SS
                                         : a.state_out + nh * SS;
@@ -396,6 +443,7 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
         if (failed && producer) {  // let copies still in flight land before the CTA exits
             for (int64_t jc = 0; jc < issued; ++jc)
                 tc::mbar_wait(&mbar_ld[(G + jc) % Cf::NSTAGE], ld_parity(jc), 1u << 16);
+            if (b_issued > 0) tc::mbar_wait(mbar_b, (uint32_t)((G + b_issued - 1) & 1), 1u << 16);
         }
         G += nfull;
     }
@@ -405,6 +453,8 @@ __device__ __forceinline__ void chain_role(const PrefillArgs& a, unsigned char* 
         for (int b = 0; b < Cf::NSTAGE; ++b) tc::mbar_inval(&mbar_ld[b]);
         tc::mbar_inval(mbar_mma);
         tc::mbar_inval(mbar_tile);
+        tc::mbar_inval(mbar_b);
+        tc::mbar_inval(mbar_bread);
     }
     tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(tmem, Cf::TMEM_COLS);

@@ -116,6 +116,13 @@ __device__ __forceinline__ void bulk_g2s(void* smem, const void* gmem, uint32_t 
         : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16, address 16-byte aligned) of global memory into L2
+// (no completion to wait for: a hint that a later copy of the same bytes hits in L2).
+__device__ __forceinline__ void prefetch_l2(const void* gmem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
 // Bulk copy shared -> global (both 16-byte aligned, bytes a multiple of 16), tracked by
 // this thread's bulk group: commit with bulk_commit, wait with bulk_wait_read.
 __device__ __forceinline__ void bulk_s2g(void* gmem, const void* smem, uint32_t bytes)

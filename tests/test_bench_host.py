@@ -35,3 +35,15 @@ def test_decode_counts_rollout_decode():
     # state written 2 x 65,536 per head
     one = b.decode_algorithmic(B, H, d, d, C, 1) - b.decode_algorithmic(B, H, d, d, C, 0)
     assert one == H * (64 * 520 + 3 * 65_536)
+
+
+def test_backward_counts_trainer_fwd():
+    b = _bench()
+    H, d, C, nc = 16, 128, 64, 160
+    f = b.backward_algorithmic(nc, H, d, d, C)
+    # chunk maps: 4 x (64 x 64 x 128) + 2 x (64 x 128 x 128) + 64^3 / 6 multiply-adds
+    assert f["chunk_maps"] == 2 * (4 * 524_288 + 2 * 1_048_576 + 43_690) * nc * H
+    # chain: one 128 x 128 by 128 x 128 product per chunk and head
+    assert f["reverse_chain"] == 2 * 2_097_152 * nc * H
+    # chunk gradients: 10 x 524,288 + 5 x 1,048,576 + 2 x 262,144 + 43,690
+    assert f["chunk_grads"] == 2 * (5_242_880 + 5_242_880 + 524_288 + 43_690) * nc * H
