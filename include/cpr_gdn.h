@@ -245,7 +245,10 @@ int32_t cpr_gdn_decode(const void* q, const void* k, const void* v, const float*
  *   state  fp32 [n_seqs, H, dk, dv] in/out;  ring in/out (B = n_seqs)
  * workspace >= cpr_gdn_prefill_workspace_size(total_tokens, n_seqs, H, dk, dv, C).  A
  * negative pos0[n] records CPR_DEV_BAD_POS in the workspace's status word and the call
- * then leaves every output as it was.
+ * then leaves every output as it was.  The first tokens' steps and resync run on the
+ * library's side stream (the one decode uses) while the remainder's chunk preparation
+ * runs on `stream`; the call joins them again, so work issued on `stream` after it sees
+ * every result.  Calls on one device take turns on that side stream.
  */
 int32_t cpr_gdn_prefill_continue(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                  const int32_t* cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t H,

@@ -336,7 +336,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb1_chunk_maps(BackwardArgs a)
 // independent: dS_b[i][:] = dS_end[i][:] M^T + C_b[i][:]).  For j = last .. 0 it stores
 // dS (the adjoint at chunk j's end) into d_end[j], then steps it to chunk j's start.  The
 // start value is d_state_out (zero if absent); the end value is d_state_in.  Chunk j-1's
-// M^T streams into shared memory (16-byte asynchronous copies) while step j runs.
+// M^T and the slice's rows of C_{j-1} stream into shared memory (16-byte asynchronous
+// copies) while step j runs.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV>
 struct Kb2Cfg {
@@ -346,7 +347,8 @@ struct Kb2Cfg {
     static_assert(RPT >= 1 && RS * NCG == RPT * kBwdThreads, "slice covers the thread grid");
     static constexpr int SS = DK + 4;                  // slice row stride (16-byte rows)
     static constexpr size_t MT_BYTES = (size_t)DK * DK * 4;
-    static constexpr size_t bytes = 2 * MT_BYTES + 2 * (size_t)RS * SS * 4;
+    static constexpr size_t CB_BYTES = (size_t)DK * RS * 4;  // the slice's columns of one C_b
+    static constexpr size_t bytes = 2 * MT_BYTES + 2 * CB_BYTES + 2 * (size_t)RS * SS * 4;
 };
 
 template <int DK, int DV>
@@ -356,7 +358,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb2_reverse_chain(BackwardArgs
     constexpr int RS = F::RS, SS = F::SS, RPT = F::RPT;
     extern __shared__ __align__(16) unsigned char smc[];
     float* mts = reinterpret_cast<float*>(smc);                          // [2][DK][DK]
-    float* sl = reinterpret_cast<float*>(smc + 2 * F::MT_BYTES);         // [2][RS][SS]
+    float* cbs = reinterpret_cast<float*>(smc + 2 * F::MT_BYTES);        // [2][DK][RS]
+    float* sl = reinterpret_cast<float*>(smc + 2 * F::MT_BYTES + 2 * F::CB_BYTES);  // [2][RS][SS]
     constexpr int NSL = DV / RS;
     const int unit = blockIdx.x, slice = unit % NSL, nh = unit / NSL;
     const int n = nh / a.H, h = nh % a.H, t = threadIdx.x;
@@ -375,13 +378,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb2_reverse_chain(BackwardArgs
         float4* dst = reinterpret_cast<float4*>(mts + (size_t)buf * DK * DK);
         for (int q = t; q < DK * DK / 4; q += kBwdThreads) tc::cp_async16(dst + q, src + q);
     };
-    if (nch > 0) fetch_mt(nch - 1, (int)((nch - 1) & 1));
+    auto fetch_cb = [&](int64_t j, int buf) {  // rows c of C_b, columns [i0, i0 + RS)
+        const float* src = a.cb + ((size_t)(cb + j) * a.H + h) * SSZ + i0;
+        float* dst = cbs + (size_t)buf * DK * RS;
+        constexpr int Q = RS / 4;  // 16-byte pieces per row
+        for (int q = t; q < DK * Q; q += kBwdThreads)
+            tc::cp_async16(dst + (q / Q) * RS + (q % Q) * 4, src + (size_t)(q / Q) * DV + (q % Q) * 4);
+    };
+    if (nch > 0) {
+        fetch_mt(nch - 1, (int)((nch - 1) & 1));
+        fetch_cb(nch - 1, (int)((nch - 1) & 1));
+    }
     const int c0 = (t % F::NCG) * 4, r0 = (t / F::NCG) * RPT;
     int cur = 0;
     for (int64_t j = nch - 1; j >= 0; --j) {
         tc::cp_async_wait_all();
         __syncthreads();  // M^T of chunk j and the slice are in shared memory
-        if (j > 0) fetch_mt(j - 1, (int)((j - 1) & 1));
+        if (j > 0) {
+            fetch_mt(j - 1, (int)((j - 1) & 1));
+            fetch_cb(j - 1, (int)((j - 1) & 1));
+        }
         const float* mt = mts + (size_t)(j & 1) * DK * DK;
         const float* s = sl + cur * RS * SS;
         float* dend = a.d_end + ((size_t)(cb + j) * a.H + h) * SSZ;
@@ -389,7 +405,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb2_reverse_chain(BackwardArgs
             const int cc = idx / RS, ii = idx % RS;
             dend[(size_t)cc * DV + i0 + ii] = s[ii * SS + cc];
         }
-        const float* cbj = a.cb + ((size_t)(cb + j) * a.H + h) * SSZ;
+        const float* cbj = cbs + (size_t)(j & 1) * DK * RS;  // [c][ii]
         float acc[RPT][4];
 #pragma unroll
         for (int r = 0; r < RPT; ++r)
@@ -412,7 +428,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb2_reverse_chain(BackwardArgs
         for (int r = 0; r < RPT; ++r)
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                o[(r0 + r) * SS + c0 + e] = __fadd_rn(acc[r][e], cbj[(size_t)(c0 + e) * DV + i0 + r0 + r]);
+                o[(r0 + r) * SS + c0 + e] = __fadd_rn(acc[r][e], cbj[(c0 + e) * RS + r0 + r]);
         cur ^= 1;
     }
     __syncthreads();

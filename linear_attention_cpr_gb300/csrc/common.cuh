@@ -220,6 +220,9 @@ constexpr size_t tmem_cap_smem(uint32_t tmem_cols)
 cudaError_t launch_chunk_index(const PrefillArgs& a, int32_t C, const int32_t* pos0, int32_t* skip,
                                int32_t* pos_last, cudaStream_t s);
 template <int DK, int DV, int C, typename T> cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+// The two halves of a prefill after its chunk index: k1 (state independent) and k23.
+template <int DK, int DV, int C, typename T> cudaError_t launch_chunk_prep(const PrefillArgs& a, cudaStream_t s);
+template <int DK, int DV, int C, typename T> cudaError_t launch_chain_and_intra(const PrefillArgs& a, cudaStream_t s);
 // Continuation (pos0: absolute position of each sequence's first token): the chunk index
 // with the fill lengths, the fill of each sequence's current chunk and its resync, then
 // the prefill of the rest and the ring.

@@ -619,10 +619,11 @@ cudaError_t launch_ring_from_prefill(const RingArgs& a, cudaStream_t s)
 }
 
 // ------------------------------------------------------------------------------------
-// Continuation prefill: the chunk index (which also takes each sequence's fill tokens),
-// the fill (k8) and the resync of the chunks it completes (k5, resync only, after k8 on the
-// same stream), the prefill of the remaining tokens from the resulting states in place,
-// and the ring for the final partial chunks.
+// Continuation prefill: the chunk index (which also takes each sequence's fill tokens);
+// then, on the library's side stream, the fill (k8) and the resync of the chunks it
+// completes (k5, resync only, after k8), while the remainder's chunk prep (k1) runs on the
+// caller's stream; once both are done, k23 runs the remaining tokens from the resulting
+// states in place, and k6 fills the ring for the final partial chunks.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C, typename T>
 cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, float* state,
@@ -649,19 +650,29 @@ cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, f
     d.status = a.status;
     d.num_sms = a.num_sms;
     d.resync_only = 1;
-    k8_chunk_fill<DK, DV, C, T><<<dim3((unsigned)a.n_seqs, a.H), 256, 0, s>>>(d, a.cu_seqlens, pos0, skip);
+    // the fill and its resync (which update the states) run on the side stream while the
+    // remainder's chunk prep (which reads only the inputs) runs on s; k23 waits for both
+    SideStream* ss = nullptr;
+    if ((e = side_stream(ss)) != cudaSuccess) return e;
+    std::lock_guard<std::mutex> turn(ss->use);
+    if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss->stream, ss->fork, 0)) != cudaSuccess) return e;
+    k8_chunk_fill<DK, DV, C, T><<<dim3((unsigned)a.n_seqs, a.H), 256, 0, ss->stream>>>(d, a.cu_seqlens, pos0, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::rs_bytes(sizeof(T)), tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
     auto k5 = d.qk_norm ? k5_resync<DK, DV, C, T, true> : k5_resync<DK, DV, C, T, false>;
     e = cudaFuncSetAttribute(k5, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm5);
     if (e != cudaSuccess) return e;
     const int grid = std::max(1, std::min(a.n_seqs * a.H, a.num_sms * (int)(232448 / sm5)));
-    k5<<<grid, DK + DV, sm5, s>>>(d);
+    k5<<<grid, DK + DV, sm5, ss->stream>>>(d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     PrefillArgs p = a;
     p.state_in = state;
     p.state_out = state;
-    if ((e = launch_prefill<DK, DV, C, T>(p, s)) != cudaSuccess) return e;
+    if ((e = launch_chunk_prep<DK, DV, C, T>(p, s)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ss->join, ss->stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, ss->join, 0)) != cudaSuccess) return e;
+    if ((e = launch_chain_and_intra<DK, DV, C, T>(p, s)) != cudaSuccess) return e;
     RingArgs ra;
     ra.k = a.k;
     ra.v = a.v;

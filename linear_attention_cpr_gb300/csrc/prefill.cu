@@ -779,7 +779,17 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     profile_mark(1, s);
+    if ((e = launch_chunk_prep<DK, DV, C, T>(a, s)) != cudaSuccess) return e;
+    profile_mark(2, s);
+    e = launch_chain_and_intra<DK, DV, C, T>(a, s);
+    profile_mark(3, s);
+    return e;
+}
 
+template <int DK, int DV, int C, typename T>
+cudaError_t launch_chunk_prep(const PrefillArgs& a, cudaStream_t s)
+{
+    cudaError_t e;
     // dynamic shared memory also caps the CTAs per SM so their TMEM columns fit in 512
     const size_t sm1 = std::max<size_t>(UCfg<DK, DV, C>::PREP_SMEM, tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
     // separate builds for grouped heads and for normalised keys: the usual one is untouched
@@ -788,10 +798,13 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
     e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
     if (e != cudaSuccess) return e;
     k1<<<dim3((unsigned)a.max_chunks, a.Hk, a.H / a.Hk), DK + DV, sm1, s>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    profile_mark(2, s);
+    return cudaGetLastError();
+}
 
+template <int DK, int DV, int C, typename T>
+cudaError_t launch_chain_and_intra(const PrefillArgs& a, cudaStream_t s)
+{
+    cudaError_t e;
     using Cf = K2Cfg<DK, DV>;
     auto kern = k23_chain_and_intra<DK, DV, C, T>;
     const size_t sm23 = std::max<size_t>(K23Cfg<DK, DV, C>::bytes, tmem_cap_smem(Cf::TMEM_COLS));
@@ -807,14 +820,17 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s)
     PrefillArgs args = a;
     int nc = n_chain;
     void* params[] = {&args, &nc};
-    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cf::THREADS), params, sm23, s);
-    profile_mark(3, s);
-    return e;
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cf::THREADS), params, sm23,
+                                       s);
 }
 
 #define CPR_INST_PREFILL(DK, DV, C)                                                                     \
     template cudaError_t launch_prefill<DK, DV, C, float>(const PrefillArgs&, cudaStream_t);           \
-    template cudaError_t launch_prefill<DK, DV, C, __nv_bfloat16>(const PrefillArgs&, cudaStream_t);
+    template cudaError_t launch_prefill<DK, DV, C, __nv_bfloat16>(const PrefillArgs&, cudaStream_t);   \
+    template cudaError_t launch_chunk_prep<DK, DV, C, float>(const PrefillArgs&, cudaStream_t);        \
+    template cudaError_t launch_chunk_prep<DK, DV, C, __nv_bfloat16>(const PrefillArgs&, cudaStream_t); \
+    template cudaError_t launch_chain_and_intra<DK, DV, C, float>(const PrefillArgs&, cudaStream_t);   \
+    template cudaError_t launch_chain_and_intra<DK, DV, C, __nv_bfloat16>(const PrefillArgs&, cudaStream_t);
 CPR_FOR_EACH_SHAPE(CPR_INST_PREFILL)
 
 }  // namespace cpr
