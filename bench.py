@@ -645,7 +645,8 @@ def run_ours(args):
         roofline["frac_of_measured"] = roofline["achieved"] / p32_meas["tflops"]
     extra = None if args.no_extra else run_extra_workloads(args, cpr, inputs, dev, dist, world, flush, p32_meas,
                                                            hbm_peak)
-    train = None if args.no_extra else run_train_fwd_bwd(args, cpr, inputs, dev, dist, world, flush, p32_meas)
+    train = None if args.no_extra or args.no_train else run_train_fwd_bwd(args, cpr, inputs, dev, dist, world, flush,
+                                                                           p32_meas)
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only) ----------------
     cpu = None
@@ -946,7 +947,9 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pik", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the rollout_prefill, varlen_stress and tiny lines")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the rollout_prefill, varlen_stress, tiny and train_fwd_bwd lines")
+    ap.add_argument("--no-train", action="store_true", help="skip the train_fwd_bwd line")
     ap.add_argument("--only-pik", action="store_true")
     ap.add_argument("--pik-size", type=int, default=8192, help="M = N = K of the pik product (a multiple of 512)")
     args = ap.parse_args()

@@ -103,22 +103,27 @@ __device__ __forceinline__ void zero(float (&acc)[TM][TN])
 }
 
 // Thread grid: 16 row groups x 16 column groups (thread t: rg = t / 16, cg = t % 16, so
-// the 16 threads of a row group are one half-warp).  An n x D tile gives each thread
-// TM = C/16 rows and two runs of D/32 columns, one in each half of the columns (so the
-// columns of a half-width product are a subset of the full-width ones).
+// the 16 threads of a row group are one half-warp).  A thread's rows are TM consecutive
+// ones; its columns are strided by 16 (column 16 j + cg), so a half-warp reading one
+// operand row touches 16 consecutive words (no bank conflicts), and a half-warp walking
+// one column per thread through a row-padded buffer hits 16 distinct banks.  An n x D tile
+// gives each thread TM = C/16 rows and D/16 columns, half of them in each half of the
+// columns (so the columns of a half-width product are a subset of the full-width ones).
 template <int C, int D>
 struct NDMap {
     static constexpr int TM = C / 16, TN = D / 16, HN = TN / 2;
     static __device__ __forceinline__ int row(int t, int i) { return (t >> 4) * TM + i; }
-    static __device__ __forceinline__ int col(int t, int j) { return (j / HN) * (D / 2) + (t & 15) * HN + j % HN; }
-    static __device__ __forceinline__ int hcol(int t, int h, int j) { return h * (D / 2) + (t & 15) * HN + j; }
+    // column j of this thread within half h: h * D/2 + hlocal(t, j)
+    static __device__ __forceinline__ int hlocal(int t, int j) { return j * 16 + (t & 15); }
+    static __device__ __forceinline__ int col(int t, int j) { return (j / HN) * (D / 2) + hlocal(t, j % HN); }
+    static __device__ __forceinline__ int hcol(int t, int h, int j) { return h * (D / 2) + hlocal(t, j); }
 };
-// An n x n tile: TM x TM contiguous per thread.
+// An n x n tile: TM consecutive rows, TM columns strided by 16.
 template <int C>
 struct NNMap {
     static constexpr int TM = C / 16;
     static __device__ __forceinline__ int row(int t, int i) { return (t >> 4) * TM + i; }
-    static __device__ __forceinline__ int col(int t, int j) { return (t & 15) * TM + j; }
+    static __device__ __forceinline__ int col(int t, int j) { return j * 16 + (t & 15); }
 };
 
 // Sum of v over the 16 threads of this thread's row group (a fixed tree over the half-warp).
@@ -305,29 +310,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb1_chunk_maps(BackwardArgs a)
         constexpr int TM = DK / 16, TN = DK / 16;
         float m[TM][TN];
         zero(m);
-        const int r0 = (t >> 4) * TM, c0 = (t & 15) * TN;
+        const int r0 = (t >> 4) * TM, cg = t & 15;  // rows r0 + i, columns 16 j + cg
         mm<TM, TN, C>(m, [&](int i, int k) { return __fmul_rn(v.dd[k], ld_f32(Kt + k * TK + r0 + i)); },
-                      [&](int k, int j) { return W[k * ND + c0 + j]; });
+                      [&](int k, int j) { return W[k * ND + 16 * j + cg]; });
         float* dst = a.mt + ch * DK * DK;
         const float gl = v.gam[C - 1];
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int j = 0; j < TN; ++j)
-                dst[(size_t)(r0 + i) * DK + c0 + j] = (r0 + i == c0 + j) ? __fsub_rn(gl, m[i][j]) : -m[i][j];
+                dst[(size_t)(r0 + i) * DK + 16 * j + cg] = (r0 + i == 16 * j + cg) ? __fsub_rn(gl, m[i][j]) : -m[i][j];
     }
     {  // C_b stored [c][i] = sum_t Qt[t][c] dO[t][i]
         constexpr int TM = DK / 16, TN = DV / 16;
         float m[TM][TN];
         zero(m);
-        const int r0 = (t >> 4) * TM, c0 = (t & 15) * TN;
+        const int r0 = (t >> 4) * TM, cg = t & 15;  // rows r0 + i, columns 16 j + cg
         mm<TM, TN, C>(m, [&](int i, int k) { return Qw[k * ND + r0 + i]; },
-                      [&](int k, int j) { return ld_f32(Ot + k * TV + c0 + j); });
+                      [&](int k, int j) { return ld_f32(Ot + k * TV + 16 * j + cg); });
         float* dst = a.cb + ch * DK * DV;
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < TN; ++j) dst[(size_t)(r0 + i) * DV + c0 + j] = m[i][j];
+            for (int j = 0; j < TN; ++j) dst[(size_t)(r0 + i) * DV + 16 * j + cg] = m[i][j];
     }
 }
 
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb3_chunk_grads(BackwardArgs a
         float y[TM][MK::HN];
         zero(y);
         mm<TM, MK::HN, DV>(y, [&](int i, int k) { return ld_f32(Ot + MK::row(t, i) * TV + k); },
-                           [&](int k, int j) { return big[((t & 15) * MK::HN + j) * NV + k]; });
+                           [&](int k, int j) { return big[MK::hlocal(t, j) * NV + k]; });
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
             const int r = MK::row(t, i);
@@ -648,7 +653,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb3_chunk_grads(BackwardArgs a
         float y[TM][MK::HN];
         zero(y);
         mm<TM, MK::HN, DV>(y, [&](int i, int k) { return n2[MK::row(t, i) * NV + k]; },
-                           [&](int k, int j) { return big[((t & 15) * MK::HN + j) * NV + k]; });
+                           [&](int k, int j) { return big[MK::hlocal(t, j) * NV + k]; });
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
             const int r = MK::row(t, i);
@@ -704,7 +709,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb3_chunk_grads(BackwardArgs a
         float y[TM][MK::HN];
         zero(y);
         mm<TM, MK::HN, DV>(y, [&](int i, int k) { return n1[MK::row(t, i) * NV + k]; },
-                           [&](int k, int j) { return big[((t & 15) * MK::HN + j) * NV + k]; });
+                           [&](int k, int j) { return big[MK::hlocal(t, j) * NV + k]; });
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
             const int r = MK::row(t, i);
