@@ -21,7 +21,7 @@ PROBE_LIB = os.path.join(BUILD, "libcprprobe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-cudart", "shared",
                      f"-I{INCLUDE}"]
-LIB_UNITS = ["api.cu", "prefill.cu", "decode.cu", "backward.cu", "noalloc.cu", "pik.cu"]
+LIB_UNITS = ["api.cu", "prefill.cu", "decode.cu", "backward.cu", "backward_tc.cu", "noalloc.cu", "pik.cu"]
 PROBE_UNITS = ["probe_peaks.cu"]
 
 

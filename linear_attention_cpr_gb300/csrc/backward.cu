@@ -32,6 +32,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "numerics.cuh"
 #include "tc.cuh"
@@ -879,10 +881,14 @@ cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s)
         k2<<<units, kBwdThreads, Kb2Cfg<DK, DV>::bytes, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_mark(3, s);
-        auto k3 = kb3_chunk_grads<DK, DV, C, T>;
-        if ((e = set_smem(k3, Kb3Cfg<DK, DV, C, T>::bytes)) != cudaSuccess) return e;
-        k3<<<grid, kBwdThreads, Kb3Cfg<DK, DV, C, T>::bytes, s>>>(a);
-        e = cudaGetLastError();
+        if constexpr (DK == 128 && DV == 128 && C == 64 && std::is_same<T, __nv_bfloat16>::value) {
+            e = launch_chunk_grads_tc(a, s);  // the tensor-core form of kb3 for this shape
+        } else {
+            auto k3 = kb3_chunk_grads<DK, DV, C, T>;
+            if ((e = set_smem(k3, Kb3Cfg<DK, DV, C, T>::bytes)) != cudaSuccess) return e;
+            k3<<<grid, kBwdThreads, Kb3Cfg<DK, DV, C, T>::bytes, s>>>(a);
+            e = cudaGetLastError();
+        }
         profile_mark(4, s);
         return e;
     }

@@ -1,0 +1,753 @@
+// backward_tc.cu — the CPR backward's per-chunk gradients on the 5th-generation tensor
+// cores, for bf16 inputs with dk = dv = 128 and C = 64 (the trainer's and the rollouts'
+// shape).  It computes what kb3_chunk_grads (backward.cu) computes, in the same WY form
+// and order of steps (see that file's header for the algebra), with every product a
+// tcgen05 MMA instead of FP32 FMAs.
+//
+// "IsoExec: Eliminating Trainer-Inference Mismatch in SkyRL", section "Chunkwise-Parallel
+// Recurrent (CPR) Gated DeltaNet", per-layer table, row "Trainer Fwd+Bwd": the pages time a
+// CPR backward; this is the chunk-local part of its adjoint.
+//
+// One CTA of 8 warps per (chunk, head).  Every product is D[128 x 64] (+)= A[128 x K] *
+// B[64 x K]^T with K = 128 or 64: the 128-row side is a key or value index (products of
+// n x n results use 64 rows of A and zero rows after them), the 64-column side a token.
+// Operands are written by the threads into shared memory as bf16 tiles in the tensor
+// cores' K-major core-matrix layout: bf16 inputs exactly (one split), everything derived in
+// fp32 as Dekker hi/lo splits (tc::split_f32), and each product is the sum of the split
+// products hi*hi (+ hi*lo) (+ lo*hi), accumulated in fp32 in TMEM (about 2^-16 relative per
+// term).  Results come back with tcgen05.ld, one accumulator row (TMEM lane) and 32
+// columns per thread; dq^T and dk^T accumulate in registers across products.  Sums over
+// the 128 rows (a key or value index) of a result use a fixed butterfly over the warp's
+// lanes and a fixed sum over the four lane quadrants, so the gradients are reproducible
+// and independent of packing, as for the FP32 kernels.  All waits are bounded.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "numerics.cuh"
+#include "tc.cuh"
+
+namespace cpr {
+
+namespace {
+
+constexpr int kD = 128;   // dk = dv
+constexpr int kN = 64;    // C, the tokens of a chunk
+constexpr int kT = 256;   // threads
+constexpr int kNN = kN + 1;
+
+// Shared memory (bytes).
+constexpr uint32_t KP_OFF = 0;                  // bf16 K [64][128] as stored (zero rows past the chunk)
+constexpr uint32_t OP_OFF = KP_OFF + 16384;     // bf16 dO [64][128]
+constexpr uint32_t TA_OFF = OP_OFF + 16384;     // A operand tiles (64 KB)
+constexpr uint32_t TB_OFF = TA_OFF + 65536;     // B operand tiles (32 KB)
+constexpr uint32_t TU_OFF = TB_OFF + 32768;     // U tile, later dT^T (32 KB)
+constexpr uint32_t PM_OFF = TU_OFF + 32768;     // fp32 Pm [64][65], later dKK
+constexpr uint32_t TM_OFF = PM_OFF + 16640;     // fp32 T [64][65] (first A^T [64][64])
+constexpr uint32_t LM_OFF = TM_OFF + 16640;     // fp32 L [64][65]
+constexpr uint32_t VEC_OFF = LM_OFF + 16640;    // 16 per-token vectors of 64 floats
+constexpr uint32_t RED_OFF = VEC_OFF + 4096;    // reduction partials [8][64]
+constexpr uint32_t BAR_OFF = RED_OFF + 2048;
+constexpr uint32_t kSmem = BAR_OFF + 64;
+static_assert(kSmem <= 232448, "one CTA's shared memory");
+
+// TMEM accumulators (columns)
+constexpr uint32_t P0 = 0, P1 = 64, P2 = 128;
+constexpr uint32_t kTmemCols = 256;
+
+template <int K>
+__device__ __forceinline__ uint32_t toff(int row, int k)
+{
+    return tc::tile_off<2>(row, k, K);
+}
+
+// The calling thread holds x[jj] = element (row 32 hc + jj, K index m) of a K-major split
+// tile (m = 32 q + lane, this thread's accumulator row).  Within each group of 8 lanes an
+// 8 x 8 register transpose (three rounds of exchanges) gives lane p the 8 consecutive K
+// elements of row 32 hc + 8 blk + p, which it stores as one 16-byte hi/lo pair.
+template <int K>
+__device__ __forceinline__ void transpose_store(const float (&x)[32], unsigned char* base, uint32_t split, int m,
+                                                int hc)
+{
+    const int p = threadIdx.x & 7, kb = m - p;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+        float a[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[e] = x[8 * blk + e];
+#pragma unroll
+        for (int sw = 4; sw >= 1; sw >>= 1) {
+            const bool upper = (p & sw) != 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (e & sw) continue;
+                const float send = upper ? a[e] : a[e + sw];
+                const float recv = __shfl_xor_sync(0xffffffffu, send, sw);
+                if (upper)
+                    a[e] = recv;
+                else
+                    a[e + sw] = recv;
+            }
+        }
+        const uint32_t off = tc::tile_off<2>(32 * hc + 8 * blk + p, kb, K);
+        tc::split8_store(a, base + off, base + split + off);
+    }
+}
+
+// D (TMEM) (+)= A (128 x K tile at a) * B (64 x K tile at b)^T; NA, NB: splits present in
+// each tile (1: hi only, exact bf16; 2: hi and lo).  Products hi*hi, then hi*lo (NB = 2),
+// then lo*hi (NA = 2), K ascending in each; the first instruction overwrites D unless
+// `accumulate`.
+template <int K, int NA, int NB>
+__device__ __forceinline__ void mma_ab(uint32_t d, uint32_t a, uint32_t b, bool accumulate)
+{
+    constexpr uint32_t SBO = (K / 8) * 128, ASPL = 128 * K * 2, BSPL = 64 * K * 2;
+    constexpr uint32_t idesc = tc::idesc_bf16(128, 64);
+    const uint32_t pa[3] = {0u, 0u, 1u}, pb[3] = {0u, 1u, 0u};
+#pragma unroll
+    for (int p = 0; p < 3; ++p) {
+        if ((p == 1 && NB != 2) || (p == 2 && NA != 2)) continue;
+#pragma unroll
+        for (int k = 0; k < K / 16; ++k)
+            tc::mma_bf16(d, tc::sdesc(a + pa[p] * ASPL + k * 256, 128, SBO),
+                         tc::sdesc(b + pb[p] * BSPL + k * 256, 128, SBO), idesc,
+                         (accumulate || p != 0 || k != 0) ? 1u : 0u);
+    }
+}
+
+// Lane l of the warp gets the sum over the warp's 32 lanes of v[l] (a fixed butterfly:
+// each round keeps one half of the remaining columns and adds the partner's copy).
+__device__ __forceinline__ float colsum32(float (&v)[32])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) {
+        const bool upper = (lane & k) != 0;
+#pragma unroll
+        for (int j = 0; j < k; ++j) {
+            const float send = upper ? v[j] : v[j + k];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, k);
+            v[j] = __fadd_rn(upper ? v[j + k] : v[j], recv);
+        }
+    }
+    return v[0];
+}
+
+struct V16 {
+    float *G, *gam, *dd, *beta, *dgam1, *dgam2, *ddv, *dbeta1, *dbeta2, *edr1, *edr2, *edc1, *edc2, *dG, *gin, *misc;
+    __device__ explicit V16(float* p)
+        : G(p), gam(p + 64), dd(p + 128), beta(p + 192), dgam1(p + 256), dgam2(p + 320), ddv(p + 384),
+          dbeta1(p + 448), dbeta2(p + 512), edr1(p + 576), edr2(p + 640), edc1(p + 704), edc2(p + 768),
+          dG(p + 832), gin(p + 896), misc(p + 960) {}
+};
+
+__global__ void __launch_bounds__(kT, 1) kb3_chunk_grads_tc(BackwardArgs a)
+{
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __nv_bfloat16* Kp = reinterpret_cast<__nv_bfloat16*>(sm + KP_OFF);
+    __nv_bfloat16* Op = reinterpret_cast<__nv_bfloat16*>(sm + OP_OFF);
+    unsigned char* TA = sm + TA_OFF;
+    unsigned char* TB = sm + TB_OFF;
+    unsigned char* TU = sm + TU_OFF;
+    float* Pm = reinterpret_cast<float*>(sm + PM_OFF);
+    float* Tm = reinterpret_cast<float*>(sm + TM_OFF);
+    float* Lm = reinterpret_cast<float*>(sm + LM_OFF);
+    V16 v(reinterpret_cast<float*>(sm + VEC_OFF));
+    float* red = reinterpret_cast<float*>(sm + RED_OFF);  // [8][64]
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + BAR_OFF);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    volatile int* okf = reinterpret_cast<volatile int*>(tslot + 1);
+
+    const int64_t c = blockIdx.x;
+    const int h = blockIdx.y, H = a.H, t = threadIdx.x;
+    if (*a.status || c >= a.cu_chunks[a.n_seqs]) return;
+    const int n = find_seq(a.cu_chunks, a.n_seqs, c);
+    const int64_t j = c - a.cu_chunks[n];
+    const int64_t t0 = (int64_t)a.cu_seqlens[n] + j * kN;
+    const int len = (int)min((int64_t)kN, (int64_t)a.cu_seqlens[n + 1] - t0);
+    const size_t ch = (size_t)c * H + h, SSZ = (size_t)kD * kD;
+    const float* Sb = a.boundary + ch * SSZ;  // [c][i] = S_b[i][c]
+    const float* dSe = a.d_end + ch * SSZ;
+    const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(a.k);
+    const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(a.v);
+    const __nv_bfloat16* go = static_cast<const __nv_bfloat16*>(a.d_out);
+
+    // epilogue mapping: accumulator row m (TMEM lane), columns [32 hc, 32 hc + 32)
+    const int w = t >> 5, lane = t & 31, q = w & 3, hc = w >> 2, m = 32 * q + lane;
+
+    if (w == 0) tc::tmem_alloc(tslot, kTmemCols);
+    if (t == 0) {
+        tc::mbar_init(mbar, 1);
+        tc::fence_mbar_init();
+    }
+    // ---- a: the chunk's K and dO as stored (zero rows past its tokens), g, beta
+    for (int idx = t; idx < kN * 16; idx += kT) {
+        const int r = idx >> 4, cv = (idx & 15) * 8;
+        uint4 wk = make_uint4(0u, 0u, 0u, 0u), wo = wk;
+        if (r < len) {
+            wk = __ldg(reinterpret_cast<const uint4*>(gk + ((t0 + r) * H + h) * kD + cv));
+            wo = __ldg(reinterpret_cast<const uint4*>(go + ((t0 + r) * H + h) * kD + cv));
+        }
+        *reinterpret_cast<uint4*>(Kp + r * kD + cv) = wk;
+        *reinterpret_cast<uint4*>(Op + r * kD + cv) = wo;
+    }
+    if (t < kN) {
+        v.gin[t] = t < len ? a.g[(t0 + t) * H + h] : 0.0f;
+        v.beta[t] = t < len ? a.beta[(t0 + t) * H + h] : 0.0f;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t lanes = (uint32_t)(32 * q) << 16;
+    if (t == 0) {
+        float G = 0.0f;
+        for (int r = 0; r < kN; ++r) {
+            G = r == 0 ? v.gin[0] : __fadd_rn(G, v.gin[r]);
+            v.G[r] = G;
+        }
+    }
+    __syncthreads();
+    if (t < kN) {
+        v.gam[t] = decay_exp(v.G[t]);
+        v.dd[t] = decay_exp(__fsub_rn(v.G[kN - 1], v.G[t]));
+    }
+
+    uint32_t phase = 0;
+    bool alive = true;
+    // Every writer has stored its tiles: make them visible to the tensor cores, let thread 0
+    // issue the products and wait for them, then every thread may read the accumulators.
+    auto run_begin = [&](auto issue) {
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (t == 0) {
+            tc::fence_after_sync();
+            issue();
+            tc::commit(mbar);
+        }
+    };
+    auto run_end = [&]() {
+        if (t == 0) *okf = tc::mbar_wait(mbar, phase) ? 1 : 0;
+        phase ^= 1u;
+        __syncthreads();
+        tc::fence_after_sync();
+        alive = alive && *okf != 0;
+    };
+    // the products of one step: issued by thread 0 once every thread's tiles are written,
+    // and done for every thread on return
+    auto run = [&](auto issue) {
+        run_begin(issue);
+        run_end();
+    };
+    auto acc = [&](uint32_t col, float (&x)[32]) { tc::tmem_ld32(tmem + lanes + col + 32 * hc, x); };
+    auto e_of = [&](int r, int i) { return decay_exp(__fsub_rn(v.G[r], v.G[i])); };
+    // zero rows [64, 128) of a tile of K elements per row (hi and, if lo_too, lo)
+    auto zero_upper = [&](unsigned char* base, int K, bool lo_too) {
+        const uint32_t half = 64u * K * 2;  // rows 64.. start half-way into each split
+        const int nv = (int)(half / 16);
+        for (int idx = t; idx < nv * (lo_too ? 2 : 1); idx += kT) {
+            const int s = idx / nv, o = idx % nv;
+            *reinterpret_cast<uint4*>(base + s * (2 * half) + half + o * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+
+    // A tile (128 rows x K = 128, hi/lo) from a stored state src[c][i] (128 x 128 fp32):
+    // transposed (rows i, K = c) or as stored (rows c, K = i).  Loads of NB items are
+    // issued before their splits are stored, so the memory latency is paid 8 / NB times per
+    // call rather than eight times.
+    auto state_tile = [&](const float* src, bool transposed) {
+        constexpr int NB = 8;
+#pragma unroll
+        for (int b = 0; b < 8 / NB; ++b) {
+            float xs[NB][8];
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const int idx = t + (NB * b + u) * kT;
+                if (transposed) {
+                    const int i = idx % kD, c8 = (idx / kD) * 8;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xs[u][e] = __ldg(src + (size_t)(c8 + e) * kD + i);
+                } else {
+                    const int cc = idx >> 4, i8 = (idx & 15) * 8;
+                    const float4 p0 = __ldg(reinterpret_cast<const float4*>(src + (size_t)cc * kD + i8));
+                    const float4 p1 = __ldg(reinterpret_cast<const float4*>(src + (size_t)cc * kD + i8 + 4));
+                    xs[u][0] = p0.x, xs[u][1] = p0.y, xs[u][2] = p0.z, xs[u][3] = p0.w;
+                    xs[u][4] = p1.x, xs[u][5] = p1.y, xs[u][6] = p1.z, xs[u][7] = p1.w;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const int idx = t + (NB * b + u) * kT;
+                const int row = transposed ? idx % kD : idx >> 4;
+                const int k8 = transposed ? (idx / kD) * 8 : (idx & 15) * 8;
+                tc::split8_store(xs[u], TA + toff<kD>(row, k8), TA + 32768 + toff<kD>(row, k8));
+            }
+        }
+    };
+    if (t == 0) {  // both states are read several times: into L2 now
+        tc::prefetch_l2(Sb, (uint32_t)(SSZ * 4));
+        tc::prefetch_l2(dSe, (uint32_t)(SSZ * 4));
+    }
+    if (t < 2 * kN && (t & 63) < len) {  // the chunk's query and value rows (read column-wise later)
+        const __nv_bfloat16* row = (t < kN ? gq : gv) + ((t0 + (t & 63)) * H + h) * kD;
+        tc::prefetch_l2(row, kD * 2);
+    }
+
+    // ---- F1, F2: K K^T and Q K^T (n x n)
+    {
+        for (int idx = t; idx < kN * 16; idx += kT) {
+            const int r = idx >> 4, cv = (idx & 15) * 8;
+            const uint4 kw = *reinterpret_cast<const uint4*>(Kp + r * kD + cv);
+            uint4 qw = make_uint4(0u, 0u, 0u, 0u);
+            if (r < len) qw = __ldg(reinterpret_cast<const uint4*>(gq + ((t0 + r) * H + h) * kD + cv));
+            *reinterpret_cast<uint4*>(TA + toff<kD>(r, cv)) = kw;
+            *reinterpret_cast<uint4*>(TA + 32768 + toff<kD>(r, cv)) = qw;
+            *reinterpret_cast<uint4*>(TB + toff<kD>(r, cv)) = kw;
+        }
+        zero_upper(TA, kD, false);
+        zero_upper(TA + 32768, kD, false);
+        run([&] {
+            mma_ab<kD, 1, 1>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false);
+            mma_ab<kD, 1, 1>(tmem + P1, tc::smem_u32(TA + 32768), tc::smem_u32(TB), false);
+        });
+        if (q < 2) {  // rows t < 64
+            float kk[32], qk[32];
+            acc(P0, kk);
+            acc(P1, qk);
+            const float br = v.beta[m];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int r = 32 * hc + jj;
+                const float e = r <= m ? e_of(m, r) : 0.0f;
+                const float l = r < m ? __fmul_rn(kk[jj], e) : 0.0f;
+                Lm[m * kNN + r] = l;
+                Tm[r * kN + m] = __fmul_rn(br, l);  // A transposed for the substitution
+                Pm[m * kNN + r] = __fmul_rn(qk[jj], e);
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        // T = (I + A)^-1 by blocks, with every thread, into TU (free until F4's epilogue)
+        invert_unit_lower<kN, kNN>(Tm, reinterpret_cast<float*>(TU), reinterpret_cast<float*>(TU + 16896), t, kT);
+        {
+            const float* X = reinterpret_cast<const float*>(TU);
+            for (int idx = t; idx < kN * kN; idx += kT) Tm[(idx >> 6) * kNN + (idx & 63)] = X[(idx >> 6) * kNN + (idx & 63)];
+        }
+        __syncthreads();
+    }
+    float dqT[32], dkT[32], RT[32];  // row m (key index for dq/dk, value index for R), columns 32 hc + jj
+
+    // ---- F3: KS^T = S_b K^T;  R^T = V^T - KS^T diag(gam)
+    if (alive) {
+        float vv[32];  // issued first: their latency overlaps the gather of S_b
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int r = 32 * hc + jj;
+            vv[jj] = r < len ? __bfloat162float(gv[((t0 + r) * H + h) * kD + m]) : 0.0f;
+        }
+        state_tile(Sb, true);  // A: S_b[i][c], rows i, K = c
+        run_begin([&] { mma_ab<kD, 2, 1>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        {  // dgam_last = <dS_end, S_b> while the product runs: a fixed order per thread, then fixed trees
+            float sd = 0.0f;
+#pragma unroll 4
+            for (int idx = t; idx < (int)SSZ; idx += kT) sd = __fmaf_rn(__ldg(dSe + idx), __ldg(Sb + idx), sd);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) sd = __fadd_rn(sd, __shfl_xor_sync(0xffffffffu, sd, o));
+            if (lane == 0) red[256 + w] = sd;
+        }
+        run_end();
+        if (t == 0) {
+            float d = 0.0f;
+            for (int i = 0; i < 8; ++i) d = __fadd_rn(d, red[256 + i]);
+            v.misc[0] = d;
+        }
+        float ks[32];
+        acc(P0, ks);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) RT[jj] = __fsub_rn(vv[jj], __fmul_rn(v.gam[32 * hc + jj], ks[jj]));
+    }
+    // ---- B1: Y^T = S_b^T dO^T:  dq^T = Y^T diag(gam);  dgam = colsum(Y^T o Q^T)
+    if (alive) {
+        state_tile(Sb, false);  // A: S_b^T, rows c, K = i (as stored)
+        for (int idx = t; idx < kN * 16; idx += kT) {  // B: dO, rows t, K = i
+            const int r = idx >> 4, cv = (idx & 15) * 8;
+            *reinterpret_cast<uint4*>(TB + toff<kD>(r, cv)) = *reinterpret_cast<const uint4*>(Op + r * kD + cv);
+        }
+        float qv[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int r = 32 * hc + jj;
+            qv[jj] = r < len ? __bfloat162float(gq[((t0 + r) * H + h) * kD + m]) : 0.0f;
+        }
+        run([&] { mma_ab<kD, 2, 1>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        float y[32];
+        acc(P0, y);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            dqT[jj] = __fmul_rn(v.gam[32 * hc + jj], y[jj]);
+            qv[jj] = __fmul_rn(y[jj], qv[jj]);
+            dkT[jj] = 0.0f;
+        }
+        red[q * 64 + 32 * hc + lane] = colsum32(qv);
+        __syncthreads();
+        if (t < kN) v.dgam1[t] = __fadd_rn(__fadd_rn(red[t], red[64 + t]), __fadd_rn(red[128 + t], red[192 + t]));
+    }
+    // ---- F4: U^T = (R^T diag(beta)) T^T  -> the U tile (rows r, K = i) for B2 and B4
+    if (alive) {
+#pragma unroll
+        for (int e8 = 0; e8 < 32; e8 += 8) {  // A: rows i, K = r (this thread's row)
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = __fmul_rn(RT[e8 + e], v.beta[32 * hc + e8 + e]);
+            tc::split8_store(xs, TA + toff<kN>(m, 32 * hc + e8), TA + 16384 + toff<kN>(m, 32 * hc + e8));
+        }
+        for (int idx = t; idx < kN * 8; idx += kT) {  // B: T, rows t, K = r
+            const int r = idx >> 3, k8 = (idx & 7) * 8;
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = Tm[r * kNN + k8 + e];
+            tc::split8_store(xs, TB + toff<kN>(r, k8), TB + 8192 + toff<kN>(r, k8));
+        }
+        run([&] { mma_ab<kN, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        float u[32];
+        acc(P0, u);
+        transpose_store<kD>(u, TU, 16384, m, hc);  // U tile rows r, K = i
+    }
+    // ---- B2: dPm = (dO U^T) o lower;  ED += dPm o Pm;  dQK = dPm o E  (tiles for B5, B6)
+    if (alive) {
+        for (int idx = t; idx < kN * 16; idx += kT) {  // A: dO, rows t, K = i
+            const int r = idx >> 4, cv = (idx & 15) * 8;
+            *reinterpret_cast<uint4*>(TA + toff<kD>(r, cv)) = *reinterpret_cast<const uint4*>(Op + r * kD + cv);
+        }
+        zero_upper(TA, kD, false);
+        run([&] { mma_ab<kD, 1, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TU), false); });
+        if (q < 2) {
+            float dp[32], col[32], rowp = 0.0f;
+            acc(P0, dp);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int r = 32 * hc + jj;
+                const float x = r <= m ? dp[jj] : 0.0f;
+                const float ed = __fmul_rn(x, Pm[m * kNN + r]);
+                rowp = __fadd_rn(rowp, ed);
+                col[jj] = ed;
+                dp[jj] = r <= m ? __fmul_rn(x, e_of(m, r)) : 0.0f;  // dQK
+            }
+#pragma unroll
+            for (int e8 = 0; e8 < 32; e8 += 8) {  // dQK tile: rows t, K = r
+                float xs[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xs[e] = dp[e8 + e];
+                tc::split8_store(xs, TB + toff<kN>(m, 32 * hc + e8), TB + 8192 + toff<kN>(m, 32 * hc + e8));
+            }
+            transpose_store<kN>(dp, TB + 16384, 8192, m, hc);  // dQK^T tile rows r, K = t
+            red[q * 64 + 32 * hc + lane] = colsum32(col);
+            red[256 + hc * 64 + m] = rowp;
+        }
+        __syncthreads();
+        if (t < kN) {
+            v.edc1[t] = __fadd_rn(red[t], red[64 + t]);
+            v.edr1[t] = __fadd_rn(red[256 + t], red[320 + t]);
+        }
+    }
+    // ---- B5, B6: dq^T += K^T dQK^T;  dk^T += Q^T dQK
+    if (alive) {
+        {  // A: K^T rows c, K = r;  Q^T rows c, K = t (the query loads of all four items first)
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            uint16_t qb[2][8];
+#pragma unroll
+            for (int uu = 0; uu < 2; ++uu) {
+                const int u = 2 * hb + uu;
+                const int idx = t + u * kT, cc = idx % kD, r8 = (idx / kD) * 8;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    qb[uu][e] = r8 + e < len ? __bfloat16_as_ushort(gq[((t0 + r8 + e) * H + h) * kD + cc]) : (uint16_t)0;
+            }
+#pragma unroll
+            for (int uu = 0; uu < 2; ++uu) {
+                const int u = 2 * hb + uu;
+                const int idx = t + u * kT, cc = idx % kD, r8 = (idx / kD) * 8;
+                uint32_t kw[4], qw[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    kw[e / 2] = (uint32_t)__bfloat16_as_ushort(Kp[(r8 + e) * kD + cc]) |
+                                ((uint32_t)__bfloat16_as_ushort(Kp[(r8 + e + 1) * kD + cc]) << 16);
+                    qw[e / 2] = (uint32_t)qb[uu][e] | ((uint32_t)qb[uu][e + 1] << 16);
+                }
+                *reinterpret_cast<uint4*>(TA + toff<kN>(cc, r8)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+                *reinterpret_cast<uint4*>(TA + 32768 + toff<kN>(cc, r8)) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+            }
+          }
+        }
+        run([&] {
+            mma_ab<kN, 1, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false);
+            mma_ab<kN, 1, 2>(tmem + P1, tc::smem_u32(TA + 32768), tc::smem_u32(TB + 16384), false);
+        });
+        float x[32];
+        acc(P0, x);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) dqT[jj] = __fadd_rn(dqT[jj], x[jj]);
+        acc(P1, x);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) dkT[jj] = __fadd_rn(dkT[jj], x[jj]);
+    }
+    // ---- B3: dU^T = dS_end (diag(d) K)^T + dO^T Pm
+    float DUT[32];
+    if (alive) {
+        state_tile(dSe, true);  // A: dS_end[i][c], rows i, K = c
+        for (int idx = t; idx < kN * 16; idx += kT) {  // B: diag(d) K, rows r, K = c
+            const int r = idx >> 4, c8 = (idx & 15) * 8;
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = __fmul_rn(v.dd[r], __bfloat162float(Kp[r * kD + c8 + e]));
+            tc::split8_store(xs, TB + toff<kD>(r, c8), TB + 16384 + toff<kD>(r, c8));
+        }
+        run([&] { mma_ab<kD, 2, 2>(tmem + P2, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+    }
+    if (alive) {
+        for (int idx = t; idx < kD * 8; idx += kT) {  // A: dO^T rows i, K = t
+            const int i = idx % kD, r8 = (idx / kD) * 8;
+            uint32_t ow[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2)
+                ow[e / 2] = (uint32_t)__bfloat16_as_ushort(Op[(r8 + e) * kD + i]) |
+                            ((uint32_t)__bfloat16_as_ushort(Op[(r8 + e + 1) * kD + i]) << 16);
+            *reinterpret_cast<uint4*>(TA + toff<kN>(i, r8)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+        for (int idx = t; idx < kN * 8; idx += kT) {  // B: Pm^T rows r, K = t
+            const int r = idx % kN, k8 = (idx / kN) * 8;
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = Pm[(k8 + e) * kNN + r];
+            tc::split8_store(xs, TB + toff<kN>(r, k8), TB + 8192 + toff<kN>(r, k8));
+        }
+        run([&] { mma_ab<kN, 1, 2>(tmem + P2, tc::smem_u32(TA), tc::smem_u32(TB), true); });
+        acc(P2, DUT);
+    }
+    // ---- B4: UdS^T = dS_end^T U^T-side:  dk^T += UdS^T diag(d);  dd = colsum(UdS^T o K^T)
+    if (alive) {
+        state_tile(dSe, false);  // A: dS_end^T rows c, K = i (as stored)
+        run([&] { mma_ab<kD, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TU), false); });
+        float x[32];
+        acc(P0, x);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int r = 32 * hc + jj;
+            dkT[jj] = __fmaf_rn(v.dd[r], x[jj], dkT[jj]);
+            x[jj] = __fmul_rn(x[jj], __bfloat162float(Kp[r * kD + m]));
+        }
+        red[q * 64 + 32 * hc + lane] = colsum32(x);
+        __syncthreads();
+        if (t < kN) v.ddv[t] = __fadd_rn(__fadd_rn(red[t], red[64 + t]), __fadd_rn(red[128 + t], red[192 + t]));
+    }
+    // ---- B7: dT = dU (diag(beta) R)^T (n x n)  -> the dT^T tile (rows t', K = t) for B10
+    if (alive) {
+        __syncthreads();  // every reader of the last reductions' partials and of TA is done
+        transpose_store<kD>(DUT, TA, 32768, m, hc);  // dU rows t, K = i
+        {
+            float br[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) br[jj] = __fmul_rn(v.beta[32 * hc + jj], RT[jj]);
+            transpose_store<kD>(br, TB, 16384, m, hc);  // beta R rows r, K = i
+        }
+        zero_upper(TA, kD, true);
+        run([&] { mma_ab<kD, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        if (q < 2) {
+            float x[32];
+            acc(P0, x);
+            transpose_store<kN>(x, TU, 8192, m, hc);  // dT^T tile rows t', K = t
+        }
+    }
+    // ---- B8: TdU^T = dU^T T:  dv = diag(beta) TdU;  dbeta = colsum(TdU^T o R^T)
+    if (alive) {
+#pragma unroll
+        for (int e8 = 0; e8 < 32; e8 += 8) {  // A: dU^T rows i, K = t (this thread's row)
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = DUT[e8 + e];
+            tc::split8_store(xs, TA + toff<kN>(m, 32 * hc + e8), TA + 16384 + toff<kN>(m, 32 * hc + e8));
+        }
+        for (int idx = t; idx < kN * 8; idx += kT) {  // B: T^T rows r, K = t
+            const int r = idx % kN, k8 = (idx / kN) * 8;
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = Tm[(k8 + e) * kNN + r];
+            tc::split8_store(xs, TB + toff<kN>(r, k8), TB + 8192 + toff<kN>(r, k8));
+        }
+        run([&] { mma_ab<kN, 2, 2>(tmem + P1, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        float x[32];
+        acc(P1, x);
+        transpose_store<kD>(x, TB, 16384, m, hc);  // TdU tile rows r, K = i, for B9 (TB is free)
+        float* dvb = a.dv + ((size_t)t0 * H + h) * kD + m;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int r = 32 * hc + jj;
+            if (r < len) dvb[(size_t)r * H * kD] = __fmul_rn(v.beta[r], x[jj]);
+            x[jj] = __fmul_rn(x[jj], RT[jj]);
+        }
+        red[q * 64 + 32 * hc + lane] = colsum32(x);
+        __syncthreads();
+        if (t < kN) v.dbeta1[t] = __fadd_rn(__fadd_rn(red[t], red[64 + t]), __fadd_rn(red[128 + t], red[192 + t]));
+    }
+    // ---- B9: Z^T = S_b^T TdU^T:  dk^T -= Z^T diag(beta gam);  dgam -= beta colsum(Z^T o K^T)
+    if (alive) {
+        state_tile(Sb, false);  // A: S_b^T rows c, K = i (as stored)
+        run([&] { mma_ab<kD, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        float x[32];
+        acc(P0, x);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int r = 32 * hc + jj;
+            dkT[jj] = __fmaf_rn(-__fmul_rn(v.beta[r], v.gam[r]), x[jj], dkT[jj]);
+            x[jj] = __fmul_rn(x[jj], __bfloat162float(Kp[r * kD + m]));
+        }
+        red[q * 64 + 32 * hc + lane] = colsum32(x);
+        __syncthreads();
+        if (t < kN)
+            v.dgam2[t] = __fmul_rn(-v.beta[t], __fadd_rn(__fadd_rn(red[t], red[64 + t]),
+                                                         __fadd_rn(red[128 + t], red[192 + t])));
+    }
+    // ---- B10: X = T^T dT (n x n) -> the X tile (rows r, K = t) for B11
+    if (alive) {
+        __syncthreads();
+        for (int idx = t; idx < kN * 8; idx += kT) {  // A: T^T rows r, K = t
+            const int r = idx % kN, k8 = (idx / kN) * 8;
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = Tm[(k8 + e) * kNN + r];
+            tc::split8_store(xs, TA + toff<kN>(r, k8), TA + 16384 + toff<kN>(r, k8));
+        }
+        zero_upper(TA, kN, true);
+        run([&] { mma_ab<kN, 2, 2>(tmem + P1, tc::smem_u32(TA), tc::smem_u32(TU), false); });
+        if (q < 2) {
+            float x[32];
+            acc(P1, x);
+#pragma unroll
+            for (int e8 = 0; e8 < 32; e8 += 8) {
+                float xs[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xs[e] = x[e8 + e];
+                tc::split8_store(xs, TA + toff<kN>(m, 32 * hc + e8), TA + 16384 + toff<kN>(m, 32 * hc + e8));
+            }
+        }
+    }
+    // ---- B11: dA = -(X T^T) o strictly lower:  dbeta += rowsum(dA o L);  dL = beta dA;
+    //      ED += dL o L;  dKK = dL o E  -> Ssym = dKK + dKK^T tile for B12
+    if (alive) {
+        for (int idx = t; idx < kN * 8; idx += kT) {  // B: T rows i, K = t
+            const int r = idx >> 3, k8 = (idx & 7) * 8;
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = Tm[r * kNN + k8 + e];
+            tc::split8_store(xs, TB + toff<kN>(r, k8), TB + 8192 + toff<kN>(r, k8));
+        }
+        run([&] { mma_ab<kN, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        if (q < 2) {
+            float x[32], col[32], rowb = 0.0f, rowe = 0.0f;
+            acc(P0, x);
+            const float br = v.beta[m];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int i = 32 * hc + jj;
+                const float da = i < m ? -x[jj] : 0.0f;
+                const float l = Lm[m * kNN + i];
+                rowb = __fmaf_rn(da, l, rowb);
+                const float dl = __fmul_rn(br, da);
+                const float ed = __fmul_rn(dl, l);
+                rowe = __fadd_rn(rowe, ed);
+                col[jj] = ed;
+                Pm[m * kNN + i] = i < m ? __fmul_rn(dl, e_of(m, i)) : 0.0f;  // dKK (Pm is dead)
+            }
+            red[q * 64 + 32 * hc + lane] = colsum32(col);
+            red[256 + hc * 64 + m] = rowe;
+            red[384 + hc * 64 + m] = rowb;
+        }
+        __syncthreads();
+        if (t < kN) {
+            v.edc2[t] = __fadd_rn(red[t], red[64 + t]);
+            v.edr2[t] = __fadd_rn(red[256 + t], red[320 + t]);
+            v.dbeta2[t] = __fadd_rn(red[384 + t], red[448 + t]);
+        }
+        for (int idx = t; idx < kN * 8; idx += kT) {  // B: Ssym rows r, K = i
+            const int r = idx >> 3, k8 = (idx & 7) * 8;
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = __fadd_rn(Pm[r * kNN + k8 + e], Pm[(k8 + e) * kNN + r]);
+            tc::split8_store(xs, TB + toff<kN>(r, k8), TB + 8192 + toff<kN>(r, k8));
+        }
+        for (int idx = t; idx < kD * 8; idx += kT) {  // A: K^T rows c, K = i
+            const int cc = idx % kD, r8 = (idx / kD) * 8;
+            uint32_t kw[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2)
+                kw[e / 2] = (uint32_t)__bfloat16_as_ushort(Kp[(r8 + e) * kD + cc]) |
+                            ((uint32_t)__bfloat16_as_ushort(Kp[(r8 + e + 1) * kD + cc]) << 16);
+            *reinterpret_cast<uint4*>(TA + toff<kN>(cc, r8)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+        }
+    }
+    // ---- B12: dk^T += K^T Ssym^T-side (dk += (dKK + dKK^T) K)
+    if (alive) {
+        run([&] { mma_ab<kN, 1, 2>(tmem + P1, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        float x[32];
+        acc(P1, x);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) dkT[jj] = __fadd_rn(dkT[jj], x[jj]);
+    }
+    // ---- the gates and the stores
+    if (alive) {
+        __syncthreads();
+        if (t == 0) {
+            const float dlast = v.misc[0];
+            float sdd = 0.0f;
+            for (int r = 0; r < kN; ++r) sdd = __fmaf_rn(v.dd[r], v.ddv[r], sdd);
+            float accg = 0.0f;
+            for (int r = kN - 1; r >= 0; --r) {
+                float dgam = __fadd_rn(v.dgam1[r], v.dgam2[r]);
+                if (r == kN - 1) dgam = __fadd_rn(dgam, dlast);
+                float dG = __fmul_rn(v.gam[r], dgam);
+                dG = __fsub_rn(dG, __fmul_rn(v.dd[r], v.ddv[r]));
+                dG = __fadd_rn(dG, __fsub_rn(__fadd_rn(v.edr1[r], v.edr2[r]), __fadd_rn(v.edc1[r], v.edc2[r])));
+                if (r == kN - 1) dG = __fadd_rn(dG, sdd);
+                accg = __fadd_rn(accg, dG);
+                v.dG[r] = accg;
+            }
+        }
+        __syncthreads();
+        if (t < len) {
+            a.dg[(t0 + t) * H + h] = v.dG[t];
+            a.dbeta[(t0 + t) * H + h] = __fadd_rn(v.dbeta1[t], v.dbeta2[t]);
+        }
+        float* dqb = a.dq + ((size_t)t0 * H + h) * kD + m;
+        float* dkb = a.dk + ((size_t)t0 * H + h) * kD + m;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int r = 32 * hc + jj;
+            if (r < len) {
+                dqb[(size_t)r * H * kD] = dqT[jj];
+                dkb[(size_t)r * H * kD] = dkT[jj];
+            }
+        }
+    } else if (t == 0) {
+        atomicOr(a.status, CPR_DEV_TIMEOUT);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (w == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+// The tensor-core chunk gradients (bf16, dk = dv = 128, C = 64) in place of kb3.
+cudaError_t launch_chunk_grads_tc(const BackwardArgs& a, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(kb3_chunk_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    kb3_chunk_grads_tc<<<dim3((unsigned)a.max_chunks, (unsigned)a.H), kT, kSmem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace cpr

@@ -233,6 +233,8 @@ template <int DK, int DV, int C, typename T> cudaError_t launch_decode(const Dec
 template <int DK, int DV, int C, typename T> cudaError_t launch_ring_from_prefill(const RingArgs& a, cudaStream_t s);
 // The CPR backward (k0, then the chunk maps, the reverse chain and the chunk gradients).
 template <int DK, int DV, int C, typename T> cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
+// The chunk gradients of the backward on the tensor cores (bf16, dk = dv = 128, C = 64).
+cudaError_t launch_chunk_grads_tc(const BackwardArgs& a, cudaStream_t s);
 // Whether the backward's chunk kernels fit one CTA's shared memory for this shape and type.
 template <int DK, int DV, int C, typename T> bool backward_fits();
 

@@ -177,4 +177,63 @@ __device__ __forceinline__ void fwd_subst(const float* At, float x[C])
     }
 }
 
+// T = (I + A)^-1 of a strictly lower-triangular C x C matrix A by blocks of 16, with all
+// `nt` threads of the caller: the four (C / 16) diagonal blocks by forward substitution,
+// one column per thread (x_r = [r == j] - sum_{i<r} A_ri x_i, fma in ascending i), then
+// the blocks below the diagonal by distance d = 1, 2, ..: Y = sum_{k=j}^{i-1} A_ik T_kj
+// (blocks k ascending, 16 terms each in ascending order), T_ij = -T_ii Y (terms in
+// ascending order).  At: A transposed (At[i * C + r] = A_ri), 16-byte aligned rows.  T
+// goes to Tout[r * TS + c], zero above the diagonal; Y needs 16 x 16 x (C/16 - 1) floats of
+// scratch.  Every element has one fixed operation sequence, whichever thread computes it.
+// Contains __syncthreads (every thread of the block must call it).
+template <int C, int TS>
+__device__ __forceinline__ void invert_unit_lower(const float* __restrict__ At, float* __restrict__ Tout,
+                                                  float* __restrict__ Y, int tid, int nt)
+{
+    static_assert(C % 16 == 0 && C <= 64, "blocks of 16, at most four");
+    constexpr int NB = C / 16;
+    for (int idx = tid; idx < C * C; idx += nt) Tout[(idx / C) * TS + idx % C] = 0.0f;
+    __syncthreads();
+    if (tid < C) {  // diagonal block k, column j
+        const int k = tid >> 4, j = tid & 15, o = 16 * k;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = (r == j) ? 1.0f : 0.0f;
+#pragma unroll
+            for (int i = 0; i < r; ++i)
+                if (i >= j) acc = __fmaf_rn(-At[(o + i) * C + o + r], x[i], acc);
+            x[r] = r >= j ? acc : 0.0f;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            if (r >= j) Tout[(o + r) * TS + o + j] = x[r];
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int d = 1; d < NB; ++d) {
+        const int nblk = NB - d;
+        for (int idx = tid; idx < nblk * 256; idx += nt) {  // Y of block (j + d, j), element (r, c)
+            const int j = idx >> 8, r = (idx >> 4) & 15, c = idx & 15, i = j + d;
+            float acc = 0.0f;
+            for (int k = j; k < i; ++k) {
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    acc = __fmaf_rn(At[(16 * k + s) * C + 16 * i + r], Tout[(16 * k + s) * TS + 16 * j + c], acc);
+            }
+            Y[idx] = acc;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < nblk * 256; idx += nt) {  // T_ij = -T_ii Y
+            const int j = idx >> 8, r = (idx >> 4) & 15, c = idx & 15, i = j + d;
+            float acc = 0.0f;
+#pragma unroll
+            for (int s = 0; s < 16; ++s)
+                if (s <= r) acc = __fmaf_rn(Tout[(16 * i + r) * TS + 16 * i + s], Y[(j << 8) + (s << 4) + c], acc);
+            Tout[(16 * i + r) * TS + 16 * j + c] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace cpr
