@@ -173,11 +173,11 @@ __device__ __forceinline__ ChunkPos chunk_pos(const int32_t* cu, const int32_t* 
 // The state-independent phase common to kb1 and kb3: per-token vectors (G, gam, d, beta),
 // L = (K K^T) o E (strict lower) into nnL, Pm = (Q K^T) o E (with diagonal) into nnP and
 // T = (I + diag(beta) L)^-1 into nnT (stride NN; nnT first holds A transposed with stride
-// C for the substitution).  Tiles Kt, Qt and g, beta of the chunk's len tokens are loaded
+// C for the inversion, and `scratch` holds C x NN + 256 (C/16 - 1) floats meanwhile).  Tiles Kt, Qt and g, beta of the chunk's len tokens are loaded
 // by the caller (zero tokens beyond len).
 template <int DK, int C, int TK, int NN, typename T>
 __device__ __forceinline__ void chunk_common(const T* Kt, const T* Qt, const float* g_in, Vecs v, float* nnL,
-                                             float* nnP, float* nnT)
+                                             float* nnP, float* nnT, float* scratch)
 {
     using M = NNMap<C>;
     constexpr int TM = M::TM;
@@ -215,17 +215,9 @@ __device__ __forceinline__ void chunk_common(const T* Kt, const T* Qt, const flo
         }
     }
     __syncthreads();
-    float x[C];
-    if (t < C) {
-#pragma unroll
-        for (int r = 0; r < C; ++r) x[r] = (r == t) ? 1.0f : 0.0f;
-        fwd_subst<C>(nnT, x);
-    }
-    __syncthreads();
-    if (t < C) {
-#pragma unroll
-        for (int r = 0; r < C; ++r) nnT[r * NN + t] = x[r];  // T[r][t]
-    }
+    // T by blocks with every thread (numerics.cuh) into the scratch, then into nnT
+    invert_unit_lower<C, NN>(nnT, scratch, scratch + ((C * NN + 3) / 4) * 4, t, kBwdThreads);
+    for (int idx = t; idx < C * C; idx += kBwdThreads) nnT[(idx / C) * NN + idx % C] = scratch[(idx / C) * NN + idx % C];
     __syncthreads();
 }
 
@@ -276,7 +268,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb1_chunk_maps(BackwardArgs a)
         v.beta[t] = t < p.len ? a.beta[(p.t0 + t) * H + h] : 0.0f;
     }
     __syncthreads();
-    chunk_common<DK, C, TK, NN>(Kt, Qt, g_in, v, nnL, nnP, nnT);
+    chunk_common<DK, C, TK, NN>(Kt, Qt, g_in, v, nnL, nnP, nnT, W);  // W's region is free until W
 
     using MK = NDMap<C, DK>;
     {  // W = T diag(beta gam) K
@@ -521,7 +513,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb3_chunk_grads(BackwardArgs a
         v.edrow[t] = 0.0f;
     }
     __syncthreads();
-    chunk_common<DK, C, TK, NN>(Kt, Qt, g_in, v, nL, nP, nT);
+    chunk_common<DK, C, TK, NN>(Kt, Qt, g_in, v, nL, nP, nT, big);  // big is free until step b
 
     using MK = NDMap<C, DK>;  // n x dk tiles (dq, dk)
     using MV = NDMap<C, DV>;  // n x dv tiles (R, U, dU, TdU)

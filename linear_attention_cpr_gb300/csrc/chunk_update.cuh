@@ -177,6 +177,10 @@ struct UCfg {
     // the (D K)^T operand region first holds the key tile of the kk product
     static constexpr uint32_t AOP_REGION = mx(2 * AOP_SPLIT, KKCfg<DK, C, float>::SPAN);
     static constexpr uint32_t VEC_OFF = AOP_OFF + AOP_REGION;
+    // the (D K)^T region also holds T (fp32, row stride C + 1) and the blocked inversion's
+    // scratch while T is computed
+    static_assert((uint32_t)(4 * (((C * (C + 1) + 3) / 4) * 4 + 256 * (C / 16 - 1))) <= AOP_REGION,
+                  "T and its scratch fit the operand region");
     static constexpr uint32_t PREP_BYTES = VEC_OFF + 4 * C * 4;
     static constexpr uint32_t TMEM_COLS = mx(2 * DK, C) <= 32 ? 32 : mx(2 * DK, C) <= 64 ? 64 : mx(2 * DK, C) <= 128 ? 128 : 256;
     // decode resync (prep and one chain step in one CTA): [R1 | Mt] [Aop | Bt] [vectors] [values]
@@ -209,6 +213,24 @@ __device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned
     const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
     if (!chunk_decays_and_A<DK, DV, C, T, KEYS_AS_GIVEN>(s, aop, tmem, mbar, phase & 1)) return false;
     ++phase;
+    // T = (I + A)^-1 by blocks with every thread (numerics.cuh), into the (D K)^T operand's
+    // region, which the key Gram product no longer needs
+    constexpr int TS = C + 1;
+    float* tfull = reinterpret_cast<float*>(aop);
+    invert_unit_lower<C, TS>(s.A, tfull, tfull + ((C * TS + 3) / 4) * 4, tid, nt);
+    // A is dead: its space holds T^T (rows j, K = r), bf16 splits
+    unsigned char* tt = reinterpret_cast<unsigned char*>(s.A);
+    float x[C];
+    if (tid < C) {
+#pragma unroll
+        for (int r = 0; r < C; ++r) x[r] = tfull[r * TS + tid];
+#pragma unroll
+        for (int r0 = 0; r0 < C; r0 += 8) {
+            const uint32_t off = tc::tile_off<2>(tid, r0, C);
+            tc::split8_store(*reinterpret_cast<const float(*)[8]>(x + r0), tt + off, tt + TT_SPLIT + off);
+        }
+    }
+    __syncthreads();  // T is read: its region takes the (D K)^T operand
     // (D K)^T rows c: d_r * k_r[c] (zero rows beyond DK)
     for (int row = tid; row < U::MPAD; row += nt) {
 #pragma unroll
@@ -218,22 +240,6 @@ __device__ __forceinline__ bool prep_operands(const PrepSmem<DK, C>& s, unsigned
             for (int e = 0; e < 8; ++e) xs[e] = row < DK ? __fmul_rn(s.dvs[r0 + e], s.kf[(r0 + e) * KS + row]) : 0.0f;
             const uint32_t off = tc::tile_off<2>(row, r0, C);
             tc::split8_store(xs, aop + off, aop + U::AOP_SPLIT + off);
-        }
-    }
-    // T = (I + A)^-1 by forward substitution, column j by thread j
-    float x[C];
-    if (tid < C) {
-#pragma unroll
-        for (int r = 0; r < C; ++r) x[r] = (r == tid) ? 1.0f : 0.0f;
-        fwd_subst<C>(s.A, x);
-    }
-    __syncthreads();  // A is dead: its space holds T^T (rows j, K = r), bf16 splits
-    unsigned char* tt = reinterpret_cast<unsigned char*>(s.A);
-    if (tid < C) {
-#pragma unroll
-        for (int r0 = 0; r0 < C; r0 += 8) {
-            const uint32_t off = tc::tile_off<2>(tid, r0, C);
-            tc::split8_store(*reinterpret_cast<const float(*)[8]>(x + r0), tt + off, tt + TT_SPLIT + off);
         }
     }
     tc::fence_proxy_async();

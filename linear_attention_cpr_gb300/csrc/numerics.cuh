@@ -28,8 +28,10 @@
 //   kk_ri = sum_j k_r[j] k_i[j]: a tcgen05 product of the keys' bf16 splits, fp32
 //           accumulation (exact products for bf16 keys; hi*hi + hi*lo + lo*hi for fp32)
 //   A_ri  = (beta_r * decay_exp(G_r - G_i)) * kk_ri              (i < r, else 0)
-//   T = (I + A)^-1, column j by substitution: T_rj = [r == j], then fma(-A_ri, T_ij, .)
-//         for i = 0 .. r-1                                          (fwd_subst below)
+//   T = (I + A)^-1 by blocks of 16 (invert_unit_lower below): each diagonal block by
+//         substitution (T_rj = [r == j], then fma(-A_ri, T_ij, .) for i ascending), then the
+//         blocks below the diagonal as T_ij = -T_ii sum_k A_ik T_kj, every sum in a fixed
+//         ascending order
 //   W0_r[c] = (beta_r * e_r) * k_r[c],  U0_r[n] = beta_r * v_r[n]   (W = T W0, U~ = T U0)
 //   then, in matrix form with D = diag(d_r) (chunk_update.cuh):
 //   Z^T = (D K)^T T, M^T = gamma I - Z^T W0, B = U0^T Z:  tcgen05 products (M = 128,
