@@ -38,6 +38,20 @@ int g_profile_n = 0;
 
 }  // namespace
 
+EncodeTiledFn cpr::tensor_map_encoder()
+{
+    static const EncodeTiledFn fn = [] {  // (thread-safe initialisation of a static)
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        const bool found =
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess;
+        return found ? reinterpret_cast<EncodeTiledFn>(p) : static_cast<EncodeTiledFn>(nullptr);
+    }();
+    return fn;
+}
+
 cudaEvent_t cpr::profile_event(int i) { return (i >= 0 && i < g_profile_n) ? g_profile_events[i] : nullptr; }
 
 namespace {

@@ -2,6 +2,7 @@
 // CPR Gated DeltaNet kernels and the C-ABI host code.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -9,6 +10,13 @@
 #include "../../include/cpr_gdn.h"
 
 namespace cpr {
+
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime (the library does
+// not link libcuda); NULL when the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 // Shapes built into the library: X(DK, DV, C).
 #define CPR_FOR_EACH_SHAPE(X) \

@@ -288,32 +288,12 @@ bool on_this_device(const void* p)
 }
 bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The driver's tensor-map encoder, looked up once through the runtime (no link to libcuda;
-// the static's initialisation is thread-safe).
-EncodeTiled encode_tiled()
-{
-    static const EncodeTiled fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        const bool found =
-            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess;
-        return found ? reinterpret_cast<EncodeTiled>(p) : static_cast<EncodeTiled>(nullptr);
-    }();
-    return fn;
-}
-
 // Tensor map of a [rows, K] bf16 matrix whose box is 64 K elements x 128 rows, landing as
 // 128 rows of 128 bytes in the 128-byte swizzle the MMA descriptors read.  Rows past the
 // end read zeros.
 bool box_map(CUtensorMap* m, const void* base, int32_t rows, int32_t K)
 {
-    const EncodeTiled f = encode_tiled();
+    const EncodeTiledFn f = tensor_map_encoder();
     if (!f) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};

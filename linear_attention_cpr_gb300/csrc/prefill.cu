@@ -479,7 +479,62 @@ struct K3Smem {
     static constexpr int NT = DV;  // threads of a group
     // keys and queries (fp32 pairs), values as stored (at most fp32), alpha and beta
     static constexpr size_t bytes = sizeof(float) * ((size_t)2 * C * ROW + (size_t)C * DV + 2 * C);
+    // 2-byte inputs arrive as tensor-map boxes: the key and query tiles as stored ([C][DK])
+    // land in the tails of the key and query regions, and are converted from there
+    static constexpr uint32_t REGION = 4u * C * ROW;  // bytes of the key (or the query) region
+    static constexpr uint32_t RAW = 2u * C * DK;      // bytes of a 2-byte tile
+    static constexpr uint32_t RAW_OFF = REGION - RAW;
+    // the fp32 rows of the first C/2 keys end before the tile begins, so those rows convert
+    // in place in any order; the other rows go through registers
+    static_assert(4u * (C / 2) * ROW <= RAW_OFF, "first half of the rows clear of the tile");
+    static_assert(RAW_OFF % 128 == 0 && REGION % 128 == 0, "tensor-map destinations 128-byte aligned");
+    static constexpr int UNITS = C * DK / 16;  // conversion units of a tile: 8 pairs each
 };
+
+// The tensor maps of the items' boxes (2-byte inputs): keys and queries as [T][Hk][DK],
+// values as [T][H][DV], one box a chunk of one head.
+struct ItemMaps {
+    CUtensorMap k, q, v;
+};
+
+// One conversion unit: pairs [8m, 8m + 8) of half hh of tile row r, i.e. 8 columns from
+// hh*DK/2 + 8m (the pairs' first members) and 8 from hh*DK/2 + DK/4 + 8m (their second).
+template <int DK, typename T>
+__device__ __forceinline__ void unit_read(const T* raw, int u, uint4& x, uint4& y)
+{
+    constexpr int UPR = DK / 16, MH = DK / 32;  // units per row, per half
+    const int r = u / UPR, hh = (u % UPR) / MH, m = u % MH;
+    const T* src = raw + r * DK + hh * (DK / 2) + 8 * m;
+    x = *reinterpret_cast<const uint4*>(src);
+    y = *reinterpret_cast<const uint4*>(src + DK / 4);
+}
+
+template <int DK, int ROW, typename T>
+__device__ __forceinline__ void unit_write(float* region, int u, const uint4& x, const uint4& y)
+{
+    constexpr int UPR = DK / 16, MH = DK / 32;
+    const int r = u / UPR, hh = (u % UPR) / MH, m = u % MH;
+    float4* d = reinterpret_cast<float4*>(region + r * ROW + hh * (DK / 2 + 4) + 16 * m);
+    const T* xe = reinterpret_cast<const T*>(&x);
+    const T* ye = reinterpret_cast<const T*>(&y);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        d[i] = make_float4(to_f32<T>(xe[2 * i]), to_f32<T>(ye[2 * i]), to_f32<T>(xe[2 * i + 1]),
+                           to_f32<T>(ye[2 * i + 1]));
+}
+
+// bar.sync of a named barrier that also returns whether p held in every participating thread.
+__device__ __forceinline__ bool named_bar_all(int id, int nthreads, bool p)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred pi, po;\nsetp.ne.u32 pi, %1, 0;\nbarrier.cta.red.and.pred po, %2, %3, pi;\n"
+        "selp.u32 %0, 1, 0, po;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)p), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 
 template <int DK>
 struct K3Row {
@@ -572,8 +627,10 @@ __device__ __forceinline__ float k3_join(float mine, int half)
     return half == 0 ? __fadd_rn(mine, other) : __fadd_rn(other, mine);
 }
 
+// Returns false when the item's boxes did not land in time (the group then stops).
 template <int DK, int DV, int C, typename T>
-__device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int hd, int tid, float* sm3, int bar)
+__device__ __forceinline__ bool intra_item(const PrefillArgs& a, const ItemMaps& maps, int64_t c, int hd, int tid,
+                                           float* sm3, int bar, uint64_t* tbar, uint32_t& tphase)
 {
     static_assert(DK % 32 == 0 && DV % 32 == 0, "DK and DV must be multiples of 32");
     using S3 = K3Smem<DK, DV, C>;
@@ -594,14 +651,75 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
     const int64_t t0 = tb + j * C;
     const int len = (int)min((int64_t)C, Ls - j * C);
     const int hk = qk_head(hd, H, a.Hk);
-    const T* q = static_cast<const T*>(a.q);
-    const T* k = static_cast<const T*>(a.k);
-    const T* v = static_cast<const T*>(a.v);
     T* out = static_cast<T*>(a.out);
 
-    // stage the chunk: values as they are (16-byte asynchronous copies, converted when
-    // used), keys and queries as fp32 pairs (loads issued a few at a time, then converted)
-    {
+    if constexpr (sizeof(T) == 2) {
+        // stage the chunk: one tensor-map box each for its keys, queries and values (the
+        // values stay as stored and are converted when used); keys and queries are then
+        // converted into fp32 pairs
+        unsigned char* base = reinterpret_cast<unsigned char*>(sm3);
+        const T* rk = reinterpret_cast<const T*>(base + S3::RAW_OFF);
+        const T* rq = reinterpret_cast<const T*>(base + S3::REGION + S3::RAW_OFF);
+        if (tid == 0) {
+            tc::mbar_arrive_expect_tx(tbar, 2 * S3::RAW + 2u * C * DV);
+            tc::tma_load_3d(base + S3::RAW_OFF, &maps.k, 0, hk, (int32_t)t0, tbar);
+            tc::tma_load_3d(base + S3::REGION + S3::RAW_OFF, &maps.q, 0, hk, (int32_t)t0, tbar);
+            tc::tma_load_3d(vs, &maps.v, 0, hd, (int32_t)t0, tbar);
+        }
+        if (tid < len) {
+            al[tid] = decay_exp(a.g[(t0 + tid) * H + hd]);
+            bt[tid] = a.beta[(t0 + tid) * H + hd];
+        }
+        const bool landed = tc::mbar_wait(tbar, tphase);
+        tphase ^= 1u;
+        constexpr int HALF = S3::UNITS / 2;  // units of rows [0, C/2)
+        constexpr int NB = (HALF + NT - 1) / NT;
+        if (landed) {  // rows [0, C/2): straight into their fp32 rows, clear of both tiles
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+                const int u = tid + i * NT;
+                if (u < HALF) {
+                    uint4 x, y;
+                    unit_read<DK, T>(rk, u, x, y);
+                    unit_write<DK, ROW, T>(kp, u, x, y);
+                    unit_read<DK, T>(rq, u, x, y);
+                    unit_write<DK, ROW, T>(qp, u, x, y);
+                }
+            }
+        }
+        // rows [C/2, C): read every unit before any thread writes over the tiles
+        uint4 kx[NB], ky[NB], qx[NB], qy[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int u = HALF + tid + i * NT;
+            if (landed && u < S3::UNITS) {
+                unit_read<DK, T>(rk, u, kx[i], ky[i]);
+                unit_read<DK, T>(rq, u, qx[i], qy[i]);
+            }
+        }
+        if (!named_bar_all(bar, NT, landed)) {
+            // a box still in flight lands (bounded wait) before the group stops
+            if (tid == 0) {
+                atomicOr(a.status, CPR_DEV_TIMEOUT);
+                if (!landed) tc::mbar_wait(tbar, tphase ^ 1u, 1u << 16);
+            }
+            named_bar(bar, NT);
+            return false;
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int u = HALF + tid + i * NT;
+            if (u < S3::UNITS) {
+                unit_write<DK, ROW, T>(kp, u, kx[i], ky[i]);
+                unit_write<DK, ROW, T>(qp, u, qx[i], qy[i]);
+            }
+        }
+    } else {
+        // 4-byte inputs: values by 16-byte asynchronous copies, keys and queries by loads
+        // issued a few at a time, then placed as fp32 pairs
+        const T* q = static_cast<const T*>(a.q);
+        const T* k = static_cast<const T*>(a.k);
+        const T* v = static_cast<const T*>(a.v);
         constexpr int VE = 16 / (int)sizeof(T);
         constexpr int KV = DK / VE, VV = DV / VE;
         constexpr int NK = (C * KV + NT - 1) / NT, NV = (C * VV + NT - 1) / NT;
@@ -640,10 +758,10 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
             }
         }
         tc::cp_async_wait_all();
-    }
-    if (tid < len) {
-        al[tid] = decay_exp(a.g[(t0 + tid) * H + hd]);
-        bt[tid] = a.beta[(t0 + tid) * H + hd];
+        if (tid < len) {
+            al[tid] = decay_exp(a.g[(t0 + tid) * H + hd]);
+            bt[tid] = a.beta[(t0 + tid) * H + hd];
+        }
     }
     if (a.qk_norm) {  // keys and queries L2-normalised in place, one row per thread
         named_bar(bar, NT);
@@ -667,7 +785,7 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
     if (!wait_ok[gi]) {
         if (tid == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
         named_bar(bar, NT);
-        return;
+        return true;
     }
     const int w = tid >> 5, lane = tid & 31, half = lane >> 4;
     const int i0 = w * 16 + (lane & 15), i1 = i0 + DV / 2;
@@ -719,6 +837,7 @@ __device__ __forceinline__ void intra_item(const PrefillArgs& a, int64_t c, int 
         }
     }
     named_bar(bar, NT);  // the group's shared memory is reused by its next item
+    return true;
 }
 
 // ------------------------------------------------------------------------------------
@@ -737,25 +856,36 @@ struct K23Cfg {
 };
 
 template <int DK, int DV, int C, typename T>
-__global__ void __launch_bounds__(K2Cfg<DK, DV>::THREADS, 1) k23_chain_and_intra(PrefillArgs a, int n_chain)
+__global__ void __launch_bounds__(K2Cfg<DK, DV>::THREADS, 1)
+    k23_chain_and_intra(PrefillArgs a, int n_chain, const __grid_constant__ ItemMaps maps)
 {
     using F = K23Cfg<DK, DV, C>;
     constexpr int NT = K3Smem<DK, DV, C>::NT;
     extern __shared__ __align__(1024) unsigned char sm23[];
+    __shared__ uint64_t tile_bar[F::GROUPS];  // each group's boxes landed
+    __shared__ uint32_t claimed[F::GROUPS];
     if (*a.status) return;
+    if (threadIdx.x < F::GROUPS) tc::mbar_init(&tile_bar[threadIdx.x], 1);
+    tc::fence_mbar_init();
+    __syncthreads();
     // chain CTAs join the items once their chains are done
     if ((int)blockIdx.x < n_chain) chain_role<DK, DV, C, T>(a, sm23, blockIdx.x, n_chain);
     const int g = threadIdx.x / NT, gtid = (int)threadIdx.x % NT;
     const uint32_t items = (uint32_t)a.cu_chunks[a.n_seqs] * (uint32_t)a.H;
     uint32_t* next_item = a.ready + (size_t)a.max_chunks * a.H;
-    __shared__ uint32_t claimed[F::GROUPS];
     float* smg = reinterpret_cast<float*>(sm23 + g * F::GROUP_BYTES);
+    uint32_t tphase = 0;
     for (;;) {  // items are claimed in chunk order, one group at a time
+        // this thread's shared-memory accesses (the last item's, or the chain's) come before
+        // the boxes the next item's copies write
+        tc::fence_proxy_async();
         if (gtid == 0) claimed[g] = atomicAdd(next_item, 1u);
         named_bar(1 + g, NT);
         const uint32_t t = claimed[g];
         if (t >= items) break;
-        intra_item<DK, DV, C, T>(a, t / a.H, (int)(t % a.H), gtid, smg, 1 + g);  // ends with a group barrier
+        // (ends with a group barrier)
+        if (!intra_item<DK, DV, C, T>(a, maps, t / a.H, (int)(t % a.H), gtid, smg, 1 + g, &tile_bar[g], tphase))
+            break;
     }
 }
 
@@ -801,6 +931,24 @@ cudaError_t launch_chunk_prep(const PrefillArgs& a, cudaStream_t s)
     return cudaGetLastError();
 }
 
+// The items' tensor maps for 2-byte inputs: keys and queries [T][Hk][DK], values
+// [T][H][DV], each box one chunk of C rows of one head (rows past the last token read zeros).
+template <int DK, int DV, int C>
+bool item_maps(ItemMaps* m, const PrefillArgs& a, int es)
+{
+    const EncodeTiledFn f = tensor_map_encoder();
+    if (!f || es != 2 || a.total_tokens < 1 || a.total_tokens > 0x7fffffff) return false;
+    auto enc = [&](CUtensorMap* map, const void* base, int d, int heads) {
+        const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)a.total_tokens};
+        const cuuint64_t strides[2] = {(cuuint64_t)d * es, (cuuint64_t)heads * d * es};
+        const cuuint32_t box[3] = {(cuuint32_t)d, 1, (cuuint32_t)C}, estr[3] = {1, 1, 1};
+        return f(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    return enc(&m->k, a.k, DK, a.Hk) && enc(&m->q, a.q, DK, a.Hk) && enc(&m->v, a.v, DV, a.H);
+}
+
 template <int DK, int DV, int C, typename T>
 cudaError_t launch_chain_and_intra(const PrefillArgs& a, cudaStream_t s)
 {
@@ -819,7 +967,10 @@ cudaError_t launch_chain_and_intra(const PrefillArgs& a, cudaStream_t s)
     const int n_chain = std::max(1, std::min(chains, grid / 4));
     PrefillArgs args = a;
     int nc = n_chain;
-    void* params[] = {&args, &nc};
+    ItemMaps maps{};
+    // (no tokens: no items, and the maps stay unused)
+    if (sizeof(T) == 2 && a.total_tokens > 0 && !item_maps<DK, DV, C>(&maps, a, 2)) return cudaErrorInvalidValue;
+    void* params[] = {&args, &nc, &maps};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cf::THREADS), params, sm23,
                                        s);
 }

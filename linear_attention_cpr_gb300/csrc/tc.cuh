@@ -116,6 +116,20 @@ __device__ __forceinline__ void bulk_g2s(void* smem, const void* gmem, uint32_t 
         : "memory");
 }
 
+// One box of a 3-dimensional tensor map (a CUtensorMap in kernel-parameter, constant or
+// global memory) at coordinates (x, y, z) into this CTA's shared memory (128-byte aligned),
+// completing its bytes on mbar.  x times the element size must be a multiple of 16 bytes;
+// elements outside the tensor land as zeros and still count towards the bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int32_t x, int32_t y, int32_t z,
+                                            uint64_t* mbar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(mbar))
+        : "memory");
+}
+
 // Prefetch `bytes` (a multiple of 16, address 16-byte aligned) of global memory into L2
 // (no completion to wait for: a hint that a later copy of the same bytes hits in L2).
 __device__ __forceinline__ void prefetch_l2(const void* gmem, uint32_t bytes)
