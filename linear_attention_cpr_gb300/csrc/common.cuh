@@ -18,6 +18,15 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn tensor_map_encoder();
 
+// Tensor maps of a call's 2-byte (bf16) inputs for chunk boxes: keys and queries as
+// [T][Hk][dk], values as [T][H][dv]; one box is C consecutive tokens of one head (rows past
+// the last token read zeros).  False if the encoder is missing or refuses the layout.
+struct ChunkMaps {
+    CUtensorMap k, q, v;
+};
+bool chunk_maps(ChunkMaps* m, const void* q, const void* k, const void* v, int64_t total_tokens, int32_t H,
+                int32_t Hk, int32_t dk, int32_t dv, int32_t C);
+
 // Shapes built into the library: X(DK, DV, C).
 #define CPR_FOR_EACH_SHAPE(X) \
     X(32, 32, 16)             \

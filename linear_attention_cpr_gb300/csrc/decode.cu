@@ -235,19 +235,27 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 // sequence's first skip[n] tokens (those that fill the chunk it is in, from position
 // pos0[n]) are stepped one after another by k4's token step on the state held in
 // registers; each token goes to its ring slot and its output to `out`.  The stepped state
-// is written back; when the chunk completes, the resync (k5) then replaces it.
+// is written back; when the chunk completes, the resync (k5) then replaces it.  2-byte
+// inputs arrive up front as one tensor-map box each for the keys, queries and values of
+// the sequence's first C tokens (with g and beta by plain loads), so the steps read only
+// shared memory; 4-byte inputs are loaded token by token.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C, typename T>
 __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t* __restrict__ cu_seqlens,
                                                      const int32_t* __restrict__ pos0,
-                                                     const int32_t* __restrict__ skip)
+                                                     const int32_t* __restrict__ skip,
+                                                     const __grid_constant__ ChunkMaps maps)
 {
     constexpr int L = DK / 8, VPT = DV / 32;
+    constexpr bool kBoxes = sizeof(T) == 2;
     __shared__ __align__(16) float kf[DK];
     __shared__ __align__(16) float qf[DK];
     __shared__ __align__(16) float part[8][DV];
     __shared__ __align__(16) float part2[8][DV];
     __shared__ float sc[4];
+    __shared__ float sg[C], sbeta[C];
+    __shared__ uint64_t tile_bar;
+    extern __shared__ __align__(128) unsigned char sm8[];  // (2-byte inputs) keys, queries, values [C][d]
 
     const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = a.H;
     const int m = tid >> 5, lane = tid & 31;
@@ -255,39 +263,88 @@ __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t
     if (*a.status || f <= 0) return;
     const int r0 = pos0[n] % C;
     const size_t nh = (size_t)n * H + h;
+    const int hk = qk_head(h, H, a.Hk);
+    const int64_t t0 = cu_seqlens[n];
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
     T* out = static_cast<T*>(a.out);
     T* rk = static_cast<T*>(a.ring.k);
     T* rv = static_cast<T*>(a.ring.v);
+    T* sk = reinterpret_cast<T*>(sm8);
+    T* sq = sk + C * DK;
+    T* sv = sq + C * DK;
 
+    if constexpr (kBoxes) {
+        if (tid == 0) {
+            tc::mbar_init(&tile_bar, 1);
+            tc::fence_mbar_init();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            tc::mbar_arrive_expect_tx(&tile_bar, (uint32_t)(2 * DK + DV) * C * 2);
+            tc::tma_load_3d(sk, &maps.k, 0, hk, (int32_t)t0, &tile_bar);
+            tc::tma_load_3d(sq, &maps.q, 0, hk, (int32_t)t0, &tile_bar);
+            tc::tma_load_3d(sv, &maps.v, 0, h, (int32_t)t0, &tile_bar);
+        }
+        if (tid < f) {
+            sg[tid] = a.g[(t0 + tid) * H + h];
+            sbeta[tid] = a.beta[(t0 + tid) * H + h];
+        }
+    }
     float s[L][VPT];
     float* st = a.state + nh * DK * DV + (size_t)(m * L) * DV + lane * VPT;
 #pragma unroll
     for (int t = 0; t < L; ++t) VecF<VPT>::load(st + (size_t)t * DV, s[t]);
-    for (int t = 0; t < f; ++t) {
-        const size_t tok = ((size_t)cu_seqlens[n] + t) * H + h;  // packed token index x H + h
-        const size_t tokk = ((size_t)cu_seqlens[n] + t) * a.Hk + qk_head(h, H, a.Hk);
-        const int r = r0 + t;                                    // its ring slot
-        for (int idx = tid; idx < DK; idx += 256) {
-            const T kk = k[tokk * DK + idx];
-            kf[idx] = to_f32<T>(kk);
-            qf[idx] = to_f32<T>(q[tokk * DK + idx]);
-            rk[(nh * C + r) * DK + idx] = kk;
+    if constexpr (kBoxes) {
+        const bool landed = tc::mbar_wait(&tile_bar, 0);
+        if (!__syncthreads_and(landed)) {  // (the boxes land, bounded, before the CTA leaves)
+            if (tid == 0) {
+                atomicOr(a.status, CPR_DEV_TIMEOUT);
+                if (!landed) tc::mbar_wait(&tile_bar, 0, 1u << 16);
+            }
+            return;
         }
-        for (int idx = tid; idx < DV; idx += 256) rv[(nh * C + r) * DV + idx] = v[tok * DV + idx];
-        if (tid == 0) {
-            const float gg = a.g[tok], bb = a.beta[tok];
-            sc[0] = decay_exp(gg);
-            sc[1] = bb;
-            a.ring.g[nh * C + r] = gg;
-            a.ring.beta[nh * C + r] = bb;
+    }
+    for (int t = 0; t < f; ++t) {
+        const size_t tok = ((size_t)t0 + t) * H + h;  // packed token index x H + h
+        const int r = r0 + t;                          // its ring slot
+        if constexpr (kBoxes) {
+            for (int idx = tid; idx < DK; idx += 256) {
+                const T kk = sk[t * DK + idx];
+                kf[idx] = to_f32<T>(kk);
+                qf[idx] = to_f32<T>(sq[t * DK + idx]);
+                rk[(nh * C + r) * DK + idx] = kk;
+            }
+            for (int idx = tid; idx < DV; idx += 256) rv[(nh * C + r) * DV + idx] = sv[t * DV + idx];
+            if (tid == 0) {
+                const float gg = sg[t], bb = sbeta[t];
+                sc[0] = decay_exp(gg);
+                sc[1] = bb;
+                a.ring.g[nh * C + r] = gg;
+                a.ring.beta[nh * C + r] = bb;
+            }
+        } else {
+            const size_t tokk = ((size_t)t0 + t) * a.Hk + hk;
+            for (int idx = tid; idx < DK; idx += 256) {
+                const T kk = k[tokk * DK + idx];
+                kf[idx] = to_f32<T>(kk);
+                qf[idx] = to_f32<T>(q[tokk * DK + idx]);
+                rk[(nh * C + r) * DK + idx] = kk;
+            }
+            for (int idx = tid; idx < DV; idx += 256) rv[(nh * C + r) * DV + idx] = v[tok * DV + idx];
+            if (tid == 0) {
+                const float gg = a.g[tok], bb = a.beta[tok];
+                sc[0] = decay_exp(gg);
+                sc[1] = bb;
+                a.ring.g[nh * C + r] = gg;
+                a.ring.beta[nh * C + r] = bb;
+            }
         }
         __syncthreads();
         if (a.qk_norm) l2_normalise_qk<DK>(kf, qf, sc + 2);
-        token_step<DK, DV, T>(s, kf, qf, part, part2, sc[0], sc[1], v + tok * DV, out + tok * DV,
-                              t + 1 == f ? st : nullptr);
+        token_step<DK, DV, T>(s, kf, qf, part, part2, sc[0], sc[1], kBoxes ? sv + t * DV : v + tok * DV,
+                              out + tok * DV, t + 1 == f ? st : nullptr);
         __syncthreads();  // kf, qf, sc and the partial sums are rewritten for the next token
     }
 }
@@ -657,7 +714,16 @@ cudaError_t launch_prefill_continue(const PrefillArgs& a, const int32_t* pos0, f
     std::lock_guard<std::mutex> turn(ss->use);
     if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(ss->stream, ss->fork, 0)) != cudaSuccess) return e;
-    k8_chunk_fill<DK, DV, C, T><<<dim3((unsigned)a.n_seqs, a.H), 256, 0, ss->stream>>>(d, a.cu_seqlens, pos0, skip);
+    ChunkMaps maps{};
+    size_t sm8 = 0;
+    if (sizeof(T) == 2 && a.total_tokens > 0) {
+        if (!chunk_maps(&maps, a.q, a.k, a.v, a.total_tokens, a.H, a.Hk, DK, DV, C)) return cudaErrorInvalidValue;
+        sm8 = (size_t)(2 * DK + DV) * C * sizeof(T);
+        e = cudaFuncSetAttribute(k8_chunk_fill<DK, DV, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm8);
+        if (e != cudaSuccess) return e;
+    }
+    k8_chunk_fill<DK, DV, C, T>
+        <<<dim3((unsigned)a.n_seqs, a.H), 256, sm8, ss->stream>>>(d, a.cu_seqlens, pos0, skip, maps);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t sm5 = std::max<size_t>(UCfg<DK, DV, C>::rs_bytes(sizeof(T)), tmem_cap_smem(UCfg<DK, DV, C>::TMEM_COLS));
     auto k5 = d.qk_norm ? k5_resync<DK, DV, C, T, true> : k5_resync<DK, DV, C, T, false>;

@@ -491,12 +491,6 @@ struct K3Smem {
     static constexpr int UNITS = C * DK / 16;  // conversion units of a tile: 8 pairs each
 };
 
-// The tensor maps of the items' boxes (2-byte inputs): keys and queries as [T][Hk][DK],
-// values as [T][H][DV], one box a chunk of one head.
-struct ItemMaps {
-    CUtensorMap k, q, v;
-};
-
 // One conversion unit: pairs [8m, 8m + 8) of half hh of tile row r, i.e. 8 columns from
 // hh*DK/2 + 8m (the pairs' first members) and 8 from hh*DK/2 + DK/4 + 8m (their second).
 template <int DK, typename T>
@@ -629,7 +623,7 @@ __device__ __forceinline__ float k3_join(float mine, int half)
 
 // Returns false when the item's boxes did not land in time (the group then stops).
 template <int DK, int DV, int C, typename T>
-__device__ __forceinline__ bool intra_item(const PrefillArgs& a, const ItemMaps& maps, int64_t c, int hd, int tid,
+__device__ __forceinline__ bool intra_item(const PrefillArgs& a, const ChunkMaps& maps, int64_t c, int hd, int tid,
                                            float* sm3, int bar, uint64_t* tbar, uint32_t& tphase)
 {
     static_assert(DK % 32 == 0 && DV % 32 == 0, "DK and DV must be multiples of 32");
@@ -857,7 +851,7 @@ struct K23Cfg {
 
 template <int DK, int DV, int C, typename T>
 __global__ void __launch_bounds__(K2Cfg<DK, DV>::THREADS, 1)
-    k23_chain_and_intra(PrefillArgs a, int n_chain, const __grid_constant__ ItemMaps maps)
+    k23_chain_and_intra(PrefillArgs a, int n_chain, const __grid_constant__ ChunkMaps maps)
 {
     using F = K23Cfg<DK, DV, C>;
     constexpr int NT = K3Smem<DK, DV, C>::NT;
@@ -931,22 +925,21 @@ cudaError_t launch_chunk_prep(const PrefillArgs& a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-// The items' tensor maps for 2-byte inputs: keys and queries [T][Hk][DK], values
-// [T][H][DV], each box one chunk of C rows of one head (rows past the last token read zeros).
-template <int DK, int DV, int C>
-bool item_maps(ItemMaps* m, const PrefillArgs& a, int es)
+bool chunk_maps(ChunkMaps* m, const void* q, const void* k, const void* v, int64_t total_tokens, int32_t H,
+                int32_t Hk, int32_t dk, int32_t dv, int32_t C)
 {
     const EncodeTiledFn f = tensor_map_encoder();
-    if (!f || es != 2 || a.total_tokens < 1 || a.total_tokens > 0x7fffffff) return false;
+    if (!f || total_tokens < 1 || total_tokens > 0x7fffffff || C < 1 || C > 256) return false;
     auto enc = [&](CUtensorMap* map, const void* base, int d, int heads) {
-        const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)a.total_tokens};
-        const cuuint64_t strides[2] = {(cuuint64_t)d * es, (cuuint64_t)heads * d * es};
+        if (d < 8 || d > 256 || d % 8 != 0 || ((uintptr_t)base & 15u)) return false;
+        const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)total_tokens};
+        const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
         const cuuint32_t box[3] = {(cuuint32_t)d, 1, (cuuint32_t)C}, estr[3] = {1, 1, 1};
         return f(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    return enc(&m->k, a.k, DK, a.Hk) && enc(&m->q, a.q, DK, a.Hk) && enc(&m->v, a.v, DV, a.H);
+    return enc(&m->k, k, dk, Hk) && enc(&m->q, q, dk, Hk) && enc(&m->v, v, dv, H);
 }
 
 template <int DK, int DV, int C, typename T>
@@ -964,12 +957,14 @@ cudaError_t launch_chain_and_intra(const PrefillArgs& a, cudaStream_t s)
     if (per_sm < 1 || a.num_sms < 2) return cudaErrorInvalidConfiguration;
     const int grid = per_sm * a.num_sms;
     const int chains = a.n_seqs * a.H;
-    const int n_chain = std::max(1, std::min(chains, grid / 4));
+    const int n_chain = std::max(1, std::min(chains, grid / 2));
     PrefillArgs args = a;
     int nc = n_chain;
-    ItemMaps maps{};
+    ChunkMaps maps{};
     // (no tokens: no items, and the maps stay unused)
-    if (sizeof(T) == 2 && a.total_tokens > 0 && !item_maps<DK, DV, C>(&maps, a, 2)) return cudaErrorInvalidValue;
+    if (sizeof(T) == 2 && a.total_tokens > 0 &&
+        !chunk_maps(&maps, a.q, a.k, a.v, a.total_tokens, a.H, a.Hk, DK, DV, C))
+        return cudaErrorInvalidValue;
     void* params[] = {&args, &nc, &maps};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cf::THREADS), params, sm23,
                                        s);
