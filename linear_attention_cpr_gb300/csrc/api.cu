@@ -178,7 +178,7 @@ int32_t cpr_gdn_backward(const void* q, const void* k, const void* v, const floa
     a.status = reinterpret_cast<uint32_t*>(ws);
     a.ready = reinterpret_cast<uint32_t*>(ws + 4);
     a.cu_chunks = reinterpret_cast<int32_t*>(ws + lay.cu_chunks);
-    a.mt = reinterpret_cast<float*>(ws + lay.mt);
+    a.mt = ws + lay.mt;
     a.cb = reinterpret_cast<float*>(ws + lay.cb);
     a.d_end = reinterpret_cast<float*>(ws + lay.d_end);
     a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);

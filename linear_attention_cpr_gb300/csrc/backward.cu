@@ -19,21 +19,23 @@
 // Qt = diag(gam) Q - Pm W (row t of Qt is the query carried back through the chunk's
 // first t token transitions).  Three kernels:
 //   kb1_chunk_maps      per (chunk, head): M^T and C_b = dO^T Qt (state-independent)
-//   kb2_reverse_chain   per (sequence, head, slice of value rows): dS at every chunk end,
-//                       from the last chunk back to the first; dS_0 is d_state_in
+//   kb2_reverse_chain   per (sequence, head): dS at every chunk end, from the last chunk
+//                       back to the first, one tensor-core product per chunk (the forward
+//                       chain's routines); dS_0 is d_state_in
 //   kb3_chunk_grads     per (chunk, head): the chunk's adjoint in WY form from S_b (the
 //                       forward's boundary state) and dS_end (the chain's), giving dq, dk,
 //                       dv, dg, dbeta of its tokens
 // A final partial chunk is evaluated as a full one with zero tokens appended (k = q = v =
 // dO = 0, g = 0, beta = 0): such tokens are identity maps, so the chunk's function of its
 // real tokens, and hence every gradient of them, is unchanged.
-// All arithmetic is fp32 on the FMA pipe in a fixed order (no atomics), so the gradients
-// are reproducible from run to run and do not depend on how the batch is packed.
+// Every reduction runs in a fixed order (no atomics), so the gradients are reproducible
+// from run to run and do not depend on how the batch is packed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <type_traits>
 
+#include "chunk_update.cuh"
 #include "common.cuh"
 #include "numerics.cuh"
 #include "tc.cuh"
@@ -225,7 +227,9 @@ __device__ __forceinline__ void chunk_common(const T* Kt, const T* Qt, const flo
 // kb1: per (chunk, head) the reverse chain's coefficients:
 //   W   = T diag(beta gam) K                                      (n x dk)
 //   Qt  = diag(gam) Q - Pm W                                       (n x dk)
-//   M^T = gam_last I - (diag(d) K)^T W   stored [c'][c] = M[c][c'] (dk x dk)
+//   M   = gam_last I - W^T diag(d) K     stored as the reverse chain's B operand: the
+//         product dS_end M^T reads M[c][c'] at (N = c, K = c'), as bf16 hi / lo splits in
+//         K-major core matrices
 //   C_b = dO^T Qt                        stored [c][i] = C_b[i][c] (like a state)
 // ------------------------------------------------------------------------------------
 template <int DK, int DV, int C, typename T>
@@ -300,20 +304,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb1_chunk_maps(BackwardArgs a)
     }
     __syncthreads();
     const size_t ch = (size_t)c * H + h;
-    {  // M^T[c'][c] = gam_last [c' == c] - sum_r d_r K[r][c'] W[r][c]
+    {  // M[c][c'] = gam_last [c' == c] - sum_r d_r K[r][c'] W[r][c]
         constexpr int TM = DK / 16, TN = DK / 16;
+        constexpr uint32_t SPLIT = DK * DK * 2;
         float m[TM][TN];
         zero(m);
-        const int r0 = (t >> 4) * TM, cg = t & 15;  // rows r0 + i, columns 16 j + cg
+        const int r0 = (t >> 4) * TM, cg = t & 15;  // rows c' = r0 + i, columns c = 16 j + cg
         mm<TM, TN, C>(m, [&](int i, int k) { return __fmul_rn(v.dd[k], ld_f32(Kt + k * TK + r0 + i)); },
                       [&](int k, int j) { return W[k * ND + 16 * j + cg]; });
-        float* dst = a.mt + ch * DK * DK;
+        unsigned char* img = a.mt + ch * 2 * SPLIT;
         const float gl = v.gam[C - 1];
+        // the thread's TM values of column c are TM consecutive K elements of one core-matrix
+        // row (TM divides 8): stored as 32-bit words of bf16 pairs
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+        for (int j = 0; j < TN; ++j) {
+            const int cc = 16 * j + cg;
+            uint32_t hw[TM / 2], lw[TM / 2];
 #pragma unroll
-            for (int j = 0; j < TN; ++j)
-                dst[(size_t)(r0 + i) * DK + 16 * j + cg] = (r0 + i == 16 * j + cg) ? __fsub_rn(gl, m[i][j]) : -m[i][j];
+            for (int i = 0; i < TM; i += 2) {
+                float h0, l0, h1, l1;
+                tc::split_f32((r0 + i == cc) ? __fsub_rn(gl, m[i][j]) : -m[i][j], h0, l0);
+                tc::split_f32((r0 + i + 1 == cc) ? __fsub_rn(gl, m[i + 1][j]) : -m[i + 1][j], h1, l1);
+                hw[i / 2] = tc::pack_upper(h0, h1);
+                lw[i / 2] = tc::pack_upper(l0, l1);
+            }
+            const uint32_t off = tc::tile_off<2>(cc, r0, DK);
+            uint32_t* hd = reinterpret_cast<uint32_t*>(img + off);
+            uint32_t* ld = reinterpret_cast<uint32_t*>(img + SPLIT + off);
+            if constexpr (TM == 8) {
+                *reinterpret_cast<uint4*>(hd) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(ld) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < TM / 2; ++e) {
+                    hd[e] = hw[e];
+                    ld[e] = lw[e];
+                }
+            }
+        }
     }
     {  // C_b stored [c][i] = sum_t Qt[t][c] dO[t][i]
         constexpr int TM = DK / 16, TN = DV / 16;
@@ -331,114 +359,114 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb1_chunk_maps(BackwardArgs a)
 }
 
 // ------------------------------------------------------------------------------------
-// kb2: the reverse chain of one (sequence, head) over a slice of RS value rows (rows are
-// independent: dS_b[i][:] = dS_end[i][:] M^T + C_b[i][:]).  For j = last .. 0 it stores
-// dS (the adjoint at chunk j's end) into d_end[j], then steps it to chunk j's start.  The
-// start value is d_state_out (zero if absent); the end value is d_state_in.  Chunk j-1's
-// M^T and the slice's rows of C_{j-1} stream into shared memory (16-byte asynchronous
-// copies) while step j runs.
+// kb2: the reverse chain of one (sequence, head), by a CTA of 8 warps.  For j = last .. 0
+// it stores dS (the adjoint at chunk j's end) into d_end[j], then steps it to chunk j's
+// start, dS_b = dS_end M_j^T + C_j, by the forward chain's routines: dS as the A operand
+// in TMEM (bf16 hi / lo, value row i in lane i), chunk j's M image (kb1) as B, three
+// tcgen05 products hi*hi + hi*lo + lo*hi accumulated in fp32, C_j added in the epilogue.
+// The images come by bulk copies two chunks deep; each chunk's C_j loads and d_end stores
+// run while its product does.  The start value is d_state_out (zero if absent); the end
+// value is d_state_in.  Every wait is bounded; a timeout ends the chain with the status
+// word set.
 // ------------------------------------------------------------------------------------
 template <int DK, int DV>
 struct Kb2Cfg {
-    static constexpr int RS = (1024 / DK > 16 ? 1024 / DK : 16) < DV ? (1024 / DK > 16 ? 1024 / DK : 16) : DV;
-    static constexpr int NCG = DK / 4;                 // column groups of 4
-    static constexpr int RPT = RS * NCG / kBwdThreads;  // rows per thread
-    static_assert(RPT >= 1 && RS * NCG == RPT * kBwdThreads, "slice covers the thread grid");
-    static constexpr int SS = DK + 4;                  // slice row stride (16-byte rows)
-    static constexpr size_t MT_BYTES = (size_t)DK * DK * 4;
-    static constexpr size_t CB_BYTES = (size_t)DK * RS * 4;  // the slice's columns of one C_b
-    static constexpr size_t bytes = 2 * MT_BYTES + 2 * CB_BYTES + 2 * (size_t)RS * SS * 4;
+    static constexpr int NW = kBwdThreads / 32;
+    static constexpr uint32_t IMG = 2u * DK * DK * 2;  // one chunk's M image (bf16 hi, lo)
+    static constexpr uint32_t PIECE = 16384;
+    static constexpr uint32_t BAR_OFF = 2 * IMG;       // two stages
+    static constexpr size_t bytes = BAR_OFF + 64;
+    // TMEM: the accumulator in columns [0, DK), the A operand in [DK, 2 DK)
+    static constexpr uint32_t TMEM_COLS = 2 * DK <= 64 ? 64 : 2 * DK <= 128 ? 128 : 256;
 };
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(kBwdThreads, 1) kb2_reverse_chain(BackwardArgs a)
 {
     using F = Kb2Cfg<DK, DV>;
-    constexpr int RS = F::RS, SS = F::SS, RPT = F::RPT;
-    extern __shared__ __align__(16) unsigned char smc[];
-    float* mts = reinterpret_cast<float*>(smc);                          // [2][DK][DK]
-    float* cbs = reinterpret_cast<float*>(smc + 2 * F::MT_BYTES);        // [2][DK][RS]
-    float* sl = reinterpret_cast<float*>(smc + 2 * F::MT_BYTES + 2 * F::CB_BYTES);  // [2][RS][SS]
-    constexpr int NSL = DV / RS;
-    const int unit = blockIdx.x, slice = unit % NSL, nh = unit / NSL;
-    const int n = nh / a.H, h = nh % a.H, t = threadIdx.x;
+    using Mp = ChainMap<DK, F::NW>;
+    extern __shared__ __align__(1024) unsigned char smc[];
+    uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(smc + F::BAR_OFF);  // [2] stage landed
+    uint64_t* mbar_mma = mbar_ld + 2;                                   // product done
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_mma + 1);
+    volatile int* ok_s = reinterpret_cast<volatile int*>(tslot + 1);     // thread 0's wait results
+
+    const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H, t = threadIdx.x, warp = t >> 5;
     if (*a.status || n >= a.n_seqs) return;
-    const int i0 = slice * RS;
     const int64_t cb = a.cu_chunks[n], nch = (int64_t)a.cu_chunks[n + 1] - cb;
     const size_t SSZ = (size_t)DK * DV;
-    const float* ds_out = a.d_state_out ? a.d_state_out + ((size_t)n * a.H + h) * SSZ : nullptr;
-    // the slice of dS: sl[ii][c] = dS[i0 + ii][c], stored [c][i] in global memory
-    for (int idx = t; idx < RS * DK; idx += kBwdThreads) {
-        const int cc = idx / RS, ii = idx % RS;
-        sl[ii * SS + cc] = ds_out ? ds_out[(size_t)cc * DV + i0 + ii] : 0.0f;
+    const float* ds_out = a.d_state_out ? a.d_state_out + (size_t)nh * SSZ : nullptr;
+    float v[Mp::CPT];
+    chain_load_state<DK, DV, F::NW>(ds_out, t, v);
+    if (nch == 0) {  // no chunk: d_state_in = d_state_out
+        if (a.d_state_in) chain_store<DK, DV, F::NW>(a.d_state_in + (size_t)nh * SSZ, t, v);
+        return;
     }
-    auto fetch_mt = [&](int64_t j, int buf) {
-        const float4* src = reinterpret_cast<const float4*>(a.mt + ((size_t)(cb + j) * a.H + h) * DK * DK);
-        float4* dst = reinterpret_cast<float4*>(mts + (size_t)buf * DK * DK);
-        for (int q = t; q < DK * DK / 4; q += kBwdThreads) tc::cp_async16(dst + q, src + q);
-    };
-    auto fetch_cb = [&](int64_t j, int buf) {  // rows c of C_b, columns [i0, i0 + RS)
-        const float* src = a.cb + ((size_t)(cb + j) * a.H + h) * SSZ + i0;
-        float* dst = cbs + (size_t)buf * DK * RS;
-        constexpr int Q = RS / 4;  // 16-byte pieces per row
-        for (int q = t; q < DK * Q; q += kBwdThreads)
-            tc::cp_async16(dst + (q / Q) * RS + (q % Q) * 4, src + (size_t)(q / Q) * DV + (q % Q) * 4);
-    };
-    if (nch > 0) {
-        fetch_mt(nch - 1, (int)((nch - 1) & 1));
-        fetch_cb(nch - 1, (int)((nch - 1) & 1));
+    if (warp == 0) tc::tmem_alloc(tslot, F::TMEM_COLS);
+    if (t == 0) {
+        tc::mbar_init(&mbar_ld[0], 1);
+        tc::mbar_init(&mbar_ld[1], 1);
+        tc::mbar_init(mbar_mma, 1);
+        tc::fence_mbar_init();
     }
-    const int c0 = (t % F::NCG) * 4, r0 = (t / F::NCG) * RPT;
-    int cur = 0;
-    for (int64_t j = nch - 1; j >= 0; --j) {
-        tc::cp_async_wait_all();
-        __syncthreads();  // M^T of chunk j and the slice are in shared memory
-        if (j > 0) {
-            fetch_mt(j - 1, (int)((j - 1) & 1));
-            fetch_cb(j - 1, (int)((j - 1) & 1));
-        }
-        const float* mt = mts + (size_t)(j & 1) * DK * DK;
-        const float* s = sl + cur * RS * SS;
-        float* dend = a.d_end + ((size_t)(cb + j) * a.H + h) * SSZ;
-        for (int idx = t; idx < RS * DK; idx += kBwdThreads) {
-            const int cc = idx / RS, ii = idx % RS;
-            dend[(size_t)cc * DV + i0 + ii] = s[ii * SS + cc];
-        }
-        const float* cbj = cbs + (size_t)(j & 1) * DK * RS;  // [c][ii]
-        float acc[RPT][4];
-#pragma unroll
-        for (int r = 0; r < RPT; ++r)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[r][e] = 0.0f;
-#pragma unroll 4
-        for (int k = 0; k < DK; ++k) {
-            const float4 m4 = *reinterpret_cast<const float4*>(mt + (size_t)k * DK + c0);
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                const float x = s[(r0 + r) * SS + k];
-                acc[r][0] = __fmaf_rn(x, m4.x, acc[r][0]);
-                acc[r][1] = __fmaf_rn(x, m4.y, acc[r][1]);
-                acc[r][2] = __fmaf_rn(x, m4.z, acc[r][2]);
-                acc[r][3] = __fmaf_rn(x, m4.w, acc[r][3]);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    int64_t issued = 0;    // (thread 0) image copies issued, step jj into stage jj & 1
+    int64_t products = 0;  // (thread 0) products issued
+    auto issue = [&]() {
+        const int64_t jj = issued++, j = nch - 1 - jj;
+        const unsigned char* src = a.mt + ((size_t)(cb + j) * a.H + h) * F::IMG;
+        unsigned char* dst = smc + (jj & 1) * F::IMG;
+        tc::mbar_arrive_expect_tx(&mbar_ld[jj & 1], F::IMG);
+        for (uint32_t off = 0; off < F::IMG; off += F::PIECE)
+            tc::bulk_g2s(dst + off, src + off, min(F::PIECE, F::IMG - off), &mbar_ld[jj & 1]);
+    };
+    if (t == 0) {
+        issue();
+        if (nch > 1) issue();
+    }
+    chain_put_a<DK, F::NW>(tmem + DK, t, v);
+    tc::fence_before_sync();
+    __syncthreads();
+    bool ok = true;
+    for (int64_t jj = 0; jj < nch; ++jj) {
+        const size_t ch = (size_t)(cb + nch - 1 - jj) * a.H + h;
+        bool issued_ok = true;
+        if (t == 0) {
+            issued_ok = tc::mbar_wait(&mbar_ld[jj & 1], (uint32_t)((jj >> 1) & 1));
+            if (issued_ok) {
+                chain_mma<DK>(tmem, tmem + DK, smc + (jj & 1) * F::IMG, mbar_mma);
+                ++products;
             }
         }
-        float* o = sl + (cur ^ 1) * RS * SS;
-#pragma unroll
-        for (int r = 0; r < RPT; ++r)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                o[(r0 + r) * SS + c0 + e] = __fadd_rn(acc[r][e], cbj[(c0 + e) * RS + r0 + r]);
-        cur ^= 1;
+        chain_store<DK, DV, F::NW>(a.d_end + ch * SSZ, t, v);  // dS at the chunk's end
+        float b[Mp::CPT];
+        chain_load_b<DK, DV, F::NW>(a.cb + ch * SSZ, t, b);
+        if (t == 0) ok_s[0] = (issued_ok && tc::mbar_wait(mbar_mma, (uint32_t)(jj & 1))) ? 1 : 0;
+        __syncthreads();
+        ok = ok_s[0] != 0;
+        if (!ok) break;
+        tc::fence_after_sync();
+        if (t == 0 && issued < nch) issue();  // the product is done: its stage is free
+        chain_values_reg<DK, F::NW>(tmem, t, b, v);
+        if (jj + 1 < nch) chain_put_a<DK, F::NW>(tmem + DK, t, v);
+        tc::fence_before_sync();
+        __syncthreads();  // (every thread has read ok_s)
     }
+    if (ok) {
+        if (a.d_state_in) chain_store<DK, DV, F::NW>(a.d_state_in + (size_t)nh * SSZ, t, v);
+    } else if (t == 0) {  // copies and a product still in flight end before the CTA exits
+        atomicOr(a.status, CPR_DEV_TIMEOUT);
+        for (int64_t jj = 0; jj < issued; ++jj) tc::mbar_wait(&mbar_ld[jj & 1], (uint32_t)((jj >> 1) & 1), 1u << 16);
+        if (products > 0) tc::mbar_wait(mbar_mma, (uint32_t)((products - 1) & 1), 1u << 16);
+    }
+    tc::fence_before_sync();
     __syncthreads();
-    if (a.d_state_in) {
-        float* dst = a.d_state_in + ((size_t)n * a.H + h) * SSZ;
-        const float* s = sl + cur * RS * SS;
-        for (int idx = t; idx < RS * DK; idx += kBwdThreads) {
-            const int cc = idx / RS, ii = idx % RS;
-            dst[(size_t)cc * DV + i0 + ii] = s[ii * SS + cc];
-        }
-    }
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, F::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------------------
@@ -861,19 +889,26 @@ cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s)
         cudaError_t e = launch_chunk_index(pa, C, nullptr, nullptr, nullptr, s);
         if (e != cudaSuccess) return e;
         profile_mark(1, s);
-        auto k1 = kb1_chunk_maps<DK, DV, C, T>;
-        if ((e = set_smem(k1, Kb1Cfg<DK, DV, C, T>::bytes)) != cudaSuccess) return e;
+        constexpr bool kTc = DK == 128 && DV == 128 && C == 64 && std::is_same<T, __nv_bfloat16>::value;
         const dim3 grid((unsigned)a.max_chunks, (unsigned)a.H);
-        k1<<<grid, kBwdThreads, Kb1Cfg<DK, DV, C, T>::bytes, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if constexpr (kTc) {
+            e = launch_chunk_maps_tc(a, s);  // the tensor-core form of kb1 for this shape
+        } else {
+            auto k1 = kb1_chunk_maps<DK, DV, C, T>;
+            if ((e = set_smem(k1, Kb1Cfg<DK, DV, C, T>::bytes)) != cudaSuccess) return e;
+            k1<<<grid, kBwdThreads, Kb1Cfg<DK, DV, C, T>::bytes, s>>>(a);
+            e = cudaGetLastError();
+        }
+        if (e != cudaSuccess) return e;
         profile_mark(2, s);
         auto k2 = kb2_reverse_chain<DK, DV>;
-        if ((e = set_smem(k2, Kb2Cfg<DK, DV>::bytes)) != cudaSuccess) return e;
-        const unsigned units = (unsigned)((int64_t)a.n_seqs * a.H * (DV / Kb2Cfg<DK, DV>::RS));
-        k2<<<units, kBwdThreads, Kb2Cfg<DK, DV>::bytes, s>>>(a);
+        // (the dynamic shared memory also caps the CTAs per SM so their TMEM columns fit)
+        const size_t sm2 = std::max<size_t>(Kb2Cfg<DK, DV>::bytes, tmem_cap_smem(Kb2Cfg<DK, DV>::TMEM_COLS));
+        if ((e = set_smem(k2, sm2)) != cudaSuccess) return e;
+        k2<<<(unsigned)((int64_t)a.n_seqs * a.H), kBwdThreads, sm2, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_mark(3, s);
-        if constexpr (DK == 128 && DV == 128 && C == 64 && std::is_same<T, __nv_bfloat16>::value) {
+        if constexpr (kTc) {
             e = launch_chunk_grads_tc(a, s);  // the tensor-core form of kb3 for this shape
         } else {
             auto k3 = kb3_chunk_grads<DK, DV, C, T>;

@@ -52,7 +52,7 @@ constexpr uint32_t kSmem = BAR_OFF + 64;
 static_assert(kSmem <= 232448, "one CTA's shared memory");
 
 // TMEM accumulators (columns)
-constexpr uint32_t P0 = 0, P1 = 64, P2 = 128;
+constexpr uint32_t P0 = 0, P1 = 64, P2 = 128, P3 = 192;
 constexpr uint32_t kTmemCols = 256;
 
 template <int K>
@@ -739,6 +739,273 @@ __global__ void __launch_bounds__(kT, 1) kb3_chunk_grads_tc(BackwardArgs a)
     if (w == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------------------------
+// kb1 on the tensor cores: one chunk's coefficients of the reverse chain (what
+// kb1_chunk_maps computes, backward.cu), one CTA of 8 warps per (chunk, head), with the
+// products as tcgen05 MMAs of bf16 splits (the conventions above); accumulator rows are
+// key indices c, columns tokens r or key/value indices:
+//   F1, F2   K K^T and Q K^T -> Pm and A^T in shared memory; T = (I + A)^-1 by blocks
+//   W        W^T = (diag(beta gam) K)^T T^T
+//   Qt, M    (Pm W)^T = W^T Pm^T, then Qt^T = Q^T diag(gam) - (Pm W)^T;
+//            M = gam_last I - W^T diag(d) K (two 64-column halves)
+//   C_b      C_b = Qt^T dO, stored [c][i] like a state (two 64-column halves)
+// M goes out as the reverse chain's B operand image (bf16 hi / lo, row c, K index c').
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kT, 1) kb1_chunk_maps_tc(BackwardArgs a)
+{
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __nv_bfloat16* Kp = reinterpret_cast<__nv_bfloat16*>(sm + KP_OFF);
+    __nv_bfloat16* Op = reinterpret_cast<__nv_bfloat16*>(sm + OP_OFF);
+    unsigned char* TA = sm + TA_OFF;
+    unsigned char* TB = sm + TB_OFF;
+    unsigned char* TU = sm + TU_OFF;
+    float* Pm = reinterpret_cast<float*>(sm + PM_OFF);
+    float* Tm = reinterpret_cast<float*>(sm + TM_OFF);
+    V16 v(reinterpret_cast<float*>(sm + VEC_OFF));
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + BAR_OFF);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    volatile int* okf = reinterpret_cast<volatile int*>(tslot + 1);
+
+    const int64_t c = blockIdx.x;
+    const int h = blockIdx.y, H = a.H, t = threadIdx.x;
+    if (*a.status || c >= a.cu_chunks[a.n_seqs]) return;
+    const int n = find_seq(a.cu_chunks, a.n_seqs, c);
+    const int64_t j = c - a.cu_chunks[n];
+    const int64_t t0 = (int64_t)a.cu_seqlens[n] + j * kN;
+    const int len = (int)min((int64_t)kN, (int64_t)a.cu_seqlens[n + 1] - t0);
+    const size_t ch = (size_t)c * H + h;
+    const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(a.k);
+    const __nv_bfloat16* go = static_cast<const __nv_bfloat16*>(a.d_out);
+    const int w = t >> 5, lane = t & 31, q = w & 3, hc = w >> 2, m = 32 * q + lane;
+
+    if (w == 0) tc::tmem_alloc(tslot, kTmemCols);
+    if (t == 0) {
+        tc::mbar_init(mbar, 1);
+        tc::fence_mbar_init();
+    }
+    // the chunk's K and dO as stored (zero rows past its tokens), g, beta
+    for (int idx = t; idx < kN * 16; idx += kT) {
+        const int r = idx >> 4, cv = (idx & 15) * 8;
+        uint4 wk = make_uint4(0u, 0u, 0u, 0u), wo = wk;
+        if (r < len) {
+            wk = __ldg(reinterpret_cast<const uint4*>(gk + ((t0 + r) * H + h) * kD + cv));
+            wo = __ldg(reinterpret_cast<const uint4*>(go + ((t0 + r) * H + h) * kD + cv));
+        }
+        *reinterpret_cast<uint4*>(Kp + r * kD + cv) = wk;
+        *reinterpret_cast<uint4*>(Op + r * kD + cv) = wo;
+    }
+    if (t < kN) {
+        v.gin[t] = t < len ? a.g[(t0 + t) * H + h] : 0.0f;
+        v.beta[t] = t < len ? a.beta[(t0 + t) * H + h] : 0.0f;
+    }
+    if (t < kN && t < len) tc::prefetch_l2(gq + ((t0 + t) * H + h) * kD, kD * 2);  // read column-wise later
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t lanes = (uint32_t)(32 * q) << 16;
+    if (t == 0) {
+        float G = 0.0f;
+        for (int r = 0; r < kN; ++r) {
+            G = r == 0 ? v.gin[0] : __fadd_rn(G, v.gin[r]);
+            v.G[r] = G;
+        }
+    }
+    __syncthreads();
+    if (t < kN) {
+        v.gam[t] = decay_exp(v.G[t]);
+        v.dd[t] = decay_exp(__fsub_rn(v.G[kN - 1], v.G[t]));
+        v.misc[t] = __fmul_rn(v.beta[t], v.gam[t]);  // the key scale of W (after gam is written)
+    }
+
+    uint32_t phase = 0;
+    bool alive = true;
+    auto run = [&](auto issue) {
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (t == 0) {
+            tc::fence_after_sync();
+            issue();
+            tc::commit(mbar);
+            *okf = tc::mbar_wait(mbar, phase) ? 1 : 0;
+        }
+        phase ^= 1u;
+        __syncthreads();
+        tc::fence_after_sync();
+        alive = alive && *okf != 0;
+    };
+    auto acc = [&](uint32_t col, float (&x)[32]) { tc::tmem_ld32(tmem + lanes + col + 32 * hc, x); };
+    // A tile of `rows` rows (c, K = the 64 tokens r, K-major) with element s_r X[r][c0 + c],
+    // X a [64][128] bf16 tile in shared memory: hi / lo splits (lo at dst + lo_off), or
+    // for s == NULL the exact bf16 values, hi only
+    auto tokens_tile = [&](const __nv_bfloat16* X, int c0, int rows, const float* s, unsigned char* dst,
+                           uint32_t lo_off) {
+        for (int idx = t; idx < rows * 8; idx += kT) {
+            const int cc = idx % rows, k8 = (idx / rows) * 8;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float xv = __bfloat162float(X[(k8 + e) * kD + c0 + cc]);
+                x[e] = s ? __fmul_rn(s[k8 + e], xv) : xv;
+            }
+            const uint32_t off = toff<kN>(cc, k8);
+            tc::split8_store(x, dst + off, s ? dst + lo_off + off : nullptr);
+        }
+    };
+    // a 64 x 64 fp32 tile X (row stride kNN) as a B operand (rows r, K = k; hi / lo)
+    auto nn_tile = [&](const float* X, unsigned char* dst) {
+        for (int idx = t; idx < kN * 8; idx += kT) {
+            const int r = idx >> 3, k8 = (idx & 7) * 8;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = X[r * kNN + k8 + e];
+            tc::split8_store(x, dst + toff<kN>(r, k8), dst + 8192 + toff<kN>(r, k8));
+        }
+    };
+
+    // ---- F1, F2: K K^T and Q K^T (n x n) -> Pm, A^T
+    {
+        for (int idx = t; idx < kN * 16; idx += kT) {
+            const int r = idx >> 4, cv = (idx & 15) * 8;
+            const uint4 kw = *reinterpret_cast<const uint4*>(Kp + r * kD + cv);
+            uint4 qw = make_uint4(0u, 0u, 0u, 0u);
+            if (r < len) qw = __ldg(reinterpret_cast<const uint4*>(gq + ((t0 + r) * H + h) * kD + cv));
+            *reinterpret_cast<uint4*>(TA + toff<kD>(r, cv)) = kw;
+            *reinterpret_cast<uint4*>(TA + 32768 + toff<kD>(r, cv)) = qw;
+            *reinterpret_cast<uint4*>(TB + toff<kD>(r, cv)) = kw;
+        }
+        for (int idx = t; idx < 2 * 1024; idx += kT) {  // rows [64, 128) of both A tiles: zero
+            const int s = idx >> 10, o = idx & 1023;
+            *reinterpret_cast<uint4*>(TA + s * 32768 + 16384 + o * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        run([&] {
+            mma_ab<kD, 1, 1>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false);
+            mma_ab<kD, 1, 1>(tmem + P1, tc::smem_u32(TA + 32768), tc::smem_u32(TB), false);
+        });
+        if (alive && q < 2) {  // rows t < 64
+            float kk[32], qk[32];
+            acc(P0, kk);
+            acc(P1, qk);
+            const float br = v.beta[m];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int r = 32 * hc + jj;
+                const float e = r <= m ? decay_exp(__fsub_rn(v.G[m], v.G[r])) : 0.0f;
+                const float l = r < m ? __fmul_rn(kk[jj], e) : 0.0f;
+                Tm[r * kN + m] = __fmul_rn(br, l);  // A transposed for the inversion
+                Pm[m * kNN + r] = __fmul_rn(qk[jj], e);
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        // T = (I + A)^-1 by blocks, with every thread (scratch in TU)
+        invert_unit_lower<kN, kNN>(Tm, reinterpret_cast<float*>(TU), reinterpret_cast<float*>(TU + 16896), t, kT);
+        {
+            const float* X = reinterpret_cast<const float*>(TU);
+            for (int idx = t; idx < kN * kN; idx += kT) Tm[(idx >> 6) * kNN + (idx & 63)] = X[(idx >> 6) * kNN + (idx & 63)];
+        }
+    }
+    // ---- W^T = (diag(beta gam) K)^T T^T: A rows c, K = r;  B = T, rows r', K = r
+    if (alive) {
+        tokens_tile(Kp, 0, kD, v.misc, TA, 16384);
+        __syncthreads();  // (Tm complete)
+        nn_tile(Tm, TB);
+        run([&] { mma_ab<kN, 2, 2>(tmem + P2, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+    }
+    // ---- Qt and M: A = W^T (rows c, K = r); B = Pm (rows r', K = r) and diag(d) K halves
+    if (alive) {
+        float wt[32];
+        acc(P2, wt);
+#pragma unroll
+        for (int e8 = 0; e8 < 32; e8 += 8) {
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = wt[e8 + e];
+            tc::split8_store(xs, TA + toff<kN>(m, 32 * hc + e8), TA + 16384 + toff<kN>(m, 32 * hc + e8));
+        }
+        nn_tile(Pm, TB);
+        for (int idx = t; idx < 2 * 64 * 8; idx += kT) {  // B: d_r K[r][c'] (rows c' of each half, K = r)
+            const int half = idx >> 9, cc = idx & 63, k8 = ((idx >> 6) & 7) * 8;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                x[e] = __fmul_rn(v.dd[k8 + e], __bfloat162float(Kp[(k8 + e) * kD + 64 * half + cc]));
+            unsigned char* dst = TU + half * 16384;
+            tc::split8_store(x, dst + toff<kN>(cc, k8), dst + 8192 + toff<kN>(cc, k8));
+        }
+        run([&] {
+            mma_ab<kN, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false);
+            mma_ab<kN, 2, 2>(tmem + P1, tc::smem_u32(TA), tc::smem_u32(TU), false);
+            mma_ab<kN, 2, 2>(tmem + P3, tc::smem_u32(TA), tc::smem_u32(TU + 16384), false);
+        });
+    }
+    // ---- Qt^T = Q^T diag(gam) - (Pm W)^T -> A tile (rows c, K = r);  M -> its image;
+    //      C_b = Qt^T dO in two halves (B = dO^T, rows i, K = r, exact bf16)
+    if (alive) {
+        float pw[32];
+        acc(P0, pw);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int r = 32 * hc + jj;
+            const float qv = r < len ? __bfloat162float(gq[((t0 + r) * H + h) * kD + m]) : 0.0f;
+            pw[jj] = __fsub_rn(__fmul_rn(v.gam[r], qv), pw[jj]);
+        }
+#pragma unroll
+        for (int e8 = 0; e8 < 32; e8 += 8) {
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = pw[e8 + e];
+            tc::split8_store(xs, TA + 32768 + toff<kN>(m, 32 * hc + e8), TA + 49152 + toff<kN>(m, 32 * hc + e8));
+        }
+        tokens_tile(Op, 0, kN, nullptr, TB, 0);
+        tokens_tile(Op, 64, kN, nullptr, TB + 16384, 0);
+        // M[c][c'] = gam_last [c == c'] - (W^T diag(d) K)[c][c'] into the image (row c, K = c')
+        unsigned char* img = a.mt + ch * (size_t)(4 * kD * kD);
+        const float gl = v.gam[kN - 1];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float mv[32];
+            acc(half ? P3 : P1, mv);
+#pragma unroll
+            for (int e8 = 0; e8 < 32; e8 += 8) {
+                float xs[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int cp = 64 * half + 32 * hc + e8 + e;
+                    xs[e] = cp == m ? __fsub_rn(gl, mv[e8 + e]) : -mv[e8 + e];
+                }
+                const uint32_t off = tc::tile_off<2>(m, 64 * half + 32 * hc + e8, kD);
+                tc::split8_store(xs, img + off, img + 2 * kD * kD + off);
+            }
+        }
+        run([&] {
+            mma_ab<kN, 2, 1>(tmem + P0, tc::smem_u32(TA + 32768), tc::smem_u32(TB), false);
+            mma_ab<kN, 2, 1>(tmem + P2, tc::smem_u32(TA + 32768), tc::smem_u32(TB + 16384), false);
+        });
+    }
+    // ---- C_b stored [c][i]
+    if (alive) {
+        float* dst = a.cb + ch * (size_t)(kD * kD) + (size_t)m * kD;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float cv[32];
+            acc(half ? P2 : P0, cv);
+#pragma unroll
+            for (int e4 = 0; e4 < 32; e4 += 4)
+                *reinterpret_cast<float4*>(dst + 64 * half + 32 * hc + e4) =
+                    make_float4(cv[e4], cv[e4 + 1], cv[e4 + 2], cv[e4 + 3]);
+        }
+    } else if (t == 0) {
+        atomicOr(a.status, CPR_DEV_TIMEOUT);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (w == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
 }  // namespace
 
 // The tensor-core chunk gradients (bf16, dk = dv = 128, C = 64) in place of kb3.
@@ -747,6 +1014,15 @@ cudaError_t launch_chunk_grads_tc(const BackwardArgs& a, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(kb3_chunk_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
     kb3_chunk_grads_tc<<<dim3((unsigned)a.max_chunks, (unsigned)a.H), kT, kSmem, s>>>(a);
+    return cudaGetLastError();
+}
+
+// The tensor-core chunk coefficients (bf16, dk = dv = 128, C = 64) in place of kb1.
+cudaError_t launch_chunk_maps_tc(const BackwardArgs& a, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(kb1_chunk_maps_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    kb1_chunk_maps_tc<<<dim3((unsigned)a.max_chunks, (unsigned)a.H), kT, kSmem, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -108,7 +108,8 @@ struct PrefillArgs {
 // Backward workspace:
 //   [0, 256)       status word (uint32) and padding (a spare word for k0's counter slot)
 //   cu_chunks      int32 [n_seqs + 1]
-//   mt             fp32 [max_chunks, H, dk, dk]: each chunk's M^T (element (c', c) = M[c][c'])
+//   mt             [max_chunks, H] x 4 dk^2 bytes: each chunk's M as the B operand of the
+//                  reverse chain's product (bf16 hi, then lo, [dk][dk] K-major core matrices)
 //   cb             fp32 [max_chunks, H, dk, dv]: each chunk's C_b = dO^T Qt, laid out like a state
 //   d_end          fp32 [max_chunks, H, dk, dv]: the adjoint of the state at each chunk's end
 struct BackwardLayout {
@@ -148,7 +149,7 @@ struct BackwardArgs {
     uint32_t* status;
     uint32_t* ready;           // k0's counter slot (a spare word of the status block)
     int32_t* cu_chunks;
-    float* mt;
+    unsigned char* mt;  // each chunk's M image for the reverse chain's products
     float* cb;
     float* d_end;
     int64_t max_chunks;
@@ -252,6 +253,7 @@ template <int DK, int DV, int C, typename T> cudaError_t launch_ring_from_prefil
 template <int DK, int DV, int C, typename T> cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
 // The chunk gradients of the backward on the tensor cores (bf16, dk = dv = 128, C = 64).
 cudaError_t launch_chunk_grads_tc(const BackwardArgs& a, cudaStream_t s);
+cudaError_t launch_chunk_maps_tc(const BackwardArgs& a, cudaStream_t s);
 // Whether the backward's chunk kernels fit one CTA's shared memory for this shape and type.
 template <int DK, int DV, int C, typename T> bool backward_fits();
 
