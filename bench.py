@@ -44,7 +44,7 @@ L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
 # of the kernel as it now stands: k23_chain_and_intra at trainer_fwd, k4_decode_step at
 # rollout_decode.  Reset to None whenever the kernel changes.
-TRAFFIC_K23_TRAINER_FWD = 559.695872e6 + 198.414336e6
+TRAFFIC_K23_TRAINER_FWD = None
 TRAFFIC_K4_ROLLOUT_DECODE = 267.607808e6 + 206.803712e6
 
 
@@ -633,7 +633,7 @@ def run_ours(args):
 
     # ---------------- decode: rollout shape ----------------
     decode = None
-    if not args.no_decode:
+    if not args.no_decode and not args.no_rollout_decode:
         decode = run_decode(args, cpr, inputs, dev, hbm_peak, dist, world)
     continuation = run_continuation(args, cpr, inputs, dev, hbm_peak, dist, world) if not args.no_decode else None
     # the K-split product is a one-GPU leg: under torchrun it is left out on every rank
@@ -645,8 +645,7 @@ def run_ours(args):
         roofline["frac_of_measured"] = roofline["achieved"] / p32_meas["tflops"]
     extra = None if args.no_extra else run_extra_workloads(args, cpr, inputs, dev, dist, world, flush, p32_meas,
                                                            hbm_peak)
-    train = None if args.no_extra or args.no_train else run_train_fwd_bwd(args, cpr, inputs, dev, dist, world, flush,
-                                                                           p32_meas)
+    train = None if args.no_train else run_train_fwd_bwd(args, cpr, inputs, dev, dist, world, flush, p32_meas)
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only) ----------------
     cpu = None
@@ -948,8 +947,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pik", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the rollout_prefill, varlen_stress, tiny and train_fwd_bwd lines")
+                    help="skip the rollout_prefill, varlen_stress and tiny lines")
     ap.add_argument("--no-train", action="store_true", help="skip the train_fwd_bwd line")
+    ap.add_argument("--no-rollout-decode", action="store_true",
+                    help="skip the rollout_decode leg (its prior prefill holds tens of GB); the continuation still runs")
     ap.add_argument("--only-pik", action="store_true")
     ap.add_argument("--pik-size", type=int, default=8192, help="M = N = K of the pik product (a multiple of 512)")
     args = ap.parse_args()
