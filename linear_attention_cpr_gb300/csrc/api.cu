@@ -176,12 +176,13 @@ int32_t cpr_gdn_backward(const void* q, const void* k, const void* v, const floa
     a.dbeta = dbeta;
     a.d_state_in = d_state_in;
     a.status = reinterpret_cast<uint32_t*>(ws);
-    a.ready = reinterpret_cast<uint32_t*>(ws + 4);
+    a.ready = reinterpret_cast<uint32_t*>(ws + lay.ready);
     a.cu_chunks = reinterpret_cast<int32_t*>(ws + lay.cu_chunks);
     a.mt = ws + lay.mt;
     a.cb = reinterpret_cast<float*>(ws + lay.cb);
     a.d_end = reinterpret_cast<float*>(ws + lay.d_end);
     a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);
+    a.num_sms = num_sms();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorInvalidValue;
 #define CPR_DISPATCH(DK, DV, CC)                                                                   \

@@ -38,6 +38,7 @@
 #include "chunk_update.cuh"
 #include "common.cuh"
 #include "numerics.cuh"
+#include "reverse_chain.cuh"
 #include "tc.cuh"
 
 namespace cpr {
@@ -359,114 +360,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kb1_chunk_maps(BackwardArgs a)
 }
 
 // ------------------------------------------------------------------------------------
-// kb2: the reverse chain of one (sequence, head), by a CTA of 8 warps.  For j = last .. 0
-// it stores dS (the adjoint at chunk j's end) into d_end[j], then steps it to chunk j's
-// start, dS_b = dS_end M_j^T + C_j, by the forward chain's routines: dS as the A operand
-// in TMEM (bf16 hi / lo, value row i in lane i), chunk j's M image (kb1) as B, three
-// tcgen05 products hi*hi + hi*lo + lo*hi accumulated in fp32, C_j added in the epilogue.
-// The images come by bulk copies two chunks deep; each chunk's C_j loads and d_end stores
-// run while its product does.  The start value is d_state_out (zero if absent); the end
-// value is d_state_in.  Every wait is bounded; a timeout ends the chain with the status
-// word set.
+// kb2: the reverse chains, one CTA per (sequence, head) (reverse_chain.cuh).
 // ------------------------------------------------------------------------------------
-template <int DK, int DV>
-struct Kb2Cfg {
-    static constexpr int NW = kBwdThreads / 32;
-    static constexpr uint32_t IMG = 2u * DK * DK * 2;  // one chunk's M image (bf16 hi, lo)
-    static constexpr uint32_t PIECE = 16384;
-    static constexpr uint32_t BAR_OFF = 2 * IMG;       // two stages
-    static constexpr size_t bytes = BAR_OFF + 64;
-    // TMEM: the accumulator in columns [0, DK), the A operand in [DK, 2 DK)
-    static constexpr uint32_t TMEM_COLS = 2 * DK <= 64 ? 64 : 2 * DK <= 128 ? 128 : 256;
-};
-
 template <int DK, int DV>
 __global__ void __launch_bounds__(kBwdThreads, 1) kb2_reverse_chain(BackwardArgs a)
 {
-    using F = Kb2Cfg<DK, DV>;
-    using Mp = ChainMap<DK, F::NW>;
     extern __shared__ __align__(1024) unsigned char smc[];
-    uint64_t* mbar_ld = reinterpret_cast<uint64_t*>(smc + F::BAR_OFF);  // [2] stage landed
-    uint64_t* mbar_mma = mbar_ld + 2;                                   // product done
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar_mma + 1);
-    volatile int* ok_s = reinterpret_cast<volatile int*>(tslot + 1);     // thread 0's wait results
-
-    const int nh = blockIdx.x, n = nh / a.H, h = nh % a.H, t = threadIdx.x, warp = t >> 5;
-    if (*a.status || n >= a.n_seqs) return;
-    const int64_t cb = a.cu_chunks[n], nch = (int64_t)a.cu_chunks[n + 1] - cb;
-    const size_t SSZ = (size_t)DK * DV;
-    const float* ds_out = a.d_state_out ? a.d_state_out + (size_t)nh * SSZ : nullptr;
-    float v[Mp::CPT];
-    chain_load_state<DK, DV, F::NW>(ds_out, t, v);
-    if (nch == 0) {  // no chunk: d_state_in = d_state_out
-        if (a.d_state_in) chain_store<DK, DV, F::NW>(a.d_state_in + (size_t)nh * SSZ, t, v);
-        return;
-    }
-    if (warp == 0) tc::tmem_alloc(tslot, F::TMEM_COLS);
-    if (t == 0) {
-        tc::mbar_init(&mbar_ld[0], 1);
-        tc::mbar_init(&mbar_ld[1], 1);
-        tc::mbar_init(mbar_mma, 1);
-        tc::fence_mbar_init();
-    }
+    __shared__ uint32_t tslot;
+    constexpr uint32_t COLS = RevChainCfg<DK, DV>::TMEM_COLS;
+    if (*a.status || (int)blockIdx.x >= a.n_seqs * a.H) return;
+    if ((threadIdx.x >> 5) == 0) tc::tmem_alloc(&tslot, COLS);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *tslot;
-
-    int64_t issued = 0;    // (thread 0) image copies issued, step jj into stage jj & 1
-    int64_t products = 0;  // (thread 0) products issued
-    auto issue = [&]() {
-        const int64_t jj = issued++, j = nch - 1 - jj;
-        const unsigned char* src = a.mt + ((size_t)(cb + j) * a.H + h) * F::IMG;
-        unsigned char* dst = smc + (jj & 1) * F::IMG;
-        tc::mbar_arrive_expect_tx(&mbar_ld[jj & 1], F::IMG);
-        for (uint32_t off = 0; off < F::IMG; off += F::PIECE)
-            tc::bulk_g2s(dst + off, src + off, min(F::PIECE, F::IMG - off), &mbar_ld[jj & 1]);
-    };
-    if (t == 0) {
-        issue();
-        if (nch > 1) issue();
-    }
-    chain_put_a<DK, F::NW>(tmem + DK, t, v);
-    tc::fence_before_sync();
-    __syncthreads();
-    bool ok = true;
-    for (int64_t jj = 0; jj < nch; ++jj) {
-        const size_t ch = (size_t)(cb + nch - 1 - jj) * a.H + h;
-        bool issued_ok = true;
-        if (t == 0) {
-            issued_ok = tc::mbar_wait(&mbar_ld[jj & 1], (uint32_t)((jj >> 1) & 1));
-            if (issued_ok) {
-                chain_mma<DK>(tmem, tmem + DK, smc + (jj & 1) * F::IMG, mbar_mma);
-                ++products;
-            }
-        }
-        chain_store<DK, DV, F::NW>(a.d_end + ch * SSZ, t, v);  // dS at the chunk's end
-        float b[Mp::CPT];
-        chain_load_b<DK, DV, F::NW>(a.cb + ch * SSZ, t, b);
-        if (t == 0) ok_s[0] = (issued_ok && tc::mbar_wait(mbar_mma, (uint32_t)(jj & 1))) ? 1 : 0;
-        __syncthreads();
-        ok = ok_s[0] != 0;
-        if (!ok) break;
-        tc::fence_after_sync();
-        if (t == 0 && issued < nch) issue();  // the product is done: its stage is free
-        chain_values_reg<DK, F::NW>(tmem, t, b, v);
-        if (jj + 1 < nch) chain_put_a<DK, F::NW>(tmem + DK, t, v);
-        tc::fence_before_sync();
-        __syncthreads();  // (every thread has read ok_s)
-    }
-    if (ok) {
-        if (a.d_state_in) chain_store<DK, DV, F::NW>(a.d_state_in + (size_t)nh * SSZ, t, v);
-    } else if (t == 0) {  // copies and a product still in flight end before the CTA exits
-        atomicOr(a.status, CPR_DEV_TIMEOUT);
-        for (int64_t jj = 0; jj < issued; ++jj) tc::mbar_wait(&mbar_ld[jj & 1], (uint32_t)((jj >> 1) & 1), 1u << 16);
-        if (products > 0) tc::mbar_wait(mbar_mma, (uint32_t)((products - 1) & 1), 1u << 16);
-    }
+    const uint32_t tmem = tslot;
+    reverse_chain<DK, DV>(a, blockIdx.x, smc, tmem, nullptr);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tmem, F::TMEM_COLS);
+    if ((threadIdx.x >> 5) == 0) tc::tmem_dealloc(tmem, COLS);
 }
 
 // ------------------------------------------------------------------------------------
@@ -882,9 +794,9 @@ cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s)
         pa.boundary_capacity = a.boundary_capacity;
         pa.cu_chunks = a.cu_chunks;
         pa.status = a.status;
-        pa.ready = a.ready;
-        pa.max_chunks = 0;
-        pa.H = 0;
+        pa.ready = a.ready;  // (k0 zeroes the hand-off counters)
+        pa.max_chunks = a.max_chunks;
+        pa.H = a.H;
         profile_mark(0, s);
         cudaError_t e = launch_chunk_index(pa, C, nullptr, nullptr, nullptr, s);
         if (e != cudaSuccess) return e;
@@ -901,16 +813,19 @@ cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s)
         }
         if (e != cudaSuccess) return e;
         profile_mark(2, s);
-        auto k2 = kb2_reverse_chain<DK, DV>;
-        // (the dynamic shared memory also caps the CTAs per SM so their TMEM columns fit)
-        const size_t sm2 = std::max<size_t>(Kb2Cfg<DK, DV>::bytes, tmem_cap_smem(Kb2Cfg<DK, DV>::TMEM_COLS));
-        if ((e = set_smem(k2, sm2)) != cudaSuccess) return e;
-        k2<<<(unsigned)((int64_t)a.n_seqs * a.H), kBwdThreads, sm2, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        profile_mark(3, s);
         if constexpr (kTc) {
-            e = launch_chunk_grads_tc(a, s);  // the tensor-core form of kb3 for this shape
+            // the chain and the tensor-core form of kb3 in one launch (the chain's and the
+            // gradients' times are not separable: both events mark its end)
+            profile_mark(3, s);
+            e = launch_chain_and_grads_tc(a, s);
         } else {
+            auto k2 = kb2_reverse_chain<DK, DV>;
+            // (the dynamic shared memory also caps the CTAs per SM so their TMEM columns fit)
+            const size_t sm2 = std::max<size_t>(RevChainCfg<DK, DV>::bytes, tmem_cap_smem(RevChainCfg<DK, DV>::TMEM_COLS));
+            if ((e = set_smem(k2, sm2)) != cudaSuccess) return e;
+            k2<<<(unsigned)((int64_t)a.n_seqs * a.H), kBwdThreads, sm2, s>>>(a);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            profile_mark(3, s);
             auto k3 = kb3_chunk_grads<DK, DV, C, T>;
             if ((e = set_smem(k3, Kb3Cfg<DK, DV, C, T>::bytes)) != cudaSuccess) return e;
             k3<<<grid, kBwdThreads, Kb3Cfg<DK, DV, C, T>::bytes, s>>>(a);

@@ -23,8 +23,12 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
+#include "handoff.cuh"
 #include "numerics.cuh"
+#include "reverse_chain.cuh"
 #include "tc.cuh"
 
 namespace cpr {
@@ -141,9 +145,13 @@ struct V16 {
           dG(p + 832), gin(p + 896), misc(p + 960) {}
 };
 
-__global__ void __launch_bounds__(kT, 1) kb3_chunk_grads_tc(BackwardArgs a)
+// The chunk gradients of one (chunk, head) item by the CTA's 8 warps.  TMEM columns
+// [tmem, tmem + 256) and the mbarrier at BAR_OFF (initialised; its next phase `phase`)
+// belong to the caller.  Starts and ends with every thread at a barrier; returns false
+// (uniformly) after a product did not complete in time, with the status word set.
+__device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t c, int h, unsigned char* sm,
+                                                 uint32_t tmem, uint32_t& phase)
 {
-    extern __shared__ __align__(1024) unsigned char sm[];
     __nv_bfloat16* Kp = reinterpret_cast<__nv_bfloat16*>(sm + KP_OFF);
     __nv_bfloat16* Op = reinterpret_cast<__nv_bfloat16*>(sm + OP_OFF);
     unsigned char* TA = sm + TA_OFF;
@@ -155,12 +163,9 @@ __global__ void __launch_bounds__(kT, 1) kb3_chunk_grads_tc(BackwardArgs a)
     V16 v(reinterpret_cast<float*>(sm + VEC_OFF));
     float* red = reinterpret_cast<float*>(sm + RED_OFF);  // [8][64]
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + BAR_OFF);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
-    volatile int* okf = reinterpret_cast<volatile int*>(tslot + 1);
+    volatile int* okf = reinterpret_cast<volatile int*>(sm + BAR_OFF + 12);
 
-    const int64_t c = blockIdx.x;
-    const int h = blockIdx.y, H = a.H, t = threadIdx.x;
-    if (*a.status || c >= a.cu_chunks[a.n_seqs]) return;
+    const int H = a.H, t = threadIdx.x;
     const int n = find_seq(a.cu_chunks, a.n_seqs, c);
     const int64_t j = c - a.cu_chunks[n];
     const int64_t t0 = (int64_t)a.cu_seqlens[n] + j * kN;
@@ -176,11 +181,6 @@ __global__ void __launch_bounds__(kT, 1) kb3_chunk_grads_tc(BackwardArgs a)
     // epilogue mapping: accumulator row m (TMEM lane), columns [32 hc, 32 hc + 32)
     const int w = t >> 5, lane = t & 31, q = w & 3, hc = w >> 2, m = 32 * q + lane;
 
-    if (w == 0) tc::tmem_alloc(tslot, kTmemCols);
-    if (t == 0) {
-        tc::mbar_init(mbar, 1);
-        tc::fence_mbar_init();
-    }
     // ---- a: the chunk's K and dO as stored (zero rows past its tokens), g, beta
     for (int idx = t; idx < kN * 16; idx += kT) {
         const int r = idx >> 4, cv = (idx & 15) * 8;
@@ -199,7 +199,6 @@ __global__ void __launch_bounds__(kT, 1) kb3_chunk_grads_tc(BackwardArgs a)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *tslot;
     const uint32_t lanes = (uint32_t)(32 * q) << 16;
     if (t == 0) {
         float G = 0.0f;
@@ -214,7 +213,6 @@ __global__ void __launch_bounds__(kT, 1) kb3_chunk_grads_tc(BackwardArgs a)
         v.dd[t] = decay_exp(__fsub_rn(v.G[kN - 1], v.G[t]));
     }
 
-    uint32_t phase = 0;
     bool alive = true;
     // Every writer has stored its tiles: make them visible to the tensor cores, let thread 0
     // issue the products and wait for them, then every thread may read the accumulators.
@@ -736,6 +734,62 @@ __global__ void __launch_bounds__(kT, 1) kb3_chunk_grads_tc(BackwardArgs a)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    return alive;
+}
+
+// ------------------------------------------------------------------------------------
+// The reverse chain and the chunk gradients in one cooperative launch of one CTA per SM:
+// CTAs [0, n_chain) run the reverse chains (reverse_chain.cuh), one (sequence, head) at a
+// time, publishing each chunk's state adjoint d_end as soon as it is stored; then every
+// CTA takes (chunk, head) items of the chunk gradients in reverse chunk order from a
+// counter, each starting once its chunk's d_end is published.  The gradients of late
+// chunks thus run while the chain is still stepping back through the early ones.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kT, 1) kb23_chain_and_grads_tc(BackwardArgs a, int n_chain)
+{
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ uint32_t tslot_s, claimed_s;
+    __shared__ int wait_ok_s;
+    static_assert(RevChainCfg<kD, kD>::bytes <= BAR_OFF, "the chain's shared memory stays clear of the items' mbarrier");
+    const int t = threadIdx.x, w = t >> 5;
+    if (*a.status) return;
+    if (w == 0) tc::tmem_alloc(&tslot_s, kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tslot_s;
+    bool ok = true;
+    if ((int)blockIdx.x < n_chain)
+        for (int ci = blockIdx.x; ci < a.n_seqs * a.H && ok; ci += n_chain)
+            ok = reverse_chain<kD, kD>(a, ci, sm, tmem, a.ready);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + BAR_OFF);
+    if (t == 0) {
+        tc::mbar_init(mbar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    const uint32_t nchunks = (uint32_t)a.cu_chunks[a.n_seqs], items = nchunks * (uint32_t)a.H;
+    uint32_t* next_item = a.ready + (size_t)a.max_chunks * a.H;
+    uint32_t phase = 0;
+    while (ok) {
+        if (t == 0) claimed_s = atomicAdd(next_item, 1u);
+        __syncthreads();
+        const uint32_t u = claimed_s;
+        if (u >= items) break;
+        const int64_t c = (int64_t)(nchunks - 1 - u / (uint32_t)a.H);
+        const int h = (int)(u % (uint32_t)a.H);
+        if (t == 0) wait_ok_s = wait_published(a.ready + (size_t)c * a.H + h, 1u, a.status, 0);
+        __syncthreads();
+        if (!wait_ok_s) {
+            if (t == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);
+            break;
+        }
+        ok = chunk_grads_item(a, c, h, sm, tmem, phase);  // (ends at a barrier)
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (t == 0) tc::mbar_inval(mbar);
     if (w == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -1008,13 +1062,22 @@ __global__ void __launch_bounds__(kT, 1) kb1_chunk_maps_tc(BackwardArgs a)
 
 }  // namespace
 
-// The tensor-core chunk gradients (bf16, dk = dv = 128, C = 64) in place of kb3.
-cudaError_t launch_chunk_grads_tc(const BackwardArgs& a, cudaStream_t s)
+// The reverse chain and the tensor-core chunk gradients (bf16, dk = dv = 128, C = 64) in
+// one cooperative launch, in place of kb2 and kb3.
+cudaError_t launch_chain_and_grads_tc(const BackwardArgs& a, cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(kb3_chunk_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    auto kern = kb23_chain_and_grads_tc;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
-    kb3_chunk_grads_tc<<<dim3((unsigned)a.max_chunks, (unsigned)a.H), kT, kSmem, s>>>(a);
-    return cudaGetLastError();
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kT, kSmem)) != cudaSuccess) return e;
+    if (per_sm < 1 || a.num_sms < 2) return cudaErrorInvalidConfiguration;
+    const int grid = per_sm * a.num_sms;
+    const int n_chain = std::max(1, std::min(a.n_seqs * a.H, grid / 2));
+    BackwardArgs args = a;
+    int nc = n_chain;
+    void* params[] = {&args, &nc};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kT), params, kSmem, s);
 }
 
 // The tensor-core chunk coefficients (bf16, dk = dv = 128, C = 64) in place of kb1.

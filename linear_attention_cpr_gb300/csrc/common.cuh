@@ -106,14 +106,16 @@ struct PrefillArgs {
 };
 
 // Backward workspace:
-//   [0, 256)       status word (uint32) and padding (a spare word for k0's counter slot)
+//   [0, 256)       status word (uint32) and padding
 //   cu_chunks      int32 [n_seqs + 1]
 //   mt             [max_chunks, H] x 4 dk^2 bytes: each chunk's M as the B operand of the
 //                  reverse chain's product (bf16 hi, then lo, [dk][dk] K-major core matrices)
 //   cb             fp32 [max_chunks, H, dk, dv]: each chunk's C_b = dO^T Qt, laid out like a state
 //   d_end          fp32 [max_chunks, H, dk, dv]: the adjoint of the state at each chunk's end
+//   ready          uint32 [max_chunks, H] + 1: publication counters of d_end and the item
+//                  counter (the fused chain-and-gradients launch), zeroed by k0
 struct BackwardLayout {
-    size_t cu_chunks, mt, cb, d_end, total;
+    size_t cu_chunks, mt, cb, d_end, ready, total;
     __host__ __device__ BackwardLayout(int64_t total_tokens, int32_t n_seqs, int32_t H, int32_t dk, int32_t dv,
                                        int32_t C)
     {
@@ -122,7 +124,8 @@ struct BackwardLayout {
         mt = align_up(cu_chunks + sizeof(int32_t) * (size_t)(n_seqs + 1), kAlign);
         cb = align_up(mt + (size_t)dk * dk * 4 * (size_t)mc * H, kAlign);
         d_end = align_up(cb + (size_t)dk * dv * 4 * (size_t)mc * H, kAlign);
-        total = align_up(d_end + (size_t)dk * dv * 4 * (size_t)mc * H, kAlign);
+        ready = align_up(d_end + (size_t)dk * dv * 4 * (size_t)mc * H, kAlign);
+        total = align_up(ready + 4 * ((size_t)mc * H + 1), kAlign);
     }
 };
 
@@ -147,12 +150,13 @@ struct BackwardArgs {
     float* dbeta;
     float* d_state_in;         // [N, H, dk, dv] or NULL (not wanted)
     uint32_t* status;
-    uint32_t* ready;           // k0's counter slot (a spare word of the status block)
+    uint32_t* ready;           // the hand-off counters (layout `ready`)
     int32_t* cu_chunks;
     unsigned char* mt;  // each chunk's M image for the reverse chain's products
     float* cb;
     float* d_end;
     int64_t max_chunks;
+    int num_sms;
 };
 
 // Decode workspace: [0, 256) status word.
@@ -252,7 +256,7 @@ template <int DK, int DV, int C, typename T> cudaError_t launch_ring_from_prefil
 // The CPR backward (k0, then the chunk maps, the reverse chain and the chunk gradients).
 template <int DK, int DV, int C, typename T> cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
 // The chunk gradients of the backward on the tensor cores (bf16, dk = dv = 128, C = 64).
-cudaError_t launch_chunk_grads_tc(const BackwardArgs& a, cudaStream_t s);
+cudaError_t launch_chain_and_grads_tc(const BackwardArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_maps_tc(const BackwardArgs& a, cudaStream_t s);
 // Whether the backward's chunk kernels fit one CTA's shared memory for this shape and type.
 template <int DK, int DV, int C, typename T> bool backward_fits();
