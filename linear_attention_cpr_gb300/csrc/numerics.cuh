@@ -186,17 +186,27 @@ __device__ __forceinline__ void fwd_subst(const float* At, float x[C])
 // (blocks k ascending, 16 terms each in ascending order), T_ij = -T_ii Y (terms in
 // ascending order).  At: A transposed (At[i * C + r] = A_ri), 16-byte aligned rows.  T
 // goes to Tout[r * TS + c], zero above the diagonal; Y needs 16 x 16 x (C/16 - 1) floats of
-// scratch.  Every element has one fixed operation sequence, whichever thread computes it.
-// Contains __syncthreads (every thread of the block must call it).
+// 16-byte aligned scratch.  Every element has one fixed operation sequence, whichever
+// thread computes it; a thread computes four elements of Y (rows r0..r0+3 of one column)
+// or of T_ij (columns c0..c0+3 of one row) side by side, so each shared-memory load feeds
+// four FMAs.  Contains __syncthreads (every thread of the block must call it); nt >= C.
 template <int C, int TS>
 __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ At, float* __restrict__ Tout,
                                                   float* __restrict__ Y, int tid, int nt)
 {
     static_assert(C % 16 == 0 && C <= 64, "blocks of 16, at most four");
     constexpr int NB = C / 16;
-    for (int idx = tid; idx < C * C; idx += nt) Tout[(idx / C) * TS + idx % C] = 0.0f;
-    __syncthreads();
-    if (tid < C) {  // diagonal block k, column j
+    constexpr int NZ = NB * (NB - 1) / 2 * 256;  // elements of the blocks above the diagonal
+    for (int idx = tid; idx < NZ; idx += nt) {   // (block pairs i < j in order, 256 elements each)
+        int q = idx >> 8, i = 0, j = 1;
+        while (q >= NB - 1 - i) {
+            q -= NB - 1 - i;
+            ++i;
+        }
+        j = i + 1 + q;
+        Tout[(16 * i + ((idx >> 4) & 15)) * TS + 16 * j + (idx & 15)] = 0.0f;
+    }
+    if (tid < C) {  // diagonal block k, column j (all 16 rows: zero above the diagonal)
         const int k = tid >> 4, j = tid & 15, o = 16 * k;
         float x[16];
 #pragma unroll
@@ -208,31 +218,53 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ At, 
             x[r] = r >= j ? acc : 0.0f;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r)
-            if (r >= j) Tout[(o + r) * TS + o + j] = x[r];
+        for (int r = 0; r < 16; ++r) Tout[(o + r) * TS + o + j] = x[r];
     }
     __syncthreads();
 #pragma unroll 1
     for (int d = 1; d < NB; ++d) {
         const int nblk = NB - d;
-        for (int idx = tid; idx < nblk * 256; idx += nt) {  // Y of block (j + d, j), element (r, c)
-            const int j = idx >> 8, r = (idx >> 4) & 15, c = idx & 15, i = j + d;
-            float acc = 0.0f;
+        // Y of block (j + d, j): rows r0..r0+3 of column c
+        for (int u = tid; u < nblk * 64; u += nt) {
+            const int j = u >> 6, r0 = ((u >> 4) & 3) * 4, c = u & 15, i = j + d;
+            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
             for (int k = j; k < i; ++k) {
 #pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    acc = __fmaf_rn(At[(16 * k + s) * C + 16 * i + r], Tout[(16 * k + s) * TS + 16 * j + c], acc);
+                for (int s = 0; s < 16; ++s) {
+                    const float4 av = *reinterpret_cast<const float4*>(At + (16 * k + s) * C + 16 * i + r0);
+                    const float t = Tout[(16 * k + s) * TS + 16 * j + c];
+                    a0 = __fmaf_rn(av.x, t, a0);
+                    a1 = __fmaf_rn(av.y, t, a1);
+                    a2 = __fmaf_rn(av.z, t, a2);
+                    a3 = __fmaf_rn(av.w, t, a3);
+                }
             }
-            Y[idx] = acc;
+            float* y = Y + (j << 8) + (r0 << 4) + c;
+            y[0] = a0;
+            y[16] = a1;
+            y[32] = a2;
+            y[48] = a3;
         }
         __syncthreads();
-        for (int idx = tid; idx < nblk * 256; idx += nt) {  // T_ij = -T_ii Y
-            const int j = idx >> 8, r = (idx >> 4) & 15, c = idx & 15, i = j + d;
-            float acc = 0.0f;
+        // T_ij = -T_ii Y: columns c0..c0+3 of row r
+        for (int u = tid; u < nblk * 64; u += nt) {
+            const int j = u >> 6, r = (u >> 2) & 15, c0 = (u & 3) * 4, i = j + d;
+            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
             for (int s = 0; s < 16; ++s)
-                if (s <= r) acc = __fmaf_rn(Tout[(16 * i + r) * TS + 16 * i + s], Y[(j << 8) + (s << 4) + c], acc);
-            Tout[(16 * i + r) * TS + 16 * j + c] = -acc;
+                if (s <= r) {
+                    const float t = Tout[(16 * i + r) * TS + 16 * i + s];
+                    const float4 yv = *reinterpret_cast<const float4*>(Y + (j << 8) + (s << 4) + c0);
+                    a0 = __fmaf_rn(t, yv.x, a0);
+                    a1 = __fmaf_rn(t, yv.y, a1);
+                    a2 = __fmaf_rn(t, yv.z, a2);
+                    a3 = __fmaf_rn(t, yv.w, a3);
+                }
+            float* o = Tout + (16 * i + r) * TS + 16 * j + c0;
+            o[0] = -a0;
+            o[1] = -a1;
+            o[2] = -a2;
+            o[3] = -a3;
         }
         __syncthreads();
     }
