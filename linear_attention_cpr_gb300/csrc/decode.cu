@@ -138,28 +138,39 @@ __device__ __forceinline__ void l2_normalise_qk(float* kf, float* qf, float* scr
 }
 
 // ------------------------------------------------------------------------------------
-// k4: decode step.  One CTA per (sequence, head), 8 warps: warp m owns key rows
-// [m*DK/8, (m+1)*DK/8) of the stored state (chain m of the canonical dot) and lane l
-// owns value columns [l*DV/32, (l+1)*DV/32).  Partial chains meet in shared memory and
-// every value column's dot is finished by the canonical tree.  Sequences whose token
-// completes a chunk are left to k5 (their stepped state is replaced by the resync).
+// k4: decode step.  NS CTAs per (sequence, head) (below), 8 warps each: warp m owns key
+// rows [m*DK/8, (m+1)*DK/8) of the stored state (chain m of the canonical dot) and lane l
+// owns value columns [l*DVS/32, (l+1)*DVS/32) of the CTA's DVS = DV/NS columns.  Partial
+// chains meet in shared memory and every value column's dot is finished by the canonical
+// tree.  Sequences whose token completes a chunk are left to k5 (their stepped state is
+// replaced by the resync).
 // ------------------------------------------------------------------------------------
+// k4 runs NS CTAs per (sequence, head), split by value columns: CTA `cp` covers columns
+// [cp DV/NS, (cp + 1) DV/NS) of every key row.  Each column's dots still take all DK keys
+// in the eight canonical chains, so the values do not depend on NS; smaller CTAs (58
+// registers a thread at DV = 128) keep four per SM resident, and more state loads in
+// flight (the step is bound by moving the state through HBM).
+template <int DV>
+__host__ __device__ constexpr int k4_splits() { return DV >= 64 ? 2 : 1; }
+
 template <int DK, int DV, int C, typename T, bool QK_NORM>
 __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
 {
-    constexpr int L = DK / 8, VPT = DV / 32;
+    constexpr int NS = k4_splits<DV>(), DVS = DV / NS;
+    constexpr int L = DK / 8, VPT = DVS / 32;
     __shared__ __align__(16) float kf[DK];
     __shared__ __align__(16) float qf[DK];
-    __shared__ __align__(16) float part[8][DV];
-    __shared__ __align__(16) float part2[8][DV];
+    __shared__ __align__(16) float part[8][DVS];
+    __shared__ __align__(16) float part2[8][DVS];
     __shared__ float sc[4];
 
-    // grid (sequence, query/key head, value head within its group): no division for the head
-    const int b = blockIdx.x, h = blockIdx.y * gridDim.z + blockIdx.z, tid = threadIdx.x, H = a.H;
+    // grid (sequence x column part, query/key head, value head within its group)
+    const int b = blockIdx.x / NS, cp = blockIdx.x % NS, h = blockIdx.y * gridDim.z + blockIdx.z;
+    const int tid = threadIdx.x, H = a.H, i0 = cp * DVS;
     const int m = tid >> 5, lane = tid & 31;
     const int p = a.pos[b];
     if (p < 0) {
-        if (tid == 0 && h == 0) atomicOr(a.status, CPR_DEV_BAD_POS);
+        if (tid == 0 && h == 0 && cp == 0) atomicOr(a.status, CPR_DEV_BAD_POS);
         return;
     }
     const int r = p % C;
@@ -176,18 +187,20 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
         const T kk = k[bhk * DK + idx];
         kf[idx] = to_f32<T>(kk);
         qf[idx] = to_f32<T>(q[bhk * DK + idx]);
-        rk[(bh * C + r) * DK + idx] = kk;
+        if (cp == 0) rk[(bh * C + r) * DK + idx] = kk;
     }
-    for (int idx = tid; idx < DV; idx += 256) rv[(bh * C + r) * DV + idx] = v[bh * DV + idx];
+    for (int idx = tid; idx < DVS; idx += 256) rv[(bh * C + r) * DV + i0 + idx] = v[bh * DV + i0 + idx];
     if (tid == 0) {
         const float gg = a.g[bh], bb = a.beta[bh];
         sc[0] = decay_exp(gg);
         sc[1] = bb;
-        a.ring.g[bh * C + r] = gg;
-        a.ring.beta[bh * C + r] = bb;
+        if (cp == 0) {
+            a.ring.g[bh * C + r] = gg;
+            a.ring.beta[bh * C + r] = bb;
+        }
     }
     float s[L][VPT];
-    float* st = a.state + bh * DK * DV + (size_t)(m * L) * DV + lane * VPT;
+    float* st = a.state + bh * DK * DV + (size_t)(m * L) * DV + i0 + lane * VPT;
 #pragma unroll
     for (int t = 0; t < L; ++t) VecF<VPT>::load(st + (size_t)t * DV, s[t]);
     __syncthreads();
@@ -207,7 +220,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
         const int i = lane * VPT + e;
         const float x = tree8(part[0][i], part[1][i], part[2][i], part[3][i], part[4][i], part[5][i], part[6][i],
                               part[7][i]);
-        const float u = step_u(alpha, beta, to_f32<T>(v[bh * DV + i]), x);
+        const float u = step_u(alpha, beta, to_f32<T>(v[bh * DV + i0 + i]), x);
 #pragma unroll
         for (int t = 0; t < L; ++t) s[t][e] = step_s(s[t][e], alpha, u, kf[m * L + t]);
         float c = __fmul_rn(s[0][e], qf[m * L]);
@@ -225,7 +238,7 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
             const int i = lane * VPT + e;
             const float o = tree8(part2[0][i], part2[1][i], part2[2][i], part2[3][i], part2[4][i], part2[5][i],
                                   part2[6][i], part2[7][i]);
-            out[bh * DV + i] = from_f32<T>(o);
+            out[bh * DV + i0 + i] = from_f32<T>(o);
         }
     }
 }
@@ -656,9 +669,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     k5<<<grid, DK + DV, sm5, ss->stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.qk_norm)
-        k4_decode_step<DK, DV, C, T, true><<<dim3(a.B, a.Hk, a.H / a.Hk), 256, 0, s>>>(a);
+        k4_decode_step<DK, DV, C, T, true><<<dim3(a.B * k4_splits<DV>(), a.Hk, a.H / a.Hk), 256, 0, s>>>(a);
     else
-        k4_decode_step<DK, DV, C, T, false><<<dim3(a.B, a.Hk, a.H / a.Hk), 256, 0, s>>>(a);
+        k4_decode_step<DK, DV, C, T, false><<<dim3(a.B * k4_splits<DV>(), a.Hk, a.H / a.Hk), 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_mark(1, s);
     // join: work issued on s after this call sees the resync's results
