@@ -340,21 +340,27 @@ int32_t cpr_gdn_prefill_noalloc_status(uint32_t* status_out, void* stream);
  * NULL to switch the hook off.  While it is on, every cpr_gdn_prefill records
  * events[0] before its first kernel and events[i] after its i-th kernel (i = 1..3:
  * chunk index, chunk prep, boundary chain with the intra-chunk recurrence; needs
- * n_events >= 4), and every cpr_gdn_decode records events[0] before and events[1],
- * events[2] after its step and resync kernels.  Process-wide; not for concurrent calls
- * from several threads.
+ * n_events >= 4), every cpr_gdn_decode records events[0] before and events[1],
+ * events[2] after its step and resync kernels, and every cpr_gdn_backward records
+ * events[0] before its first kernel and events[1..4] after the chunk index, the chunk
+ * maps, the reverse chain and the chunk gradients (needs n_events >= 5; where the last two
+ * share one launch, events[3] is recorded before it).  Process-wide; not for concurrent
+ * calls from several threads.
  */
 int32_t cpr_gdn_set_profile_events(void* const* events, int32_t n_events);
 
 /*
- * Test hook for the failure path of the prefill's one device-side wait on other CTAs
- * (an intra-chunk item waiting for its boundary state to be published by the chain).
- * While extra_publications > 0, every item waits for that many publications more than
- * the chain ever makes, so each wait runs out after limit_ns nanoseconds (0: the
- * default of about 4 s), the item is skipped (its outputs are not written) and the call
- * records CPR_DEV_TIMEOUT in its status word; the context stays usable.
+ * Test hook for the failure path of the device-side waits on other CTAs: the prefill's
+ * (an intra-chunk item waiting for its boundary state to be published by the chain) and
+ * the backward's where its chain and chunk gradients share one launch (dk = dv = 128,
+ * C = 64, bf16: a chunk's gradients waiting for its state adjoint).  While
+ * extra_publications > 0, every such item waits for that many publications more than the
+ * chain ever makes, so each wait runs out after limit_ns nanoseconds (0: the default of
+ * about 4 s), the item is skipped (its outputs are not written) and the call records
+ * CPR_DEV_TIMEOUT in its status word; the context stays usable.
  * cpr_gdn_set_wait_test(0, 0) restores normal operation.  Process-wide, read when a
- * prefill is enqueued; not for concurrent use with other calls.  Returns CPR_OK.
+ * prefill or backward is enqueued; not for concurrent use with other calls.  Returns
+ * CPR_OK.
  */
 int32_t cpr_gdn_set_wait_test(uint32_t extra_publications, uint64_t limit_ns);
 

@@ -183,6 +183,8 @@ int32_t cpr_gdn_backward(const void* q, const void* k, const void* v, const floa
     a.d_end = reinterpret_cast<float*>(ws + lay.d_end);
     a.max_chunks = max_chunks_bound(total_tokens, n_seqs, C);
     a.num_sms = num_sms();
+    a.wait_extra = g_wait_extra;
+    a.wait_limit_ns = g_wait_limit_ns;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorInvalidValue;
 #define CPR_DISPATCH(DK, DV, CC)                                                                   \

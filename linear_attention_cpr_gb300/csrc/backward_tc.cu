@@ -778,7 +778,8 @@ __global__ void __launch_bounds__(kT, 1) kb23_chain_and_grads_tc(BackwardArgs a,
         if (u >= items) break;
         const int64_t c = (int64_t)(nchunks - 1 - u / (uint32_t)a.H);
         const int h = (int)(u % (uint32_t)a.H);
-        if (t == 0) wait_ok_s = wait_published(a.ready + (size_t)c * a.H + h, 1u, a.status, 0);
+        if (t == 0)
+            wait_ok_s = wait_published(a.ready + (size_t)c * a.H + h, 1u + a.wait_extra, a.status, a.wait_limit_ns);
         __syncthreads();
         if (!wait_ok_s) {
             if (t == 0) atomicOr(a.status, CPR_DEV_TIMEOUT);

@@ -157,6 +157,10 @@ struct BackwardArgs {
     float* d_end;
     int64_t max_chunks;
     int num_sms;
+    // the chunk gradients' wait for a published d_end (fused launch): the count it waits
+    // for is 1 + wait_extra (0 except in the timeout test), limit as PrefillArgs
+    uint32_t wait_extra;
+    uint64_t wait_limit_ns;
 };
 
 // Decode workspace: [0, 256) status word.
