@@ -252,36 +252,29 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
     };
 
     // A tile (128 rows x K = 128, hi/lo) from a stored state src[c][i] (128 x 128 fp32):
-    // transposed (rows i, K = c) or as stored (rows c, K = i).  Loads of NB items are
-    // issued before their splits are stored, so the memory latency is paid 8 / NB times per
-    // call rather than eight times.
+    // transposed (rows i, K = c) or as stored (rows c, K = i).  Consecutive threads take
+    // consecutive rows of one 8-element K group, so each warp's 16-byte stores fill whole
+    // 128-byte core-matrix rows (no bank conflicts); all eight loads of a thread are issued
+    // before its splits are stored.
     auto state_tile = [&](const float* src, bool transposed) {
-        constexpr int NB = 8;
+        float xs[8][8];
 #pragma unroll
-        for (int b = 0; b < 8 / NB; ++b) {
-            float xs[NB][8];
+        for (int u = 0; u < 8; ++u) {
+            const int idx = t + u * kT, row = idx % kD, k8 = (idx / kD) * 8;
+            if (transposed) {
 #pragma unroll
-            for (int u = 0; u < NB; ++u) {
-                const int idx = t + (NB * b + u) * kT;
-                if (transposed) {
-                    const int i = idx % kD, c8 = (idx / kD) * 8;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) xs[u][e] = __ldg(src + (size_t)(c8 + e) * kD + i);
-                } else {
-                    const int cc = idx >> 4, i8 = (idx & 15) * 8;
-                    const float4 p0 = __ldg(reinterpret_cast<const float4*>(src + (size_t)cc * kD + i8));
-                    const float4 p1 = __ldg(reinterpret_cast<const float4*>(src + (size_t)cc * kD + i8 + 4));
-                    xs[u][0] = p0.x, xs[u][1] = p0.y, xs[u][2] = p0.z, xs[u][3] = p0.w;
-                    xs[u][4] = p1.x, xs[u][5] = p1.y, xs[u][6] = p1.z, xs[u][7] = p1.w;
-                }
+                for (int e = 0; e < 8; ++e) xs[u][e] = __ldg(src + (size_t)(k8 + e) * kD + row);
+            } else {
+                const float4 p0 = __ldg(reinterpret_cast<const float4*>(src + (size_t)row * kD + k8));
+                const float4 p1 = __ldg(reinterpret_cast<const float4*>(src + (size_t)row * kD + k8 + 4));
+                xs[u][0] = p0.x, xs[u][1] = p0.y, xs[u][2] = p0.z, xs[u][3] = p0.w;
+                xs[u][4] = p1.x, xs[u][5] = p1.y, xs[u][6] = p1.z, xs[u][7] = p1.w;
             }
+        }
 #pragma unroll
-            for (int u = 0; u < NB; ++u) {
-                const int idx = t + (NB * b + u) * kT;
-                const int row = transposed ? idx % kD : idx >> 4;
-                const int k8 = transposed ? (idx / kD) * 8 : (idx & 15) * 8;
-                tc::split8_store(xs[u], TA + toff<kD>(row, k8), TA + 32768 + toff<kD>(row, k8));
-            }
+        for (int u = 0; u < 8; ++u) {
+            const int idx = t + u * kT, row = idx % kD, k8 = (idx / kD) * 8;
+            tc::split8_store(xs[u], TA + toff<kD>(row, k8), TA + 32768 + toff<kD>(row, k8));
         }
     };
     if (t == 0) {  // both states are read several times: into L2 now
@@ -347,10 +340,28 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
         }
         state_tile(Sb, true);  // A: S_b[i][c], rows i, K = c
         run_begin([&] { mma_ab<kD, 2, 1>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
-        {  // dgam_last = <dS_end, S_b> while the product runs: a fixed order per thread, then fixed trees
-            float sd = 0.0f;
-#pragma unroll 4
-            for (int idx = t; idx < (int)SSZ; idx += kT) sd = __fmaf_rn(__ldg(dSe + idx), __ldg(Sb + idx), sd);
+        {  // dgam_last = <dS_end, S_b> while the product runs: a fixed order per thread (four
+           // component sums over its float4s, eight of each state's loads in flight), then
+           // fixed trees
+            float4 a4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float4 xd[8], xs[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i4 = t + (8 * b + u) * kT;
+                    xd[u] = __ldg(reinterpret_cast<const float4*>(dSe) + i4);
+                    xs[u] = __ldg(reinterpret_cast<const float4*>(Sb) + i4);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    a4.x = __fmaf_rn(xd[u].x, xs[u].x, a4.x);
+                    a4.y = __fmaf_rn(xd[u].y, xs[u].y, a4.y);
+                    a4.z = __fmaf_rn(xd[u].z, xs[u].z, a4.z);
+                    a4.w = __fmaf_rn(xd[u].w, xs[u].w, a4.w);
+                }
+            }
+            float sd = __fadd_rn(__fadd_rn(a4.x, a4.y), __fadd_rn(a4.z, a4.w));
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) sd = __fadd_rn(sd, __shfl_xor_sync(0xffffffffu, sd, o));
             if (lane == 0) red[256 + w] = sd;
