@@ -694,6 +694,8 @@ def run_ours(args):
 
 def run_decode(args, cpr, inputs, dev, hbm_peak, dist, world):
     w = inputs.workload("rollout_decode")
+    if args.decode_context:  # shorter prior contexts (profiling): the same positions modulo C
+        w.seqlens = [(int(L) - 1) % args.decode_context + 1 for L in w.seqlens]
     B, H, dk, dv, C = len(w.seqlens), w.H, w.dk, w.dv, w.C
     x = inputs.prefill_inputs(w, device=dev)  # prior context, drawn on the device
     n_chunks = cpr.cpr_gdn_num_chunks(inputs.cu_seqlens_of(w.seqlens), C)
@@ -701,6 +703,7 @@ def run_decode(args, cpr, inputs, dev, hbm_peak, dist, world):
                                          n_chunks=n_chunks)
     ring = cpr.cpr_gdn_ring_from_prefill(x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], C, bnd, st)
     del x, bnd, ws
+    torch.cuda.empty_cache()
     state = st
     n_steps = args.decode_steps
     toks = [inputs.decode_inputs(w, s, device=dev) for s in range(n_steps)]
@@ -762,7 +765,8 @@ def run_decode(args, cpr, inputs, dev, hbm_peak, dist, world):
     return {
         "metric": "decode steps/s per layer", "value": 1e3 / ms * world, "unit": "steps/s",
         "ms_per_step": ms, "steps": n_steps, "workload": f"rollout_decode: B={B}, H={H}, dk=dv={dk}, C={C}, "
-        "prior lengths U[1,4096], state resident (> L2)",
+        + (f"prior lengths U[1,4096] capped at {args.decode_context} (profiling)" if args.decode_context
+           else "prior lengths U[1,4096]") + ", state resident (> L2)",
         "kernels_ms": {"step_with_concurrent_resync": k4_ms, "join": statistics.fmean(k5)},
         "resyncs_per_step": n_res / n_steps,
         "roofline": {"kernel": "k4_decode_step", "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
@@ -947,6 +951,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="trainer_fwd")
     ap.add_argument("--decode-steps", type=int, default=512)
+    ap.add_argument("--decode-context", type=int, default=0,
+                    help="cap the rollout_decode prior contexts at this many tokens (a multiple of C, for "
+                         "profiling: the state and the step are unchanged, the prior prefill smaller)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pik", action="store_true")
