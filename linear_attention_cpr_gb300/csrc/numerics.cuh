@@ -156,29 +156,6 @@ __device__ __forceinline__ float a_entry(float beta_r, float Gr, float Gi, float
     return __fmul_rn(__fmul_rn(beta_r, decay_exp(__fsub_rn(Gr, Gi))), kk);
 }
 
-// Forward substitution of one column: x[r] = init[r] - sum_{i<r} A[r][i] x[i],
-// accumulated as fma(-A_ri, x_i, .) for i ascending.  At: fp32 smem [C][C] holding A
-// transposed (At[i * C + r] = A_ri, 16-byte aligned rows).  The loops run column-outermost
-// (x[t] is final once the terms of columns < t are in), so consecutive instructions are
-// independent and a column's coefficients come in 16-byte loads; every row still adds
-// its terms in ascending i, which is the operation sequence above.
-template <int C>
-__device__ __forceinline__ void fwd_subst(const float* At, float x[C])
-{
-#pragma unroll
-    for (int t = 0; t < C - 1; ++t) {
-        const float xt = x[t];
-#pragma unroll
-        for (int r4 = ((t + 1) / 4) * 4; r4 < C; r4 += 4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(At + t * C + r4);
-            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (r4 + e > t) x[r4 + e] = __fmaf_rn(-av[e], xt, x[r4 + e]);
-        }
-    }
-}
-
 // T = (I + A)^-1 of a strictly lower-triangular C x C matrix A by blocks of 16, with all
 // `nt` threads of the caller: the four (C / 16) diagonal blocks by forward substitution,
 // one column per thread (x_r = [r == j] - sum_{i<r} A_ri x_i, fma in ascending i), then

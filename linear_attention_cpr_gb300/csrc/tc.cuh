@@ -138,7 +138,7 @@ __device__ __forceinline__ void prefetch_l2(const void* gmem, uint32_t bytes)
 }
 
 // Bulk copy shared -> global (both 16-byte aligned, bytes a multiple of 16), tracked by
-// this thread's bulk group: commit with bulk_commit, wait with bulk_wait_read.
+// this thread's bulk group: commit with bulk_commit, wait with bulk_wait_all.
 __device__ __forceinline__ void bulk_s2g(void* gmem, const void* smem, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gmem), "r"(smem_u32(smem)),
@@ -146,8 +146,6 @@ __device__ __forceinline__ void bulk_s2g(void* gmem, const void* smem, uint32_t 
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
-// Wait until every committed bulk store of this thread has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 // Wait until every committed bulk store of this thread is complete.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 
