@@ -183,6 +183,12 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
     T* rk = static_cast<T*>(a.ring.k);
     T* rv = static_cast<T*>(a.ring.v);
 
+    // the state's loads first: their latency overlaps the token's loads below (the ring's
+    // stores there could otherwise keep them from being issued early)
+    float s[L][VPT];
+    float* st = a.state + bh * DK * DV + (size_t)(m * L) * DV + i0 + lane * VPT;
+#pragma unroll
+    for (int t = 0; t < L; ++t) VecF<VPT>::load(st + (size_t)t * DV, s[t]);
     for (int idx = tid; idx < DK; idx += 256) {
         const T kk = k[bhk * DK + idx];
         kf[idx] = to_f32<T>(kk);
@@ -199,10 +205,6 @@ __global__ void __launch_bounds__(256) k4_decode_step(DecodeArgs a)
             a.ring.beta[bh * C + r] = bb;
         }
     }
-    float s[L][VPT];
-    float* st = a.state + bh * DK * DV + (size_t)(m * L) * DV + i0 + lane * VPT;
-#pragma unroll
-    for (int t = 0; t < L; ++t) VecF<VPT>::load(st + (size_t)t * DV, s[t]);
     __syncthreads();
     if (QK_NORM) l2_normalise_qk<DK>(kf, qf, sc + 2);  // (a separate build: the usual one is untouched)
 
@@ -621,6 +623,9 @@ __global__ void __launch_bounds__(256) k6_ring_fill(RingArgs a)
 
 namespace {
 // Per-device side stream and fork/join events of the decode launch (created on first use).
+// The side stream has the device's greatest priority: its few resync CTAs are placed as
+// soon as an SM has room, ahead of the step kernel's waiting CTAs, so they run beside the
+// step instead of after it.
 struct SideStream {
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
@@ -637,7 +642,10 @@ cudaError_t side_stream(SideStream*& out)
     SideStream& ss = per_device[dev];
     std::lock_guard<std::mutex> lock(create);
     if (!ss.join) {
-        if (!ss.stream && (e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        int least = 0, greatest = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+        if (!ss.stream && (e = cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, greatest)) != cudaSuccess)
+            return e;
         if (!ss.fork && (e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
         if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
     }
