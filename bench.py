@@ -45,7 +45,7 @@ L2_BYTES = 129 * 1024 * 1024
 # of the kernel as it now stands: k23_chain_and_intra at trainer_fwd, k4_decode_step at
 # rollout_decode.  Reset to None whenever the kernel changes.
 TRAFFIC_K23_TRAINER_FWD = 531.102976e6 + 194.182912e6
-TRAFFIC_K4_ROLLOUT_DECODE = None
+TRAFFIC_K4_ROLLOUT_DECODE = 267.595520e6 + 208.146688e6
 
 
 def _peaks():
