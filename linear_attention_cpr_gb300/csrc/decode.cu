@@ -263,11 +263,13 @@ __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t
 {
     constexpr int L = DK / 8, VPT = DV / 32;
     constexpr bool kBoxes = sizeof(T) == 2;
-    __shared__ __align__(16) float kf[DK];
-    __shared__ __align__(16) float qf[DK];
-    __shared__ __align__(16) float part[8][DV];
-    __shared__ __align__(16) float part2[8][DV];
-    __shared__ float sc[4];
+    // token t uses buffer t & 1 of the key, query, scalars and partial sums, so the next
+    // token's staging may start while warp 0 still finishes this token's output
+    __shared__ __align__(16) float kf2[2][DK];
+    __shared__ __align__(16) float qf2[2][DK];
+    __shared__ __align__(16) float pa2[2][8][DV];
+    __shared__ __align__(16) float pb2[2][8][DV];
+    __shared__ float sc2[2][4];
     __shared__ float sg[C], sbeta[C];
     __shared__ uint64_t tile_bar;
     extern __shared__ __align__(128) unsigned char sm8[];  // (2-byte inputs) keys, queries, values [C][d]
@@ -324,6 +326,9 @@ __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t
     for (int t = 0; t < f; ++t) {
         const size_t tok = ((size_t)t0 + t) * H + h;  // packed token index x H + h
         const int r = r0 + t;                          // its ring slot
+        float* kf = kf2[t & 1];
+        float* qf = qf2[t & 1];
+        float* sc = sc2[t & 1];
         if constexpr (kBoxes) {
             for (int idx = tid; idx < DK; idx += 256) {
                 const T kk = sk[t * DK + idx];
@@ -358,9 +363,11 @@ __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t
         }
         __syncthreads();
         if (a.qk_norm) l2_normalise_qk<DK>(kf, qf, sc + 2);
-        token_step<DK, DV, T>(s, kf, qf, part, part2, sc[0], sc[1], kBoxes ? sv + t * DV : v + tok * DV,
+        token_step<DK, DV, T>(s, kf, qf, pa2[t & 1], pb2[t & 1], sc[0], sc[1], kBoxes ? sv + t * DV : v + tok * DV,
                               out + tok * DV, t + 1 == f ? st : nullptr);
-        __syncthreads();  // kf, qf, sc and the partial sums are rewritten for the next token
+        // (no barrier: the next token writes the other buffers; this token's were last read
+        // before a barrier the next token's threads pass, or by warp 0 before it reaches the
+        // next token's first barrier)
     }
 }
 
