@@ -385,11 +385,16 @@ __global__ void __launch_bounds__(256) k8_chunk_fill(DecodeArgs a, const int32_t
 // The output of this step's token for (b, h), from the state before the step, by the
 // element sequence of k4 (per value column i: the eight chains of S k as fmul then fma
 // over their DK/8 rows, the canonical tree, u, then the chains of S' q over the stepped
-// rows).  Threads i < DV take column i; the stepped state itself is not kept.  kf, qf:
-// DK floats of shared scratch each, part: 8 * DV.  Ends with a barrier.
+// rows).  Threads i < DV take column i; the stepped state itself is not kept.  The state
+// is read from a shared-memory copy (Ssm, laid out as stored) whose bulk copy completes on
+// mbar's phase `phase` (the step kernel keeps HBM busy meanwhile, so one copy in flight
+// beats a round trip per chain).  kf, qf: DK floats of shared scratch each, part: 8 DV
+// (the key normalisation's scratch, then the chains of each value column).  Returns false
+// (uniformly) if the copy did not land in time.
+// Ends with a barrier.
 template <int DK, int DV, int C, typename T, bool QK_NORM>
-__device__ __forceinline__ void completing_token_output(const DecodeArgs& a, size_t bh, float* kf, float* qf,
-                                                        float* part)
+__device__ __forceinline__ bool completing_token_output(const DecodeArgs& a, size_t bh, const float* Ssm, float* kf,
+                                                        float* qf, float* part, uint64_t* mbar, uint32_t& phase)
 {
     constexpr int L = DK / 8;
     const int tid = threadIdx.x;
@@ -400,34 +405,42 @@ __device__ __forceinline__ void completing_token_output(const DecodeArgs& a, siz
         kf[idx] = to_f32<T>(k[bhk * DK + idx]);
         qf[idx] = to_f32<T>(q[bhk * DK + idx]);
     }
-    __syncthreads();
-    if (QK_NORM) l2_normalise_qk<DK>(kf, qf, part);  // (part is free until the dots)
+    float g = 0.0f, beta = 0.0f, vi = 0.0f;
+    if (tid < DV) {
+        g = a.g[bh];
+        beta = a.beta[bh];
+        vi = to_f32<T>(static_cast<const T*>(a.v)[bh * DV + tid]);
+    }
+    const bool ok = __syncthreads_and(tc::mbar_wait(mbar, phase & 1));
+    ++phase;
+    if (!ok) return false;
+    if (QK_NORM) l2_normalise_qk<DK>(kf, qf, part);
     if (tid < DV) {
         const int i = tid;
-        const float* S = a.state + bh * DK * DV + i;  // S[c][i] at c * DV
-        const float alpha = decay_exp(a.g[bh]), beta = a.beta[bh];
+        const float* S = Ssm + i;  // S[c][i] at c * DV
+        const float alpha = decay_exp(g);
         float* c = part + i;  // chain m at c[m * DV]
 #pragma unroll 1
         for (int m = 0; m < 8; ++m) {
-            float acc = __fmul_rn(S[(size_t)(m * L) * DV], kf[m * L]);
+            float acc = __fmul_rn(S[(m * L) * DV], kf[m * L]);
 #pragma unroll
-            for (int t = 1; t < L; ++t) acc = __fmaf_rn(S[(size_t)(m * L + t) * DV], kf[m * L + t], acc);
+            for (int t = 1; t < L; ++t) acc = __fmaf_rn(S[(m * L + t) * DV], kf[m * L + t], acc);
             c[m * DV] = acc;
         }
         const float x = tree8(c[0], c[DV], c[2 * DV], c[3 * DV], c[4 * DV], c[5 * DV], c[6 * DV], c[7 * DV]);
-        const float u = step_u(alpha, beta, to_f32<T>(static_cast<const T*>(a.v)[bh * DV + i]), x);
+        const float u = step_u(alpha, beta, vi, x);
 #pragma unroll 1
         for (int m = 0; m < 8; ++m) {
-            float acc = __fmul_rn(step_s(S[(size_t)(m * L) * DV], alpha, u, kf[m * L]), qf[m * L]);
+            float acc = __fmul_rn(step_s(S[(m * L) * DV], alpha, u, kf[m * L]), qf[m * L]);
 #pragma unroll
-            for (int t = 1; t < L; ++t)
-                acc = __fmaf_rn(step_s(S[(size_t)(m * L + t) * DV], alpha, u, kf[m * L + t]), qf[m * L + t], acc);
+            for (int t = 1; t < L; ++t) acc = __fmaf_rn(step_s(S[(m * L + t) * DV], alpha, u, kf[m * L + t]), qf[m * L + t], acc);
             c[m * DV] = acc;
         }
         const float o = tree8(c[0], c[DV], c[2 * DV], c[3 * DV], c[4 * DV], c[5 * DV], c[6 * DV], c[7 * DV]);
         static_cast<T*>(a.out)[bh * DV + i] = from_f32<T>(o);
     }
-    __syncthreads();  // every read of the old state is done before the resync replaces it
+    __syncthreads();  // every read of the copy is done before its space is reused
+    return true;
 }
 template <int DK, int DV, int C, typename T, bool QK_NORM>
 __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, unsigned char* sm5, uint32_t tmem,
@@ -453,17 +466,52 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     const size_t bhk = (size_t)b * a.Hk + qk_head(h, H, a.Hk);
     const T* tk = a.resync_only ? rk + (size_t)(C - 1) * DK : static_cast<const T*>(a.k) + bhk * DK;
     const T* tv = a.resync_only ? rv + (size_t)(C - 1) * DV : static_cast<const T*>(a.v) + bh * DV;
-    if (!a.resync_only)
-        completing_token_output<DK, DV, C, T, QK_NORM>(a, bh, reinterpret_cast<float*>(sm5), reinterpret_cast<float*>(sm5) + DK,
-                                              reinterpret_cast<float*>(sm5) + 2 * DK);
-
-    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-        const int r = idx / DK, j = idx % DK;
-        s.kf[r * KS + j] = to_f32<T>(r < C - 1 ? rk[idx] : tk[j]);
+    float* Ssm = reinterpret_cast<float*>(sm5 + U::RS_BT_OFF);  // the state's copy (the prep's later regions)
+    if (tid == 0) {
+        tc::prefetch_l2(a.ring.S_b + bh * SS, (uint32_t)(SS * sizeof(float)));  // read by the chain step
+        if (!a.resync_only) {
+            constexpr uint32_t BYTES = (uint32_t)(DK * DV * sizeof(float)), PIECE = 16384;
+            tc::fence_proxy_async();  // (the previous pair's generic accesses to the region)
+            tc::mbar_arrive_expect_tx(mbar, BYTES);
+            for (uint32_t off = 0; off < BYTES; off += PIECE)
+                tc::bulk_g2s(reinterpret_cast<unsigned char*>(Ssm) + off,
+                             reinterpret_cast<const unsigned char*>(a.state + bh * SS) + off, min(PIECE, BYTES - off),
+                             mbar);
+        }
     }
-    for (int idx = tid; idx < C * DV; idx += blockDim.x) {
-        const int r = idx / DV, n = idx % DV;
-        vsm[idx] = r < C - 1 ? rv[idx] : tv[n];
+    // the chunk's keys and values, 16 bytes a load, every load of a thread in flight at once
+    // (issued before the token's output, stored after it)
+    constexpr int VE = 16 / (int)sizeof(T), KV = DK / VE, VV = DV / VE;
+    constexpr int NKV = C * KV, NVEC = NKV + C * VV, PT = (NVEC + DK + DV - 1) / (DK + DV);
+    uint4 w[PT];
+#pragma unroll
+    for (int e = 0; e < PT; ++e) {
+        const int idx = tid + e * (DK + DV);
+        if (idx < NKV) {
+            const int r = idx / KV, j = (idx % KV) * VE;
+            w[e] = __ldg(reinterpret_cast<const uint4*>((r < C - 1 ? rk + (size_t)r * DK : tk) + j));
+        } else if (idx < NVEC) {
+            const int r = (idx - NKV) / VV, n = ((idx - NKV) % VV) * VE;
+            w[e] = __ldg(reinterpret_cast<const uint4*>((r < C - 1 ? rv + (size_t)r * DV : tv) + n));
+        }
+    }
+    if (!a.resync_only &&
+        !completing_token_output<DK, DV, C, T, QK_NORM>(a, bh, Ssm, reinterpret_cast<float*>(sm5),
+                                                        reinterpret_cast<float*>(sm5) + DK,
+                                                        reinterpret_cast<float*>(sm5) + 2 * DK, mbar, phase))
+        return false;
+#pragma unroll
+    for (int e = 0; e < PT; ++e) {
+        const int idx = tid + e * (DK + DV);
+        if (idx < NKV) {
+            const int r = idx / KV, j = (idx % KV) * VE;
+            const T* x = reinterpret_cast<const T*>(&w[e]);
+#pragma unroll
+            for (int q = 0; q < VE; ++q) s.kf[r * KS + j + q] = to_f32<T>(x[q]);
+        } else if (idx < NVEC) {
+            const int r = (idx - NKV) / VV, n = ((idx - NKV) % VV) * VE;
+            *reinterpret_cast<uint4*>(vsm + (size_t)r * DV + n) = w[e];
+        }
     }
     if (tid < C) {
         const bool ring_slot = tid < C - 1 || a.resync_only;
