@@ -15,7 +15,10 @@
 // cores' K-major core-matrix layout: bf16 inputs exactly (one split), everything derived in
 // fp32 as Dekker hi/lo splits (tc::split_f32), and each product is the sum of the split
 // products hi*hi (+ hi*lo) (+ lo*hi), accumulated in fp32 in TMEM (about 2^-16 relative per
-// term).  Results come back with tcgen05.ld, one accumulator row (TMEM lane) and 32
+// term).  A tile can also be read MN-major (the descriptor's transpose bit), so the chunk's
+// keys, its dO and each state are written once and serve as a matrix and its transpose:
+// the products that read S_b both ways (and dS_end both ways) share one run.  Results
+// come back with tcgen05.ld, one accumulator row (TMEM lane) and 32
 // columns per thread; dq^T and dk^T accumulate in registers across products.  Sums over
 // the 128 rows (a key or value index) of a result use a fixed butterfly over the warp's
 // lanes and a fixed sum over the four lane quadrants, so the gradients are reproducible
@@ -65,39 +68,6 @@ __device__ __forceinline__ uint32_t toff(int row, int k)
     return tc::tile_off<2>(row, k, K);
 }
 
-// The calling thread holds x[jj] = element (row 32 hc + jj, K index m) of a K-major split
-// tile (m = 32 q + lane, this thread's accumulator row).  Within each group of 8 lanes an
-// 8 x 8 register transpose (three rounds of exchanges) gives lane p the 8 consecutive K
-// elements of row 32 hc + 8 blk + p, which it stores as one 16-byte hi/lo pair.
-template <int K>
-__device__ __forceinline__ void transpose_store(const float (&x)[32], unsigned char* base, uint32_t split, int m,
-                                                int hc)
-{
-    const int p = threadIdx.x & 7, kb = m - p;
-#pragma unroll
-    for (int blk = 0; blk < 4; ++blk) {
-        float a[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a[e] = x[8 * blk + e];
-#pragma unroll
-        for (int sw = 4; sw >= 1; sw >>= 1) {
-            const bool upper = (p & sw) != 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (e & sw) continue;
-                const float send = upper ? a[e] : a[e + sw];
-                const float recv = __shfl_xor_sync(0xffffffffu, send, sw);
-                if (upper)
-                    a[e] = recv;
-                else
-                    a[e + sw] = recv;
-            }
-        }
-        const uint32_t off = tc::tile_off<2>(32 * hc + 8 * blk + p, kb, K);
-        tc::split8_store(a, base + off, base + split + off);
-    }
-}
-
 // D (TMEM) (+)= A (128 x K tile at a) * B (64 x K tile at b)^T; NA, NB: splits present in
 // each tile (1: hi only, exact bf16; 2: hi and lo).  Products hi*hi, then hi*lo (NB = 2),
 // then lo*hi (NA = 2), K ascending in each; the first instruction overwrites D unless
@@ -115,6 +85,43 @@ __device__ __forceinline__ void mma_ab(uint32_t d, uint32_t a, uint32_t b, bool 
         for (int k = 0; k < K / 16; ++k)
             tc::mma_bf16(d, tc::sdesc(a + pa[p] * ASPL + k * 256, 128, SBO),
                          tc::sdesc(b + pb[p] * BSPL + k * 256, 128, SBO), idesc,
+                         (accumulate || p != 0 || k != 0) ? 1u : 0u);
+    }
+}
+
+// One operand of a product in shared memory: its hi split at `base` (lo at base + split),
+// the descriptor's LBO and SBO, the byte step per 16 K elements, and whether the tensor
+// cores read it MN-major (the instruction descriptor's transpose bit for A or B).
+struct Opnd {
+    uint32_t base, split, lbo, sbo, kstep;
+    bool mn;
+};
+// A K-major tile of `rows` rows x K elements (toff<K>(row, k)): rows are the operand's M or N.
+__device__ __forceinline__ Opnd kmaj(const unsigned char* p, int rows, int K)
+{
+    return Opnd{tc::smem_u32(p), (uint32_t)(rows * K * 2), 128u, (uint32_t)(K / 8 * 128), 256u, false};
+}
+// The same kind of tile, X[a][b] at toff<W>(a, b) with `rows` rows a, read MN-major: the
+// operand's M or N index is b and its K index a (LBO steps 8 rows a, SBO 8 columns b), so
+// one image serves a matrix and its transpose.
+__device__ __forceinline__ Opnd mnview(const unsigned char* p, int rows, int W)
+{
+    return Opnd{tc::smem_u32(p), (uint32_t)(rows * W * 2), (uint32_t)(W / 8 * 128), 128u, (uint32_t)(W * 32), true};
+}
+
+// D (TMEM, 128 x 64) (+)= A * B^T over K elements, the split products as in mma_ab.
+template <int K, int NA, int NB>
+__device__ __forceinline__ void mma2(uint32_t d, const Opnd& A, const Opnd& B, bool accumulate)
+{
+    const uint32_t idesc = tc::idesc_bf16(128, 64) | (A.mn ? 1u << 15 : 0u) | (B.mn ? 1u << 16 : 0u);
+    const uint32_t pa[3] = {0u, 0u, 1u}, pb[3] = {0u, 1u, 0u};
+#pragma unroll
+    for (int p = 0; p < 3; ++p) {
+        if ((p == 1 && NB != 2) || (p == 2 && NA != 2)) continue;
+#pragma unroll
+        for (int k = 0; k < K / 16; ++k)
+            tc::mma_bf16(d, tc::sdesc(A.base + pa[p] * A.split + k * A.kstep, A.lbo, A.sbo),
+                         tc::sdesc(B.base + pb[p] * B.split + k * B.kstep, B.lbo, B.sbo), idesc,
                          (accumulate || p != 0 || k != 0) ? 1u : 0u);
     }
 }
@@ -152,8 +159,10 @@ struct V16 {
 __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t c, int h, unsigned char* sm,
                                                  uint32_t tmem, uint32_t& phase)
 {
-    __nv_bfloat16* Kp = reinterpret_cast<__nv_bfloat16*>(sm + KP_OFF);
-    __nv_bfloat16* Op = reinterpret_cast<__nv_bfloat16*>(sm + OP_OFF);
+    // the chunk's K and dO as K-major images (rows r, K = c: toff<kD>(r, c)), read in both
+    // orientations by the products
+    unsigned char* KI = sm + KP_OFF;
+    unsigned char* OI = sm + OP_OFF;
     unsigned char* TA = sm + TA_OFF;
     unsigned char* TB = sm + TB_OFF;
     unsigned char* TU = sm + TU_OFF;
@@ -189,8 +198,8 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
             wk = __ldg(reinterpret_cast<const uint4*>(gk + ((t0 + r) * H + h) * kD + cv));
             wo = __ldg(reinterpret_cast<const uint4*>(go + ((t0 + r) * H + h) * kD + cv));
         }
-        *reinterpret_cast<uint4*>(Kp + r * kD + cv) = wk;
-        *reinterpret_cast<uint4*>(Op + r * kD + cv) = wo;
+        *reinterpret_cast<uint4*>(KI + toff<kD>(r, cv)) = wk;
+        *reinterpret_cast<uint4*>(OI + toff<kD>(r, cv)) = wo;
     }
     if (t < kN) {
         v.gin[t] = t < len ? a.g[(t0 + t) * H + h] : 0.0f;
@@ -199,6 +208,7 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    auto kp = [&](int r, int c) { return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(KI + toff<kD>(r, c))); };
     const uint32_t lanes = (uint32_t)(32 * q) << 16;
     if (t == 0) {
         float G = 0.0f;
@@ -288,20 +298,19 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
 
     // ---- F1, F2: K K^T and Q K^T (n x n)
     {
-        for (int idx = t; idx < kN * 16; idx += kT) {
+        for (int idx = t; idx < kN * 16; idx += kT) {  // A: K and Q, rows t < 64 (zero rows after)
             const int r = idx >> 4, cv = (idx & 15) * 8;
-            const uint4 kw = *reinterpret_cast<const uint4*>(Kp + r * kD + cv);
+            const uint4 kw = *reinterpret_cast<const uint4*>(KI + toff<kD>(r, cv));
             uint4 qw = make_uint4(0u, 0u, 0u, 0u);
             if (r < len) qw = __ldg(reinterpret_cast<const uint4*>(gq + ((t0 + r) * H + h) * kD + cv));
             *reinterpret_cast<uint4*>(TA + toff<kD>(r, cv)) = kw;
             *reinterpret_cast<uint4*>(TA + 32768 + toff<kD>(r, cv)) = qw;
-            *reinterpret_cast<uint4*>(TB + toff<kD>(r, cv)) = kw;
         }
         zero_upper(TA, kD, false);
         zero_upper(TA + 32768, kD, false);
         run([&] {
-            mma_ab<kD, 1, 1>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false);
-            mma_ab<kD, 1, 1>(tmem + P1, tc::smem_u32(TA + 32768), tc::smem_u32(TB), false);
+            mma2<kD, 1, 1>(tmem + P0, kmaj(TA, 128, kD), kmaj(KI, kN, kD), false);
+            mma2<kD, 1, 1>(tmem + P1, kmaj(TA + 32768, 128, kD), kmaj(KI, kN, kD), false);
         });
         if (q < 2) {  // rows t < 64
             float kk[32], qk[32];
@@ -330,7 +339,10 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
     }
     float dqT[32], dkT[32], RT[32];  // row m (key index for dq/dk, value index for R), columns 32 hc + jj
 
-    // ---- F3: KS^T = S_b K^T;  R^T = V^T - KS^T diag(gam)
+    // ---- F3 and B1 in one run, both from one image of S_b as stored (rows c, K = i), F3
+    //      reading it MN-major:
+    //      F3: KS^T = S_b K^T;  R^T = V^T - KS^T diag(gam)
+    //      B1: Y^T = S_b^T dO^T:  dq^T = Y^T diag(gam);  dgam = colsum(Y^T o Q^T)
     if (alive) {
         float vv[32];  // issued first: their latency overlaps the gather of S_b
 #pragma unroll
@@ -338,9 +350,12 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
             const int r = 32 * hc + jj;
             vv[jj] = r < len ? __bfloat162float(gv[((t0 + r) * H + h) * kD + m]) : 0.0f;
         }
-        state_tile(Sb, true);  // A: S_b[i][c], rows i, K = c
-        run_begin([&] { mma_ab<kD, 2, 1>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
-        {  // dgam_last = <dS_end, S_b> while the product runs: a fixed order per thread (four
+        state_tile(Sb, false);
+        run_begin([&] {
+            mma2<kD, 2, 1>(tmem + P0, mnview(TA, kD, kD), kmaj(KI, kN, kD), false);
+            mma2<kD, 2, 1>(tmem + P1, kmaj(TA, kD, kD), kmaj(OI, kN, kD), false);
+        });
+        {  // dgam_last = <dS_end, S_b> while the products run: a fixed order per thread (four
            // component sums over its float4s, eight of each state's loads in flight), then
            // fixed trees
             float4 a4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -366,33 +381,26 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
             for (int o = 16; o >= 1; o >>= 1) sd = __fadd_rn(sd, __shfl_xor_sync(0xffffffffu, sd, o));
             if (lane == 0) red[256 + w] = sd;
         }
+        float qv[32];  // (their latency overlaps the products' end)
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int r = 32 * hc + jj;
+            qv[jj] = r < len ? __bfloat162float(gq[((t0 + r) * H + h) * kD + m]) : 0.0f;
+        }
         run_end();
         if (t == 0) {
             float d = 0.0f;
             for (int i = 0; i < 8; ++i) d = __fadd_rn(d, red[256 + i]);
             v.misc[0] = d;
         }
-        float ks[32];
-        acc(P0, ks);
+        {
+            float ks[32];
+            acc(P0, ks);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) RT[jj] = __fsub_rn(vv[jj], __fmul_rn(v.gam[32 * hc + jj], ks[jj]));
-    }
-    // ---- B1: Y^T = S_b^T dO^T:  dq^T = Y^T diag(gam);  dgam = colsum(Y^T o Q^T)
-    if (alive) {
-        state_tile(Sb, false);  // A: S_b^T, rows c, K = i (as stored)
-        for (int idx = t; idx < kN * 16; idx += kT) {  // B: dO, rows t, K = i
-            const int r = idx >> 4, cv = (idx & 15) * 8;
-            *reinterpret_cast<uint4*>(TB + toff<kD>(r, cv)) = *reinterpret_cast<const uint4*>(Op + r * kD + cv);
+            for (int jj = 0; jj < 32; ++jj) RT[jj] = __fsub_rn(vv[jj], __fmul_rn(v.gam[32 * hc + jj], ks[jj]));
         }
-        float qv[32];
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int r = 32 * hc + jj;
-            qv[jj] = r < len ? __bfloat162float(gq[((t0 + r) * H + h) * kD + m]) : 0.0f;
-        }
-        run([&] { mma_ab<kD, 2, 1>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
         float y[32];
-        acc(P0, y);
+        acc(P1, y);
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
             dqT[jj] = __fmul_rn(v.gam[32 * hc + jj], y[jj]);
@@ -403,7 +411,8 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
         __syncthreads();
         if (t < kN) v.dgam1[t] = __fadd_rn(__fadd_rn(red[t], red[64 + t]), __fadd_rn(red[128 + t], red[192 + t]));
     }
-    // ---- F4: U^T = (R^T diag(beta)) T^T  -> the U tile (rows r, K = i) for B2 and B4
+    // ---- F4: U^T = (R^T diag(beta)) T^T  -> the U^T image (rows i, 64 columns t), B of B2
+    //      and B4 read MN-major
     if (alive) {
 #pragma unroll
         for (int e8 = 0; e8 < 32; e8 += 8) {  // A: rows i, K = r (this thread's row)
@@ -422,16 +431,20 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
         run([&] { mma_ab<kN, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
         float u[32];
         acc(P0, u);
-        transpose_store<kD>(u, TU, 16384, m, hc);  // U tile rows r, K = i
+#pragma unroll
+        for (int e8 = 0; e8 < 32; e8 += 8) {
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = u[e8 + e];
+            tc::split8_store(xs, TU + toff<kN>(m, 32 * hc + e8), TU + 16384 + toff<kN>(m, 32 * hc + e8));
+        }
     }
     // ---- B2: dPm = (dO U^T) o lower;  ED += dPm o Pm;  dQK = dPm o E  (tiles for B5, B6)
     if (alive) {
-        for (int idx = t; idx < kN * 16; idx += kT) {  // A: dO, rows t, K = i
-            const int r = idx >> 4, cv = (idx & 15) * 8;
-            *reinterpret_cast<uint4*>(TA + toff<kD>(r, cv)) = *reinterpret_cast<const uint4*>(Op + r * kD + cv);
-        }
+        for (int idx = t; idx < kN * 16; idx += kT)  // A: dO, rows t < 64 (its image), zero rows after
+            reinterpret_cast<uint4*>(TA)[idx] = reinterpret_cast<const uint4*>(OI)[idx];
         zero_upper(TA, kD, false);
-        run([&] { mma_ab<kD, 1, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TU), false); });
+        run([&] { mma2<kD, 1, 2>(tmem + P0, kmaj(TA, 128, kD), mnview(TU, kD, kN), false); });
         if (q < 2) {
             float dp[32], col[32], rowp = 0.0f;
             acc(P0, dp);
@@ -445,13 +458,12 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
                 dp[jj] = r <= m ? __fmul_rn(x, e_of(m, r)) : 0.0f;  // dQK
             }
 #pragma unroll
-            for (int e8 = 0; e8 < 32; e8 += 8) {  // dQK tile: rows t, K = r
+            for (int e8 = 0; e8 < 32; e8 += 8) {  // the dQK image: rows t, K = r (B6 reads it MN-major)
                 float xs[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) xs[e] = dp[e8 + e];
                 tc::split8_store(xs, TB + toff<kN>(m, 32 * hc + e8), TB + 8192 + toff<kN>(m, 32 * hc + e8));
             }
-            transpose_store<kN>(dp, TB + 16384, 8192, m, hc);  // dQK^T tile rows r, K = t
             red[q * 64 + 32 * hc + lane] = colsum32(col);
             red[256 + hc * 64 + m] = rowp;
         }
@@ -461,39 +473,19 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
             v.edr1[t] = __fadd_rn(red[256 + t], red[320 + t]);
         }
     }
-    // ---- B5, B6: dq^T += K^T dQK^T;  dk^T += Q^T dQK
+    // ---- B5, B6: dq += dQK K and dk += dQK^T Q, as dq^T = K^T dQK^T-side and dk^T = Q^T
+    //      dQK-side: K^T and Q^T are the K image and a Q image (rows t, K = c), and dQK^T the
+    //      dQK image, each read MN-major
     if (alive) {
-        {  // A: K^T rows c, K = r;  Q^T rows c, K = t (the query loads of all four items first)
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            uint16_t qb[2][8];
-#pragma unroll
-            for (int uu = 0; uu < 2; ++uu) {
-                const int u = 2 * hb + uu;
-                const int idx = t + u * kT, cc = idx % kD, r8 = (idx / kD) * 8;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    qb[uu][e] = r8 + e < len ? __bfloat16_as_ushort(gq[((t0 + r8 + e) * H + h) * kD + cc]) : (uint16_t)0;
-            }
-#pragma unroll
-            for (int uu = 0; uu < 2; ++uu) {
-                const int u = 2 * hb + uu;
-                const int idx = t + u * kT, cc = idx % kD, r8 = (idx / kD) * 8;
-                uint32_t kw[4], qw[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    kw[e / 2] = (uint32_t)__bfloat16_as_ushort(Kp[(r8 + e) * kD + cc]) |
-                                ((uint32_t)__bfloat16_as_ushort(Kp[(r8 + e + 1) * kD + cc]) << 16);
-                    qw[e / 2] = (uint32_t)qb[uu][e] | ((uint32_t)qb[uu][e + 1] << 16);
-                }
-                *reinterpret_cast<uint4*>(TA + toff<kN>(cc, r8)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
-                *reinterpret_cast<uint4*>(TA + 32768 + toff<kN>(cc, r8)) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-            }
-          }
+        for (int idx = t; idx < kN * 16; idx += kT) {
+            const int r = idx >> 4, cv = (idx & 15) * 8;
+            uint4 qw = make_uint4(0u, 0u, 0u, 0u);
+            if (r < len) qw = __ldg(reinterpret_cast<const uint4*>(gq + ((t0 + r) * H + h) * kD + cv));
+            *reinterpret_cast<uint4*>(TA + toff<kD>(r, cv)) = qw;
         }
         run([&] {
-            mma_ab<kN, 1, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false);
-            mma_ab<kN, 1, 2>(tmem + P1, tc::smem_u32(TA + 32768), tc::smem_u32(TB + 16384), false);
+            mma2<kN, 1, 2>(tmem + P0, mnview(KI, kN, kD), kmaj(TB, kN, kN), false);
+            mma2<kN, 1, 2>(tmem + P1, mnview(TA, kN, kD), mnview(TB, kN, kN), false);
         });
         float x[32];
         acc(P0, x);
@@ -503,29 +495,40 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) dkT[jj] = __fadd_rn(dkT[jj], x[jj]);
     }
-    // ---- B3: dU^T = dS_end (diag(d) K)^T + dO^T Pm
+    // ---- B3a and B4 in one run, both from one image of dS_end as stored (rows c, K = i),
+    //      B3a reading it MN-major:
+    //      B3a: dU^T = dS_end (diag(d) K)^T  (B3b adds dO^T Pm below)
+    //      B4:  UdS^T = dS_end^T U-side:  dk^T += UdS^T diag(d);  dd = colsum(UdS^T o K^T)
     float DUT[32];
     if (alive) {
-        state_tile(dSe, true);  // A: dS_end[i][c], rows i, K = c
-        for (int idx = t; idx < kN * 16; idx += kT) {  // B: diag(d) K, rows r, K = c
+        state_tile(dSe, false);
+        for (int idx = t; idx < kN * 16; idx += kT) {  // B of B3a: diag(d) K, rows r, K = c
             const int r = idx >> 4, c8 = (idx & 15) * 8;
+            const uint4 kw = *reinterpret_cast<const uint4*>(KI + toff<kD>(r, c8));
+            const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kw);
             float xs[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xs[e] = __fmul_rn(v.dd[r], __bfloat162float(Kp[r * kD + c8 + e]));
+            for (int e = 0; e < 8; ++e) xs[e] = __fmul_rn(v.dd[r], __bfloat162float(kb[e]));
             tc::split8_store(xs, TB + toff<kD>(r, c8), TB + 16384 + toff<kD>(r, c8));
         }
-        run([&] { mma_ab<kD, 2, 2>(tmem + P2, tc::smem_u32(TA), tc::smem_u32(TB), false); });
-    }
-    if (alive) {
-        for (int idx = t; idx < kD * 8; idx += kT) {  // A: dO^T rows i, K = t
-            const int i = idx % kD, r8 = (idx / kD) * 8;
-            uint32_t ow[4];
+        run([&] {
+            mma2<kD, 2, 2>(tmem + P2, mnview(TA, kD, kD), kmaj(TB, kN, kD), false);
+            mma2<kD, 2, 2>(tmem + P0, kmaj(TA, kD, kD), mnview(TU, kD, kN), false);
+        });
+        float x[32];
+        acc(P0, x);
 #pragma unroll
-            for (int e = 0; e < 8; e += 2)
-                ow[e / 2] = (uint32_t)__bfloat16_as_ushort(Op[(r8 + e) * kD + i]) |
-                            ((uint32_t)__bfloat16_as_ushort(Op[(r8 + e + 1) * kD + i]) << 16);
-            *reinterpret_cast<uint4*>(TA + toff<kN>(i, r8)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        for (int jj = 0; jj < 32; ++jj) {
+            const int r = 32 * hc + jj;
+            dkT[jj] = __fmaf_rn(v.dd[r], x[jj], dkT[jj]);
+            x[jj] = __fmul_rn(x[jj], kp(r, m));
         }
+        red[q * 64 + 32 * hc + lane] = colsum32(x);
+        __syncthreads();
+        if (t < kN) v.ddv[t] = __fadd_rn(__fadd_rn(red[t], red[64 + t]), __fadd_rn(red[128 + t], red[192 + t]));
+    }
+    // ---- B3b: dU^T += dO^T Pm (dO^T: the dO image read MN-major)
+    if (alive) {
         for (int idx = t; idx < kN * 8; idx += kT) {  // B: Pm^T rows r, K = t
             const int r = idx % kN, k8 = (idx / kN) * 8;
             float xs[8];
@@ -533,52 +536,44 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
             for (int e = 0; e < 8; ++e) xs[e] = Pm[(k8 + e) * kNN + r];
             tc::split8_store(xs, TB + toff<kN>(r, k8), TB + 8192 + toff<kN>(r, k8));
         }
-        run([&] { mma_ab<kN, 1, 2>(tmem + P2, tc::smem_u32(TA), tc::smem_u32(TB), true); });
+        run([&] { mma2<kN, 1, 2>(tmem + P2, mnview(OI, kN, kD), kmaj(TB, kN, kN), true); });
         acc(P2, DUT);
     }
-    // ---- B4: UdS^T = dS_end^T U^T-side:  dk^T += UdS^T diag(d);  dd = colsum(UdS^T o K^T)
-    if (alive) {
-        state_tile(dSe, false);  // A: dS_end^T rows c, K = i (as stored)
-        run([&] { mma_ab<kD, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TU), false); });
-        float x[32];
-        acc(P0, x);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int r = 32 * hc + jj;
-            dkT[jj] = __fmaf_rn(v.dd[r], x[jj], dkT[jj]);
-            x[jj] = __fmul_rn(x[jj], __bfloat162float(Kp[r * kD + m]));
-        }
-        red[q * 64 + 32 * hc + lane] = colsum32(x);
-        __syncthreads();
-        if (t < kN) v.ddv[t] = __fadd_rn(__fadd_rn(red[t], red[64 + t]), __fadd_rn(red[128 + t], red[192 + t]));
-    }
-    // ---- B7: dT = dU (diag(beta) R)^T (n x n)  -> the dT^T tile (rows t', K = t) for B10
+    // ---- B7: dT = dU (diag(beta) R)^T (n x n): A = dU from the dU^T image (rows i, 128
+    //      columns t, zero past 64) and B = beta R from the (beta R)^T image (rows i, 64
+    //      columns r), both read MN-major; dT -> the dT image (rows t, K = t') for B10
     if (alive) {
         __syncthreads();  // every reader of the last reductions' partials and of TA is done
-        transpose_store<kD>(DUT, TA, 32768, m, hc);  // dU rows t, K = i
         {
-            float br[32];
+            float br[8];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) br[jj] = __fmul_rn(v.beta[32 * hc + jj], RT[jj]);
-            transpose_store<kD>(br, TB, 16384, m, hc);  // beta R rows r, K = i
+            for (int e8 = 0; e8 < 32; e8 += 8) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) br[e] = DUT[e8 + e];
+                tc::split8_store(br, TA + toff<kD>(m, 32 * hc + e8), TA + 32768 + toff<kD>(m, 32 * hc + e8));
+                *reinterpret_cast<uint4*>(TA + toff<kD>(m, 64 + 32 * hc + e8)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(TA + 32768 + toff<kD>(m, 64 + 32 * hc + e8)) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) br[e] = __fmul_rn(v.beta[32 * hc + e8 + e], RT[e8 + e]);
+                tc::split8_store(br, TB + toff<kN>(m, 32 * hc + e8), TB + 16384 + toff<kN>(m, 32 * hc + e8));
+            }
         }
-        zero_upper(TA, kD, true);
-        run([&] { mma_ab<kD, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        run([&] { mma2<kD, 2, 2>(tmem + P0, mnview(TA, kD, kD), mnview(TB, kD, kN), false); });
         if (q < 2) {
             float x[32];
             acc(P0, x);
-            transpose_store<kN>(x, TU, 8192, m, hc);  // dT^T tile rows t', K = t
+#pragma unroll
+            for (int e8 = 0; e8 < 32; e8 += 8) {
+                float xs[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xs[e] = x[e8 + e];
+                tc::split8_store(xs, TU + toff<kN>(m, 32 * hc + e8), TU + 8192 + toff<kN>(m, 32 * hc + e8));
+            }
         }
     }
-    // ---- B8: TdU^T = dU^T T:  dv = diag(beta) TdU;  dbeta = colsum(TdU^T o R^T)
+    // ---- B8: TdU^T = dU^T T:  dv = diag(beta) TdU;  dbeta = colsum(TdU^T o R^T)  (A: the dU^T
+    //      image, K-major; TdU^T -> its image, rows i, 64 columns r, for B9)
     if (alive) {
-#pragma unroll
-        for (int e8 = 0; e8 < 32; e8 += 8) {  // A: dU^T rows i, K = t (this thread's row)
-            float xs[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xs[e] = DUT[e8 + e];
-            tc::split8_store(xs, TA + toff<kN>(m, 32 * hc + e8), TA + 16384 + toff<kN>(m, 32 * hc + e8));
-        }
         for (int idx = t; idx < kN * 8; idx += kT) {  // B: T^T rows r, K = t
             const int r = idx % kN, k8 = (idx / kN) * 8;
             float xs[8];
@@ -586,10 +581,16 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
             for (int e = 0; e < 8; ++e) xs[e] = Tm[(k8 + e) * kNN + r];
             tc::split8_store(xs, TB + toff<kN>(r, k8), TB + 8192 + toff<kN>(r, k8));
         }
-        run([&] { mma_ab<kN, 2, 2>(tmem + P1, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        run([&] { mma2<kN, 2, 2>(tmem + P1, kmaj(TA, kD, kD), kmaj(TB, kN, kN), false); });
         float x[32];
         acc(P1, x);
-        transpose_store<kD>(x, TB, 16384, m, hc);  // TdU tile rows r, K = i, for B9 (TB is free)
+#pragma unroll
+        for (int e8 = 0; e8 < 32; e8 += 8) {
+            float xs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xs[e] = x[e8 + e];
+            tc::split8_store(xs, TB + toff<kN>(m, 32 * hc + e8), TB + 16384 + toff<kN>(m, 32 * hc + e8));
+        }
         float* dvb = a.dv + ((size_t)t0 * H + h) * kD + m;
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
@@ -604,14 +605,14 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
     // ---- B9: Z^T = S_b^T TdU^T:  dk^T -= Z^T diag(beta gam);  dgam -= beta colsum(Z^T o K^T)
     if (alive) {
         state_tile(Sb, false);  // A: S_b^T rows c, K = i (as stored)
-        run([&] { mma_ab<kD, 2, 2>(tmem + P0, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        run([&] { mma2<kD, 2, 2>(tmem + P0, kmaj(TA, kD, kD), mnview(TB, kD, kN), false); });
         float x[32];
         acc(P0, x);
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
             const int r = 32 * hc + jj;
             dkT[jj] = __fmaf_rn(-__fmul_rn(v.beta[r], v.gam[r]), x[jj], dkT[jj]);
-            x[jj] = __fmul_rn(x[jj], __bfloat162float(Kp[r * kD + m]));
+            x[jj] = __fmul_rn(x[jj], kp(r, m));
         }
         red[q * 64 + 32 * hc + lane] = colsum32(x);
         __syncthreads();
@@ -619,7 +620,8 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
             v.dgam2[t] = __fmul_rn(-v.beta[t], __fadd_rn(__fadd_rn(red[t], red[64 + t]),
                                                          __fadd_rn(red[128 + t], red[192 + t])));
     }
-    // ---- B10: X = T^T dT (n x n) -> the X tile (rows r, K = t) for B11
+    // ---- B10: X = T^T dT (n x n; dT from its image read MN-major) -> the X tile (rows r,
+    //      K = t) for B11
     if (alive) {
         __syncthreads();
         for (int idx = t; idx < kN * 8; idx += kT) {  // A: T^T rows r, K = t
@@ -630,7 +632,7 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
             tc::split8_store(xs, TA + toff<kN>(r, k8), TA + 16384 + toff<kN>(r, k8));
         }
         zero_upper(TA, kN, true);
-        run([&] { mma_ab<kN, 2, 2>(tmem + P1, tc::smem_u32(TA), tc::smem_u32(TU), false); });
+        run([&] { mma2<kN, 2, 2>(tmem + P1, kmaj(TA, 128, kN), mnview(TU, kN, kN), false); });
         if (q < 2) {
             float x[32];
             acc(P1, x);
@@ -687,19 +689,10 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
             for (int e = 0; e < 8; ++e) xs[e] = __fadd_rn(Pm[r * kNN + k8 + e], Pm[(k8 + e) * kNN + r]);
             tc::split8_store(xs, TB + toff<kN>(r, k8), TB + 8192 + toff<kN>(r, k8));
         }
-        for (int idx = t; idx < kD * 8; idx += kT) {  // A: K^T rows c, K = i
-            const int cc = idx % kD, r8 = (idx / kD) * 8;
-            uint32_t kw[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2)
-                kw[e / 2] = (uint32_t)__bfloat16_as_ushort(Kp[(r8 + e) * kD + cc]) |
-                            ((uint32_t)__bfloat16_as_ushort(Kp[(r8 + e + 1) * kD + cc]) << 16);
-            *reinterpret_cast<uint4*>(TA + toff<kN>(cc, r8)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
-        }
     }
-    // ---- B12: dk^T += K^T Ssym^T-side (dk += (dKK + dKK^T) K)
+    // ---- B12: dk^T += K^T Ssym^T-side (dk += (dKK + dKK^T) K; K^T: the K image read MN-major)
     if (alive) {
-        run([&] { mma_ab<kN, 1, 2>(tmem + P1, tc::smem_u32(TA), tc::smem_u32(TB), false); });
+        run([&] { mma2<kN, 1, 2>(tmem + P1, mnview(KI, kN, kD), kmaj(TB, kN, kN), false); });
         float x[32];
         acc(P1, x);
 #pragma unroll
