@@ -126,6 +126,12 @@ __device__ __forceinline__ void mma2(uint32_t d, const Opnd& A, const Opnd& B, b
     }
 }
 
+// The 16-byte group idx of a 64-row K-major tile with kD elements per row: its row and first
+// column, chosen so that toff<kD>(row, col) = 16 idx (consecutive threads touch consecutive
+// shared-memory bytes: no bank conflicts).
+__device__ __forceinline__ int img_row(int idx) { return (idx & 7) | ((idx >> 7) << 3); }
+__device__ __forceinline__ int img_col(int idx) { return ((idx >> 3) & 15) * 8; }
+
 // Lane l of the warp gets the sum over the warp's 32 lanes of v[l] (a fixed butterfly:
 // each round keeps one half of the remaining columns and adds the partner's copy).
 __device__ __forceinline__ float colsum32(float (&v)[32])
@@ -192,7 +198,7 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
 
     // ---- a: the chunk's K and dO as stored (zero rows past its tokens), g, beta
     for (int idx = t; idx < kN * 16; idx += kT) {
-        const int r = idx >> 4, cv = (idx & 15) * 8;
+        const int r = img_row(idx), cv = img_col(idx);
         uint4 wk = make_uint4(0u, 0u, 0u, 0u), wo = wk;
         if (r < len) {
             wk = __ldg(reinterpret_cast<const uint4*>(gk + ((t0 + r) * H + h) * kD + cv));
@@ -299,7 +305,7 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
     // ---- F1, F2: K K^T and Q K^T (n x n)
     {
         for (int idx = t; idx < kN * 16; idx += kT) {  // A: K and Q, rows t < 64 (zero rows after)
-            const int r = idx >> 4, cv = (idx & 15) * 8;
+            const int r = img_row(idx), cv = img_col(idx);
             const uint4 kw = *reinterpret_cast<const uint4*>(KI + toff<kD>(r, cv));
             uint4 qw = make_uint4(0u, 0u, 0u, 0u);
             if (r < len) qw = __ldg(reinterpret_cast<const uint4*>(gq + ((t0 + r) * H + h) * kD + cv));
@@ -478,7 +484,7 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
     //      dQK image, each read MN-major
     if (alive) {
         for (int idx = t; idx < kN * 16; idx += kT) {
-            const int r = idx >> 4, cv = (idx & 15) * 8;
+            const int r = img_row(idx), cv = img_col(idx);
             uint4 qw = make_uint4(0u, 0u, 0u, 0u);
             if (r < len) qw = __ldg(reinterpret_cast<const uint4*>(gq + ((t0 + r) * H + h) * kD + cv));
             *reinterpret_cast<uint4*>(TA + toff<kD>(r, cv)) = qw;
@@ -503,7 +509,7 @@ __device__ __forceinline__ bool chunk_grads_item(const BackwardArgs& a, int64_t 
     if (alive) {
         state_tile(dSe, false);
         for (int idx = t; idx < kN * 16; idx += kT) {  // B of B3a: diag(d) K, rows r, K = c
-            const int r = idx >> 4, c8 = (idx & 15) * 8;
+            const int r = img_row(idx), c8 = img_col(idx);
             const uint4 kw = *reinterpret_cast<const uint4*>(KI + toff<kD>(r, c8));
             const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kw);
             float xs[8];
