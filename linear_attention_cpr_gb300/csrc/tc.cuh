@@ -7,6 +7,10 @@
 // 16 bytes, core (i, kk) stored at byte (i * (K*esize/16) + kk) * 128, row r of a core at
 // +16*r.  In the descriptor, LBO is the byte step between cores adjacent along K (128)
 // and SBO the step between 8-row groups (K*esize/16 * 128).
+// The same tile read MN-major (the instruction descriptor's transpose bit for A or B, bits
+// 15 and 16): the operand's M or N index runs along the 16-byte rows, its K index across
+// them; LBO is then the byte step between 8-element K groups and SBO the step between
+// 8-element M or N groups (checked on this GPU against a CPU product).
 // (pik.cu uses the 128-byte-swizzled K-major layout instead, with its own descriptor.)
 // Accumulator layout: M = 128 -> row m in TMEM lane m; M = 64 -> rows 16q..16q+15 in
 // lanes 32q..32q+15.  Column j of D is TMEM column (base + j).
