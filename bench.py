@@ -43,9 +43,11 @@ FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
 # of the kernel as it now stands: k23_chain_and_intra at trainer_fwd, k4_decode_step at
-# rollout_decode.  Reset to None whenever the kernel changes.
+# rollout_decode, kb23_chain_and_grads_tc at the trainer's forward + backward.  Reset to
+# None whenever the kernel changes.
 TRAFFIC_K23_TRAINER_FWD = 531.102976e6 + 194.182912e6
 TRAFFIC_K4_ROLLOUT_DECODE = 267.595520e6 + 208.146688e6
+TRAFFIC_KB23_TRAINER = 834.262528e6 + 391.001600e6
 
 
 def _peaks():
@@ -439,7 +441,8 @@ def run_train_fwd_bwd(args, cpr, inputs, dev, dist, world, flush, p32_meas):
     f_cg = flops["reverse_chain"] + flops["chunk_grads"]
     ach = f_cg / (kern_ms["chain_and_grads"] / 1e3) / 1e12
     roof = {"kernel": "kb23_chain_and_grads_tc", "bound": "alu", "achieved": ach, "peak": FP32_PEAK_TFLOPS,
-            "unit": "TFLOP/s", "frac": ach / FP32_PEAK_TFLOPS, "traffic": None, "flops_per_launch": f_cg,
+            "unit": "TFLOP/s", "frac": ach / FP32_PEAK_TFLOPS, "traffic": TRAFFIC_KB23_TRAINER,
+            "flops_per_launch": f_cg,
             "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz; FP32-equivalent work (the kernels "
                          "run the products as bf16 hi/lo splits on the tensor cores)"}
     if p32_meas:
