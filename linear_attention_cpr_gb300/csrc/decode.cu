@@ -557,8 +557,10 @@ __device__ __forceinline__ bool resync_one(const DecodeArgs& a, int b, int h, un
     return true;
 }
 
+// At most 192 registers a thread (none spilled): with 256 threads that leaves room on the
+// SM for one CTA of the step kernel, which runs beside the resync.
 template <int DK, int DV, int C, typename T, bool QK_NORM>
-__global__ void __launch_bounds__(DK + DV) k5_resync(DecodeArgs a)
+__global__ void __maxnreg__(192) k5_resync(DecodeArgs a)
 {
     using U = UCfg<DK, DV, C>;
     extern __shared__ __align__(1024) unsigned char sm5[];
