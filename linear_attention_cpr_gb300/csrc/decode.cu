@@ -412,8 +412,12 @@ __device__ __forceinline__ bool completing_token_output(const DecodeArgs& a, siz
         vi = to_f32<T>(static_cast<const T*>(a.v)[bh * DV + tid]);
     }
     const bool ok = __syncthreads_and(tc::mbar_wait(mbar, phase & 1));
+    if (!ok) {  // the copy still lands (bounded) before the CTA gives up its shared memory
+        if (threadIdx.x == 0) tc::mbar_wait(mbar, phase & 1, 1u << 16);
+        ++phase;
+        return false;
+    }
     ++phase;
-    if (!ok) return false;
     if (QK_NORM) l2_normalise_qk<DK>(kf, qf, part);
     if (tid < DV) {
         const int i = tid;
